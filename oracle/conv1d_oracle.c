@@ -1,0 +1,293 @@
+/*
+ * Depthwise causal conv1d -- plain CPU oracle, fp64 arithmetic.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the slow, obviously-correct
+ * restatement of the operation that the CUDA path is checked against.  Only the
+ * tests, the smoke check and the benchmark's CPU-baseline leg may load it.  It
+ * shares no code, header, table or helper with the CUDA library.
+ *
+ * What it computes (cuDNN frontend "Causal Conv1d" page: the list of tensors,
+ * the paragraph on the optimized route -- width four, SiLU, W-1 initial and
+ * final state, cu_seqlens packing -- and the paragraph on causal_conv1d_update;
+ * tap order from the causal-padding derivation on the POPCORNBENCH conv1d page,
+ * where tap k of a width-K filter reads input position t + k - (K-1)):
+ *
+ *   extended sequence   xe[j] = x[j]            for 0 <= j < len
+ *                       xe[j] = init[j + 3]     for -3 <= j < 0 (0 if no init)
+ *   pre-activation      pre[t] = bias + sum_{k=0..3} w[k] * xe[t - 3 + k]
+ *   output              out[t] = silu(pre[t]) = pre[t] * s(pre[t]),  s(p) = 1/(1+exp(-p))
+ *                       (or out = pre with the identity activation)
+ *   final state         final[i] = xe[len - 3 + i], i = 0..2
+ *
+ * A "sequence" is one batch row of a dense call, or one cu_seqlens range of a
+ * packed call (each with its own initial/final state, nothing crosses a
+ * boundary).
+ *
+ * Backward (gradients of L with g = dL/dout and gf = dL/dfinal):
+ *   gp[t]    = g[t] * silu'(pre[t]),   silu'(p) = s(p) * (1 + p * (1 - s(p)))
+ *   dxe[j]   = sum_k w[k] * gp[j + 3 - k]   (only terms with 0 <= j+3-k < len)
+ *              + gf[j - (len - 3)]          (when j >= len - 3)
+ *   dx[t]    = dxe[t],   dinit[i] = dxe[i - 3]
+ *   dw[k]    = sum_seq sum_t gp[t] * xe[t - 3 + k],    db = sum_seq sum_t gp[t]
+ *
+ * Single-token update (causal_conv1d_update): xe = [s0, s1, s2, x],
+ * out = act(bias + sum_k w[k] * xe[k]), new state = [s1, s2, x].
+ *
+ * Every input and output here is a double.  The Python side decodes BF16
+ * inputs exactly into doubles and rounds results once (nearest-even) to the
+ * output type with oracle_bf16_encode_array below.  Products of a BF16 value
+ * and a BF16/FP32 weight are exact in double, so pre[] is the exact value up to
+ * the double rounding of a five-term sum.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define CONV_W 4
+#define CONV_S 3
+
+enum { ORC_OK = 0, ORC_BAD_CU_SEQLENS = 7, ORC_NO_MEMORY = 100 };
+
+/* ---- BF16 rounding ------------------------------------------------------ */
+
+/* Round a double to the nearest BF16 value (ties to even), returned as bits.
+ * BF16 keeps 8 significant bits; for |v| in [2^(e-1), 2^e) the spacing of
+ * representable values is 2^(e-8).  Below the smallest normal (2^-126) the
+ * spacing stays 2^-133.  Values that round to 2^128 or beyond overflow to inf. */
+uint16_t oracle_bf16_encode(double v)
+{
+    if (isnan(v))
+        return 0x7FC0;
+    uint16_t sign = signbit(v) ? 0x8000 : 0;
+    double a = fabs(v);
+    if (a == 0.0)
+        return sign;
+    if (isinf(a))
+        return (uint16_t)(sign | 0x7F80);
+    int e;
+    (void)frexp(a, &e);
+    int qexp = (e < -125 ? -125 : e) - 8;
+    double r = rint(ldexp(a, -qexp)); /* default rounding mode: nearest-even */
+    double q = ldexp(r, qexp);
+    if (q >= ldexp(1.0, 128))
+        return (uint16_t)(sign | 0x7F80);
+    float f = (float)q; /* exact: q is a BF16 value */
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return (uint16_t)(sign | ((u >> 16) & 0x7FFF));
+}
+
+void oracle_bf16_encode_array(const double *v, int64_t n, uint16_t *out)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = oracle_bf16_encode(v[i]);
+}
+
+/* ---- activation --------------------------------------------------------- */
+
+static double sigmoid(double p) { return 1.0 / (1.0 + exp(-p)); }
+
+static double activate(double p, int act) { return act ? p * sigmoid(p) : p; }
+
+static double activate_grad(double p, int act)
+{
+    if (!act)
+        return 1.0;
+    double s = sigmoid(p);
+    return s * (1.0 + p * (1.0 - s));
+}
+
+/* ---- sequences ---------------------------------------------------------- */
+
+/* cu_seqlens rules (cuDNN page, paragraph on packed metadata): first offset 0,
+ * last offset equal to the runtime token total, strictly increasing offsets
+ * (an empty sequence is malformed). */
+int oracle_check_cu_seqlens(const int32_t *cu, int n_seq, int64_t total)
+{
+    if (n_seq < 1 || cu[0] != 0 || (int64_t)cu[n_seq] != total)
+        return ORC_BAD_CU_SEQLENS;
+    for (int n = 0; n < n_seq; ++n)
+        if (cu[n + 1] <= cu[n])
+            return ORC_BAD_CU_SEQLENS;
+    return ORC_OK;
+}
+
+/* Sequence n: batch row, first token within the row, and length.  Dense: row
+ * n, tokens 0..T-1.  Packed: row 0, tokens cu[n]..cu[n+1]-1. */
+static void seq_range(int n, const int32_t *cu, int64_t T, int64_t *row, int64_t *start, int64_t *len)
+{
+    if (cu) {
+        *row = 0;
+        *start = cu[n];
+        *len = (int64_t)cu[n + 1] - cu[n];
+    } else {
+        *row = n;
+        *start = 0;
+        *len = T;
+    }
+}
+
+/* xe[j] of one (sequence, channel); x points at token 0 of the sequence,
+ * init at its three state entries (or NULL). */
+static double xe(const double *x, const double *init, int64_t j)
+{
+    if (j >= 0)
+        return x[j];
+    return init ? init[j + CONV_S] : 0.0;
+}
+
+static double pre_activation(const double *x, const double *init, const double *w, double b, int64_t t)
+{
+    double p = b;
+    for (int k = 0; k < CONV_W; ++k)
+        p += w[k] * xe(x, init, t - (CONV_W - 1) + k);
+    return p;
+}
+
+/* ---- forward ------------------------------------------------------------ */
+
+/*
+ * x:     [B][D][T] (packed: B == 1 and T == token total)
+ * w:     [D][4];  bias: [D] or NULL
+ * cu:    [n_seq + 1] or NULL (dense: n_seq is taken as B)
+ * init:  [n_seq][D][3] or NULL
+ * out, pre: [B][D][T] (pre may be NULL);  fin: [n_seq][D][3] or NULL
+ */
+int oracle_fwd(const double *x, int64_t B, int64_t D, int64_t T,
+               const double *w, const double *bias, const int32_t *cu, int n_seq,
+               const double *init, int act, double *out, double *pre, double *fin)
+{
+    if (cu && oracle_check_cu_seqlens(cu, n_seq, T))
+        return ORC_BAD_CU_SEQLENS;
+    if (!cu)
+        n_seq = (int)B;
+    for (int n = 0; n < n_seq; ++n) {
+        int64_t row, start, len;
+        seq_range(n, cu, T, &row, &start, &len);
+        for (int64_t d = 0; d < D; ++d) {
+            const double *wd = w + d * CONV_W;
+            double b = bias ? bias[d] : 0.0;
+            int64_t base = (row * D + d) * T + start;
+            const double *xs = x + base;
+            const double *is = init ? init + ((int64_t)n * D + d) * CONV_S : NULL;
+            for (int64_t t = 0; t < len; ++t) {
+                double p = pre_activation(xs, is, wd, b, t);
+                out[base + t] = activate(p, act);
+                if (pre)
+                    pre[base + t] = p;
+            }
+            if (fin) {
+                double *fs = fin + ((int64_t)n * D + d) * CONV_S;
+                for (int i = 0; i < CONV_S; ++i)
+                    fs[i] = xe(xs, is, len - CONV_S + i);
+            }
+        }
+    }
+    return ORC_OK;
+}
+
+/* ---- backward ----------------------------------------------------------- */
+
+/*
+ * Inputs as oracle_fwd, plus g: [B][D][T] and gfin: [n_seq][D][3] or NULL.
+ * Outputs (any may be NULL):
+ *   dx [B][D][T];  dinit [n_seq][D][3]
+ *   dw [D][4], dw_abs [D][4] = sum |gp * xe|;  db [D], db_abs [D] = sum |gp|
+ * The sums run over sequences in ascending order, then tokens in ascending
+ * order, in one double accumulator per (channel, tap).
+ */
+int oracle_bwd(const double *x, int64_t B, int64_t D, int64_t T,
+               const double *w, const double *bias, const int32_t *cu, int n_seq,
+               const double *init, int act, const double *g, const double *gfin,
+               double *dx, double *dinit, double *dw, double *dw_abs, double *db, double *db_abs)
+{
+    if (cu && oracle_check_cu_seqlens(cu, n_seq, T))
+        return ORC_BAD_CU_SEQLENS;
+    if (!cu)
+        n_seq = (int)B;
+    double *gp = (double *)malloc((size_t)(T > 0 ? T : 1) * sizeof(double));
+    if (!gp)
+        return ORC_NO_MEMORY;
+    for (int64_t d = 0; d < D; ++d) {
+        const double *wd = w + d * CONV_W;
+        double b = bias ? bias[d] : 0.0;
+        double sdw[CONV_W] = {0, 0, 0, 0}, sdw_abs[CONV_W] = {0, 0, 0, 0};
+        double sdb = 0.0, sdb_abs = 0.0;
+        for (int n = 0; n < n_seq; ++n) {
+            int64_t row, start, len;
+            seq_range(n, cu, T, &row, &start, &len);
+            int64_t base = (row * D + d) * T + start;
+            const double *xs = x + base;
+            const double *gs = g + base;
+            const double *is = init ? init + ((int64_t)n * D + d) * CONV_S : NULL;
+            const double *gfs = gfin ? gfin + ((int64_t)n * D + d) * CONV_S : NULL;
+            /* gradient at the pre-activation; weight and bias sums */
+            for (int64_t t = 0; t < len; ++t) {
+                gp[t] = gs[t] * activate_grad(pre_activation(xs, is, wd, b, t), act);
+                for (int k = 0; k < CONV_W; ++k) {
+                    double term = gp[t] * xe(xs, is, t - (CONV_W - 1) + k);
+                    sdw[k] += term;
+                    sdw_abs[k] += fabs(term);
+                }
+                sdb += gp[t];
+                sdb_abs += fabs(gp[t]);
+            }
+            /* gradient at every entry of the extended sequence */
+            for (int64_t j = -CONV_S; j < len; ++j) {
+                double acc = 0.0;
+                for (int k = 0; k < CONV_W; ++k) {
+                    int64_t t = j + (CONV_W - 1) - k; /* the output that tap k reads xe[j] for */
+                    if (t >= 0 && t < len)
+                        acc += wd[k] * gp[t];
+                }
+                if (gfs && j >= len - CONV_S)
+                    acc += gfs[j - (len - CONV_S)];
+                if (j >= 0) {
+                    if (dx)
+                        dx[base + j] = acc;
+                } else if (dinit) {
+                    dinit[((int64_t)n * D + d) * CONV_S + (j + CONV_S)] = acc;
+                }
+            }
+        }
+        for (int k = 0; k < CONV_W; ++k) {
+            if (dw)
+                dw[d * CONV_W + k] = sdw[k];
+            if (dw_abs)
+                dw_abs[d * CONV_W + k] = sdw_abs[k];
+        }
+        if (db)
+            db[d] = sdb;
+        if (db_abs)
+            db_abs[d] = sdb_abs;
+    }
+    free(gp);
+    return ORC_OK;
+}
+
+/* ---- single-token update ------------------------------------------------ */
+
+/*
+ * x:     [B][D] (one token);  w [D][4];  bias [D] or NULL
+ * state: [B][D][3], read, then overwritten with [s1, s2, x]
+ * out:   [B][D]
+ */
+void oracle_update(const double *x, int64_t B, int64_t D, const double *w, const double *bias,
+                   int act, double *state, double *out)
+{
+    for (int64_t bb = 0; bb < B; ++bb) {
+        for (int64_t d = 0; d < D; ++d) {
+            const double *wd = w + d * CONV_W;
+            double *s = state + (bb * D + d) * CONV_S;
+            double ext[CONV_W] = {s[0], s[1], s[2], x[bb * D + d]};
+            double p = bias ? bias[d] : 0.0;
+            for (int k = 0; k < CONV_W; ++k)
+                p += wd[k] * ext[k];
+            out[bb * D + d] = activate(p, act);
+            s[0] = ext[1];
+            s[1] = ext[2];
+            s[2] = ext[3];
+        }
+    }
+}

@@ -1,0 +1,204 @@
+"""Seeded synthetic inputs for the depthwise causal conv1d.
+
+This module holds input generation only -- none of the operation's arithmetic.
+It is the one piece of code that both the CUDA path's callers and the CPU
+oracle's callers share, so that both sides see byte-identical inputs.
+
+Recipe (every tensor): draw with ``torch.Generator().manual_seed(seed)`` on the
+CPU, in the order the workload lists its tensors, in float32, then round to
+bfloat16 (round-to-nearest-even) unless the tensor is float32 by definition.
+``N(0,1)`` is ``torch.randn``; ``U(a,b)`` is ``a + (b-a) * torch.rand``.
+"Channel-last" storage means the tensor is allocated ``[B, T, D]`` and handed
+to the operation as its ``transpose(1, 2)`` view of logical shape ``[B, D, T]``
+(the cuDNN "Causal Conv1d" page, paragraph on models that own ``[B, T, D]``
+storage).
+
+The five named workloads follow the shapes, dtypes and distributions of the
+task's benchmark configurations; the packed workload's sequence lengths are
+drawn with ``torch.randint(1, 4097, (16,))`` from the same generator, before
+any tensor.
+"""
+
+from __future__ import annotations
+
+import dataclasses
+from typing import Optional
+
+import numpy as np
+import torch
+
+BF16 = torch.bfloat16
+
+
+def _normal(gen, shape):
+    return torch.randn(shape, generator=gen, dtype=torch.float32)
+
+
+def _uniform(gen, shape, lo, hi):
+    return lo + (hi - lo) * torch.rand(shape, generator=gen, dtype=torch.float32)
+
+
+@dataclasses.dataclass
+class ConvInputs:
+    """One call's inputs (CPU tensors).  ``x``/``g`` are logical [B, D, T] views."""
+
+    x: torch.Tensor
+    weight: torch.Tensor
+    bias: Optional[torch.Tensor]
+    initial_states: Optional[torch.Tensor]
+    cu_seqlens: Optional[torch.Tensor]
+    g: Optional[torch.Tensor]
+    dfinal_states: Optional[torch.Tensor]
+    activation: Optional[str]
+    channel_last: bool
+    deterministic: bool = False
+
+    @property
+    def n_seq(self) -> int:
+        return self.x.shape[0] if self.cu_seqlens is None else self.cu_seqlens.numel() - 1
+
+    @property
+    def tokens(self) -> int:
+        return self.x.shape[0] * self.x.shape[2]
+
+    def to(self, device) -> "ConvInputs":
+        def mv(t):
+            if t is None:
+                return None
+            if self.channel_last and t.dim() == 3 and t is not self.initial_states and t is not self.dfinal_states:
+                # keep the [B, T, D] storage behind the [B, D, T] view
+                return t.transpose(1, 2).contiguous().to(device).transpose(1, 2)
+            return t.to(device)
+
+        return dataclasses.replace(
+            self,
+            x=mv(self.x), weight=mv(self.weight), bias=mv(self.bias),
+            initial_states=mv(self.initial_states), cu_seqlens=mv(self.cu_seqlens),
+            g=mv(self.g), dfinal_states=mv(self.dfinal_states),
+        )
+
+
+def make_inputs(B: int, D: int, T: int, *, channel_last: bool = True, seed: int = 0,
+                weight_dtype=BF16, bias: bool = True, initial_states: bool = False,
+                grad: bool = False, dfinal_states: bool = False, lengths=None,
+                activation: Optional[str] = "silu", deterministic: bool = False,
+                x_scale: float = 1.0) -> ConvInputs:
+    """Inputs of one call.  ``lengths`` (list of ints) makes a packed call:
+    B must be 1 and T == sum(lengths).  Draw order: x, weight, bias,
+    initial_states, g, dfinal_states."""
+    gen = torch.Generator().manual_seed(seed)
+    cu = None
+    if lengths is not None:
+        if B != 1 or int(sum(lengths)) != T:
+            raise ValueError("packed inputs take B == 1 and T == sum(lengths)")
+        cu = torch.zeros(len(lengths) + 1, dtype=torch.int32)
+        cu[1:] = torch.cumsum(torch.tensor(lengths, dtype=torch.int64), 0).to(torch.int32)
+    n_seq = B if cu is None else cu.numel() - 1
+
+    def act_tensor():
+        if channel_last:
+            return (_normal(gen, (B, T, D)) * x_scale).to(BF16).transpose(1, 2)
+        return (_normal(gen, (B, D, T)) * x_scale).to(BF16)
+
+    x = act_tensor()
+    w = _uniform(gen, (D, 4), -0.5, 0.5)
+    w = w if weight_dtype == torch.float32 else w.to(BF16)
+    b = _uniform(gen, (D,), -0.1, 0.1).to(BF16) if bias else None
+    init = _normal(gen, (n_seq, D, 3)).to(BF16) if initial_states else None
+    g = act_tensor() if grad else None
+    gf = _normal(gen, (n_seq, D, 3)).to(BF16) if dfinal_states else None
+    return ConvInputs(x=x, weight=w, bias=b, initial_states=init, cu_seqlens=cu, g=g,
+                      dfinal_states=gf, activation=activation, channel_last=channel_last,
+                      deterministic=deterministic)
+
+
+def packed_lengths(seed: int = 0, n_seq: int = 16, max_len: int = 4096):
+    """Sequence lengths of the packed workload: U[1, max_len] integers, drawn
+    first from the workload's generator."""
+    gen = torch.Generator().manual_seed(seed)
+    return torch.randint(1, max_len + 1, (n_seq,), generator=gen).tolist(), gen
+
+
+# ---- the five named workloads ------------------------------------------------
+
+def dense_small(seed: int = 0) -> ConvInputs:
+    """Forward only, dense: x [2, 64, 128] contiguous, BF16 weight and bias, no state."""
+    return make_inputs(2, 64, 128, channel_last=False, seed=seed)
+
+
+def dense_state(seed: int = 0) -> ConvInputs:
+    """Dense forward+backward with state: x stored [4, 2048, 1536] channel-last,
+    BF16 weight/bias, initial_states [4, 1536, 3], return final_states, grad_out."""
+    return make_inputs(4, 1536, 2048, seed=seed, initial_states=True, grad=True)
+
+
+def packed_varlen(seed: int = 0) -> ConvInputs:
+    """Packed varlen forward+backward: 16 sequences of U[1, 4096] tokens, D = 2048,
+    channel-last, FP32 weight, no bias, per-sequence initial states,
+    deterministic weight gradient."""
+    lengths, gen = packed_lengths(seed)
+    T = int(sum(lengths))
+    D = 2048
+    cu = torch.zeros(len(lengths) + 1, dtype=torch.int32)
+    cu[1:] = torch.cumsum(torch.tensor(lengths), 0).to(torch.int32)
+    x = _normal(gen, (1, T, D)).to(BF16).transpose(1, 2)
+    w = _uniform(gen, (D, 4), -0.5, 0.5)
+    init = _normal(gen, (len(lengths), D, 3)).to(BF16)
+    g = _normal(gen, (1, T, D)).to(BF16).transpose(1, 2)
+    return ConvInputs(x=x, weight=w, bias=None, initial_states=init, cu_seqlens=cu, g=g,
+                      dfinal_states=None, activation="silu", channel_last=True,
+                      deterministic=True)
+
+
+@dataclasses.dataclass
+class UpdateInputs:
+    conv_state: torch.Tensor   # [B, D, 3]
+    x_seq: torch.Tensor        # [steps, B, D]
+    weight: torch.Tensor
+    bias: Optional[torch.Tensor]
+    activation: Optional[str] = "silu"
+
+
+def decode_update(seed: int = 0, B: int = 256, D: int = 4096, steps: int = 1000) -> UpdateInputs:
+    """Decode update: state [256, 4096, 3], one token x [256, 4096] per step for
+    ``steps`` chained steps, BF16 weight and bias."""
+    gen = torch.Generator().manual_seed(seed)
+    state = _normal(gen, (B, D, 3)).to(BF16)
+    x_seq = _normal(gen, (steps, B, D)).to(BF16)
+    w = _uniform(gen, (D, 4), -0.5, 0.5).to(BF16)
+    b = _uniform(gen, (D,), -0.1, 0.1).to(BF16)
+    return UpdateInputs(conv_state=state, x_seq=x_seq, weight=w, bias=b)
+
+
+def dense_large(seed: int = 0, bias: bool = True) -> ConvInputs:
+    """Large dense forward+backward: x stored [8, 8192, 5120] channel-last, BF16
+    weight; with bias (atomic weight gradient) or bias-free (deterministic)."""
+    return make_inputs(8, 5120, 8192, seed=seed, bias=bias, initial_states=True, grad=True,
+                       deterministic=not bias)
+
+
+WORKLOADS = {
+    "dense_small": dense_small,
+    "dense_state": dense_state,
+    "packed_varlen": packed_varlen,
+    "decode_update": decode_update,
+    "dense_large": dense_large,
+}
+
+
+# ---- marshalling helpers (bit patterns, no arithmetic) ----------------------
+
+def bits(t: Optional[torch.Tensor]):
+    """BF16 tensor -> numpy uint16 bit patterns (logical shape kept); float32 and
+    int32 tensors are returned as numpy arrays of their own dtype."""
+    if t is None:
+        return None
+    t = t.detach().cpu()
+    if t.dtype == BF16:
+        return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    return t.contiguous().numpy()
+
+
+def from_bits(a: np.ndarray) -> torch.Tensor:
+    """numpy uint16 bit patterns -> BF16 tensor."""
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(BF16)
