@@ -1,0 +1,566 @@
+"""Throughput of the depthwise causal conv1d on GB300: forward + backward of the
+dense channel-last workload with state (x stored [4, 2048, 1536] BF16, BF16
+weight/bias, initial/final state, grad_out), as achieved HBM GB/s
+(algorithmic bytes / time) and tokens/s, with the other workloads (dense
+[2, 64, 128] forward, packed varlen, decode update, large dense) reported per
+kernel under "breakdown".
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line.  Under torchrun (N > 1) every rank runs the same
+workload on its own GPU (independent replicas, no collective on the data
+path); the time is the max over ranks and the value counts all ranks' work.
+
+--impl reference times the CPU oracle (oracle/, plain C in fp64) on the host
+cores on a bounded sample of the same workload: the only comparison system the
+pages leave us, a deliberately slow baseline.
+"""
+
+from __future__ import annotations
+
+import argparse
+import dataclasses
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "fwd/bwd/update achieved HBM GB/s and tokens/s vs ~8 TB/s GB300 peak"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 2 ** 20
+
+# DRAM traffic of the dominant kernel from an ncu capture, per launch, valid
+# only for the kernel sources whose digest is recorded with it.
+TRAFFIC = {"sources_sha256": None, "bytes_per_launch": None}
+
+
+def kernel_sources_digest() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "depthwise_causal_conv1d_channel_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()
+
+
+# ---- sizes ------------------------------------------------------------------------
+
+def act_bytes(x):
+    return x.numel() * x.element_size()
+
+
+def fwd_bytes(x, w, b, init, fin):
+    """Algorithmic minimum: read x, write out, read weight/bias/initial state,
+    write final state."""
+    n = 2 * act_bytes(x) + act_bytes(w)
+    for t in (b, init, fin):
+        if t is not None:
+            n += act_bytes(t)
+    return n
+
+
+def bwd_bytes(x, w, b, init, dfin, dinit):
+    """Read x and grad_out, write dx, read weight, write dweight, read bias and
+    write dbias, read initial state / final-state gradient, write dinitial_states."""
+    n = 3 * act_bytes(x) + 2 * act_bytes(w)
+    if b is not None:
+        n += 2 * act_bytes(b)
+    for t in (init, dfin, dinit):
+        if t is not None:
+            n += act_bytes(t)
+    return n
+
+
+def update_bytes(B, D, w, b):
+    """Read and write the [B, D, 3] state, read x, write out, read weight/bias."""
+    n = 2 * B * D * 3 * 2 + 2 * B * D * 2 + act_bytes(w)
+    if b is not None:
+        n += act_bytes(b)
+    return n
+
+
+# ---- clocks -----------------------------------------------------------------------
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    p = [s.strip() for s in line.split(",")]
+                    if len(p) >= 9 and p[1].isdigit():
+                        rows.append(p)
+        finally:
+            os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"]}
+        sm = [int(r[1]) for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": int(rows[0][2]),
+                "reasons": reasons, "samples": len(rows)}
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---- the timed step ---------------------------------------------------------------
+
+class DenseStep:
+    """Forward + backward through the C ABI on preallocated device buffers.
+    `sets` copies of the activations rotate so that no step finds its inputs
+    in L2 (total footprint well above the L2 size)."""
+
+    def __init__(self, inp: workloads.ConvInputs, device, deterministic=False, sets=None):
+        from depthwise_causal_conv1d_channel_gb300 import _abi
+
+        self.abi = _abi
+        self.dev = device
+        d = inp.to(device)
+        self.inp = inp
+        self.w, self.b, self.cu = d.weight, d.bias, d.cu_seqlens
+        self.init, self.dfin = d.initial_states, d.dfinal_states
+        self.det = deterministic
+        self.act = _abi.CCC_ACT_SILU if inp.activation == "silu" else _abi.CCC_ACT_NONE
+        per_set = 4 * act_bytes(d.x)
+        if sets is None:
+            sets = max(1, min(16, -(-3 * L2_BYTES // per_set)))
+        self.sets = sets
+        self.x = [d.x if i == 0 else d.x.clone() if not inp.channel_last else
+                  d.x.transpose(1, 2).clone().transpose(1, 2) for i in range(sets)]
+        self.g = [None if d.g is None else d.g if i == 0 else
+                  d.g.transpose(1, 2).clone().transpose(1, 2) if inp.channel_last else
+                  d.g.clone() for i in range(sets)]
+        self.out = [torch.empty_like(x) for x in self.x]
+        self.dx = [torch.empty_like(x) for x in self.x]
+        S = inp.n_seq
+        D = d.x.shape[1]
+        self.fin = torch.empty(S, D, 3, dtype=torch.bfloat16, device=device) if self.init is not None else None
+        self.dinit = torch.empty_like(self.init) if self.init is not None else None
+        self.dw = torch.empty_like(self.w)
+        self.db = torch.empty_like(self.b) if self.b is not None else None
+        self.ws = torch.empty(_abi.ccc_conv1d_bwd_workspace_size(d.x, deterministic),
+                              dtype=torch.uint8, device=device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        self.fwd_bytes = fwd_bytes(d.x, self.w, self.b, self.init, self.fin)
+        self.bwd_bytes = bwd_bytes(d.x, self.w, self.b, self.init, self.dfin, self.dinit)
+        self.tokens = inp.tokens if inp.cu_seqlens is None else d.x.shape[2]
+        self.launches_fwd = 1
+        self.launches_bwd = 2  # backward kernel + fixed-order finalize (plus a memset node)
+
+    def fwd(self, i, stream):
+        k = i % self.sets
+        rc = self.abi.ccc_conv1d_fwd(self.x[k], self.w, self.b, self.cu, self.init, self.out[k],
+                                     self.fin, self.act, self.status, stream)
+        assert rc == 0, self.abi.status_string(rc)
+
+    def bwd(self, i, stream):
+        k = i % self.sets
+        rc = self.abi.ccc_conv1d_bwd(self.x[k], self.w, self.b, self.cu, self.init, self.g[k],
+                                     self.dfin, self.dx[k], self.dw, self.db, self.dinit, self.act,
+                                     self.det, self.ws, self.status, stream)
+        assert rc == 0, self.abi.status_string(rc)
+
+    def check_status(self, stream):
+        rc = self.abi.ccc_read_status(self.status, stream)
+        assert rc == 0, self.abi.status_string(rc)
+
+
+def time_fwd_bwd(step: DenseStep, steps: int, warmup: int, stream, barrier=lambda: None):
+    for i in range(warmup):
+        step.fwd(i, stream)
+        step.bwd(i, stream)
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for i in range(steps):
+        e = evs[i]
+        e[0].record(stream)
+        step.fwd(warmup + i, stream)
+        e[1].record(stream)
+        step.bwd(warmup + i, stream)
+        e[2].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    total_ms = t0.elapsed_time(t1)
+    fwd_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    bwd_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    step.check_status(stream)
+    return total_ms, fwd_ms, bwd_ms
+
+
+# ---- breakdown over the other workloads ---------------------------------------------
+
+def _median_ms(fn, iters, stream):
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(iters)]
+    for i, (a, b) in enumerate(evs):
+        a.record(stream)
+        fn(i)
+        b.record(stream)
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in evs)
+
+
+def bench_conv_workload(name, inp, device, stream, peak, deterministic, iters=30, do_bwd=True):
+    st = DenseStep(inp, device, deterministic=deterministic)
+    for i in range(3):
+        st.fwd(i, stream)
+        if do_bwd:
+            st.bwd(i, stream)
+    torch.cuda.synchronize()
+    r = {"workload": name, "tokens": st.tokens, "rotating_sets": st.sets}
+    f_ms = _median_ms(lambda i: st.fwd(i, stream), iters, stream)
+    r["fwd"] = _rate(st.fwd_bytes, f_ms, st.tokens, peak)
+    if do_bwd:
+        b_ms = _median_ms(lambda i: st.bwd(i, stream), iters, stream)
+        r["bwd"] = _rate(st.bwd_bytes, b_ms, st.tokens, peak)
+    st.check_status(stream)
+    del st
+    torch.cuda.empty_cache()
+    return r
+
+
+def _rate(nbytes, ms, tokens, peak):
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"us": round(ms * 1e3, 2), "bytes": int(nbytes), "GB/s": round(gbs, 1),
+            "frac_of_peak": round(gbs / peak, 4), "tokens_per_s": round(tokens / (ms * 1e-3))}
+
+
+def bench_update(device, stream, peak, iters=50):
+    from depthwise_causal_conv1d_channel_gb300 import _abi
+
+    gen = torch.Generator(device=device).manual_seed(0)
+    B, D = 256, 4096
+    per = B * D * 3 * 2 + 2 * B * D * 2
+    sets = max(1, -(-3 * L2_BYTES // per))
+    state = [torch.randn(B, D, 3, device=device, generator=gen).to(torch.bfloat16) for _ in range(sets)]
+    x = [torch.randn(B, D, device=device, generator=gen).to(torch.bfloat16) for _ in range(sets)]
+    out = [torch.empty(B, D, dtype=torch.bfloat16, device=device) for _ in range(sets)]
+    w = (torch.rand(D, 4, device=device, generator=gen) - 0.5).to(torch.bfloat16)
+    b = ((torch.rand(D, device=device, generator=gen) - 0.5) * 0.2).to(torch.bfloat16)
+
+    def upd(i):
+        k = i % sets
+        rc = _abi.ccc_conv1d_update(x[k], state[k], w, b, out[k], _abi.CCC_ACT_SILU, stream)
+        assert rc == 0
+
+    for i in range(3):
+        upd(i)
+    ms = _median_ms(upd, iters, stream)
+    r = {"workload": "decode_update", "batch": B, "dim": D, "rotating_sets": sets,
+         "update": _rate(update_bytes(B, D, w, b), ms, B, peak)}
+    # 1000 chained steps on one state captured in a CUDA graph (hot in L2; context only)
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream(device)
+    s.wait_stream(torch.cuda.current_stream(device))
+    with torch.cuda.stream(s):
+        for _ in range(2):
+            upd(0)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=s):
+            for _ in range(1000):
+                rc = _abi.ccc_conv1d_update(x[0], state[0], w, b, out[0], _abi.CCC_ACT_SILU,
+                                            torch.cuda.current_stream(device))
+                assert rc == 0
+    torch.cuda.synchronize()
+    a, c = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    g.replay()
+    c.record(stream)
+    torch.cuda.synchronize()
+    r["graph_chain_1000"] = {"us_per_step": round(a.elapsed_time(c) * 1e3 / 1000, 3),
+                             "note": "one state, L2-resident, CUDA graph; not an HBM figure"}
+    return r
+
+
+# ---- end to end through the public API with host buffers ----------------------------
+
+def time_e2e(inp: workloads.ConvInputs, device, steps, warmup, stream):
+    """causal_conv1d + autograd backward, with the step's inputs copied from
+    pinned host memory and every result copied back, inside the timed region."""
+    import depthwise_causal_conv1d_channel_gb300 as ccc
+
+    def pinned(t):
+        if t is None:
+            return None
+        if inp.channel_last and t.dim() == 3 and t.shape == inp.x.shape:
+            return t.transpose(1, 2).contiguous().pin_memory()  # [B, T, D] storage
+        return t.contiguous().pin_memory()
+
+    hx, hg = pinned(inp.x), pinned(inp.g)
+    hw, hb, hi = pinned(inp.weight), pinned(inp.bias), pinned(inp.initial_states)
+    S, D = inp.n_seq, inp.x.shape[1]
+    ho = torch.empty_like(hx).pin_memory()
+    hdx = torch.empty_like(hx).pin_memory()
+    hf = torch.empty(S, D, 3, dtype=torch.bfloat16).pin_memory()
+    hdi = torch.empty_like(hi).pin_memory()
+    hdw = torch.empty_like(hw).pin_memory()
+    hdb = torch.empty_like(hb).pin_memory() if hb is not None else None
+    h2d = sum(act_bytes(t) for t in (hx, hg, hw, hb, hi) if t is not None)
+    d2h = sum(act_bytes(t) for t in (ho, hdx, hf, hdi, hdw, hdb) if t is not None)
+
+    def one():
+        x = hx.to(device, non_blocking=True)
+        g = hg.to(device, non_blocking=True)
+        if inp.channel_last:
+            x, g = x.transpose(1, 2), g.transpose(1, 2)
+        w = hw.to(device, non_blocking=True).requires_grad_(True)
+        b = hb.to(device, non_blocking=True).requires_grad_(True)
+        init = hi.to(device, non_blocking=True).requires_grad_(True)
+        x.requires_grad_(True)
+        out, fin = ccc.causal_conv1d(x, w, b, initial_states=init, return_final_states=True)
+        out.backward(g)
+        o = out.detach().transpose(1, 2) if inp.channel_last else out.detach()
+        dx = x.grad.transpose(1, 2) if inp.channel_last else x.grad
+        ho.copy_(o, non_blocking=True)
+        hdx.copy_(dx, non_blocking=True)
+        hf.copy_(fin.detach(), non_blocking=True)
+        hdi.copy_(init.grad, non_blocking=True)
+        hdw.copy_(w.grad, non_blocking=True)
+        hdb.copy_(b.grad, non_blocking=True)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    a, c = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        one()
+    c.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(c) / steps, h2d, d2h
+
+
+# ---- CPU oracle ---------------------------------------------------------------------
+
+def oracle_step_seconds(inp, min_seconds=10.0, max_reps=20, channels=None):
+    """The oracle's forward + backward on the workload (all channels unless a
+    sample is given), repeated until `min_seconds` have passed."""
+    import oracle
+    from workloads import bits
+
+    x, g, w, b, init = inp.x, inp.g, inp.weight, inp.bias, inp.initial_states
+    if channels is not None:
+        x, g, w = x[:, channels], g[:, channels], w[channels]
+        b = b[channels] if b is not None else None
+        init = init[:, channels] if init is not None else None
+    cu = None if inp.cu_seqlens is None else inp.cu_seqlens.numpy()
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.fwd(bits(x), bits(w), bits(b), cu, bits(init), inp.activation)
+        oracle.bwd(bits(x), bits(w), bits(g), bits(b), cu, bits(init), None, inp.activation)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds or reps >= max_reps:
+            break
+    nb = fwd_bytes(x, w, b, init, init) + bwd_bytes(x, w, b, init, None, init)
+    return el / reps, nb, reps, x.shape
+
+
+# ---- main ---------------------------------------------------------------------------
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    inp = workloads.dense_state()
+    D = inp.x.shape[1]
+    channels = list(range(0, D, 16))  # a 1/16 sample of the channels, every token
+    ms = []
+    for _ in range(args.warmup):
+        oracle_step_seconds(inp, 0.0, 1, channels)
+    for _ in range(args.steps):
+        s, nb, reps, shape = oracle_step_seconds(inp, 0.0, 1, channels)
+        ms.append(s * 1e3)
+    per = statistics.mean(ms)
+    value = nb / (per * 1e-3) / 1e9
+    sample = (f"dense_state workload, forward+backward on {len(channels)} of {D} channels "
+              f"(every 16th), all {inp.tokens} tokens, per step")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(per, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "dense_state", "x": [4, 2048, 1536], "layout": "channel-last",
+                   "sample_channels": len(channels)},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-breakdown", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+
+    rank, world, local = dist_env()
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+        pg = dist
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    import depthwise_causal_conv1d_channel_gb300  # noqa: F401  (loads the CUDA library)
+
+    stream = torch.cuda.current_stream(device)
+    peak, peak_kind = measured_peak()
+    inp = workloads.dense_state()
+    step = DenseStep(inp, device)
+
+    def barrier():
+        if pg is not None:
+            pg.barrier()
+
+    with ClockSampler(local) as clk:
+        total_ms, fwd_ms, bwd_ms = time_fwd_bwd(step, args.steps, args.warmup, stream, barrier)
+    clocks = clk.summary()
+
+    ms_step = total_ms / args.steps
+    if pg is not None:
+        t = torch.tensor([ms_step], device=device)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms_step = float(t.item())
+    step_bytes = step.fwd_bytes + step.bwd_bytes
+    value = world * step_bytes / (ms_step * 1e-3) / 1e9
+    tokens_per_s = world * step.tokens / (ms_step * 1e-3)
+
+    f_ms, b_ms = statistics.mean(fwd_ms), statistics.mean(bwd_ms)
+    dominant = ("bwd", b_ms, step.bwd_bytes) if b_ms >= f_ms else ("fwd", f_ms, step.fwd_bytes)
+    achieved = dominant[2] / (dominant[1] * 1e-3) / 1e9
+    traffic = TRAFFIC["bytes_per_launch"] if TRAFFIC["sources_sha256"] == kernel_sources_digest() else None
+
+    e2e_ms, h2d, d2h = time_e2e(inp, device, max(5, args.steps // 5), 3, stream)
+    e2e_value = world * step_bytes / (e2e_ms * 1e-3) / 1e9
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "dense_state", "x": [4, 2048, 1536], "layout": "channel-last",
+                   "weight": "bf16", "bias": True, "initial_states": True,
+                   "final_states": True, "dweight": "fp32-atomic",
+                   "step": "forward + backward", "parallelism": f"replicas{world}",
+                   "l2": f"rotating {step.sets} buffer sets, "
+                         f"{step.sets * 4 * act_bytes(step.x[0]) / 2**20:.0f} MiB > L2"},
+        "tokens_per_s": round(tokens_per_s),
+        "fwd_us": round(f_ms * 1e3, 2), "bwd_us": round(b_ms * 1e3, 2),
+        "gpu_launches": args.steps * (step.launches_fwd + step.launches_bwd),
+        "roofline": {"bound": "hbm", "kernel": f"{dominant[0]} call (dense_state)",
+                     "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "bytes_per_launch": dominant[2]},
+        "clocks": clocks,
+        "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
+                "api": "causal_conv1d + autograd backward"},
+    }
+
+    if not args.no_breakdown:
+        bd = [bench_conv_workload("dense_small", workloads.dense_small(), device, stream, peak,
+                                  False, do_bwd=False),
+              bench_conv_workload("dense_state", inp, device, stream, peak, False),
+              bench_conv_workload("packed_varlen", workloads.packed_varlen(), device, stream, peak,
+                                  True),
+              bench_update(device, stream, peak)]
+        large = workloads.dense_large(bias=True)
+        bd.append(bench_conv_workload("dense_large_bias", large, device, stream, peak, False,
+                                      iters=10))
+        large = dataclasses.replace(large, bias=None, deterministic=True)
+        bd.append(bench_conv_workload("dense_large_det", large, device, stream, peak, True,
+                                      iters=10))
+        line["breakdown"] = bd
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        s, nb, reps, shape = oracle_step_seconds(inp, 10.0, 10)
+        line["cpu_baseline"] = {"value": round(nb / s / 1e9, 4), "unit": UNIT, "cores": 1,
+                                "kind": "oracle",
+                                "sample": f"whole dense_state workload fwd+bwd, {reps} reps, "
+                                          f"{s:.2f} s each"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

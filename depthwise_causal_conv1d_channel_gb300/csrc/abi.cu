@@ -1,0 +1,489 @@
+// C ABI of the depthwise causal conv1d library: argument checks, layout
+// detection, aliasing checks, launch planning and dispatch.  Every check runs
+// before anything is enqueued, so a rejected call writes nothing.
+#include <algorithm>
+#include <atomic>
+#include <stdint.h>
+
+#include "ccc_conv1d.h"
+#include "launch.h"
+
+namespace {
+
+using ccc::kState;
+using ccc::kWidth;
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+int next_pow2(int64_t v) {
+  int p = 1;
+  while (p < v && p < (1 << 30)) p <<= 1;
+  return p;
+}
+
+size_t elem_size(int dtype) { return dtype == CCC_BF16 ? 2 : 4; }
+
+bool valid_dtype(int dtype) { return dtype == CCC_BF16 || dtype == CCC_F32 || dtype == CCC_I32; }
+
+int64_t numel(const ccc_tensor* t) {
+  int64_t n = 1;
+  for (int i = 0; i < t->ndim; ++i) n *= t->shape[i];
+  return n;
+}
+
+// Basic sanity of a descriptor: rank, non-negative sizes and strides, data
+// present when the tensor is non-empty.
+bool well_formed(const ccc_tensor* t, int ndim) {
+  if (!t || t->ndim != ndim || !valid_dtype(t->dtype)) return false;
+  for (int i = 0; i < ndim; ++i)
+    if (t->shape[i] < 0 || t->stride[i] < 0) return false;
+  return numel(t) == 0 || t->data != nullptr;
+}
+
+bool shape_is(const ccc_tensor* t, int64_t a, int64_t b = -1, int64_t c = -1) {
+  const int64_t s[3] = {a, b, c};
+  for (int i = 0; i < t->ndim; ++i)
+    if (t->shape[i] != s[i]) return false;
+  return true;
+}
+
+// [first, last) byte range the tensor's elements occupy; empty when numel == 0.
+void byte_range(const ccc_tensor* t, uintptr_t& first, uintptr_t& last) {
+  if (!t || numel(t) == 0) { first = last = 0; return; }
+  int64_t span = 0;
+  for (int i = 0; i < t->ndim; ++i) span += (t->shape[i] - 1) * t->stride[i];
+  first = reinterpret_cast<uintptr_t>(t->data);
+  last = first + uintptr_t((span + 1) * int64_t(elem_size(t->dtype)));
+}
+
+bool overlaps(const ccc_tensor* a, const ccc_tensor* b) {
+  uintptr_t a0, a1, b0, b1;
+  byte_range(a, a0, a1);
+  byte_range(b, b0, b1);
+  return a0 < a1 && b0 < b1 && a0 < b1 && b0 < a1;
+}
+
+// No two index tuples of the tensor share an element (needed for outputs).
+bool self_disjoint(const ccc_tensor* t) {
+  int idx[3];
+  int n = 0;
+  for (int i = 0; i < t->ndim; ++i)
+    if (t->shape[i] > 1) idx[n++] = i;
+  for (int i = 1; i < n; ++i)  // insertion sort by stride (n <= 3)
+    for (int j = i; j > 0 && t->stride[idx[j]] < t->stride[idx[j - 1]]; --j) {
+      const int tmp = idx[j];
+      idx[j] = idx[j - 1];
+      idx[j - 1] = tmp;
+    }
+  int64_t reach = 0;  // largest offset reachable with the smaller-stride dims
+  for (int j = 0; j < n; ++j) {
+    const int i = idx[j];
+    if (t->stride[i] <= reach) return false;
+    reach += (t->shape[i] - 1) * t->stride[i];
+  }
+  return true;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// Layout of a [B, D, T] activation.  Size-1 dims do not constrain the layout.
+int layout_of(const ccc_tensor* t) {
+  const bool d_unit = t->shape[1] <= 1 || t->stride[1] == 1;
+  const bool t_unit = t->shape[2] <= 1 || t->stride[2] == 1;
+  if (d_unit) return ccc::kLayoutChannelLast;
+  if (t_unit) return ccc::kLayoutTimeContiguous;
+  return -1;
+}
+
+// Effective strides with size-1 dims normalised to what the kernels expect.
+void act_strides(const ccc_tensor* t, int layout, int64_t& sb, int64_t& sd, int64_t& st) {
+  sb = t->shape[0] <= 1 ? 0 : t->stride[0];
+  sd = t->shape[1] <= 1 ? (layout == ccc::kLayoutChannelLast ? 1 : 0) : t->stride[1];
+  st = t->shape[2] <= 1 ? (layout == ccc::kLayoutTimeContiguous ? 1 : 0) : t->stride[2];
+}
+
+// State tensors: [S, D, 3] BF16, contiguous.
+bool state_ok(const ccc_tensor* t, int64_t S, int64_t D) {
+  if (!well_formed(t, 3) || t->dtype != CCC_BF16 || !shape_is(t, S, D, kState)) return false;
+  if (numel(t) == 0) return true;
+  return (S <= 1 || t->stride[0] == D * kState) && (D <= 1 || t->stride[1] == kState) &&
+         t->stride[2] == 1;
+}
+
+int device_sm_count() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return sms;
+}
+
+// Common checks of the tensors forward and backward share.
+struct Problem {
+  int B = 0, D = 0;
+  int64_t T = 0;
+  int n_seq = 0;  // sequences (states): B, or N when packed
+  bool packed = false;
+  int layout = -1;
+  int w_f32 = 0;
+};
+
+ccc_status check_common(const ccc_tensor* x, const ccc_tensor* weight, const ccc_tensor* bias,
+                        const ccc_tensor* cu, const ccc_tensor* init, int activation, Problem& pb) {
+  if (!well_formed(x, 3) || x->dtype != CCC_BF16) return CCC_ERR_INVALID_ARG;
+  if (x->shape[1] < 1) return CCC_ERR_INVALID_ARG;
+  if (x->shape[0] > INT32_MAX || x->shape[1] > INT32_MAX) return CCC_ERR_UNSUPPORTED;
+  pb.B = int(x->shape[0]);
+  pb.D = int(x->shape[1]);
+  pb.T = x->shape[2];
+  pb.layout = layout_of(x);
+  if (pb.layout < 0) return CCC_ERR_UNSUPPORTED;
+  if (activation != CCC_ACT_NONE && activation != CCC_ACT_SILU) return CCC_ERR_INVALID_ARG;
+
+  if (!weight || weight->ndim != 2) return CCC_ERR_INVALID_ARG;
+  if (!well_formed(weight, 2) || weight->shape[0] != pb.D) return CCC_ERR_INVALID_ARG;
+  if (weight->shape[1] != kWidth) return CCC_ERR_UNSUPPORTED;  // width four only
+  if (weight->dtype != CCC_BF16 && weight->dtype != CCC_F32) return CCC_ERR_INVALID_ARG;
+  pb.w_f32 = weight->dtype == CCC_F32;
+
+  if (bias) {
+    if (!well_formed(bias, 1) || bias->dtype != CCC_BF16 || !shape_is(bias, pb.D))
+      return CCC_ERR_INVALID_ARG;
+    if (pb.w_f32) return CCC_ERR_UNSUPPORTED;  // FP32 weight with bias declines
+  }
+
+  pb.packed = cu != nullptr;
+  if (pb.packed) {
+    if (!well_formed(cu, 1) || cu->dtype != CCC_I32 || cu->shape[0] < 2) return CCC_ERR_INVALID_ARG;
+    if (cu->stride[0] != 1) return CCC_ERR_UNSUPPORTED;
+    if (pb.B != 1 || pb.T > INT32_MAX || cu->shape[0] - 1 > INT32_MAX) return CCC_ERR_UNSUPPORTED;
+    if (pb.T == 0) return CCC_ERR_INVALID_ARG;  // N >= 1 non-empty sequences need tokens
+    pb.n_seq = int(cu->shape[0] - 1);
+  } else {
+    pb.n_seq = pb.B;
+  }
+  if (init && !state_ok(init, pb.n_seq, pb.D)) return CCC_ERR_INVALID_ARG;
+  return CCC_OK;
+}
+
+bool same_act_shape(const ccc_tensor* t, const Problem& pb) {
+  return well_formed(t, 3) && t->dtype == CCC_BF16 && shape_is(t, pb.B, pb.D, pb.T);
+}
+
+// Whether 16-byte vectors of 8 channels can serve every channel-last tensor.
+bool vec8_ok(const Problem& pb, std::initializer_list<const ccc_tensor*> acts,
+             std::initializer_list<const ccc_tensor*> states) {
+  if (pb.layout != ccc::kLayoutChannelLast || pb.D % 8 != 0) return false;
+  for (const ccc_tensor* t : acts) {
+    int64_t sb, sd, st;
+    act_strides(t, pb.layout, sb, sd, st);
+    if (!aligned16(t->data) || sb % 8 != 0 || st % 8 != 0) return false;
+  }
+  for (const ccc_tensor* t : states)
+    if (t && !aligned16(t->data)) return false;
+  return true;
+}
+
+ccc::WeightRef weight_ref(const ccc_tensor* weight, const ccc_tensor* bias) {
+  ccc::WeightRef r{};
+  r.w = weight->data;
+  r.w_f32 = weight->dtype == CCC_F32;
+  r.w_sd = weight->stride[0];
+  r.w_sk = weight->stride[1];
+  r.bias = bias ? static_cast<const uint16_t*>(bias->data) : nullptr;
+  r.b_sd = bias ? bias->stride[0] : 0;
+  return r;
+}
+
+ccc::Seqs seqs_of(const Problem& pb, const ccc_tensor* cu) {
+  ccc::Seqs s{};
+  s.cu = pb.packed ? static_cast<const int*>(cu->data) : nullptr;
+  s.n_seq = pb.n_seq;
+  s.T = pb.T;
+  s.Q = pb.packed ? pb.T : int64_t(pb.B) * pb.T;
+  return s;
+}
+
+}  // namespace
+
+namespace ccc {
+
+// Channel-last launch shape: a block is (tx channel groups) x (ty token ranges);
+// the token ranges are sized so the grid holds about `waves` full waves of
+// resident blocks, each range at least `min_seg` tokens long.
+static FwdPlan plan_cl(int vec, int64_t Q, int D, int sm_count, int blocks_per_sm, int waves,
+                       int64_t min_seg) {
+  FwdPlan p{};
+  p.kind = kLayoutChannelLast;
+  p.vec = vec;
+  const int64_t G = ceil_div(D, vec);
+  p.tx = int(std::min<int64_t>(32, next_pow2(G)));
+  p.ty = 256 / p.tx;
+  p.gx = unsigned(ceil_div(G, p.tx));
+  const int64_t want = std::max<int64_t>(1, int64_t(sm_count) * std::max(1, blocks_per_sm) * waves);
+  int64_t gy = std::max<int64_t>(1, want / p.gx);
+  int64_t seg = std::max<int64_t>(min_seg, ceil_div(std::max<int64_t>(Q, 1), gy * p.ty));
+  int64_t n_seg = ceil_div(std::max<int64_t>(Q, 1), seg);
+  gy = ceil_div(n_seg, p.ty);
+  if (gy > 65535) {
+    seg = ceil_div(Q, int64_t(65535) * p.ty);
+    n_seg = ceil_div(Q, seg);
+    gy = ceil_div(n_seg, p.ty);
+  }
+  p.gy = unsigned(gy);
+  p.seg_len = seg;
+  p.n_seg = n_seg;
+  return p;
+}
+
+static FwdPlan plan_bdt(int64_t rows) {
+  FwdPlan p{};
+  p.kind = kLayoutTimeContiguous;
+  p.vec = 1;
+  p.tx = 256;
+  p.ty = 1;
+  p.gx = unsigned(ceil_div(std::max<int64_t>(rows, 1), 8));  // 8 warps, one row each
+  p.gy = 1;
+  return p;
+}
+
+FwdPlan plan_fwd(int kind, int vec_ok, int64_t Q, int D, int64_t rows, int sm_count) {
+  if (kind == kLayoutTimeContiguous) return plan_bdt(rows);
+  const int vec = vec_ok ? 8 : 1;
+  return plan_cl(vec, Q, D, sm_count, fwd_blocks_per_sm(vec), 4, 8);
+}
+
+BwdPlan plan_bwd(int kind, int vec_ok, int64_t Q, int D, int64_t rows, int sm_count) {
+  if (kind == kLayoutTimeContiguous) return plan_bdt(rows);
+  const int vec = vec_ok ? 8 : 1;
+  return plan_cl(vec, Q, D, sm_count, bwd_blocks_per_sm(vec), 4, 16);
+}
+
+int64_t bwd_partial_rows(const BwdPlan& p, int B, bool packed) {
+  if (p.kind == kLayoutTimeContiguous) return packed ? 1 : std::max(B, 1);
+  return p.gy;
+}
+
+}  // namespace ccc
+
+extern "C" {
+
+int ccc_conv1d_abi_version(void) { return CCC_CONV1D_ABI_VERSION; }
+
+const char* ccc_status_string(int status) {
+  switch (status) {
+    case CCC_OK: return "ok";
+    case CCC_ERR_INVALID_ARG: return "invalid argument";
+    case CCC_ERR_UNSUPPORTED: return "unsupported (declined) configuration";
+    case CCC_ERR_ALIAS: return "an output overlaps an input or another output";
+    case CCC_ERR_NONDETERMINISTIC: return "no deterministic route for a call with bias";
+    case CCC_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
+    case CCC_ERR_CUDA: return "CUDA error";
+    case CCC_ERR_BAD_CU_SEQLENS: return "malformed cu_seqlens";
+    default: return "unknown status";
+  }
+}
+
+ccc_status ccc_conv1d_fwd(const ccc_tensor* x, const ccc_tensor* weight, const ccc_tensor* bias,
+                          const ccc_tensor* cu_seqlens, const ccc_tensor* initial_states,
+                          const ccc_tensor* out, const ccc_tensor* final_states, int activation,
+                          int* d_status, cudaStream_t stream) {
+  Problem pb;
+  ccc_status st = check_common(x, weight, bias, cu_seqlens, initial_states, activation, pb);
+  if (st != CCC_OK) return st;
+  if (!same_act_shape(out, pb)) return CCC_ERR_INVALID_ARG;
+  if (layout_of(out) != pb.layout || !self_disjoint(out)) return CCC_ERR_UNSUPPORTED;
+  if (final_states && !state_ok(final_states, pb.n_seq, pb.D)) return CCC_ERR_INVALID_ARG;
+  // final_states must not share memory with the inputs (cuDNN page, aliasing rule);
+  // neither may out.
+  for (const ccc_tensor* in : {x, weight, bias, cu_seqlens, initial_states}) {
+    if (!in) continue;
+    if ((final_states && overlaps(final_states, in)) || overlaps(out, in)) return CCC_ERR_ALIAS;
+  }
+  if (final_states && overlaps(final_states, out)) return CCC_ERR_ALIAS;
+
+  const int sms = device_sm_count();
+  if (sms <= 0) return CCC_ERR_CUDA;
+  ccc::FwdArgs a{};
+  a.x = static_cast<const uint16_t*>(x->data);
+  a.out = static_cast<uint16_t*>(out->data);
+  act_strides(x, pb.layout, a.x_sb, a.x_sd, a.x_st);
+  act_strides(out, pb.layout, a.o_sb, a.o_sd, a.o_st);
+  a.wr = weight_ref(weight, bias);
+  a.init = initial_states ? static_cast<const uint16_t*>(initial_states->data) : nullptr;
+  a.fin = final_states ? static_cast<uint16_t*>(final_states->data) : nullptr;
+  a.seqs = seqs_of(pb, cu_seqlens);
+  a.B = pb.B;
+  a.D = pb.D;
+  a.status = d_status;
+  if (pb.n_seq == 0) return CCC_OK;
+  const bool v8 = vec8_ok(pb, {x, out}, {initial_states, final_states});
+  const int64_t rows = pb.packed ? pb.D : int64_t(pb.B) * pb.D;
+  const ccc::FwdPlan p = ccc::plan_fwd(pb.layout, v8, a.seqs.Q, pb.D, rows, sms);
+  a.seg_len = p.seg_len;
+  a.n_seg = p.n_seg;
+  return ccc::launch_fwd(a, p, activation, stream) == cudaSuccess ? CCC_OK : CCC_ERR_CUDA;
+}
+
+// Shared by the size query and the call itself, so both agree.
+static bool bwd_plan_for(const ccc_tensor* x, const Problem& pb, bool v8, ccc::BwdPlan& p) {
+  const int sms = device_sm_count();
+  if (sms <= 0) return false;
+  const int64_t Q = pb.packed ? pb.T : int64_t(pb.B) * pb.T;
+  const int64_t rows = pb.packed ? pb.D : int64_t(pb.B) * pb.D;
+  (void)x;
+  p = ccc::plan_bwd(pb.layout, v8, Q, pb.D, rows, sms);
+  return true;
+}
+
+static size_t bwd_ws_bytes(const ccc::BwdPlan& p, const Problem& pb, int deterministic) {
+  const int64_t rows = deterministic ? ccc::bwd_partial_rows(p, pb.B, pb.packed) : 1;
+  return size_t(std::max<int64_t>(rows, 1)) * size_t(pb.D) * (kWidth + 1) * sizeof(float);
+}
+
+size_t ccc_conv1d_bwd_workspace_size(const ccc_tensor* x, int deterministic) {
+  if (!well_formed(x, 3) || x->dtype != CCC_BF16 || x->shape[1] < 1) return 0;
+  if (x->shape[0] > INT32_MAX || x->shape[1] > INT32_MAX) return 0;
+  Problem pb;
+  pb.B = int(x->shape[0]);
+  pb.D = int(x->shape[1]);
+  pb.T = x->shape[2];
+  pb.layout = layout_of(x);
+  if (pb.layout < 0) return 0;
+  // The call picks 8-channel vectors or scalars from the alignment of all its
+  // tensors, and a packed call needs no more than a dense one: cover both.
+  ccc::BwdPlan p8{}, p1{};
+  if (!bwd_plan_for(x, pb, true, p8) || !bwd_plan_for(x, pb, false, p1)) return 0;
+  const size_t n = std::max(bwd_ws_bytes(p8, pb, deterministic), bwd_ws_bytes(p1, pb, deterministic));
+  return (n + 255) / 256 * 256;
+}
+
+ccc_status ccc_conv1d_bwd(const ccc_tensor* x, const ccc_tensor* weight, const ccc_tensor* bias,
+                          const ccc_tensor* cu_seqlens, const ccc_tensor* initial_states,
+                          const ccc_tensor* dout, const ccc_tensor* dfinal_states,
+                          const ccc_tensor* dx, const ccc_tensor* dweight, const ccc_tensor* dbias,
+                          const ccc_tensor* dinitial_states, int activation, int deterministic,
+                          void* workspace, size_t workspace_bytes, int* d_status,
+                          cudaStream_t stream) {
+  Problem pb;
+  ccc_status st = check_common(x, weight, bias, cu_seqlens, initial_states, activation, pb);
+  if (st != CCC_OK) return st;
+  if (!same_act_shape(dout, pb) || !same_act_shape(dx, pb)) return CCC_ERR_INVALID_ARG;
+  if (layout_of(dout) != pb.layout || layout_of(dx) != pb.layout || !self_disjoint(dx))
+    return CCC_ERR_UNSUPPORTED;
+  if (dfinal_states && !state_ok(dfinal_states, pb.n_seq, pb.D)) return CCC_ERR_INVALID_ARG;
+  if (!dweight || !well_formed(dweight, 2) || !shape_is(dweight, pb.D, kWidth) ||
+      dweight->dtype != weight->dtype || !self_disjoint(dweight))
+    return CCC_ERR_INVALID_ARG;
+  if ((bias == nullptr) != (dbias == nullptr)) return CCC_ERR_INVALID_ARG;
+  if (dbias && (!well_formed(dbias, 1) || dbias->dtype != CCC_BF16 || !shape_is(dbias, pb.D) ||
+                !self_disjoint(dbias)))
+    return CCC_ERR_INVALID_ARG;
+  if (dinitial_states && (!initial_states || !state_ok(dinitial_states, pb.n_seq, pb.D)))
+    return CCC_ERR_INVALID_ARG;
+  if (deterministic != 0 && deterministic != 1) return CCC_ERR_INVALID_ARG;
+  if (deterministic && bias) return CCC_ERR_NONDETERMINISTIC;
+
+  // outputs vs inputs, and outputs vs each other
+  const ccc_tensor* ins[] = {x, weight, bias, cu_seqlens, initial_states, dout, dfinal_states};
+  const ccc_tensor* outs[] = {dx, dweight, dbias, dinitial_states};
+  for (const ccc_tensor* o : outs) {
+    if (!o) continue;
+    for (const ccc_tensor* in : ins)
+      if (in && overlaps(o, in)) return CCC_ERR_ALIAS;
+  }
+  for (int i = 0; i < 4; ++i)
+    for (int j = i + 1; j < 4; ++j)
+      if (outs[i] && outs[j] && overlaps(outs[i], outs[j])) return CCC_ERR_ALIAS;
+
+  const bool v8 = vec8_ok(pb, {x, dout, dx}, {initial_states, dfinal_states, dinitial_states});
+  ccc::BwdPlan p{};
+  if (!bwd_plan_for(x, pb, v8, p)) return CCC_ERR_CUDA;
+  const size_t need = bwd_ws_bytes(p, pb, deterministic);
+  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return CCC_ERR_WORKSPACE;
+  {
+    // the workspace is an output too
+    ccc_tensor wt{workspace, CCC_F32, 1, {int64_t(need / 4), 0, 0}, {1, 0, 0}};
+    for (const ccc_tensor* in : ins)
+      if (in && overlaps(&wt, in)) return CCC_ERR_ALIAS;
+    for (const ccc_tensor* o : outs)
+      if (o && overlaps(&wt, o)) return CCC_ERR_ALIAS;
+  }
+
+  ccc::BwdArgs a{};
+  a.x = static_cast<const uint16_t*>(x->data);
+  a.g = static_cast<const uint16_t*>(dout->data);
+  a.dx = static_cast<uint16_t*>(dx->data);
+  act_strides(x, pb.layout, a.x_sb, a.x_sd, a.x_st);
+  act_strides(dout, pb.layout, a.g_sb, a.g_sd, a.g_st);
+  act_strides(dx, pb.layout, a.dx_sb, a.dx_sd, a.dx_st);
+  a.wr = weight_ref(weight, bias);
+  a.init = initial_states ? static_cast<const uint16_t*>(initial_states->data) : nullptr;
+  a.dfin = dfinal_states ? static_cast<const uint16_t*>(dfinal_states->data) : nullptr;
+  a.dinit = dinitial_states ? static_cast<uint16_t*>(dinitial_states->data) : nullptr;
+  a.seqs = seqs_of(pb, cu_seqlens);
+  a.B = pb.B;
+  a.D = pb.D;
+  a.seg_len = p.seg_len;
+  a.n_seg = p.n_seg;
+  a.ws = static_cast<float*>(workspace);
+  a.deterministic = deterministic;
+  a.status = d_status;
+
+  ccc::WgradOut o{};
+  o.dw = dweight->data;
+  o.dw_f32 = dweight->dtype == CCC_F32;
+  o.dw_sd = dweight->stride[0];
+  o.dw_sk = dweight->stride[1];
+  o.db = dbias ? static_cast<uint16_t*>(dbias->data) : nullptr;
+  o.db_sd = dbias ? dbias->stride[0] : 0;
+  const int64_t R = ccc::bwd_partial_rows(p, pb.B, pb.packed);
+  return ccc::launch_bwd(a, p, activation, o, R, stream) == cudaSuccess ? CCC_OK : CCC_ERR_CUDA;
+}
+
+ccc_status ccc_conv1d_update(const ccc_tensor* x, const ccc_tensor* conv_state,
+                             const ccc_tensor* weight, const ccc_tensor* bias,
+                             const ccc_tensor* out, int activation, cudaStream_t stream) {
+  if (!well_formed(x, 2) || x->dtype != CCC_BF16 || x->shape[1] < 1) return CCC_ERR_INVALID_ARG;
+  if (x->shape[0] > INT32_MAX || x->shape[1] > INT32_MAX) return CCC_ERR_UNSUPPORTED;
+  const int B = int(x->shape[0]), D = int(x->shape[1]);
+  if (D > 1 && x->stride[1] != 1) return CCC_ERR_UNSUPPORTED;
+  if (activation != CCC_ACT_NONE && activation != CCC_ACT_SILU) return CCC_ERR_INVALID_ARG;
+  if (!state_ok(conv_state, B, D)) return CCC_ERR_INVALID_ARG;
+  if (!weight || !well_formed(weight, 2) || weight->shape[0] != D) return CCC_ERR_INVALID_ARG;
+  if (weight->shape[1] != kWidth) return CCC_ERR_UNSUPPORTED;
+  if (weight->dtype != CCC_BF16 && weight->dtype != CCC_F32) return CCC_ERR_INVALID_ARG;
+  if (bias) {
+    if (!well_formed(bias, 1) || bias->dtype != CCC_BF16 || !shape_is(bias, D))
+      return CCC_ERR_INVALID_ARG;
+    if (weight->dtype == CCC_F32) return CCC_ERR_UNSUPPORTED;
+  }
+  if (!well_formed(out, 2) || out->dtype != CCC_BF16 || !shape_is(out, B, D)) return CCC_ERR_INVALID_ARG;
+  if ((D > 1 && out->stride[1] != 1) || !self_disjoint(out)) return CCC_ERR_UNSUPPORTED;
+  for (const ccc_tensor* in : {conv_state, weight, bias})
+    if (in && overlaps(out, in)) return CCC_ERR_ALIAS;
+  if (overlaps(x, conv_state)) return CCC_ERR_ALIAS;
+
+  ccc::UpdArgs a{};
+  a.x = static_cast<const uint16_t*>(x->data);
+  a.x_sb = B > 1 ? x->stride[0] : 0;
+  a.state = static_cast<uint16_t*>(conv_state->data);
+  a.out = static_cast<uint16_t*>(out->data);
+  a.o_sb = B > 1 ? out->stride[0] : 0;
+  a.wr = weight_ref(weight, bias);
+  a.B = B;
+  a.D = D;
+  const bool v8 = D % 8 == 0 && aligned16(x->data) && aligned16(out->data) &&
+                  aligned16(conv_state->data) && a.x_sb % 8 == 0 && a.o_sb % 8 == 0;
+  return ccc::launch_update(a, v8 ? 8 : 1, activation, stream) == cudaSuccess ? CCC_OK : CCC_ERR_CUDA;
+}
+
+ccc_status ccc_read_status(int* d_status, cudaStream_t stream) {
+  if (!d_status) return CCC_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return CCC_ERR_CUDA;
+  int h = 0;
+  if (cudaMemcpy(&h, d_status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return CCC_ERR_CUDA;
+  if (h != 0 && cudaMemset(d_status, 0, sizeof(int)) != cudaSuccess) return CCC_ERR_CUDA;
+  return static_cast<ccc_status>(h);
+}
+
+}  // extern "C"

@@ -1,0 +1,344 @@
+// Backward kernels of the depthwise causal conv1d (cuDNN frontend docs, "Causal
+// Conv1d" page: forward and backward on the optimized route; the paragraph on
+// determinism -- FP32 atomics by default, unique FP32 partials plus a
+// fixed-order reduction when deterministic).
+//
+// With gp[t] = dout[t] * act'(pre[t]) (pre recomputed from x, nothing saved):
+//   dxe[j] = sum_k w[k] * gp[j + 3 - k]  (+ dfinal[j - (len-3)] for j >= len-3)
+//   dx = dxe[0 .. len), dinit = dxe[-3 .. 0)
+//   dw[k] = sum gp[t] * xe[t - 3 + k],  db = sum gp[t]
+// A thread owns V channels and a token range [a, e); it walks m from a to
+// e + 2, computing gp[m] (three tokens past e are recomputed, not
+// accumulated) and emitting dxe[m - 3] once gp[m-3 .. m] are known.  The
+// thread whose range starts a sequence also emits the three dinit entries.
+#include <atomic>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace ccc {
+
+template <int V, int ACT, int U>
+__device__ __forceinline__ void bwd_walk(const BwdArgs& a, const Seqs& seqs, const Stream& xs,
+                                         const Stream& gs, const Stream& ds, int n_base, int d0,
+                                         const float (&w)[V][kWidth], const float (&b)[V],
+                                         int64_t q, int64_t q_end, float (&aw)[V][kWidth],
+                                         float (&ab)[V]) {
+  using VT = Vec<V>;
+  int n = find_seq(seqs, q);
+  while (q < q_end) {
+    int64_t lo, hi;
+    seq_bounds(seqs, n, lo, hi);
+    const int64_t a0 = q;
+    const int64_t e = q_end < hi ? q_end : hi;
+    const bool starts = a0 == lo;
+    const int64_t state_row = (int64_t(n_base) + n) * a.D + d0;
+
+    float xw[kState][V];  // xe[m-3 .. m-1]
+    float gw[kState][V];  // gp[m-3 .. m-1]; entries before a0 are never emitted from,
+                          // except before a sequence start, where gp is zero
+    float di[kState][V];  // dinit entries of this sequence (only when starts)
+    {
+      float init[kState][V];
+      if (a0 - kState < lo && a.init) {
+        load_state<V>(a.init + state_row * kState, init);
+      } else {
+#pragma unroll
+        for (int i = 0; i < kState; ++i)
+#pragma unroll
+          for (int c = 0; c < V; ++c) init[i][c] = 0.0f;
+      }
+#pragma unroll
+      for (int j = 0; j < kState; ++j) {
+        const int64_t tok = a0 - kState + j;
+        if (tok >= lo) {
+          VT::unpack(VT::ld(a.x + xs.at(n, tok)), xw[j]);
+        } else {
+          const int64_t i = tok - lo + kState;
+#pragma unroll
+          for (int c = 0; c < V; ++c)
+            xw[j][c] = i == 0 ? init[0][c] : (i == 1 ? init[1][c] : init[2][c]);
+        }
+#pragma unroll
+        for (int c = 0; c < V; ++c) { gw[j][c] = 0.0f; di[j][c] = 0.0f; }
+      }
+    }
+
+    // gp at token m from its inputs; accumulate the weight/bias sums when m is
+    // one of this thread's tokens; shift the input window.
+    auto grad_at = [&](typename VT::Raw xr, typename VT::Raw gr, bool own, float (&gp)[V]) {
+      float xc[V], gc[V];
+      VT::unpack(xr, xc);
+      VT::unpack(gr, gc);
+#pragma unroll
+      for (int c = 0; c < V; ++c) {
+        float p = b[c];
+        p = fmaf(w[c][0], xw[0][c], p);
+        p = fmaf(w[c][1], xw[1][c], p);
+        p = fmaf(w[c][2], xw[2][c], p);
+        p = fmaf(w[c][3], xc[c], p);
+        gp[c] = gc[c] * act_grad<ACT>(p);
+        if (own) {
+          aw[c][0] = fmaf(gp[c], xw[0][c], aw[c][0]);
+          aw[c][1] = fmaf(gp[c], xw[1][c], aw[c][1]);
+          aw[c][2] = fmaf(gp[c], xw[2][c], aw[c][2]);
+          aw[c][3] = fmaf(gp[c], xc[c], aw[c][3]);
+          ab[c] += gp[c];
+        }
+        xw[0][c] = xw[1][c];
+        xw[1][c] = xw[2][c];
+        xw[2][c] = xc[c];
+      }
+    };
+    // dxe[m - 3] from gp[m] and the window gp[m-3 .. m-1]; shift the window.
+    auto emit = [&](const float (&gp)[V], float (&v)[V]) {
+#pragma unroll
+      for (int c = 0; c < V; ++c) {
+        float s = w[c][0] * gp[c];
+        s = fmaf(w[c][1], gw[2][c], s);
+        s = fmaf(w[c][2], gw[1][c], s);
+        s = fmaf(w[c][3], gw[0][c], s);
+        v[c] = s;
+        gw[0][c] = gw[1][c];
+        gw[1][c] = gw[2][c];
+        gw[2][c] = gp[c];
+      }
+    };
+
+    // General step: any m in [a0, e + 3).
+    auto slow = [&](int64_t m) {
+      float gp[V], v[V];
+      if (m < hi) {
+        grad_at(VT::ld(a.x + xs.at(n, m)), VT::ld(a.g + gs.at(n, m)), m < e, gp);
+      } else {
+#pragma unroll
+        for (int c = 0; c < V; ++c) gp[c] = 0.0f;
+      }
+      const int64_t j = m - kState;
+      emit(gp, v);
+      if (j >= a0 || starts) {
+        if (a.dfin && j >= hi - kState) {
+          const int64_t i = j - (hi - kState);
+#pragma unroll
+          for (int c = 0; c < V; ++c) v[c] += bf16_to_f32(__ldg(a.dfin + (state_row + c) * kState + i));
+        }
+        if (j >= lo) {
+          VT::st(a.dx + ds.at(n, j), VT::pack(v));
+        } else if (a.dinit) {
+          const int64_t i = j - lo + kState;
+#pragma unroll
+          for (int c = 0; c < V; ++c) {
+            if (i == 0) di[0][c] = v[c];
+            else if (i == 1) di[1][c] = v[c];
+            else di[2][c] = v[c];
+          }
+          if (i == kState - 1) store_state<V>(a.dinit + state_row * kState, di);
+        }
+      }
+    };
+
+    int64_t m = a0;
+    const int64_t m_end = e + kState;
+    const int64_t pro_end = a0 + kState < m_end ? a0 + kState : m_end;
+    for (; m < pro_end; ++m) slow(m);
+    // steady state: own tokens, emissions land in [a0, e - 3), no state involved
+    for (; m + U <= e; m += U) {
+      typename VT::Raw xr[U], gr[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        xr[u] = VT::ld(a.x + xs.at(n, m + u));
+        gr[u] = VT::ld(a.g + gs.at(n, m + u));
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        float gp[V], v[V];
+        grad_at(xr[u], gr[u], true, gp);
+        emit(gp, v);
+        VT::st(a.dx + ds.at(n, m + u - kState), VT::pack(v));
+      }
+    }
+    for (; m < m_end; ++m) slow(m);
+
+    q = e;
+    ++n;
+  }
+}
+
+// Block-wide sum of the per-thread weight/bias sums over threadIdx.y (threads
+// with equal threadIdx.x own the same channels), in a fixed order, then either
+// FP32 atomics into ws[0] or a store into this block row's partial ws[blockIdx.y].
+template <int V>
+__device__ __forceinline__ void block_wgrad_out(const BwdArgs& a, int d0, bool active,
+                                                const float (&aw)[V][kWidth], const float (&ab)[V]) {
+  extern __shared__ float red[];  // [ty][tx][V * 5]
+  constexpr int P = V * (kWidth + 1);
+  float* mine = red + (threadIdx.y * blockDim.x + threadIdx.x) * P;
+#pragma unroll
+  for (int c = 0; c < V; ++c) {
+#pragma unroll
+    for (int k = 0; k < kWidth; ++k) mine[c * (kWidth + 1) + k] = active ? aw[c][k] : 0.0f;
+    mine[c * (kWidth + 1) + kWidth] = active ? ab[c] : 0.0f;
+  }
+  __syncthreads();
+  // each of the block's threads finalises a slice of the tx * P values
+  const int nthr = blockDim.x * blockDim.y;
+  const int tid = threadIdx.y * blockDim.x + threadIdx.x;
+  const int total = blockDim.x * P;
+  const int dbase = blockIdx.x * blockDim.x * V;
+  for (int i = tid; i < total; i += nthr) {
+    const int tx = i / P, r = i % P;
+    const int d = dbase + tx * V + r / (kWidth + 1);
+    if (d >= a.D) continue;
+    float s = 0.0f;
+    for (int y = 0; y < int(blockDim.y); ++y) s += red[(y * blockDim.x + tx) * P + r];
+    const int k = r % (kWidth + 1);
+    if (a.deterministic)
+      a.ws[(int64_t(blockIdx.y) * a.D + d) * (kWidth + 1) + k] = s;
+    else
+      atomicAdd(a.ws + int64_t(d) * (kWidth + 1) + k, s);
+  }
+}
+
+template <int V, int ACT>
+__global__ void __launch_bounds__(256) bwd_cl_kernel(BwdArgs a) {
+  if (block_rejects_cu_seqlens(a.seqs, a.status)) return;
+  const int d0 = (blockIdx.x * blockDim.x + threadIdx.x) * V;
+  const int64_t seg = int64_t(blockIdx.y) * blockDim.y + threadIdx.y;
+  const bool active = d0 < a.D && seg < a.n_seg;
+  float aw[V][kWidth], ab[V];
+#pragma unroll
+  for (int c = 0; c < V; ++c) {
+    ab[c] = 0.0f;
+#pragma unroll
+    for (int k = 0; k < kWidth; ++k) aw[c][k] = 0.0f;
+  }
+  if (active) {
+    float w[V][kWidth], b[V];
+    load_weights<V>(a.wr, d0, w, b);
+    const int64_t q0 = seg * a.seg_len;
+    const int64_t q1 = q0 + a.seg_len < a.seqs.Q ? q0 + a.seg_len : a.seqs.Q;
+    const bool dense = a.seqs.cu == nullptr;
+    const Stream xs{d0, dense ? a.x_sb - a.seqs.T * a.x_st : 0, a.x_st};
+    const Stream gs{d0, dense ? a.g_sb - a.seqs.T * a.g_st : 0, a.g_st};
+    const Stream ds{d0, dense ? a.dx_sb - a.seqs.T * a.dx_st : 0, a.dx_st};
+    bwd_walk<V, ACT, 4>(a, a.seqs, xs, gs, ds, 0, d0, w, b, q0, q1, aw, ab);
+  }
+  block_wgrad_out<V>(a, d0, active, aw, ab);
+}
+
+// Time-contiguous layout: one warp per (batch, channel) row, lane l walks
+// tokens [8l + 256i, 8l + 256i + 8).  The row's sums are reduced across the
+// warp in a fixed butterfly order; partial row = batch index.
+template <int ACT>
+__global__ void __launch_bounds__(256) bwd_bdt_kernel(BwdArgs a) {
+  if (block_rejects_cu_seqlens(a.seqs, a.status)) return;
+  const int lane = threadIdx.x & 31;
+  const int64_t row = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const bool dense = a.seqs.cu == nullptr;
+  const int64_t rows = dense ? int64_t(a.B) * a.D : a.D;
+  if (row >= rows) return;
+  const int bb = int(row / a.D);
+  const int d = int(row % a.D);
+  float w[1][kWidth], b[1];
+  load_weights<1>(a.wr, d, w, b);
+  Seqs rs = a.seqs;
+  if (dense) { rs.Q = a.seqs.T; rs.n_seq = 1; }
+  const Stream xs{bb * a.x_sb + d * a.x_sd, 0, 1};
+  const Stream gs{bb * a.g_sb + d * a.g_sd, 0, 1};
+  const Stream ds{bb * a.dx_sb + d * a.dx_sd, 0, 1};
+  float aw[1][kWidth] = {{0.0f, 0.0f, 0.0f, 0.0f}}, ab[1] = {0.0f};
+  for (int64_t q0 = int64_t(lane) * 8; q0 < rs.Q; q0 += 256) {
+    const int64_t q1 = q0 + 8 < rs.Q ? q0 + 8 : rs.Q;
+    bwd_walk<1, ACT, 4>(a, rs, xs, gs, ds, dense ? bb : 0, d, w, b, q0, q1, aw, ab);
+  }
+  float v[kWidth + 1] = {aw[0][0], aw[0][1], aw[0][2], aw[0][3], ab[0]};
+#pragma unroll
+  for (int k = 0; k < kWidth + 1; ++k)
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v[k] += __shfl_xor_sync(0xffffffffu, v[k], off);
+  if (lane == 0) {
+    for (int k = 0; k < kWidth + 1; ++k) {
+      if (a.deterministic)
+        a.ws[(int64_t(dense ? bb : 0) * a.D + d) * (kWidth + 1) + k] = v[k];
+      else
+        atomicAdd(a.ws + int64_t(d) * (kWidth + 1) + k, v[k]);
+    }
+  }
+}
+
+// dweight/dbias from the FP32 sums: rows r = 0 .. R-1 added in that order.
+__global__ void wgrad_finalize_kernel(const float* ws, int64_t R, int D, WgradOut o) {
+  const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= int64_t(D) * (kWidth + 1)) return;
+  const int d = int(i / (kWidth + 1)), k = int(i % (kWidth + 1));
+  float s = 0.0f;
+  for (int64_t r = 0; r < R; ++r) s += ws[r * D * (kWidth + 1) + i];
+  if (k < kWidth) {
+    const int64_t off = d * o.dw_sd + k * o.dw_sk;
+    if (o.dw_f32) static_cast<float*>(o.dw)[off] = s;
+    else static_cast<uint16_t*>(o.dw)[off] = f32_to_bf16(s);
+  } else if (o.db) {
+    o.db[d * o.db_sd] = f32_to_bf16(s);
+  }
+}
+
+// T == 0: dinit = dfinal (the final state is the initial state), or zero.
+__global__ void bwd_empty_kernel(const uint16_t* dfin, uint16_t* dinit, int64_t n) {
+  const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i < n) dinit[i] = dfin ? dfin[i] : uint16_t(0);
+}
+
+// ---- host launchers ------------------------------------------------------------
+
+int bwd_blocks_per_sm(int vec) {
+  static std::atomic<int> cache[2];
+  const int i = vec == 8 ? 0 : 1;
+  int v = cache[i].load(std::memory_order_relaxed);
+  if (v == 0) {
+    int n = 0;
+    const size_t smem = size_t(256) * vec * (kWidth + 1) * sizeof(float);
+    const cudaError_t err =
+        vec == 8 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, bwd_cl_kernel<8, kActSilu>, 256, smem)
+                 : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, bwd_cl_kernel<1, kActSilu>, 256, smem);
+    v = (err == cudaSuccess && n > 0) ? n : 1;
+    cache[i].store(v, std::memory_order_relaxed);
+  }
+  return v;
+}
+
+template <int ACT>
+static void launch_bwd_act(const BwdArgs& a, const BwdPlan& p, cudaStream_t stream) {
+  if (p.kind == kLayoutChannelLast) {
+    dim3 block(p.tx, p.ty), grid(p.gx, p.gy);
+    const size_t smem = size_t(p.tx) * p.ty * p.vec * (kWidth + 1) * sizeof(float);
+    if (p.vec == 8) bwd_cl_kernel<8, ACT><<<grid, block, smem, stream>>>(a);
+    else bwd_cl_kernel<1, ACT><<<grid, block, smem, stream>>>(a);
+  } else {
+    bwd_bdt_kernel<ACT><<<p.gx, 256, 0, stream>>>(a);
+  }
+}
+
+cudaError_t launch_bwd(const BwdArgs& a, const BwdPlan& p, int act, const WgradOut& o,
+                       int64_t partial_rows, cudaStream_t stream) {
+  const size_t acc_bytes = size_t(a.D) * (kWidth + 1) * sizeof(float);
+  const bool empty = a.seqs.Q == 0;
+  if (!a.deterministic || empty) {
+    cudaError_t err = cudaMemsetAsync(a.ws, 0, acc_bytes, stream);
+    if (err != cudaSuccess) return err;
+  }
+  if (empty) {
+    const int64_t n = int64_t(a.seqs.n_seq) * a.D * kState;
+    if (a.dinit && n > 0)
+      bwd_empty_kernel<<<unsigned((n + 255) / 256), 256, 0, stream>>>(a.dfin, a.dinit, n);
+  } else if (act == kActSilu) {
+    launch_bwd_act<kActSilu>(a, p, stream);
+  } else {
+    launch_bwd_act<kActNone>(a, p, stream);
+  }
+  const int64_t R = (a.deterministic && !empty) ? partial_rows : 1;
+  const int64_t n_out = int64_t(a.D) * (kWidth + 1);
+  wgrad_finalize_kernel<<<unsigned((n_out + 255) / 256), 256, 0, stream>>>(a.ws, R, a.D, o);
+  return cudaGetLastError();
+}
+
+}  // namespace ccc

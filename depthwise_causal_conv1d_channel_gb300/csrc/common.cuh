@@ -1,0 +1,224 @@
+// Shared device helpers for the depthwise causal conv1d kernels (sm_103a).
+//
+// The operation (cuDNN frontend docs, "Causal Conv1d" page): per channel d,
+//   out[t] = act(bias[d] + sum_{k<4} w[d,k] * xe[t-3+k])
+// on the extended sequence xe (three initial-state entries, then x).  Tap 3
+// multiplies the current token (POPCORNBENCH conv1d page, causal-padding
+// derivation).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace ccc {
+
+constexpr int kWidth = 4;
+constexpr int kState = 3;  // W - 1
+
+constexpr int kStatusBadCuSeqlens = 7;  // == CCC_ERR_BAD_CU_SEQLENS
+
+// ---- BF16 <-> FP32 ---------------------------------------------------------
+
+__device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
+__device__ __forceinline__ float bf16_to_f32(uint16_t h) { return __uint_as_float(uint32_t(h) << 16); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);  // .x (low half) = lo
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint16_t f32_to_bf16(float f) {
+  __nv_bfloat16 b = __float2bfloat16_rn(f);
+  return *reinterpret_cast<uint16_t*>(&b);
+}
+
+// ---- activation ------------------------------------------------------------
+
+enum Act { kActNone = 0, kActSilu = 1 };
+
+// silu(p) = p * sigmoid(p) = p / (1 + e^-p).  For p below about -87 the
+// denominator overflows and the quotient is 0, the correct limit.
+template <int ACT>
+__device__ __forceinline__ float act_fwd(float p) {
+  if constexpr (ACT == kActSilu) {
+    return __fdividef(p, 1.0f + __expf(-p));
+  } else {
+    return p;
+  }
+}
+
+// d act / d p:  silu'(p) = s * (1 + p * (1 - s)),  s = sigmoid(p).
+template <int ACT>
+__device__ __forceinline__ float act_grad(float p) {
+  if constexpr (ACT == kActSilu) {
+    const float s = __fdividef(1.0f, 1.0f + __expf(-p));
+    return s * fmaf(p, 1.0f - s, 1.0f);
+  } else {
+    return 1.0f;
+  }
+}
+
+// ---- vectors of V consecutive channels ---------------------------------------
+
+template <int V>
+struct Vec;
+
+template <>
+struct Vec<8> {
+  using Raw = uint4;  // 8 x BF16 = 16 bytes
+  __device__ __forceinline__ static Raw ld(const uint16_t* p) {
+    return __ldg(reinterpret_cast<const uint4*>(p));
+  }
+  __device__ __forceinline__ static void st(uint16_t* p, Raw r) {
+    __stcs(reinterpret_cast<uint4*>(p), r);
+  }
+  __device__ __forceinline__ static void unpack(Raw r, float (&f)[8]) {
+    f[0] = bf16_lo(r.x); f[1] = bf16_hi(r.x);
+    f[2] = bf16_lo(r.y); f[3] = bf16_hi(r.y);
+    f[4] = bf16_lo(r.z); f[5] = bf16_hi(r.z);
+    f[6] = bf16_lo(r.w); f[7] = bf16_hi(r.w);
+  }
+  __device__ __forceinline__ static Raw pack(const float (&f)[8]) {
+    return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
+                      pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+  }
+};
+
+template <>
+struct Vec<1> {
+  using Raw = uint16_t;
+  __device__ __forceinline__ static Raw ld(const uint16_t* p) { return __ldg(p); }
+  __device__ __forceinline__ static void st(uint16_t* p, Raw r) { __stcs(p, r); }
+  __device__ __forceinline__ static void unpack(Raw r, float (&f)[1]) { f[0] = bf16_to_f32(r); }
+  __device__ __forceinline__ static Raw pack(const float (&f)[1]) { return f32_to_bf16(f[0]); }
+};
+
+// State rows: V consecutive channels of one sequence's [D][3] block, 3*V
+// contiguous BF16 values, entry (c, i) at c*3 + i.  win[i][c] = state(c, i).
+template <int V>
+__device__ __forceinline__ void load_state(const uint16_t* s, float (&win)[kState][V]) {
+  if constexpr (V == 8) {
+    union { uint4 q[3]; uint16_t h[24]; } u;
+    const uint4* p = reinterpret_cast<const uint4*>(s);
+    u.q[0] = __ldg(p); u.q[1] = __ldg(p + 1); u.q[2] = __ldg(p + 2);
+#pragma unroll
+    for (int c = 0; c < V; ++c)
+#pragma unroll
+      for (int i = 0; i < kState; ++i) win[i][c] = bf16_to_f32(u.h[c * 3 + i]);
+  } else {
+#pragma unroll
+    for (int c = 0; c < V; ++c)
+#pragma unroll
+      for (int i = 0; i < kState; ++i) win[i][c] = bf16_to_f32(__ldg(s + c * 3 + i));
+  }
+}
+
+template <int V>
+__device__ __forceinline__ void store_state(uint16_t* s, const float (&win)[kState][V]) {
+  if constexpr (V == 8) {
+    union { uint4 q[3]; uint16_t h[24]; } u;
+#pragma unroll
+    for (int c = 0; c < V; ++c)
+#pragma unroll
+      for (int i = 0; i < kState; ++i) u.h[c * 3 + i] = f32_to_bf16(win[i][c]);
+    uint4* p = reinterpret_cast<uint4*>(s);
+    p[0] = u.q[0]; p[1] = u.q[1]; p[2] = u.q[2];
+  } else {
+#pragma unroll
+    for (int c = 0; c < V; ++c)
+#pragma unroll
+      for (int i = 0; i < kState; ++i) s[c * 3 + i] = f32_to_bf16(win[i][c]);
+  }
+}
+
+// ---- weights -----------------------------------------------------------------
+
+struct WeightRef {
+  const void* w;    // [D, 4] BF16 or FP32
+  int w_f32;
+  int64_t w_sd, w_sk;
+  const uint16_t* bias;  // [D] BF16 or nullptr
+  int64_t b_sd;
+};
+
+template <int V>
+__device__ __forceinline__ void load_weights(const WeightRef& r, int d0, float (&w)[V][kWidth],
+                                             float (&b)[V]) {
+#pragma unroll
+  for (int c = 0; c < V; ++c) {
+    const int64_t d = d0 + c;
+#pragma unroll
+    for (int k = 0; k < kWidth; ++k) {
+      const int64_t o = d * r.w_sd + k * r.w_sk;
+      w[c][k] = r.w_f32 ? __ldg(static_cast<const float*>(r.w) + o)
+                        : bf16_to_f32(__ldg(static_cast<const uint16_t*>(r.w) + o));
+    }
+    b[c] = r.bias ? bf16_to_f32(__ldg(r.bias + d * r.b_sd)) : 0.0f;
+  }
+}
+
+// ---- sequences -----------------------------------------------------------------
+//
+// A call's tokens form one index space q in [0, Q).  Dense calls: sequence n is
+// [n*T, (n+1)*T).  Packed calls: sequence n is [cu[n], cu[n+1]) (cuDNN page:
+// packed cu_seqlens, per-sequence state, no mixing across boundaries).
+
+struct Seqs {
+  const int* cu;  // packed offsets (device), nullptr when dense
+  int n_seq;
+  int64_t T;      // dense: tokens per sequence
+  int64_t Q;      // total tokens
+};
+
+__device__ __forceinline__ int find_seq(const Seqs& s, int64_t q) {
+  if (!s.cu) return static_cast<int>(q / s.T);
+  int lo = 0, hi = s.n_seq;  // invariant: cu[lo] <= q < cu[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(s.cu + mid) <= q) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ void seq_bounds(const Seqs& s, int n, int64_t& lo, int64_t& hi) {
+  if (!s.cu) {
+    lo = int64_t(n) * s.T;
+    hi = lo + s.T;
+  } else {
+    lo = __ldg(s.cu + n);
+    hi = __ldg(s.cu + n + 1);
+  }
+}
+
+// Every block checks the whole offsets array before touching memory (cuDNN page:
+// first offset 0, last offset equal to the token total, strictly increasing).
+// Must be reached by every thread of the block.  Returns true when malformed;
+// the first thread then records the error.
+__device__ __forceinline__ bool block_rejects_cu_seqlens(const Seqs& s, int* status) {
+  if (!s.cu) return false;
+  const int tid = threadIdx.x + blockDim.x * (threadIdx.y + blockDim.y * threadIdx.z);
+  const int nthr = blockDim.x * blockDim.y * blockDim.z;
+  int bad = 0;
+  for (int i = tid; i < s.n_seq; i += nthr) {
+    if (__ldg(s.cu + i + 1) <= __ldg(s.cu + i)) bad = 1;
+  }
+  if (tid == 0 && (__ldg(s.cu) != 0 || int64_t(__ldg(s.cu + s.n_seq)) != s.Q)) bad = 1;
+  bad = __syncthreads_or(bad);
+  if (bad && tid == 0 && status) atomicCAS(status, 0, kStatusBadCuSeqlens);
+  return bad != 0;
+}
+
+// Element offsets of token q of sequence n in an activation tensor, for the
+// V channels starting at the thread's channel:  off + n * seq_step + q * st.
+// Dense channel-last: seq_step = batch stride - T * token stride.  Packed, or
+// a time-contiguous row handled as its own stream: seq_step = 0.
+struct Stream {
+  int64_t off;
+  int64_t seq_step;
+  int64_t st;
+  __device__ __forceinline__ int64_t at(int n, int64_t q) const { return off + n * seq_step + q * st; }
+};
+
+}  // namespace ccc

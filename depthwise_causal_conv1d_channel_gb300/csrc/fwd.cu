@@ -1,0 +1,184 @@
+// Forward kernels of the depthwise causal conv1d (cuDNN frontend docs, "Causal
+// Conv1d" page: BF16 activations, width four, SiLU, W-1 initial and final
+// state, dense or cu_seqlens-packed).
+//
+// Each thread owns V consecutive channels and walks a contiguous range of
+// tokens, keeping the last three inputs of every channel in registers, so each
+// input is read from HBM once (plus a three-token halo per range) and each
+// output written once.  Nothing is staged: the op is a streaming stencil with
+// about one FLOP per byte, bound by HBM bandwidth, not a contraction.
+#include <atomic>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace ccc {
+
+// One thread: channels [d0, d0 + V), tokens [q, q_end) of one token stream.
+// `n_base` is the state index of the stream's sequence 0.
+template <int V, int ACT, int U>
+__device__ __forceinline__ void fwd_walk(const FwdArgs& a, const Seqs& seqs, const Stream& xs,
+                                         const Stream& os, int n_base, int d0,
+                                         const float (&w)[V][kWidth], const float (&b)[V],
+                                         int64_t q, int64_t q_end) {
+  using VT = Vec<V>;
+  int n = find_seq(seqs, q);
+  while (q < q_end) {
+    int64_t lo, hi;
+    seq_bounds(seqs, n, lo, hi);
+    const int64_t e = q_end < hi ? q_end : hi;
+    const int64_t state_row = (int64_t(n_base) + n) * a.D + d0;
+
+    // win[j] = xe[q - 3 + j]: from x, or from the initial state before the
+    // sequence start, or zero.
+    float win[kState][V];
+    {
+      float init[kState][V];
+      if (q - kState < lo && a.init) {
+        load_state<V>(a.init + state_row * kState, init);
+      } else {
+#pragma unroll
+        for (int i = 0; i < kState; ++i)
+#pragma unroll
+          for (int c = 0; c < V; ++c) init[i][c] = 0.0f;
+      }
+#pragma unroll
+      for (int j = 0; j < kState; ++j) {
+        const int64_t tok = q - kState + j;
+        if (tok >= lo) {
+          VT::unpack(VT::ld(a.x + xs.at(n, tok)), win[j]);
+        } else {
+          const int64_t i = tok - lo + kState;  // 0..2
+#pragma unroll
+          for (int c = 0; c < V; ++c)
+            win[j][c] = i == 0 ? init[0][c] : (i == 1 ? init[1][c] : init[2][c]);
+        }
+      }
+    }
+
+    auto step = [&](typename VT::Raw raw, int64_t t) {
+      float cur[V], y[V];
+      VT::unpack(raw, cur);
+#pragma unroll
+      for (int c = 0; c < V; ++c) {
+        float p = b[c];
+        p = fmaf(w[c][0], win[0][c], p);
+        p = fmaf(w[c][1], win[1][c], p);
+        p = fmaf(w[c][2], win[2][c], p);
+        p = fmaf(w[c][3], cur[c], p);
+        y[c] = act_fwd<ACT>(p);
+        win[0][c] = win[1][c];
+        win[1][c] = win[2][c];
+        win[2][c] = cur[c];
+      }
+      VT::st(a.out + os.at(n, t), VT::pack(y));
+    };
+
+    // steady state: U loads in flight, then U outputs
+    for (; q + U <= e; q += U) {
+      typename VT::Raw raw[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) raw[u] = VT::ld(a.x + xs.at(n, q + u));
+#pragma unroll
+      for (int u = 0; u < U; ++u) step(raw[u], q + u);
+    }
+    for (; q < e; ++q) step(VT::ld(a.x + xs.at(n, q)), q);
+
+    // the thread that finishes a sequence writes its final state: xe[len-3 .. len-1]
+    if (e == hi && a.fin) store_state<V>(a.fin + state_row * kState, win);
+    ++n;
+  }
+}
+
+// Channel-last x ([B, T, D] storage seen as [B, D, T]; stride of D is 1).
+// Block (TX, TY): threadIdx.x runs over groups of V channels, threadIdx.y over
+// token ranges of seg_len tokens.  A warp reads 32 * V * 2 contiguous bytes
+// per token.
+template <int V, int ACT>
+__global__ void __launch_bounds__(256) fwd_cl_kernel(FwdArgs a) {
+  if (block_rejects_cu_seqlens(a.seqs, a.status)) return;
+  const int d0 = (blockIdx.x * blockDim.x + threadIdx.x) * V;
+  const int64_t seg = int64_t(blockIdx.y) * blockDim.y + threadIdx.y;
+  if (d0 >= a.D || seg >= a.n_seg) return;
+  float w[V][kWidth], b[V];
+  load_weights<V>(a.wr, d0, w, b);
+  const int64_t q0 = seg * a.seg_len;
+  const int64_t q1 = q0 + a.seg_len < a.seqs.Q ? q0 + a.seg_len : a.seqs.Q;
+  const bool dense = a.seqs.cu == nullptr;
+  const Stream xs{d0, dense ? a.x_sb - a.seqs.T * a.x_st : 0, a.x_st};
+  const Stream os{d0, dense ? a.o_sb - a.seqs.T * a.o_st : 0, a.o_st};
+  fwd_walk<V, ACT, 4>(a, a.seqs, xs, os, 0, d0, w, b, q0, q1);
+}
+
+// Time-contiguous x (stride of T is 1).  One warp per (batch, channel) row;
+// lane l walks tokens [8l + 256i, 8l + 256i + 8).
+template <int ACT>
+__global__ void __launch_bounds__(256) fwd_bdt_kernel(FwdArgs a) {
+  if (block_rejects_cu_seqlens(a.seqs, a.status)) return;
+  const int lane = threadIdx.x & 31;
+  const int64_t row = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const bool dense = a.seqs.cu == nullptr;
+  const int64_t rows = dense ? int64_t(a.B) * a.D : a.D;
+  if (row >= rows) return;
+  const int bb = int(row / a.D);
+  const int d = int(row % a.D);
+  float w[1][kWidth], b[1];
+  load_weights<1>(a.wr, d, w, b);
+  // Within a row, a dense call is one sequence of T tokens (state index bb).
+  Seqs rs = a.seqs;
+  if (dense) { rs.Q = a.seqs.T; rs.n_seq = 1; }
+  const Stream xs{bb * a.x_sb + d * a.x_sd, 0, 1};
+  const Stream os{bb * a.o_sb + d * a.o_sd, 0, 1};
+  for (int64_t q0 = int64_t(lane) * 8; q0 < rs.Q; q0 += 256) {
+    const int64_t q1 = q0 + 8 < rs.Q ? q0 + 8 : rs.Q;
+    fwd_walk<1, ACT, 4>(a, rs, xs, os, dense ? bb : 0, d, w, b, q0, q1);
+  }
+}
+
+// T == 0: every sequence's final state is its initial state (or zeros).
+__global__ void fwd_empty_kernel(const uint16_t* init, uint16_t* fin, int64_t n) {
+  const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i < n) fin[i] = init ? init[i] : uint16_t(0);
+}
+
+// ---- host launchers ------------------------------------------------------------
+
+int fwd_blocks_per_sm(int vec) {
+  static std::atomic<int> cache[2];
+  const int i = vec == 8 ? 0 : 1;
+  int v = cache[i].load(std::memory_order_relaxed);
+  if (v == 0) {
+    int n = 0;
+    const cudaError_t err =
+        vec == 8 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fwd_cl_kernel<8, kActSilu>, 256, 0)
+                 : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fwd_cl_kernel<1, kActSilu>, 256, 0);
+    v = (err == cudaSuccess && n > 0) ? n : 1;
+    cache[i].store(v, std::memory_order_relaxed);
+  }
+  return v;
+}
+
+template <int ACT>
+static cudaError_t launch_fwd_act(const FwdArgs& a, const FwdPlan& p, cudaStream_t stream) {
+  if (p.kind == kLayoutChannelLast) {
+    dim3 block(p.tx, p.ty), grid(p.gx, p.gy);
+    if (p.vec == 8) fwd_cl_kernel<8, ACT><<<grid, block, 0, stream>>>(a);
+    else fwd_cl_kernel<1, ACT><<<grid, block, 0, stream>>>(a);
+  } else {
+    fwd_bdt_kernel<ACT><<<p.gx, 256, 0, stream>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fwd(const FwdArgs& a, const FwdPlan& p, int act, cudaStream_t stream) {
+  if (a.seqs.Q == 0) {
+    const int64_t n = int64_t(a.seqs.n_seq) * a.D * kState;
+    if (a.fin && n > 0)
+      fwd_empty_kernel<<<unsigned((n + 255) / 256), 256, 0, stream>>>(a.init, a.fin, n);
+    return cudaGetLastError();
+  }
+  return act == kActSilu ? launch_fwd_act<kActSilu>(a, p, stream)
+                         : launch_fwd_act<kActNone>(a, p, stream);
+}
+
+}  // namespace ccc

@@ -1,0 +1,89 @@
+// Internal interface between the C-ABI layer (abi.cu) and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace ccc {
+
+enum Layout { kLayoutChannelLast = 0, kLayoutTimeContiguous = 1 };
+
+struct FwdArgs {
+  const uint16_t* x;
+  uint16_t* out;
+  int64_t x_sb, x_sd, x_st;  // element strides of x ([B, D, T] view)
+  int64_t o_sb, o_sd, o_st;
+  WeightRef wr;
+  const uint16_t* init;  // [S, D, 3] contiguous or nullptr
+  uint16_t* fin;         // [S, D, 3] contiguous or nullptr
+  Seqs seqs;
+  int B, D;
+  int64_t seg_len, n_seg;  // channel-last: tokens per thread range, number of ranges
+  int* status;
+};
+
+struct BwdArgs {
+  const uint16_t* x;
+  const uint16_t* g;   // dL/dout
+  uint16_t* dx;
+  int64_t x_sb, x_sd, x_st;
+  int64_t g_sb, g_sd, g_st;
+  int64_t dx_sb, dx_sd, dx_st;
+  WeightRef wr;
+  const uint16_t* init;   // [S, D, 3] or nullptr
+  const uint16_t* dfin;   // [S, D, 3] or nullptr (zero gradient)
+  uint16_t* dinit;        // [S, D, 3] or nullptr
+  Seqs seqs;
+  int B, D;
+  int64_t seg_len, n_seg;
+  float* ws;              // FP32 weight/bias-gradient sums, [R, D, 5]
+  int deterministic;      // 1: block row r writes ws[r]; 0: atomics into ws[0]
+  int* status;
+};
+
+// Launch shape of one call, chosen on the host from the sizes and the SM count.
+struct FwdPlan {
+  int kind;      // Layout
+  int vec;       // channels per thread (channel-last): 8 or 1
+  int tx, ty;    // block shape (channel-last)
+  unsigned gx, gy;
+  int64_t seg_len, n_seg;
+};
+
+using BwdPlan = FwdPlan;
+
+struct UpdArgs {
+  const uint16_t* x;  // [B, D], channel stride 1
+  int64_t x_sb;
+  uint16_t* state;    // [B, D, 3] contiguous
+  uint16_t* out;      // [B, D], channel stride 1
+  int64_t o_sb;
+  WeightRef wr;
+  int B, D;
+};
+
+struct WgradOut {
+  void* dw;          // [D, 4] BF16 or FP32
+  int dw_f32;
+  int64_t dw_sd, dw_sk;
+  uint16_t* db;      // [D] BF16 or nullptr
+  int64_t db_sd;
+};
+
+FwdPlan plan_fwd(int kind, int vec_ok, int64_t Q, int D, int64_t rows, int sm_count);
+BwdPlan plan_bwd(int kind, int vec_ok, int64_t Q, int D, int64_t rows, int sm_count);
+// Rows of FP32 partial sums the backward writes in deterministic mode.
+int64_t bwd_partial_rows(const BwdPlan& p, int B, bool packed);
+
+// Resident blocks per SM of the channel-last kernels (SiLU instance), cached.
+int fwd_blocks_per_sm(int vec);
+int bwd_blocks_per_sm(int vec);
+
+cudaError_t launch_fwd(const FwdArgs& a, const FwdPlan& p, int act, cudaStream_t stream);
+cudaError_t launch_bwd(const BwdArgs& a, const BwdPlan& p, int act, const WgradOut& o,
+                       int64_t partial_rows, cudaStream_t stream);
+cudaError_t launch_update(const UpdArgs& a, int vec, int act, cudaStream_t stream);
+
+}  // namespace ccc

@@ -1,0 +1,185 @@
+"""Model-facing operations: causal_conv1d (with autograd) and causal_conv1d_update.
+
+The argument lists follow the cuDNN frontend "Causal Conv1d" page (the
+commonly consumed causal-conv1d interface): x [B, D, T] -- or the
+transpose(1, 2) view of [B, T, D] storage, read in place --, weight [D, 4],
+optional bias [D], the reserved seq_idx keyword (only None), optional packed
+cu_seqlens [N + 1], optional initial_states and returned final_states of width
+W - 1 = 3, and a SiLU activation.  Every step runs in the CUDA library through
+the C ABI; this module allocates outputs, picks the determinism mode and maps
+status codes to Python exceptions.
+"""
+
+from __future__ import annotations
+
+import os
+import warnings
+from typing import Optional
+
+import torch
+
+from . import _abi
+
+_ACTIVATIONS = {"silu": _abi.CCC_ACT_SILU, "swish": _abi.CCC_ACT_SILU, None: _abi.CCC_ACT_NONE,
+                "identity": _abi.CCC_ACT_NONE, "none": _abi.CCC_ACT_NONE}
+
+_status_words = {}
+
+
+def _activation_code(activation) -> int:
+    if activation not in _ACTIVATIONS:
+        raise ValueError(f"activation must be 'silu' or None, got {activation!r}")
+    return _ACTIVATIONS[activation]
+
+
+def status_word(device: torch.device) -> torch.Tensor:
+    """The per-device int32 status word every call of this module passes to the
+    kernels (malformed cu_seqlens are reported there instead of a device trap)."""
+    idx = torch.device(device).index
+    if idx is None:
+        idx = torch.cuda.current_device()
+    w = _status_words.get(idx)
+    if w is None:
+        w = torch.zeros(1, dtype=torch.int32, device=torch.device("cuda", idx))
+        _status_words[idx] = w
+    return w
+
+
+def check_status(device=None, stream=None) -> None:
+    """Synchronise and raise if a kernel recorded a device-side error since the
+    last check (for example malformed cu_seqlens); clears the word."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    st = _abi.ccc_read_status(status_word(dev), stream or torch.cuda.current_stream(dev))
+    if st != _abi.CCC_OK:
+        raise _abi.Conv1dError(st, "device status")
+
+
+def _raise(st: int, where: str):
+    if st == _abi.CCC_OK:
+        return
+    if st == _abi.CCC_ERR_ALIAS:
+        raise ValueError(f"{where}: {_abi.status_string(st)}")
+    if st == _abi.CCC_ERR_INVALID_ARG:
+        raise ValueError(f"{where}: {_abi.status_string(st)}")
+    if st == _abi.CCC_ERR_UNSUPPORTED:
+        raise NotImplementedError(f"{where}: {_abi.status_string(st)}")
+    raise _abi.Conv1dError(st, where)
+
+
+def _debug_check(device):
+    if os.environ.get("CCC_CONV1D_CHECK_STATUS", "0") not in ("", "0"):
+        check_status(device)
+
+
+def _like_x(t: torch.Tensor, x: torch.Tensor) -> torch.Tensor:
+    """t laid out like x (same strides), copying only when the layouts differ."""
+    if t.stride() == x.stride():
+        return t
+    out = torch.empty_strided(x.shape, x.stride(), dtype=t.dtype, device=t.device)
+    out.copy_(t)
+    return out
+
+
+def _deterministic_mode(has_bias: bool, deterministic: Optional[bool]) -> bool:
+    """The cuDNN page's rule: torch.use_deterministic_algorithms selects the
+    deterministic dweight route for bias-free calls; with a bias there is none,
+    so raise RuntimeError, or warn and use atomics under warn_only=True.  A
+    per-call deterministic=True/False overrides the global setting."""
+    want = torch.are_deterministic_algorithms_enabled() if deterministic is None else deterministic
+    if not want:
+        return False
+    if not has_bias:
+        return True
+    msg = ("causal_conv1d backward with bias has no deterministic dbias route "
+           "(dweight/dbias accumulate with FP32 atomics)")
+    if deterministic is None and torch.is_deterministic_algorithms_warn_only_enabled():
+        warnings.warn(msg)
+        return False
+    raise RuntimeError(msg)
+
+
+class _CausalConv1dFn(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, x, weight, bias, cu_seqlens, initial_states, final_states_out, want_final,
+                act, deterministic):
+        out = torch.empty_like(x)  # same strides as x: channel-last in, channel-last out
+        S = x.shape[0] if cu_seqlens is None else cu_seqlens.numel() - 1
+        final = None
+        if want_final:
+            final = final_states_out if final_states_out is not None else torch.empty(
+                (S, x.shape[1], 3), dtype=x.dtype, device=x.device)
+        st = _abi.ccc_conv1d_fwd(x, weight, bias, cu_seqlens, initial_states, out, final, act,
+                                 status_word(x.device), torch.cuda.current_stream(x.device))
+        _raise(st, "causal_conv1d")
+        _debug_check(x.device)
+        ctx.save_for_backward(x, weight, bias, cu_seqlens, initial_states)
+        ctx.act = act
+        ctx.deterministic = deterministic
+        if final_states_out is not None:
+            ctx.mark_dirty(final_states_out)
+        return out, final
+
+    @staticmethod
+    def backward(ctx, dout, dfinal):
+        x, weight, bias, cu_seqlens, initial_states = ctx.saved_tensors
+        det = _deterministic_mode(bias is not None, ctx.deterministic)
+        if dout is None:
+            dout = torch.zeros_like(x)
+        dout = _like_x(dout, x)
+        if dfinal is not None:
+            dfinal = dfinal.contiguous()
+        dx = torch.empty_like(x)
+        dweight = torch.empty_like(weight, memory_format=torch.contiguous_format)
+        dbias = torch.empty_like(bias) if bias is not None else None
+        dinit = None
+        if initial_states is not None and ctx.needs_input_grad[4]:
+            dinit = torch.empty_like(initial_states)
+        ws = torch.empty(_abi.ccc_conv1d_bwd_workspace_size(x, det), dtype=torch.uint8,
+                         device=x.device)
+        st = _abi.ccc_conv1d_bwd(x, weight, bias, cu_seqlens, initial_states, dout, dfinal, dx,
+                                 dweight, dbias, dinit, ctx.act, det, ws, status_word(x.device),
+                                 torch.cuda.current_stream(x.device))
+        _raise(st, "causal_conv1d backward")
+        _debug_check(x.device)
+        return dx, dweight, dbias, None, dinit, None, None, None, None
+
+
+def causal_conv1d(x: torch.Tensor, weight: torch.Tensor, bias: Optional[torch.Tensor] = None,
+                  seq_idx: Optional[torch.Tensor] = None, cu_seqlens: Optional[torch.Tensor] = None,
+                  initial_states: Optional[torch.Tensor] = None, return_final_states: bool = False,
+                  final_states_out: Optional[torch.Tensor] = None, activation: Optional[str] = "silu",
+                  deterministic: Optional[bool] = None):
+    """Depthwise causal conv1d, width 4, BF16 activations.
+
+    out[b, d, t] = act(bias[d] + sum_k weight[d, k] * xe[b, d, t - 3 + k]) where xe
+    is x preceded by the three initial-state entries (zeros when none).
+
+    Returns ``out`` (same shape and strides as x) or ``(out, final_states)`` when
+    ``return_final_states`` is set or ``final_states_out`` is given.  Differentiable
+    in x, weight, bias and initial_states.  ``deterministic`` (default: follow
+    ``torch.use_deterministic_algorithms``) selects the reproducible dweight route.
+    """
+    if seq_idx is not None:
+        raise NotImplementedError("seq_idx is reserved; only None is accepted")
+    if cu_seqlens is not None and cu_seqlens.dtype != torch.int32:
+        raise ValueError("cu_seqlens must be int32")
+    act = _activation_code(activation)
+    want_final = bool(return_final_states) or final_states_out is not None
+    out, final = _CausalConv1dFn.apply(x, weight, bias, cu_seqlens, initial_states,
+                                       final_states_out, want_final, act, deterministic)
+    return (out, final) if want_final else out
+
+
+def causal_conv1d_update(x: torch.Tensor, conv_state: torch.Tensor, weight: torch.Tensor,
+                         bias: Optional[torch.Tensor] = None, activation: Optional[str] = "silu",
+                         out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """One decode step: x [B, D] is the new token; conv_state [B, D, 3] (the
+    layout final_states uses) is read and mutated in place to [s1, s2, x].
+    Returns out [B, D]."""
+    act = _activation_code(activation)
+    if out is None:
+        out = torch.empty_like(x, memory_format=torch.contiguous_format)
+    st = _abi.ccc_conv1d_update(x, conv_state, weight, bias, out, act,
+                                torch.cuda.current_stream(x.device))
+    _raise(st, "causal_conv1d_update")
+    return out

@@ -1,0 +1,181 @@
+/*
+ * ccc_conv1d -- depthwise causal conv1d on BF16 activations, width four.
+ *
+ * C ABI of the CUDA library (libccc_conv1d.so).  All tensor memory is owned by
+ * the caller; the library allocates nothing and keeps no mutable global state,
+ * so calls on different streams may run concurrently (on disjoint outputs).
+ *
+ * The operation (cuDNN frontend docs, "Causal Conv1d" page):
+ *
+ *   out[b,d,t] = act(bias[d] + sum_{k<4} weight[d,k] * xe[b,d,t-3+k])
+ *
+ * where xe is x extended on the left by the three entries of initial_states
+ * (zeros when none are given); index 0 of the state axis is the oldest entry.
+ * Tap 3 multiplies the current token (POPCORNBENCH conv1d page, the reasoning
+ * section's causal-padding derivation: tap k reads position t + k - (K-1)).
+ * act is SiLU, p * sigmoid(p), or the identity.
+ *
+ * Tensors are passed as ccc_tensor descriptors: a data pointer, a dtype, the
+ * number of dimensions, and shape/stride arrays with strides in ELEMENTS.
+ * Unless stated otherwise a data pointer is a DEVICE pointer on the current
+ * device, and every kernel runs on the given stream (NULL = legacy default
+ * stream, following the frontend overview page's stream convention).
+ *
+ * Error behaviour.  Every argument check runs on the host before any work is
+ * enqueued; on a non-CCC_OK return nothing has been written.  The only
+ * device-side error is malformed cu_seqlens.  The cuDNN page executes a device
+ * trap for it; this library instead has every thread block validate the
+ * offsets, skip all of its writes and, when d_status is not NULL, record
+ * CCC_ERR_BAD_CU_SEQLENS in *d_status (first error wins).  The CUDA context
+ * stays usable; the outputs of that call are unspecified.  Read the word with
+ * ccc_read_status.
+ */
+#ifndef CCC_CONV1D_H
+#define CCC_CONV1D_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h> /* cudaStream_t */
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define CCC_CONV1D_ABI_VERSION 1
+#define CCC_CONV1D_WIDTH 4
+
+typedef enum {
+    CCC_OK = 0,
+    CCC_ERR_INVALID_ARG = 1,      /* NULL where required, bad shape/dtype/rank, unknown enum */
+    CCC_ERR_UNSUPPORTED = 2,      /* well-formed but declined: width != 4, FP32 weight with
+                                     bias, strides this library does not read, B != 1 when packed */
+    CCC_ERR_ALIAS = 3,            /* an output overlaps an input or another output */
+    CCC_ERR_NONDETERMINISTIC = 4, /* deterministic backward requested with a bias */
+    CCC_ERR_WORKSPACE = 5,        /* workspace NULL, too small or not 16-byte aligned */
+    CCC_ERR_CUDA = 6,             /* a CUDA runtime call or launch failed */
+    CCC_ERR_BAD_CU_SEQLENS = 7    /* device-detected malformed cu_seqlens (via d_status) */
+} ccc_status;
+
+typedef enum { CCC_BF16 = 0, CCC_F32 = 1, CCC_I32 = 2 } ccc_dtype;
+
+typedef enum { CCC_ACT_NONE = 0, CCC_ACT_SILU = 1 } ccc_act;
+
+typedef struct {
+    void *data;        /* device pointer (may be NULL only when numel == 0) */
+    int32_t dtype;     /* ccc_dtype */
+    int32_t ndim;      /* 1, 2 or 3 */
+    int64_t shape[3];  /* entries past ndim are ignored */
+    int64_t stride[3]; /* in elements */
+} ccc_tensor;
+
+/*
+ * Forward (cuDNN "Causal Conv1d" page: the tensor list, the paragraph on
+ * [B, T, D] storage passed as a transpose(1, 2) view, and the paragraph on the
+ * optimized route: dense and cu_seqlens-packed, BF16 activations, width four,
+ * W-1 initial and final state).
+ *
+ *   x               [B, D, T] BF16.  Two layouts are read in place:
+ *                     channel-last: stride[1] == 1 (the transpose view of
+ *                       [B, T, D] storage; stride[2] >= D);
+ *                     time-contiguous: stride[2] == 1.
+ *                   Any other layout returns CCC_ERR_UNSUPPORTED.
+ *   weight          [D, 4] BF16, or FP32 only when bias is NULL (the page
+ *                   declines FP32 weight with bias); any strides.
+ *   bias            [D] BF16 or NULL.
+ *   cu_seqlens      [N + 1] int32 or NULL.  When given, x has B == 1 and holds
+ *                   N sequences back to back along T; no tap reads across a
+ *                   boundary.  Validated on the device (see above): offsets
+ *                   start at 0, end at T, and strictly increase.
+ *   initial_states  [S, D, 3] BF16 contiguous or NULL; S = B (dense) or N (packed).
+ *   out             [B, D, T] BF16, same layout kind as x (its own strides).
+ *   final_states    [S, D, 3] BF16 contiguous or NULL: xe[T-3 .. T-1] of each
+ *                   sequence, a bitwise copy (initial-state entries when T < 3).
+ *                   Must not overlap x, weight, bias, cu_seqlens or
+ *                   initial_states (CCC_ERR_ALIAS, the page's aliasing rule).
+ *   activation      ccc_act.
+ *   d_status        device int or NULL; see "Error behaviour".
+ *
+ * T == 0 is allowed (final_states then equals initial_states, or zeros).
+ */
+ccc_status ccc_conv1d_fwd(const ccc_tensor *x, const ccc_tensor *weight, const ccc_tensor *bias,
+                          const ccc_tensor *cu_seqlens, const ccc_tensor *initial_states,
+                          const ccc_tensor *out, const ccc_tensor *final_states, int activation,
+                          int *d_status, cudaStream_t stream);
+
+/*
+ * Workspace bytes that ccc_conv1d_bwd needs for this x (shape and layout) and
+ * mode, on the current device.  Returns 0 for an x that ccc_conv1d_bwd would
+ * reject.  The value depends on the device's SM count, so query it on the
+ * device you launch on.
+ */
+size_t ccc_conv1d_bwd_workspace_size(const ccc_tensor *x, int deterministic);
+
+/*
+ * Backward (cuDNN "Causal Conv1d" page: forward and backward on the optimized
+ * route; the paragraph on determinism).  The pre-activation is recomputed
+ * from x; nothing from the forward is needed.
+ *
+ *   x, weight, bias, cu_seqlens, initial_states   as in ccc_conv1d_fwd.
+ *   dout            [B, D, T] BF16, same layout kind as x: dL/dout.
+ *   dfinal_states   [S, D, 3] BF16 contiguous or NULL (NULL = zero gradient).
+ *   dx              [B, D, T] BF16, same layout kind as x.
+ *   dweight         [D, 4], dtype of weight, any strides.
+ *   dbias           [D] BF16; required when bias is given, else must be NULL.
+ *   dinitial_states [S, D, 3] BF16 contiguous or NULL (allowed only with
+ *                   initial_states).
+ *   deterministic   0: dweight/dbias accumulate with FP32 atomics (not bitwise
+ *                   reproducible).  1: unique FP32 per-block partials followed
+ *                   by a fixed-order reduction (bitwise reproducible); only for
+ *                   bias-free calls, else CCC_ERR_NONDETERMINISTIC.
+ *   workspace       device buffer of at least
+ *                   ccc_conv1d_bwd_workspace_size(x, deterministic) bytes,
+ *                   16-byte aligned; contents on entry are ignored.
+ *
+ * Outputs must not overlap each other or any input (CCC_ERR_ALIAS).
+ */
+ccc_status ccc_conv1d_bwd(const ccc_tensor *x, const ccc_tensor *weight, const ccc_tensor *bias,
+                          const ccc_tensor *cu_seqlens, const ccc_tensor *initial_states,
+                          const ccc_tensor *dout, const ccc_tensor *dfinal_states,
+                          const ccc_tensor *dx, const ccc_tensor *dweight, const ccc_tensor *dbias,
+                          const ccc_tensor *dinitial_states, int activation, int deterministic,
+                          void *workspace, size_t workspace_bytes, int *d_status,
+                          cudaStream_t stream);
+
+/*
+ * Single-token update (cuDNN "Causal Conv1d" page, the paragraph on passing
+ * final_states to causal_conv1d_update, which mutates that state in place).
+ *
+ *   x           [B, D] BF16, stride[1] == 1: this step's token.
+ *   conv_state  [B, D, 3] BF16 contiguous, read and overwritten in place with
+ *               [s1, s2, x] (bitwise): the layout final_states uses.
+ *   weight      [D, 4] as in ccc_conv1d_fwd;  bias [D] BF16 or NULL.
+ *   out         [B, D] BF16, stride[1] == 1:
+ *               act(bias + w0*s0 + w1*s1 + w2*s2 + w3*x).
+ *
+ * out must not overlap conv_state, weight or bias; x must not overlap
+ * conv_state (CCC_ERR_ALIAS).
+ */
+ccc_status ccc_conv1d_update(const ccc_tensor *x, const ccc_tensor *conv_state,
+                             const ccc_tensor *weight, const ccc_tensor *bias,
+                             const ccc_tensor *out, int activation, cudaStream_t stream);
+
+/*
+ * Synchronise `stream`, read the device status word written by the kernels
+ * (d_status, a device pointer), reset it to 0, and return it as a ccc_status
+ * (CCC_OK when no error was recorded).  Returns CCC_ERR_CUDA if the
+ * synchronisation or copy fails.
+ */
+ccc_status ccc_read_status(int *d_status, cudaStream_t stream);
+
+/* Static, NUL-terminated description of a status code. */
+const char *ccc_status_string(int status);
+
+/* CCC_CONV1D_ABI_VERSION of the built library. */
+int ccc_conv1d_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CCC_CONV1D_H */

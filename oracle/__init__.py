@@ -57,7 +57,9 @@ def build(force: bool = False) -> str:
 def _load():
     global _lib
     if _lib is None:
-        lib = ctypes.CDLL(build())
+        # CCC_ORACLE_LIB lets the oracle's own mutation tests load a deliberately
+        # broken copy; nothing else sets it.
+        lib = ctypes.CDLL(os.environ.get("CCC_ORACLE_LIB") or build())
         P, I64, I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
         lib.oracle_fwd.argtypes = [P, I64, I64, I64, P, P, P, I, P, I, P, P, P]
         lib.oracle_fwd.restype = I

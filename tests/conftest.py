@@ -17,3 +17,22 @@ def golden(name):
 
     with open(os.path.join(ROOT, "tests", "golden", name)) as f:
         return json.load(f)
+
+
+def _build_libraries():
+    """Build the oracle (gcc) and the CUDA library (nvcc, sm_103a) if stale."""
+    import __graft_entry__
+
+    __graft_entry__.build()
+
+
+_build_libraries()
+
+
+@pytest.fixture(scope="session")
+def cuda_device():
+    import torch
+
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return torch.device("cuda", 0)

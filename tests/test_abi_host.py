@@ -1,0 +1,205 @@
+"""CPU-only checks of the C ABI: the library loads, exports every function the
+header declares, and rejects bad arguments on the host before touching any
+device memory.  The data pointers below are never dereferenced: every call here
+fails a host-side check that runs before the first CUDA call.
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+import depthwise_causal_conv1d_channel_gb300 as ccc
+from depthwise_causal_conv1d_channel_gb300 import _abi
+
+HEADER = os.path.join(ROOT, "include", "ccc_conv1d.h")
+
+BF16, F32, I32 = _abi.CCC_BF16, _abi.CCC_F32, _abi.CCC_I32
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(ccc_\w+)\s*\(", src)))
+
+
+def test_header_declarations_are_exported():
+    names = declared_functions()
+    assert set(names) == set(_abi.EXPORTED)
+    lib = ctypes.CDLL(ccc._abi.lib._name)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_header_compiles_as_c():
+    import subprocess
+    import tempfile
+
+    with tempfile.TemporaryDirectory() as d:
+        src = os.path.join(d, "t.c")
+        with open(src, "w") as f:
+            f.write('#include "ccc_conv1d.h"\nint main(void){return ccc_conv1d_abi_version() != '
+                    'CCC_CONV1D_ABI_VERSION;}\n')
+        r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-c", src, "-o",
+                            os.path.join(d, "t.o"), "-I", os.path.join(ROOT, "include"),
+                            "-I", "/usr/local/cuda/include"], capture_output=True, text=True)
+        assert r.returncode == 0, r.stderr
+
+
+def test_abi_version_and_status_strings():
+    assert _abi.lib.ccc_conv1d_abi_version() == _abi.ABI_VERSION
+    for code in range(8):
+        assert _abi.status_string(code) != "unknown status"
+    assert _abi.status_string(99) == "unknown status"
+
+
+# ---- fake descriptors --------------------------------------------------------
+
+_BASE = 0x7f0000000000
+
+
+def T(addr_off, dtype, shape, stride=None):
+    d = _abi.ccc_tensor()
+    d.data = _BASE + addr_off
+    d.dtype = dtype
+    d.ndim = len(shape)
+    if stride is None:  # contiguous
+        stride, s = [], 1
+        for n in reversed(shape):
+            stride.insert(0, s)
+            s *= n
+    for i, (n, st) in enumerate(zip(shape, stride)):
+        d.shape[i] = n
+        d.stride[i] = st
+    return d
+
+
+def cl(off, B, D, Tn):
+    """Channel-last [B, D, T] view of [B, T, D] storage."""
+    return T(off, BF16, (B, D, Tn), (Tn * D, 1, D))
+
+
+MB = 1 << 20
+
+
+def fwd(x, w, b=None, cu=None, init=None, out=None, fin=None, act=1):
+    r = lambda d: None if d is None else ctypes.byref(d)
+    return _abi.lib.ccc_conv1d_fwd(r(x), r(w), r(b), r(cu), r(init), r(out), r(fin), act, None, None)
+
+
+def bwd(x, w, b, cu, init, g, gf, dx, dw, db, dinit, det=0, act=1, ws=None, ws_bytes=0):
+    r = lambda d: None if d is None else ctypes.byref(d)
+    return _abi.lib.ccc_conv1d_bwd(r(x), r(w), r(b), r(cu), r(init), r(g), r(gf), r(dx), r(dw),
+                                   r(db), r(dinit), act, det, ws, ws_bytes, None, None)
+
+
+B_, D_, T_ = 2, 16, 32
+
+
+def good():
+    return dict(x=cl(0, B_, D_, T_), w=T(10 * MB, BF16, (D_, 4)), b=T(11 * MB, BF16, (D_,)),
+                init=T(12 * MB, BF16, (B_, D_, 3)), out=cl(20 * MB, B_, D_, T_),
+                fin=T(30 * MB, BF16, (B_, D_, 3)))
+
+
+def test_fwd_rejects_bad_arguments_on_host():
+    g = good()
+    bad_x = cl(0, B_, D_, T_)
+    bad_x.dtype = F32
+    assert fwd(bad_x, g["w"], out=g["out"]) == _abi.CCC_ERR_INVALID_ARG
+    assert fwd(g["x"], T(10 * MB, BF16, (D_, 3)), out=g["out"]) == _abi.CCC_ERR_UNSUPPORTED  # width 3
+    assert fwd(g["x"], T(10 * MB, BF16, (D_ + 1, 4)), out=g["out"]) == _abi.CCC_ERR_INVALID_ARG
+    # FP32 weight with bias declines (cuDNN page)
+    assert fwd(g["x"], T(10 * MB, F32, (D_, 4)), g["b"], out=g["out"]) == _abi.CCC_ERR_UNSUPPORTED
+    # unknown activation
+    assert fwd(g["x"], g["w"], out=g["out"], act=7) == _abi.CCC_ERR_INVALID_ARG
+    # neither channel-last nor time-contiguous
+    odd = T(0, BF16, (B_, D_, T_), (D_ * T_ * 4, 2, 2 * D_))
+    assert fwd(odd, g["w"], out=cl(20 * MB, B_, D_, T_)) == _abi.CCC_ERR_UNSUPPORTED
+    # out with a different layout kind than x
+    assert fwd(g["x"], g["w"], out=T(20 * MB, BF16, (B_, D_, T_))) == _abi.CCC_ERR_UNSUPPORTED
+    # states: wrong shape, non-contiguous
+    assert fwd(g["x"], g["w"], init=T(12 * MB, BF16, (B_, D_, 4)), out=g["out"]) == _abi.CCC_ERR_INVALID_ARG
+    assert fwd(g["x"], g["w"], out=g["out"],
+               fin=T(30 * MB, BF16, (B_, D_, 3), (D_ * 3, 1, D_))) == _abi.CCC_ERR_INVALID_ARG
+    # packed with batch 2
+    cu = T(40 * MB, I32, (3,))
+    assert fwd(g["x"], g["w"], cu=cu, out=g["out"]) == _abi.CCC_ERR_UNSUPPORTED
+    # NULL x
+    assert fwd(None, g["w"], out=g["out"]) == _abi.CCC_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("victim", ["x", "w", "b", "init", "cu"])
+def test_fwd_final_states_aliasing_is_rejected(victim):
+    """cuDNN page: final_states_out must not share memory with x, weight, bias,
+    cu_seqlens or initial_states."""
+    g = good()
+    x = cl(0, 1, D_, T_)
+    cu = T(40 * MB, I32, (3,))
+    init = T(12 * MB, BF16, (2, D_, 3))
+    out = cl(20 * MB, 1, D_, T_)
+    addr = {"x": 0, "w": 10 * MB, "b": 11 * MB, "init": 12 * MB, "cu": 40 * MB}[victim]
+    fin = T(addr, BF16, (2, D_, 3))
+    assert fwd(x, g["w"], g["b"], cu, init, out, fin) == _abi.CCC_ERR_ALIAS
+
+
+def test_fwd_out_overlapping_input_is_rejected():
+    g = good()
+    assert fwd(g["x"], g["w"], g["b"], None, g["init"], cl(64, B_, D_, T_), g["fin"]) == _abi.CCC_ERR_ALIAS
+
+
+def test_bwd_rejects_bad_arguments_on_host():
+    g = good()
+    dout = cl(50 * MB, B_, D_, T_)
+    dx = cl(60 * MB, B_, D_, T_)
+    dw = T(70 * MB, BF16, (D_, 4))
+    db = T(71 * MB, BF16, (D_,))
+    dinit = T(72 * MB, BF16, (B_, D_, 3))
+    # deterministic with bias: no deterministic dbias route (cuDNN page)
+    assert bwd(g["x"], g["w"], g["b"], None, g["init"], dout, None, dx, dw, db, dinit,
+               det=1) == _abi.CCC_ERR_NONDETERMINISTIC
+    # dbias required iff bias
+    assert bwd(g["x"], g["w"], g["b"], None, g["init"], dout, None, dx, dw, None, dinit) == _abi.CCC_ERR_INVALID_ARG
+    assert bwd(g["x"], g["w"], None, None, g["init"], dout, None, dx, dw, db, dinit) == _abi.CCC_ERR_INVALID_ARG
+    # dweight dtype must follow weight
+    assert bwd(g["x"], g["w"], g["b"], None, g["init"], dout, None, dx,
+               T(70 * MB, F32, (D_, 4)), db, dinit) == _abi.CCC_ERR_INVALID_ARG
+    # dinitial_states without initial_states
+    assert bwd(g["x"], g["w"], g["b"], None, None, dout, None, dx, dw, db, dinit) == _abi.CCC_ERR_INVALID_ARG
+    # dx overlapping dout
+    assert bwd(g["x"], g["w"], g["b"], None, g["init"], dout, None, cl(50 * MB + 2, B_, D_, T_), dw,
+               db, dinit) == _abi.CCC_ERR_ALIAS
+    # dweight overlapping dbias
+    assert bwd(g["x"], g["w"], g["b"], None, g["init"], dout, None, dx, dw,
+               T(70 * MB + 8, BF16, (D_,)), dinit) == _abi.CCC_ERR_ALIAS
+    assert bwd(g["x"], g["w"], g["b"], None, g["init"], dout, None, dx, dw, db, dinit,
+               det=2) == _abi.CCC_ERR_INVALID_ARG
+
+
+def test_update_rejects_bad_arguments_on_host():
+    r = lambda d: None if d is None else ctypes.byref(d)
+    x = T(0, BF16, (4, D_))
+    st = T(MB, BF16, (4, D_, 3))
+    w = T(2 * MB, BF16, (D_, 4))
+    b = T(3 * MB, BF16, (D_,))
+    out = T(4 * MB, BF16, (4, D_))
+    upd = lambda *a, act=1: _abi.lib.ccc_conv1d_update(*[r(d) for d in a], act, None)
+    assert upd(x, T(MB, BF16, (4, D_, 4)), w, b, out) == _abi.CCC_ERR_INVALID_ARG
+    assert upd(x, st, w, b, T(MB + 6, BF16, (4, D_))) == _abi.CCC_ERR_ALIAS  # out on the state
+    assert upd(T(MB, BF16, (4, D_)), st, w, b, out) == _abi.CCC_ERR_ALIAS    # x on the state
+    assert upd(x, st, T(2 * MB, F32, (D_, 4)), b, out) == _abi.CCC_ERR_UNSUPPORTED
+    assert upd(T(0, BF16, (4, D_), (1, 4)), st, w, b, out) == _abi.CCC_ERR_UNSUPPORTED
+
+
+def test_python_api_rejects_seq_idx_and_bad_activation():
+    import torch
+
+    x = torch.zeros(1, 8, 4, dtype=torch.bfloat16)
+    w = torch.zeros(8, 4, dtype=torch.bfloat16)
+    with pytest.raises(NotImplementedError):
+        ccc.causal_conv1d(x, w, seq_idx=torch.zeros(1, 4, dtype=torch.int32))
+    with pytest.raises(ValueError):
+        ccc.causal_conv1d(x, w, activation="gelu")

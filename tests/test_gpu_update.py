@@ -1,0 +1,69 @@
+"""GPU parity of causal_conv1d_update (the single-token decode step that
+mutates the width-four state in place) against the oracle, including the
+hand-off from the forward's final_states."""
+
+import numpy as np
+import pytest
+import torch
+
+import depthwise_causal_conv1d_channel_gb300 as ccc
+import oracle
+from helpers import assert_bf16_close, assert_bits_equal
+from workloads import bits, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("B,D", [(4, 264), (3, 100), (1, 8), (2, 1), (256, 64)])
+@pytest.mark.parametrize("act", ["silu", None])
+def test_update_parity(B, D, act, cuda_device):
+    gen = torch.Generator().manual_seed(B * 7 + D)
+    state = torch.randn(B, D, 3, generator=gen).to(torch.bfloat16)
+    x = torch.randn(B, D, generator=gen).to(torch.bfloat16)
+    w = (torch.rand(D, 4, generator=gen) - 0.5).to(torch.bfloat16)
+    b = ((torch.rand(D, generator=gen) - 0.5) * 0.2).to(torch.bfloat16)
+    ref = oracle.update(bits(x), bits(state), bits(w), bits(b), act)
+    s_dev = state.to(cuda_device)
+    out = ccc.causal_conv1d_update(x.to(cuda_device), s_dev, w.to(cuda_device), b.to(cuda_device), act)
+    torch.cuda.synchronize()
+    assert_bf16_close(bits(out.cpu()), ref["out"], "out")
+    assert_bits_equal(bits(s_dev.cpu()), ref["state"], "state")
+
+
+def test_update_fp32_weight_no_bias(cuda_device):
+    B, D = 8, 40
+    gen = torch.Generator().manual_seed(3)
+    state = torch.randn(B, D, 3, generator=gen).to(torch.bfloat16)
+    x = torch.randn(B, D, generator=gen).to(torch.bfloat16)
+    w = torch.rand(D, 4, generator=gen) - 0.5
+    ref = oracle.update(bits(x), bits(state), w.numpy(), None)
+    s_dev = state.to(cuda_device)
+    out = ccc.causal_conv1d_update(x.to(cuda_device), s_dev, w.to(cuda_device))
+    torch.cuda.synchronize()
+    assert_bf16_close(bits(out.cpu()), ref["out"], "out")
+    assert_bits_equal(bits(s_dev.cpu()), ref["state"], "state")
+
+
+def test_forward_final_state_feeds_update_chain(cuda_device):
+    """Prefill with the forward, then decode token by token: equals one
+    forward over the whole sequence (cuDNN page: final_states pass directly to
+    causal_conv1d_update, no layout conversion)."""
+    B, D, T, steps = 3, 136, 40, 25
+    full = make_inputs(B, D, T + steps, seed=17, initial_states=True)
+    d = full.to(cuda_device)
+    out_pre, state = ccc.causal_conv1d(d.x[:, :, :T], d.weight, d.bias,
+                                       initial_states=d.initial_states, return_final_states=True)
+    outs = []
+    for s in range(steps):
+        xt = d.x[:, :, T + s].contiguous()
+        outs.append(ccc.causal_conv1d_update(xt, state, d.weight, d.bias))
+    torch.cuda.synchronize()
+    ref = oracle.fwd(bits(full.x), bits(full.weight), bits(full.bias), None, bits(full.initial_states))
+    assert_bf16_close(bits(out_pre.cpu()), np.ascontiguousarray(ref["out"][:, :, :T]), "prefill")
+    chain = torch.stack(outs, dim=2).cpu()
+    assert_bf16_close(bits(chain), np.ascontiguousarray(ref["out"][:, :, T:]), "decode chain")
+    assert_bits_equal(bits(state.cpu()), ref["final"], "state after chain")
+    # the GPU forward and the GPU update chain evaluate the same FMA sequence
+    gpu_full = ccc.causal_conv1d(d.x, d.weight, d.bias, initial_states=d.initial_states)
+    assert torch.equal(gpu_full[:, :, T:].contiguous().view(torch.int16).cpu(),
+                       chain.contiguous().view(torch.int16))

@@ -1,0 +1,61 @@
+"""The pins must catch plausible mistakes in the oracle.
+
+Each case plants one mistake in a copy of conv1d_oracle.c (a wrong tap offset,
+reversed state order, a sign flip in the SiLU derivative, transposed taps in
+the input gradient, ...), compiles it, and runs the pin suite against it in a
+subprocess: the suite has to fail.  Every planted mistake keeps all memory
+accesses in bounds.
+"""
+
+import os
+import subprocess
+import sys
+import tempfile
+
+import pytest
+
+from conftest import ROOT
+
+SRC = os.path.join(ROOT, "oracle", "conv1d_oracle.c")
+
+MUTANTS = {
+    "tap_offset": ("p += w[k] * xe(x, init, t - (CONV_W - 1) + k);",
+                   "p += w[k] * xe(x, init, t - (CONV_W - 1) + (k + 1) % CONV_W);"),
+    "init_order_reversed": ("return init ? init[j + CONV_S] : 0.0;",
+                            "return init ? init[CONV_S - 1 - (j + CONV_S)] : 0.0;"),
+    "silu_grad_sign": ("return s * (1.0 + p * (1.0 - s));", "return s * (1.0 - p * (1.0 - s));"),
+    "silu_forward": ("return act ? p * sigmoid(p) : p;", "return act ? sigmoid(p) : p;"),
+    "dx_taps_transposed": ("acc += wd[k] * gp[t];", "acc += wd[CONV_W - 1 - k] * gp[t];"),
+    "dfinal_reversed": ("acc += gfs[j - (len - CONV_S)];", "acc += gfs[len - 1 - j];"),
+    "final_state_reversed": ("fs[i] = xe(xs, is, len - CONV_S + i);",
+                             "fs[CONV_S - 1 - i] = xe(xs, is, len - CONV_S + i);"),
+    "dw_taps_reversed": ("double term = gp[t] * xe(xs, is, t - (CONV_W - 1) + k);",
+                         "double term = gp[t] * xe(xs, is, t - k);"),
+    "db_without_act_grad": ("sdb += gp[t];", "sdb += gs[t];"),
+    "empty_sequence_accepted": ("if (cu[n + 1] <= cu[n])", "if (cu[n + 1] < cu[n])"),
+    "update_shift": ("s[0] = ext[1];", "s[0] = ext[0];"),
+    "update_drops_bias": ("double p = bias ? bias[d] : 0.0;\n            for (int k = 0; k < CONV_W; ++k)\n                p += wd[k] * ext[k];",
+                          "double p = 0.0;\n            for (int k = 0; k < CONV_W; ++k)\n                p += wd[k] * ext[k];"),
+    "bf16_truncates": ("double r = rint(ldexp(a, -qexp));", "double r = floor(ldexp(a, -qexp));"),
+    "bias_dropped": ("double p = b;\n    for (int k = 0; k < CONV_W; ++k)\n        p += w[k]",
+                     "double p = 0.0 * b;\n    for (int k = 0; k < CONV_W; ++k)\n        p += w[k]"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_reject_planted_mistake(name):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation site for {name} not found exactly once"
+    with tempfile.TemporaryDirectory() as d:
+        msrc = os.path.join(d, "mutant.c")
+        lib = os.path.join(d, "libmutant.so")
+        with open(msrc, "w") as f:
+            f.write(src.replace(old, new))
+        subprocess.check_call(["gcc", "-O2", "-std=c99", "-ffp-contract=off", "-fPIC", "-shared",
+                               msrc, "-o", lib, "-lm"])
+        env = dict(os.environ, CCC_ORACLE_LIB=lib)
+        r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                            os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                           cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+        assert r.returncode != 0, f"pins did not catch mutant {name}:\n{r.stdout[-2000:]}"
