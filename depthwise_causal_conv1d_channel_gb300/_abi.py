@@ -11,6 +11,7 @@ from __future__ import annotations
 
 import ctypes
 import os
+import struct
 
 import torch
 
@@ -97,21 +98,31 @@ def status_string(status: int) -> str:
     return lib.ccc_status_string(int(status)).decode()
 
 
+_PACK = struct.Struct("<Qii3q3q")  # the ccc_tensor layout: 64 bytes
+_desc_memo = {}
+
+
 def desc(t):
-    """ccc_tensor descriptor of a torch tensor, or None."""
+    """ccc_tensor descriptor of a torch tensor, or None.  Descriptors are a pure
+    function of (address, dtype, shape, strides) and are memoised on that key."""
     if t is None:
         return None
-    if t.dtype not in _DTYPES:
+    key = (t.data_ptr(), t.dtype, t.shape, t.stride())
+    d = _desc_memo.get(key)
+    if d is not None:
+        return d
+    code = _DTYPES.get(t.dtype)
+    if code is None:
         raise TypeError(f"unsupported dtype {t.dtype}")
-    if t.dim() > 3:
+    n = t.dim()
+    if n > 3:
         raise ValueError("tensors have at most 3 dimensions")
-    d = ccc_tensor()
-    d.data = t.data_ptr() if t.numel() > 0 else None
-    d.dtype = _DTYPES[t.dtype]
-    d.ndim = t.dim()
-    for i in range(t.dim()):
-        d.shape[i] = t.shape[i]
-        d.stride[i] = t.stride(i)
+    pad = (0,) * (3 - n)
+    d = ccc_tensor.from_buffer_copy(_PACK.pack(t.data_ptr() if t.numel() > 0 else 0, code, n,
+                                               *tuple(t.shape), *pad, *t.stride(), *pad))
+    if len(_desc_memo) > 4096:
+        _desc_memo.clear()
+    _desc_memo[key] = d
     return d
 
 

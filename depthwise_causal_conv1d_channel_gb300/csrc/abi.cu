@@ -169,18 +169,38 @@ bool same_act_shape(const ccc_tensor* t, const Problem& pb) {
   return well_formed(t, 3) && t->dtype == CCC_BF16 && shape_is(t, pb.B, pb.D, pb.T);
 }
 
-// Whether 16-byte vectors of 8 channels can serve every channel-last tensor.
-bool vec8_ok(const Problem& pb, std::initializer_list<const ccc_tensor*> acts,
-             std::initializer_list<const ccc_tensor*> states) {
-  if (pb.layout != ccc::kLayoutChannelLast || pb.D % 8 != 0) return false;
+bool aligned(const void* p, uintptr_t bytes) { return (reinterpret_cast<uintptr_t>(p) % bytes) == 0; }
+
+// Whether vectors of V channels (2V bytes) can serve every channel-last tensor:
+// every row start and every state block must be 2V-byte aligned (state blocks
+// of V channels are 6V bytes; 8 bytes suffices for V = 4).
+bool vec_ok(int V, const Problem& pb, std::initializer_list<const ccc_tensor*> acts,
+            std::initializer_list<const ccc_tensor*> states) {
+  if (pb.layout != ccc::kLayoutChannelLast || pb.D % V != 0) return false;
   for (const ccc_tensor* t : acts) {
     int64_t sb, sd, st;
     act_strides(t, pb.layout, sb, sd, st);
-    if (!aligned16(t->data) || sb % 8 != 0 || st % 8 != 0) return false;
+    if (!aligned(t->data, 2 * V) || sb % V != 0 || st % V != 0) return false;
   }
   for (const ccc_tensor* t : states)
-    if (t && !aligned16(t->data)) return false;
+    if (t && !aligned(t->data, V == 8 ? 16 : 8)) return false;
   return true;
+}
+
+#ifndef CCC_FWD_VEC
+#define CCC_FWD_VEC 4
+#endif
+#ifndef CCC_BWD_VEC
+#define CCC_BWD_VEC 4
+#endif
+
+// Channels per thread: the preferred width when the tensors allow it, else 4,
+// else 1 (scalar).
+int pick_vec(int preferred, const Problem& pb, std::initializer_list<const ccc_tensor*> acts,
+             std::initializer_list<const ccc_tensor*> states) {
+  if (vec_ok(preferred, pb, acts, states)) return preferred;
+  if (preferred != 4 && vec_ok(4, pb, acts, states)) return 4;
+  return 1;
 }
 
 ccc::WeightRef weight_ref(const ccc_tensor* weight, const ccc_tensor* bias) {
@@ -211,13 +231,13 @@ namespace ccc {
 // the token ranges are sized so the grid holds about `waves` full waves of
 // resident blocks, each range at least `min_seg` tokens long.
 static FwdPlan plan_cl(int vec, int64_t Q, int D, int sm_count, int blocks_per_sm, int waves,
-                       int64_t min_seg) {
+                       int64_t min_seg, int threads) {
   FwdPlan p{};
   p.kind = kLayoutChannelLast;
   p.vec = vec;
   const int64_t G = ceil_div(D, vec);
   p.tx = int(std::min<int64_t>(32, next_pow2(G)));
-  p.ty = 256 / p.tx;
+  p.ty = threads / p.tx;
   p.gx = unsigned(ceil_div(G, p.tx));
   const int64_t want = std::max<int64_t>(1, int64_t(sm_count) * std::max(1, blocks_per_sm) * waves);
   int64_t gy = std::max<int64_t>(1, want / p.gx);
@@ -246,16 +266,14 @@ static FwdPlan plan_bdt(int64_t rows) {
   return p;
 }
 
-FwdPlan plan_fwd(int kind, int vec_ok, int64_t Q, int D, int64_t rows, int sm_count) {
+FwdPlan plan_fwd(int kind, int vec, int64_t Q, int D, int64_t rows, int sm_count) {
   if (kind == kLayoutTimeContiguous) return plan_bdt(rows);
-  const int vec = vec_ok ? 8 : 1;
-  return plan_cl(vec, Q, D, sm_count, fwd_blocks_per_sm(vec), 4, 8);
+  return plan_cl(vec, Q, D, sm_count, fwd_blocks_per_sm(vec), 1, 8, 256);
 }
 
-BwdPlan plan_bwd(int kind, int vec_ok, int64_t Q, int D, int64_t rows, int sm_count) {
+BwdPlan plan_bwd(int kind, int vec, int64_t Q, int D, int64_t rows, int sm_count) {
   if (kind == kLayoutTimeContiguous) return plan_bdt(rows);
-  const int vec = vec_ok ? 8 : 1;
-  return plan_cl(vec, Q, D, sm_count, bwd_blocks_per_sm(vec), 4, 16);
+  return plan_cl(vec, Q, D, sm_count, bwd_blocks_per_sm(vec), 1, 16, bwd_block_threads(vec));
 }
 
 int64_t bwd_partial_rows(const BwdPlan& p, int B, bool packed) {
@@ -316,22 +334,22 @@ ccc_status ccc_conv1d_fwd(const ccc_tensor* x, const ccc_tensor* weight, const c
   a.D = pb.D;
   a.status = d_status;
   if (pb.n_seq == 0) return CCC_OK;
-  const bool v8 = vec8_ok(pb, {x, out}, {initial_states, final_states});
+  const int vec = pick_vec(CCC_FWD_VEC, pb, {x, out}, {initial_states, final_states});
   const int64_t rows = pb.packed ? pb.D : int64_t(pb.B) * pb.D;
-  const ccc::FwdPlan p = ccc::plan_fwd(pb.layout, v8, a.seqs.Q, pb.D, rows, sms);
+  const ccc::FwdPlan p = ccc::plan_fwd(pb.layout, vec, a.seqs.Q, pb.D, rows, sms);
   a.seg_len = p.seg_len;
   a.n_seg = p.n_seg;
   return ccc::launch_fwd(a, p, activation, stream) == cudaSuccess ? CCC_OK : CCC_ERR_CUDA;
 }
 
 // Shared by the size query and the call itself, so both agree.
-static bool bwd_plan_for(const ccc_tensor* x, const Problem& pb, bool v8, ccc::BwdPlan& p) {
+static bool bwd_plan_for(const ccc_tensor* x, const Problem& pb, int vec, ccc::BwdPlan& p) {
   const int sms = device_sm_count();
   if (sms <= 0) return false;
   const int64_t Q = pb.packed ? pb.T : int64_t(pb.B) * pb.T;
   const int64_t rows = pb.packed ? pb.D : int64_t(pb.B) * pb.D;
   (void)x;
-  p = ccc::plan_bwd(pb.layout, v8, Q, pb.D, rows, sms);
+  p = ccc::plan_bwd(pb.layout, vec, Q, pb.D, rows, sms);
   return true;
 }
 
@@ -349,11 +367,14 @@ size_t ccc_conv1d_bwd_workspace_size(const ccc_tensor* x, int deterministic) {
   pb.T = x->shape[2];
   pb.layout = layout_of(x);
   if (pb.layout < 0) return 0;
-  // The call picks 8-channel vectors or scalars from the alignment of all its
-  // tensors, and a packed call needs no more than a dense one: cover both.
-  ccc::BwdPlan p8{}, p1{};
-  if (!bwd_plan_for(x, pb, true, p8) || !bwd_plan_for(x, pb, false, p1)) return 0;
-  const size_t n = std::max(bwd_ws_bytes(p8, pb, deterministic), bwd_ws_bytes(p1, pb, deterministic));
+  // The call picks its vector width from the alignment of all its tensors, and
+  // a packed call needs no more than a dense one: cover every width.
+  size_t n = 0;
+  for (int vec : {8, 4, 1}) {
+    ccc::BwdPlan p{};
+    if (!bwd_plan_for(x, pb, vec, p)) return 0;
+    n = std::max(n, bwd_ws_bytes(p, pb, deterministic));
+  }
   return (n + 255) / 256 * 256;
 }
 
@@ -395,9 +416,10 @@ ccc_status ccc_conv1d_bwd(const ccc_tensor* x, const ccc_tensor* weight, const c
     for (int j = i + 1; j < 4; ++j)
       if (outs[i] && outs[j] && overlaps(outs[i], outs[j])) return CCC_ERR_ALIAS;
 
-  const bool v8 = vec8_ok(pb, {x, dout, dx}, {initial_states, dfinal_states, dinitial_states});
+  const int vec = pick_vec(CCC_BWD_VEC, pb, {x, dout, dx},
+                           {initial_states, dfinal_states, dinitial_states});
   ccc::BwdPlan p{};
-  if (!bwd_plan_for(x, pb, v8, p)) return CCC_ERR_CUDA;
+  if (!bwd_plan_for(x, pb, vec, p)) return CCC_ERR_CUDA;
   const size_t need = bwd_ws_bytes(p, pb, deterministic);
   if (!workspace || workspace_bytes < need || !aligned16(workspace)) return CCC_ERR_WORKSPACE;
   {

@@ -12,13 +12,14 @@
 // accumulated) and emitting dxe[m - 3] once gp[m-3 .. m] are known.  The
 // thread whose range starts a sequence also emits the three dinit entries.
 #include <atomic>
+#include <type_traits>
 
 #include "common.cuh"
 #include "launch.h"
 
 namespace ccc {
 
-template <int V, int ACT, int U>
+template <int V, int ACT, int U, int P>
 __device__ __forceinline__ void bwd_walk(const BwdArgs& a, const Seqs& seqs, const Stream& xs,
                                          const Stream& gs, const Stream& ds, int n_base, int d0,
                                          const float (&w)[V][kWidth], const float (&b)[V],
@@ -140,9 +141,27 @@ __device__ __forceinline__ void bwd_walk(const BwdArgs& a, const Seqs& seqs, con
     int64_t m = a0;
     const int64_t m_end = e + kState;
     const int64_t pro_end = a0 + kState < m_end ? a0 + kState : m_end;
+    // rows this piece reads: [a0, min(e + 3, hi)); prefetch P rows ahead into L2
+    const int64_t r_end = m_end < hi ? m_end : hi;
+    if constexpr (P > 0) {
+      for (int64_t t = a0 + kState; t < a0 + kState + P && t < r_end; ++t) {
+        prefetch_l2(a.x + xs.at(n, t));
+        prefetch_l2(a.g + gs.at(n, t));
+      }
+    }
     for (; m < pro_end; ++m) slow(m);
     // steady state: own tokens, emissions land in [a0, e - 3), no state involved
     for (; m + U <= e; m += U) {
+      if constexpr (P > 0) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int64_t t = m + P + u;
+          if (t < r_end) {
+            prefetch_l2(a.x + xs.at(n, t));
+            prefetch_l2(a.g + gs.at(n, t));
+          }
+        }
+      }
       typename VT::Raw xr[U], gr[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
@@ -201,7 +220,10 @@ __device__ __forceinline__ void block_wgrad_out(const BwdArgs& a, int d0, bool a
 
 template <int V, int ACT>
 __global__ void __launch_bounds__(256) bwd_cl_kernel(BwdArgs a) {
+  __shared__ __align__(16) float wsm[(kWidth + 1) * kMaxBlockChannels];
   if (block_rejects_cu_seqlens(a.seqs, a.status)) return;
+  const int n_blk = blockDim.x * V;
+  stage_weights(a.wr, blockIdx.x * n_blk, n_blk, a.D, wsm);
   const int d0 = (blockIdx.x * blockDim.x + threadIdx.x) * V;
   const int64_t seg = int64_t(blockIdx.y) * blockDim.y + threadIdx.y;
   const bool active = d0 < a.D && seg < a.n_seg;
@@ -214,14 +236,225 @@ __global__ void __launch_bounds__(256) bwd_cl_kernel(BwdArgs a) {
   }
   if (active) {
     float w[V][kWidth], b[V];
-    load_weights<V>(a.wr, d0, w, b);
+    weights_from_smem<V>(wsm, n_blk, threadIdx.x * V, w, b);
     const int64_t q0 = seg * a.seg_len;
     const int64_t q1 = q0 + a.seg_len < a.seqs.Q ? q0 + a.seg_len : a.seqs.Q;
     const bool dense = a.seqs.cu == nullptr;
     const Stream xs{d0, dense ? a.x_sb - a.seqs.T * a.x_st : 0, a.x_st};
     const Stream gs{d0, dense ? a.g_sb - a.seqs.T * a.g_st : 0, a.g_st};
     const Stream ds{d0, dense ? a.dx_sb - a.seqs.T * a.dx_st : 0, a.dx_st};
-    bwd_walk<V, ACT, 4>(a, a.seqs, xs, gs, ds, 0, d0, w, b, q0, q1, aw, ab);
+    bwd_walk<V, ACT, 4, (V == 8 ? 16 : 0)>(a, a.seqs, xs, gs, ds, 0, d0, w, b, q0, q1, aw, ab);
+  }
+  block_wgrad_out<V>(a, d0, active, aw, ab);
+}
+
+// Channel-last backward with vectors of V = 8 or 4 channels (the fast path).
+// Same walk as bwd_walk, specialised like fwd_clv_kernel: the input window
+// and the gradient window rotate through three register slots, steady state
+// runs in groups of three tokens, rows kBwdPrefetch tokens ahead of both x and
+// grad_out are prefetched into L2.  128-thread blocks, two resident per SM
+// (the windows, weights and sums need ~200 registers a thread; a tighter
+// bound spills).
+#ifndef CCC_BWD_MIN_BLOCKS
+#define CCC_BWD_MIN_BLOCKS 2
+#endif
+#ifndef CCC_BWD_PREFETCH
+#define CCC_BWD_PREFETCH 9
+#endif
+constexpr int kBwdPrefetch = CCC_BWD_PREFETCH;
+constexpr int kBwdThreads = 128;
+
+template <int V, int ACT>
+__global__ void __launch_bounds__(kBwdThreads, V == 8 ? CCC_BWD_MIN_BLOCKS : 4)
+    bwd_clv_kernel(BwdArgs a) {
+  using VT = Vec<V>;
+  __shared__ __align__(16) float wsm[(kWidth + 1) * kMaxBlockChannels];
+  if (block_rejects_cu_seqlens(a.seqs, a.status)) return;
+  const int n_blk = blockDim.x * V;
+  stage_weights(a.wr, blockIdx.x * n_blk, n_blk, a.D, wsm);
+  const int d0 = (blockIdx.x * blockDim.x + threadIdx.x) * V;
+  const int64_t seg = int64_t(blockIdx.y) * blockDim.y + threadIdx.y;
+  const bool active = d0 < a.D && seg < a.n_seg;
+  float aw[V][kWidth], ab[V];
+#pragma unroll
+  for (int c = 0; c < V; ++c) {
+    ab[c] = 0.0f;
+#pragma unroll
+    for (int k = 0; k < kWidth; ++k) aw[c][k] = 0.0f;
+  }
+  if (active) {
+    float w[V][kWidth], b[V];
+    weights_from_smem<V>(wsm, n_blk, threadIdx.x * V, w, b);
+    int64_t q = seg * a.seg_len;
+    const int64_t q_end = q + a.seg_len < a.seqs.Q ? q + a.seg_len : a.seqs.Q;
+    const bool dense = a.seqs.cu == nullptr;
+    int n = find_seq(a.seqs, q);
+    using P0 = std::integral_constant<int, 0>;
+    using P1 = std::integral_constant<int, 1>;
+    using P2 = std::integral_constant<int, 2>;
+    while (q < q_end) {
+      int64_t lo, hi;
+      seq_bounds(a.seqs, n, lo, hi);
+      const int64_t a0 = q;
+      const int64_t e = q_end < hi ? q_end : hi;
+      const bool starts = a0 == lo;
+      const int64_t state_row = int64_t(n) * a.D + d0;
+      const int64_t xst = a.x_st, gst = a.g_st, dst = a.dx_st;
+      // pointers at token a0
+      const uint16_t* xp = a.x + (dense ? n * a.x_sb + (a0 - lo) * xst : a0 * xst) + d0;
+      const uint16_t* gq = a.g + (dense ? n * a.g_sb + (a0 - lo) * gst : a0 * gst) + d0;
+      uint16_t* dp = a.dx + (dense ? n * a.dx_sb + (a0 - lo) * dst : a0 * dst) + d0;
+
+      float X[kState][V], G[kState][V];
+      {
+        float init[kState][V];
+        if (a0 - kState < lo && a.init) {
+          load_state<V>(a.init + state_row * kState, init);
+        } else {
+#pragma unroll
+          for (int i = 0; i < kState; ++i)
+#pragma unroll
+            for (int c = 0; c < V; ++c) init[i][c] = 0.0f;
+        }
+#pragma unroll
+        for (int j = 0; j < kState; ++j) {
+          const int64_t tok = a0 - kState + j;
+          if (tok >= lo) {
+            VT::unpack(VT::ld(xp - (kState - j) * xst), X[j]);
+          } else {
+            const int64_t i = tok - lo + kState;
+#pragma unroll
+            for (int c = 0; c < V; ++c)
+              X[j][c] = i == 0 ? init[0][c] : (i == 1 ? init[1][c] : init[2][c]);
+          }
+#pragma unroll
+          for (int c = 0; c < V; ++c) G[j][c] = 0.0f;
+        }
+      }
+      const int64_t m_end = e + kState;
+      const int64_t r_end = m_end < hi ? m_end : hi;  // rows read: [a0, r_end)
+      for (int64_t t = a0 + kState; t < a0 + kState + kBwdPrefetch && t < r_end; ++t) {
+        prefetch_l2(xp + (t - a0) * xst);
+        prefetch_l2(gq + (t - a0) * gst);
+      }
+
+      // general step at token m, window at phase 0 (physical shifts)
+      auto slow = [&](int64_t m) {
+        float gp[V], v[V];
+        if (m < hi) {
+          float xc[V], gc[V];
+          VT::unpack(VT::ld(xp + (m - a0) * xst), xc);
+          VT::unpack(VT::ld(gq + (m - a0) * gst), gc);
+          const bool own = m < e;
+#pragma unroll
+          for (int c = 0; c < V; ++c) {
+            float p = b[c];
+            p = fmaf(w[c][0], X[0][c], p);
+            p = fmaf(w[c][1], X[1][c], p);
+            p = fmaf(w[c][2], X[2][c], p);
+            p = fmaf(w[c][3], xc[c], p);
+            gp[c] = gc[c] * act_grad<ACT>(p);
+            if (own) {
+              aw[c][0] = fmaf(gp[c], X[0][c], aw[c][0]);
+              aw[c][1] = fmaf(gp[c], X[1][c], aw[c][1]);
+              aw[c][2] = fmaf(gp[c], X[2][c], aw[c][2]);
+              aw[c][3] = fmaf(gp[c], xc[c], aw[c][3]);
+              ab[c] += gp[c];
+            }
+            X[0][c] = X[1][c];
+            X[1][c] = X[2][c];
+            X[2][c] = xc[c];
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < V; ++c) gp[c] = 0.0f;
+        }
+#pragma unroll
+        for (int c = 0; c < V; ++c) {
+          float sacc = w[c][0] * gp[c];
+          sacc = fmaf(w[c][1], G[2][c], sacc);
+          sacc = fmaf(w[c][2], G[1][c], sacc);
+          sacc = fmaf(w[c][3], G[0][c], sacc);
+          v[c] = sacc;
+          G[0][c] = G[1][c];
+          G[1][c] = G[2][c];
+          G[2][c] = gp[c];
+        }
+        const int64_t j = m - kState;
+        if (j >= a0 || starts) {
+          if (a.dfin && j >= hi - kState) {
+            const int64_t i = j - (hi - kState);
+#pragma unroll
+            for (int c = 0; c < V; ++c)
+              v[c] += bf16_to_f32(__ldg(a.dfin + (state_row + c) * kState + i));
+          }
+          if (j >= lo) {
+            VT::st(dp + (j - a0) * dst, VT::pack(v));
+          } else if (a.dinit) {  // one of the three entries before the sequence
+            const int64_t i = j - lo + kState;
+#pragma unroll
+            for (int c = 0; c < V; ++c) a.dinit[(state_row + c) * kState + i] = f32_to_bf16(v[c]);
+          }
+        }
+      };
+
+      // steady step at window phase J for token m (own token, emission to dx[m-3])
+      auto fast = [&](auto phase, typename VT::Raw xr, typename VT::Raw gr, uint16_t* drow) {
+        constexpr int J = decltype(phase)::value;
+        constexpr int J1 = (J + 1) % 3, J2 = (J + 2) % 3;
+        float xc[V], gc[V], v[V];
+        VT::unpack(xr, xc);
+        VT::unpack(gr, gc);
+#pragma unroll
+        for (int c = 0; c < V; ++c) {
+          float p = b[c];
+          p = fmaf(w[c][0], X[J][c], p);
+          p = fmaf(w[c][1], X[J1][c], p);
+          p = fmaf(w[c][2], X[J2][c], p);
+          p = fmaf(w[c][3], xc[c], p);
+          const float gp = gc[c] * act_grad<ACT>(p);
+          aw[c][0] = fmaf(gp, X[J][c], aw[c][0]);
+          aw[c][1] = fmaf(gp, X[J1][c], aw[c][1]);
+          aw[c][2] = fmaf(gp, X[J2][c], aw[c][2]);
+          aw[c][3] = fmaf(gp, xc[c], aw[c][3]);
+          ab[c] += gp;
+          X[J][c] = xc[c];
+          float sacc = w[c][0] * gp;
+          sacc = fmaf(w[c][1], G[J2][c], sacc);
+          sacc = fmaf(w[c][2], G[J1][c], sacc);
+          sacc = fmaf(w[c][3], G[J][c], sacc);
+          v[c] = sacc;
+          G[J][c] = gp;
+        }
+        VT::st(drow, VT::pack(v));
+      };
+
+      int64_t m = a0;
+      const int64_t pro_end = a0 + kState < m_end ? a0 + kState : m_end;
+      for (; m < pro_end; ++m) slow(m);
+      for (; m + 3 <= e; m += 3) {
+        const uint16_t* xm = xp + (m - a0) * xst;
+        const uint16_t* gm = gq + (m - a0) * gst;
+#pragma unroll
+        for (int u = 0; u < 3; ++u) {
+          const int64_t t = m + kBwdPrefetch + u;
+          if (t < r_end) {
+            prefetch_l2(xm + (kBwdPrefetch + u) * xst);
+            prefetch_l2(gm + (kBwdPrefetch + u) * gst);
+          }
+        }
+        typename VT::Raw xr0 = VT::ld(xm), xr1 = VT::ld(xm + xst), xr2 = VT::ld(xm + 2 * xst);
+        typename VT::Raw gr0 = VT::ld(gm), gr1 = VT::ld(gm + gst), gr2 = VT::ld(gm + 2 * gst);
+        uint16_t* drow = dp + (m - kState - a0) * dst;
+        fast(P0{}, xr0, gr0, drow);
+        fast(P1{}, xr1, gr1, drow + dst);
+        fast(P2{}, xr2, gr2, drow + 2 * dst);
+      }
+      for (; m < m_end; ++m) slow(m);
+
+      q = e;
+      ++n;
+    }
   }
   block_wgrad_out<V>(a, d0, active, aw, ab);
 }
@@ -240,7 +473,7 @@ __global__ void __launch_bounds__(256) bwd_bdt_kernel(BwdArgs a) {
   const int bb = int(row / a.D);
   const int d = int(row % a.D);
   float w[1][kWidth], b[1];
-  load_weights<1>(a.wr, d, w, b);
+  load_weights_1(a.wr, d, w, b);
   Seqs rs = a.seqs;
   if (dense) { rs.Q = a.seqs.T; rs.n_seq = 1; }
   const Stream xs{bb * a.x_sb + d * a.x_sd, 0, 1};
@@ -249,7 +482,7 @@ __global__ void __launch_bounds__(256) bwd_bdt_kernel(BwdArgs a) {
   float aw[1][kWidth] = {{0.0f, 0.0f, 0.0f, 0.0f}}, ab[1] = {0.0f};
   for (int64_t q0 = int64_t(lane) * 8; q0 < rs.Q; q0 += 256) {
     const int64_t q1 = q0 + 8 < rs.Q ? q0 + 8 : rs.Q;
-    bwd_walk<1, ACT, 4>(a, rs, xs, gs, ds, dense ? bb : 0, d, w, b, q0, q1, aw, ab);
+    bwd_walk<1, ACT, 4, 0>(a, rs, xs, gs, ds, dense ? bb : 0, d, w, b, q0, q1, aw, ab);
   }
   float v[kWidth + 1] = {aw[0][0], aw[0][1], aw[0][2], aw[0][3], ab[0]};
 #pragma unroll
@@ -290,16 +523,20 @@ __global__ void bwd_empty_kernel(const uint16_t* dfin, uint16_t* dinit, int64_t 
 
 // ---- host launchers ------------------------------------------------------------
 
+int bwd_block_threads(int vec) { return vec >= 4 ? kBwdThreads : 256; }
+
 int bwd_blocks_per_sm(int vec) {
-  static std::atomic<int> cache[2];
-  const int i = vec == 8 ? 0 : 1;
+  static std::atomic<int> cache[3];
+  const int i = vec == 8 ? 0 : vec == 4 ? 1 : 2;
   int v = cache[i].load(std::memory_order_relaxed);
   if (v == 0) {
     int n = 0;
-    const size_t smem = size_t(256) * vec * (kWidth + 1) * sizeof(float);
+    const int threads = bwd_block_threads(vec);
+    const size_t smem = size_t(threads) * vec * (kWidth + 1) * sizeof(float);
     const cudaError_t err =
-        vec == 8 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, bwd_cl_kernel<8, kActSilu>, 256, smem)
-                 : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, bwd_cl_kernel<1, kActSilu>, 256, smem);
+        vec == 8   ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, bwd_clv_kernel<8, kActSilu>, threads, smem)
+        : vec == 4 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, bwd_clv_kernel<4, kActSilu>, threads, smem)
+                   : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, bwd_cl_kernel<1, kActSilu>, threads, smem);
     v = (err == cudaSuccess && n > 0) ? n : 1;
     cache[i].store(v, std::memory_order_relaxed);
   }
@@ -311,7 +548,8 @@ static void launch_bwd_act(const BwdArgs& a, const BwdPlan& p, cudaStream_t stre
   if (p.kind == kLayoutChannelLast) {
     dim3 block(p.tx, p.ty), grid(p.gx, p.gy);
     const size_t smem = size_t(p.tx) * p.ty * p.vec * (kWidth + 1) * sizeof(float);
-    if (p.vec == 8) bwd_cl_kernel<8, ACT><<<grid, block, smem, stream>>>(a);
+    if (p.vec == 8) bwd_clv_kernel<8, ACT><<<grid, block, smem, stream>>>(a);
+    else if (p.vec == 4) bwd_clv_kernel<4, ACT><<<grid, block, smem, stream>>>(a);
     else bwd_cl_kernel<1, ACT><<<grid, block, smem, stream>>>(a);
   } else {
     bwd_bdt_kernel<ACT><<<p.gx, 256, 0, stream>>>(a);

@@ -38,22 +38,30 @@ __device__ __forceinline__ uint16_t f32_to_bf16(float f) {
 
 enum Act { kActNone = 0, kActSilu = 1 };
 
-// silu(p) = p * sigmoid(p) = p / (1 + e^-p).  For p below about -87 the
-// denominator overflows and the quotient is 0, the correct limit.
+__device__ __forceinline__ float tanh_approx(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// silu(p) = p * sigmoid(p), with sigmoid(p) = (1 + tanh(p / 2)) / 2 from the
+// hardware tanh (one MUFU operation; relative error about 2^-11, so the
+// absolute error of silu stays below |p| * 2^-12).
 template <int ACT>
 __device__ __forceinline__ float act_fwd(float p) {
   if constexpr (ACT == kActSilu) {
-    return __fdividef(p, 1.0f + __expf(-p));
+    return p * fmaf(0.5f, tanh_approx(0.5f * p), 0.5f);
   } else {
     return p;
   }
 }
 
-// d act / d p:  silu'(p) = s * (1 + p * (1 - s)),  s = sigmoid(p).
+// d act / d p:  silu'(p) = s * (1 + p * (1 - s)),  s = sigmoid(p), with s from
+// the hardware tanh as in act_fwd (absolute error of s below 2^-12).
 template <int ACT>
 __device__ __forceinline__ float act_grad(float p) {
   if constexpr (ACT == kActSilu) {
-    const float s = __fdividef(1.0f, 1.0f + __expf(-p));
+    const float s = fmaf(0.5f, tanh_approx(0.5f * p), 0.5f);
     return s * fmaf(p, 1.0f - s, 1.0f);
   } else {
     return 1.0f;
@@ -87,6 +95,24 @@ struct Vec<8> {
 };
 
 template <>
+struct Vec<4> {
+  using Raw = uint2;  // 4 x BF16 = 8 bytes
+  __device__ __forceinline__ static Raw ld(const uint16_t* p) {
+    return __ldg(reinterpret_cast<const uint2*>(p));
+  }
+  __device__ __forceinline__ static void st(uint16_t* p, Raw r) {
+    __stcs(reinterpret_cast<uint2*>(p), r);
+  }
+  __device__ __forceinline__ static void unpack(Raw r, float (&f)[4]) {
+    f[0] = bf16_lo(r.x); f[1] = bf16_hi(r.x);
+    f[2] = bf16_lo(r.y); f[3] = bf16_hi(r.y);
+  }
+  __device__ __forceinline__ static Raw pack(const float (&f)[4]) {
+    return make_uint2(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]));
+  }
+};
+
+template <>
 struct Vec<1> {
   using Raw = uint16_t;
   __device__ __forceinline__ static Raw ld(const uint16_t* p) { return __ldg(p); }
@@ -99,9 +125,17 @@ struct Vec<1> {
 // contiguous BF16 values, entry (c, i) at c*3 + i.  win[i][c] = state(c, i).
 template <int V>
 __device__ __forceinline__ void load_state(const uint16_t* s, float (&win)[kState][V]) {
-  if constexpr (V == 8) {
+  if constexpr (V == 8) {  // 48 bytes, 16-byte aligned
     union { uint4 q[3]; uint16_t h[24]; } u;
     const uint4* p = reinterpret_cast<const uint4*>(s);
+    u.q[0] = __ldg(p); u.q[1] = __ldg(p + 1); u.q[2] = __ldg(p + 2);
+#pragma unroll
+    for (int c = 0; c < V; ++c)
+#pragma unroll
+      for (int i = 0; i < kState; ++i) win[i][c] = bf16_to_f32(u.h[c * 3 + i]);
+  } else if constexpr (V == 4) {  // 24 bytes, 8-byte aligned
+    union { uint2 q[3]; uint16_t h[12]; } u;
+    const uint2* p = reinterpret_cast<const uint2*>(s);
     u.q[0] = __ldg(p); u.q[1] = __ldg(p + 1); u.q[2] = __ldg(p + 2);
 #pragma unroll
     for (int c = 0; c < V; ++c)
@@ -125,6 +159,14 @@ __device__ __forceinline__ void store_state(uint16_t* s, const float (&win)[kSta
       for (int i = 0; i < kState; ++i) u.h[c * 3 + i] = f32_to_bf16(win[i][c]);
     uint4* p = reinterpret_cast<uint4*>(s);
     p[0] = u.q[0]; p[1] = u.q[1]; p[2] = u.q[2];
+  } else if constexpr (V == 4) {
+    union { uint2 q[3]; uint16_t h[12]; } u;
+#pragma unroll
+    for (int c = 0; c < V; ++c)
+#pragma unroll
+      for (int i = 0; i < kState; ++i) u.h[c * 3 + i] = f32_to_bf16(win[i][c]);
+    uint2* p = reinterpret_cast<uint2*>(s);
+    p[0] = u.q[0]; p[1] = u.q[1]; p[2] = u.q[2];
   } else {
 #pragma unroll
     for (int c = 0; c < V; ++c)
@@ -143,20 +185,91 @@ struct WeightRef {
   int64_t b_sd;
 };
 
-template <int V>
-__device__ __forceinline__ void load_weights(const WeightRef& r, int d0, float (&w)[V][kWidth],
-                                             float (&b)[V]) {
+// Widest channel slice a block stages: 32 threads x 8 channels.
+constexpr int kMaxBlockChannels = 256;
+
+// Block-cooperative copy of the weights and bias of channels
+// [d_base, d_base + n) into shared memory as FP32, tap-major: ws[k*n + i] is
+// w[d_base + i, k] for k < 4 and ws[4*n + i] the bias (0 without one, or past
+// D).  Consecutive threads read consecutive channels, so the global reads are
+// coalesced for the usual [D, 4] layout.  Every thread of the block must call it.
+__device__ __forceinline__ void stage_weights(const WeightRef& r, int d_base, int n, int D,
+                                              float* ws) {
+  const int tid = threadIdx.x + blockDim.x * (threadIdx.y + blockDim.y * threadIdx.z);
+  const int nthr = blockDim.x * blockDim.y * blockDim.z;
+  const int total = n * (kWidth + 1);
+  // all loads of a batch are issued before any is consumed
+  constexpr int kBatch = 5;
+  for (int e0 = tid; e0 < total; e0 += kBatch * nthr) {
+    float v[kBatch];
 #pragma unroll
-  for (int c = 0; c < V; ++c) {
-    const int64_t d = d0 + c;
-#pragma unroll
-    for (int k = 0; k < kWidth; ++k) {
-      const int64_t o = d * r.w_sd + k * r.w_sk;
-      w[c][k] = r.w_f32 ? __ldg(static_cast<const float*>(r.w) + o)
-                        : bf16_to_f32(__ldg(static_cast<const uint16_t*>(r.w) + o));
+    for (int j = 0; j < kBatch; ++j) {
+      const int e = e0 + j * nthr;
+      v[j] = 0.0f;
+      if (e < total) {
+        const int k = e / n, i = e - k * n;
+        const int64_t d = int64_t(d_base) + i;
+        if (d < D) {
+          if (k < kWidth) {
+            const int64_t o = d * r.w_sd + k * r.w_sk;
+            v[j] = r.w_f32 ? __ldg(static_cast<const float*>(r.w) + o)
+                           : bf16_to_f32(__ldg(static_cast<const uint16_t*>(r.w) + o));
+          } else if (r.bias) {
+            v[j] = bf16_to_f32(__ldg(r.bias + d * r.b_sd));
+          }
+        }
+      }
     }
-    b[c] = r.bias ? bf16_to_f32(__ldg(r.bias + d * r.b_sd)) : 0.0f;
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j)
+      if (e0 + j * nthr < total) ws[e0 + j * nthr] = v[j];
   }
+  __syncthreads();
+}
+
+// A thread's V channels (local index i0, a multiple of V) from the staged slice.
+template <int V>
+__device__ __forceinline__ void weights_from_smem(const float* ws, int n, int i0,
+                                                  float (&w)[V][kWidth], float (&b)[V]) {
+  if constexpr (V % 4 == 0) {
+#pragma unroll
+    for (int k = 0; k <= kWidth; ++k) {
+#pragma unroll
+      for (int c = 0; c < V; c += 4) {
+        const float4 v = *reinterpret_cast<const float4*>(ws + k * n + i0 + c);
+        const float f[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if (k < kWidth) w[c + j][k] = f[j]; else b[c + j] = f[j];
+        }
+      }
+    }
+  } else {
+#pragma unroll
+    for (int c = 0; c < V; ++c) {
+#pragma unroll
+      for (int k = 0; k < kWidth; ++k) w[c][k] = ws[k * n + i0 + c];
+      b[c] = ws[kWidth * n + i0 + c];
+    }
+  }
+}
+
+// Weights of one channel straight from global memory (warp-uniform channel:
+// every lane reads the same addresses).
+__device__ __forceinline__ void load_weights_1(const WeightRef& r, int64_t d, float (&w)[1][kWidth],
+                                               float (&b)[1]) {
+#pragma unroll
+  for (int k = 0; k < kWidth; ++k) {
+    const int64_t o = d * r.w_sd + k * r.w_sk;
+    w[0][k] = r.w_f32 ? __ldg(static_cast<const float*>(r.w) + o)
+                      : bf16_to_f32(__ldg(static_cast<const uint16_t*>(r.w) + o));
+  }
+  b[0] = r.bias ? bf16_to_f32(__ldg(r.bias + d * r.b_sd)) : 0.0f;
+}
+
+// Hint: bring the 32-byte sector holding p into L2 ahead of its load.
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
 // ---- sequences -----------------------------------------------------------------
@@ -173,7 +286,11 @@ struct Seqs {
 };
 
 __device__ __forceinline__ int find_seq(const Seqs& s, int64_t q) {
-  if (!s.cu) return static_cast<int>(q / s.T);
+  if (!s.cu) {
+    if (q < 0x7fffffff && s.T < 0x7fffffff)  // 32-bit division when it fits
+      return static_cast<int>(static_cast<uint32_t>(q) / static_cast<uint32_t>(s.T));
+    return static_cast<int>(q / s.T);
+  }
   int lo = 0, hi = s.n_seq;  // invariant: cu[lo] <= q < cu[hi]
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;

@@ -8,6 +8,7 @@
 // output written once.  Nothing is staged: the op is a streaming stencil with
 // about one FLOP per byte, bound by HBM bandwidth, not a contraction.
 #include <atomic>
+#include <type_traits>
 
 #include "common.cuh"
 #include "launch.h"
@@ -15,8 +16,10 @@
 namespace ccc {
 
 // One thread: channels [d0, d0 + V), tokens [q, q_end) of one token stream.
-// `n_base` is the state index of the stream's sequence 0.
-template <int V, int ACT, int U>
+// `n_base` is the state index of the stream's sequence 0.  U token loads are
+// in flight per step; rows P tokens further on are prefetched into L2 (P = 0:
+// none), so the bytes in flight do not depend on registers.
+template <int V, int ACT, int U, int P>
 __device__ __forceinline__ void fwd_walk(const FwdArgs& a, const Seqs& seqs, const Stream& xs,
                                          const Stream& os, int n_base, int d0,
                                          const float (&w)[V][kWidth], const float (&b)[V],
@@ -74,8 +77,18 @@ __device__ __forceinline__ void fwd_walk(const FwdArgs& a, const Seqs& seqs, con
       VT::st(a.out + os.at(n, t), VT::pack(y));
     };
 
+    if constexpr (P > 0) {
+      for (int64_t t = q + U; t < q + U + P && t < e; ++t) prefetch_l2(a.x + xs.at(n, t));
+    }
     // steady state: U loads in flight, then U outputs
     for (; q + U <= e; q += U) {
+      if constexpr (P > 0) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int64_t t = q + U + P + u;
+          if (t < e) prefetch_l2(a.x + xs.at(n, t));
+        }
+      }
       typename VT::Raw raw[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) raw[u] = VT::ld(a.x + xs.at(n, q + u));
@@ -96,18 +109,152 @@ __device__ __forceinline__ void fwd_walk(const FwdArgs& a, const Seqs& seqs, con
 // per token.
 template <int V, int ACT>
 __global__ void __launch_bounds__(256) fwd_cl_kernel(FwdArgs a) {
+  __shared__ __align__(16) float ws[(kWidth + 1) * kMaxBlockChannels];
   if (block_rejects_cu_seqlens(a.seqs, a.status)) return;
+  const int n_blk = blockDim.x * V;
+  stage_weights(a.wr, blockIdx.x * n_blk, n_blk, a.D, ws);
   const int d0 = (blockIdx.x * blockDim.x + threadIdx.x) * V;
   const int64_t seg = int64_t(blockIdx.y) * blockDim.y + threadIdx.y;
   if (d0 >= a.D || seg >= a.n_seg) return;
   float w[V][kWidth], b[V];
-  load_weights<V>(a.wr, d0, w, b);
+  weights_from_smem<V>(ws, n_blk, threadIdx.x * V, w, b);
   const int64_t q0 = seg * a.seg_len;
   const int64_t q1 = q0 + a.seg_len < a.seqs.Q ? q0 + a.seg_len : a.seqs.Q;
   const bool dense = a.seqs.cu == nullptr;
   const Stream xs{d0, dense ? a.x_sb - a.seqs.T * a.x_st : 0, a.x_st};
   const Stream os{d0, dense ? a.o_sb - a.seqs.T * a.o_st : 0, a.o_st};
-  fwd_walk<V, ACT, 4>(a, a.seqs, xs, os, 0, d0, w, b, q0, q1);
+  fwd_walk<V, ACT, 4, (V == 8 ? 16 : 0)>(a, a.seqs, xs, os, 0, d0, w, b, q0, q1);
+}
+
+// Channel-last x with vectors of V = 8 or 4 channels (the fast path).  Same
+// walk as fwd_walk, specialised: the three-token window lives in three register
+// slots that rotate (the newest token overwrites the oldest slot), so steady
+// state runs in groups of three tokens with no register copies; x and out are
+// addressed through running pointers; rows kPrefetch tokens ahead are
+// prefetched into L2.
+#ifndef CCC_FWD_PREFETCH
+#define CCC_FWD_PREFETCH 0
+#endif
+constexpr int kFwdGroup = 6;                 // tokens per steady-state step (multiple of 3)
+constexpr int kFwdPrefetch = CCC_FWD_PREFETCH;  // tokens of L2 prefetch distance
+
+template <int V, int ACT>
+__global__ void __launch_bounds__(256, V == 8 ? 2 : 3) fwd_clv_kernel(FwdArgs a) {
+  using VT = Vec<V>;
+  __shared__ __align__(16) float ws[(kWidth + 1) * kMaxBlockChannels];
+  if (block_rejects_cu_seqlens(a.seqs, a.status)) return;
+  const int n_blk = blockDim.x * V;
+  stage_weights(a.wr, blockIdx.x * n_blk, n_blk, a.D, ws);
+  const int d0 = (blockIdx.x * blockDim.x + threadIdx.x) * V;
+  const int64_t seg = int64_t(blockIdx.y) * blockDim.y + threadIdx.y;
+  if (d0 >= a.D || seg >= a.n_seg) return;
+  float w[V][kWidth], b[V];
+  weights_from_smem<V>(ws, n_blk, threadIdx.x * V, w, b);
+  int64_t q = seg * a.seg_len;
+  const int64_t q_end = q + a.seg_len < a.seqs.Q ? q + a.seg_len : a.seqs.Q;
+  const bool dense = a.seqs.cu == nullptr;
+  int n = find_seq(a.seqs, q);
+  while (q < q_end) {
+    int64_t lo, hi;
+    seq_bounds(a.seqs, n, lo, hi);
+    const int64_t e = q_end < hi ? q_end : hi;
+    const int64_t state_row = int64_t(n) * a.D + d0;
+    // running pointers at token q
+    const uint16_t* xp = a.x + (dense ? n * a.x_sb + (q - lo) * a.x_st : q * a.x_st) + d0;
+    uint16_t* op = a.out + (dense ? n * a.o_sb + (q - lo) * a.o_st : q * a.o_st) + d0;
+    const int64_t xst = a.x_st, ost = a.o_st;
+
+    // W[j] = xe[q - 3 + j]
+    float W[kState][V];
+    {
+      float init[kState][V];
+      if (q - kState < lo && a.init) {
+        load_state<V>(a.init + state_row * kState, init);
+      } else {
+#pragma unroll
+        for (int i = 0; i < kState; ++i)
+#pragma unroll
+          for (int c = 0; c < V; ++c) init[i][c] = 0.0f;
+      }
+#pragma unroll
+      for (int j = 0; j < kState; ++j) {
+        const int64_t tok = q - kState + j;
+        if (tok >= lo) {
+          VT::unpack(VT::ld(xp - (kState - j) * xst), W[j]);
+        } else {
+          const int64_t i = tok - lo + kState;
+#pragma unroll
+          for (int c = 0; c < V; ++c)
+            W[j][c] = i == 0 ? init[0][c] : (i == 1 ? init[1][c] : init[2][c]);
+        }
+      }
+    }
+    for (int64_t t = kFwdGroup; t < kFwdGroup + kFwdPrefetch && q + t < e; ++t)
+      prefetch_l2(xp + t * xst);
+
+    // one token at window phase J: taps W[J], W[J+1], W[J+2] (mod 3), then the
+    // new token replaces W[J]
+    auto step = [&](auto phase, typename VT::Raw raw, uint16_t* dst) {
+      constexpr int J = decltype(phase)::value;
+      float cur[V], y[V];
+      VT::unpack(raw, cur);
+#pragma unroll
+      for (int c = 0; c < V; ++c) {
+        float p = b[c];
+        p = fmaf(w[c][0], W[J][c], p);
+        p = fmaf(w[c][1], W[(J + 1) % 3][c], p);
+        p = fmaf(w[c][2], W[(J + 2) % 3][c], p);
+        p = fmaf(w[c][3], cur[c], p);
+        y[c] = act_fwd<ACT>(p);
+        W[J][c] = cur[c];
+      }
+      VT::st(dst, VT::pack(y));
+    };
+    using P0 = std::integral_constant<int, 0>;
+    using P1 = std::integral_constant<int, 1>;
+    using P2 = std::integral_constant<int, 2>;
+
+    for (; q + kFwdGroup <= e; q += kFwdGroup) {
+#pragma unroll
+      for (int u = 0; u < kFwdGroup; ++u) {
+        const int64_t t = kFwdGroup + kFwdPrefetch + u;
+        if (q + t < e) prefetch_l2(xp + t * xst);
+      }
+      typename VT::Raw r[kFwdGroup];
+#pragma unroll
+      for (int u = 0; u < kFwdGroup; ++u) r[u] = VT::ld(xp + u * xst);
+#pragma unroll
+      for (int u = 0; u < kFwdGroup; u += 3) {
+        step(P0{}, r[u], op + u * ost);
+        step(P1{}, r[u + 1], op + (u + 1) * ost);
+        step(P2{}, r[u + 2], op + (u + 2) * ost);
+      }
+      xp += kFwdGroup * xst;
+      op += kFwdGroup * ost;
+    }
+    // remainder: physical shift keeps the window at phase 0
+    for (; q < e; ++q) {
+      float cur[V], y[V];
+      VT::unpack(VT::ld(xp), cur);
+#pragma unroll
+      for (int c = 0; c < V; ++c) {
+        float p = b[c];
+        p = fmaf(w[c][0], W[0][c], p);
+        p = fmaf(w[c][1], W[1][c], p);
+        p = fmaf(w[c][2], W[2][c], p);
+        p = fmaf(w[c][3], cur[c], p);
+        y[c] = act_fwd<ACT>(p);
+        W[0][c] = W[1][c];
+        W[1][c] = W[2][c];
+        W[2][c] = cur[c];
+      }
+      VT::st(op, VT::pack(y));
+      xp += xst;
+      op += ost;
+    }
+    if (e == hi && a.fin) store_state<V>(a.fin + state_row * kState, W);
+    ++n;
+  }
 }
 
 // Time-contiguous x (stride of T is 1).  One warp per (batch, channel) row;
@@ -123,7 +270,7 @@ __global__ void __launch_bounds__(256) fwd_bdt_kernel(FwdArgs a) {
   const int bb = int(row / a.D);
   const int d = int(row % a.D);
   float w[1][kWidth], b[1];
-  load_weights<1>(a.wr, d, w, b);
+  load_weights_1(a.wr, d, w, b);
   // Within a row, a dense call is one sequence of T tokens (state index bb).
   Seqs rs = a.seqs;
   if (dense) { rs.Q = a.seqs.T; rs.n_seq = 1; }
@@ -131,7 +278,7 @@ __global__ void __launch_bounds__(256) fwd_bdt_kernel(FwdArgs a) {
   const Stream os{bb * a.o_sb + d * a.o_sd, 0, 1};
   for (int64_t q0 = int64_t(lane) * 8; q0 < rs.Q; q0 += 256) {
     const int64_t q1 = q0 + 8 < rs.Q ? q0 + 8 : rs.Q;
-    fwd_walk<1, ACT, 4>(a, rs, xs, os, dense ? bb : 0, d, w, b, q0, q1);
+    fwd_walk<1, ACT, 4, 0>(a, rs, xs, os, dense ? bb : 0, d, w, b, q0, q1);
   }
 }
 
@@ -144,14 +291,15 @@ __global__ void fwd_empty_kernel(const uint16_t* init, uint16_t* fin, int64_t n)
 // ---- host launchers ------------------------------------------------------------
 
 int fwd_blocks_per_sm(int vec) {
-  static std::atomic<int> cache[2];
-  const int i = vec == 8 ? 0 : 1;
+  static std::atomic<int> cache[3];
+  const int i = vec == 8 ? 0 : vec == 4 ? 1 : 2;
   int v = cache[i].load(std::memory_order_relaxed);
   if (v == 0) {
     int n = 0;
     const cudaError_t err =
-        vec == 8 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fwd_cl_kernel<8, kActSilu>, 256, 0)
-                 : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fwd_cl_kernel<1, kActSilu>, 256, 0);
+        vec == 8   ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fwd_clv_kernel<8, kActSilu>, 256, 0)
+        : vec == 4 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fwd_clv_kernel<4, kActSilu>, 256, 0)
+                   : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fwd_cl_kernel<1, kActSilu>, 256, 0);
     v = (err == cudaSuccess && n > 0) ? n : 1;
     cache[i].store(v, std::memory_order_relaxed);
   }
@@ -162,7 +310,8 @@ template <int ACT>
 static cudaError_t launch_fwd_act(const FwdArgs& a, const FwdPlan& p, cudaStream_t stream) {
   if (p.kind == kLayoutChannelLast) {
     dim3 block(p.tx, p.ty), grid(p.gx, p.gy);
-    if (p.vec == 8) fwd_cl_kernel<8, ACT><<<grid, block, 0, stream>>>(a);
+    if (p.vec == 8) fwd_clv_kernel<8, ACT><<<grid, block, 0, stream>>>(a);
+    else if (p.vec == 4) fwd_clv_kernel<4, ACT><<<grid, block, 0, stream>>>(a);
     else fwd_cl_kernel<1, ACT><<<grid, block, 0, stream>>>(a);
   } else {
     fwd_bdt_kernel<ACT><<<p.gx, 256, 0, stream>>>(a);

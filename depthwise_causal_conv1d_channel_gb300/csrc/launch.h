@@ -80,6 +80,8 @@ int64_t bwd_partial_rows(const BwdPlan& p, int B, bool packed);
 // Resident blocks per SM of the channel-last kernels (SiLU instance), cached.
 int fwd_blocks_per_sm(int vec);
 int bwd_blocks_per_sm(int vec);
+// Threads per block of the channel-last backward kernel for this vector width.
+int bwd_block_threads(int vec);
 
 cudaError_t launch_fwd(const FwdArgs& a, const FwdPlan& p, int act, cudaStream_t stream);
 cudaError_t launch_bwd(const BwdArgs& a, const BwdPlan& p, int act, const WgradOut& o,

@@ -5,53 +5,75 @@
 //   out[b,d]   = act(bias[d] + w0*s0 + w1*s1 + w2*s2 + w3*x[b,d])
 //   state[b,d] = [s1, s2, x[b,d]]      (bitwise)
 //
-// One thread per V consecutive channels of one batch row: one 16-byte load of
-// x, three of the state, one 16-byte store of out, three of the state.
+// A thread owns V consecutive channels of R batch rows: per row one 16-byte
+// load of x, three of the state, one 16-byte store of out, three of the state.
 #include "common.cuh"
 #include "launch.h"
 
 namespace ccc {
 
-template <int V, int ACT>
+// Block (tx, ty): threadIdx.x over groups of V channels, threadIdx.y over
+// groups of R batch rows.  The block stages its channels' weights once; each
+// thread issues the loads of all its R rows before computing any of them.
+template <int V, int ACT, int R>
 __global__ void __launch_bounds__(256) update_kernel(UpdArgs a) {
   using VT = Vec<V>;
-  const int groups = a.D / V;
-  const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= int64_t(a.B) * groups) return;
-  const int bb = int(i / groups);
-  const int d0 = int(i % groups) * V;
+  __shared__ __align__(16) float ws[(kWidth + 1) * kMaxBlockChannels];
+  const int n_blk = blockDim.x * V;
+  stage_weights(a.wr, blockIdx.x * n_blk, n_blk, a.D, ws);
+  const int d0 = (blockIdx.x * blockDim.x + threadIdx.x) * V;
+  const int b0 = (blockIdx.y * blockDim.y + threadIdx.y) * R;
+  if (d0 >= a.D || b0 >= a.B) return;
   float w[V][kWidth], b[V];
-  load_weights<V>(a.wr, d0, w, b);
-  uint16_t* s = a.state + (int64_t(bb) * a.D + d0) * kState;
-  float win[kState][V], xc[V], y[V];
-  load_state<V>(s, win);
-  VT::unpack(VT::ld(a.x + bb * a.x_sb + d0), xc);
+  weights_from_smem<V>(ws, n_blk, threadIdx.x * V, w, b);
+  float win[R][kState][V];
+  typename VT::Raw xr[R];
 #pragma unroll
-  for (int c = 0; c < V; ++c) {
-    float p = b[c];
-    p = fmaf(w[c][0], win[0][c], p);
-    p = fmaf(w[c][1], win[1][c], p);
-    p = fmaf(w[c][2], win[2][c], p);
-    p = fmaf(w[c][3], xc[c], p);
-    y[c] = act_fwd<ACT>(p);
-    win[0][c] = win[1][c];
-    win[1][c] = win[2][c];
-    win[2][c] = xc[c];
+  for (int r = 0; r < R; ++r) {
+    if (b0 + r < a.B) {
+      load_state<V>(a.state + (int64_t(b0 + r) * a.D + d0) * kState, win[r]);
+      xr[r] = VT::ld(a.x + int64_t(b0 + r) * a.x_sb + d0);
+    }
   }
-  VT::st(a.out + bb * a.o_sb + d0, VT::pack(y));
-  store_state<V>(s, win);
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    if (b0 + r >= a.B) break;
+    float xc[V], y[V];
+    VT::unpack(xr[r], xc);
+#pragma unroll
+    for (int c = 0; c < V; ++c) {
+      float p = b[c];
+      p = fmaf(w[c][0], win[r][0][c], p);
+      p = fmaf(w[c][1], win[r][1][c], p);
+      p = fmaf(w[c][2], win[r][2][c], p);
+      p = fmaf(w[c][3], xc[c], p);
+      y[c] = act_fwd<ACT>(p);
+      win[r][0][c] = win[r][1][c];
+      win[r][1][c] = win[r][2][c];
+      win[r][2][c] = xc[c];
+    }
+    VT::st(a.out + int64_t(b0 + r) * a.o_sb + d0, VT::pack(y));
+    store_state<V>(a.state + (int64_t(b0 + r) * a.D + d0) * kState, win[r]);
+  }
 }
 
+constexpr int kUpdateRows = 2;
+
 cudaError_t launch_update(const UpdArgs& a, int vec, int act, cudaStream_t stream) {
-  const int64_t threads = int64_t(a.B) * (a.D / vec);
-  if (threads == 0) return cudaSuccess;
-  const unsigned grid = unsigned((threads + 255) / 256);
+  if (a.B == 0) return cudaSuccess;
+  const int64_t groups = (a.D + vec - 1) / vec;
+  int tx = 1;
+  while (tx < groups && tx < 32) tx <<= 1;
+  const int ty = 256 / tx;
+  dim3 block(tx, ty);
+  dim3 grid(unsigned((groups + tx - 1) / tx),
+            unsigned((a.B + int64_t(ty) * kUpdateRows - 1) / (int64_t(ty) * kUpdateRows)));
   if (vec == 8) {
-    if (act == kActSilu) update_kernel<8, kActSilu><<<grid, 256, 0, stream>>>(a);
-    else update_kernel<8, kActNone><<<grid, 256, 0, stream>>>(a);
+    if (act == kActSilu) update_kernel<8, kActSilu, kUpdateRows><<<grid, block, 0, stream>>>(a);
+    else update_kernel<8, kActNone, kUpdateRows><<<grid, block, 0, stream>>>(a);
   } else {
-    if (act == kActSilu) update_kernel<1, kActSilu><<<grid, 256, 0, stream>>>(a);
-    else update_kernel<1, kActNone><<<grid, 256, 0, stream>>>(a);
+    if (act == kActSilu) update_kernel<1, kActSilu, kUpdateRows><<<grid, block, 0, stream>>>(a);
+    else update_kernel<1, kActNone, kUpdateRows><<<grid, block, 0, stream>>>(a);
   }
   return cudaGetLastError();
 }
