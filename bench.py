@@ -197,7 +197,9 @@ class DenseStep:
         self.bwd_bytes = bwd_bytes(d.x, self.w, self.b, self.init, self.dfin, self.dinit)
         self.tokens = inp.tokens if inp.cu_seqlens is None else d.x.shape[2]
         self.launches_fwd = 1
-        self.launches_bwd = 2  # backward kernel + fixed-order finalize (plus a memset node)
+        # backward kernel (+ the fixed-order finalize kernel in deterministic mode),
+        # after a memset node
+        self.launches_bwd = 2 if deterministic else 1
 
     def fwd(self, i, stream):
         k = i % self.sets
@@ -217,59 +219,82 @@ class DenseStep:
         assert rc == 0, self.abi.status_string(rc)
 
 
+def _graph_of(fn, device, eager_first=True):
+    """Capture fn(stream) into a CUDA graph (after one eager call, by default)."""
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream(device)
+    s.wait_stream(torch.cuda.current_stream(device))
+    with torch.cuda.stream(s):
+        if eager_first:
+            fn(torch.cuda.current_stream(device))
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=s):
+            fn(torch.cuda.current_stream(device))
+    torch.cuda.synchronize()
+    return g
+
+
 def time_fwd_bwd(step: DenseStep, steps: int, warmup: int, stream, barrier=lambda: None):
+    """W eager warm-up steps; then the K steps as two CUDA graphs -- the K
+    forward calls (buffer set k % sets for step k), then the K backward calls,
+    as a training step runs every forward before every backward -- each
+    replayed once untimed (graph upload) and then once timed, with events on
+    the launching stream before, between and after the two replays.  Returns
+    the total and the per-call forward and backward times."""
+    n = step.sets
     for i in range(warmup):
-        step.fwd(i, stream)
-        step.bwd(i, stream)
+        step.fwd(i % n, stream)
+        step.bwd(i % n, stream)
     torch.cuda.synchronize()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
+    dev = step.dev
+    fg = _graph_of(lambda s: [step.fwd((warmup + i) % n, s) for i in range(steps)], dev,
+                   eager_first=False)
+    bg = _graph_of(lambda s: [step.bwd((warmup + i) % n, s) for i in range(steps)], dev,
+                   eager_first=False)
+    fg.replay()
+    bg.replay()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
     barrier()
     torch.cuda.synchronize()
-    t0.record(stream)
-    for i in range(steps):
-        e = evs[i]
-        e[0].record(stream)
-        step.fwd(warmup + i, stream)
-        e[1].record(stream)
-        step.bwd(warmup + i, stream)
-        e[2].record(stream)
-    t1.record(stream)
+    ev[0].record(stream)
+    fg.replay()
+    ev[1].record(stream)
+    bg.replay()
+    ev[2].record(stream)
     torch.cuda.synchronize()
     barrier()
-    total_ms = t0.elapsed_time(t1)
-    fwd_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    bwd_ms = [e[1].elapsed_time(e[2]) for e in evs]
     step.check_status(stream)
-    return total_ms, fwd_ms, bwd_ms
+    fwd_ms = ev[0].elapsed_time(ev[1]) / steps
+    bwd_ms = ev[1].elapsed_time(ev[2]) / steps
+    return ev[0].elapsed_time(ev[2]), fwd_ms, bwd_ms
 
 
 # ---- breakdown over the other workloads ---------------------------------------------
 
-def _median_ms(fn, iters, stream):
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(iters)]
-    for i, (a, b) in enumerate(evs):
+def _per_call_ms(call, sets, device, stream, per=20, reps=5):
+    """Median over `reps` replays of one graph holding `per` calls on rotating
+    buffer sets: per-call device time with launch overhead amortised."""
+    g = _graph_of(lambda s: [call(i % sets, s) for i in range(per)], device)
+    g.replay()
+    torch.cuda.synchronize()
+    out = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        fn(i)
+        g.replay()
         b.record(stream)
-    torch.cuda.synchronize()
-    return statistics.median(a.elapsed_time(b) for a, b in evs)
+        torch.cuda.synchronize()
+        out.append(a.elapsed_time(b) / per)
+    return statistics.median(out)
 
 
-def bench_conv_workload(name, inp, device, stream, peak, deterministic, iters=30, do_bwd=True):
+def bench_conv_workload(name, inp, device, stream, peak, deterministic, do_bwd=True):
     st = DenseStep(inp, device, deterministic=deterministic)
-    for i in range(3):
-        st.fwd(i, stream)
-        if do_bwd:
-            st.bwd(i, stream)
-    torch.cuda.synchronize()
     r = {"workload": name, "tokens": st.tokens, "rotating_sets": st.sets}
-    f_ms = _median_ms(lambda i: st.fwd(i, stream), iters, stream)
+    f_ms = _per_call_ms(st.fwd, st.sets, device, stream)
     r["fwd"] = _rate(st.fwd_bytes, f_ms, st.tokens, peak)
     if do_bwd:
-        b_ms = _median_ms(lambda i: st.bwd(i, stream), iters, stream)
+        b_ms = _per_call_ms(st.bwd, st.sets, device, stream)
         r["bwd"] = _rate(st.bwd_bytes, b_ms, st.tokens, peak)
     st.check_status(stream)
     del st
@@ -296,29 +321,16 @@ def bench_update(device, stream, peak, iters=50):
     w = (torch.rand(D, 4, device=device, generator=gen) - 0.5).to(torch.bfloat16)
     b = ((torch.rand(D, device=device, generator=gen) - 0.5) * 0.2).to(torch.bfloat16)
 
-    def upd(i):
+    def upd(i, s):
         k = i % sets
-        rc = _abi.ccc_conv1d_update(x[k], state[k], w, b, out[k], _abi.CCC_ACT_SILU, stream)
+        rc = _abi.ccc_conv1d_update(x[k], state[k], w, b, out[k], _abi.CCC_ACT_SILU, s)
         assert rc == 0
 
-    for i in range(3):
-        upd(i)
-    ms = _median_ms(upd, iters, stream)
+    ms = _per_call_ms(upd, sets, device, stream, per=40)
     r = {"workload": "decode_update", "batch": B, "dim": D, "rotating_sets": sets,
          "update": _rate(update_bytes(B, D, w, b), ms, B, peak)}
-    # 1000 chained steps on one state captured in a CUDA graph (hot in L2; context only)
-    g = torch.cuda.CUDAGraph()
-    s = torch.cuda.Stream(device)
-    s.wait_stream(torch.cuda.current_stream(device))
-    with torch.cuda.stream(s):
-        for _ in range(2):
-            upd(0)
-        torch.cuda.synchronize()
-        with torch.cuda.graph(g, stream=s):
-            for _ in range(1000):
-                rc = _abi.ccc_conv1d_update(x[0], state[0], w, b, out[0], _abi.CCC_ACT_SILU,
-                                            torch.cuda.current_stream(device))
-                assert rc == 0
+    # 1000 chained steps on one state in one CUDA graph (hot in L2; context only)
+    g = _graph_of(lambda s: [upd(0, s) for _ in range(1000)], device)
     torch.cuda.synchronize()
     a, c = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(stream)
@@ -491,7 +503,7 @@ def main():
             pg.barrier()
 
     with ClockSampler(local) as clk:
-        total_ms, fwd_ms, bwd_ms = time_fwd_bwd(step, args.steps, args.warmup, stream, barrier)
+        total_ms, f_ms, b_ms = time_fwd_bwd(step, args.steps, args.warmup, stream, barrier)
     clocks = clk.summary()
 
     ms_step = total_ms / args.steps
@@ -503,7 +515,6 @@ def main():
     value = world * step_bytes / (ms_step * 1e-3) / 1e9
     tokens_per_s = world * step.tokens / (ms_step * 1e-3)
 
-    f_ms, b_ms = statistics.mean(fwd_ms), statistics.mean(bwd_ms)
     dominant = ("bwd", b_ms, step.bwd_bytes) if b_ms >= f_ms else ("fwd", f_ms, step.fwd_bytes)
     achieved = dominant[2] / (dominant[1] * 1e-3) / 1e9
     traffic = TRAFFIC["bytes_per_launch"] if TRAFFIC["sources_sha256"] == kernel_sources_digest() else None
@@ -525,6 +536,8 @@ def main():
         "tokens_per_s": round(tokens_per_s),
         "fwd_us": round(f_ms * 1e3, 2), "bwd_us": round(b_ms * 1e3, 2),
         "gpu_launches": args.steps * (step.launches_fwd + step.launches_bwd),
+        "timing": "K forward calls then K backward calls, each as one CUDA graph replay "
+                  "(after an untimed upload replay); events before, between and after",
         "roofline": {"bound": "hbm", "kernel": f"{dominant[0]} call (dense_state)",
                      "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
@@ -543,11 +556,9 @@ def main():
                                   True),
               bench_update(device, stream, peak)]
         large = workloads.dense_large(bias=True)
-        bd.append(bench_conv_workload("dense_large_bias", large, device, stream, peak, False,
-                                      iters=10))
+        bd.append(bench_conv_workload("dense_large_bias", large, device, stream, peak, False))
         large = dataclasses.replace(large, bias=None, deterministic=True)
-        bd.append(bench_conv_workload("dense_large_det", large, device, stream, peak, True,
-                                      iters=10))
+        bd.append(bench_conv_workload("dense_large_det", large, device, stream, peak, True))
         line["breakdown"] = bd
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -187,12 +187,20 @@ bool vec_ok(int V, const Problem& pb, std::initializer_list<const ccc_tensor*> a
   return true;
 }
 
-#ifndef CCC_FWD_VEC
-#define CCC_FWD_VEC 4
-#endif
 #ifndef CCC_BWD_VEC
-#define CCC_BWD_VEC 4
+#define CCC_BWD_VEC 0  // 0: chosen per call by bwd_preferred_vec
 #endif
+
+// Backward vector width.  Eight channels a thread halve the per-token load,
+// address and prefetch work but need ~210 registers (two 128-thread blocks an
+// SM); four channels fit four blocks.  Long per-thread token ranges favour
+// eight, short ones the extra parallelism of four.
+int bwd_preferred_vec(int64_t Q, int D, int sm_count) {
+  if (CCC_BWD_VEC) return CCC_BWD_VEC;
+  const int64_t resident_threads = int64_t(sm_count) * ccc::bwd_blocks_per_sm(8) * 128;
+  const int64_t tokens_per_thread = Q * ((D + 7) / 8) / std::max<int64_t>(resident_threads, 1);
+  return tokens_per_thread >= 128 ? 8 : 4;
+}
 
 // Channels per thread: the preferred width when the tensors allow it, else 4,
 // else 1 (scalar).
@@ -334,7 +342,7 @@ ccc_status ccc_conv1d_fwd(const ccc_tensor* x, const ccc_tensor* weight, const c
   a.D = pb.D;
   a.status = d_status;
   if (pb.n_seq == 0) return CCC_OK;
-  const int vec = pick_vec(CCC_FWD_VEC, pb, {x, out}, {initial_states, final_states});
+  const int vec = pick_vec(4, pb, {x, out}, {initial_states, final_states});
   const int64_t rows = pb.packed ? pb.D : int64_t(pb.B) * pb.D;
   const ccc::FwdPlan p = ccc::plan_fwd(pb.layout, vec, a.seqs.Q, pb.D, rows, sms);
   a.seg_len = p.seg_len;
@@ -416,7 +424,10 @@ ccc_status ccc_conv1d_bwd(const ccc_tensor* x, const ccc_tensor* weight, const c
     for (int j = i + 1; j < 4; ++j)
       if (outs[i] && outs[j] && overlaps(outs[i], outs[j])) return CCC_ERR_ALIAS;
 
-  const int vec = pick_vec(CCC_BWD_VEC, pb, {x, dout, dx},
+  const int sms = device_sm_count();
+  if (sms <= 0) return CCC_ERR_CUDA;
+  const int64_t Q = pb.packed ? pb.T : int64_t(pb.B) * pb.T;
+  const int vec = pick_vec(bwd_preferred_vec(Q, pb.D, sms), pb, {x, dout, dx},
                            {initial_states, dfinal_states, dinitial_states});
   ccc::BwdPlan p{};
   if (!bwd_plan_for(x, pb, vec, p)) return CCC_ERR_CUDA;
@@ -494,9 +505,14 @@ ccc_status ccc_conv1d_update(const ccc_tensor* x, const ccc_tensor* conv_state,
   a.wr = weight_ref(weight, bias);
   a.B = B;
   a.D = D;
-  const bool v8 = D % 8 == 0 && aligned16(x->data) && aligned16(out->data) &&
-                  aligned16(conv_state->data) && a.x_sb % 8 == 0 && a.o_sb % 8 == 0;
-  return ccc::launch_update(a, v8 ? 8 : 1, activation, stream) == cudaSuccess ? CCC_OK : CCC_ERR_CUDA;
+  // vectors of V channels: 2V-byte aligned rows; a state block of V channels
+  // is 6V bytes (16-byte alignment for V = 8, 8 for V = 4)
+  auto fits = [&](int V) {
+    return D % V == 0 && aligned(x->data, 2 * V) && aligned(out->data, 2 * V) &&
+           aligned(conv_state->data, V == 8 ? 16 : 8) && a.x_sb % V == 0 && a.o_sb % V == 0;
+  };
+  const int vec = fits(8) ? 8 : fits(4) ? 4 : 1;
+  return ccc::launch_update(a, vec, activation, stream) == cudaSuccess ? CCC_OK : CCC_ERR_CUDA;
 }
 
 ccc_status ccc_read_status(int* d_status, cudaStream_t stream) {

@@ -268,23 +268,24 @@ template <int V, int ACT>
 __global__ void __launch_bounds__(kBwdThreads, V == 8 ? CCC_BWD_MIN_BLOCKS : 4)
     bwd_clv_kernel(BwdArgs a) {
   using VT = Vec<V>;
+  constexpr int H = V / 2;  // channel pairs
   __shared__ __align__(16) float wsm[(kWidth + 1) * kMaxBlockChannels];
   if (block_rejects_cu_seqlens(a.seqs, a.status)) return;
   const int n_blk = blockDim.x * V;
-  stage_weights(a.wr, blockIdx.x * n_blk, n_blk, a.D, wsm);
   const int d0 = (blockIdx.x * blockDim.x + threadIdx.x) * V;
   const int64_t seg = int64_t(blockIdx.y) * blockDim.y + threadIdx.y;
   const bool active = d0 < a.D && seg < a.n_seg;
-  float aw[V][kWidth], ab[V];
+  stage_weights(a.wr, blockIdx.x * n_blk, n_blk, a.D, wsm);
+  float2 aw[H][kWidth], ab[H];
 #pragma unroll
-  for (int c = 0; c < V; ++c) {
-    ab[c] = 0.0f;
+  for (int h = 0; h < H; ++h) {
+    ab[h] = splat2(0.0f);
 #pragma unroll
-    for (int k = 0; k < kWidth; ++k) aw[c][k] = 0.0f;
+    for (int k = 0; k < kWidth; ++k) aw[h][k] = splat2(0.0f);
   }
   if (active) {
-    float w[V][kWidth], b[V];
-    weights_from_smem<V>(wsm, n_blk, threadIdx.x * V, w, b);
+    float2 w[H][kWidth], b[H];
+    weights_from_smem2<V>(wsm, n_blk, threadIdx.x * V, w, b);
     int64_t q = seg * a.seg_len;
     const int64_t q_end = q + a.seg_len < a.seqs.Q ? q + a.seg_len : a.seqs.Q;
     const bool dense = a.seqs.cu == nullptr;
@@ -305,95 +306,102 @@ __global__ void __launch_bounds__(kBwdThreads, V == 8 ? CCC_BWD_MIN_BLOCKS : 4)
       const uint16_t* gq = a.g + (dense ? n * a.g_sb + (a0 - lo) * gst : a0 * gst) + d0;
       uint16_t* dp = a.dx + (dense ? n * a.dx_sb + (a0 - lo) * dst : a0 * dst) + d0;
 
-      float X[kState][V], G[kState][V];
+      float2 X[kState][H], G[kState][H];  // xe[m-3 .. m-1], gp[m-3 .. m-1]
       {
-        float init[kState][V];
+        float2 init[kState][H];
         if (a0 - kState < lo && a.init) {
-          load_state<V>(a.init + state_row * kState, init);
+          load_state2<V>(a.init + state_row * kState, init);
         } else {
 #pragma unroll
           for (int i = 0; i < kState; ++i)
 #pragma unroll
-            for (int c = 0; c < V; ++c) init[i][c] = 0.0f;
+            for (int h = 0; h < H; ++h) init[i][h] = splat2(0.0f);
         }
 #pragma unroll
         for (int j = 0; j < kState; ++j) {
           const int64_t tok = a0 - kState + j;
           if (tok >= lo) {
-            VT::unpack(VT::ld(xp - (kState - j) * xst), X[j]);
+            VT::unpack2(VT::ld(xp - (kState - j) * xst), X[j]);
           } else {
             const int64_t i = tok - lo + kState;
 #pragma unroll
-            for (int c = 0; c < V; ++c)
-              X[j][c] = i == 0 ? init[0][c] : (i == 1 ? init[1][c] : init[2][c]);
+            for (int h = 0; h < H; ++h)
+              X[j][h] = i == 0 ? init[0][h] : (i == 1 ? init[1][h] : init[2][h]);
           }
 #pragma unroll
-          for (int c = 0; c < V; ++c) G[j][c] = 0.0f;
+          for (int h = 0; h < H; ++h) G[j][h] = splat2(0.0f);
         }
       }
       const int64_t m_end = e + kState;
       const int64_t r_end = m_end < hi ? m_end : hi;  // rows read: [a0, r_end)
-      for (int64_t t = a0 + kState; t < a0 + kState + kBwdPrefetch && t < r_end; ++t) {
-        prefetch_l2(xp + (t - a0) * xst);
-        prefetch_l2(gq + (t - a0) * gst);
+      if constexpr (kBwdPrefetch > 0) {
+        for (int64_t t = a0 + kState; t < a0 + kState + kBwdPrefetch && t < r_end; ++t) {
+          prefetch_l2(xp + (t - a0) * xst);
+          prefetch_l2(gq + (t - a0) * gst);
+        }
       }
 
-      // general step at token m, window at phase 0 (physical shifts)
+      // general step at token m, windows at phase 0 (physical shifts)
       auto slow = [&](int64_t m) {
-        float gp[V], v[V];
+        float2 gp[H], v[H];
         if (m < hi) {
-          float xc[V], gc[V];
-          VT::unpack(VT::ld(xp + (m - a0) * xst), xc);
-          VT::unpack(VT::ld(gq + (m - a0) * gst), gc);
+          float2 xc[H], gc[H];
+          VT::unpack2(VT::ld(xp + (m - a0) * xst), xc);
+          VT::unpack2(VT::ld(gq + (m - a0) * gst), gc);
           const bool own = m < e;
 #pragma unroll
-          for (int c = 0; c < V; ++c) {
-            float p = b[c];
-            p = fmaf(w[c][0], X[0][c], p);
-            p = fmaf(w[c][1], X[1][c], p);
-            p = fmaf(w[c][2], X[2][c], p);
-            p = fmaf(w[c][3], xc[c], p);
-            gp[c] = gc[c] * act_grad<ACT>(p);
+          for (int h = 0; h < H; ++h) {
+            float2 p = b[h];
+            p = ffma2(w[h][0], X[0][h], p);
+            p = ffma2(w[h][1], X[1][h], p);
+            p = ffma2(w[h][2], X[2][h], p);
+            p = ffma2(w[h][3], xc[h], p);
+            gp[h] = fmul2(gc[h], act_grad2<ACT>(p));
             if (own) {
-              aw[c][0] = fmaf(gp[c], X[0][c], aw[c][0]);
-              aw[c][1] = fmaf(gp[c], X[1][c], aw[c][1]);
-              aw[c][2] = fmaf(gp[c], X[2][c], aw[c][2]);
-              aw[c][3] = fmaf(gp[c], xc[c], aw[c][3]);
-              ab[c] += gp[c];
+              aw[h][0] = ffma2(gp[h], X[0][h], aw[h][0]);
+              aw[h][1] = ffma2(gp[h], X[1][h], aw[h][1]);
+              aw[h][2] = ffma2(gp[h], X[2][h], aw[h][2]);
+              aw[h][3] = ffma2(gp[h], xc[h], aw[h][3]);
+              ab[h] = fadd2(ab[h], gp[h]);
             }
-            X[0][c] = X[1][c];
-            X[1][c] = X[2][c];
-            X[2][c] = xc[c];
+            X[0][h] = X[1][h];
+            X[1][h] = X[2][h];
+            X[2][h] = xc[h];
           }
         } else {
 #pragma unroll
-          for (int c = 0; c < V; ++c) gp[c] = 0.0f;
+          for (int h = 0; h < H; ++h) gp[h] = splat2(0.0f);
         }
 #pragma unroll
-        for (int c = 0; c < V; ++c) {
-          float sacc = w[c][0] * gp[c];
-          sacc = fmaf(w[c][1], G[2][c], sacc);
-          sacc = fmaf(w[c][2], G[1][c], sacc);
-          sacc = fmaf(w[c][3], G[0][c], sacc);
-          v[c] = sacc;
-          G[0][c] = G[1][c];
-          G[1][c] = G[2][c];
-          G[2][c] = gp[c];
+        for (int h = 0; h < H; ++h) {
+          float2 acc = fmul2(w[h][0], gp[h]);
+          acc = ffma2(w[h][1], G[2][h], acc);
+          acc = ffma2(w[h][2], G[1][h], acc);
+          acc = ffma2(w[h][3], G[0][h], acc);
+          v[h] = acc;
+          G[0][h] = G[1][h];
+          G[1][h] = G[2][h];
+          G[2][h] = gp[h];
         }
         const int64_t j = m - kState;
         if (j >= a0 || starts) {
           if (a.dfin && j >= hi - kState) {
             const int64_t i = j - (hi - kState);
 #pragma unroll
-            for (int c = 0; c < V; ++c)
-              v[c] += bf16_to_f32(__ldg(a.dfin + (state_row + c) * kState + i));
+            for (int h = 0; h < H; ++h) {
+              v[h].x += bf16_to_f32(__ldg(a.dfin + (state_row + 2 * h) * kState + i));
+              v[h].y += bf16_to_f32(__ldg(a.dfin + (state_row + 2 * h + 1) * kState + i));
+            }
           }
           if (j >= lo) {
-            VT::st(dp + (j - a0) * dst, VT::pack(v));
+            VT::st(dp + (j - a0) * dst, VT::pack2(v));
           } else if (a.dinit) {  // one of the three entries before the sequence
             const int64_t i = j - lo + kState;
 #pragma unroll
-            for (int c = 0; c < V; ++c) a.dinit[(state_row + c) * kState + i] = f32_to_bf16(v[c]);
+            for (int h = 0; h < H; ++h) {
+              a.dinit[(state_row + 2 * h) * kState + i] = f32_to_bf16(v[h].x);
+              a.dinit[(state_row + 2 * h + 1) * kState + i] = f32_to_bf16(v[h].y);
+            }
           }
         }
       };
@@ -402,31 +410,31 @@ __global__ void __launch_bounds__(kBwdThreads, V == 8 ? CCC_BWD_MIN_BLOCKS : 4)
       auto fast = [&](auto phase, typename VT::Raw xr, typename VT::Raw gr, uint16_t* drow) {
         constexpr int J = decltype(phase)::value;
         constexpr int J1 = (J + 1) % 3, J2 = (J + 2) % 3;
-        float xc[V], gc[V], v[V];
-        VT::unpack(xr, xc);
-        VT::unpack(gr, gc);
+        float2 xc[H], gc[H], v[H];
+        VT::unpack2(xr, xc);
+        VT::unpack2(gr, gc);
 #pragma unroll
-        for (int c = 0; c < V; ++c) {
-          float p = b[c];
-          p = fmaf(w[c][0], X[J][c], p);
-          p = fmaf(w[c][1], X[J1][c], p);
-          p = fmaf(w[c][2], X[J2][c], p);
-          p = fmaf(w[c][3], xc[c], p);
-          const float gp = gc[c] * act_grad<ACT>(p);
-          aw[c][0] = fmaf(gp, X[J][c], aw[c][0]);
-          aw[c][1] = fmaf(gp, X[J1][c], aw[c][1]);
-          aw[c][2] = fmaf(gp, X[J2][c], aw[c][2]);
-          aw[c][3] = fmaf(gp, xc[c], aw[c][3]);
-          ab[c] += gp;
-          X[J][c] = xc[c];
-          float sacc = w[c][0] * gp;
-          sacc = fmaf(w[c][1], G[J2][c], sacc);
-          sacc = fmaf(w[c][2], G[J1][c], sacc);
-          sacc = fmaf(w[c][3], G[J][c], sacc);
-          v[c] = sacc;
-          G[J][c] = gp;
+        for (int h = 0; h < H; ++h) {
+          float2 p = b[h];
+          p = ffma2(w[h][0], X[J][h], p);
+          p = ffma2(w[h][1], X[J1][h], p);
+          p = ffma2(w[h][2], X[J2][h], p);
+          p = ffma2(w[h][3], xc[h], p);
+          const float2 gp = fmul2(gc[h], act_grad2<ACT>(p));
+          aw[h][0] = ffma2(gp, X[J][h], aw[h][0]);
+          aw[h][1] = ffma2(gp, X[J1][h], aw[h][1]);
+          aw[h][2] = ffma2(gp, X[J2][h], aw[h][2]);
+          aw[h][3] = ffma2(gp, xc[h], aw[h][3]);
+          ab[h] = fadd2(ab[h], gp);
+          X[J][h] = xc[h];
+          float2 acc = fmul2(w[h][0], gp);
+          acc = ffma2(w[h][1], G[J2][h], acc);
+          acc = ffma2(w[h][2], G[J1][h], acc);
+          acc = ffma2(w[h][3], G[J][h], acc);
+          v[h] = acc;
+          G[J][h] = gp;
         }
-        VT::st(drow, VT::pack(v));
+        VT::st(drow, VT::pack2(v));
       };
 
       int64_t m = a0;
@@ -435,12 +443,13 @@ __global__ void __launch_bounds__(kBwdThreads, V == 8 ? CCC_BWD_MIN_BLOCKS : 4)
       for (; m + 3 <= e; m += 3) {
         const uint16_t* xm = xp + (m - a0) * xst;
         const uint16_t* gm = gq + (m - a0) * gst;
+        if constexpr (kBwdPrefetch > 0) {
 #pragma unroll
-        for (int u = 0; u < 3; ++u) {
-          const int64_t t = m + kBwdPrefetch + u;
-          if (t < r_end) {
-            prefetch_l2(xm + (kBwdPrefetch + u) * xst);
-            prefetch_l2(gm + (kBwdPrefetch + u) * gst);
+          for (int u = 0; u < 3; ++u) {
+            if (m + kBwdPrefetch + u < r_end) {
+              prefetch_l2(xm + (kBwdPrefetch + u) * xst);
+              prefetch_l2(gm + (kBwdPrefetch + u) * gst);
+            }
           }
         }
         typename VT::Raw xr0 = VT::ld(xm), xr1 = VT::ld(xm + xst), xr2 = VT::ld(xm + 2 * xst);
@@ -456,7 +465,15 @@ __global__ void __launch_bounds__(kBwdThreads, V == 8 ? CCC_BWD_MIN_BLOCKS : 4)
       ++n;
     }
   }
-  block_wgrad_out<V>(a, d0, active, aw, ab);
+  float awf[V][kWidth], abf[V];
+#pragma unroll
+  for (int h = 0; h < H; ++h) {
+#pragma unroll
+    for (int k = 0; k < kWidth; ++k) { awf[2 * h][k] = aw[h][k].x; awf[2 * h + 1][k] = aw[h][k].y; }
+    abf[2 * h] = ab[h].x;
+    abf[2 * h + 1] = ab[h].y;
+  }
+  block_wgrad_out<V>(a, d0, active, awf, abf);
 }
 
 // Time-contiguous layout: one warp per (batch, channel) row, lane l walks
@@ -499,13 +516,23 @@ __global__ void __launch_bounds__(256) bwd_bdt_kernel(BwdArgs a) {
   }
 }
 
-// dweight/dbias from the FP32 sums: rows r = 0 .. R-1 added in that order.
+// dweight/dbias from the FP32 sums: rows r = 0 .. R-1 added in that order
+// (loads issued eight rows at a time; the additions keep the row order).
 __global__ void wgrad_finalize_kernel(const float* ws, int64_t R, int D, WgradOut o) {
   const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= int64_t(D) * (kWidth + 1)) return;
   const int d = int(i / (kWidth + 1)), k = int(i % (kWidth + 1));
+  const int64_t stride = int64_t(D) * (kWidth + 1);
   float s = 0.0f;
-  for (int64_t r = 0; r < R; ++r) s += ws[r * D * (kWidth + 1) + i];
+  int64_t r = 0;
+  for (; r + 8 <= R; r += 8) {
+    float v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = __ldcg(ws + (r + j) * stride + i);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) s += v[j];
+  }
+  for (; r < R; ++r) s += __ldcg(ws + r * stride + i);
   if (k < kWidth) {
     const int64_t off = d * o.dw_sd + k * o.dw_sk;
     if (o.dw_f32) static_cast<float*>(o.dw)[off] = s;

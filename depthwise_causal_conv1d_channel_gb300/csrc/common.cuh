@@ -68,6 +68,47 @@ __device__ __forceinline__ float act_grad(float p) {
   }
 }
 
+// ---- channel pairs ---------------------------------------------------------------
+//
+// The vector kernels compute on pairs of adjacent channels held in a float2,
+// with the paired FP32 instructions of sm_100+ (one instruction, two
+// independent IEEE operations, each rounded exactly like its scalar form).
+
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 splat2(float v) { return make_float2(v, v); }
+
+// BF16 pair (one 32-bit word, low half first) <-> float2.
+__device__ __forceinline__ float2 unpack_bf16x2(uint32_t u) { return make_float2(bf16_lo(u), bf16_hi(u)); }
+__device__ __forceinline__ uint32_t pack_bf16x2(float2 v) { return pack_bf16x2(v.x, v.y); }
+
+// silu on a pair; same operations, in the same order, as act_fwd.
+template <int ACT>
+__device__ __forceinline__ float2 act_fwd2(float2 p) {
+  if constexpr (ACT == kActSilu) {
+    const float2 h = fmul2(p, splat2(0.5f));
+    const float2 t = make_float2(tanh_approx(h.x), tanh_approx(h.y));
+    return fmul2(p, ffma2(t, splat2(0.5f), splat2(0.5f)));
+  } else {
+    return p;
+  }
+}
+
+// silu' on a pair; same operations, in the same order, as act_grad.
+template <int ACT>
+__device__ __forceinline__ float2 act_grad2(float2 p) {
+  if constexpr (ACT == kActSilu) {
+    const float2 h = fmul2(p, splat2(0.5f));
+    const float2 t = make_float2(tanh_approx(h.x), tanh_approx(h.y));
+    const float2 s = ffma2(t, splat2(0.5f), splat2(0.5f));
+    const float2 one_minus_s = fadd2(splat2(1.0f), make_float2(-s.x, -s.y));
+    return fmul2(s, ffma2(p, one_minus_s, splat2(1.0f)));
+  } else {
+    return splat2(1.0f);
+  }
+}
+
 // ---- vectors of V consecutive channels ---------------------------------------
 
 template <int V>
@@ -92,6 +133,13 @@ struct Vec<8> {
     return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
                       pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
   }
+  __device__ __forceinline__ static void unpack2(Raw r, float2 (&f)[4]) {
+    f[0] = unpack_bf16x2(r.x); f[1] = unpack_bf16x2(r.y);
+    f[2] = unpack_bf16x2(r.z); f[3] = unpack_bf16x2(r.w);
+  }
+  __device__ __forceinline__ static Raw pack2(const float2 (&f)[4]) {
+    return make_uint4(pack_bf16x2(f[0]), pack_bf16x2(f[1]), pack_bf16x2(f[2]), pack_bf16x2(f[3]));
+  }
 };
 
 template <>
@@ -109,6 +157,12 @@ struct Vec<4> {
   }
   __device__ __forceinline__ static Raw pack(const float (&f)[4]) {
     return make_uint2(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]));
+  }
+  __device__ __forceinline__ static void unpack2(Raw r, float2 (&f)[2]) {
+    f[0] = unpack_bf16x2(r.x); f[1] = unpack_bf16x2(r.y);
+  }
+  __device__ __forceinline__ static Raw pack2(const float2 (&f)[2]) {
+    return make_uint2(pack_bf16x2(f[0]), pack_bf16x2(f[1]));
   }
 };
 
@@ -173,6 +227,27 @@ __device__ __forceinline__ void store_state(uint16_t* s, const float (&win)[kSta
 #pragma unroll
       for (int i = 0; i < kState; ++i) s[c * 3 + i] = f32_to_bf16(win[i][c]);
   }
+}
+
+// Pair forms: win[i][h] = (state(2h, i), state(2h+1, i)).
+template <int V>
+__device__ __forceinline__ void load_state2(const uint16_t* s, float2 (&win)[kState][V / 2]) {
+  float f[kState][V];
+  load_state<V>(s, f);
+#pragma unroll
+  for (int i = 0; i < kState; ++i)
+#pragma unroll
+    for (int h = 0; h < V / 2; ++h) win[i][h] = make_float2(f[i][2 * h], f[i][2 * h + 1]);
+}
+
+template <int V>
+__device__ __forceinline__ void store_state2(uint16_t* s, const float2 (&win)[kState][V / 2]) {
+  float f[kState][V];
+#pragma unroll
+  for (int i = 0; i < kState; ++i)
+#pragma unroll
+    for (int h = 0; h < V / 2; ++h) { f[i][2 * h] = win[i][h].x; f[i][2 * h + 1] = win[i][h].y; }
+  store_state<V>(s, f);
 }
 
 // ---- weights -----------------------------------------------------------------
@@ -254,6 +329,27 @@ __device__ __forceinline__ void weights_from_smem(const float* ws, int n, int i0
   }
 }
 
+// Pair form: w[h][k] = (w[2h, k], w[2h+1, k]), b[h] likewise.
+template <int V>
+__device__ __forceinline__ void weights_from_smem2(const float* ws, int n, int i0,
+                                                   float2 (&w)[V / 2][kWidth], float2 (&b)[V / 2]) {
+  static_assert(V % 4 == 0, "pairs are read four channels at a time");
+#pragma unroll
+  for (int k = 0; k <= kWidth; ++k) {
+#pragma unroll
+    for (int c = 0; c < V; c += 4) {
+      const float4 v = *reinterpret_cast<const float4*>(ws + k * n + i0 + c);
+      if (k < kWidth) {
+        w[c / 2][k] = make_float2(v.x, v.y);
+        w[c / 2 + 1][k] = make_float2(v.z, v.w);
+      } else {
+        b[c / 2] = make_float2(v.x, v.y);
+        b[c / 2 + 1] = make_float2(v.z, v.w);
+      }
+    }
+  }
+}
+
 // Weights of one channel straight from global memory (warp-uniform channel:
 // every lane reads the same addresses).
 __device__ __forceinline__ void load_weights_1(const WeightRef& r, int64_t d, float (&w)[1][kWidth],
@@ -325,6 +421,23 @@ __device__ __forceinline__ bool block_rejects_cu_seqlens(const Seqs& s, int* sta
   bad = __syncthreads_or(bad);
   if (bad && tid == 0 && status) atomicCAS(status, 0, kStatusBadCuSeqlens);
   return bad != 0;
+}
+
+// Before a block stages its weights, each thread prefetches into L2 the first
+// rows it will read -- rows [first - back, first + ahead) of the sequence that
+// holds token `first`, clipped to that sequence -- so the two latencies overlap.
+// Row t of sequence n (tokens [lo, hi)) sits at base + n * seq_step + t * st
+// (dense: seq_step = batch stride - T * token stride; packed: 0).
+__device__ __forceinline__ void prefetch_first_rows(const Seqs& s, const uint16_t* base,
+                                                    int64_t seq_step, int64_t st, int64_t first,
+                                                    int back, int ahead) {
+  if (first >= s.Q) return;
+  const int n = find_seq(s, first);
+  int64_t lo, hi;
+  seq_bounds(s, n, lo, hi);
+  const int64_t t0 = first - back > lo ? first - back : lo;
+  const int64_t t1 = first + ahead < hi ? first + ahead : hi;
+  for (int64_t t = t0; t < t1; ++t) prefetch_l2(base + n * seq_step + t * st);
 }
 
 // Element offsets of token q of sequence n in an activation tensor, for the

@@ -126,7 +126,8 @@ __global__ void __launch_bounds__(256) fwd_cl_kernel(FwdArgs a) {
   fwd_walk<V, ACT, 4, (V == 8 ? 16 : 0)>(a, a.seqs, xs, os, 0, d0, w, b, q0, q1);
 }
 
-// Channel-last x with vectors of V = 8 or 4 channels (the fast path).  Same
+// Channel-last x with vectors of V = 4 channels, computed as two channel
+// pairs (the fast path; eight channels a thread measured no faster).  Same
 // walk as fwd_walk, specialised: the three-token window lives in three register
 // slots that rotate (the newest token overwrites the oldest slot), so steady
 // state runs in groups of three tokens with no register copies; x and out are
@@ -139,21 +140,29 @@ constexpr int kFwdGroup = 6;                 // tokens per steady-state step (mu
 constexpr int kFwdPrefetch = CCC_FWD_PREFETCH;  // tokens of L2 prefetch distance
 
 template <int V, int ACT>
-__global__ void __launch_bounds__(256, V == 8 ? 2 : 3) fwd_clv_kernel(FwdArgs a) {
+__global__ void __launch_bounds__(256, 3) fwd_clv_kernel(FwdArgs a) {
   using VT = Vec<V>;
+  constexpr int H = V / 2;  // channel pairs
   __shared__ __align__(16) float ws[(kWidth + 1) * kMaxBlockChannels];
   if (block_rejects_cu_seqlens(a.seqs, a.status)) return;
   const int n_blk = blockDim.x * V;
-  stage_weights(a.wr, blockIdx.x * n_blk, n_blk, a.D, ws);
   const int d0 = (blockIdx.x * blockDim.x + threadIdx.x) * V;
   const int64_t seg = int64_t(blockIdx.y) * blockDim.y + threadIdx.y;
+  const bool dense0 = a.seqs.cu == nullptr;
+  if (d0 < a.D && seg < a.n_seg)
+    prefetch_first_rows(a.seqs, a.x + d0, dense0 ? a.x_sb - a.seqs.T * a.x_st : 0, a.x_st,
+                        seg * a.seg_len, kState, kFwdGroup);
+  stage_weights(a.wr, blockIdx.x * n_blk, n_blk, a.D, ws);
   if (d0 >= a.D || seg >= a.n_seg) return;
-  float w[V][kWidth], b[V];
-  weights_from_smem<V>(ws, n_blk, threadIdx.x * V, w, b);
+  float2 w[H][kWidth], b[H];
+  weights_from_smem2<V>(ws, n_blk, threadIdx.x * V, w, b);
   int64_t q = seg * a.seg_len;
   const int64_t q_end = q + a.seg_len < a.seqs.Q ? q + a.seg_len : a.seqs.Q;
   const bool dense = a.seqs.cu == nullptr;
   int n = find_seq(a.seqs, q);
+  using P0 = std::integral_constant<int, 0>;
+  using P1 = std::integral_constant<int, 1>;
+  using P2 = std::integral_constant<int, 2>;
   while (q < q_end) {
     int64_t lo, hi;
     seq_bounds(a.seqs, n, lo, hi);
@@ -165,60 +174,61 @@ __global__ void __launch_bounds__(256, V == 8 ? 2 : 3) fwd_clv_kernel(FwdArgs a)
     const int64_t xst = a.x_st, ost = a.o_st;
 
     // W[j] = xe[q - 3 + j]
-    float W[kState][V];
+    float2 W[kState][H];
     {
-      float init[kState][V];
+      float2 init[kState][H];
       if (q - kState < lo && a.init) {
-        load_state<V>(a.init + state_row * kState, init);
+        load_state2<V>(a.init + state_row * kState, init);
       } else {
 #pragma unroll
         for (int i = 0; i < kState; ++i)
 #pragma unroll
-          for (int c = 0; c < V; ++c) init[i][c] = 0.0f;
+          for (int h = 0; h < H; ++h) init[i][h] = splat2(0.0f);
       }
 #pragma unroll
       for (int j = 0; j < kState; ++j) {
         const int64_t tok = q - kState + j;
         if (tok >= lo) {
-          VT::unpack(VT::ld(xp - (kState - j) * xst), W[j]);
+          VT::unpack2(VT::ld(xp - (kState - j) * xst), W[j]);
         } else {
           const int64_t i = tok - lo + kState;
 #pragma unroll
-          for (int c = 0; c < V; ++c)
-            W[j][c] = i == 0 ? init[0][c] : (i == 1 ? init[1][c] : init[2][c]);
+          for (int h = 0; h < H; ++h)
+            W[j][h] = i == 0 ? init[0][h] : (i == 1 ? init[1][h] : init[2][h]);
         }
       }
     }
-    for (int64_t t = kFwdGroup; t < kFwdGroup + kFwdPrefetch && q + t < e; ++t)
-      prefetch_l2(xp + t * xst);
+    if constexpr (kFwdPrefetch > 0) {
+      for (int64_t t = kFwdGroup; t < kFwdGroup + kFwdPrefetch && q + t < e; ++t)
+        prefetch_l2(xp + t * xst);
+    }
 
     // one token at window phase J: taps W[J], W[J+1], W[J+2] (mod 3), then the
     // new token replaces W[J]
     auto step = [&](auto phase, typename VT::Raw raw, uint16_t* dst) {
       constexpr int J = decltype(phase)::value;
-      float cur[V], y[V];
-      VT::unpack(raw, cur);
+      float2 cur[H], y[H];
+      VT::unpack2(raw, cur);
 #pragma unroll
-      for (int c = 0; c < V; ++c) {
-        float p = b[c];
-        p = fmaf(w[c][0], W[J][c], p);
-        p = fmaf(w[c][1], W[(J + 1) % 3][c], p);
-        p = fmaf(w[c][2], W[(J + 2) % 3][c], p);
-        p = fmaf(w[c][3], cur[c], p);
-        y[c] = act_fwd<ACT>(p);
-        W[J][c] = cur[c];
+      for (int h = 0; h < H; ++h) {
+        float2 p = b[h];
+        p = ffma2(w[h][0], W[J][h], p);
+        p = ffma2(w[h][1], W[(J + 1) % 3][h], p);
+        p = ffma2(w[h][2], W[(J + 2) % 3][h], p);
+        p = ffma2(w[h][3], cur[h], p);
+        y[h] = act_fwd2<ACT>(p);
+        W[J][h] = cur[h];
       }
-      VT::st(dst, VT::pack(y));
+      VT::st(dst, VT::pack2(y));
     };
-    using P0 = std::integral_constant<int, 0>;
-    using P1 = std::integral_constant<int, 1>;
-    using P2 = std::integral_constant<int, 2>;
 
     for (; q + kFwdGroup <= e; q += kFwdGroup) {
+      if constexpr (kFwdPrefetch > 0) {
 #pragma unroll
-      for (int u = 0; u < kFwdGroup; ++u) {
-        const int64_t t = kFwdGroup + kFwdPrefetch + u;
-        if (q + t < e) prefetch_l2(xp + t * xst);
+        for (int u = 0; u < kFwdGroup; ++u) {
+          const int64_t t = kFwdGroup + kFwdPrefetch + u;
+          if (q + t < e) prefetch_l2(xp + t * xst);
+        }
       }
       typename VT::Raw r[kFwdGroup];
 #pragma unroll
@@ -234,25 +244,25 @@ __global__ void __launch_bounds__(256, V == 8 ? 2 : 3) fwd_clv_kernel(FwdArgs a)
     }
     // remainder: physical shift keeps the window at phase 0
     for (; q < e; ++q) {
-      float cur[V], y[V];
-      VT::unpack(VT::ld(xp), cur);
+      float2 cur[H], y[H];
+      VT::unpack2(VT::ld(xp), cur);
 #pragma unroll
-      for (int c = 0; c < V; ++c) {
-        float p = b[c];
-        p = fmaf(w[c][0], W[0][c], p);
-        p = fmaf(w[c][1], W[1][c], p);
-        p = fmaf(w[c][2], W[2][c], p);
-        p = fmaf(w[c][3], cur[c], p);
-        y[c] = act_fwd<ACT>(p);
-        W[0][c] = W[1][c];
-        W[1][c] = W[2][c];
-        W[2][c] = cur[c];
+      for (int h = 0; h < H; ++h) {
+        float2 p = b[h];
+        p = ffma2(w[h][0], W[0][h], p);
+        p = ffma2(w[h][1], W[1][h], p);
+        p = ffma2(w[h][2], W[2][h], p);
+        p = ffma2(w[h][3], cur[h], p);
+        y[h] = act_fwd2<ACT>(p);
+        W[0][h] = W[1][h];
+        W[1][h] = W[2][h];
+        W[2][h] = cur[h];
       }
-      VT::st(op, VT::pack(y));
+      VT::st(op, VT::pack2(y));
       xp += xst;
       op += ost;
     }
-    if (e == hi && a.fin) store_state<V>(a.fin + state_row * kState, W);
+    if (e == hi && a.fin) store_state2<V>(a.fin + state_row * kState, W);
     ++n;
   }
 }
@@ -291,15 +301,14 @@ __global__ void fwd_empty_kernel(const uint16_t* init, uint16_t* fin, int64_t n)
 // ---- host launchers ------------------------------------------------------------
 
 int fwd_blocks_per_sm(int vec) {
-  static std::atomic<int> cache[3];
-  const int i = vec == 8 ? 0 : vec == 4 ? 1 : 2;
+  static std::atomic<int> cache[2];
+  const int i = vec == 4 ? 0 : 1;
   int v = cache[i].load(std::memory_order_relaxed);
   if (v == 0) {
     int n = 0;
     const cudaError_t err =
-        vec == 8   ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fwd_clv_kernel<8, kActSilu>, 256, 0)
-        : vec == 4 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fwd_clv_kernel<4, kActSilu>, 256, 0)
-                   : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fwd_cl_kernel<1, kActSilu>, 256, 0);
+        vec == 4 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fwd_clv_kernel<4, kActSilu>, 256, 0)
+                 : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fwd_cl_kernel<1, kActSilu>, 256, 0);
     v = (err == cudaSuccess && n > 0) ? n : 1;
     cache[i].store(v, std::memory_order_relaxed);
   }
@@ -310,8 +319,7 @@ template <int ACT>
 static cudaError_t launch_fwd_act(const FwdArgs& a, const FwdPlan& p, cudaStream_t stream) {
   if (p.kind == kLayoutChannelLast) {
     dim3 block(p.tx, p.ty), grid(p.gx, p.gy);
-    if (p.vec == 8) fwd_clv_kernel<8, ACT><<<grid, block, 0, stream>>>(a);
-    else if (p.vec == 4) fwd_clv_kernel<4, ACT><<<grid, block, 0, stream>>>(a);
+    if (p.vec == 4) fwd_clv_kernel<4, ACT><<<grid, block, 0, stream>>>(a);
     else fwd_cl_kernel<1, ACT><<<grid, block, 0, stream>>>(a);
   } else {
     fwd_bdt_kernel<ACT><<<p.gx, 256, 0, stream>>>(a);

@@ -24,6 +24,14 @@ struct FwdArgs {
   int* status;
 };
 
+struct WgradOut {
+  void* dw;          // [D, 4] BF16 or FP32
+  int dw_f32;
+  int64_t dw_sd, dw_sk;
+  uint16_t* db;      // [D] BF16 or nullptr
+  int64_t db_sd;
+};
+
 struct BwdArgs {
   const uint16_t* x;
   const uint16_t* g;   // dL/dout
@@ -42,6 +50,7 @@ struct BwdArgs {
   int deterministic;      // 1: block row r writes ws[r]; 0: atomics into ws[0]
   int* status;
 };
+
 
 // Launch shape of one call, chosen on the host from the sizes and the SM count.
 struct FwdPlan {
@@ -64,13 +73,6 @@ struct UpdArgs {
   int B, D;
 };
 
-struct WgradOut {
-  void* dw;          // [D, 4] BF16 or FP32
-  int dw_f32;
-  int64_t dw_sd, dw_sk;
-  uint16_t* db;      // [D] BF16 or nullptr
-  int64_t db_sd;
-};
 
 FwdPlan plan_fwd(int kind, int vec_ok, int64_t Q, int D, int64_t rows, int sm_count);
 BwdPlan plan_bwd(int kind, int vec_ok, int64_t Q, int D, int64_t rows, int sm_count);

@@ -24,40 +24,78 @@ __global__ void __launch_bounds__(256) update_kernel(UpdArgs a) {
   const int d0 = (blockIdx.x * blockDim.x + threadIdx.x) * V;
   const int b0 = (blockIdx.y * blockDim.y + threadIdx.y) * R;
   if (d0 >= a.D || b0 >= a.B) return;
-  float w[V][kWidth], b[V];
-  weights_from_smem<V>(ws, n_blk, threadIdx.x * V, w, b);
-  float win[R][kState][V];
-  typename VT::Raw xr[R];
+  if constexpr (V >= 4) {
+    constexpr int H = V / 2;  // channel pairs, same arithmetic as the forward
+    float2 w[H][kWidth], b[H];
+    weights_from_smem2<V>(ws, n_blk, threadIdx.x * V, w, b);
+    float2 win[R][kState][H];
+    typename VT::Raw xr[R];
 #pragma unroll
-  for (int r = 0; r < R; ++r) {
-    if (b0 + r < a.B) {
-      load_state<V>(a.state + (int64_t(b0 + r) * a.D + d0) * kState, win[r]);
-      xr[r] = VT::ld(a.x + int64_t(b0 + r) * a.x_sb + d0);
+    for (int r = 0; r < R; ++r) {
+      if (b0 + r < a.B) {
+        load_state2<V>(a.state + (int64_t(b0 + r) * a.D + d0) * kState, win[r]);
+        xr[r] = VT::ld(a.x + int64_t(b0 + r) * a.x_sb + d0);
+      }
     }
-  }
 #pragma unroll
-  for (int r = 0; r < R; ++r) {
-    if (b0 + r >= a.B) break;
-    float xc[V], y[V];
-    VT::unpack(xr[r], xc);
+    for (int r = 0; r < R; ++r) {
+      if (b0 + r >= a.B) break;
+      float2 xc[H], y[H];
+      VT::unpack2(xr[r], xc);
 #pragma unroll
-    for (int c = 0; c < V; ++c) {
-      float p = b[c];
-      p = fmaf(w[c][0], win[r][0][c], p);
-      p = fmaf(w[c][1], win[r][1][c], p);
-      p = fmaf(w[c][2], win[r][2][c], p);
-      p = fmaf(w[c][3], xc[c], p);
-      y[c] = act_fwd<ACT>(p);
-      win[r][0][c] = win[r][1][c];
-      win[r][1][c] = win[r][2][c];
-      win[r][2][c] = xc[c];
+      for (int h = 0; h < H; ++h) {
+        float2 p = b[h];
+        p = ffma2(w[h][0], win[r][0][h], p);
+        p = ffma2(w[h][1], win[r][1][h], p);
+        p = ffma2(w[h][2], win[r][2][h], p);
+        p = ffma2(w[h][3], xc[h], p);
+        y[h] = act_fwd2<ACT>(p);
+        win[r][0][h] = win[r][1][h];
+        win[r][1][h] = win[r][2][h];
+        win[r][2][h] = xc[h];
+      }
+      VT::st(a.out + int64_t(b0 + r) * a.o_sb + d0, VT::pack2(y));
+      store_state2<V>(a.state + (int64_t(b0 + r) * a.D + d0) * kState, win[r]);
     }
-    VT::st(a.out + int64_t(b0 + r) * a.o_sb + d0, VT::pack(y));
-    store_state<V>(a.state + (int64_t(b0 + r) * a.D + d0) * kState, win[r]);
+  } else {
+    float w[V][kWidth], b[V];
+    weights_from_smem<V>(ws, n_blk, threadIdx.x * V, w, b);
+    float win[R][kState][V];
+    typename VT::Raw xr[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      if (b0 + r < a.B) {
+        load_state<V>(a.state + (int64_t(b0 + r) * a.D + d0) * kState, win[r]);
+        xr[r] = VT::ld(a.x + int64_t(b0 + r) * a.x_sb + d0);
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      if (b0 + r >= a.B) break;
+      float xc[V], y[V];
+      VT::unpack(xr[r], xc);
+#pragma unroll
+      for (int c = 0; c < V; ++c) {
+        float p = b[c];
+        p = fmaf(w[c][0], win[r][0][c], p);
+        p = fmaf(w[c][1], win[r][1][c], p);
+        p = fmaf(w[c][2], win[r][2][c], p);
+        p = fmaf(w[c][3], xc[c], p);
+        y[c] = act_fwd<ACT>(p);
+        win[r][0][c] = win[r][1][c];
+        win[r][1][c] = win[r][2][c];
+        win[r][2][c] = xc[c];
+      }
+      VT::st(a.out + int64_t(b0 + r) * a.o_sb + d0, VT::pack(y));
+      store_state<V>(a.state + (int64_t(b0 + r) * a.D + d0) * kState, win[r]);
+    }
   }
 }
 
-constexpr int kUpdateRows = 2;
+#ifndef CCC_UPDATE_ROWS
+#define CCC_UPDATE_ROWS 2
+#endif
+constexpr int kUpdateRows = CCC_UPDATE_ROWS;
 
 cudaError_t launch_update(const UpdArgs& a, int vec, int act, cudaStream_t stream) {
   if (a.B == 0) return cudaSuccess;
@@ -71,6 +109,9 @@ cudaError_t launch_update(const UpdArgs& a, int vec, int act, cudaStream_t strea
   if (vec == 8) {
     if (act == kActSilu) update_kernel<8, kActSilu, kUpdateRows><<<grid, block, 0, stream>>>(a);
     else update_kernel<8, kActNone, kUpdateRows><<<grid, block, 0, stream>>>(a);
+  } else if (vec == 4) {
+    if (act == kActSilu) update_kernel<4, kActSilu, kUpdateRows><<<grid, block, 0, stream>>>(a);
+    else update_kernel<4, kActNone, kUpdateRows><<<grid, block, 0, stream>>>(a);
   } else {
     if (act == kActSilu) update_kernel<1, kActSilu, kUpdateRows><<<grid, block, 0, stream>>>(a);
     else update_kernel<1, kActNone, kUpdateRows><<<grid, block, 0, stream>>>(a);

@@ -270,3 +270,24 @@ def test_use_deterministic_algorithms_flag(cuda_device):
         check_bwd(nb, gpu_run(nb, cuda_device))
     finally:
         torch.use_deterministic_algorithms(prev, warn_only=prev_warn)
+
+
+def test_long_packed_many_short_sequences(cuda_device):
+    """Enough tokens per thread that the backward takes its 8-channel path, with
+    thousands of sequence boundaries (lengths 1..6), initial states and a
+    final-state gradient; a sample of whole channels against the oracle."""
+    rng = np.random.default_rng(21)
+    lengths = rng.integers(1, 7, size=220_000).tolist()
+    T = int(sum(lengths))
+    inp = make_inputs(1, 64, T, seed=22, lengths=lengths, initial_states=True, grad=True,
+                      dfinal_states=True, bias=False, weight_dtype=torch.float32)
+    res = gpu_run(inp, cuda_device, deterministic=True)
+    ch = [0, 5, 31, 32, 63]
+    idx = torch.tensor(ch)
+    rf = oracle_fwd(inp, ch)
+    rb = oracle_bwd(inp, ch)
+    assert_bf16_close(bits(res["out"][:, idx]), rf["out"], "out")
+    assert_bits_equal(bits(res["final"][:, idx]), rf["final"], "final")
+    assert_bf16_close(bits(res["dx"][:, idx]), rb["dx"], "dx")
+    assert_bf16_close(bits(res["dinit"][:, idx]), rb["dinit"], "dinit")
+    assert_wgrad_close(tensor_values(res["dw"][idx]), rb["dw64"], rb["dw_abs"], False, "dweight")
