@@ -41,9 +41,14 @@ UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 2 ** 20
 
-# DRAM traffic of the dominant kernel from an ncu capture, per launch, valid
-# only for the kernel sources whose digest is recorded with it.
-TRAFFIC = {"sources_sha256": None, "bytes_per_launch": None}
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the dominant
+# call -- the backward on the dense_state workload: backward kernel plus the
+# finalize kernel -- from one ncu --set full capture (profiles/kernels_dense_state.md),
+# per launch.  Valid only for the kernel sources whose digest is recorded here.
+# The capture flushes caches before each launch; the 25 MB dx written to L2 is
+# mostly not yet written back when the kernel ends, so writes are undercounted.
+TRAFFIC = {"sources_sha256": "e6bb931435158de7da723d54aeb325ea4b5e947afc2d4adc39c86ac5d12d184c",
+           "bytes_per_launch": 50452736 + 1045504 + 40448}
 
 
 def kernel_sources_digest() -> str:
@@ -197,9 +202,9 @@ class DenseStep:
         self.bwd_bytes = bwd_bytes(d.x, self.w, self.b, self.init, self.dfin, self.dinit)
         self.tokens = inp.tokens if inp.cu_seqlens is None else d.x.shape[2]
         self.launches_fwd = 1
-        # backward kernel (+ the fixed-order finalize kernel in deterministic mode),
-        # after a memset node
-        self.launches_bwd = 2 if deterministic else 1
+        # backward kernel + the fixed-order finalize kernel (after a memset node in
+        # atomic mode)
+        self.launches_bwd = 2
 
     def fwd(self, i, stream):
         k = i % self.sets
@@ -428,6 +433,16 @@ def oracle_step_seconds(inp, min_seconds=10.0, max_reps=20, channels=None):
 
 # ---- main ---------------------------------------------------------------------------
 
+def reduce_max(value: float, device) -> float:
+    """Max of a per-rank number over all ranks (the job's time is the slowest
+    rank's)."""
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -467,6 +482,45 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+PROFILE_WORKLOADS = ("dense_small", "dense_state", "packed_varlen", "decode_update",
+                     "dense_large_bias", "dense_large_det")
+
+
+def run_profile(name: str, calls: int):
+    """A few eager calls of one workload's kernels and nothing else, for an ncu
+    launch list or capture: forward + backward (or the update)."""
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    from depthwise_causal_conv1d_channel_gb300 import _abi
+
+    stream = torch.cuda.current_stream(device)
+    if name == "decode_update":
+        wl = workloads.decode_update(steps=calls)
+        st = wl.conv_state.to(device)
+        w, b = wl.weight.to(device), wl.bias.to(device)
+        out = torch.empty(st.shape[0], st.shape[1], dtype=torch.bfloat16, device=device)
+        for i in range(calls):
+            assert _abi.ccc_conv1d_update(wl.x_seq[i].to(device), st, w, b, out,
+                                          _abi.CCC_ACT_SILU, stream) == 0
+    else:
+        if name == "dense_small":
+            inp = workloads.dense_small()
+        elif name == "dense_state":
+            inp = workloads.dense_state()
+        elif name == "packed_varlen":
+            inp = workloads.packed_varlen()
+        else:
+            inp = workloads.dense_large(bias=name == "dense_large_bias")
+        step = DenseStep(inp, device, deterministic=inp.deterministic, sets=1)
+        for i in range(calls):
+            step.fwd(0, stream)
+            if step.g[0] is not None:
+                step.bwd(0, stream)
+        step.check_status(stream)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile": name, "calls": calls}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -475,7 +529,12 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-breakdown", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", choices=PROFILE_WORKLOADS,
+                    help="run only a few eager calls of this workload (for ncu) and exit")
+    ap.add_argument("--calls", type=int, default=3)
     args = ap.parse_args()
+    if args.profile:
+        return run_profile(args.profile, args.calls)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
@@ -508,9 +567,7 @@ def main():
 
     ms_step = total_ms / args.steps
     if pg is not None:
-        t = torch.tensor([ms_step], device=device)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms_step = float(t.item())
+        ms_step = reduce_max(ms_step, device)
     step_bytes = step.fwd_bytes + step.bwd_bytes
     value = world * step_bytes / (ms_step * 1e-3) / 1e9
     tokens_per_s = world * step.tokens / (ms_step * 1e-3)
