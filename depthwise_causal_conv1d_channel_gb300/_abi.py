@@ -25,6 +25,7 @@ CCC_ERR_NONDETERMINISTIC = 4
 CCC_ERR_WORKSPACE = 5
 CCC_ERR_CUDA = 6
 CCC_ERR_BAD_CU_SEQLENS = 7
+CCC_ERR_SCRATCH_LIMIT = 8
 
 CCC_BF16, CCC_F32, CCC_I32 = 0, 1, 2
 CCC_ACT_NONE, CCC_ACT_SILU = 0, 1
@@ -35,6 +36,7 @@ EXPORTED = (
     "ccc_conv1d_fwd",
     "ccc_conv1d_bwd_workspace_size",
     "ccc_conv1d_bwd",
+    "ccc_conv1d_bwd_noalloc",
     "ccc_conv1d_update",
     "ccc_read_status",
     "ccc_status_string",
@@ -78,6 +80,8 @@ def _load():
     lib.ccc_conv1d_bwd_workspace_size.restype = ctypes.c_size_t
     lib.ccc_conv1d_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, P, I, I, V, ctypes.c_size_t, V, V]
     lib.ccc_conv1d_bwd.restype = I
+    lib.ccc_conv1d_bwd_noalloc.argtypes = [P, P, P, P, P, P, P, P, P, P, P, I, I, V, V]
+    lib.ccc_conv1d_bwd_noalloc.restype = I
     lib.ccc_conv1d_update.argtypes = [P, P, P, P, P, I, V]
     lib.ccc_conv1d_update.restype = I
     lib.ccc_read_status.argtypes = [V, V]
@@ -162,6 +166,18 @@ def ccc_conv1d_bwd(x, weight, bias, cu_seqlens, initial_states, dout, dfinal_sta
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     return lib.ccc_conv1d_bwd(*[_ref(d) for d in ds], int(activation), int(bool(deterministic)),
                               ws_ptr, ws_bytes, _status_ptr(status), _stream(stream))
+
+
+def ccc_conv1d_bwd_noalloc(x, weight, bias, cu_seqlens, initial_states, dout, dfinal_states,
+                           dx, dweight, dbias, dinitial_states, activation: int,
+                           deterministic: bool, status=None, stream=None) -> int:
+    """ccc_conv1d_bwd with the library's built-in scratch instead of a workspace
+    (for callers that cannot allocate device memory)."""
+    ds = [desc(t) for t in (x, weight, bias, cu_seqlens, initial_states, dout, dfinal_states,
+                            dx, dweight, dbias, dinitial_states)]
+    return lib.ccc_conv1d_bwd_noalloc(*[_ref(d) for d in ds], int(activation),
+                                      int(bool(deterministic)), _status_ptr(status),
+                                      _stream(stream))
 
 
 def ccc_conv1d_update(x, conv_state, weight, bias, out, activation: int, stream=None) -> int:

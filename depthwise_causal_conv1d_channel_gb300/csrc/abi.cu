@@ -305,6 +305,7 @@ const char* ccc_status_string(int status) {
     case CCC_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
     case CCC_ERR_CUDA: return "CUDA error";
     case CCC_ERR_BAD_CU_SEQLENS: return "malformed cu_seqlens";
+    case CCC_ERR_SCRATCH_LIMIT: return "problem exceeds the built-in scratch of ccc_conv1d_bwd_noalloc";
     default: return "unknown status";
   }
 }

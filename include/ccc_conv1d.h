@@ -2,8 +2,10 @@
  * ccc_conv1d -- depthwise causal conv1d on BF16 activations, width four.
  *
  * C ABI of the CUDA library (libccc_conv1d.so).  All tensor memory is owned by
- * the caller; the library allocates nothing and keeps no mutable global state,
- * so calls on different streams may run concurrently (on disjoint outputs).
+ * the caller and the library allocates nothing.  Its only global state is a
+ * cache of per-device launch limits and the built-in scratch array of
+ * ccc_conv1d_bwd_noalloc; every other call may run concurrently with others on
+ * different streams (on disjoint outputs).
  *
  * The operation (cuDNN frontend docs, "Causal Conv1d" page):
  *
@@ -54,7 +56,9 @@ typedef enum {
     CCC_ERR_NONDETERMINISTIC = 4, /* deterministic backward requested with a bias */
     CCC_ERR_WORKSPACE = 5,        /* workspace NULL, too small or not 16-byte aligned */
     CCC_ERR_CUDA = 6,             /* a CUDA runtime call or launch failed */
-    CCC_ERR_BAD_CU_SEQLENS = 7    /* device-detected malformed cu_seqlens (via d_status) */
+    CCC_ERR_BAD_CU_SEQLENS = 7,   /* device-detected malformed cu_seqlens (via d_status) */
+    CCC_ERR_SCRATCH_LIMIT = 8     /* ccc_conv1d_bwd_noalloc: the problem needs more scratch
+                                     than CCC_CONV1D_NOALLOC_SCRATCH_BYTES */
 } ccc_status;
 
 typedef enum { CCC_BF16 = 0, CCC_F32 = 1, CCC_I32 = 2 } ccc_dtype;
@@ -141,6 +145,40 @@ ccc_status ccc_conv1d_bwd(const ccc_tensor *x, const ccc_tensor *weight, const c
                           const ccc_tensor *dinitial_states, int activation, int deterministic,
                           void *workspace, size_t workspace_bytes, int *d_status,
                           cudaStream_t stream);
+
+/*
+ * Backward without any allocation -- no counterpart in the pages; it exists for
+ * callers that cannot allocate device memory.  Such callers are programs
+ * embedded in a host that owns all device memory and forbids allocation while
+ * it runs (a server with a fixed memory budget, a plugin interface that hands
+ * over only the operation's own tensors): they cannot provide the workspace
+ * ccc_conv1d_bwd asks for.
+ *
+ * Same arguments and results as ccc_conv1d_bwd, minus the workspace: the FP32
+ * sums live in a scratch array of CCC_CONV1D_NOALLOC_SCRATCH_BYTES built into
+ * the library, present in device memory on every GPU that loads it, until the
+ * library is unloaded.  Nothing is allocated (no cudaMalloc, no cudaFree, no
+ * allocating library routine).
+ *
+ *   - The first call on a device, with that device current, looks up the
+ *     array's device address (cudaGetSymbolAddress); make that first call
+ *     before any stream capture.
+ *   - A problem whose workspace (ccc_conv1d_bwd_workspace_size) exceeds the
+ *     scratch returns CCC_ERR_SCRATCH_LIMIT and enqueues nothing.
+ *   - All calls on a device share the array.  Calls whose work overlaps on
+ *     the GPU (different streams at once) race on it; calls on one stream are
+ *     ordered.  Each call zeroes or overwrites what it reads, so an earlier
+ *     call's contents never leak into a result.
+ */
+#define CCC_CONV1D_NOALLOC_SCRATCH_BYTES ((size_t)4 << 20)
+
+ccc_status ccc_conv1d_bwd_noalloc(const ccc_tensor *x, const ccc_tensor *weight,
+                                  const ccc_tensor *bias, const ccc_tensor *cu_seqlens,
+                                  const ccc_tensor *initial_states, const ccc_tensor *dout,
+                                  const ccc_tensor *dfinal_states, const ccc_tensor *dx,
+                                  const ccc_tensor *dweight, const ccc_tensor *dbias,
+                                  const ccc_tensor *dinitial_states, int activation,
+                                  int deterministic, int *d_status, cudaStream_t stream);
 
 /*
  * Single-token update (cuDNN "Causal Conv1d" page, the paragraph on passing
