@@ -219,6 +219,9 @@ ccc::WeightRef weight_ref(const ccc_tensor* weight, const ccc_tensor* bias) {
   r.w_sk = weight->stride[1];
   r.bias = bias ? static_cast<const uint16_t*>(bias->data) : nullptr;
   r.b_sd = bias ? bias->stride[0] : 0;
+  const int64_t D = weight->shape[0];
+  r.w_vec = (D <= 1 || r.w_sd == kWidth) && r.w_sk == 1 && aligned16(weight->data) &&
+            (!bias || ((D <= 1 || r.b_sd == 1) && aligned16(bias->data)));
   return r;
 }
 

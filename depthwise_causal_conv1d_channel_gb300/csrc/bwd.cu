@@ -275,7 +275,7 @@ __global__ void __launch_bounds__(kBwdThreads, V == 8 ? CCC_BWD_MIN_BLOCKS : 4)
   const int d0 = (blockIdx.x * blockDim.x + threadIdx.x) * V;
   const int64_t seg = int64_t(blockIdx.y) * blockDim.y + threadIdx.y;
   const bool active = d0 < a.D && seg < a.n_seg;
-  stage_weights(a.wr, blockIdx.x * n_blk, n_blk, a.D, wsm);
+  if (!a.wr.w_vec) stage_weights(a.wr, blockIdx.x * n_blk, n_blk, a.D, wsm);  // block-uniform
   float2 aw[H][kWidth], ab[H];
 #pragma unroll
   for (int h = 0; h < H; ++h) {
@@ -285,7 +285,8 @@ __global__ void __launch_bounds__(kBwdThreads, V == 8 ? CCC_BWD_MIN_BLOCKS : 4)
   }
   if (active) {
     float2 w[H][kWidth], b[H];
-    weights_from_smem2<V>(wsm, n_blk, threadIdx.x * V, w, b);
+    if (a.wr.w_vec) weights_direct2<V>(a.wr, d0, w, b);
+    else weights_from_smem2<V>(wsm, n_blk, threadIdx.x * V, w, b);
     int64_t q = seg * a.seg_len;
     const int64_t q_end = q + a.seg_len < a.seqs.Q ? q + a.seg_len : a.seqs.Q;
     const bool dense = a.seqs.cu == nullptr;

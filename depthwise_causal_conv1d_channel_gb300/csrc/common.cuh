@@ -258,6 +258,7 @@ struct WeightRef {
   int64_t w_sd, w_sk;
   const uint16_t* bias;  // [D] BF16 or nullptr
   int64_t b_sd;
+  int w_vec;        // contiguous [D, 4] and bias, 16-byte aligned: read with vectors
 };
 
 // Widest channel slice a block stages: 32 threads x 8 channels.
@@ -347,6 +348,55 @@ __device__ __forceinline__ void weights_from_smem2(const float* ws, int n, int i
         b[c / 2 + 1] = make_float2(v.z, v.w);
       }
     }
+  }
+}
+
+// Pair form read by each thread straight from global memory, for a contiguous
+// [D, 4] weight (and contiguous bias) aligned to 16 bytes: a thread's V
+// channels are 8V (BF16) or 16V (FP32) consecutive bytes, so a handful of
+// 16-byte loads replace the block-wide staging (no barrier, and the loads
+// overlap the first activation loads).
+template <int V>
+__device__ __forceinline__ void weights_direct2(const WeightRef& r, int d0,
+                                                float2 (&w)[V / 2][kWidth], float2 (&b)[V / 2]) {
+  static_assert(V % 4 == 0, "vector weights need four channels at a time");
+  if (r.w_f32) {
+    const float4* p = static_cast<const float4*>(r.w) + d0;  // one float4 per channel
+    float4 c[V];
+#pragma unroll
+    for (int i = 0; i < V; ++i) c[i] = __ldg(p + i);
+#pragma unroll
+    for (int h = 0; h < V / 2; ++h) {
+      w[h][0] = make_float2(c[2 * h].x, c[2 * h + 1].x);
+      w[h][1] = make_float2(c[2 * h].y, c[2 * h + 1].y);
+      w[h][2] = make_float2(c[2 * h].z, c[2 * h + 1].z);
+      w[h][3] = make_float2(c[2 * h].w, c[2 * h + 1].w);
+    }
+  } else {
+    const uint4* p = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(r.w) + int64_t(d0) * kWidth);
+    uint4 q[V / 2];  // two channels (8 BF16) per uint4
+#pragma unroll
+    for (int i = 0; i < V / 2; ++i) q[i] = __ldg(p + i);
+#pragma unroll
+    for (int h = 0; h < V / 2; ++h) {  // q[h] = channel 2h taps 0..3, channel 2h+1 taps 0..3
+      w[h][0] = make_float2(bf16_lo(q[h].x), bf16_lo(q[h].z));
+      w[h][1] = make_float2(bf16_hi(q[h].x), bf16_hi(q[h].z));
+      w[h][2] = make_float2(bf16_lo(q[h].y), bf16_lo(q[h].w));
+      w[h][3] = make_float2(bf16_hi(q[h].y), bf16_hi(q[h].w));
+    }
+  }
+  if (r.bias) {
+    if constexpr (V == 8) {
+      const uint4 u = __ldg(reinterpret_cast<const uint4*>(r.bias + d0));
+      b[0] = unpack_bf16x2(u.x); b[1] = unpack_bf16x2(u.y);
+      b[2] = unpack_bf16x2(u.z); b[3] = unpack_bf16x2(u.w);
+    } else {
+      const uint2 u = __ldg(reinterpret_cast<const uint2*>(r.bias + d0));
+      b[0] = unpack_bf16x2(u.x); b[1] = unpack_bf16x2(u.y);
+    }
+  } else {
+#pragma unroll
+    for (int h = 0; h < V / 2; ++h) b[h] = splat2(0.0f);
   }
 }
 

@@ -152,10 +152,11 @@ __global__ void __launch_bounds__(256, 3) fwd_clv_kernel(FwdArgs a) {
   if (d0 < a.D && seg < a.n_seg)
     prefetch_first_rows(a.seqs, a.x + d0, dense0 ? a.x_sb - a.seqs.T * a.x_st : 0, a.x_st,
                         seg * a.seg_len, kState, kFwdGroup);
-  stage_weights(a.wr, blockIdx.x * n_blk, n_blk, a.D, ws);
+  if (!a.wr.w_vec) stage_weights(a.wr, blockIdx.x * n_blk, n_blk, a.D, ws);  // block-uniform
   if (d0 >= a.D || seg >= a.n_seg) return;
   float2 w[H][kWidth], b[H];
-  weights_from_smem2<V>(ws, n_blk, threadIdx.x * V, w, b);
+  if (a.wr.w_vec) weights_direct2<V>(a.wr, d0, w, b);
+  else weights_from_smem2<V>(ws, n_blk, threadIdx.x * V, w, b);
   int64_t q = seg * a.seg_len;
   const int64_t q_end = q + a.seg_len < a.seqs.Q ? q + a.seg_len : a.seqs.Q;
   const bool dense = a.seqs.cu == nullptr;

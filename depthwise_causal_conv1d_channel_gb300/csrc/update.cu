@@ -20,14 +20,16 @@ __global__ void __launch_bounds__(256) update_kernel(UpdArgs a) {
   using VT = Vec<V>;
   __shared__ __align__(16) float ws[(kWidth + 1) * kMaxBlockChannels];
   const int n_blk = blockDim.x * V;
-  stage_weights(a.wr, blockIdx.x * n_blk, n_blk, a.D, ws);
+  const bool vec_w = V >= 4 && a.wr.w_vec;
+  if (!vec_w) stage_weights(a.wr, blockIdx.x * n_blk, n_blk, a.D, ws);  // block-uniform
   const int d0 = (blockIdx.x * blockDim.x + threadIdx.x) * V;
   const int b0 = (blockIdx.y * blockDim.y + threadIdx.y) * R;
   if (d0 >= a.D || b0 >= a.B) return;
   if constexpr (V >= 4) {
     constexpr int H = V / 2;  // channel pairs, same arithmetic as the forward
     float2 w[H][kWidth], b[H];
-    weights_from_smem2<V>(ws, n_blk, threadIdx.x * V, w, b);
+    if (vec_w) weights_direct2<V>(a.wr, d0, w, b);
+    else weights_from_smem2<V>(ws, n_blk, threadIdx.x * V, w, b);
     float2 win[R][kState][H];
     typename VT::Raw xr[R];
 #pragma unroll

@@ -291,3 +291,37 @@ def test_long_packed_many_short_sequences(cuda_device):
     assert_bf16_close(bits(res["dx"][:, idx]), rb["dx"], "dx")
     assert_bf16_close(bits(res["dinit"][:, idx]), rb["dinit"], "dinit")
     assert_wgrad_close(tensor_values(res["dw"][idx]), rb["dw64"], rb["dw_abs"], False, "dweight")
+
+
+@pytest.mark.parametrize("wdtype", [torch.bfloat16, torch.float32])
+def test_strided_weight_and_bias(wdtype, cuda_device):
+    """Weight stored transposed ([4, D] memory seen as [D, 4]) and a strided bias:
+    the kernels stage them through shared memory instead of vector loads."""
+    B, D, T = 2, 136, 90
+    inp = make_inputs(B, D, T, seed=41, initial_states=True, grad=True, weight_dtype=wdtype,
+                      bias=wdtype == torch.bfloat16)
+    d = inp.to(cuda_device)
+    w_t = d.weight.t().contiguous().t()                          # strides (1, D)
+    assert w_t.stride() == (1, D)
+    b_s = None
+    if d.bias is not None:
+        b_s = torch.zeros(2 * D, dtype=d.bias.dtype, device=cuda_device)[::2]
+        b_s.copy_(d.bias)
+    x = d.x.detach().requires_grad_(True)
+    w = w_t.detach().requires_grad_(True)
+    out, fin = ccc.causal_conv1d(x, w, b_s, initial_states=d.initial_states,
+                                 return_final_states=True)
+    out.backward(d.g)
+    ccc.check_status(cuda_device)
+    ref = oracle_fwd(inp)
+    assert_bf16_close(bits(out.detach().cpu()), ref["out"], "out")
+    assert_bits_equal(bits(fin.cpu()), ref["final"], "final")
+    rb = oracle_bwd(inp)
+    assert_bf16_close(bits(x.grad.cpu()), rb["dx"], "dx")
+    assert_wgrad_close(tensor_values(w.grad), rb["dw64"], rb["dw_abs"], wdtype == torch.bfloat16,
+                       "dweight")
+    st = torch.empty(B, D, 3, dtype=torch.bfloat16, device=cuda_device).copy_(d.initial_states)
+    xt = d.x[:, :, 0].contiguous()
+    u = ccc.causal_conv1d_update(xt, st, w_t, b_s)
+    ru = oracle.update(bits(xt), bits(inp.initial_states), bits(inp.weight), bits(inp.bias))
+    assert_bf16_close(bits(u.cpu()), ru["out"], "update out")
