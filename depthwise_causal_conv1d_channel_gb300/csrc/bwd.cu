@@ -191,6 +191,7 @@ __device__ __forceinline__ void block_wgrad_out(const BwdArgs& a, int d0, bool a
                                                 const float (&aw)[V][kWidth], const float (&ab)[V]) {
   extern __shared__ float red[];  // [ty][tx][V * 5]
   constexpr int P = V * (kWidth + 1);
+  pdl_wait();  // atomic mode: the accumulator is zeroed by the kernel before this one
   float* mine = red + (threadIdx.y * blockDim.x + threadIdx.x) * P;
 #pragma unroll
   for (int c = 0; c < V; ++c) {
@@ -245,6 +246,7 @@ __global__ void __launch_bounds__(256) bwd_cl_kernel(BwdArgs a) {
     const Stream ds{d0, dense ? a.dx_sb - a.seqs.T * a.dx_st : 0, a.dx_st};
     bwd_walk<V, ACT, 4, (V == 8 ? 16 : 0)>(a, a.seqs, xs, gs, ds, 0, d0, w, b, q0, q1, aw, ab);
   }
+  pdl_release();
   block_wgrad_out<V>(a, d0, active, aw, ab);
 }
 
@@ -474,6 +476,7 @@ __global__ void __launch_bounds__(kBwdThreads, V == 8 ? CCC_BWD_MIN_BLOCKS : 4)
     abf[2 * h] = ab[h].x;
     abf[2 * h + 1] = ab[h].y;
   }
+  pdl_release();  // the finalize kernel may start launching
   block_wgrad_out<V>(a, d0, active, awf, abf);
 }
 
@@ -502,6 +505,8 @@ __global__ void __launch_bounds__(256) bwd_bdt_kernel(BwdArgs a) {
     const int64_t q1 = q0 + 8 < rs.Q ? q0 + 8 : rs.Q;
     bwd_walk<1, ACT, 4, 0>(a, rs, xs, gs, ds, dense ? bb : 0, d, w, b, q0, q1, aw, ab);
   }
+  pdl_release();
+  pdl_wait();  // atomic mode: the accumulator is zeroed by the kernel before this one
   float v[kWidth + 1] = {aw[0][0], aw[0][1], aw[0][2], aw[0][3], ab[0]};
 #pragma unroll
   for (int k = 0; k < kWidth + 1; ++k)
@@ -520,6 +525,7 @@ __global__ void __launch_bounds__(256) bwd_bdt_kernel(BwdArgs a) {
 // dweight/dbias from the FP32 sums: rows r = 0 .. R-1 added in that order
 // (loads issued eight rows at a time; the additions keep the row order).
 __global__ void wgrad_finalize_kernel(const float* ws, int64_t R, int D, WgradOut o) {
+  pdl_wait();  // the backward kernel's sums
   const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= int64_t(D) * (kWidth + 1)) return;
   const int d = int(i / (kWidth + 1)), k = int(i % (kWidth + 1));
@@ -541,6 +547,16 @@ __global__ void wgrad_finalize_kernel(const float* ws, int64_t R, int D, WgradOu
   } else if (o.db) {
     o.db[d * o.db_sd] = f32_to_bf16(s);
   }
+}
+
+// Zeroes the FP32 accumulator of the atomic mode.  Launched the ordinary way,
+// it starts only once all earlier work in the stream has completed; it then
+// releases the backward kernel (launched as its programmatic dependent), which
+// may read its inputs at once and waits for this kernel only before its atomics.
+__global__ void zero_acc_kernel(float* p, int64_t n) {
+  pdl_release();
+  const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i < n) p[i] = 0.0f;
 }
 
 // T == 0: dinit = dfinal (the final state is the initial state), or zero.
@@ -572,38 +588,49 @@ int bwd_blocks_per_sm(int vec) {
 }
 
 template <int ACT>
-static void launch_bwd_act(const BwdArgs& a, const BwdPlan& p, cudaStream_t stream) {
+static cudaError_t launch_bwd_act(const BwdArgs& a, const BwdPlan& p, bool pdl,
+                                  cudaStream_t stream) {
   if (p.kind == kLayoutChannelLast) {
     dim3 block(p.tx, p.ty), grid(p.gx, p.gy);
     const size_t smem = size_t(p.tx) * p.ty * p.vec * (kWidth + 1) * sizeof(float);
-    if (p.vec == 8) bwd_clv_kernel<8, ACT><<<grid, block, smem, stream>>>(a);
-    else if (p.vec == 4) bwd_clv_kernel<4, ACT><<<grid, block, smem, stream>>>(a);
-    else bwd_cl_kernel<1, ACT><<<grid, block, smem, stream>>>(a);
-  } else {
-    bwd_bdt_kernel<ACT><<<p.gx, 256, 0, stream>>>(a);
+    if (p.vec == 8) return launch_kernel(bwd_clv_kernel<8, ACT>, grid, block, smem, stream, pdl, a);
+    if (p.vec == 4) return launch_kernel(bwd_clv_kernel<4, ACT>, grid, block, smem, stream, pdl, a);
+    return launch_kernel(bwd_cl_kernel<1, ACT>, grid, block, smem, stream, pdl, a);
   }
+  return launch_kernel(bwd_bdt_kernel<ACT>, dim3(p.gx), dim3(256), 0, stream, pdl, a);
 }
 
+// Atomic mode: zero_acc_kernel, then the backward as its programmatic
+// dependent (overlapping the zeroing and its own launch), then the finalize as
+// the backward's dependent.  Deterministic mode: the backward launched the
+// ordinary way (nothing to zero; it reads inputs before any wait), then the
+// finalize.
 cudaError_t launch_bwd(const BwdArgs& a, const BwdPlan& p, int act, const WgradOut& o,
                        int64_t partial_rows, cudaStream_t stream) {
-  const size_t acc_bytes = size_t(a.D) * (kWidth + 1) * sizeof(float);
+  const int64_t n_acc = int64_t(a.D) * (kWidth + 1);
   const bool empty = a.seqs.Q == 0;
-  if (!a.deterministic || empty) {
-    cudaError_t err = cudaMemsetAsync(a.ws, 0, acc_bytes, stream);
-    if (err != cudaSuccess) return err;
-  }
+  cudaError_t err = cudaSuccess;
   if (empty) {
+    err = cudaMemsetAsync(a.ws, 0, size_t(n_acc) * sizeof(float), stream);
+    if (err != cudaSuccess) return err;
     const int64_t n = int64_t(a.seqs.n_seq) * a.D * kState;
     if (a.dinit && n > 0)
       bwd_empty_kernel<<<unsigned((n + 255) / 256), 256, 0, stream>>>(a.dfin, a.dinit, n);
-  } else if (act == kActSilu) {
-    launch_bwd_act<kActSilu>(a, p, stream);
   } else {
-    launch_bwd_act<kActNone>(a, p, stream);
+    if (!a.deterministic) {
+      zero_acc_kernel<<<unsigned((n_acc + 255) / 256), 256, 0, stream>>>(a.ws, n_acc);
+      err = cudaGetLastError();
+      if (err != cudaSuccess) return err;
+    }
+    const bool pdl = !a.deterministic;
+    err = act == kActSilu ? launch_bwd_act<kActSilu>(a, p, pdl, stream)
+                          : launch_bwd_act<kActNone>(a, p, pdl, stream);
+    if (err != cudaSuccess) return err;
   }
   const int64_t R = (a.deterministic && !empty) ? partial_rows : 1;
-  const int64_t n_out = int64_t(a.D) * (kWidth + 1);
-  wgrad_finalize_kernel<<<unsigned((n_out + 255) / 256), 256, 0, stream>>>(a.ws, R, a.D, o);
+  err = launch_kernel(wgrad_finalize_kernel, dim3(unsigned((n_acc + 255) / 256)), dim3(256), 0,
+                      stream, true, static_cast<const float*>(a.ws), R, a.D, o);
+  if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
 

@@ -18,6 +18,19 @@ constexpr int kState = 3;  // W - 1
 
 constexpr int kStatusBadCuSeqlens = 7;  // == CCC_ERR_BAD_CU_SEQLENS
 
+// ---- programmatic dependent launch -------------------------------------------
+//
+// Kernels launched with programmatic stream serialization (launch_kernel with
+// pdl = true) may start while the previous kernel in the stream is finishing.
+// pdl_wait() blocks until that kernel has completed and its writes are
+// visible, so it must precede any read of memory another kernel may have
+// written; pdl_release() lets the next such kernel start launching.  Both are
+// no-ops for a kernel launched the ordinary way.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_release() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- BF16 <-> FP32 ---------------------------------------------------------
 
 __device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }

@@ -109,6 +109,8 @@ __device__ __forceinline__ void fwd_walk(const FwdArgs& a, const Seqs& seqs, con
 // per token.
 template <int V, int ACT>
 __global__ void __launch_bounds__(256) fwd_cl_kernel(FwdArgs a) {
+  pdl_wait();     // inputs may come from the previous kernel in the stream
+  pdl_release();
   __shared__ __align__(16) float ws[(kWidth + 1) * kMaxBlockChannels];
   if (block_rejects_cu_seqlens(a.seqs, a.status)) return;
   const int n_blk = blockDim.x * V;
@@ -141,6 +143,8 @@ constexpr int kFwdPrefetch = CCC_FWD_PREFETCH;  // tokens of L2 prefetch distanc
 
 template <int V, int ACT>
 __global__ void __launch_bounds__(256, 3) fwd_clv_kernel(FwdArgs a) {
+  pdl_wait();     // inputs may come from the previous kernel in the stream
+  pdl_release();
   using VT = Vec<V>;
   constexpr int H = V / 2;  // channel pairs
   __shared__ __align__(16) float ws[(kWidth + 1) * kMaxBlockChannels];
@@ -272,6 +276,8 @@ __global__ void __launch_bounds__(256, 3) fwd_clv_kernel(FwdArgs a) {
 // lane l walks tokens [8l + 256i, 8l + 256i + 8).
 template <int ACT>
 __global__ void __launch_bounds__(256) fwd_bdt_kernel(FwdArgs a) {
+  pdl_wait();     // inputs may come from the previous kernel in the stream
+  pdl_release();
   if (block_rejects_cu_seqlens(a.seqs, a.status)) return;
   const int lane = threadIdx.x & 31;
   const int64_t row = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -320,12 +326,10 @@ template <int ACT>
 static cudaError_t launch_fwd_act(const FwdArgs& a, const FwdPlan& p, cudaStream_t stream) {
   if (p.kind == kLayoutChannelLast) {
     dim3 block(p.tx, p.ty), grid(p.gx, p.gy);
-    if (p.vec == 4) fwd_clv_kernel<4, ACT><<<grid, block, 0, stream>>>(a);
-    else fwd_cl_kernel<1, ACT><<<grid, block, 0, stream>>>(a);
-  } else {
-    fwd_bdt_kernel<ACT><<<p.gx, 256, 0, stream>>>(a);
+    if (p.vec == 4) return launch_kernel(fwd_clv_kernel<4, ACT>, grid, block, 0, stream, true, a);
+    return launch_kernel(fwd_cl_kernel<1, ACT>, grid, block, 0, stream, true, a);
   }
-  return cudaGetLastError();
+  return launch_kernel(fwd_bdt_kernel<ACT>, dim3(p.gx), dim3(256), 0, stream, true, a);
 }
 
 cudaError_t launch_fwd(const FwdArgs& a, const FwdPlan& p, int act, cudaStream_t stream) {

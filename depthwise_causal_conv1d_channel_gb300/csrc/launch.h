@@ -8,6 +8,25 @@
 
 namespace ccc {
 
+// Launch `kernel`; with pdl, as a programmatic dependent of the previous
+// kernel in the stream (it may begin before that kernel ends and must call
+// pdl_wait() before reading memory that kernel could have written).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t stream, bool pdl, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = pdl ? attr : nullptr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 enum Layout { kLayoutChannelLast = 0, kLayoutTimeContiguous = 1 };
 
 struct FwdArgs {

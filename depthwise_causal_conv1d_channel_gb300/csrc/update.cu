@@ -17,6 +17,8 @@ namespace ccc {
 // thread issues the loads of all its R rows before computing any of them.
 template <int V, int ACT, int R>
 __global__ void __launch_bounds__(256) update_kernel(UpdArgs a) {
+  pdl_wait();     // the state and x may come from the previous kernel (the previous step)
+  pdl_release();
   using VT = Vec<V>;
   __shared__ __align__(16) float ws[(kWidth + 1) * kMaxBlockChannels];
   const int n_blk = blockDim.x * V;
@@ -108,17 +110,14 @@ cudaError_t launch_update(const UpdArgs& a, int vec, int act, cudaStream_t strea
   dim3 block(tx, ty);
   dim3 grid(unsigned((groups + tx - 1) / tx),
             unsigned((a.B + int64_t(ty) * kUpdateRows - 1) / (int64_t(ty) * kUpdateRows)));
-  if (vec == 8) {
-    if (act == kActSilu) update_kernel<8, kActSilu, kUpdateRows><<<grid, block, 0, stream>>>(a);
-    else update_kernel<8, kActNone, kUpdateRows><<<grid, block, 0, stream>>>(a);
-  } else if (vec == 4) {
-    if (act == kActSilu) update_kernel<4, kActSilu, kUpdateRows><<<grid, block, 0, stream>>>(a);
-    else update_kernel<4, kActNone, kUpdateRows><<<grid, block, 0, stream>>>(a);
-  } else {
-    if (act == kActSilu) update_kernel<1, kActSilu, kUpdateRows><<<grid, block, 0, stream>>>(a);
-    else update_kernel<1, kActNone, kUpdateRows><<<grid, block, 0, stream>>>(a);
-  }
-  return cudaGetLastError();
+  if (vec == 8)
+    return act == kActSilu ? launch_kernel(update_kernel<8, kActSilu, kUpdateRows>, grid, block, 0, stream, true, a)
+                           : launch_kernel(update_kernel<8, kActNone, kUpdateRows>, grid, block, 0, stream, true, a);
+  if (vec == 4)
+    return act == kActSilu ? launch_kernel(update_kernel<4, kActSilu, kUpdateRows>, grid, block, 0, stream, true, a)
+                           : launch_kernel(update_kernel<4, kActNone, kUpdateRows>, grid, block, 0, stream, true, a);
+  return act == kActSilu ? launch_kernel(update_kernel<1, kActSilu, kUpdateRows>, grid, block, 0, stream, true, a)
+                         : launch_kernel(update_kernel<1, kActNone, kUpdateRows>, grid, block, 0, stream, true, a);
 }
 
 }  // namespace ccc
