@@ -5,8 +5,10 @@
 //   out[b,d]   = act(bias[d] + w0*s0 + w1*s1 + w2*s2 + w3*x[b,d])
 //   state[b,d] = [s1, s2, x[b,d]]      (bitwise)
 //
-// A thread owns V consecutive channels of R batch rows: per row one 16-byte
-// load of x, three of the state, one 16-byte store of out, three of the state.
+// A thread owns V consecutive channels of one or more batch rows.  With eight
+// channels and a contiguous weight, each warp moves the state of its 256
+// channels as one coalesced run (update_w8_kernel); otherwise each thread
+// reads and writes its own channels' state directly (update_kernel).
 #include "common.cuh"
 #include "launch.h"
 
@@ -96,6 +98,111 @@ __global__ void __launch_bounds__(256) update_kernel(UpdArgs a) {
   }
 }
 
+// Eight-channel groups with a contiguous [D, 4] weight.  Block (32, TY): each
+// warp owns 32 consecutive groups (256 channels) of R batch rows (TY = 4,
+// R = 1 measured fastest: a 256 x 4096 step is 1024 small blocks, about seven
+// per SM, all resident at once).  The state
+// of those channels in one row is a single contiguous run of 32 x 48 bytes;
+// the warp reads and writes it as three fully used 512-byte slices and passes
+// it through shared memory, where each lane takes its own 48 bytes (a
+// 48-byte lane stride puts the eight lanes of each shared-memory phase on
+// eight distinct 16-byte bank groups, so the exchange is conflict-free).
+// Read with per-lane 48-byte strides instead, every load instruction would
+// touch twice the sectors it uses.
+template <int ACT, int TY, int R>
+__global__ void __launch_bounds__(32 * TY) update_w8_kernel(UpdArgs a) {
+  pdl_wait();
+  pdl_release();
+  constexpr int kChunks = 32 * kState;  // 16-byte chunks of one warp-row of state
+  __shared__ uint4 sbuf[TY][R][kChunks];
+  const int lane = threadIdx.x, wy = threadIdx.y;
+  const int groups = a.D / 8;
+  const int g0 = blockIdx.x * 32;
+  const int n_lanes = min(32, groups - g0);
+  const int n_chunks = kState * n_lanes;
+  const bool valid = lane < n_lanes;
+  const int d0 = (g0 + lane) * 8;
+  const int b0 = (blockIdx.y * blockDim.y + wy) * R;
+  if (b0 >= a.B) return;  // the whole warp: it shares b0
+  float2 w[4][kWidth], bias[4];
+  if (valid) weights_direct2<8>(a.wr, d0, w, bias);
+  uint4 sr[R][kState], xr[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    if (b0 + r < a.B) {
+      const uint4* run = reinterpret_cast<const uint4*>(a.state + (int64_t(b0 + r) * a.D + int64_t(g0) * 8) * kState);
+#pragma unroll
+      for (int j = 0; j < kState; ++j)
+        if (lane + 32 * j < n_chunks) sr[r][j] = run[lane + 32 * j];
+      if (valid) xr[r] = Vec<8>::ld(a.x + int64_t(b0 + r) * a.x_sb + d0);
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < R; ++r)
+    if (b0 + r < a.B)
+#pragma unroll
+      for (int j = 0; j < kState; ++j)
+        if (lane + 32 * j < n_chunks) sbuf[wy][r][lane + 32 * j] = sr[r][j];
+  __syncwarp();
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    if (b0 + r >= a.B || !valid) continue;
+    union { uint4 q[kState]; uint16_t h[3 * 8]; } u;
+#pragma unroll
+    for (int j = 0; j < kState; ++j) u.q[j] = sbuf[wy][r][kState * lane + j];
+    float2 win[kState][4], xc[4], y[4];
+#pragma unroll
+    for (int i = 0; i < kState; ++i)
+#pragma unroll
+      for (int h = 0; h < 4; ++h)
+        win[i][h] = make_float2(bf16_to_f32(u.h[(2 * h) * 3 + i]), bf16_to_f32(u.h[(2 * h + 1) * 3 + i]));
+    Vec<8>::unpack2(xr[r], xc);
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      float2 p = bias[h];
+      p = ffma2(w[h][0], win[0][h], p);
+      p = ffma2(w[h][1], win[1][h], p);
+      p = ffma2(w[h][2], win[2][h], p);
+      p = ffma2(w[h][3], xc[h], p);
+      y[h] = act_fwd2<ACT>(p);
+    }
+    Vec<8>::st(a.out + int64_t(b0 + r) * a.o_sb + d0, Vec<8>::pack2(y));
+    // new state [s1, s2, x]: shift each channel's three entries down by one
+    uint16_t xh[8];
+    {
+      union { uint4 q; uint16_t h[8]; } xv;
+      xv.q = xr[r];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) xh[c] = xv.h[c];
+    }
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      u.h[c * 3 + 0] = u.h[c * 3 + 1];
+      u.h[c * 3 + 1] = u.h[c * 3 + 2];
+      u.h[c * 3 + 2] = xh[c];
+    }
+#pragma unroll
+    for (int j = 0; j < kState; ++j) sbuf[wy][r][kState * lane + j] = u.q[j];
+  }
+  __syncwarp();
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    if (b0 + r >= a.B) continue;
+    uint4* run = reinterpret_cast<uint4*>(a.state + (int64_t(b0 + r) * a.D + int64_t(g0) * 8) * kState);
+#pragma unroll
+    for (int j = 0; j < kState; ++j)
+      if (lane + 32 * j < n_chunks) run[lane + 32 * j] = sbuf[wy][r][lane + 32 * j];
+  }
+}
+
+template <int ACT>
+static cudaError_t launch_update_w8(const UpdArgs& a, cudaStream_t stream) {
+  constexpr int TY = 4, R = 1;
+  const int64_t groups = a.D / 8;
+  dim3 grid(unsigned((groups + 31) / 32), unsigned((a.B + int64_t(TY) * R - 1) / (int64_t(TY) * R)));
+  return launch_kernel(update_w8_kernel<ACT, TY, R>, grid, dim3(32, TY), 0, stream, true, a);
+}
+
 #ifndef CCC_UPDATE_ROWS
 #define CCC_UPDATE_ROWS 2
 #endif
@@ -103,6 +210,9 @@ constexpr int kUpdateRows = CCC_UPDATE_ROWS;
 
 cudaError_t launch_update(const UpdArgs& a, int vec, int act, cudaStream_t stream) {
   if (a.B == 0) return cudaSuccess;
+  if (vec == 8 && a.wr.w_vec)
+    return act == kActSilu ? launch_update_w8<kActSilu>(a, stream)
+                           : launch_update_w8<kActNone>(a, stream);
   const int64_t groups = (a.D + vec - 1) / vec;
   int tx = 1;
   while (tx < groups && tx < 32) tx <<= 1;

@@ -14,7 +14,8 @@ from workloads import bits, make_inputs
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("B,D", [(4, 264), (3, 100), (1, 8), (2, 1), (256, 64)])
+@pytest.mark.parametrize("B,D", [(4, 264), (3, 100), (1, 8), (2, 1), (256, 64), (37, 4104),
+                                 (300, 1028), (129, 4096)])
 @pytest.mark.parametrize("act", ["silu", None])
 def test_update_parity(B, D, act, cuda_device):
     gen = torch.Generator().manual_seed(B * 7 + D)
@@ -28,6 +29,27 @@ def test_update_parity(B, D, act, cuda_device):
     torch.cuda.synchronize()
     assert_bf16_close(bits(out.cpu()), ref["out"], "out")
     assert_bits_equal(bits(s_dev.cpu()), ref["state"], "state")
+
+
+def test_update_strided_rows(cuda_device):
+    """x and out rows with a stride larger than D (slices of wider buffers)."""
+    B, D = 70, 2048
+    gen = torch.Generator().manual_seed(11)
+    state = torch.randn(B, D, 3, generator=gen).to(torch.bfloat16)
+    xw = torch.randn(B, D + 64, generator=gen).to(torch.bfloat16)
+    w = (torch.rand(D, 4, generator=gen) - 0.5).to(torch.bfloat16)
+    b = ((torch.rand(D, generator=gen) - 0.5) * 0.2).to(torch.bfloat16)
+    x = xw[:, 8:8 + D]
+    ref = oracle.update(bits(x), bits(state), bits(w), bits(b))
+    s_dev = state.to(cuda_device)
+    ow = torch.zeros(B, D + 32, dtype=torch.bfloat16, device=cuda_device)
+    out = ow[:, 16:16 + D]
+    ccc.causal_conv1d_update(xw.to(cuda_device)[:, 8:8 + D], s_dev, w.to(cuda_device),
+                             b.to(cuda_device), out=out)
+    torch.cuda.synchronize()
+    assert_bf16_close(bits(out.cpu()), ref["out"], "out")
+    assert_bits_equal(bits(s_dev.cpu()), ref["state"], "state")
+    assert not ow[:, :16].any() and not ow[:, 16 + D:].any()
 
 
 def test_update_fp32_weight_no_bias(cuda_device):
