@@ -242,7 +242,7 @@ namespace ccc {
 // the token ranges are sized so the grid holds about `waves` full waves of
 // resident blocks, each range at least `min_seg` tokens long.
 static FwdPlan plan_cl(int vec, int64_t Q, int D, int sm_count, int blocks_per_sm, int waves,
-                       int64_t min_seg, int threads) {
+                       int64_t min_seg, int threads, int64_t seg_multiple = 1) {
   FwdPlan p{};
   p.kind = kLayoutChannelLast;
   p.vec = vec;
@@ -253,10 +253,11 @@ static FwdPlan plan_cl(int vec, int64_t Q, int D, int sm_count, int blocks_per_s
   const int64_t want = std::max<int64_t>(1, int64_t(sm_count) * std::max(1, blocks_per_sm) * waves);
   int64_t gy = std::max<int64_t>(1, want / p.gx);
   int64_t seg = std::max<int64_t>(min_seg, ceil_div(std::max<int64_t>(Q, 1), gy * p.ty));
+  seg = ceil_div(seg, seg_multiple) * seg_multiple;
   int64_t n_seg = ceil_div(std::max<int64_t>(Q, 1), seg);
   gy = ceil_div(n_seg, p.ty);
   if (gy > 65535) {
-    seg = ceil_div(Q, int64_t(65535) * p.ty);
+    seg = ceil_div(ceil_div(Q, int64_t(65535) * p.ty), seg_multiple) * seg_multiple;
     n_seg = ceil_div(Q, seg);
     gy = ceil_div(n_seg, p.ty);
   }
@@ -284,7 +285,9 @@ FwdPlan plan_fwd(int kind, int vec, int64_t Q, int D, int64_t rows, int sm_count
 
 BwdPlan plan_bwd(int kind, int vec, int64_t Q, int D, int64_t rows, int sm_count) {
   if (kind == kLayoutTimeContiguous) return plan_bdt(rows);
-  return plan_cl(vec, Q, D, sm_count, bwd_blocks_per_sm(vec), 1, 16, bwd_block_threads(vec));
+  // segments of a multiple of three tokens: the vector kernel's steady groups
+  // of three then cover a whole segment inside a sequence, head and tail included
+  return plan_cl(vec, Q, D, sm_count, bwd_blocks_per_sm(vec), 1, 18, bwd_block_threads(vec), 3);
 }
 
 int64_t bwd_partial_rows(const BwdPlan& p, int B, bool packed) {

@@ -95,10 +95,10 @@ __device__ __forceinline__ void bwd_walk(const BwdArgs& a, const Seqs& seqs, con
     auto emit = [&](const float (&gp)[V], float (&v)[V]) {
 #pragma unroll
       for (int c = 0; c < V; ++c) {
-        float s = w[c][0] * gp[c];
-        s = fmaf(w[c][1], gw[2][c], s);
+        float s = w[c][3] * gw[0][c];  // oldest first: gp[m] enters last
         s = fmaf(w[c][2], gw[1][c], s);
-        s = fmaf(w[c][3], gw[0][c], s);
+        s = fmaf(w[c][1], gw[2][c], s);
+        s = fmaf(w[c][0], gp[c], s);
         v[c] = s;
         gw[0][c] = gw[1][c];
         gw[1][c] = gw[2][c];
@@ -183,13 +183,22 @@ __device__ __forceinline__ void bwd_walk(const BwdArgs& a, const Seqs& seqs, con
   }
 }
 
+// Dynamic shared memory of the channel-last backward kernels: the block's
+// weight/bias sums for the final reduction ([ty][tx][V * 5] floats), then (the
+// vector kernels) each thread's ring of staged input rows.
+extern __shared__ __align__(16) float bwd_dyn_smem[];
+template <int V>
+__host__ __device__ constexpr size_t bwd_red_bytes(int threads) {
+  return size_t(threads) * V * (kWidth + 1) * sizeof(float);
+}
+
 // Block-wide sum of the per-thread weight/bias sums over threadIdx.y (threads
 // with equal threadIdx.x own the same channels), in a fixed order, then either
 // FP32 atomics into ws[0] or a store into this block row's partial ws[blockIdx.y].
 template <int V>
 __device__ __forceinline__ void block_wgrad_out(const BwdArgs& a, int d0, bool active,
                                                 const float (&aw)[V][kWidth], const float (&ab)[V]) {
-  extern __shared__ float red[];  // [ty][tx][V * 5]
+  float* red = bwd_dyn_smem;  // [ty][tx][V * 5]
   constexpr int P = V * (kWidth + 1);
   pdl_wait();  // atomic mode: the accumulator is zeroed by the kernel before this one
   float* mine = red + (threadIdx.y * blockDim.x + threadIdx.x) * P;
@@ -251,26 +260,38 @@ __global__ void __launch_bounds__(256) bwd_cl_kernel(BwdArgs a) {
 }
 
 // Channel-last backward with vectors of V = 8 or 4 channels (the fast path).
-// Same walk as bwd_walk, specialised like fwd_clv_kernel: the input window
-// and the gradient window rotate through three register slots, steady state
-// runs in groups of three tokens, rows kBwdPrefetch tokens ahead of both x and
-// grad_out are prefetched into L2.  128-thread blocks, two resident per SM
-// (the windows, weights and sums need ~200 registers a thread; a tighter
-// bound spills).
+// Same walk as bwd_walk, specialised like fwd_clv_kernel: the input window and
+// the gradient window rotate through three register slots and the own tokens
+// of a piece are taken in groups of three.  Those groups' rows (x and
+// grad_out) stream through the thread's own ring of kBwdRing stages in shared
+// memory with cp.async, kBwdRing - 1 groups ahead of the group being computed,
+// so the steady loop never waits on a load it has just issued and holds no
+// registers for loads in flight.  The ring's first group is the head (own
+// tokens whose dx rows belong to the previous piece) and its last the tail
+// (the three tokens after the piece, which emit its last dx rows); the few
+// tokens at sequence edges take the general step, their rows loaded together.
+// 128-thread blocks (two resident per SM for V = 8, four for V = 4).
 #ifndef CCC_BWD_MIN_BLOCKS
 #define CCC_BWD_MIN_BLOCKS 2
 #endif
-#ifndef CCC_BWD_PREFETCH
-#define CCC_BWD_PREFETCH 9
+#ifndef CCC_BWD_RING
+#define CCC_BWD_RING 4
 #endif
-constexpr int kBwdPrefetch = CCC_BWD_PREFETCH;
+constexpr int kBwdRing = CCC_BWD_RING;
+static_assert(kBwdRing >= 2, "the ring needs a stage being filled and one being read");
+template <int V>
+constexpr size_t bwd_ring_bytes(int threads) {
+  return size_t(threads) * kBwdRing * 3 * 2 * (2 * V);
+}
 constexpr int kBwdThreads = 128;
 
 template <int V, int ACT>
 __global__ void __launch_bounds__(kBwdThreads, V == 8 ? CCC_BWD_MIN_BLOCKS : 4)
     bwd_clv_kernel(BwdArgs a) {
   using VT = Vec<V>;
+  using Raw = typename VT::Raw;
   constexpr int H = V / 2;  // channel pairs
+  constexpr int RB = int(sizeof(Raw));
   __shared__ __align__(16) float wsm[(kWidth + 1) * kMaxBlockChannels];
   if (block_rejects_cu_seqlens(a.seqs, a.status)) return;
   const int n_blk = blockDim.x * V;
@@ -289,6 +310,15 @@ __global__ void __launch_bounds__(kBwdThreads, V == 8 ? CCC_BWD_MIN_BLOCKS : 4)
     float2 w[H][kWidth], b[H];
     if (a.wr.w_vec) weights_direct2<V>(a.wr, d0, w, b);
     else weights_from_smem2<V>(wsm, n_blk, threadIdx.x * V, w, b);
+    // this thread's ring: slot (stage, row u, tensor t) at byte
+    // (((stage * 3 + u) * 2 + t) * threads + tid) * RB past the ring base
+    const int nthr = blockDim.x * blockDim.y;
+    const int tid = threadIdx.y * blockDim.x + threadIdx.x;
+    const char* ring = reinterpret_cast<const char*>(bwd_dyn_smem) + bwd_red_bytes<V>(nthr) +
+                       size_t(tid) * RB;
+    const uint32_t ring_s = smem_u32(ring);
+    const uint32_t slot = uint32_t(nthr) * RB;
+
     int64_t q = seg * a.seg_len;
     const int64_t q_end = q + a.seg_len < a.seqs.Q ? q + a.seg_len : a.seqs.Q;
     const bool dense = a.seqs.cu == nullptr;
@@ -296,6 +326,8 @@ __global__ void __launch_bounds__(kBwdThreads, V == 8 ? CCC_BWD_MIN_BLOCKS : 4)
     using P0 = std::integral_constant<int, 0>;
     using P1 = std::integral_constant<int, 1>;
     using P2 = std::integral_constant<int, 2>;
+    using Yes = std::true_type;
+    using No = std::false_type;
     while (q < q_end) {
       int64_t lo, hi;
       seq_bounds(a.seqs, n, lo, hi);
@@ -308,6 +340,7 @@ __global__ void __launch_bounds__(kBwdThreads, V == 8 ? CCC_BWD_MIN_BLOCKS : 4)
       const uint16_t* xp = a.x + (dense ? n * a.x_sb + (a0 - lo) * xst : a0 * xst) + d0;
       const uint16_t* gq = a.g + (dense ? n * a.g_sb + (a0 - lo) * gst : a0 * gst) + d0;
       uint16_t* dp = a.dx + (dense ? n * a.dx_sb + (a0 - lo) * dst : a0 * dst) + d0;
+      const int64_t m_end = e + kState;  // tokens stepped: [a0, e + 3)
 
       float2 X[kState][H], G[kState][H];  // xe[m-3 .. m-1], gp[m-3 .. m-1]
       {
@@ -333,14 +366,6 @@ __global__ void __launch_bounds__(kBwdThreads, V == 8 ? CCC_BWD_MIN_BLOCKS : 4)
           }
 #pragma unroll
           for (int h = 0; h < H; ++h) G[j][h] = splat2(0.0f);
-        }
-      }
-      const int64_t m_end = e + kState;
-      const int64_t r_end = m_end < hi ? m_end : hi;  // rows read: [a0, r_end)
-      if constexpr (kBwdPrefetch > 0) {
-        for (int64_t t = a0 + kState; t < a0 + kState + kBwdPrefetch && t < r_end; ++t) {
-          prefetch_l2(xp + (t - a0) * xst);
-          prefetch_l2(gq + (t - a0) * gst);
         }
       }
 
@@ -377,10 +402,10 @@ __global__ void __launch_bounds__(kBwdThreads, V == 8 ? CCC_BWD_MIN_BLOCKS : 4)
         }
 #pragma unroll
         for (int h = 0; h < H; ++h) {
-          float2 acc = fmul2(w[h][0], gp[h]);
-          acc = ffma2(w[h][1], G[2][h], acc);
+          float2 acc = fmul2(w[h][3], G[0][h]);
           acc = ffma2(w[h][2], G[1][h], acc);
-          acc = ffma2(w[h][3], G[0][h], acc);
+          acc = ffma2(w[h][1], G[2][h], acc);
+          acc = ffma2(w[h][0], gp[h], acc);
           v[h] = acc;
           G[0][h] = G[1][h];
           G[1][h] = G[2][h];
@@ -409,9 +434,11 @@ __global__ void __launch_bounds__(kBwdThreads, V == 8 ? CCC_BWD_MIN_BLOCKS : 4)
         }
       };
 
-      // steady step at window phase J for token m (own token, emission to dx[m-3])
-      auto fast = [&](auto phase, typename VT::Raw xr, typename VT::Raw gr, uint16_t* drow) {
+      // steady step at window phase J for token m: with ACC, m is an own token
+      // (weight/bias sums); with STORE, the emission dx[m-3] is an own row.
+      auto fast = [&](auto phase, auto acc_flag, auto store_flag, Raw xr, Raw gr, uint16_t* drow) {
         constexpr int J = decltype(phase)::value;
+        constexpr bool ACC = decltype(acc_flag)::value, STORE = decltype(store_flag)::value;
         constexpr int J1 = (J + 1) % 3, J2 = (J + 2) % 3;
         float2 xc[H], gc[H], v[H];
         VT::unpack2(xr, xc);
@@ -424,45 +451,93 @@ __global__ void __launch_bounds__(kBwdThreads, V == 8 ? CCC_BWD_MIN_BLOCKS : 4)
           p = ffma2(w[h][2], X[J2][h], p);
           p = ffma2(w[h][3], xc[h], p);
           const float2 gp = fmul2(gc[h], act_grad2<ACT>(p));
-          aw[h][0] = ffma2(gp, X[J][h], aw[h][0]);
-          aw[h][1] = ffma2(gp, X[J1][h], aw[h][1]);
-          aw[h][2] = ffma2(gp, X[J2][h], aw[h][2]);
-          aw[h][3] = ffma2(gp, xc[h], aw[h][3]);
-          ab[h] = fadd2(ab[h], gp);
+          if constexpr (ACC) {
+            aw[h][0] = ffma2(gp, X[J][h], aw[h][0]);
+            aw[h][1] = ffma2(gp, X[J1][h], aw[h][1]);
+            aw[h][2] = ffma2(gp, X[J2][h], aw[h][2]);
+            aw[h][3] = ffma2(gp, xc[h], aw[h][3]);
+            ab[h] = fadd2(ab[h], gp);
+          }
           X[J][h] = xc[h];
-          float2 acc = fmul2(w[h][0], gp);
-          acc = ffma2(w[h][1], G[J2][h], acc);
+          float2 acc = fmul2(w[h][3], G[J][h]);  // independent of this token's gp
           acc = ffma2(w[h][2], G[J1][h], acc);
-          acc = ffma2(w[h][3], G[J][h], acc);
+          acc = ffma2(w[h][1], G[J2][h], acc);
+          acc = ffma2(w[h][0], gp, acc);
           v[h] = acc;
           G[J][h] = gp;
         }
-        VT::st(drow, VT::pack2(v));
+        if constexpr (STORE) VT::st(drow, VT::pack2(v));
+      };
+      auto group = [&](auto acc_flag, auto store_flag, const Raw (&xr)[3], const Raw (&gr)[3],
+                       uint16_t* drow) {
+        fast(P0{}, acc_flag, store_flag, xr[0], gr[0], drow);
+        fast(P1{}, acc_flag, store_flag, xr[1], gr[1], drow + dst);
+        fast(P2{}, acc_flag, store_flag, xr[2], gr[2], drow + 2 * dst);
       };
 
+      // The ring's groups: rows r0 + 3k .. r0 + 3k + 2 for k < n_total.  With a
+      // head (the window came from x rows and a0 .. a0+2 are own) r0 = a0 and
+      // group 0 computes own tokens whose emissions are the previous piece's
+      // rows; otherwise the first three tokens take the general step and
+      // r0 = a0 + 3.  Then the groups of own tokens emitting own rows; then,
+      // when those end on e with three more rows in the sequence, the tail
+      // group, which emits the last own rows; else the general step finishes.
       int64_t m = a0;
-      const int64_t pro_end = a0 + kState < m_end ? a0 + kState : m_end;
-      for (; m < pro_end; ++m) slow(m);
-      for (; m + 3 <= e; m += 3) {
-        const uint16_t* xm = xp + (m - a0) * xst;
-        const uint16_t* gm = gq + (m - a0) * gst;
-        if constexpr (kBwdPrefetch > 0) {
-#pragma unroll
-          for (int u = 0; u < 3; ++u) {
-            if (m + kBwdPrefetch + u < r_end) {
-              prefetch_l2(xm + (kBwdPrefetch + u) * xst);
-              prefetch_l2(gm + (kBwdPrefetch + u) * gst);
-            }
-          }
-        }
-        typename VT::Raw xr0 = VT::ld(xm), xr1 = VT::ld(xm + xst), xr2 = VT::ld(xm + 2 * xst);
-        typename VT::Raw gr0 = VT::ld(gm), gr1 = VT::ld(gm + gst), gr2 = VT::ld(gm + 2 * gst);
-        uint16_t* drow = dp + (m - kState - a0) * dst;
-        fast(P0{}, xr0, gr0, drow);
-        fast(P1{}, xr1, gr1, drow + dst);
-        fast(P2{}, xr2, gr2, drow + 2 * dst);
+      const bool head = a0 - kState >= lo && a0 + 3 <= e;
+      if (!head) {
+        const int64_t pro_end = a0 + kState < m_end ? a0 + kState : m_end;
+        for (; m < pro_end; ++m) slow(m);
       }
-      for (; m < m_end; ++m) slow(m);
+      const int64_t r0 = m;
+      const int64_t n_main = e > r0 ? (e - r0) / 3 : 0;
+      const bool tail = e > r0 && (e - r0) % 3 == 0 && e + kState <= hi && e - a0 >= kState;
+      const int64_t n_total = n_main + (tail ? 1 : 0);
+      const uint16_t* xr0p = xp + (r0 - a0) * xst;
+      const uint16_t* gr0p = gq + (r0 - a0) * gst;
+      auto issue = [&](int64_t k) {
+        const uint32_t s0 = ring_s + uint32_t(int(k % kBwdRing) * 6) * slot;
+        const uint16_t* xm = xr0p + 3 * k * xst;
+        const uint16_t* gm = gr0p + 3 * k * gst;
+#pragma unroll
+        for (int u = 0; u < 3; ++u) {
+          cp_async<RB>(s0 + uint32_t(2 * u) * slot, xm + u * xst);
+          cp_async<RB>(s0 + uint32_t(2 * u + 1) * slot, gm + u * gst);
+        }
+      };
+      auto take = [&](int64_t k, Raw (&xr)[3], Raw (&gr)[3]) {
+        if (k + kBwdRing - 1 < n_total) issue(k + kBwdRing - 1);
+        cp_async_commit();
+        cp_async_wait<kBwdRing - 1>();  // group k has landed
+        const char* s0 = ring + size_t(int(k % kBwdRing) * 6) * slot;
+#pragma unroll
+        for (int u = 0; u < 3; ++u) {
+          xr[u] = *reinterpret_cast<const Raw*>(s0 + size_t(2 * u) * slot);
+          gr[u] = *reinterpret_cast<const Raw*>(s0 + size_t(2 * u + 1) * slot);
+        }
+      };
+#pragma unroll
+      for (int k = 0; k < kBwdRing - 1; ++k) {
+        if (k < n_total) issue(k);
+        cp_async_commit();
+      }
+      Raw xr[3], gr[3];
+      int64_t k = 0;
+      if (head) {
+        take(0, xr, gr);
+        group(Yes{}, No{}, xr, gr, dp);
+        k = 1;
+      }
+      for (; k < n_main; ++k) {
+        take(k, xr, gr);
+        group(Yes{}, Yes{}, xr, gr, dp + (r0 + 3 * k - kState - a0) * dst);
+      }
+      m = r0 + 3 * n_main;
+      if (tail) {
+        take(n_main, xr, gr);
+        group(No{}, Yes{}, xr, gr, dp + (m - kState - a0) * dst);
+      } else {
+        for (; m < m_end; ++m) slow(m);
+      }
 
       q = e;
       ++n;
@@ -569,6 +644,27 @@ __global__ void bwd_empty_kernel(const uint16_t* dfin, uint16_t* dinit, int64_t 
 
 int bwd_block_threads(int vec) { return vec >= 4 ? kBwdThreads : 256; }
 
+// Dynamic shared memory of one channel-last backward block of `threads` threads.
+static size_t bwd_smem_bytes(int vec, int threads) {
+  if (vec == 8) return bwd_red_bytes<8>(threads) + bwd_ring_bytes<8>(threads);
+  if (vec == 4) return bwd_red_bytes<4>(threads) + bwd_ring_bytes<4>(threads);
+  return bwd_red_bytes<1>(threads);
+}
+
+// Opt the vector kernels in to more than 48 KB of dynamic shared memory (once).
+static cudaError_t bwd_smem_attributes() {
+  static std::atomic<int> done{0};
+  if (done.load(std::memory_order_acquire)) return cudaSuccess;
+  cudaError_t err = cudaSuccess;
+  const int b8 = int(bwd_smem_bytes(8, kBwdThreads)), b4 = int(bwd_smem_bytes(4, kBwdThreads));
+  for (auto f : {bwd_clv_kernel<8, kActSilu>, bwd_clv_kernel<8, kActNone>})
+    if (err == cudaSuccess) err = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, b8);
+  for (auto f : {bwd_clv_kernel<4, kActSilu>, bwd_clv_kernel<4, kActNone>})
+    if (err == cudaSuccess) err = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, b4);
+  if (err == cudaSuccess) done.store(1, std::memory_order_release);
+  return err;
+}
+
 int bwd_blocks_per_sm(int vec) {
   static std::atomic<int> cache[3];
   const int i = vec == 8 ? 0 : vec == 4 ? 1 : 2;
@@ -576,7 +672,8 @@ int bwd_blocks_per_sm(int vec) {
   if (v == 0) {
     int n = 0;
     const int threads = bwd_block_threads(vec);
-    const size_t smem = size_t(threads) * vec * (kWidth + 1) * sizeof(float);
+    const size_t smem = bwd_smem_bytes(vec, threads);
+    bwd_smem_attributes();
     const cudaError_t err =
         vec == 8   ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, bwd_clv_kernel<8, kActSilu>, threads, smem)
         : vec == 4 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, bwd_clv_kernel<4, kActSilu>, threads, smem)
@@ -592,7 +689,11 @@ static cudaError_t launch_bwd_act(const BwdArgs& a, const BwdPlan& p, bool pdl,
                                   cudaStream_t stream) {
   if (p.kind == kLayoutChannelLast) {
     dim3 block(p.tx, p.ty), grid(p.gx, p.gy);
-    const size_t smem = size_t(p.tx) * p.ty * p.vec * (kWidth + 1) * sizeof(float);
+    const size_t smem = bwd_smem_bytes(p.vec, p.tx * p.ty);
+    if (p.vec >= 4) {
+      const cudaError_t err = bwd_smem_attributes();
+      if (err != cudaSuccess) return err;
+    }
     if (p.vec == 8) return launch_kernel(bwd_clv_kernel<8, ACT>, grid, block, smem, stream, pdl, a);
     if (p.vec == 4) return launch_kernel(bwd_clv_kernel<4, ACT>, grid, block, smem, stream, pdl, a);
     return launch_kernel(bwd_cl_kernel<1, ACT>, grid, block, smem, stream, pdl, a);

@@ -69,13 +69,18 @@ __device__ __forceinline__ float act_fwd(float p) {
   }
 }
 
-// d act / d p:  silu'(p) = s * (1 + p * (1 - s)),  s = sigmoid(p), with s from
-// the hardware tanh as in act_fwd (absolute error of s below 2^-12).
+// d act / d p:  silu'(p) = s + p * s * (1 - s),  s = sigmoid(p).  With
+// t = tanh(p / 2) from the hardware tanh as in act_fwd, s = (1 + t) / 2 and
+// s * (1 - s) = (1 - t^2) / 4, so silu'(p) = (1 + t) / 2 + (p / 4) * (1 - t^2):
+// two independent FMAs on t, then one more (a short dependent chain after the
+// tanh).  The error is that of t (relative about 2^-11) carried through.
 template <int ACT>
 __device__ __forceinline__ float act_grad(float p) {
   if constexpr (ACT == kActSilu) {
-    const float s = fmaf(0.5f, tanh_approx(0.5f * p), 0.5f);
-    return s * fmaf(p, 1.0f - s, 1.0f);
+    const float t = tanh_approx(0.5f * p);
+    const float u = fmaf(0.5f, t, 0.5f);
+    const float v = fmaf(-t, t, 1.0f);
+    return fmaf(0.25f * p, v, u);
   } else {
     return 1.0f;
   }
@@ -114,9 +119,9 @@ __device__ __forceinline__ float2 act_grad2(float2 p) {
   if constexpr (ACT == kActSilu) {
     const float2 h = fmul2(p, splat2(0.5f));
     const float2 t = make_float2(tanh_approx(h.x), tanh_approx(h.y));
-    const float2 s = ffma2(t, splat2(0.5f), splat2(0.5f));
-    const float2 one_minus_s = fadd2(splat2(1.0f), make_float2(-s.x, -s.y));
-    return fmul2(s, ffma2(p, one_minus_s, splat2(1.0f)));
+    const float2 u = ffma2(t, splat2(0.5f), splat2(0.5f));
+    const float2 v = ffma2(make_float2(-t.x, -t.y), t, splat2(1.0f));
+    return ffma2(fmul2(p, splat2(0.25f)), v, u);
   } else {
     return splat2(1.0f);
   }
@@ -261,6 +266,27 @@ __device__ __forceinline__ void store_state2(uint16_t* s, const float2 (&win)[kS
 #pragma unroll
     for (int h = 0; h < V / 2; ++h) { f[i][2 * h] = win[i][h].x; f[i][2 * h + 1] = win[i][h].y; }
   store_state<V>(s, f);
+}
+
+// ---- per-thread asynchronous copies, global -> shared ---------------------------
+//
+// cp.async moves BYTES (8 or 16) without passing through registers; a thread
+// groups its copies with commit and waits until at most N of its groups are
+// still in flight.  A thread that only ever reads back what it copied itself
+// needs no barrier: after the wait its own copies are visible to it.
+template <int BYTES>
+__device__ __forceinline__ void cp_async(uint32_t smem_addr, const void* gmem) {
+  static_assert(BYTES == 8 || BYTES == 16, "cp.async moves 4, 8 or 16 bytes");
+  if constexpr (BYTES == 16)
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr), "l"(gmem) : "memory");
+  else
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_addr), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
 // ---- weights -----------------------------------------------------------------
