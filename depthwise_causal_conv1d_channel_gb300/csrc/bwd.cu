@@ -11,6 +11,9 @@
 // e + 2, computing gp[m] (three tokens past e are recomputed, not
 // accumulated) and emitting dxe[m - 3] once gp[m-3 .. m] are known.  The
 // thread whose range starts a sequence also emits the three dinit entries.
+// The kernels work with the halved weights and gp2 = 2 gp (see the activation
+// section of common.cuh), which leaves dxe unchanged and doubles the sums,
+// halved once before they are written.
 #include <atomic>
 #include <type_traits>
 
@@ -78,7 +81,7 @@ __device__ __forceinline__ void bwd_walk(const BwdArgs& a, const Seqs& seqs, con
         p = fmaf(w[c][1], xw[1][c], p);
         p = fmaf(w[c][2], xw[2][c], p);
         p = fmaf(w[c][3], xc[c], p);
-        gp[c] = gc[c] * act_grad<ACT>(p);
+        gp[c] = act_bwd<ACT>(p, gc[c]);
         if (own) {
           aw[c][0] = fmaf(gp[c], xw[0][c], aw[c][0]);
           aw[c][1] = fmaf(gp[c], xw[1][c], aw[c][1]);
@@ -192,7 +195,8 @@ __host__ __device__ constexpr size_t bwd_red_bytes(int threads) {
   return size_t(threads) * V * (kWidth + 1) * sizeof(float);
 }
 
-// Block-wide sum of the per-thread weight/bias sums over threadIdx.y (threads
+// Block-wide sum of the per-thread weight/bias sums (sums of gp2 = 2 gp, halved
+// here) over threadIdx.y (threads
 // with equal threadIdx.x own the same channels), in a fixed order, then either
 // FP32 atomics into ws[0] or a store into this block row's partial ws[blockIdx.y].
 template <int V>
@@ -205,8 +209,8 @@ __device__ __forceinline__ void block_wgrad_out(const BwdArgs& a, int d0, bool a
 #pragma unroll
   for (int c = 0; c < V; ++c) {
 #pragma unroll
-    for (int k = 0; k < kWidth; ++k) mine[c * (kWidth + 1) + k] = active ? aw[c][k] : 0.0f;
-    mine[c * (kWidth + 1) + kWidth] = active ? ab[c] : 0.0f;
+    for (int k = 0; k < kWidth; ++k) mine[c * (kWidth + 1) + k] = active ? 0.5f * aw[c][k] : 0.0f;
+    mine[c * (kWidth + 1) + kWidth] = active ? 0.5f * ab[c] : 0.0f;
   }
   __syncthreads();
   // each of the block's threads finalises a slice of the tx * P values
@@ -384,7 +388,7 @@ __global__ void __launch_bounds__(kBwdThreads, V == 8 ? CCC_BWD_MIN_BLOCKS : 4)
             p = ffma2(w[h][1], X[1][h], p);
             p = ffma2(w[h][2], X[2][h], p);
             p = ffma2(w[h][3], xc[h], p);
-            gp[h] = fmul2(gc[h], act_grad2<ACT>(p));
+            gp[h] = act_bwd2<ACT>(p, gc[h]);
             if (own) {
               aw[h][0] = ffma2(gp[h], X[0][h], aw[h][0]);
               aw[h][1] = ffma2(gp[h], X[1][h], aw[h][1]);
@@ -450,7 +454,7 @@ __global__ void __launch_bounds__(kBwdThreads, V == 8 ? CCC_BWD_MIN_BLOCKS : 4)
           p = ffma2(w[h][1], X[J1][h], p);
           p = ffma2(w[h][2], X[J2][h], p);
           p = ffma2(w[h][3], xc[h], p);
-          const float2 gp = fmul2(gc[h], act_grad2<ACT>(p));
+          const float2 gp = act_bwd2<ACT>(p, gc[h]);
           if constexpr (ACC) {
             aw[h][0] = ffma2(gp, X[J][h], aw[h][0]);
             aw[h][1] = ffma2(gp, X[J1][h], aw[h][1]);
@@ -582,7 +586,9 @@ __global__ void __launch_bounds__(256) bwd_bdt_kernel(BwdArgs a) {
   }
   pdl_release();
   pdl_wait();  // atomic mode: the accumulator is zeroed by the kernel before this one
-  float v[kWidth + 1] = {aw[0][0], aw[0][1], aw[0][2], aw[0][3], ab[0]};
+  // the sums are of gp2 = 2 gp: halve them (exact)
+  float v[kWidth + 1] = {0.5f * aw[0][0], 0.5f * aw[0][1], 0.5f * aw[0][2], 0.5f * aw[0][3],
+                         0.5f * ab[0]};
 #pragma unroll
   for (int k = 0; k < kWidth + 1; ++k)
 #pragma unroll

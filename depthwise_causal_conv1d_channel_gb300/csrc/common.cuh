@@ -57,32 +57,34 @@ __device__ __forceinline__ float tanh_approx(float x) {
   return y;
 }
 
-// silu(p) = p * sigmoid(p), with sigmoid(p) = (1 + tanh(p / 2)) / 2 from the
-// hardware tanh (one MUFU operation; relative error about 2^-11, so the
-// absolute error of silu stays below |p| * 2^-12).
+// The kernels hold the weights and the bias times one half (an exact
+// scaling), so every pre-activation they form is h = p / 2, exactly the half
+// of the p the full weights would give.  With t = tanh(h) from the hardware
+// tanh (one MUFU operation, relative error about 2^-11):
+//   silu(p)      = p * sigmoid(p) = p (1 + t) / 2 = h + h t
+//   2 * silu'(p) = 2 sigmoid(p) (1 + p (1 - sigmoid(p))) = 1 + t + h (1 - t^2)
+// The backward carries gp2 = 2 * grad_out * act'(p): its weight and bias sums
+// are halved once at the end, and dx = sum_k w_k gp = sum_k (w_k / 2) gp2 uses
+// the halved weights as they are.
 template <int ACT>
-__device__ __forceinline__ float act_fwd(float p) {
+__device__ __forceinline__ float act_fwd(float h) {
   if constexpr (ACT == kActSilu) {
-    return p * fmaf(0.5f, tanh_approx(0.5f * p), 0.5f);
+    return fmaf(h, tanh_approx(h), h);
   } else {
-    return p;
+    return h + h;
   }
 }
 
-// d act / d p:  silu'(p) = s + p * s * (1 - s),  s = sigmoid(p).  With
-// t = tanh(p / 2) from the hardware tanh as in act_fwd, s = (1 + t) / 2 and
-// s * (1 - s) = (1 - t^2) / 4, so silu'(p) = (1 + t) / 2 + (p / 4) * (1 - t^2):
-// two independent FMAs on t, then one more (a short dependent chain after the
-// tanh).  The error is that of t (relative about 2^-11) carried through.
+// gp2 = 2 * g * act'(p) from h = p / 2 and the incoming gradient g.
 template <int ACT>
-__device__ __forceinline__ float act_grad(float p) {
+__device__ __forceinline__ float act_bwd(float h, float g) {
   if constexpr (ACT == kActSilu) {
-    const float t = tanh_approx(0.5f * p);
-    const float u = fmaf(0.5f, t, 0.5f);
-    const float v = fmaf(-t, t, 1.0f);
-    return fmaf(0.25f * p, v, u);
+    const float t = tanh_approx(h);
+    const float v = fmaf(-t, t, 1.0f);  // 1 - t^2
+    const float r = fmaf(h, v, t);      // t + h (1 - t^2)
+    return fmaf(g, r, g);
   } else {
-    return 1.0f;
+    return g + g;
   }
 }
 
@@ -101,29 +103,26 @@ __device__ __forceinline__ float2 splat2(float v) { return make_float2(v, v); }
 __device__ __forceinline__ float2 unpack_bf16x2(uint32_t u) { return make_float2(bf16_lo(u), bf16_hi(u)); }
 __device__ __forceinline__ uint32_t pack_bf16x2(float2 v) { return pack_bf16x2(v.x, v.y); }
 
-// silu on a pair; same operations, in the same order, as act_fwd.
+// Pair forms: the same operations, in the same order, as act_fwd / act_bwd.
 template <int ACT>
-__device__ __forceinline__ float2 act_fwd2(float2 p) {
+__device__ __forceinline__ float2 act_fwd2(float2 h) {
   if constexpr (ACT == kActSilu) {
-    const float2 h = fmul2(p, splat2(0.5f));
     const float2 t = make_float2(tanh_approx(h.x), tanh_approx(h.y));
-    return fmul2(p, ffma2(t, splat2(0.5f), splat2(0.5f)));
+    return ffma2(h, t, h);
   } else {
-    return p;
+    return fadd2(h, h);
   }
 }
 
-// silu' on a pair; same operations, in the same order, as act_grad.
 template <int ACT>
-__device__ __forceinline__ float2 act_grad2(float2 p) {
+__device__ __forceinline__ float2 act_bwd2(float2 h, float2 g) {
   if constexpr (ACT == kActSilu) {
-    const float2 h = fmul2(p, splat2(0.5f));
     const float2 t = make_float2(tanh_approx(h.x), tanh_approx(h.y));
-    const float2 u = ffma2(t, splat2(0.5f), splat2(0.5f));
     const float2 v = ffma2(make_float2(-t.x, -t.y), t, splat2(1.0f));
-    return ffma2(fmul2(p, splat2(0.25f)), v, u);
+    const float2 r = ffma2(h, v, t);
+    return ffma2(g, r, g);
   } else {
-    return splat2(1.0f);
+    return fadd2(g, g);
   }
 }
 
@@ -303,10 +302,13 @@ struct WeightRef {
 // Widest channel slice a block stages: 32 threads x 8 channels.
 constexpr int kMaxBlockChannels = 256;
 
-// Block-cooperative copy of the weights and bias of channels
+// The weight loaders below all return the weights and the bias times one half
+// (see the activation section).
+//
+// Block-cooperative copy of the halved weights and bias of channels
 // [d_base, d_base + n) into shared memory as FP32, tap-major: ws[k*n + i] is
-// w[d_base + i, k] for k < 4 and ws[4*n + i] the bias (0 without one, or past
-// D).  Consecutive threads read consecutive channels, so the global reads are
+// w[d_base + i, k] / 2 for k < 4 and ws[4*n + i] the bias / 2 (0 without one,
+// or past D).  Consecutive threads read consecutive channels, so the global reads are
 // coalesced for the usual [D, 4] layout.  Every thread of the block must call it.
 __device__ __forceinline__ void stage_weights(const WeightRef& r, int d_base, int n, int D,
                                               float* ws) {
@@ -327,10 +329,10 @@ __device__ __forceinline__ void stage_weights(const WeightRef& r, int d_base, in
         if (d < D) {
           if (k < kWidth) {
             const int64_t o = d * r.w_sd + k * r.w_sk;
-            v[j] = r.w_f32 ? __ldg(static_cast<const float*>(r.w) + o)
-                           : bf16_to_f32(__ldg(static_cast<const uint16_t*>(r.w) + o));
+            v[j] = 0.5f * (r.w_f32 ? __ldg(static_cast<const float*>(r.w) + o)
+                                   : bf16_to_f32(__ldg(static_cast<const uint16_t*>(r.w) + o)));
           } else if (r.bias) {
-            v[j] = bf16_to_f32(__ldg(r.bias + d * r.b_sd));
+            v[j] = 0.5f * bf16_to_f32(__ldg(r.bias + d * r.b_sd));
           }
         }
       }
@@ -437,6 +439,12 @@ __device__ __forceinline__ void weights_direct2(const WeightRef& r, int d0,
 #pragma unroll
     for (int h = 0; h < V / 2; ++h) b[h] = splat2(0.0f);
   }
+#pragma unroll
+  for (int h = 0; h < V / 2; ++h) {
+    b[h] = fmul2(b[h], splat2(0.5f));
+#pragma unroll
+    for (int k = 0; k < kWidth; ++k) w[h][k] = fmul2(w[h][k], splat2(0.5f));
+  }
 }
 
 // Weights of one channel straight from global memory (warp-uniform channel:
@@ -446,10 +454,10 @@ __device__ __forceinline__ void load_weights_1(const WeightRef& r, int64_t d, fl
 #pragma unroll
   for (int k = 0; k < kWidth; ++k) {
     const int64_t o = d * r.w_sd + k * r.w_sk;
-    w[0][k] = r.w_f32 ? __ldg(static_cast<const float*>(r.w) + o)
-                      : bf16_to_f32(__ldg(static_cast<const uint16_t*>(r.w) + o));
+    w[0][k] = 0.5f * (r.w_f32 ? __ldg(static_cast<const float*>(r.w) + o)
+                              : bf16_to_f32(__ldg(static_cast<const uint16_t*>(r.w) + o)));
   }
-  b[0] = r.bias ? bf16_to_f32(__ldg(r.bias + d * r.b_sd)) : 0.0f;
+  b[0] = r.bias ? 0.5f * bf16_to_f32(__ldg(r.bias + d * r.b_sd)) : 0.0f;
 }
 
 // Hint: bring the 32-byte sector holding p into L2 ahead of its load.

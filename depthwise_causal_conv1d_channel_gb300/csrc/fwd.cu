@@ -6,7 +6,9 @@
 // tokens, keeping the last three inputs of every channel in registers, so each
 // input is read from HBM once (plus a three-token halo per range) and each
 // output written once.  Nothing is staged: the op is a streaming stencil with
-// about one FLOP per byte, bound by HBM bandwidth, not a contraction.
+// about one FLOP per byte, bound by HBM bandwidth, not a contraction.  The
+// weights are held halved, so the sums below are h = pre / 2 (see the
+// activation section of common.cuh).
 #include <atomic>
 #include <type_traits>
 
