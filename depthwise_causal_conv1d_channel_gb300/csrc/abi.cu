@@ -280,7 +280,9 @@ static FwdPlan plan_bdt(int64_t rows) {
 
 FwdPlan plan_fwd(int kind, int vec, int64_t Q, int D, int64_t rows, int sm_count) {
   if (kind == kLayoutTimeContiguous) return plan_bdt(rows);
-  return plan_cl(vec, Q, D, sm_count, fwd_blocks_per_sm(vec), 1, 8, 256);
+  // segments of a multiple of six tokens: the vector kernel's ring groups then
+  // cover a segment inside a sequence exactly
+  return plan_cl(vec, Q, D, sm_count, fwd_blocks_per_sm(vec), 1, 12, 256, vec == 4 ? 6 : 1);
 }
 
 BwdPlan plan_bwd(int kind, int vec, int64_t Q, int D, int64_t rows, int sm_count) {

@@ -133,36 +133,53 @@ __global__ void __launch_bounds__(256) fwd_cl_kernel(FwdArgs a) {
 // Channel-last x with vectors of V = 4 channels, computed as two channel
 // pairs (the fast path; eight channels a thread measured no faster).  Same
 // walk as fwd_walk, specialised: the three-token window lives in three register
-// slots that rotate (the newest token overwrites the oldest slot), so steady
-// state runs in groups of three tokens with no register copies; x and out are
-// addressed through running pointers; rows kPrefetch tokens ahead are
-// prefetched into L2.
-#ifndef CCC_FWD_PREFETCH
-#define CCC_FWD_PREFETCH 0
+// slots that rotate (the newest token overwrites the oldest slot), so full
+// groups of kFwdGroup tokens (a multiple of three) need no register copies.
+// The x rows stream through the thread's own ring of kFwdRing stages of one
+// group each in shared memory, filled with cp.async kFwdRing - 1 groups ahead
+// of the group being computed: no step waits on a load it has just issued, and
+// no registers are held by loads in flight.  Segments are planned in multiples
+// of kFwdGroup tokens, so only a sequence's last group can be partial; its
+// tokens take the physically shifting step from the same ring.
+constexpr int kFwdGroup = 6;  // tokens per ring stage (multiple of 3)
+#ifndef CCC_FWD_RING
+#define CCC_FWD_RING 4
 #endif
-constexpr int kFwdGroup = 6;                 // tokens per steady-state step (multiple of 3)
-constexpr int kFwdPrefetch = CCC_FWD_PREFETCH;  // tokens of L2 prefetch distance
+constexpr int kFwdRing = CCC_FWD_RING;
+static_assert(kFwdRing >= 2, "the ring needs a stage being filled and one being read");
+constexpr int kFwdThreads = 256;
+template <int V>
+constexpr size_t fwd_ring_bytes(int threads) {
+  return size_t(threads) * kFwdRing * kFwdGroup * (2 * V);
+}
+extern __shared__ __align__(16) char fwd_dyn_smem[];
 
 template <int V, int ACT>
-__global__ void __launch_bounds__(256, 3) fwd_clv_kernel(FwdArgs a) {
+__global__ void __launch_bounds__(kFwdThreads, 3) fwd_clv_kernel(FwdArgs a) {
   pdl_wait();     // inputs may come from the previous kernel in the stream
   pdl_release();
   using VT = Vec<V>;
+  using Raw = typename VT::Raw;
   constexpr int H = V / 2;  // channel pairs
+  constexpr int RB = int(sizeof(Raw));
+  constexpr int G = kFwdGroup;
   __shared__ __align__(16) float ws[(kWidth + 1) * kMaxBlockChannels];
   if (block_rejects_cu_seqlens(a.seqs, a.status)) return;
   const int n_blk = blockDim.x * V;
   const int d0 = (blockIdx.x * blockDim.x + threadIdx.x) * V;
   const int64_t seg = int64_t(blockIdx.y) * blockDim.y + threadIdx.y;
-  const bool dense0 = a.seqs.cu == nullptr;
-  if (d0 < a.D && seg < a.n_seg)
-    prefetch_first_rows(a.seqs, a.x + d0, dense0 ? a.x_sb - a.seqs.T * a.x_st : 0, a.x_st,
-                        seg * a.seg_len, kState, kFwdGroup);
   if (!a.wr.w_vec) stage_weights(a.wr, blockIdx.x * n_blk, n_blk, a.D, ws);  // block-uniform
   if (d0 >= a.D || seg >= a.n_seg) return;
   float2 w[H][kWidth], b[H];
   if (a.wr.w_vec) weights_direct2<V>(a.wr, d0, w, b);
   else weights_from_smem2<V>(ws, n_blk, threadIdx.x * V, w, b);
+  // this thread's ring: slot (stage, row u) at byte ((stage * G + u) * threads + tid) * RB
+  const int nthr = blockDim.x * blockDim.y;
+  const int tid = threadIdx.y * blockDim.x + threadIdx.x;
+  const char* ring = fwd_dyn_smem + size_t(tid) * RB;
+  const uint32_t ring_s = smem_u32(ring);
+  const uint32_t slot = uint32_t(nthr) * RB;
+
   int64_t q = seg * a.seg_len;
   const int64_t q_end = q + a.seg_len < a.seqs.Q ? q + a.seg_len : a.seqs.Q;
   const bool dense = a.seqs.cu == nullptr;
@@ -175,10 +192,26 @@ __global__ void __launch_bounds__(256, 3) fwd_clv_kernel(FwdArgs a) {
     seq_bounds(a.seqs, n, lo, hi);
     const int64_t e = q_end < hi ? q_end : hi;
     const int64_t state_row = int64_t(n) * a.D + d0;
-    // running pointers at token q
+    // pointers at token q
     const uint16_t* xp = a.x + (dense ? n * a.x_sb + (q - lo) * a.x_st : q * a.x_st) + d0;
     uint16_t* op = a.out + (dense ? n * a.o_sb + (q - lo) * a.o_st : q * a.o_st) + d0;
     const int64_t xst = a.x_st, ost = a.o_st;
+    const int n_tok = int(e - q);  // a segment's tokens: below 2^31
+    const int n_grp = (n_tok + G - 1) / G;  // the last one may be partial
+
+    // group k: rows q + kG .. q + kG + G - 1 (those below e) into stage k % kFwdRing
+    auto issue = [&](int k) {
+      const uint32_t s0 = ring_s + uint32_t((k % kFwdRing) * G) * slot;
+      const uint16_t* xm = xp + int64_t(k) * G * xst;
+#pragma unroll
+      for (int u = 0; u < G; ++u)
+        if (k * G + u < n_tok) cp_async<RB>(s0 + uint32_t(u) * slot, xm + u * xst);
+    };
+#pragma unroll
+    for (int k = 0; k < kFwdRing - 1; ++k) {
+      if (k < n_grp) issue(k);
+      cp_async_commit();
+    }
 
     // W[j] = xe[q - 3 + j]
     float2 W[kState][H];
@@ -205,14 +238,10 @@ __global__ void __launch_bounds__(256, 3) fwd_clv_kernel(FwdArgs a) {
         }
       }
     }
-    if constexpr (kFwdPrefetch > 0) {
-      for (int64_t t = kFwdGroup; t < kFwdGroup + kFwdPrefetch && q + t < e; ++t)
-        prefetch_l2(xp + t * xst);
-    }
 
     // one token at window phase J: taps W[J], W[J+1], W[J+2] (mod 3), then the
     // new token replaces W[J]
-    auto step = [&](auto phase, typename VT::Raw raw, uint16_t* dst) {
+    auto step = [&](auto phase, Raw raw, uint16_t* dst) {
       constexpr int J = decltype(phase)::value;
       float2 cur[H], y[H];
       VT::unpack2(raw, cur);
@@ -228,31 +257,10 @@ __global__ void __launch_bounds__(256, 3) fwd_clv_kernel(FwdArgs a) {
       }
       VT::st(dst, VT::pack2(y));
     };
-
-    for (; q + kFwdGroup <= e; q += kFwdGroup) {
-      if constexpr (kFwdPrefetch > 0) {
-#pragma unroll
-        for (int u = 0; u < kFwdGroup; ++u) {
-          const int64_t t = kFwdGroup + kFwdPrefetch + u;
-          if (q + t < e) prefetch_l2(xp + t * xst);
-        }
-      }
-      typename VT::Raw r[kFwdGroup];
-#pragma unroll
-      for (int u = 0; u < kFwdGroup; ++u) r[u] = VT::ld(xp + u * xst);
-#pragma unroll
-      for (int u = 0; u < kFwdGroup; u += 3) {
-        step(P0{}, r[u], op + u * ost);
-        step(P1{}, r[u + 1], op + (u + 1) * ost);
-        step(P2{}, r[u + 2], op + (u + 2) * ost);
-      }
-      xp += kFwdGroup * xst;
-      op += kFwdGroup * ost;
-    }
-    // remainder: physical shift keeps the window at phase 0
-    for (; q < e; ++q) {
+    // one token with a physical shift (keeps the window at phase 0)
+    auto shift_step = [&](Raw raw, uint16_t* dst) {
       float2 cur[H], y[H];
-      VT::unpack2(VT::ld(xp), cur);
+      VT::unpack2(raw, cur);
 #pragma unroll
       for (int h = 0; h < H; ++h) {
         float2 p = b[h];
@@ -265,11 +273,33 @@ __global__ void __launch_bounds__(256, 3) fwd_clv_kernel(FwdArgs a) {
         W[1][h] = W[2][h];
         W[2][h] = cur[h];
       }
-      VT::st(op, VT::pack2(y));
-      xp += xst;
-      op += ost;
+      VT::st(dst, VT::pack2(y));
+    };
+
+    for (int k = 0; k < n_grp; ++k) {
+      if (k + kFwdRing - 1 < n_grp) issue(k + kFwdRing - 1);
+      cp_async_commit();
+      cp_async_wait<kFwdRing - 1>();  // group k has landed
+      const char* s0 = ring + size_t((k % kFwdRing) * G) * slot;
+      Raw r[G];
+#pragma unroll
+      for (int u = 0; u < G; ++u) r[u] = *reinterpret_cast<const Raw*>(s0 + size_t(u) * slot);
+      uint16_t* om = op + int64_t(k) * G * ost;
+      if (k * G + G <= n_tok) {
+#pragma unroll
+        for (int u = 0; u < G; u += 3) {
+          step(P0{}, r[u], om + u * ost);
+          step(P1{}, r[u + 1], om + (u + 1) * ost);
+          step(P2{}, r[u + 2], om + (u + 2) * ost);
+        }
+      } else {
+#pragma unroll
+        for (int u = 0; u < G; ++u)
+          if (k * G + u < n_tok) shift_step(r[u], om + u * ost);
+      }
     }
     if (e == hi && a.fin) store_state2<V>(a.fin + state_row * kState, W);
+    q = e;
     ++n;
   }
 }
@@ -309,14 +339,30 @@ __global__ void fwd_empty_kernel(const uint16_t* init, uint16_t* fin, int64_t n)
 
 // ---- host launchers ------------------------------------------------------------
 
+// Opt the vector kernel in to its ring's dynamic shared memory (once).
+static cudaError_t fwd_smem_attributes() {
+  static std::atomic<int> done{0};
+  if (done.load(std::memory_order_acquire)) return cudaSuccess;
+  const int bytes = int(fwd_ring_bytes<4>(kFwdThreads));
+  cudaError_t err = cudaFuncSetAttribute(fwd_clv_kernel<4, kActSilu>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (err == cudaSuccess)
+    err = cudaFuncSetAttribute(fwd_clv_kernel<4, kActNone>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (err == cudaSuccess) done.store(1, std::memory_order_release);
+  return err;
+}
+
 int fwd_blocks_per_sm(int vec) {
   static std::atomic<int> cache[2];
   const int i = vec == 4 ? 0 : 1;
   int v = cache[i].load(std::memory_order_relaxed);
   if (v == 0) {
     int n = 0;
+    fwd_smem_attributes();
     const cudaError_t err =
-        vec == 4 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fwd_clv_kernel<4, kActSilu>, 256, 0)
+        vec == 4 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fwd_clv_kernel<4, kActSilu>, 256,
+                                                                 fwd_ring_bytes<4>(256))
                  : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fwd_cl_kernel<1, kActSilu>, 256, 0);
     v = (err == cudaSuccess && n > 0) ? n : 1;
     cache[i].store(v, std::memory_order_relaxed);
@@ -328,7 +374,12 @@ template <int ACT>
 static cudaError_t launch_fwd_act(const FwdArgs& a, const FwdPlan& p, cudaStream_t stream) {
   if (p.kind == kLayoutChannelLast) {
     dim3 block(p.tx, p.ty), grid(p.gx, p.gy);
-    if (p.vec == 4) return launch_kernel(fwd_clv_kernel<4, ACT>, grid, block, 0, stream, true, a);
+    if (p.vec == 4) {
+      const cudaError_t err = fwd_smem_attributes();
+      if (err != cudaSuccess) return err;
+      return launch_kernel(fwd_clv_kernel<4, ACT>, grid, block, fwd_ring_bytes<4>(p.tx * p.ty),
+                           stream, true, a);
+    }
     return launch_kernel(fwd_cl_kernel<1, ACT>, grid, block, 0, stream, true, a);
   }
   return launch_kernel(fwd_bdt_kernel<ACT>, dim3(p.gx), dim3(256), 0, stream, true, a);
