@@ -202,8 +202,7 @@ class DenseStep:
         self.bwd_bytes = bwd_bytes(d.x, self.w, self.b, self.init, self.dfin, self.dinit)
         self.tokens = inp.tokens if inp.cu_seqlens is None else d.x.shape[2]
         self.launches_fwd = 1
-        # backward kernel + the fixed-order finalize kernel (after a memset node in
-        # atomic mode)
+        # backward kernel + the fixed-order finalize kernel
         self.launches_bwd = 2
 
     def fwd(self, i, stream):
@@ -586,7 +585,7 @@ def main():
         "data": "synthetic",
         "config": {"workload": "dense_state", "x": [4, 2048, 1536], "layout": "channel-last",
                    "weight": "bf16", "bias": True, "initial_states": True,
-                   "final_states": True, "dweight": "fp32-atomic",
+                   "final_states": True, "dweight": "fp32-partials",
                    "step": "forward + backward", "parallelism": f"replicas{world}",
                    "l2": f"rotating {step.sets} buffer sets, "
                          f"{step.sets * 4 * act_bytes(step.x[0]) / 2**20:.0f} MiB > L2"},

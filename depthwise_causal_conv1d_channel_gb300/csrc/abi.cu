@@ -371,7 +371,8 @@ static bool bwd_plan_for(const ccc_tensor* x, const Problem& pb, int vec, ccc::B
 }
 
 static size_t bwd_ws_bytes(const ccc::BwdPlan& p, const Problem& pb, int deterministic) {
-  const int64_t rows = deterministic ? ccc::bwd_partial_rows(p, pb.B, pb.packed) : 1;
+  (void)deterministic;  // both modes write per-block partial rows
+  const int64_t rows = ccc::bwd_partial_rows(p, pb.B, pb.packed);
   return size_t(std::max<int64_t>(rows, 1)) * size_t(pb.D) * (kWidth + 1) * sizeof(float);
 }
 
@@ -468,7 +469,6 @@ ccc_status ccc_conv1d_bwd(const ccc_tensor* x, const ccc_tensor* weight, const c
   a.seg_len = p.seg_len;
   a.n_seg = p.n_seg;
   a.ws = static_cast<float*>(workspace);
-  a.deterministic = deterministic;
   a.status = d_status;
 
   ccc::WgradOut o{};

@@ -1,7 +1,10 @@
 // Backward kernels of the depthwise causal conv1d (cuDNN frontend docs, "Causal
 // Conv1d" page: forward and backward on the optimized route; the paragraph on
 // determinism -- FP32 atomics by default, unique FP32 partials plus a
-// fixed-order reduction when deterministic).
+// fixed-order reduction when deterministic).  Both modes here take the second
+// route: every block writes its own row of FP32 partial sums and the finalize
+// kernel adds the rows in a fixed order, so the weight gradient is always
+// bitwise repeatable and no accumulator needs zeroing first.
 //
 // With gp[t] = dout[t] * act'(pre[t]) (pre recomputed from x, nothing saved):
 //   dxe[j] = sum_k w[k] * gp[j + 3 - k]  (+ dfinal[j - (len-3)] for j >= len-3)
@@ -204,7 +207,6 @@ __device__ __forceinline__ void block_wgrad_out(const BwdArgs& a, int d0, bool a
                                                 const float (&aw)[V][kWidth], const float (&ab)[V]) {
   float* red = bwd_dyn_smem;  // [ty][tx][V * 5]
   constexpr int P = V * (kWidth + 1);
-  pdl_wait();  // atomic mode: the accumulator is zeroed by the kernel before this one
   float* mine = red + (threadIdx.y * blockDim.x + threadIdx.x) * P;
 #pragma unroll
   for (int c = 0; c < V; ++c) {
@@ -225,16 +227,14 @@ __device__ __forceinline__ void block_wgrad_out(const BwdArgs& a, int d0, bool a
     float s = 0.0f;
     for (int y = 0; y < int(blockDim.y); ++y) s += red[(y * blockDim.x + tx) * P + r];
     const int k = r % (kWidth + 1);
-    if (a.deterministic)
-      a.ws[(int64_t(blockIdx.y) * a.D + d) * (kWidth + 1) + k] = s;
-    else
-      atomicAdd(a.ws + int64_t(d) * (kWidth + 1) + k, s);
+    a.ws[(int64_t(blockIdx.y) * a.D + d) * (kWidth + 1) + k] = s;
   }
 }
 
 template <int V, int ACT>
 __global__ void __launch_bounds__(256) bwd_cl_kernel(BwdArgs a) {
   __shared__ __align__(16) float wsm[(kWidth + 1) * kMaxBlockChannels];
+  pdl_wait();  // inputs may come from the previous kernel in the stream
   if (block_rejects_cu_seqlens(a.seqs, a.status)) return;
   const int n_blk = blockDim.x * V;
   stage_weights(a.wr, blockIdx.x * n_blk, n_blk, a.D, wsm);
@@ -297,6 +297,7 @@ __global__ void __launch_bounds__(kBwdThreads, V == 8 ? CCC_BWD_MIN_BLOCKS : 4)
   constexpr int H = V / 2;  // channel pairs
   constexpr int RB = int(sizeof(Raw));
   __shared__ __align__(16) float wsm[(kWidth + 1) * kMaxBlockChannels];
+  pdl_wait();  // inputs may come from the previous kernel in the stream
   if (block_rejects_cu_seqlens(a.seqs, a.status)) return;
   const int n_blk = blockDim.x * V;
   const int d0 = (blockIdx.x * blockDim.x + threadIdx.x) * V;
@@ -564,6 +565,7 @@ __global__ void __launch_bounds__(kBwdThreads, V == 8 ? CCC_BWD_MIN_BLOCKS : 4)
 // warp in a fixed butterfly order; partial row = batch index.
 template <int ACT>
 __global__ void __launch_bounds__(256) bwd_bdt_kernel(BwdArgs a) {
+  pdl_wait();  // inputs may come from the previous kernel in the stream
   if (block_rejects_cu_seqlens(a.seqs, a.status)) return;
   const int lane = threadIdx.x & 31;
   const int64_t row = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -585,7 +587,6 @@ __global__ void __launch_bounds__(256) bwd_bdt_kernel(BwdArgs a) {
     bwd_walk<1, ACT, 4, 0>(a, rs, xs, gs, ds, dense ? bb : 0, d, w, b, q0, q1, aw, ab);
   }
   pdl_release();
-  pdl_wait();  // atomic mode: the accumulator is zeroed by the kernel before this one
   // the sums are of gp2 = 2 gp: halve them (exact)
   float v[kWidth + 1] = {0.5f * aw[0][0], 0.5f * aw[0][1], 0.5f * aw[0][2], 0.5f * aw[0][3],
                          0.5f * ab[0]};
@@ -594,50 +595,51 @@ __global__ void __launch_bounds__(256) bwd_bdt_kernel(BwdArgs a) {
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) v[k] += __shfl_xor_sync(0xffffffffu, v[k], off);
   if (lane == 0) {
-    for (int k = 0; k < kWidth + 1; ++k) {
-      if (a.deterministic)
-        a.ws[(int64_t(dense ? bb : 0) * a.D + d) * (kWidth + 1) + k] = v[k];
-      else
-        atomicAdd(a.ws + int64_t(d) * (kWidth + 1) + k, v[k]);
-    }
+    for (int k = 0; k < kWidth + 1; ++k)
+      a.ws[(int64_t(dense ? bb : 0) * a.D + d) * (kWidth + 1) + k] = v[k];
   }
 }
 
-// dweight/dbias from the FP32 sums: rows r = 0 .. R-1 added in that order
-// (loads issued eight rows at a time; the additions keep the row order).
-__global__ void wgrad_finalize_kernel(const float* ws, int64_t R, int D, WgradOut o) {
+// dweight/dbias from R rows of FP32 partial sums ws[r][D][5].  A block takes
+// 32 consecutive values in eight row classes: thread (value v, class c) adds
+// rows c, c + 8, c + 16, ... in increasing order (loads issued eight at a
+// time), then the eight class sums of each value are added in class order --
+// one fixed order for a given R, so the result is bitwise repeatable.
+constexpr int kFinClasses = 8;
+__global__ void __launch_bounds__(32 * kFinClasses) wgrad_finalize_kernel(const float* ws, int64_t R,
+                                                                          int D, WgradOut o) {
   pdl_wait();  // the backward kernel's sums
-  const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= int64_t(D) * (kWidth + 1)) return;
-  const int d = int(i / (kWidth + 1)), k = int(i % (kWidth + 1));
-  const int64_t stride = int64_t(D) * (kWidth + 1);
+  __shared__ float part[kFinClasses][32];
+  const int tx = threadIdx.x & 31, c = threadIdx.x >> 5;
+  const int64_t n_val = int64_t(D) * (kWidth + 1);
+  const int64_t i = int64_t(blockIdx.x) * 32 + tx;
   float s = 0.0f;
-  int64_t r = 0;
-  for (; r + 8 <= R; r += 8) {
-    float v[8];
+  if (i < n_val) {
+    constexpr int64_t kStep = kFinClasses * 8;
+    int64_t r = c;
+    for (; r + kStep - kFinClasses < R; r += kStep) {
+      float v[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) v[j] = __ldcg(ws + (r + j) * stride + i);
+      for (int j = 0; j < 8; ++j) v[j] = __ldcg(ws + (r + j * kFinClasses) * n_val + i);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) s += v[j];
+      for (int j = 0; j < 8; ++j) s += v[j];
+    }
+    for (; r < R; r += kFinClasses) s += __ldcg(ws + r * n_val + i);
   }
-  for (; r < R; ++r) s += __ldcg(ws + r * stride + i);
+  part[c][tx] = s;
+  __syncthreads();
+  if (c != 0 || i >= n_val) return;
+  float t = part[0][tx];
+#pragma unroll
+  for (int j = 1; j < kFinClasses; ++j) t += part[j][tx];
+  const int d = int(i / (kWidth + 1)), k = int(i % (kWidth + 1));
   if (k < kWidth) {
     const int64_t off = d * o.dw_sd + k * o.dw_sk;
-    if (o.dw_f32) static_cast<float*>(o.dw)[off] = s;
-    else static_cast<uint16_t*>(o.dw)[off] = f32_to_bf16(s);
+    if (o.dw_f32) static_cast<float*>(o.dw)[off] = t;
+    else static_cast<uint16_t*>(o.dw)[off] = f32_to_bf16(t);
   } else if (o.db) {
-    o.db[d * o.db_sd] = f32_to_bf16(s);
+    o.db[d * o.db_sd] = f32_to_bf16(t);
   }
-}
-
-// Zeroes the FP32 accumulator of the atomic mode.  Launched the ordinary way,
-// it starts only once all earlier work in the stream has completed; it then
-// releases the backward kernel (launched as its programmatic dependent), which
-// may read its inputs at once and waits for this kernel only before its atomics.
-__global__ void zero_acc_kernel(float* p, int64_t n) {
-  pdl_release();
-  const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i < n) p[i] = 0.0f;
 }
 
 // T == 0: dinit = dfinal (the final state is the initial state), or zero.
@@ -707,11 +709,10 @@ static cudaError_t launch_bwd_act(const BwdArgs& a, const BwdPlan& p, bool pdl,
   return launch_kernel(bwd_bdt_kernel<ACT>, dim3(p.gx), dim3(256), 0, stream, pdl, a);
 }
 
-// Atomic mode: zero_acc_kernel, then the backward as its programmatic
-// dependent (overlapping the zeroing and its own launch), then the finalize as
-// the backward's dependent.  Deterministic mode: the backward launched the
-// ordinary way (nothing to zero; it reads inputs before any wait), then the
-// finalize.
+// The backward kernel (launched as the programmatic dependent of whatever came
+// before it: it waits before reading its inputs) writes one row of partial
+// weight/bias sums per block row; the finalize kernel, its own dependent, adds
+// the rows in a fixed order.  With no tokens, the rows are one zero row.
 cudaError_t launch_bwd(const BwdArgs& a, const BwdPlan& p, int act, const WgradOut& o,
                        int64_t partial_rows, cudaStream_t stream) {
   const int64_t n_acc = int64_t(a.D) * (kWidth + 1);
@@ -724,19 +725,13 @@ cudaError_t launch_bwd(const BwdArgs& a, const BwdPlan& p, int act, const WgradO
     if (a.dinit && n > 0)
       bwd_empty_kernel<<<unsigned((n + 255) / 256), 256, 0, stream>>>(a.dfin, a.dinit, n);
   } else {
-    if (!a.deterministic) {
-      zero_acc_kernel<<<unsigned((n_acc + 255) / 256), 256, 0, stream>>>(a.ws, n_acc);
-      err = cudaGetLastError();
-      if (err != cudaSuccess) return err;
-    }
-    const bool pdl = !a.deterministic;
-    err = act == kActSilu ? launch_bwd_act<kActSilu>(a, p, pdl, stream)
-                          : launch_bwd_act<kActNone>(a, p, pdl, stream);
+    err = act == kActSilu ? launch_bwd_act<kActSilu>(a, p, true, stream)
+                          : launch_bwd_act<kActNone>(a, p, true, stream);
     if (err != cudaSuccess) return err;
   }
-  const int64_t R = (a.deterministic && !empty) ? partial_rows : 1;
-  err = launch_kernel(wgrad_finalize_kernel, dim3(unsigned((n_acc + 255) / 256)), dim3(256), 0,
-                      stream, true, static_cast<const float*>(a.ws), R, a.D, o);
+  const int64_t R = empty ? 1 : partial_rows;
+  err = launch_kernel(wgrad_finalize_kernel, dim3(unsigned((n_acc + 31) / 32)), dim3(32 * kFinClasses),
+                      0, stream, true, static_cast<const float*>(a.ws), R, a.D, o);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }

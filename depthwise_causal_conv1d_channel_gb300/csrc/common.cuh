@@ -520,23 +520,6 @@ __device__ __forceinline__ bool block_rejects_cu_seqlens(const Seqs& s, int* sta
   return bad != 0;
 }
 
-// Before a block stages its weights, each thread prefetches into L2 the first
-// rows it will read -- rows [first - back, first + ahead) of the sequence that
-// holds token `first`, clipped to that sequence -- so the two latencies overlap.
-// Row t of sequence n (tokens [lo, hi)) sits at base + n * seq_step + t * st
-// (dense: seq_step = batch stride - T * token stride; packed: 0).
-__device__ __forceinline__ void prefetch_first_rows(const Seqs& s, const uint16_t* base,
-                                                    int64_t seq_step, int64_t st, int64_t first,
-                                                    int back, int ahead) {
-  if (first >= s.Q) return;
-  const int n = find_seq(s, first);
-  int64_t lo, hi;
-  seq_bounds(s, n, lo, hi);
-  const int64_t t0 = first - back > lo ? first - back : lo;
-  const int64_t t1 = first + ahead < hi ? first + ahead : hi;
-  for (int64_t t = t0; t < t1; ++t) prefetch_l2(base + n * seq_step + t * st);
-}
-
 // Element offsets of token q of sequence n in an activation tensor, for the
 // V channels starting at the thread's channel:  off + n * seq_step + q * st.
 // Dense channel-last: seq_step = batch stride - T * token stride.  Packed, or

@@ -65,8 +65,7 @@ struct BwdArgs {
   Seqs seqs;
   int B, D;
   int64_t seg_len, n_seg;
-  float* ws;              // FP32 weight/bias-gradient sums, [R, D, 5]
-  int deterministic;      // 1: block row r writes ws[r]; 0: atomics into ws[0]
+  float* ws;              // FP32 weight/bias-gradient partial sums, [R, D, 5]: block row r writes ws[r]
   int* status;
 };
 
@@ -95,7 +94,7 @@ struct UpdArgs {
 
 FwdPlan plan_fwd(int kind, int vec_ok, int64_t Q, int D, int64_t rows, int sm_count);
 BwdPlan plan_bwd(int kind, int vec_ok, int64_t Q, int D, int64_t rows, int sm_count);
-// Rows of FP32 partial sums the backward writes in deterministic mode.
+// Rows of FP32 partial sums the backward writes.
 int64_t bwd_partial_rows(const BwdPlan& p, int B, bool packed);
 
 // Resident blocks per SM of the channel-last kernels (SiLU instance), cached.

@@ -13,10 +13,9 @@
 // once per device, on the first call made with that device current.  All calls
 // on a device share the one array: calls whose work overlaps on the GPU (for
 // example on two streams at once) race on it; calls on one stream are ordered
-// and safe.  The backward itself zeroes what must start at zero (the atomic
-// accumulators) and fully overwrites everything else it reads (the
-// deterministic per-block partials), so stale contents from an earlier call
-// are never used.
+// and safe.  The backward fully writes every per-block partial row before the
+// finalize kernel reads it, so stale contents from an earlier call are never
+// used.
 #include <atomic>
 #include <mutex>
 
@@ -24,8 +23,7 @@
 
 namespace {
 
-// 4 MiB: enough for the FP32 sums of D up to ~200 000 channels in atomic mode,
-// or (block rows x D) up to ~200 000 in deterministic mode.
+// 4 MiB: enough for the FP32 partial sums of (block rows x D) up to ~200 000.
 constexpr size_t kScratchBytes = CCC_CONV1D_NOALLOC_SCRATCH_BYTES;
 
 static __device__ __align__(256) float g_bwd_scratch[kScratchBytes / sizeof(float)];

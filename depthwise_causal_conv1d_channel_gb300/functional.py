@@ -83,15 +83,16 @@ def _like_x(t: torch.Tensor, x: torch.Tensor) -> torch.Tensor:
 def _deterministic_mode(has_bias: bool, deterministic: Optional[bool]) -> bool:
     """The cuDNN page's rule: torch.use_deterministic_algorithms selects the
     deterministic dweight route for bias-free calls; with a bias there is none,
-    so raise RuntimeError, or warn and use atomics under warn_only=True.  A
-    per-call deterministic=True/False overrides the global setting."""
+    so raise RuntimeError, or warn and take the default route under
+    warn_only=True.  A per-call deterministic=True/False overrides the global
+    setting.  (The kernels compute both routes as fixed-order sums of per-block
+    partials, so the default route is bitwise repeatable too.)"""
     want = torch.are_deterministic_algorithms_enabled() if deterministic is None else deterministic
     if not want:
         return False
     if not has_bias:
         return True
-    msg = ("causal_conv1d backward with bias has no deterministic dbias route "
-           "(dweight/dbias accumulate with FP32 atomics)")
+    msg = "causal_conv1d backward with bias has no deterministic dbias route"
     if deterministic is None and torch.is_deterministic_algorithms_warn_only_enabled():
         warnings.warn(msg)
         return False

@@ -128,10 +128,12 @@ size_t ccc_conv1d_bwd_workspace_size(const ccc_tensor *x, int deterministic);
  *   dbias           [D] BF16; required when bias is given, else must be NULL.
  *   dinitial_states [S, D, 3] BF16 contiguous or NULL (allowed only with
  *                   initial_states).
- *   deterministic   0: dweight/dbias accumulate with FP32 atomics (not bitwise
- *                   reproducible).  1: unique FP32 per-block partials followed
- *                   by a fixed-order reduction (bitwise reproducible); only for
- *                   bias-free calls, else CCC_ERR_NONDETERMINISTIC.
+ *   deterministic   0 or 1.  The page's rule is kept: 1 (the deterministic
+ *                   route) is declined for calls with a bias
+ *                   (CCC_ERR_NONDETERMINISTIC).  This library computes both
+ *                   modes the same way -- unique FP32 per-block partial sums
+ *                   followed by a fixed-order reduction -- so dweight/dbias
+ *                   are bitwise reproducible in either.
  *   workspace       device buffer of at least
  *                   ccc_conv1d_bwd_workspace_size(x, deterministic) bytes,
  *                   16-byte aligned; contents on entry are ignored.

@@ -44,7 +44,7 @@ def test_malformed_cu_seqlens_sets_status(case, cl, cuda_device):
                              torch.cuda.current_stream())
     assert rc == _abi.CCC_OK  # the host does not read cu_seqlens
     assert _abi.ccc_read_status(st, torch.cuda.current_stream()) == _abi.CCC_ERR_BAD_CU_SEQLENS
-    # backward, deterministic and atomic
+    # backward, deterministic flag on and off
     for det in (False, True):
         dx = torch.empty_like(d.x)
         dw = torch.empty_like(d.weight)

@@ -247,6 +247,21 @@ def test_deterministic_backward_bitwise_repeatable(cuda_device):
             assert torch.equal(res["dx"].view(torch.int16), first["dx"].view(torch.int16))
 
 
+def test_default_route_with_bias_is_bitwise_repeatable(cuda_device):
+    """The default (non-deterministic flag) route also sums fixed per-block
+    partials in a fixed order: dweight and dbias repeat bitwise."""
+    inp = make_inputs(3, 520, 700, seed=29, initial_states=True, grad=True)
+    first = None
+    for _ in range(5):
+        res = gpu_run(inp, cuda_device, deterministic=False)
+        if first is None:
+            first = res
+            check_bwd(inp, res)
+        else:
+            assert torch.equal(res["dw"], first["dw"])
+            assert torch.equal(res["db"], first["db"])
+
+
 def test_deterministic_with_bias_raises(cuda_device):
     inp = make_inputs(1, 16, 8, seed=1, grad=True)
     with pytest.raises(RuntimeError):

@@ -88,7 +88,7 @@ def test_dense_small_forward(cuda_device):
 
 
 def test_dense_state_fwd_bwd(cuda_device):
-    """x stored [4, 2048, 1536] channel-last, initial/final state, atomic dW."""
+    """x stored [4, 2048, 1536] channel-last, initial/final state, default (non-deterministic flag) dW."""
     inp = workloads.dense_state()
     res = run_fwd_bwd(inp, cuda_device, deterministic=False)
     check_sampled(inp, res, sample_channels(1536, 48, 1))
@@ -111,9 +111,9 @@ def test_packed_varlen_deterministic(cuda_device):
         assert torch.equal(r["dw"], dw0)
 
 
-@pytest.mark.parametrize("bias", [True, False], ids=["bias-atomic", "nobias-deterministic"])
+@pytest.mark.parametrize("bias", [True, False], ids=["bias-default", "nobias-deterministic"])
 def test_dense_large(bias, cuda_device):
-    """x stored [8, 8192, 5120] channel-last; with bias (atomic dW/db) or
+    """x stored [8, 8192, 5120] channel-last; with bias (default route) or
     bias-free deterministic."""
     inp = workloads.dense_large(bias=bias)
     res = run_fwd_bwd(inp, cuda_device, deterministic=not bias)

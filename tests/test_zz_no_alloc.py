@@ -33,7 +33,7 @@ CASES = [
 ]
 
 
-@pytest.mark.parametrize("case", CASES, ids=["dense-atomic", "packed-deterministic"])
+@pytest.mark.parametrize("case", CASES, ids=["dense-default", "packed-deterministic"])
 def test_noalloc_backward_matches_workspace_backward_twice(case, cuda_device):
     det = case["det"]
     inp = make_inputs(case["B"], case["D"], case["T"], seed=31, lengths=case["lengths"],
@@ -77,7 +77,7 @@ def test_noalloc_backward_matches_workspace_backward_twice(case, cuda_device):
 
 
 def test_noalloc_rejects_problems_beyond_the_scratch(cuda_device):
-    # atomic mode needs D * 5 FP32 sums: 262144 channels need 5 MiB > 4 MiB
+    # at least one row of D * 5 FP32 partial sums: 262144 channels need 5 MiB > 4 MiB
     D = 262144
     x = torch.zeros(1, 1, D, dtype=torch.bfloat16, device=cuda_device).transpose(1, 2)
     assert _abi.ccc_conv1d_bwd_workspace_size(x, False) > 4 << 20
