@@ -494,52 +494,61 @@ __global__ void __launch_bounds__(kBwdThreads, V == 8 ? CCC_BWD_MIN_BLOCKS : 4)
         for (; m < pro_end; ++m) slow(m);
       }
       const int64_t r0 = m;
-      const int64_t n_main = e > r0 ? (e - r0) / 3 : 0;
+      const int n_main = e > r0 ? int((e - r0) / 3) : 0;  // a segment's groups: below 2^31
       const bool tail = e > r0 && (e - r0) % 3 == 0 && e + kState <= hi && e - a0 >= kState;
-      const int64_t n_total = n_main + (tail ? 1 : 0);
-      const uint16_t* xr0p = xp + (r0 - a0) * xst;
-      const uint16_t* gr0p = gq + (r0 - a0) * gst;
-      auto issue = [&](int64_t k) {
-        const uint32_t s0 = ring_s + uint32_t(int(k % kBwdRing) * 6) * slot;
-        const uint16_t* xm = xr0p + 3 * k * xst;
-        const uint16_t* gm = gr0p + 3 * k * gst;
+      const int n_total = n_main + (tail ? 1 : 0);
+      // running pointers: the next group to issue (rows and ring stage), the
+      // group being taken (stage, dx rows)
+      const uint16_t* xi = xp + (r0 - a0) * xst;
+      const uint16_t* gi = gq + (r0 - a0) * gst;
+      int ki = 0, si = 0;  // next group to issue, its stage
+      auto issue_next = [&]() {
+        if (ki < n_total) {
+          const uint32_t s0 = ring_s + uint32_t(si * 6) * slot;
 #pragma unroll
-        for (int u = 0; u < 3; ++u) {
-          cp_async<RB>(s0 + uint32_t(2 * u) * slot, xm + u * xst);
-          cp_async<RB>(s0 + uint32_t(2 * u + 1) * slot, gm + u * gst);
+          for (int u = 0; u < 3; ++u) {
+            cp_async<RB>(s0 + uint32_t(2 * u) * slot, xi + u * xst);
+            cp_async<RB>(s0 + uint32_t(2 * u + 1) * slot, gi + u * gst);
+          }
+          xi += 3 * xst;
+          gi += 3 * gst;
         }
-      };
-      auto take = [&](int64_t k, Raw (&xr)[3], Raw (&gr)[3]) {
-        if (k + kBwdRing - 1 < n_total) issue(k + kBwdRing - 1);
+        ++ki;
+        si = si + 1 == kBwdRing ? 0 : si + 1;
         cp_async_commit();
-        cp_async_wait<kBwdRing - 1>();  // group k has landed
-        const char* s0 = ring + size_t(int(k % kBwdRing) * 6) * slot;
+      };
+      int st = 0;  // stage of the group being taken
+      auto take = [&](Raw (&xr)[3], Raw (&gr)[3]) {
+        issue_next();
+        cp_async_wait<kBwdRing - 1>();  // the group being taken has landed
+        const char* s0 = ring + size_t(st * 6) * slot;
 #pragma unroll
         for (int u = 0; u < 3; ++u) {
           xr[u] = *reinterpret_cast<const Raw*>(s0 + size_t(2 * u) * slot);
           gr[u] = *reinterpret_cast<const Raw*>(s0 + size_t(2 * u + 1) * slot);
         }
+        st = st + 1 == kBwdRing ? 0 : st + 1;
       };
 #pragma unroll
-      for (int k = 0; k < kBwdRing - 1; ++k) {
-        if (k < n_total) issue(k);
-        cp_async_commit();
-      }
+      for (int j = 0; j < kBwdRing - 1; ++j) issue_next();
       Raw xr[3], gr[3];
-      int64_t k = 0;
+      int k = 0;
+      uint16_t* drow = dp + (r0 - kState - a0) * dst;  // dx rows of group k
       if (head) {
-        take(0, xr, gr);
-        group(Yes{}, No{}, xr, gr, dp);
+        take(xr, gr);
+        group(Yes{}, No{}, xr, gr, drow);
         k = 1;
+        drow += 3 * dst;
       }
       for (; k < n_main; ++k) {
-        take(k, xr, gr);
-        group(Yes{}, Yes{}, xr, gr, dp + (r0 + 3 * k - kState - a0) * dst);
+        take(xr, gr);
+        group(Yes{}, Yes{}, xr, gr, drow);
+        drow += 3 * dst;
       }
-      m = r0 + 3 * n_main;
+      m = r0 + 3 * int64_t(n_main);
       if (tail) {
-        take(n_main, xr, gr);
-        group(No{}, Yes{}, xr, gr, dp + (m - kState - a0) * dst);
+        take(xr, gr);
+        group(No{}, Yes{}, xr, gr, drow);
       } else {
         for (; m < m_end; ++m) slow(m);
       }
@@ -603,7 +612,7 @@ __global__ void __launch_bounds__(256) bwd_bdt_kernel(BwdArgs a) {
 // dweight/dbias from R rows of FP32 partial sums ws[r][D][5].  A block takes
 // 32 consecutive values in eight row classes: thread (value v, class c) adds
 // rows c, c + 8, c + 16, ... in increasing order (loads issued eight at a
-// time), then the eight class sums of each value are added in class order --
+// time, so up to 64 rows cost one round trip), then the eight class sums of each value are added in class order --
 // one fixed order for a given R, so the result is bitwise repeatable.
 constexpr int kFinClasses = 8;
 __global__ void __launch_bounds__(32 * kFinClasses) wgrad_finalize_kernel(const float* ws, int64_t R,
@@ -616,15 +625,17 @@ __global__ void __launch_bounds__(32 * kFinClasses) wgrad_finalize_kernel(const 
   float s = 0.0f;
   if (i < n_val) {
     constexpr int64_t kStep = kFinClasses * 8;
-    int64_t r = c;
-    for (; r + kStep - kFinClasses < R; r += kStep) {
+    for (int64_t r0 = c; r0 < R; r0 += kStep) {
       float v[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) v[j] = __ldcg(ws + (r + j * kFinClasses) * n_val + i);
+      for (int j = 0; j < 8; ++j) {
+        const int64_t r = r0 + j * kFinClasses;
+        v[j] = r < R ? __ldcg(ws + r * n_val + i) : 0.0f;
+      }
 #pragma unroll
-      for (int j = 0; j < 8; ++j) s += v[j];
+      for (int j = 0; j < 8; ++j)
+        if (r0 + j * kFinClasses < R) s += v[j];
     }
-    for (; r < R; r += kFinClasses) s += __ldcg(ws + r * n_val + i);
   }
   part[c][tx] = s;
   __syncthreads();
