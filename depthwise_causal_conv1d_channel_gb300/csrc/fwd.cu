@@ -203,9 +203,14 @@ __global__ void __launch_bounds__(kFwdThreads, 3) fwd_clv_kernel(FwdArgs a) {
     auto issue = [&](int k) {
       const uint32_t s0 = ring_s + uint32_t((k % kFwdRing) * G) * slot;
       const uint16_t* xm = xp + int64_t(k) * G * xst;
+      if (k * G + G <= n_tok) {
 #pragma unroll
-      for (int u = 0; u < G; ++u)
-        if (k * G + u < n_tok) cp_async<RB>(s0 + uint32_t(u) * slot, xm + u * xst);
+        for (int u = 0; u < G; ++u) cp_async<RB>(s0 + uint32_t(u) * slot, xm + u * xst);
+      } else {
+#pragma unroll
+        for (int u = 0; u < G; ++u)
+          if (k * G + u < n_tok) cp_async<RB>(s0 + uint32_t(u) * slot, xm + u * xst);
+      }
     };
 #pragma unroll
     for (int k = 0; k < kFwdRing - 1; ++k) {
