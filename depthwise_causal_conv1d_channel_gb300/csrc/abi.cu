@@ -65,6 +65,7 @@ bool overlaps(const ccc_tensor* a, const ccc_tensor* b) {
 
 // No two index tuples of the tensor share an element (needed for outputs).
 bool self_disjoint(const ccc_tensor* t) {
+  if (numel(t) == 0) return true;  // no elements, nothing to share
   int idx[3];
   int n = 0;
   for (int i = 0; i < t->ndim; ++i)
@@ -482,12 +483,24 @@ ccc_status ccc_conv1d_bwd(const ccc_tensor* x, const ccc_tensor* weight, const c
   return ccc::launch_bwd(a, p, activation, o, R, stream) == cudaSuccess ? CCC_OK : CCC_ERR_CUDA;
 }
 
+// Same data pointer, shape and strides: the call updates in place.
+static bool same_view(const ccc_tensor* a, const ccc_tensor* b) {
+  if (a->data != b->data || a->ndim != b->ndim || a->dtype != b->dtype) return false;
+  for (int i = 0; i < a->ndim; ++i)
+    if (a->shape[i] != b->shape[i] || (a->shape[i] > 1 && a->stride[i] != b->stride[i])) return false;
+  return true;
+}
+
 ccc_status ccc_conv1d_update(const ccc_tensor* x, const ccc_tensor* conv_state,
                              const ccc_tensor* weight, const ccc_tensor* bias,
                              const ccc_tensor* out, int activation, cudaStream_t stream) {
-  if (!well_formed(x, 2) || x->dtype != CCC_BF16 || x->shape[1] < 1) return CCC_ERR_INVALID_ARG;
-  if (x->shape[0] > INT32_MAX || x->shape[1] > INT32_MAX) return CCC_ERR_UNSUPPORTED;
+  if (!x || (x->ndim != 2 && x->ndim != 3)) return CCC_ERR_INVALID_ARG;
+  const bool multi = x->ndim == 3;
+  if (!well_formed(x, x->ndim) || x->dtype != CCC_BF16 || x->shape[1] < 1) return CCC_ERR_INVALID_ARG;
+  if (x->shape[0] > INT32_MAX || x->shape[1] > INT32_MAX || (multi && x->shape[2] > INT32_MAX))
+    return CCC_ERR_UNSUPPORTED;
   const int B = int(x->shape[0]), D = int(x->shape[1]);
+  const int L = multi ? int(x->shape[2]) : 1;
   if (D > 1 && x->stride[1] != 1) return CCC_ERR_UNSUPPORTED;
   if (activation != CCC_ACT_NONE && activation != CCC_ACT_SILU) return CCC_ERR_INVALID_ARG;
   if (!state_ok(conv_state, B, D)) return CCC_ERR_INVALID_ARG;
@@ -499,26 +512,36 @@ ccc_status ccc_conv1d_update(const ccc_tensor* x, const ccc_tensor* conv_state,
       return CCC_ERR_INVALID_ARG;
     if (weight->dtype == CCC_F32) return CCC_ERR_UNSUPPORTED;
   }
-  if (!well_formed(out, 2) || out->dtype != CCC_BF16 || !shape_is(out, B, D)) return CCC_ERR_INVALID_ARG;
+  if (!out || out->ndim != x->ndim || !well_formed(out, out->ndim) || out->dtype != CCC_BF16 ||
+      !shape_is(out, B, D, multi ? L : -1))
+    return CCC_ERR_INVALID_ARG;
   if ((D > 1 && out->stride[1] != 1) || !self_disjoint(out)) return CCC_ERR_UNSUPPORTED;
   for (const ccc_tensor* in : {conv_state, weight, bias})
     if (in && overlaps(out, in)) return CCC_ERR_ALIAS;
   if (overlaps(x, conv_state)) return CCC_ERR_ALIAS;
+  // out either is x (in place: every element is read before its thread writes
+  // it) or stays clear of it (another thread's x otherwise)
+  if (overlaps(out, x) && !same_view(out, x)) return CCC_ERR_ALIAS;
+  if (B == 0 || L == 0) return CCC_OK;  // nothing to compute; the state is unchanged
 
   ccc::UpdArgs a{};
   a.x = static_cast<const uint16_t*>(x->data);
   a.x_sb = B > 1 ? x->stride[0] : 0;
+  a.x_sl = multi && L > 1 ? x->stride[2] : 0;
   a.state = static_cast<uint16_t*>(conv_state->data);
   a.out = static_cast<uint16_t*>(out->data);
   a.o_sb = B > 1 ? out->stride[0] : 0;
+  a.o_sl = multi && L > 1 ? out->stride[2] : 0;
   a.wr = weight_ref(weight, bias);
   a.B = B;
   a.D = D;
+  a.L = L;
   // vectors of V channels: 2V-byte aligned rows; a state block of V channels
   // is 6V bytes (16-byte alignment for V = 8, 8 for V = 4)
   auto fits = [&](int V) {
     return D % V == 0 && aligned(x->data, 2 * V) && aligned(out->data, 2 * V) &&
-           aligned(conv_state->data, V == 8 ? 16 : 8) && a.x_sb % V == 0 && a.o_sb % V == 0;
+           aligned(conv_state->data, V == 8 ? 16 : 8) && a.x_sb % V == 0 && a.o_sb % V == 0 &&
+           a.x_sl % V == 0 && a.o_sl % V == 0;
   };
   const int vec = fits(8) ? 8 : fits(4) ? 4 : 1;
   return ccc::launch_update(a, vec, activation, stream) == cudaSuccess ? CCC_OK : CCC_ERR_CUDA;

@@ -82,13 +82,14 @@ struct FwdPlan {
 using BwdPlan = FwdPlan;
 
 struct UpdArgs {
-  const uint16_t* x;  // [B, D], channel stride 1
-  int64_t x_sb;
+  const uint16_t* x;  // [B, D, L], channel stride 1
+  int64_t x_sb, x_sl;
   uint16_t* state;    // [B, D, 3] contiguous
-  uint16_t* out;      // [B, D], channel stride 1
-  int64_t o_sb;
+  uint16_t* out;      // [B, D, L], channel stride 1
+  int64_t o_sb, o_sl;
   WeightRef wr;
   int B, D;
+  int L;              // tokens per row, >= 1
 };
 
 

@@ -1,9 +1,13 @@
-// Single-token update (cuDNN frontend docs, "Causal Conv1d" page: the returned
+// Decode update (cuDNN frontend docs, "Causal Conv1d" page: the returned
 // width-four final_states[B, D, 3] feed causal_conv1d_update, which mutates
-// that state in place).
+// that state in place; the commonly consumed causal-conv1d interface the page
+// matches also takes L > 1 new tokens per row).  For each row, token by token:
 //
-//   out[b,d]   = act(bias[d] + w0*s0 + w1*s1 + w2*s2 + w3*x[b,d])
-//   state[b,d] = [s1, s2, x[b,d]]      (bitwise)
+//   out[b,d,l] = act(bias[d] + w0*s0 + w1*s1 + w2*s2 + w3*x[b,d,l])
+//   state[b,d] <- [s1, s2, x[b,d,l]]      (bitwise)
+//
+// which is the forward over the L tokens with the state as initial state and
+// the new state as its final state, evaluated in the same order (bitwise equal).
 //
 // A thread owns V consecutive channels of one or more batch rows.  With eight
 // channels and a contiguous weight, each warp moves the state of its 256
@@ -17,8 +21,9 @@ namespace ccc {
 // Block (tx, ty): threadIdx.x over groups of V channels, threadIdx.y over
 // groups of R batch rows.  The block stages its channels' weights once; each
 // thread issues the loads of all its R rows before computing any of them.
-template <int V, int ACT, int R>
+template <int V, int ACT, int R, bool MULTI>
 __global__ void __launch_bounds__(256) update_kernel(UpdArgs a) {
+  const int L = MULTI ? a.L : 1;
   pdl_wait();     // the state and x may come from the previous kernel (the previous step)
   pdl_release();
   using VT = Vec<V>;
@@ -46,21 +51,30 @@ __global__ void __launch_bounds__(256) update_kernel(UpdArgs a) {
 #pragma unroll
     for (int r = 0; r < R; ++r) {
       if (b0 + r >= a.B) break;
-      float2 xc[H], y[H];
-      VT::unpack2(xr[r], xc);
+      const uint16_t* xrow = a.x + int64_t(b0 + r) * a.x_sb + d0;
+      uint16_t* orow = a.out + int64_t(b0 + r) * a.o_sb + d0;
+      typename VT::Raw cur = xr[r];
+      for (int l = 0; l < L; ++l) {
+        // the next token's load is in flight while this one is computed
+        typename VT::Raw nxt = cur;
+        if (l + 1 < L) nxt = VT::ld(xrow + int64_t(l + 1) * a.x_sl);
+        float2 xc[H], y[H];
+        VT::unpack2(cur, xc);
 #pragma unroll
-      for (int h = 0; h < H; ++h) {
-        float2 p = b[h];
-        p = ffma2(w[h][0], win[r][0][h], p);
-        p = ffma2(w[h][1], win[r][1][h], p);
-        p = ffma2(w[h][2], win[r][2][h], p);
-        p = ffma2(w[h][3], xc[h], p);
-        y[h] = act_fwd2<ACT>(p);
-        win[r][0][h] = win[r][1][h];
-        win[r][1][h] = win[r][2][h];
-        win[r][2][h] = xc[h];
+        for (int h = 0; h < H; ++h) {
+          float2 p = b[h];
+          p = ffma2(w[h][0], win[r][0][h], p);
+          p = ffma2(w[h][1], win[r][1][h], p);
+          p = ffma2(w[h][2], win[r][2][h], p);
+          p = ffma2(w[h][3], xc[h], p);
+          y[h] = act_fwd2<ACT>(p);
+          win[r][0][h] = win[r][1][h];
+          win[r][1][h] = win[r][2][h];
+          win[r][2][h] = xc[h];
+        }
+        VT::st(orow + int64_t(l) * a.o_sl, VT::pack2(y));
+        cur = nxt;
       }
-      VT::st(a.out + int64_t(b0 + r) * a.o_sb + d0, VT::pack2(y));
       store_state2<V>(a.state + (int64_t(b0 + r) * a.D + d0) * kState, win[r]);
     }
   } else {
@@ -78,21 +92,29 @@ __global__ void __launch_bounds__(256) update_kernel(UpdArgs a) {
 #pragma unroll
     for (int r = 0; r < R; ++r) {
       if (b0 + r >= a.B) break;
-      float xc[V], y[V];
-      VT::unpack(xr[r], xc);
+      const uint16_t* xrow = a.x + int64_t(b0 + r) * a.x_sb + d0;
+      uint16_t* orow = a.out + int64_t(b0 + r) * a.o_sb + d0;
+      typename VT::Raw cur = xr[r];
+      for (int l = 0; l < L; ++l) {
+        typename VT::Raw nxt = cur;
+        if (l + 1 < L) nxt = VT::ld(xrow + int64_t(l + 1) * a.x_sl);
+        float xc[V], y[V];
+        VT::unpack(cur, xc);
 #pragma unroll
-      for (int c = 0; c < V; ++c) {
-        float p = b[c];
-        p = fmaf(w[c][0], win[r][0][c], p);
-        p = fmaf(w[c][1], win[r][1][c], p);
-        p = fmaf(w[c][2], win[r][2][c], p);
-        p = fmaf(w[c][3], xc[c], p);
-        y[c] = act_fwd<ACT>(p);
-        win[r][0][c] = win[r][1][c];
-        win[r][1][c] = win[r][2][c];
-        win[r][2][c] = xc[c];
+        for (int c = 0; c < V; ++c) {
+          float p = b[c];
+          p = fmaf(w[c][0], win[r][0][c], p);
+          p = fmaf(w[c][1], win[r][1][c], p);
+          p = fmaf(w[c][2], win[r][2][c], p);
+          p = fmaf(w[c][3], xc[c], p);
+          y[c] = act_fwd<ACT>(p);
+          win[r][0][c] = win[r][1][c];
+          win[r][1][c] = win[r][2][c];
+          win[r][2][c] = xc[c];
+        }
+        VT::st(orow + int64_t(l) * a.o_sl, VT::pack(y));
+        cur = nxt;
       }
-      VT::st(a.out + int64_t(b0 + r) * a.o_sb + d0, VT::pack(y));
       store_state<V>(a.state + (int64_t(b0 + r) * a.D + d0) * kState, win[r]);
     }
   }
@@ -109,7 +131,7 @@ __global__ void __launch_bounds__(256) update_kernel(UpdArgs a) {
 // eight distinct 16-byte bank groups, so the exchange is conflict-free).
 // Read with per-lane 48-byte strides instead, every load instruction would
 // touch twice the sectors it uses.
-template <int ACT, int TY, int R>
+template <int ACT, int TY, int R, bool MULTI>
 __global__ void __launch_bounds__(32 * TY) update_w8_kernel(UpdArgs a) {
   pdl_wait();
   pdl_release();
@@ -144,6 +166,7 @@ __global__ void __launch_bounds__(32 * TY) update_w8_kernel(UpdArgs a) {
       for (int j = 0; j < kState; ++j)
         if (lane + 32 * j < n_chunks) sbuf[wy][r][lane + 32 * j] = sr[r][j];
   __syncwarp();
+  if constexpr (!MULTI) {
 #pragma unroll
   for (int r = 0; r < R; ++r) {
     if (b0 + r >= a.B || !valid) continue;
@@ -184,6 +207,55 @@ __global__ void __launch_bounds__(32 * TY) update_w8_kernel(UpdArgs a) {
 #pragma unroll
     for (int j = 0; j < kState; ++j) sbuf[wy][r][kState * lane + j] = u.q[j];
   }
+  } else {
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    if (b0 + r >= a.B || !valid) continue;
+    union { uint4 q[kState]; uint16_t h[3 * 8]; } u;
+#pragma unroll
+    for (int j = 0; j < kState; ++j) u.q[j] = sbuf[wy][r][kState * lane + j];
+    float2 win[kState][4];
+#pragma unroll
+    for (int i = 0; i < kState; ++i)
+#pragma unroll
+      for (int h = 0; h < 4; ++h)
+        win[i][h] = make_float2(bf16_to_f32(u.h[(2 * h) * 3 + i]), bf16_to_f32(u.h[(2 * h + 1) * 3 + i]));
+    const uint16_t* xrow = a.x + int64_t(b0 + r) * a.x_sb + d0;
+    uint16_t* orow = a.out + int64_t(b0 + r) * a.o_sb + d0;
+    uint4 cur = xr[r];
+    for (int l = 0; l < a.L; ++l) {
+      // the next token's load is in flight while this one is computed
+      uint4 nxt = cur;
+      if (l + 1 < a.L) nxt = Vec<8>::ld(xrow + int64_t(l + 1) * a.x_sl);
+      float2 xc[4], y[4];
+      Vec<8>::unpack2(cur, xc);
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        float2 p = bias[h];
+        p = ffma2(w[h][0], win[0][h], p);
+        p = ffma2(w[h][1], win[1][h], p);
+        p = ffma2(w[h][2], win[2][h], p);
+        p = ffma2(w[h][3], xc[h], p);
+        y[h] = act_fwd2<ACT>(p);
+        win[0][h] = win[1][h];
+        win[1][h] = win[2][h];
+        win[2][h] = xc[h];
+      }
+      Vec<8>::st(orow + int64_t(l) * a.o_sl, Vec<8>::pack2(y));
+      cur = nxt;
+    }
+    // new state: the last three extended inputs, BF16 values held exactly in FP32
+#pragma unroll
+    for (int i = 0; i < kState; ++i)
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        u.h[(2 * h) * 3 + i] = f32_to_bf16(win[i][h].x);
+        u.h[(2 * h + 1) * 3 + i] = f32_to_bf16(win[i][h].y);
+      }
+#pragma unroll
+    for (int j = 0; j < kState; ++j) sbuf[wy][r][kState * lane + j] = u.q[j];
+  }
+  }
   __syncwarp();
 #pragma unroll
   for (int r = 0; r < R; ++r) {
@@ -200,7 +272,9 @@ static cudaError_t launch_update_w8(const UpdArgs& a, cudaStream_t stream) {
   constexpr int TY = 4, R = 1;
   const int64_t groups = a.D / 8;
   dim3 grid(unsigned((groups + 31) / 32), unsigned((a.B + int64_t(TY) * R - 1) / (int64_t(TY) * R)));
-  return launch_kernel(update_w8_kernel<ACT, TY, R>, grid, dim3(32, TY), 0, stream, true, a);
+  if (a.L == 1)
+    return launch_kernel(update_w8_kernel<ACT, TY, R, false>, grid, dim3(32, TY), 0, stream, true, a);
+  return launch_kernel(update_w8_kernel<ACT, TY, R, true>, grid, dim3(32, TY), 0, stream, true, a);
 }
 
 #ifndef CCC_UPDATE_ROWS
@@ -220,14 +294,19 @@ cudaError_t launch_update(const UpdArgs& a, int vec, int act, cudaStream_t strea
   dim3 block(tx, ty);
   dim3 grid(unsigned((groups + tx - 1) / tx),
             unsigned((a.B + int64_t(ty) * kUpdateRows - 1) / (int64_t(ty) * kUpdateRows)));
-  if (vec == 8)
-    return act == kActSilu ? launch_kernel(update_kernel<8, kActSilu, kUpdateRows>, grid, block, 0, stream, true, a)
-                           : launch_kernel(update_kernel<8, kActNone, kUpdateRows>, grid, block, 0, stream, true, a);
-  if (vec == 4)
-    return act == kActSilu ? launch_kernel(update_kernel<4, kActSilu, kUpdateRows>, grid, block, 0, stream, true, a)
-                           : launch_kernel(update_kernel<4, kActNone, kUpdateRows>, grid, block, 0, stream, true, a);
-  return act == kActSilu ? launch_kernel(update_kernel<1, kActSilu, kUpdateRows>, grid, block, 0, stream, true, a)
-                         : launch_kernel(update_kernel<1, kActNone, kUpdateRows>, grid, block, 0, stream, true, a);
+  const bool multi = a.L > 1;
+  auto go = [&](auto kernel) { return launch_kernel(kernel, grid, block, 0, stream, true, a); };
+  constexpr int R = kUpdateRows;
+  if (vec == 8) {
+    if (act == kActSilu) return multi ? go(update_kernel<8, kActSilu, R, true>) : go(update_kernel<8, kActSilu, R, false>);
+    return multi ? go(update_kernel<8, kActNone, R, true>) : go(update_kernel<8, kActNone, R, false>);
+  }
+  if (vec == 4) {
+    if (act == kActSilu) return multi ? go(update_kernel<4, kActSilu, R, true>) : go(update_kernel<4, kActSilu, R, false>);
+    return multi ? go(update_kernel<4, kActNone, R, true>) : go(update_kernel<4, kActNone, R, false>);
+  }
+  if (act == kActSilu) return multi ? go(update_kernel<1, kActSilu, R, true>) : go(update_kernel<1, kActSilu, R, false>);
+  return multi ? go(update_kernel<1, kActNone, R, true>) : go(update_kernel<1, kActNone, R, false>);
 }
 
 }  // namespace ccc

@@ -174,12 +174,22 @@ def causal_conv1d(x: torch.Tensor, weight: torch.Tensor, bias: Optional[torch.Te
 def causal_conv1d_update(x: torch.Tensor, conv_state: torch.Tensor, weight: torch.Tensor,
                          bias: Optional[torch.Tensor] = None, activation: Optional[str] = "silu",
                          out: Optional[torch.Tensor] = None) -> torch.Tensor:
-    """One decode step: x [B, D] is the new token; conv_state [B, D, 3] (the
-    layout final_states uses) is read and mutated in place to [s1, s2, x].
-    Returns out [B, D]."""
+    """Decode step(s): x [B, D] is the new token, or x [B, D, L] the next L
+    tokens of every row; conv_state [B, D, 3] (the layout final_states uses) is
+    read and mutated in place, token by token, to the last three extended
+    inputs.  Returns out shaped like x.  The kernels read each token's D
+    channels contiguously: a [B, D, L] x whose channel stride is not 1 is
+    restrided first (a copy), and a new out is allocated with channel stride 1
+    ([B, L, D] storage seen as [B, D, L])."""
     act = _activation_code(activation)
+    if x.dim() == 3 and x.shape[1] > 1 and x.stride(1) != 1:
+        x = x.transpose(1, 2).contiguous().transpose(1, 2)
     if out is None:
-        out = torch.empty_like(x, memory_format=torch.contiguous_format)
+        if x.dim() == 3:
+            out = torch.empty(x.shape[0], x.shape[2], x.shape[1], dtype=x.dtype,
+                              device=x.device).transpose(1, 2)
+        else:
+            out = torch.empty_like(x, memory_format=torch.contiguous_format)
     st = _abi.ccc_conv1d_update(x, conv_state, weight, bias, out, act,
                                 torch.cuda.current_stream(x.device))
     _raise(st, "causal_conv1d_update")

@@ -183,18 +183,25 @@ ccc_status ccc_conv1d_bwd_noalloc(const ccc_tensor *x, const ccc_tensor *weight,
                                   int deterministic, int *d_status, cudaStream_t stream);
 
 /*
- * Single-token update (cuDNN "Causal Conv1d" page, the paragraph on passing
- * final_states to causal_conv1d_update, which mutates that state in place).
+ * Decode update (cuDNN "Causal Conv1d" page, the paragraph on passing
+ * final_states to causal_conv1d_update, which mutates that state in place;
+ * the page's "commonly consumed causal-conv1d interface" also takes several
+ * new tokens per row).
  *
- *   x           [B, D] BF16, stride[1] == 1: this step's token.
- *   conv_state  [B, D, 3] BF16 contiguous, read and overwritten in place with
- *               [s1, s2, x] (bitwise): the layout final_states uses.
+ *   x           [B, D] BF16 (one token per row) or [B, D, L] BF16 (L >= 0 tokens
+ *               per row, any token stride), stride[1] == 1.
+ *   conv_state  [B, D, 3] BF16 contiguous, read and overwritten in place: after
+ *               each token, [s1, s2, x] (bitwise): the layout final_states uses.
  *   weight      [D, 4] as in ccc_conv1d_fwd;  bias [D] BF16 or NULL.
- *   out         [B, D] BF16, stride[1] == 1:
+ *   out         shaped like x, stride[1] == 1; for each token in order:
  *               act(bias + w0*s0 + w1*s1 + w2*s2 + w3*x).
  *
- * out must not overlap conv_state, weight or bias; x must not overlap
- * conv_state (CCC_ERR_ALIAS).
+ * The result equals ccc_conv1d_fwd over the L tokens with conv_state as the
+ * initial state and the new state as the final state, bitwise.  L == 0 (or
+ * B == 0) computes nothing and leaves the state unchanged.  out may be x itself
+ * (same pointer, shape and strides: the update is then in place) but must not
+ * otherwise overlap it; out must not overlap conv_state, weight or bias, and x
+ * must not overlap conv_state (CCC_ERR_ALIAS).
  */
 ccc_status ccc_conv1d_update(const ccc_tensor *x, const ccc_tensor *conv_state,
                              const ccc_tensor *weight, const ccc_tensor *bias,

@@ -194,6 +194,32 @@ def test_update_rejects_bad_arguments_on_host():
     assert upd(T(0, BF16, (4, D_), (1, 4)), st, w, b, out) == _abi.CCC_ERR_UNSUPPORTED
 
 
+def test_multi_token_update_host_checks():
+    """x [B, D, L]: out must have x's rank and shape, channel stride 1, and may
+    be x itself but not a shifted view of it; L == 0 is a no-op that touches
+    no memory (the fake pointers here are never dereferenced)."""
+    r = lambda d: None if d is None else ctypes.byref(d)
+    upd = lambda *a, act=1: _abi.lib.ccc_conv1d_update(*[r(d) for d in a], act, None)
+    L = 5
+    cl3 = lambda off, Ln=L: T(off, BF16, (4, D_, Ln), (Ln * D_, 1, D_))  # [B, L, D] storage
+    st = T(MB, BF16, (4, D_, 3))
+    w = T(2 * MB, BF16, (D_, 4))
+    b = T(3 * MB, BF16, (D_,))
+    x = cl3(0)
+    # rank or shape mismatch between x and out
+    assert upd(x, st, w, b, T(4 * MB, BF16, (4, D_))) == _abi.CCC_ERR_INVALID_ARG
+    assert upd(x, st, w, b, cl3(4 * MB, L + 1)) == _abi.CCC_ERR_INVALID_ARG
+    # time-contiguous x or out (channel stride != 1) is declined: the wrapper restrides
+    assert upd(T(0, BF16, (4, D_, L)), st, w, b, cl3(4 * MB)) == _abi.CCC_ERR_UNSUPPORTED
+    assert upd(x, st, w, b, T(4 * MB, BF16, (4, D_, L))) == _abi.CCC_ERR_UNSUPPORTED
+    # out a shifted view of x: another thread's tokens would be overwritten
+    assert upd(x, st, w, b, cl3(2 * D_)) == _abi.CCC_ERR_ALIAS
+    # out on the state
+    assert upd(x, st, w, b, cl3(MB)) == _abi.CCC_ERR_ALIAS
+    # no tokens: nothing to do, nothing touched
+    assert upd(cl3(0, 0), st, w, b, cl3(4 * MB, 0)) == _abi.CCC_OK
+
+
 def test_python_api_rejects_seq_idx_and_bad_activation():
     import torch
 
