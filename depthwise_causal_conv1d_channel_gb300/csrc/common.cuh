@@ -99,18 +99,26 @@ __device__ __forceinline__ float2 fmul2(float2 a, float2 b) { return __fmul2_rn(
 __device__ __forceinline__ float2 fadd2(float2 a, float2 b) { return __fadd2_rn(a, b); }
 __device__ __forceinline__ float2 splat2(float v) { return make_float2(v, v); }
 
+// The same operations as two scalar instructions (bitwise the same results).
+// A paired instruction holds the FMA pipe twice as long as a scalar one, so
+// pairing only saves issue slots; the forward's short dependent chains
+// measured faster split, the backward paired.
+__device__ __forceinline__ float2 ffma2_split(float2 a, float2 b, float2 c) {
+  return make_float2(__fmaf_rn(a.x, b.x, c.x), __fmaf_rn(a.y, b.y, c.y));
+}
+
 // BF16 pair (one 32-bit word, low half first) <-> float2.
 __device__ __forceinline__ float2 unpack_bf16x2(uint32_t u) { return make_float2(bf16_lo(u), bf16_hi(u)); }
 __device__ __forceinline__ uint32_t pack_bf16x2(float2 v) { return pack_bf16x2(v.x, v.y); }
 
 // Pair forms: the same operations, in the same order, as act_fwd / act_bwd.
-template <int ACT>
+template <int ACT, bool SPLIT = false>
 __device__ __forceinline__ float2 act_fwd2(float2 h) {
   if constexpr (ACT == kActSilu) {
     const float2 t = make_float2(tanh_approx(h.x), tanh_approx(h.y));
-    return ffma2(h, t, h);
+    return SPLIT ? ffma2_split(h, t, h) : ffma2(h, t, h);
   } else {
-    return fadd2(h, h);
+    return make_float2(h.x + h.x, h.y + h.y);
   }
 }
 

@@ -131,7 +131,8 @@ __global__ void __launch_bounds__(256) fwd_cl_kernel(FwdArgs a) {
 }
 
 // Channel-last x with vectors of V = 4 channels, computed as two channel
-// pairs (the fast path; eight channels a thread measured no faster).  Same
+// pairs of scalar instructions (the fast path; eight channels a thread
+// measured no faster, paired instructions 1-2% slower).  Same
 // walk as fwd_walk, specialised: the three-token window lives in three register
 // slots that rotate (the newest token overwrites the oldest slot), so full
 // groups of kFwdGroup tokens (a multiple of three) need no register copies.
@@ -253,11 +254,11 @@ __global__ void __launch_bounds__(kFwdThreads, 3) fwd_clv_kernel(FwdArgs a) {
 #pragma unroll
       for (int h = 0; h < H; ++h) {
         float2 p = b[h];
-        p = ffma2(w[h][0], W[J][h], p);
-        p = ffma2(w[h][1], W[(J + 1) % 3][h], p);
-        p = ffma2(w[h][2], W[(J + 2) % 3][h], p);
-        p = ffma2(w[h][3], cur[h], p);
-        y[h] = act_fwd2<ACT>(p);
+        p = ffma2_split(w[h][0], W[J][h], p);
+        p = ffma2_split(w[h][1], W[(J + 1) % 3][h], p);
+        p = ffma2_split(w[h][2], W[(J + 2) % 3][h], p);
+        p = ffma2_split(w[h][3], cur[h], p);
+        y[h] = act_fwd2<ACT, true>(p);
         W[J][h] = cur[h];
       }
       VT::st(dst, VT::pack2(y));
@@ -269,11 +270,11 @@ __global__ void __launch_bounds__(kFwdThreads, 3) fwd_clv_kernel(FwdArgs a) {
 #pragma unroll
       for (int h = 0; h < H; ++h) {
         float2 p = b[h];
-        p = ffma2(w[h][0], W[0][h], p);
-        p = ffma2(w[h][1], W[1][h], p);
-        p = ffma2(w[h][2], W[2][h], p);
-        p = ffma2(w[h][3], cur[h], p);
-        y[h] = act_fwd2<ACT>(p);
+        p = ffma2_split(w[h][0], W[0][h], p);
+        p = ffma2_split(w[h][1], W[1][h], p);
+        p = ffma2_split(w[h][2], W[2][h], p);
+        p = ffma2_split(w[h][3], cur[h], p);
+        y[h] = act_fwd2<ACT, true>(p);
         W[0][h] = W[1][h];
         W[1][h] = W[2][h];
         W[2][h] = cur[h];
