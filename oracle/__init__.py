@@ -18,7 +18,8 @@ Two layers:
 
 Shapes: ``x`` / ``g`` are the logical ``[B, D, T]`` tensor (copied to
 contiguous here); packed calls have ``B == 1`` and ``cu_seqlens`` of ``N + 1``
-int32 offsets; ``weight`` is ``[D, 4]``; states are ``[B or N, D, 3]``.
+int32 offsets; ``weight`` is ``[D, W]`` with a width W in 2..4 (4 on the
+page's optimized route); states are ``[B or N, D, W - 1]``.
 What the core computes, and the page passages it follows, is written at the
 top of ``conv1d_oracle.c``.
 """
@@ -61,12 +62,12 @@ def _load():
         # broken copy; nothing else sets it.
         lib = ctypes.CDLL(os.environ.get("CCC_ORACLE_LIB") or build())
         P, I64, I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
-        lib.oracle_fwd.argtypes = [P, I64, I64, I64, P, P, P, I, P, I, P, P, P]
+        lib.oracle_fwd.argtypes = [P, I64, I64, I64, P, I, P, P, I, P, I, P, P, P]
         lib.oracle_fwd.restype = I
-        lib.oracle_bwd.argtypes = [P, I64, I64, I64, P, P, P, I, P, I, P, P, P, P, P, P, P, P]
+        lib.oracle_bwd.argtypes = [P, I64, I64, I64, P, I, P, P, I, P, I, P, P, P, P, P, P, P, P]
         lib.oracle_bwd.restype = I
-        lib.oracle_update.argtypes = [P, I64, I64, P, P, I, P, P]
-        lib.oracle_update.restype = None
+        lib.oracle_update.argtypes = [P, I64, I64, P, I, P, I, P, P]
+        lib.oracle_update.restype = I
         lib.oracle_check_cu_seqlens.argtypes = [P, I, I64]
         lib.oracle_check_cu_seqlens.restype = I
         lib.oracle_bf16_encode.argtypes = [ctypes.c_double]
@@ -129,6 +130,13 @@ def _weight_f64(weight):
     raise TypeError(f"weight must be BF16 bits (uint16) or float32, got {w.dtype}")
 
 
+def _width(w) -> int:
+    """The filter width W of a [D, W] weight (2..4)."""
+    if w.ndim != 2 or not 2 <= w.shape[1] <= 4:
+        raise ValueError(f"weight must be [D, W] with 2 <= W <= 4, got shape {w.shape}")
+    return int(w.shape[1])
+
+
 def check_cu_seqlens(cu_seqlens, total: int) -> bool:
     """True when the offsets follow the page's rules (first 0, last == total,
     strictly increasing)."""
@@ -139,15 +147,17 @@ def check_cu_seqlens(cu_seqlens, total: int) -> bool:
 # ---- fp64 core ---------------------------------------------------------------
 
 def fwd_f64(x, weight, bias=None, cu_seqlens=None, initial_states=None, activation="silu"):
-    """Returns dict(out, pre: [B,D,T], final: [S,D,3]) in float64."""
+    """Returns dict(out, pre: [B,D,T], final: [S,D,W-1]) in float64."""
     lib = _load()
     x = _f64(x)
     B, D, T = x.shape
+    w = _f64(weight)
+    W = _width(w)
     cu, S = _cu(B, cu_seqlens)
     out = np.empty((B, D, T))
     pre = np.empty((B, D, T))
-    fin = np.empty((S, D, 3))
-    rc = lib.oracle_fwd(_ptr(x), B, D, T, _ptr(_f64(weight)), _ptr(_f64(bias)), _ptr(cu), S,
+    fin = np.empty((S, D, W - 1))
+    rc = lib.oracle_fwd(_ptr(x), B, D, T, _ptr(w), W, _ptr(_f64(bias)), _ptr(cu), S,
                         _ptr(_f64(initial_states)), _act(activation), _ptr(out), _ptr(pre),
                         _ptr(fin))
     if rc != 0:
@@ -157,23 +167,25 @@ def fwd_f64(x, weight, bias=None, cu_seqlens=None, initial_states=None, activati
 
 def bwd_f64(x, weight, g, bias=None, cu_seqlens=None, initial_states=None, dfinal_states=None,
             activation="silu"):
-    """Returns dict(dx [B,D,T], dinit [S,D,3], dw, dw_abs [D,4], db, db_abs [D]) in float64.
-    ``dinit`` is the gradient at the three positions before each sequence, given
-    whether or not initial states were passed."""
+    """Returns dict(dx [B,D,T], dinit [S,D,W-1], dw, dw_abs [D,W], db, db_abs [D]) in
+    float64.  ``dinit`` is the gradient at the W - 1 positions before each
+    sequence, given whether or not initial states were passed."""
     lib = _load()
     x = _f64(x)
     B, D, T = x.shape
+    w = _f64(weight)
+    W = _width(w)
     g = _f64(g)
     if g.shape != x.shape:
         raise ValueError("g must have the shape of x")
     cu, S = _cu(B, cu_seqlens)
     dx = np.empty((B, D, T))
-    dinit = np.empty((S, D, 3))
-    dw = np.empty((D, 4))
-    dw_abs = np.empty((D, 4))
+    dinit = np.empty((S, D, W - 1))
+    dw = np.empty((D, W))
+    dw_abs = np.empty((D, W))
     db = np.empty((D,))
     db_abs = np.empty((D,))
-    rc = lib.oracle_bwd(_ptr(x), B, D, T, _ptr(_f64(weight)), _ptr(_f64(bias)), _ptr(cu), S,
+    rc = lib.oracle_bwd(_ptr(x), B, D, T, _ptr(w), W, _ptr(_f64(bias)), _ptr(cu), S,
                         _ptr(_f64(initial_states)), _act(activation), _ptr(g),
                         _ptr(_f64(dfinal_states)), _ptr(dx), _ptr(dinit), _ptr(dw),
                         _ptr(dw_abs), _ptr(db), _ptr(db_abs))
@@ -183,15 +195,17 @@ def bwd_f64(x, weight, g, bias=None, cu_seqlens=None, initial_states=None, dfina
 
 
 def update_f64(x, conv_state, weight, bias=None, activation="silu"):
-    """Returns dict(out [B,D], state [B,D,3]) in float64; the input state is not modified."""
+    """Returns dict(out [B,D], state [B,D,W-1]) in float64; the input state is not modified."""
     lib = _load()
     x = _f64(x)
     B, D = x.shape
+    w = _f64(weight)
+    W = _width(w)
     state = np.array(conv_state, dtype=np.float64, copy=True)
-    if state.shape != (B, D, 3):
-        raise ValueError("conv_state must be [B, D, 3]")
+    if state.shape != (B, D, W - 1):
+        raise ValueError("conv_state must be [B, D, W - 1]")
     out = np.empty((B, D))
-    lib.oracle_update(_ptr(x), B, D, _ptr(_f64(weight)), _ptr(_f64(bias)), _act(activation),
+    lib.oracle_update(_ptr(x), B, D, _ptr(w), W, _ptr(_f64(bias)), _act(activation),
                       _ptr(state), _ptr(out))
     return dict(out=out, state=state)
 

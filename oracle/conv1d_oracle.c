@@ -6,18 +6,19 @@
  * tests, the smoke check and the benchmark's CPU-baseline leg may load it.  It
  * shares no code, header, table or helper with the CUDA library.
  *
- * What it computes (cuDNN frontend "Causal Conv1d" page: the list of tensors,
- * the paragraph on the optimized route -- width four, SiLU, W-1 initial and
- * final state, cu_seqlens packing -- and the paragraph on causal_conv1d_update;
- * tap order from the causal-padding derivation on the POPCORNBENCH conv1d page,
- * where tap k of a width-K filter reads input position t + k - (K-1)):
+ * What it computes (cuDNN frontend "Causal Conv1d" page: the list of tensors
+ * -- weight[D, W], states [., D, W - 1] -- the paragraph on the optimized route
+ * -- width four, SiLU, W-1 initial and final state, cu_seqlens packing -- and
+ * the paragraph on causal_conv1d_update; tap order from the causal-padding
+ * derivation on the POPCORNBENCH conv1d page, where tap k of a width-K filter
+ * reads input position t + k - (K-1)).  For a width W in 2..4 and S = W - 1:
  *
  *   extended sequence   xe[j] = x[j]            for 0 <= j < len
- *                       xe[j] = init[j + 3]     for -3 <= j < 0 (0 if no init)
- *   pre-activation      pre[t] = bias + sum_{k=0..3} w[k] * xe[t - 3 + k]
+ *                       xe[j] = init[j + S]     for -S <= j < 0 (0 if no init)
+ *   pre-activation      pre[t] = bias + sum_{k=0..W-1} w[k] * xe[t - S + k]
  *   output              out[t] = silu(pre[t]) = pre[t] * s(pre[t]),  s(p) = 1/(1+exp(-p))
  *                       (or out = pre with the identity activation)
- *   final state         final[i] = xe[len - 3 + i], i = 0..2
+ *   final state         final[i] = xe[len - S + i], i = 0..S-1
  *
  * A "sequence" is one batch row of a dense call, or one cu_seqlens range of a
  * packed call (each with its own initial/final state, nothing crosses a
@@ -25,29 +26,28 @@
  *
  * Backward (gradients of L with g = dL/dout and gf = dL/dfinal):
  *   gp[t]    = g[t] * silu'(pre[t]),   silu'(p) = s(p) * (1 + p * (1 - s(p)))
- *   dxe[j]   = sum_k w[k] * gp[j + 3 - k]   (only terms with 0 <= j+3-k < len)
- *              + gf[j - (len - 3)]          (when j >= len - 3)
- *   dx[t]    = dxe[t],   dinit[i] = dxe[i - 3]
- *   dw[k]    = sum_seq sum_t gp[t] * xe[t - 3 + k],    db = sum_seq sum_t gp[t]
+ *   dxe[j]   = sum_k w[k] * gp[j + S - k]   (only terms with 0 <= j+S-k < len)
+ *              + gf[j - (len - S)]          (when j >= len - S)
+ *   dx[t]    = dxe[t],   dinit[i] = dxe[i - S]
+ *   dw[k]    = sum_seq sum_t gp[t] * xe[t - S + k],    db = sum_seq sum_t gp[t]
  *
- * Single-token update (causal_conv1d_update): xe = [s0, s1, s2, x],
- * out = act(bias + sum_k w[k] * xe[k]), new state = [s1, s2, x].
+ * Single-token update (causal_conv1d_update): xe = [s0 .. s(S-1), x],
+ * out = act(bias + sum_k w[k] * xe[k]), new state = [s1 .. s(S-1), x].
  *
  * Every input and output here is a double.  The Python side decodes BF16
  * inputs exactly into doubles and rounds results once (nearest-even) to the
  * output type with oracle_bf16_encode_array below.  Products of a BF16 value
  * and a BF16/FP32 weight are exact in double, so pre[] is the exact value up to
- * the double rounding of a five-term sum.
+ * the double rounding of a (W+1)-term sum.
  */
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
 
-#define CONV_W 4
-#define CONV_S 3
+#define CONV_WMAX 4 /* widths 2..4 */
 
-enum { ORC_OK = 0, ORC_BAD_CU_SEQLENS = 7, ORC_NO_MEMORY = 100 };
+enum { ORC_OK = 0, ORC_BAD_CU_SEQLENS = 7, ORC_NO_MEMORY = 100, ORC_BAD_WIDTH = 101 };
 
 /* ---- BF16 rounding ------------------------------------------------------ */
 
@@ -129,19 +129,20 @@ static void seq_range(int n, const int32_t *cu, int64_t T, int64_t *row, int64_t
 }
 
 /* xe[j] of one (sequence, channel); x points at token 0 of the sequence,
- * init at its three state entries (or NULL). */
-static double xe(const double *x, const double *init, int64_t j)
+ * init at its S state entries (or NULL). */
+static double xe(const double *x, const double *init, int S, int64_t j)
 {
     if (j >= 0)
         return x[j];
-    return init ? init[j + CONV_S] : 0.0;
+    return init ? init[j + S] : 0.0;
 }
 
-static double pre_activation(const double *x, const double *init, const double *w, double b, int64_t t)
+static double pre_activation(const double *x, const double *init, const double *w, int W,
+                             double b, int64_t t)
 {
     double p = b;
-    for (int k = 0; k < CONV_W; ++k)
-        p += w[k] * xe(x, init, t - (CONV_W - 1) + k);
+    for (int k = 0; k < W; ++k)
+        p += w[k] * xe(x, init, W - 1, t - (W - 1) + k);
     return p;
 }
 
@@ -149,15 +150,18 @@ static double pre_activation(const double *x, const double *init, const double *
 
 /*
  * x:     [B][D][T] (packed: B == 1 and T == token total)
- * w:     [D][4];  bias: [D] or NULL
+ * w:     [D][W], 2 <= W <= 4;  bias: [D] or NULL
  * cu:    [n_seq + 1] or NULL (dense: n_seq is taken as B)
- * init:  [n_seq][D][3] or NULL
- * out, pre: [B][D][T] (pre may be NULL);  fin: [n_seq][D][3] or NULL
+ * init:  [n_seq][D][W-1] or NULL
+ * out, pre: [B][D][T] (pre may be NULL);  fin: [n_seq][D][W-1] or NULL
  */
 int oracle_fwd(const double *x, int64_t B, int64_t D, int64_t T,
-               const double *w, const double *bias, const int32_t *cu, int n_seq,
+               const double *w, int W, const double *bias, const int32_t *cu, int n_seq,
                const double *init, int act, double *out, double *pre, double *fin)
 {
+    if (W < 2 || W > CONV_WMAX)
+        return ORC_BAD_WIDTH;
+    const int S = W - 1;
     if (cu && oracle_check_cu_seqlens(cu, n_seq, T))
         return ORC_BAD_CU_SEQLENS;
     if (!cu)
@@ -166,21 +170,21 @@ int oracle_fwd(const double *x, int64_t B, int64_t D, int64_t T,
         int64_t row, start, len;
         seq_range(n, cu, T, &row, &start, &len);
         for (int64_t d = 0; d < D; ++d) {
-            const double *wd = w + d * CONV_W;
+            const double *wd = w + d * W;
             double b = bias ? bias[d] : 0.0;
             int64_t base = (row * D + d) * T + start;
             const double *xs = x + base;
-            const double *is = init ? init + ((int64_t)n * D + d) * CONV_S : NULL;
+            const double *is = init ? init + ((int64_t)n * D + d) * S : NULL;
             for (int64_t t = 0; t < len; ++t) {
-                double p = pre_activation(xs, is, wd, b, t);
+                double p = pre_activation(xs, is, wd, W, b, t);
                 out[base + t] = activate(p, act);
                 if (pre)
                     pre[base + t] = p;
             }
             if (fin) {
-                double *fs = fin + ((int64_t)n * D + d) * CONV_S;
-                for (int i = 0; i < CONV_S; ++i)
-                    fs[i] = xe(xs, is, len - CONV_S + i);
+                double *fs = fin + ((int64_t)n * D + d) * S;
+                for (int i = 0; i < S; ++i)
+                    fs[i] = xe(xs, is, S, len - S + i);
             }
         }
     }
@@ -190,18 +194,21 @@ int oracle_fwd(const double *x, int64_t B, int64_t D, int64_t T,
 /* ---- backward ----------------------------------------------------------- */
 
 /*
- * Inputs as oracle_fwd, plus g: [B][D][T] and gfin: [n_seq][D][3] or NULL.
+ * Inputs as oracle_fwd, plus g: [B][D][T] and gfin: [n_seq][D][W-1] or NULL.
  * Outputs (any may be NULL):
- *   dx [B][D][T];  dinit [n_seq][D][3]
- *   dw [D][4], dw_abs [D][4] = sum |gp * xe|;  db [D], db_abs [D] = sum |gp|
+ *   dx [B][D][T];  dinit [n_seq][D][W-1]
+ *   dw [D][W], dw_abs [D][W] = sum |gp * xe|;  db [D], db_abs [D] = sum |gp|
  * The sums run over sequences in ascending order, then tokens in ascending
  * order, in one double accumulator per (channel, tap).
  */
 int oracle_bwd(const double *x, int64_t B, int64_t D, int64_t T,
-               const double *w, const double *bias, const int32_t *cu, int n_seq,
+               const double *w, int W, const double *bias, const int32_t *cu, int n_seq,
                const double *init, int act, const double *g, const double *gfin,
                double *dx, double *dinit, double *dw, double *dw_abs, double *db, double *db_abs)
 {
+    if (W < 2 || W > CONV_WMAX)
+        return ORC_BAD_WIDTH;
+    const int S = W - 1;
     if (cu && oracle_check_cu_seqlens(cu, n_seq, T))
         return ORC_BAD_CU_SEQLENS;
     if (!cu)
@@ -210,9 +217,9 @@ int oracle_bwd(const double *x, int64_t B, int64_t D, int64_t T,
     if (!gp)
         return ORC_NO_MEMORY;
     for (int64_t d = 0; d < D; ++d) {
-        const double *wd = w + d * CONV_W;
+        const double *wd = w + d * W;
         double b = bias ? bias[d] : 0.0;
-        double sdw[CONV_W] = {0, 0, 0, 0}, sdw_abs[CONV_W] = {0, 0, 0, 0};
+        double sdw[CONV_WMAX] = {0, 0, 0, 0}, sdw_abs[CONV_WMAX] = {0, 0, 0, 0};
         double sdb = 0.0, sdb_abs = 0.0;
         for (int n = 0; n < n_seq; ++n) {
             int64_t row, start, len;
@@ -220,13 +227,13 @@ int oracle_bwd(const double *x, int64_t B, int64_t D, int64_t T,
             int64_t base = (row * D + d) * T + start;
             const double *xs = x + base;
             const double *gs = g + base;
-            const double *is = init ? init + ((int64_t)n * D + d) * CONV_S : NULL;
-            const double *gfs = gfin ? gfin + ((int64_t)n * D + d) * CONV_S : NULL;
+            const double *is = init ? init + ((int64_t)n * D + d) * S : NULL;
+            const double *gfs = gfin ? gfin + ((int64_t)n * D + d) * S : NULL;
             /* gradient at the pre-activation; weight and bias sums */
             for (int64_t t = 0; t < len; ++t) {
-                gp[t] = gs[t] * activate_grad(pre_activation(xs, is, wd, b, t), act);
-                for (int k = 0; k < CONV_W; ++k) {
-                    double term = gp[t] * xe(xs, is, t - (CONV_W - 1) + k);
+                gp[t] = gs[t] * activate_grad(pre_activation(xs, is, wd, W, b, t), act);
+                for (int k = 0; k < W; ++k) {
+                    double term = gp[t] * xe(xs, is, S, t - (W - 1) + k);
                     sdw[k] += term;
                     sdw_abs[k] += fabs(term);
                 }
@@ -234,28 +241,28 @@ int oracle_bwd(const double *x, int64_t B, int64_t D, int64_t T,
                 sdb_abs += fabs(gp[t]);
             }
             /* gradient at every entry of the extended sequence */
-            for (int64_t j = -CONV_S; j < len; ++j) {
+            for (int64_t j = -S; j < len; ++j) {
                 double acc = 0.0;
-                for (int k = 0; k < CONV_W; ++k) {
-                    int64_t t = j + (CONV_W - 1) - k; /* the output that tap k reads xe[j] for */
+                for (int k = 0; k < W; ++k) {
+                    int64_t t = j + (W - 1) - k; /* the output that tap k reads xe[j] for */
                     if (t >= 0 && t < len)
                         acc += wd[k] * gp[t];
                 }
-                if (gfs && j >= len - CONV_S)
-                    acc += gfs[j - (len - CONV_S)];
+                if (gfs && j >= len - S)
+                    acc += gfs[j - (len - S)];
                 if (j >= 0) {
                     if (dx)
                         dx[base + j] = acc;
                 } else if (dinit) {
-                    dinit[((int64_t)n * D + d) * CONV_S + (j + CONV_S)] = acc;
+                    dinit[((int64_t)n * D + d) * S + (j + S)] = acc;
                 }
             }
         }
-        for (int k = 0; k < CONV_W; ++k) {
+        for (int k = 0; k < W; ++k) {
             if (dw)
-                dw[d * CONV_W + k] = sdw[k];
+                dw[d * W + k] = sdw[k];
             if (dw_abs)
-                dw_abs[d * CONV_W + k] = sdw_abs[k];
+                dw_abs[d * W + k] = sdw_abs[k];
         }
         if (db)
             db[d] = sdb;
@@ -269,25 +276,31 @@ int oracle_bwd(const double *x, int64_t B, int64_t D, int64_t T,
 /* ---- single-token update ------------------------------------------------ */
 
 /*
- * x:     [B][D] (one token);  w [D][4];  bias [D] or NULL
- * state: [B][D][3], read, then overwritten with [s1, s2, x]
+ * x:     [B][D] (one token);  w [D][W], 2 <= W <= 4;  bias [D] or NULL
+ * state: [B][D][W-1], read, then overwritten with [s1 .. s(W-2), x]
  * out:   [B][D]
  */
-void oracle_update(const double *x, int64_t B, int64_t D, const double *w, const double *bias,
-                   int act, double *state, double *out)
+int oracle_update(const double *x, int64_t B, int64_t D, const double *w, int W,
+                  const double *bias, int act, double *state, double *out)
 {
+    if (W < 2 || W > CONV_WMAX)
+        return ORC_BAD_WIDTH;
+    const int S = W - 1;
     for (int64_t bb = 0; bb < B; ++bb) {
         for (int64_t d = 0; d < D; ++d) {
-            const double *wd = w + d * CONV_W;
-            double *s = state + (bb * D + d) * CONV_S;
-            double ext[CONV_W] = {s[0], s[1], s[2], x[bb * D + d]};
+            const double *wd = w + d * W;
+            double *s = state + (bb * D + d) * S;
+            double ext[CONV_WMAX];
+            for (int i = 0; i < S; ++i)
+                ext[i] = s[i];
+            ext[S] = x[bb * D + d];
             double p = bias ? bias[d] : 0.0;
-            for (int k = 0; k < CONV_W; ++k)
+            for (int k = 0; k < W; ++k)
                 p += wd[k] * ext[k];
             out[bb * D + d] = activate(p, act);
-            s[0] = ext[1];
-            s[1] = ext[2];
-            s[2] = ext[3];
+            for (int i = 0; i < S; ++i)
+                s[i] = ext[i + 1];
         }
     }
+    return ORC_OK;
 }

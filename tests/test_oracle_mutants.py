@@ -19,26 +19,28 @@ from conftest import ROOT
 SRC = os.path.join(ROOT, "oracle", "conv1d_oracle.c")
 
 MUTANTS = {
-    "tap_offset": ("p += w[k] * xe(x, init, t - (CONV_W - 1) + k);",
-                   "p += w[k] * xe(x, init, t - (CONV_W - 1) + (k + 1) % CONV_W);"),
-    "init_order_reversed": ("return init ? init[j + CONV_S] : 0.0;",
-                            "return init ? init[CONV_S - 1 - (j + CONV_S)] : 0.0;"),
+    "tap_offset": ("p += w[k] * xe(x, init, W - 1, t - (W - 1) + k);",
+                   "p += w[k] * xe(x, init, W - 1, t - (W - 1) + (k + 1) % W);"),
+    "init_order_reversed": ("return init ? init[j + S] : 0.0;",
+                            "return init ? init[S - 1 - (j + S)] : 0.0;"),
     "silu_grad_sign": ("return s * (1.0 + p * (1.0 - s));", "return s * (1.0 - p * (1.0 - s));"),
     "silu_forward": ("return act ? p * sigmoid(p) : p;", "return act ? sigmoid(p) : p;"),
-    "dx_taps_transposed": ("acc += wd[k] * gp[t];", "acc += wd[CONV_W - 1 - k] * gp[t];"),
-    "dfinal_reversed": ("acc += gfs[j - (len - CONV_S)];", "acc += gfs[len - 1 - j];"),
-    "final_state_reversed": ("fs[i] = xe(xs, is, len - CONV_S + i);",
-                             "fs[CONV_S - 1 - i] = xe(xs, is, len - CONV_S + i);"),
-    "dw_taps_reversed": ("double term = gp[t] * xe(xs, is, t - (CONV_W - 1) + k);",
-                         "double term = gp[t] * xe(xs, is, t - k);"),
+    "dx_taps_transposed": ("acc += wd[k] * gp[t];", "acc += wd[W - 1 - k] * gp[t];"),
+    "dfinal_reversed": ("acc += gfs[j - (len - S)];", "acc += gfs[len - 1 - j];"),
+    "final_state_reversed": ("fs[i] = xe(xs, is, S, len - S + i);",
+                             "fs[S - 1 - i] = xe(xs, is, S, len - S + i);"),
+    "dw_taps_reversed": ("double term = gp[t] * xe(xs, is, S, t - (W - 1) + k);",
+                         "double term = gp[t] * xe(xs, is, S, t - k);"),
     "db_without_act_grad": ("sdb += gp[t];", "sdb += gs[t];"),
     "empty_sequence_accepted": ("if (cu[n + 1] <= cu[n])", "if (cu[n + 1] < cu[n])"),
-    "update_shift": ("s[0] = ext[1];", "s[0] = ext[0];"),
-    "update_drops_bias": ("double p = bias ? bias[d] : 0.0;\n            for (int k = 0; k < CONV_W; ++k)\n                p += wd[k] * ext[k];",
-                          "double p = 0.0;\n            for (int k = 0; k < CONV_W; ++k)\n                p += wd[k] * ext[k];"),
+    "update_shift": ("s[i] = ext[i + 1];", "s[i] = ext[i];"),
+    "update_drops_bias": ("double p = bias ? bias[d] : 0.0;\n            for (int k = 0; k < W; ++k)\n                p += wd[k] * ext[k];",
+                          "double p = 0.0;\n            for (int k = 0; k < W; ++k)\n                p += wd[k] * ext[k];"),
     "bf16_truncates": ("double r = rint(ldexp(a, -qexp));", "double r = floor(ldexp(a, -qexp));"),
-    "bias_dropped": ("double p = b;\n    for (int k = 0; k < CONV_W; ++k)\n        p += w[k]",
-                     "double p = 0.0 * b;\n    for (int k = 0; k < CONV_W; ++k)\n        p += w[k]"),
+    "bias_dropped": ("double p = b;\n    for (int k = 0; k < W; ++k)\n        p += w[k]",
+                     "double p = 0.0 * b;\n    for (int k = 0; k < W; ++k)\n        p += w[k]"),
+    "width_state_offset": ("const double *is = init ? init + ((int64_t)n * D + d) * S : NULL;\n            for (int64_t t = 0; t < len; ++t) {",
+                           "const double *is = init ? init + ((int64_t)n * D + d) * 3 : NULL;\n            for (int64_t t = 0; t < len; ++t) {"),
 }
 
 

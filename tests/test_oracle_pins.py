@@ -421,3 +421,132 @@ def test_bwd_bf16_interface_rounds_fp64_results():
     wb = _rand_bf16((D, 4), 0.3)
     r = oracle.bwd(x, wb, g, _rand_bf16((D,), 0.05))
     assert r["dw"].dtype == np.uint16 and r["db"].dtype == np.uint16
+
+
+# ---- other filter widths (W = 2, 3; the page's tensors are weight[D, W] and
+# states [., D, W - 1]) ---------------------------------------------------------
+
+
+def _toeplitz_pre_w(x, w, b, init):
+    """Brute force for any width: the T x (T + W - 1) banded matrix per channel
+    times the extended sequence (initial state as its first W - 1 entries)."""
+    B, D, T = x.shape
+    W = w.shape[1]
+    S = W - 1
+    pre = np.zeros((B, D, T))
+    for bb in range(B):
+        for d in range(D):
+            xe = np.concatenate([init[bb, d] if init is not None else np.zeros(S), x[bb, d]])
+            M = np.zeros((T, T + S))
+            for t in range(T):
+                M[t, t:t + W] = w[d]
+            pre[bb, d] = M @ xe + (b[d] if b is not None else 0.0)
+    return pre
+
+
+@pytest.mark.parametrize("W", [2, 3])
+@pytest.mark.parametrize("T", [1, 2, 5, 9])
+def test_fwd_other_widths_match_toeplitz_brute_force(W, T):
+    B, D = 2, 3
+    x = RNG.standard_normal((B, D, T))
+    w = RNG.uniform(-0.5, 0.5, (D, W))
+    b = RNG.uniform(-0.1, 0.1, D)
+    init = RNG.standard_normal((B, D, W - 1))
+    r = oracle.fwd_f64(x, w, b, None, init, "silu")
+    ref = _toeplitz_pre_w(x, w, b, init)
+    np.testing.assert_allclose(r["pre"], ref, rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(r["out"], _silu(ref), rtol=1e-13, atol=1e-14)
+    xe = np.concatenate([init, x], axis=2)
+    np.testing.assert_array_equal(r["final"], xe[:, :, -(W - 1):])
+
+
+@pytest.mark.parametrize("W", [2, 3, 4])
+def test_fwd_widths_match_torch_grouped_conv1d_packed(W):
+    lengths = [4, 1, 6]
+    D, T = 3, 11
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    x = RNG.standard_normal((1, D, T))
+    w = RNG.uniform(-0.5, 0.5, (D, W))
+    b = RNG.uniform(-0.1, 0.1, D)
+    init = RNG.standard_normal((len(lengths), D, W - 1))
+    r = oracle.fwd_f64(x, w, b, cu, init, "silu")
+    for n in range(len(lengths)):
+        xe = torch.cat([torch.from_numpy(init[n:n + 1]), torch.from_numpy(x[:, :, cu[n]:cu[n + 1]])], dim=2)
+        ref = F.silu(F.conv1d(xe, torch.from_numpy(w)[:, None, :], torch.from_numpy(b), groups=D))
+        np.testing.assert_allclose(r["out"][:, :, cu[n]:cu[n + 1]], ref.numpy(), rtol=1e-13, atol=1e-14)
+        np.testing.assert_array_equal(r["final"][n], xe[0, :, -(W - 1):].numpy())
+
+
+@pytest.mark.parametrize("W", [2, 3])
+def test_update_chain_equals_forward_other_widths(W):
+    B, D, T = 2, 4, 9
+    x = _rand_bf16((B, D, T))
+    w = _rand_bf16((D, W), 0.3)
+    b = _rand_bf16((D,), 0.05)
+    init = _rand_bf16((B, D, W - 1))
+    full = oracle.fwd(x, w, b, None, init)
+    state, outs = init.copy(), []
+    for t in range(T):
+        r = oracle.update(np.ascontiguousarray(x[:, :, t]), state, w, b)
+        outs.append(r["out"])
+        state = r["state"]
+    assert np.array_equal(np.stack(outs, axis=2), full["out"])
+    assert np.array_equal(state, full["final"])
+
+
+@pytest.mark.parametrize("W", [2, 3])
+@pytest.mark.parametrize("case", [dict(B=2, D=2, T=1), dict(B=2, D=2, T=6), dict(B=1, D=2, T=0, lengths=[1, 3, 2])],
+                         ids=["T1", "T6", "packed"])
+def test_bwd_other_widths_match_central_finite_differences(W, case):
+    rng = np.random.default_rng(W * 10 + case["T"])
+    lengths = case.get("lengths")
+    if lengths is not None:
+        B, T = 1, sum(lengths)
+        cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+        S = len(lengths)
+    else:
+        B, T, cu, S = case["B"], case["T"], None, case["B"]
+    D = case["D"]
+    x = rng.standard_normal((B, D, T))
+    g = rng.standard_normal((B, D, T))
+    w = rng.uniform(-0.8, 0.8, (D, W))
+    b = rng.uniform(-0.3, 0.3, D)
+    init = rng.standard_normal((S, D, W - 1))
+    gf = rng.standard_normal((S, D, W - 1))
+
+    def L():
+        return _loss(oracle.fwd_f64(x, w, b, cu, init, "silu"), g, gf)
+
+    r = oracle.bwd_f64(x, w, g, b, cu, init, gf, "silu")
+    tol = dict(rtol=1e-6, atol=1e-7)
+    np.testing.assert_allclose(r["dx"], _central_diff(L, x), **tol)
+    np.testing.assert_allclose(r["dw"], _central_diff(L, w), **tol)
+    np.testing.assert_allclose(r["db"], _central_diff(L, b), **tol)
+    np.testing.assert_allclose(r["dinit"], _central_diff(L, init), **tol)
+
+
+@pytest.mark.parametrize("W", [2, 3])
+def test_bwd_other_widths_match_torch_autograd_float64(W):
+    rng = np.random.default_rng(70 + W)
+    B, D, T = 2, 3, 8
+    x = rng.standard_normal((B, D, T))
+    g = rng.standard_normal((B, D, T))
+    w = rng.uniform(-0.5, 0.5, (D, W))
+    b = rng.uniform(-0.1, 0.1, D)
+    init = rng.standard_normal((B, D, W - 1))
+    gf = rng.standard_normal((B, D, W - 1))
+    tx, tw, tb, ti = (torch.tensor(a, requires_grad=True) for a in (x, w, b, init))
+    xe = torch.cat([ti, tx], dim=2)
+    out = F.silu(F.conv1d(xe, tw[:, None, :], tb, groups=D))
+    L = (out * torch.from_numpy(g)).sum() + (xe[:, :, -(W - 1):] * torch.from_numpy(gf)).sum()
+    L.backward()
+    r = oracle.bwd_f64(x, w, g, b, None, init, gf, "silu")
+    for got, ref in ((r["dx"], tx.grad), (r["dw"], tw.grad), (r["db"], tb.grad), (r["dinit"], ti.grad)):
+        np.testing.assert_allclose(got, ref.numpy(), rtol=1e-12, atol=1e-13)
+
+
+def test_widths_outside_two_to_four_are_rejected():
+    with pytest.raises(ValueError):
+        oracle.fwd_f64(np.zeros((1, 2, 3)), np.zeros((2, 5)))
+    with pytest.raises(ValueError):
+        oracle.fwd_f64(np.zeros((1, 2, 3)), np.zeros((2, 1)))
