@@ -191,7 +191,9 @@ class DenseStep:
         self.dx = [torch.empty_like(x) for x in self.x]
         S = inp.n_seq
         D = d.x.shape[1]
-        self.fin = torch.empty(S, D, 3, dtype=torch.bfloat16, device=device) if self.init is not None else None
+        W = d.weight.shape[1]
+        self.fin = (torch.empty(S, D, W - 1, dtype=torch.bfloat16, device=device)
+                    if self.init is not None else None)
         self.dinit = torch.empty_like(self.init) if self.init is not None else None
         self.dw = torch.empty_like(self.w)
         self.db = torch.empty_like(self.b) if self.b is not None else None
@@ -369,7 +371,7 @@ def time_e2e(inp: workloads.ConvInputs, device, steps, warmup, stream):
     S, D = inp.n_seq, inp.x.shape[1]
     ho = torch.empty_like(hx).pin_memory()
     hdx = torch.empty_like(hx).pin_memory()
-    hf = torch.empty(S, D, 3, dtype=torch.bfloat16).pin_memory()
+    hf = torch.empty(S, D, inp.weight.shape[1] - 1, dtype=torch.bfloat16).pin_memory()
     hdi = torch.empty_like(hi).pin_memory()
     hdw = torch.empty_like(hw).pin_memory()
     hdb = torch.empty_like(hb).pin_memory() if hb is not None else None
@@ -665,6 +667,9 @@ def main():
               bench_conv_workload("packed_varlen", workloads.packed_varlen(), device, stream, peak,
                                   True),
               bench_update(device, stream, peak)]
+        # the same dense step with a width-three filter (weight [D, 3], states [., D, 2])
+        w3 = workloads.make_inputs(4, 1536, 2048, seed=0, initial_states=True, grad=True, width=3)
+        bd.append(bench_conv_workload("dense_state_width3", w3, device, stream, peak, False))
         large = workloads.dense_large(bias=True)
         bd.append(bench_conv_workload("dense_large_bias", large, device, stream, peak, False))
         large = dataclasses.replace(large, bias=None, deterministic=True)

@@ -103,12 +103,12 @@ void act_strides(const ccc_tensor* t, int layout, int64_t& sb, int64_t& sd, int6
   st = t->shape[2] <= 1 ? (layout == ccc::kLayoutTimeContiguous ? 1 : 0) : t->stride[2];
 }
 
-// State tensors: [S, D, 3] BF16, contiguous.
-bool state_ok(const ccc_tensor* t, int64_t S, int64_t D) {
-  if (!well_formed(t, 3) || t->dtype != CCC_BF16 || !shape_is(t, S, D, kState)) return false;
+// State tensors: [S, D, sw] BF16 (sw = W - 1 entries per channel), contiguous.
+bool state_ok(const ccc_tensor* t, int64_t S, int64_t D, int64_t sw) {
+  if (!well_formed(t, 3) || t->dtype != CCC_BF16 || !shape_is(t, S, D, sw)) return false;
   if (numel(t) == 0) return true;
-  return (S <= 1 || t->stride[0] == D * kState) && (D <= 1 || t->stride[1] == kState) &&
-         t->stride[2] == 1;
+  return (S <= 1 || t->stride[0] == D * sw) && (D <= 1 || t->stride[1] == sw) &&
+         (sw <= 1 || t->stride[2] == 1);
 }
 
 int device_sm_count() {
@@ -126,6 +126,8 @@ struct Problem {
   bool packed = false;
   int layout = -1;
   int w_f32 = 0;
+  int W = kWidth;  // filter width, 2..4 (four on the optimized route)
+  int sw = kState; // state entries per channel, W - 1
 };
 
 ccc_status check_common(const ccc_tensor* x, const ccc_tensor* weight, const ccc_tensor* bias,
@@ -142,9 +144,11 @@ ccc_status check_common(const ccc_tensor* x, const ccc_tensor* weight, const ccc
 
   if (!weight || weight->ndim != 2) return CCC_ERR_INVALID_ARG;
   if (!well_formed(weight, 2) || weight->shape[0] != pb.D) return CCC_ERR_INVALID_ARG;
-  if (weight->shape[1] != kWidth) return CCC_ERR_UNSUPPORTED;  // width four only
+  if (weight->shape[1] < 2 || weight->shape[1] > kWidth) return CCC_ERR_UNSUPPORTED;  // W in 2..4
   if (weight->dtype != CCC_BF16 && weight->dtype != CCC_F32) return CCC_ERR_INVALID_ARG;
   pb.w_f32 = weight->dtype == CCC_F32;
+  pb.W = int(weight->shape[1]);
+  pb.sw = pb.W - 1;
 
   if (bias) {
     if (!well_formed(bias, 1) || bias->dtype != CCC_BF16 || !shape_is(bias, pb.D))
@@ -162,7 +166,7 @@ ccc_status check_common(const ccc_tensor* x, const ccc_tensor* weight, const ccc
   } else {
     pb.n_seq = pb.B;
   }
-  if (init && !state_ok(init, pb.n_seq, pb.D)) return CCC_ERR_INVALID_ARG;
+  if (init && !state_ok(init, pb.n_seq, pb.D, pb.sw)) return CCC_ERR_INVALID_ARG;
   return CCC_OK;
 }
 
@@ -218,10 +222,11 @@ ccc::WeightRef weight_ref(const ccc_tensor* weight, const ccc_tensor* bias) {
   r.w_f32 = weight->dtype == CCC_F32;
   r.w_sd = weight->stride[0];
   r.w_sk = weight->stride[1];
+  r.W = int(weight->shape[1]);
   r.bias = bias ? static_cast<const uint16_t*>(bias->data) : nullptr;
   r.b_sd = bias ? bias->stride[0] : 0;
   const int64_t D = weight->shape[0];
-  r.w_vec = (D <= 1 || r.w_sd == kWidth) && r.w_sk == 1 && aligned16(weight->data) &&
+  r.w_vec = r.W == kWidth && (D <= 1 || r.w_sd == kWidth) && r.w_sk == 1 && aligned16(weight->data) &&
             (!bias || ((D <= 1 || r.b_sd == 1) && aligned16(bias->data)));
   return r;
 }
@@ -328,7 +333,7 @@ ccc_status ccc_conv1d_fwd(const ccc_tensor* x, const ccc_tensor* weight, const c
   if (st != CCC_OK) return st;
   if (!same_act_shape(out, pb)) return CCC_ERR_INVALID_ARG;
   if (layout_of(out) != pb.layout || !self_disjoint(out)) return CCC_ERR_UNSUPPORTED;
-  if (final_states && !state_ok(final_states, pb.n_seq, pb.D)) return CCC_ERR_INVALID_ARG;
+  if (final_states && !state_ok(final_states, pb.n_seq, pb.D, pb.sw)) return CCC_ERR_INVALID_ARG;
   // final_states must not share memory with the inputs (cuDNN page, aliasing rule);
   // neither may out.
   for (const ccc_tensor* in : {x, weight, bias, cu_seqlens, initial_states}) {
@@ -347,6 +352,7 @@ ccc_status ccc_conv1d_fwd(const ccc_tensor* x, const ccc_tensor* weight, const c
   a.wr = weight_ref(weight, bias);
   a.init = initial_states ? static_cast<const uint16_t*>(initial_states->data) : nullptr;
   a.fin = final_states ? static_cast<uint16_t*>(final_states->data) : nullptr;
+  a.sw = pb.sw;
   a.seqs = seqs_of(pb, cu_seqlens);
   a.B = pb.B;
   a.D = pb.D;
@@ -410,15 +416,15 @@ ccc_status ccc_conv1d_bwd(const ccc_tensor* x, const ccc_tensor* weight, const c
   if (!same_act_shape(dout, pb) || !same_act_shape(dx, pb)) return CCC_ERR_INVALID_ARG;
   if (layout_of(dout) != pb.layout || layout_of(dx) != pb.layout || !self_disjoint(dx))
     return CCC_ERR_UNSUPPORTED;
-  if (dfinal_states && !state_ok(dfinal_states, pb.n_seq, pb.D)) return CCC_ERR_INVALID_ARG;
-  if (!dweight || !well_formed(dweight, 2) || !shape_is(dweight, pb.D, kWidth) ||
+  if (dfinal_states && !state_ok(dfinal_states, pb.n_seq, pb.D, pb.sw)) return CCC_ERR_INVALID_ARG;
+  if (!dweight || !well_formed(dweight, 2) || !shape_is(dweight, pb.D, pb.W) ||
       dweight->dtype != weight->dtype || !self_disjoint(dweight))
     return CCC_ERR_INVALID_ARG;
   if ((bias == nullptr) != (dbias == nullptr)) return CCC_ERR_INVALID_ARG;
   if (dbias && (!well_formed(dbias, 1) || dbias->dtype != CCC_BF16 || !shape_is(dbias, pb.D) ||
                 !self_disjoint(dbias)))
     return CCC_ERR_INVALID_ARG;
-  if (dinitial_states && (!initial_states || !state_ok(dinitial_states, pb.n_seq, pb.D)))
+  if (dinitial_states && (!initial_states || !state_ok(dinitial_states, pb.n_seq, pb.D, pb.sw)))
     return CCC_ERR_INVALID_ARG;
   if (deterministic != 0 && deterministic != 1) return CCC_ERR_INVALID_ARG;
   if (deterministic && bias) return CCC_ERR_NONDETERMINISTIC;
@@ -464,6 +470,7 @@ ccc_status ccc_conv1d_bwd(const ccc_tensor* x, const ccc_tensor* weight, const c
   a.init = initial_states ? static_cast<const uint16_t*>(initial_states->data) : nullptr;
   a.dfin = dfinal_states ? static_cast<const uint16_t*>(dfinal_states->data) : nullptr;
   a.dinit = dinitial_states ? static_cast<uint16_t*>(dinitial_states->data) : nullptr;
+  a.sw = pb.sw;
   a.seqs = seqs_of(pb, cu_seqlens);
   a.B = pb.B;
   a.D = pb.D;
@@ -475,6 +482,7 @@ ccc_status ccc_conv1d_bwd(const ccc_tensor* x, const ccc_tensor* weight, const c
   ccc::WgradOut o{};
   o.dw = dweight->data;
   o.dw_f32 = dweight->dtype == CCC_F32;
+  o.W = pb.W;
   o.dw_sd = dweight->stride[0];
   o.dw_sk = dweight->stride[1];
   o.db = dbias ? static_cast<uint16_t*>(dbias->data) : nullptr;
@@ -503,9 +511,10 @@ ccc_status ccc_conv1d_update(const ccc_tensor* x, const ccc_tensor* conv_state,
   const int L = multi ? int(x->shape[2]) : 1;
   if (D > 1 && x->stride[1] != 1) return CCC_ERR_UNSUPPORTED;
   if (activation != CCC_ACT_NONE && activation != CCC_ACT_SILU) return CCC_ERR_INVALID_ARG;
-  if (!state_ok(conv_state, B, D)) return CCC_ERR_INVALID_ARG;
   if (!weight || !well_formed(weight, 2) || weight->shape[0] != D) return CCC_ERR_INVALID_ARG;
-  if (weight->shape[1] != kWidth) return CCC_ERR_UNSUPPORTED;
+  if (weight->shape[1] < 2 || weight->shape[1] > kWidth) return CCC_ERR_UNSUPPORTED;  // W in 2..4
+  const int sw = int(weight->shape[1]) - 1;
+  if (!state_ok(conv_state, B, D, sw)) return CCC_ERR_INVALID_ARG;
   if (weight->dtype != CCC_BF16 && weight->dtype != CCC_F32) return CCC_ERR_INVALID_ARG;
   if (bias) {
     if (!well_formed(bias, 1) || bias->dtype != CCC_BF16 || !shape_is(bias, D))
@@ -529,6 +538,7 @@ ccc_status ccc_conv1d_update(const ccc_tensor* x, const ccc_tensor* conv_state,
   a.x_sb = B > 1 ? x->stride[0] : 0;
   a.x_sl = multi && L > 1 ? x->stride[2] : 0;
   a.state = static_cast<uint16_t*>(conv_state->data);
+  a.sw = sw;
   a.out = static_cast<uint16_t*>(out->data);
   a.o_sb = B > 1 ? out->stride[0] : 0;
   a.o_sl = multi && L > 1 ? out->stride[2] : 0;

@@ -48,7 +48,7 @@ __device__ __forceinline__ void bwd_walk(const BwdArgs& a, const Seqs& seqs, con
     {
       float init[kState][V];
       if (a0 - kState < lo && a.init) {
-        load_state<V>(a.init + state_row * kState, init);
+        load_state<V>(a.init, state_row, a.sw, init);
       } else {
 #pragma unroll
         for (int i = 0; i < kState; ++i)
@@ -125,9 +125,12 @@ __device__ __forceinline__ void bwd_walk(const BwdArgs& a, const Seqs& seqs, con
       emit(gp, v);
       if (j >= a0 || starts) {
         if (a.dfin && j >= hi - kState) {
-          const int64_t i = j - (hi - kState);
+          const int i = int(j - (hi - kState));  // window slot of the final state
 #pragma unroll
-          for (int c = 0; c < V; ++c) v[c] += bf16_to_f32(__ldg(a.dfin + (state_row + c) * kState + i));
+          for (int c = 0; c < V; ++c) {
+            const int64_t k = state_slot(state_row + c, i, a.sw);
+            if (k >= 0) v[c] += bf16_to_f32(__ldg(a.dfin + k));
+          }
         }
         if (j >= lo) {
           VT::st(a.dx + ds.at(n, j), VT::pack(v));
@@ -139,7 +142,7 @@ __device__ __forceinline__ void bwd_walk(const BwdArgs& a, const Seqs& seqs, con
             else if (i == 1) di[1][c] = v[c];
             else di[2][c] = v[c];
           }
-          if (i == kState - 1) store_state<V>(a.dinit + state_row * kState, di);
+          if (i == kState - 1) store_state<V>(a.dinit, state_row, a.sw, di);
         }
       }
     };
@@ -351,7 +354,7 @@ __global__ void __launch_bounds__(kBwdThreads, V == 8 ? CCC_BWD_MIN_BLOCKS : 4)
       {
         float2 init[kState][H];
         if (a0 - kState < lo && a.init) {
-          load_state2<V>(a.init + state_row * kState, init);
+          load_state2<V>(a.init, state_row, a.sw, init);
         } else {
 #pragma unroll
           for (int i = 0; i < kState; ++i)
@@ -419,21 +422,25 @@ __global__ void __launch_bounds__(kBwdThreads, V == 8 ? CCC_BWD_MIN_BLOCKS : 4)
         const int64_t j = m - kState;
         if (j >= a0 || starts) {
           if (a.dfin && j >= hi - kState) {
-            const int64_t i = j - (hi - kState);
+            const int i = int(j - (hi - kState));  // window slot of the final state
 #pragma unroll
             for (int h = 0; h < H; ++h) {
-              v[h].x += bf16_to_f32(__ldg(a.dfin + (state_row + 2 * h) * kState + i));
-              v[h].y += bf16_to_f32(__ldg(a.dfin + (state_row + 2 * h + 1) * kState + i));
+              const int64_t k0 = state_slot(state_row + 2 * h, i, a.sw);
+              const int64_t k1 = state_slot(state_row + 2 * h + 1, i, a.sw);
+              if (k0 >= 0) v[h].x += bf16_to_f32(__ldg(a.dfin + k0));
+              if (k1 >= 0) v[h].y += bf16_to_f32(__ldg(a.dfin + k1));
             }
           }
           if (j >= lo) {
             VT::st(dp + (j - a0) * dst, VT::pack2(v));
           } else if (a.dinit) {  // one of the three entries before the sequence
-            const int64_t i = j - lo + kState;
+            const int i = int(j - lo + kState);
 #pragma unroll
             for (int h = 0; h < H; ++h) {
-              a.dinit[(state_row + 2 * h) * kState + i] = f32_to_bf16(v[h].x);
-              a.dinit[(state_row + 2 * h + 1) * kState + i] = f32_to_bf16(v[h].y);
+              const int64_t k0 = state_slot(state_row + 2 * h, i, a.sw);
+              const int64_t k1 = state_slot(state_row + 2 * h + 1, i, a.sw);
+              if (k0 >= 0) a.dinit[k0] = f32_to_bf16(v[h].x);
+              if (k1 >= 0) a.dinit[k1] = f32_to_bf16(v[h].y);
             }
           }
         }
@@ -645,7 +652,9 @@ __global__ void __launch_bounds__(32 * kFinClasses) wgrad_finalize_kernel(const 
   for (int j = 1; j < kFinClasses; ++j) t += part[j][tx];
   const int d = int(i / (kWidth + 1)), k = int(i % (kWidth + 1));
   if (k < kWidth) {
-    const int64_t off = d * o.dw_sd + k * o.dw_sk;
+    const int kt = k - (kWidth - o.W);  // the weight's own tap; zero taps have none
+    if (kt < 0) return;
+    const int64_t off = d * o.dw_sd + kt * o.dw_sk;
     if (o.dw_f32) static_cast<float*>(o.dw)[off] = t;
     else static_cast<uint16_t*>(o.dw)[off] = f32_to_bf16(t);
   } else if (o.db) {
@@ -732,7 +741,7 @@ cudaError_t launch_bwd(const BwdArgs& a, const BwdPlan& p, int act, const WgradO
   if (empty) {
     err = cudaMemsetAsync(a.ws, 0, size_t(n_acc) * sizeof(float), stream);
     if (err != cudaSuccess) return err;
-    const int64_t n = int64_t(a.seqs.n_seq) * a.D * kState;
+    const int64_t n = int64_t(a.seqs.n_seq) * a.D * a.sw;
     if (a.dinit && n > 0)
       bwd_empty_kernel<<<unsigned((n + 255) / 256), 256, 0, stream>>>(a.dfin, a.dinit, n);
   } else {

@@ -200,10 +200,54 @@ struct Vec<1> {
   __device__ __forceinline__ static Raw pack(const float (&f)[1]) { return f32_to_bf16(f[0]); }
 };
 
-// State rows: V consecutive channels of one sequence's [D][3] block, 3*V
-// contiguous BF16 values, entry (c, i) at c*3 + i.  win[i][c] = state(c, i).
+// States are [S, D, sw] BF16 tensors, sw = W - 1 in 1..3 entries per channel
+// (entry j of channel row r -- r = sequence * D + channel -- at r * sw + j).
+// The kernels embed a width-W filter in width four (leading zero taps) and
+// keep a three-entry window win[i] = xe[i - 3]; for sw < 3 its first 3 - sw
+// entries only ever meet zero taps: they read as 0 and are never written.
+// Element index of window slot i (0..2) of channel row r, or -1 when the
+// state has no such entry.
+__device__ __forceinline__ int64_t state_slot(int64_t r, int i, int sw) {
+  const int j = i - (kState - sw);
+  return j >= 0 ? r * sw + j : -1;
+}
+
+// Narrower states (W < 4), kept out of line so that the width-four kernels'
+// register allocation does not carry them.
 template <int V>
-__device__ __forceinline__ void load_state(const uint16_t* s, float (&win)[kState][V]) {
+__device__ __noinline__ void load_state_narrow(const uint16_t* base, int64_t r, int sw,
+                                               float (&win)[kState][V]) {
+#pragma unroll
+  for (int c = 0; c < V; ++c)
+#pragma unroll
+    for (int i = 0; i < kState; ++i) {
+      const int64_t k = state_slot(r + c, i, sw);
+      win[i][c] = k >= 0 ? bf16_to_f32(__ldg(base + k)) : 0.0f;
+    }
+}
+
+template <int V>
+__device__ __noinline__ void store_state_narrow(uint16_t* base, int64_t r, int sw,
+                                                const float (&win)[kState][V]) {
+#pragma unroll
+  for (int c = 0; c < V; ++c)
+#pragma unroll
+    for (int i = 0; i < kState; ++i) {
+      const int64_t k = state_slot(r + c, i, sw);
+      if (k >= 0) base[k] = f32_to_bf16(win[i][c]);
+    }
+}
+
+// The window of V consecutive channel rows r .. r+V-1: win[i][c] = slot i of
+// row r + c.  Width four (sw = 3) reads 3*V contiguous values as vectors.
+template <int V>
+__device__ __forceinline__ void load_state(const uint16_t* base, int64_t r, int sw,
+                                           float (&win)[kState][V]) {
+  if (sw != kState) {
+    load_state_narrow<V>(base, r, sw, win);
+    return;
+  }
+  const uint16_t* s = base + r * kState;
   if constexpr (V == 8) {  // 48 bytes, 16-byte aligned
     union { uint4 q[3]; uint16_t h[24]; } u;
     const uint4* p = reinterpret_cast<const uint4*>(s);
@@ -228,8 +272,15 @@ __device__ __forceinline__ void load_state(const uint16_t* s, float (&win)[kStat
   }
 }
 
+// Writes the state entries of rows r .. r+V-1 from the window (its last sw slots).
 template <int V>
-__device__ __forceinline__ void store_state(uint16_t* s, const float (&win)[kState][V]) {
+__device__ __forceinline__ void store_state(uint16_t* base, int64_t r, int sw,
+                                            const float (&win)[kState][V]) {
+  if (sw != kState) {
+    store_state_narrow<V>(base, r, sw, win);
+    return;
+  }
+  uint16_t* s = base + r * kState;
   if constexpr (V == 8) {
     union { uint4 q[3]; uint16_t h[24]; } u;
 #pragma unroll
@@ -254,11 +305,12 @@ __device__ __forceinline__ void store_state(uint16_t* s, const float (&win)[kSta
   }
 }
 
-// Pair forms: win[i][h] = (state(2h, i), state(2h+1, i)).
+// Pair forms: win[i][h] = (slot i of row r + 2h, slot i of row r + 2h + 1).
 template <int V>
-__device__ __forceinline__ void load_state2(const uint16_t* s, float2 (&win)[kState][V / 2]) {
+__device__ __forceinline__ void load_state2(const uint16_t* base, int64_t r, int sw,
+                                            float2 (&win)[kState][V / 2]) {
   float f[kState][V];
-  load_state<V>(s, f);
+  load_state<V>(base, r, sw, f);
 #pragma unroll
   for (int i = 0; i < kState; ++i)
 #pragma unroll
@@ -266,13 +318,14 @@ __device__ __forceinline__ void load_state2(const uint16_t* s, float2 (&win)[kSt
 }
 
 template <int V>
-__device__ __forceinline__ void store_state2(uint16_t* s, const float2 (&win)[kState][V / 2]) {
+__device__ __forceinline__ void store_state2(uint16_t* base, int64_t r, int sw,
+                                             const float2 (&win)[kState][V / 2]) {
   float f[kState][V];
 #pragma unroll
   for (int i = 0; i < kState; ++i)
 #pragma unroll
     for (int h = 0; h < V / 2; ++h) { f[i][2 * h] = win[i][h].x; f[i][2 * h + 1] = win[i][h].y; }
-  store_state<V>(s, f);
+  store_state<V>(base, r, sw, f);
 }
 
 // ---- per-thread asynchronous copies, global -> shared ---------------------------
@@ -299,8 +352,9 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 // ---- weights -----------------------------------------------------------------
 
 struct WeightRef {
-  const void* w;    // [D, 4] BF16 or FP32
+  const void* w;    // [D, W] BF16 or FP32, W in 2..4
   int w_f32;
+  int W;            // taps; kernel tap k (0..3) is weight tap k - (4 - W), zero below 0
   int64_t w_sd, w_sk;
   const uint16_t* bias;  // [D] BF16 or nullptr
   int64_t b_sd;
@@ -336,9 +390,12 @@ __device__ __forceinline__ void stage_weights(const WeightRef& r, int d_base, in
         const int64_t d = int64_t(d_base) + i;
         if (d < D) {
           if (k < kWidth) {
-            const int64_t o = d * r.w_sd + k * r.w_sk;
-            v[j] = 0.5f * (r.w_f32 ? __ldg(static_cast<const float*>(r.w) + o)
-                                   : bf16_to_f32(__ldg(static_cast<const uint16_t*>(r.w) + o)));
+            const int kt = k - (kWidth - r.W);  // the weight's own tap
+            if (kt >= 0) {
+              const int64_t o = d * r.w_sd + kt * r.w_sk;
+              v[j] = 0.5f * (r.w_f32 ? __ldg(static_cast<const float*>(r.w) + o)
+                                     : bf16_to_f32(__ldg(static_cast<const uint16_t*>(r.w) + o)));
+            }
           } else if (r.bias) {
             v[j] = 0.5f * bf16_to_f32(__ldg(r.bias + d * r.b_sd));
           }
@@ -461,9 +518,11 @@ __device__ __forceinline__ void load_weights_1(const WeightRef& r, int64_t d, fl
                                                float (&b)[1]) {
 #pragma unroll
   for (int k = 0; k < kWidth; ++k) {
-    const int64_t o = d * r.w_sd + k * r.w_sk;
-    w[0][k] = 0.5f * (r.w_f32 ? __ldg(static_cast<const float*>(r.w) + o)
-                              : bf16_to_f32(__ldg(static_cast<const uint16_t*>(r.w) + o)));
+    const int kt = k - (kWidth - r.W);  // the weight's own tap
+    const int64_t o = d * r.w_sd + kt * r.w_sk;
+    w[0][k] = kt < 0 ? 0.0f
+                     : 0.5f * (r.w_f32 ? __ldg(static_cast<const float*>(r.w) + o)
+                                       : bf16_to_f32(__ldg(static_cast<const uint16_t*>(r.w) + o)));
   }
   b[0] = r.bias ? 0.5f * bf16_to_f32(__ldg(r.bias + d * r.b_sd)) : 0.0f;
 }

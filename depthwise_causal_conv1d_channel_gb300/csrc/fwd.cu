@@ -40,7 +40,7 @@ __device__ __forceinline__ void fwd_walk(const FwdArgs& a, const Seqs& seqs, con
     {
       float init[kState][V];
       if (q - kState < lo && a.init) {
-        load_state<V>(a.init + state_row * kState, init);
+        load_state<V>(a.init, state_row, a.sw, init);
       } else {
 #pragma unroll
         for (int i = 0; i < kState; ++i)
@@ -100,7 +100,7 @@ __device__ __forceinline__ void fwd_walk(const FwdArgs& a, const Seqs& seqs, con
     for (; q < e; ++q) step(VT::ld(a.x + xs.at(n, q)), q);
 
     // the thread that finishes a sequence writes its final state: xe[len-3 .. len-1]
-    if (e == hi && a.fin) store_state<V>(a.fin + state_row * kState, win);
+    if (e == hi && a.fin) store_state<V>(a.fin, state_row, a.sw, win);
     ++n;
   }
 }
@@ -224,7 +224,7 @@ __global__ void __launch_bounds__(kFwdThreads, 3) fwd_clv_kernel(FwdArgs a) {
     {
       float2 init[kState][H];
       if (q - kState < lo && a.init) {
-        load_state2<V>(a.init + state_row * kState, init);
+        load_state2<V>(a.init, state_row, a.sw, init);
       } else {
 #pragma unroll
         for (int i = 0; i < kState; ++i)
@@ -304,7 +304,7 @@ __global__ void __launch_bounds__(kFwdThreads, 3) fwd_clv_kernel(FwdArgs a) {
           if (k * G + u < n_tok) shift_step(r[u], om + u * ost);
       }
     }
-    if (e == hi && a.fin) store_state2<V>(a.fin + state_row * kState, W);
+    if (e == hi && a.fin) store_state2<V>(a.fin, state_row, a.sw, W);
     q = e;
     ++n;
   }
@@ -393,7 +393,7 @@ static cudaError_t launch_fwd_act(const FwdArgs& a, const FwdPlan& p, cudaStream
 
 cudaError_t launch_fwd(const FwdArgs& a, const FwdPlan& p, int act, cudaStream_t stream) {
   if (a.seqs.Q == 0) {
-    const int64_t n = int64_t(a.seqs.n_seq) * a.D * kState;
+    const int64_t n = int64_t(a.seqs.n_seq) * a.D * a.sw;
     if (a.fin && n > 0)
       fwd_empty_kernel<<<unsigned((n + 255) / 256), 256, 0, stream>>>(a.init, a.fin, n);
     return cudaGetLastError();

@@ -35,8 +35,9 @@ struct FwdArgs {
   int64_t x_sb, x_sd, x_st;  // element strides of x ([B, D, T] view)
   int64_t o_sb, o_sd, o_st;
   WeightRef wr;
-  const uint16_t* init;  // [S, D, 3] contiguous or nullptr
-  uint16_t* fin;         // [S, D, 3] contiguous or nullptr
+  const uint16_t* init;  // [S, D, sw] contiguous or nullptr
+  uint16_t* fin;         // [S, D, sw] contiguous or nullptr
+  int sw;                // state entries per channel: W - 1
   Seqs seqs;
   int B, D;
   int64_t seg_len, n_seg;  // channel-last: tokens per thread range, number of ranges
@@ -44,8 +45,9 @@ struct FwdArgs {
 };
 
 struct WgradOut {
-  void* dw;          // [D, 4] BF16 or FP32
+  void* dw;          // [D, W] BF16 or FP32
   int dw_f32;
+  int W;             // kernel taps 4 - W .. 3 are the weight's taps 0 .. W-1
   int64_t dw_sd, dw_sk;
   uint16_t* db;      // [D] BF16 or nullptr
   int64_t db_sd;
@@ -59,9 +61,10 @@ struct BwdArgs {
   int64_t g_sb, g_sd, g_st;
   int64_t dx_sb, dx_sd, dx_st;
   WeightRef wr;
-  const uint16_t* init;   // [S, D, 3] or nullptr
-  const uint16_t* dfin;   // [S, D, 3] or nullptr (zero gradient)
-  uint16_t* dinit;        // [S, D, 3] or nullptr
+  const uint16_t* init;   // [S, D, sw] or nullptr
+  const uint16_t* dfin;   // [S, D, sw] or nullptr (zero gradient)
+  uint16_t* dinit;        // [S, D, sw] or nullptr
+  int sw;                 // state entries per channel: W - 1
   Seqs seqs;
   int B, D;
   int64_t seg_len, n_seg;
@@ -84,7 +87,8 @@ using BwdPlan = FwdPlan;
 struct UpdArgs {
   const uint16_t* x;  // [B, D, L], channel stride 1
   int64_t x_sb, x_sl;
-  uint16_t* state;    // [B, D, 3] contiguous
+  uint16_t* state;    // [B, D, sw] contiguous
+  int sw;             // state entries per channel: W - 1
   uint16_t* out;      // [B, D, L], channel stride 1
   int64_t o_sb, o_sl;
   WeightRef wr;

@@ -44,7 +44,7 @@ __global__ void __launch_bounds__(256) update_kernel(UpdArgs a) {
 #pragma unroll
     for (int r = 0; r < R; ++r) {
       if (b0 + r < a.B) {
-        load_state2<V>(a.state + (int64_t(b0 + r) * a.D + d0) * kState, win[r]);
+        load_state2<V>(a.state, int64_t(b0 + r) * a.D + d0, a.sw, win[r]);
         xr[r] = VT::ld(a.x + int64_t(b0 + r) * a.x_sb + d0);
       }
     }
@@ -75,7 +75,7 @@ __global__ void __launch_bounds__(256) update_kernel(UpdArgs a) {
         VT::st(orow + int64_t(l) * a.o_sl, VT::pack2(y));
         cur = nxt;
       }
-      store_state2<V>(a.state + (int64_t(b0 + r) * a.D + d0) * kState, win[r]);
+      store_state2<V>(a.state, int64_t(b0 + r) * a.D + d0, a.sw, win[r]);
     }
   } else {
     float w[V][kWidth], b[V];
@@ -85,7 +85,7 @@ __global__ void __launch_bounds__(256) update_kernel(UpdArgs a) {
 #pragma unroll
     for (int r = 0; r < R; ++r) {
       if (b0 + r < a.B) {
-        load_state<V>(a.state + (int64_t(b0 + r) * a.D + d0) * kState, win[r]);
+        load_state<V>(a.state, int64_t(b0 + r) * a.D + d0, a.sw, win[r]);
         xr[r] = VT::ld(a.x + int64_t(b0 + r) * a.x_sb + d0);
       }
     }
@@ -115,7 +115,7 @@ __global__ void __launch_bounds__(256) update_kernel(UpdArgs a) {
         VT::st(orow + int64_t(l) * a.o_sl, VT::pack(y));
         cur = nxt;
       }
-      store_state<V>(a.state + (int64_t(b0 + r) * a.D + d0) * kState, win[r]);
+      store_state<V>(a.state, int64_t(b0 + r) * a.D + d0, a.sw, win[r]);
     }
   }
 }
@@ -284,7 +284,7 @@ constexpr int kUpdateRows = CCC_UPDATE_ROWS;
 
 cudaError_t launch_update(const UpdArgs& a, int vec, int act, cudaStream_t stream) {
   if (a.B == 0) return cudaSuccess;
-  if (vec == 8 && a.wr.w_vec)
+  if (vec == 8 && a.wr.w_vec && a.sw == kState)  // whole-warp state runs: width four
     return act == kActSilu ? launch_update_w8<kActSilu>(a, stream)
                            : launch_update_w8<kActNone>(a, stream);
   const int64_t groups = (a.D + vec - 1) / vec;

@@ -108,7 +108,7 @@ class _CausalConv1dFn(torch.autograd.Function):
         final = None
         if want_final:
             final = final_states_out if final_states_out is not None else torch.empty(
-                (S, x.shape[1], 3), dtype=x.dtype, device=x.device)
+                (S, x.shape[1], weight.shape[1] - 1), dtype=x.dtype, device=x.device)
         st = _abi.ccc_conv1d_fwd(x, weight, bias, cu_seqlens, initial_states, out, final, act,
                                  status_word(x.device), torch.cuda.current_stream(x.device))
         _raise(st, "causal_conv1d")
@@ -150,10 +150,12 @@ def causal_conv1d(x: torch.Tensor, weight: torch.Tensor, bias: Optional[torch.Te
                   initial_states: Optional[torch.Tensor] = None, return_final_states: bool = False,
                   final_states_out: Optional[torch.Tensor] = None, activation: Optional[str] = "silu",
                   deterministic: Optional[bool] = None):
-    """Depthwise causal conv1d, width 4, BF16 activations.
+    """Depthwise causal conv1d of width W = weight.shape[1] (2..4; four is the
+    page's optimized route), BF16 activations.
 
-    out[b, d, t] = act(bias[d] + sum_k weight[d, k] * xe[b, d, t - 3 + k]) where xe
-    is x preceded by the three initial-state entries (zeros when none).
+    out[b, d, t] = act(bias[d] + sum_k weight[d, k] * xe[b, d, t - (W-1) + k]) where
+    xe is x preceded by the W - 1 initial-state entries (zeros when none);
+    initial_states and final_states are [B or N, D, W - 1].
 
     Returns ``out`` (same shape and strides as x) or ``(out, final_states)`` when
     ``return_final_states`` is set or ``final_states_out`` is given.  Differentiable
@@ -175,7 +177,7 @@ def causal_conv1d_update(x: torch.Tensor, conv_state: torch.Tensor, weight: torc
                          bias: Optional[torch.Tensor] = None, activation: Optional[str] = "silu",
                          out: Optional[torch.Tensor] = None) -> torch.Tensor:
     """Decode step(s): x [B, D] is the new token, or x [B, D, L] the next L
-    tokens of every row; conv_state [B, D, 3] (the layout final_states uses) is
+    tokens of every row; conv_state [B, D, W - 1] (the layout final_states uses) is
     read and mutated in place, token by token, to the last three extended
     inputs.  Returns out shaped like x.  The kernels read each token's D
     channels contiguously: a [B, D, L] x whose channel stride is not 1 is

@@ -110,7 +110,11 @@ def test_fwd_rejects_bad_arguments_on_host():
     bad_x = cl(0, B_, D_, T_)
     bad_x.dtype = F32
     assert fwd(bad_x, g["w"], out=g["out"]) == _abi.CCC_ERR_INVALID_ARG
-    assert fwd(g["x"], T(10 * MB, BF16, (D_, 3)), out=g["out"]) == _abi.CCC_ERR_UNSUPPORTED  # width 3
+    # widths 2..4 are served; 1 and 5 decline
+    assert fwd(g["x"], T(10 * MB, BF16, (D_, 5)), out=g["out"]) == _abi.CCC_ERR_UNSUPPORTED
+    assert fwd(g["x"], T(10 * MB, BF16, (D_, 1)), out=g["out"]) == _abi.CCC_ERR_UNSUPPORTED
+    # a width-3 weight takes [S, D, 2] states
+    assert fwd(g["x"], T(10 * MB, BF16, (D_, 3)), init=g["init"], out=g["out"]) == _abi.CCC_ERR_INVALID_ARG
     assert fwd(g["x"], T(10 * MB, BF16, (D_ + 1, 4)), out=g["out"]) == _abi.CCC_ERR_INVALID_ARG
     # FP32 weight with bias declines (cuDNN page)
     assert fwd(g["x"], T(10 * MB, F32, (D_, 4)), g["b"], out=g["out"]) == _abi.CCC_ERR_UNSUPPORTED

@@ -71,8 +71,8 @@ def test_host_side_errors_raise_python_exceptions(cuda_device):
     d = inp.to(cuda_device)
     with pytest.raises(NotImplementedError):   # FP32 weight with bias declines
         ccc.causal_conv1d(d.x, d.weight.float(), d.bias)
-    with pytest.raises(NotImplementedError):   # width other than four
-        ccc.causal_conv1d(d.x, torch.zeros(16, 3, dtype=torch.bfloat16, device=cuda_device))
+    with pytest.raises(NotImplementedError):   # width outside 2..4
+        ccc.causal_conv1d(d.x, torch.zeros(16, 5, dtype=torch.bfloat16, device=cuda_device))
     with pytest.raises(ValueError):            # final_states_out aliasing x
         ccc.causal_conv1d(d.x, d.weight, d.bias, initial_states=d.initial_states,
                           final_states_out=d.x.transpose(1, 2).reshape(-1)[: 2 * 16 * 3].view(2, 16, 3))

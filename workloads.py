@@ -82,9 +82,10 @@ def make_inputs(B: int, D: int, T: int, *, channel_last: bool = True, seed: int 
                 weight_dtype=BF16, bias: bool = True, initial_states: bool = False,
                 grad: bool = False, dfinal_states: bool = False, lengths=None,
                 activation: Optional[str] = "silu", deterministic: bool = False,
-                x_scale: float = 1.0) -> ConvInputs:
+                x_scale: float = 1.0, width: int = 4) -> ConvInputs:
     """Inputs of one call.  ``lengths`` (list of ints) makes a packed call:
-    B must be 1 and T == sum(lengths).  Draw order: x, weight, bias,
+    B must be 1 and T == sum(lengths).  ``width`` is the filter width W (weight
+    [D, W], states [., D, W - 1]).  Draw order: x, weight, bias,
     initial_states, g, dfinal_states."""
     gen = torch.Generator().manual_seed(seed)
     cu = None
@@ -101,12 +102,12 @@ def make_inputs(B: int, D: int, T: int, *, channel_last: bool = True, seed: int 
         return (_normal(gen, (B, D, T)) * x_scale).to(BF16)
 
     x = act_tensor()
-    w = _uniform(gen, (D, 4), -0.5, 0.5)
+    w = _uniform(gen, (D, width), -0.5, 0.5)
     w = w if weight_dtype == torch.float32 else w.to(BF16)
     b = _uniform(gen, (D,), -0.1, 0.1).to(BF16) if bias else None
-    init = _normal(gen, (n_seq, D, 3)).to(BF16) if initial_states else None
+    init = _normal(gen, (n_seq, D, width - 1)).to(BF16) if initial_states else None
     g = act_tensor() if grad else None
-    gf = _normal(gen, (n_seq, D, 3)).to(BF16) if dfinal_states else None
+    gf = _normal(gen, (n_seq, D, width - 1)).to(BF16) if dfinal_states else None
     return ConvInputs(x=x, weight=w, bias=b, initial_states=init, cu_seqlens=cu, g=g,
                       dfinal_states=gf, activation=activation, channel_last=channel_last,
                       deterministic=deterministic)
