@@ -1,5 +1,6 @@
 /*
- * ccc_conv1d -- depthwise causal conv1d on BF16 activations, width four.
+ * ccc_conv1d -- depthwise causal conv1d on BF16 activations, filter width W in
+ * 2..4 (four is the page's optimized route).
  *
  * C ABI of the CUDA library (libccc_conv1d.so).  All tensor memory is owned by
  * the caller and the library allocates nothing.  Its only global state is a
@@ -9,7 +10,7 @@
  *
  * The operation (cuDNN frontend docs, "Causal Conv1d" page):
  *
- *   out[b,d,t] = act(bias[d] + sum_{k<4} weight[d,k] * xe[b,d,t-3+k])
+ *   out[b,d,t] = act(bias[d] + sum_{k<W} weight[d,k] * xe[b,d,t-(W-1)+k])
  *
  * where xe is x extended on the left by the three entries of initial_states
  * (zeros when none are given); index 0 of the state axis is the oldest entry.
@@ -50,7 +51,7 @@ extern "C" {
 typedef enum {
     CCC_OK = 0,
     CCC_ERR_INVALID_ARG = 1,      /* NULL where required, bad shape/dtype/rank, unknown enum */
-    CCC_ERR_UNSUPPORTED = 2,      /* well-formed but declined: width != 4, FP32 weight with
+    CCC_ERR_UNSUPPORTED = 2,      /* well-formed but declined: width outside 2..4, FP32 weight with
                                      bias, strides this library does not read, B != 1 when packed */
     CCC_ERR_ALIAS = 3,            /* an output overlaps an input or another output */
     CCC_ERR_NONDETERMINISTIC = 4, /* deterministic backward requested with a bias */
@@ -84,17 +85,20 @@ typedef struct {
  *                       [B, T, D] storage; stride[2] >= D);
  *                     time-contiguous: stride[2] == 1.
  *                   Any other layout returns CCC_ERR_UNSUPPORTED.
- *   weight          [D, 4] BF16, or FP32 only when bias is NULL (the page
- *                   declines FP32 weight with bias); any strides.
+ *   weight          [D, W] BF16, W in 2..4 (the page's tensor list gives
+ *                   weight[D, W]; its optimized route is W = 4), or FP32 only
+ *                   when bias is NULL (the page declines FP32 weight with
+ *                   bias); any strides.  Every state below is [S, D, W - 1].
  *   bias            [D] BF16 or NULL.
  *   cu_seqlens      [N + 1] int32 or NULL.  When given, x has B == 1 and holds
  *                   N sequences back to back along T; no tap reads across a
  *                   boundary.  Validated on the device (see above): offsets
  *                   start at 0, end at T, and strictly increase.
- *   initial_states  [S, D, 3] BF16 contiguous or NULL; S = B (dense) or N (packed).
+ *   initial_states  [S, D, W-1] BF16 contiguous or NULL; S = B (dense) or N (packed).
  *   out             [B, D, T] BF16, same layout kind as x (its own strides).
- *   final_states    [S, D, 3] BF16 contiguous or NULL: xe[T-3 .. T-1] of each
- *                   sequence, a bitwise copy (initial-state entries when T < 3).
+ *   final_states    [S, D, W-1] BF16 contiguous or NULL: xe[T-W+1 .. T-1] of
+ *                   each sequence, a bitwise copy (initial-state entries when
+ *                   T < W - 1).
  *                   Must not overlap x, weight, bias, cu_seqlens or
  *                   initial_states (CCC_ERR_ALIAS, the page's aliasing rule).
  *   activation      ccc_act.
@@ -122,11 +126,11 @@ size_t ccc_conv1d_bwd_workspace_size(const ccc_tensor *x, int deterministic);
  *
  *   x, weight, bias, cu_seqlens, initial_states   as in ccc_conv1d_fwd.
  *   dout            [B, D, T] BF16, same layout kind as x: dL/dout.
- *   dfinal_states   [S, D, 3] BF16 contiguous or NULL (NULL = zero gradient).
+ *   dfinal_states   [S, D, W-1] BF16 contiguous or NULL (NULL = zero gradient).
  *   dx              [B, D, T] BF16, same layout kind as x.
- *   dweight         [D, 4], dtype of weight, any strides.
+ *   dweight         [D, W], dtype of weight, any strides.
  *   dbias           [D] BF16; required when bias is given, else must be NULL.
- *   dinitial_states [S, D, 3] BF16 contiguous or NULL (allowed only with
+ *   dinitial_states [S, D, W-1] BF16 contiguous or NULL (allowed only with
  *                   initial_states).
  *   deterministic   0 or 1.  The page's rule is kept: 1 (the deterministic
  *                   route) is declined for calls with a bias
@@ -190,11 +194,12 @@ ccc_status ccc_conv1d_bwd_noalloc(const ccc_tensor *x, const ccc_tensor *weight,
  *
  *   x           [B, D] BF16 (one token per row) or [B, D, L] BF16 (L >= 0 tokens
  *               per row, any token stride), stride[1] == 1.
- *   conv_state  [B, D, 3] BF16 contiguous, read and overwritten in place: after
- *               each token, [s1, s2, x] (bitwise): the layout final_states uses.
- *   weight      [D, 4] as in ccc_conv1d_fwd;  bias [D] BF16 or NULL.
+ *   conv_state  [B, D, W-1] BF16 contiguous, read and overwritten in place: after
+ *               each token, [s1 .. s(W-2), x] (bitwise): the layout final_states
+ *               uses.
+ *   weight      [D, W] as in ccc_conv1d_fwd;  bias [D] BF16 or NULL.
  *   out         shaped like x, stride[1] == 1; for each token in order:
- *               act(bias + w0*s0 + w1*s1 + w2*s2 + w3*x).
+ *               act(bias + sum_{k<W-1} w_k*s_k + w_(W-1)*x).
  *
  * The result equals ccc_conv1d_fwd over the L tokens with conv_state as the
  * initial state and the new state as the final state, bitwise.  L == 0 (or
