@@ -47,8 +47,8 @@ L2_BYTES = 129 * 2 ** 20
 # per launch.  Valid only for the kernel sources whose digest is recorded here.
 # The capture flushes caches before each launch; the 25 MB dx written to L2 is
 # mostly not yet written back when the kernel ends, so writes are undercounted.
-TRAFFIC = {"sources_sha256": "be160c0ecbf96988e7d6d3091885892aae8ad86675ff95f33f86f4365f77c426",
-           "bytes_per_launch": (50432768 + 1113088) + (1512704 + 0)}
+TRAFFIC = {"sources_sha256": "0c5fd61aa11d1f3f7b7c4a088cc4fdca9017c1053bab907fa499b34a22cfd7c0",
+           "bytes_per_launch": (50438912 + 985088) + (1512960 + 0)}
 
 
 def kernel_sources_digest() -> str:
