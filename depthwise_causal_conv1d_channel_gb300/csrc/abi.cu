@@ -207,6 +207,18 @@ int bwd_preferred_vec(int64_t Q, int D, int sm_count) {
   return tokens_per_thread >= 128 ? 8 : 4;
 }
 
+// Time-contiguous dense tensors whose rows are 16-byte aligned runs of a
+// multiple of 8 tokens: the warp-per-row kernels take 8 tokens a lane.
+bool bdt_vec_ok(const Problem& pb, std::initializer_list<const ccc_tensor*> acts) {
+  if (pb.layout != ccc::kLayoutTimeContiguous || pb.packed || pb.T % 8 != 0) return false;
+  for (const ccc_tensor* t : acts) {
+    int64_t sb, sd, st;
+    act_strides(t, pb.layout, sb, sd, st);
+    if (!aligned(t->data, 16) || sb % 8 != 0 || sd % 8 != 0 || st != 1) return false;
+  }
+  return true;
+}
+
 // Channels per thread: the preferred width when the tensors allow it, else 4,
 // else 1 (scalar).
 int pick_vec(int preferred, const Problem& pb, std::initializer_list<const ccc_tensor*> acts,
@@ -285,7 +297,11 @@ static FwdPlan plan_bdt(int64_t rows) {
 }
 
 FwdPlan plan_fwd(int kind, int vec, int64_t Q, int D, int64_t rows, int sm_count) {
-  if (kind == kLayoutTimeContiguous) return plan_bdt(rows);
+  if (kind == kLayoutTimeContiguous) {
+    FwdPlan p = plan_bdt(rows);
+    p.vec = vec;  // 8: 16-byte token chunks per lane
+    return p;
+  }
   // segments of a multiple of six tokens: the vector kernel's ring groups then
   // cover a segment inside a sequence exactly
   return plan_cl(vec, Q, D, sm_count, fwd_blocks_per_sm(vec), 1, 12, 256, vec == 4 ? 6 : 1);
@@ -358,7 +374,8 @@ ccc_status ccc_conv1d_fwd(const ccc_tensor* x, const ccc_tensor* weight, const c
   a.D = pb.D;
   a.status = d_status;
   if (pb.n_seq == 0) return CCC_OK;
-  const int vec = pick_vec(4, pb, {x, out}, {initial_states, final_states});
+  const int vec = pb.layout == ccc::kLayoutTimeContiguous ? (bdt_vec_ok(pb, {x, out}) ? 8 : 1)
+                                                          : pick_vec(4, pb, {x, out}, {initial_states, final_states});
   const int64_t rows = pb.packed ? pb.D : int64_t(pb.B) * pb.D;
   const ccc::FwdPlan p = ccc::plan_fwd(pb.layout, vec, a.seqs.Q, pb.D, rows, sms);
   a.seg_len = p.seg_len;

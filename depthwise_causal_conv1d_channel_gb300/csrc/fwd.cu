@@ -310,6 +310,76 @@ __global__ void __launch_bounds__(kFwdThreads, 3) fwd_clv_kernel(FwdArgs a) {
   }
 }
 
+// Time-contiguous x, dense, T a multiple of 8 and 16-byte aligned rows (the
+// usual contiguous [B, D, T] tensor).  One warp per (batch, channel) row; each
+// lane takes 8 consecutive tokens per step with one 16-byte load and one
+// 16-byte store, so a warp moves 256 tokens (512 contiguous bytes) a step.
+// The three inputs before a lane's chunk are the previous lane's last three,
+// passed by shuffle; lane 0 takes them from the previous step's lane 31, or
+// from the initial state.  The next step's chunk is loaded while this one is
+// computed.  Same per-element operations as every other forward path.
+template <int ACT>
+__global__ void __launch_bounds__(256) fwd_bdt8_kernel(FwdArgs a) {
+  pdl_wait();     // inputs may come from the previous kernel in the stream
+  pdl_release();
+  using VT = Vec<8>;
+  const unsigned kAll = 0xffffffffu;
+  const int lane = threadIdx.x & 31;
+  const int64_t row = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (row >= int64_t(a.B) * a.D) return;  // the whole warp shares the row
+  const int bb = int(row / a.D), d = int(row % a.D);
+  float w[1][kWidth], b[1];
+  load_weights_1(a.wr, d, w, b);
+  const int64_t T = a.seqs.T;
+  const uint16_t* xr = a.x + bb * a.x_sb + d * a.x_sd;
+  uint16_t* orow = a.out + bb * a.o_sb + d * a.o_sd;
+  float carry[kState];  // xe[-3 .. -1] before the row's first token
+  {
+    float init[kState][1] = {{0.0f}, {0.0f}, {0.0f}};
+    if (a.init) load_state<1>(a.init, row, a.sw, init);
+#pragma unroll
+    for (int i = 0; i < kState; ++i) carry[i] = init[i][0];
+  }
+  typename VT::Raw nxt = make_uint4(0, 0, 0, 0);
+  if (int64_t(lane) * 8 < T) nxt = VT::ld(xr + lane * 8);
+  for (int64_t base = 0; base < T; base += 256) {
+    const int64_t t0 = base + lane * 8;
+    const bool valid = t0 < T;
+    const typename VT::Raw cur = nxt;
+    if (t0 + 256 < T) nxt = VT::ld(xr + t0 + 256);
+    float c[8];
+    VT::unpack(cur, c);
+    float win[kState];
+#pragma unroll
+    for (int i = 0; i < kState; ++i) {
+      win[i] = __shfl_up_sync(kAll, c[8 - kState + i], 1);
+      if (lane == 0) win[i] = carry[i];
+    }
+    float y[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      float p = b[0];
+      p = fmaf(w[0][0], win[0], p);
+      p = fmaf(w[0][1], win[1], p);
+      p = fmaf(w[0][2], win[2], p);
+      p = fmaf(w[0][3], c[u], p);
+      y[u] = act_fwd<ACT>(p);
+      win[0] = win[1];
+      win[1] = win[2];
+      win[2] = c[u];
+    }
+    if (valid) VT::st(orow + t0, VT::pack(y));
+    if (valid && t0 + 8 == T && a.fin) {  // the row's last chunk: xe[T-3 .. T-1]
+      float fin[kState][1];
+#pragma unroll
+      for (int i = 0; i < kState; ++i) fin[i][0] = c[8 - kState + i];
+      store_state<1>(a.fin, row, a.sw, fin);
+    }
+#pragma unroll
+    for (int i = 0; i < kState; ++i) carry[i] = __shfl_sync(kAll, c[8 - kState + i], 31);
+  }
+}
+
 // Time-contiguous x (stride of T is 1).  One warp per (batch, channel) row;
 // lane l walks tokens [8l + 256i, 8l + 256i + 8).
 template <int ACT>
@@ -388,6 +458,7 @@ static cudaError_t launch_fwd_act(const FwdArgs& a, const FwdPlan& p, cudaStream
     }
     return launch_kernel(fwd_cl_kernel<1, ACT>, grid, block, 0, stream, true, a);
   }
+  if (p.vec == 8) return launch_kernel(fwd_bdt8_kernel<ACT>, dim3(p.gx), dim3(256), 0, stream, true, a);
   return launch_kernel(fwd_bdt_kernel<ACT>, dim3(p.gx), dim3(256), 0, stream, true, a);
 }
 

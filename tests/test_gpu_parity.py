@@ -78,6 +78,10 @@ DENSE_CASES = [
     (2, 40, 300, False, dict(initial_states=True, grad=True, dfinal_states=True)),     # [B, D, T]
     (2, 64, 128, False, dict(grad=True)),
     (1, 33, 7, False, dict(initial_states=True, grad=True, bias=False, weight_dtype=torch.float32)),
+    # time-contiguous rows of a multiple of 8 tokens: 8 tokens a lane, warp steps of 256
+    (3, 24, 264, False, dict(initial_states=True, grad=True, dfinal_states=True)),
+    (2, 16, 512, False, dict(initial_states=True, grad=True)),
+    (1, 8, 2056, False, dict(grad=True, activation=None)),
 ]
 
 
@@ -140,6 +144,28 @@ def test_packed_without_state(cuda_device):
     res = gpu_run(inp, cuda_device)
     check_fwd(inp, res)
     check_bwd(inp, res)
+
+
+def test_time_contiguous_unaligned_rows_take_the_scalar_path(cuda_device):
+    """A [B, D, T] view starting one element into its storage: rows are not
+    16-byte aligned, so the per-token kernel runs; results match the oracle."""
+    B, D, T = 2, 16, 64
+    inp = make_inputs(B, D, T, channel_last=False, seed=77, initial_states=True, grad=True)
+    big = torch.zeros(B * D * T + 8, dtype=torch.bfloat16)
+    big[1:1 + B * D * T] = inp.x.reshape(-1)
+    x_un = big[1:1 + B * D * T].view(B, D, T)
+    d = inp.to(cuda_device)
+    xg = big.to(cuda_device)[1:1 + B * D * T].view(B, D, T).detach().requires_grad_(True)
+    assert xg.data_ptr() % 16 != 0
+    out, fin = ccc.causal_conv1d(xg, d.weight, d.bias, initial_states=d.initial_states,
+                                 return_final_states=True)
+    out.backward(d.g)
+    ccc.check_status(cuda_device)
+    ref = oracle_fwd(inp)
+    assert_bf16_close(bits(out.detach().cpu()), ref["out"], "out")
+    assert_bits_equal(bits(fin.cpu()), ref["final"], "final")
+    assert_bf16_close(bits(xg.grad.cpu()), oracle_bwd(inp)["dx"], "dx")
+    assert torch.equal(x_un, inp.x)
 
 
 def test_unaligned_base_pointer_uses_scalar_path(cuda_device):

@@ -51,6 +51,7 @@ CASES = [
     (1, 136, 0, [7, 1, 40, 2], True, torch.float32, False),
     (2, 48, 50, None, False, torch.bfloat16, True),
     (1, 24, 0, [5, 9, 1], False, torch.bfloat16, True),
+    (2, 16, 264, None, False, torch.bfloat16, True),   # time-contiguous, 8 tokens a lane
 ]
 
 
