@@ -308,7 +308,11 @@ FwdPlan plan_fwd(int kind, int vec, int64_t Q, int D, int64_t rows, int sm_count
 }
 
 BwdPlan plan_bwd(int kind, int vec, int64_t Q, int D, int64_t rows, int sm_count) {
-  if (kind == kLayoutTimeContiguous) return plan_bdt(rows);
+  if (kind == kLayoutTimeContiguous) {
+    BwdPlan p = plan_bdt(rows);
+    p.vec = vec;  // 8: 16-byte token chunks per lane
+    return p;
+  }
   // segments of a multiple of three tokens: the vector kernel's steady groups
   // of three then cover a whole segment inside a sequence, head and tail included
   return plan_cl(vec, Q, D, sm_count, bwd_blocks_per_sm(vec), 1, 18, bwd_block_threads(vec), 3);
@@ -461,8 +465,10 @@ ccc_status ccc_conv1d_bwd(const ccc_tensor* x, const ccc_tensor* weight, const c
   const int sms = device_sm_count();
   if (sms <= 0) return CCC_ERR_CUDA;
   const int64_t Q = pb.packed ? pb.T : int64_t(pb.B) * pb.T;
-  const int vec = pick_vec(bwd_preferred_vec(Q, pb.D, sms), pb, {x, dout, dx},
-                           {initial_states, dfinal_states, dinitial_states});
+  const int vec = pb.layout == ccc::kLayoutTimeContiguous
+                      ? (bdt_vec_ok(pb, {x, dout, dx}) ? 8 : 1)
+                      : pick_vec(bwd_preferred_vec(Q, pb.D, sms), pb, {x, dout, dx},
+                                 {initial_states, dfinal_states, dinitial_states});
   ccc::BwdPlan p{};
   if (!bwd_plan_for(x, pb, vec, p)) return CCC_ERR_CUDA;
   const size_t need = bwd_ws_bytes(p, pb, deterministic);

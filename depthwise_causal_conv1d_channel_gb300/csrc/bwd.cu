@@ -616,6 +616,142 @@ __global__ void __launch_bounds__(256) bwd_bdt_kernel(BwdArgs a) {
   }
 }
 
+// Time-contiguous, dense, T a multiple of 8 and 16-byte aligned rows: one warp
+// per (batch, channel) row, each lane 8 consecutive tokens per step (16-byte
+// loads of x and grad_out, 16-byte stores of dx), a warp step 256 tokens.  A
+// lane's dx rows need gp2 of the three tokens after its chunk: every lane
+// recomputes those from the next lane's first three x and grad_out values
+// (shuffled down; lane 31 takes them from lane 0's prefetched next chunk).  The
+// inputs before a chunk come from the previous lane (lane 0: the previous
+// step's lane 31, or the initial state).  The row's sums are reduced across the
+// warp in a fixed butterfly order; partial row = batch index.
+template <int ACT>
+__global__ void __launch_bounds__(256) bwd_bdt8_kernel(BwdArgs a) {
+  pdl_wait();  // inputs may come from the previous kernel in the stream
+  using VT = Vec<8>;
+  const unsigned kAll = 0xffffffffu;
+  const int lane = threadIdx.x & 31;
+  const int64_t row = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (row >= int64_t(a.B) * a.D) return;  // the whole warp shares the row
+  const int bb = int(row / a.D), d = int(row % a.D);
+  float w[1][kWidth], b[1];
+  load_weights_1(a.wr, d, w, b);
+  const float w0 = w[0][0], w1 = w[0][1], w2 = w[0][2], w3 = w[0][3];
+  const int64_t T = a.seqs.T;
+  const uint16_t* xr = a.x + bb * a.x_sb + d * a.x_sd;
+  const uint16_t* gr = a.g + bb * a.g_sb + d * a.g_sd;
+  uint16_t* dxr = a.dx + bb * a.dx_sb + d * a.dx_sd;
+  float carry[kState];  // xe[t0 - 3 .. t0 - 1] for lane 0
+  {
+    float init[kState][1] = {{0.0f}, {0.0f}, {0.0f}};
+    if (a.init) load_state<1>(a.init, row, a.sw, init);
+#pragma unroll
+    for (int i = 0; i < kState; ++i) carry[i] = init[i][0];
+  }
+  float aw[kWidth] = {0.0f, 0.0f, 0.0f, 0.0f}, ab = 0.0f;
+  typename VT::Raw xn = make_uint4(0, 0, 0, 0), gn = make_uint4(0, 0, 0, 0);
+  if (int64_t(lane) * 8 < T) { xn = VT::ld(xr + lane * 8); gn = VT::ld(gr + lane * 8); }
+  for (int64_t base = 0; base < T; base += 256) {
+    const int64_t t0 = base + lane * 8;
+    const bool valid = t0 < T;
+    const typename VT::Raw xcur = xn, gcur = gn;
+    if (t0 + 256 < T) { xn = VT::ld(xr + t0 + 256); gn = VT::ld(gr + t0 + 256); }
+    // xe[t0 - 3 .. t0 + 10] and grad_out[t0 .. t0 + 10]
+    float xe[14], gv[11];
+    {
+      float cx[8], cg[8];
+      VT::unpack(xcur, cx);
+      VT::unpack(gcur, cg);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) { xe[3 + u] = cx[u]; gv[u] = cg[u]; }
+    }
+    {
+      float nx[8], ng[8];  // lane 0's next chunk, for lane 31
+      VT::unpack(xn, nx);
+      VT::unpack(gn, ng);
+#pragma unroll
+      for (int i = 0; i < kState; ++i) {
+        const float px = __shfl_up_sync(kAll, xe[3 + 8 - kState + i], 1);
+        xe[i] = lane == 0 ? carry[i] : px;
+        const float dxv = __shfl_down_sync(kAll, xe[3 + i], 1);
+        const float dgv = __shfl_down_sync(kAll, gv[i], 1);
+        const float lx = __shfl_sync(kAll, nx[i], 0);
+        const float lg = __shfl_sync(kAll, ng[i], 0);
+        const bool more = t0 + 8 < T;  // the row goes on after this chunk
+        xe[11 + i] = !more ? 0.0f : lane == 31 ? lx : dxv;
+        gv[8 + i] = !more ? 0.0f : lane == 31 ? lg : dgv;
+      }
+    }
+    // gp2 for tokens t0 .. t0 + 10 (beyond the row: zero)
+    float gp[11];
+#pragma unroll
+    for (int u = 0; u < 11; ++u) {
+      float p = b[0];
+      p = fmaf(w0, xe[u], p);
+      p = fmaf(w1, xe[u + 1], p);
+      p = fmaf(w2, xe[u + 2], p);
+      p = fmaf(w3, xe[u + 3], p);
+      gp[u] = act_bwd<ACT>(p, gv[u]);
+    }
+    if (t0 + 8 >= T) {
+#pragma unroll
+      for (int u = 8; u < 11; ++u) gp[u] = 0.0f;
+    }
+    if (valid) {
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        aw[0] = fmaf(gp[u], xe[u], aw[0]);
+        aw[1] = fmaf(gp[u], xe[u + 1], aw[1]);
+        aw[2] = fmaf(gp[u], xe[u + 2], aw[2]);
+        aw[3] = fmaf(gp[u], xe[u + 3], aw[3]);
+        ab += gp[u];
+      }
+      // dx[t0 + u] = w3 gp[u] + w2 gp[u+1] + w1 gp[u+2] + w0 gp[u+3] (halved weights)
+      float v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        float acc = w3 * gp[u];
+        acc = fmaf(w2, gp[u + 1], acc);
+        acc = fmaf(w1, gp[u + 2], acc);
+        acc = fmaf(w0, gp[u + 3], acc);
+        v[u] = acc;
+      }
+      if (a.dfin && t0 + 8 == T) {  // the last three positions take dfinal_states
+#pragma unroll
+        for (int i = 0; i < kState; ++i) {
+          const int64_t k = state_slot(row, i, a.sw);
+          if (k >= 0) v[8 - kState + i] += bf16_to_f32(__ldg(a.dfin + k));
+        }
+      }
+      VT::st(dxr + t0, VT::pack(v));
+      if (t0 == 0 && a.dinit) {  // dinit[j + 3] = dxe[j], j = -3 .. -1 (gp before 0 is zero)
+        const float g3[kState + 3] = {0.0f, 0.0f, 0.0f, gp[0], gp[1], gp[2]};
+#pragma unroll
+        for (int i = 0; i < kState; ++i) {
+          float acc = w3 * g3[i];
+          acc = fmaf(w2, g3[i + 1], acc);
+          acc = fmaf(w1, g3[i + 2], acc);
+          acc = fmaf(w0, g3[i + 3], acc);
+          const int64_t k = state_slot(row, i, a.sw);
+          if (k >= 0) a.dinit[k] = f32_to_bf16(acc);
+        }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kState; ++i) carry[i] = __shfl_sync(kAll, xe[3 + 8 - kState + i], 31);
+  }
+  pdl_release();
+  // the sums are of gp2 = 2 gp: halve them (exact)
+  float vs[kWidth + 1] = {0.5f * aw[0], 0.5f * aw[1], 0.5f * aw[2], 0.5f * aw[3], 0.5f * ab};
+#pragma unroll
+  for (int k = 0; k < kWidth + 1; ++k)
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) vs[k] += __shfl_xor_sync(kAll, vs[k], off);
+  if (lane == 0) {
+    for (int k = 0; k < kWidth + 1; ++k) a.ws[(int64_t(bb) * a.D + d) * (kWidth + 1) + k] = vs[k];
+  }
+}
+
 // dweight/dbias from R rows of FP32 partial sums ws[r][D][5].  A block takes
 // 32 consecutive values in eight row classes: thread (value v, class c) adds
 // rows c, c + 8, c + 16, ... in increasing order (loads issued eight at a
@@ -726,6 +862,7 @@ static cudaError_t launch_bwd_act(const BwdArgs& a, const BwdPlan& p, bool pdl,
     if (p.vec == 4) return launch_kernel(bwd_clv_kernel<4, ACT>, grid, block, smem, stream, pdl, a);
     return launch_kernel(bwd_cl_kernel<1, ACT>, grid, block, smem, stream, pdl, a);
   }
+  if (p.vec == 8) return launch_kernel(bwd_bdt8_kernel<ACT>, dim3(p.gx), dim3(256), 0, stream, pdl, a);
   return launch_kernel(bwd_bdt_kernel<ACT>, dim3(p.gx), dim3(256), 0, stream, pdl, a);
 }
 
