@@ -618,13 +618,15 @@ __global__ void __launch_bounds__(256) bwd_bdt_kernel(BwdArgs a) {
 
 // Time-contiguous, dense, T a multiple of 8 and 16-byte aligned rows: one warp
 // per (batch, channel) row, each lane 8 consecutive tokens per step (16-byte
-// loads of x and grad_out, 16-byte stores of dx), a warp step 256 tokens.  A
-// lane's dx rows need gp2 of the three tokens after its chunk: every lane
-// recomputes those from the next lane's first three x and grad_out values
-// (shuffled down; lane 31 takes them from lane 0's prefetched next chunk).  The
-// inputs before a chunk come from the previous lane (lane 0: the previous
-// step's lane 31, or the initial state).  The row's sums are reduced across the
-// warp in a fixed butterfly order; partial row = batch index.
+// loads of x and grad_out, 16-byte stores of dx), a warp step 256 tokens.  The
+// steps are software-pipelined by one: step s computes gp2 (and the weight
+// sums) of chunk s + 1 and emits the dx rows of chunk s, whose last three need
+// gp2 of the three tokens after the chunk -- the next lane's first three of
+// chunk s (shuffled down), or for lane 31 lane 0's of chunk s + 1.  The inputs
+// before a chunk come from the previous lane (lane 0: lane 31 of the previous
+// chunk, or the initial state).  Every gp2 is computed once.  The row's sums
+// are reduced across the warp in a fixed butterfly order; partial row = batch
+// index.
 template <int ACT>
 __global__ void __launch_bounds__(256) bwd_bdt8_kernel(BwdArgs a) {
   pdl_wait();  // inputs may come from the previous kernel in the stream
@@ -641,7 +643,7 @@ __global__ void __launch_bounds__(256) bwd_bdt8_kernel(BwdArgs a) {
   const uint16_t* xr = a.x + bb * a.x_sb + d * a.x_sd;
   const uint16_t* gr = a.g + bb * a.g_sb + d * a.g_sd;
   uint16_t* dxr = a.dx + bb * a.dx_sb + d * a.dx_sd;
-  float carry[kState];  // xe[t0 - 3 .. t0 - 1] for lane 0
+  float carry[kState];  // for lane 0: xe of the three tokens before its next chunk
   {
     float init[kState][1] = {{0.0f}, {0.0f}, {0.0f}};
     if (a.init) load_state<1>(a.init, row, a.sw, init);
@@ -649,53 +651,32 @@ __global__ void __launch_bounds__(256) bwd_bdt8_kernel(BwdArgs a) {
     for (int i = 0; i < kState; ++i) carry[i] = init[i][0];
   }
   float aw[kWidth] = {0.0f, 0.0f, 0.0f, 0.0f}, ab = 0.0f;
-  typename VT::Raw xn = make_uint4(0, 0, 0, 0), gn = make_uint4(0, 0, 0, 0);
-  if (int64_t(lane) * 8 < T) { xn = VT::ld(xr + lane * 8); gn = VT::ld(gr + lane * 8); }
-  for (int64_t base = 0; base < T; base += 256) {
-    const int64_t t0 = base + lane * 8;
+
+  // gp2 of the chunk at t0 (zero for t0 >= T); accumulates the weight sums
+  auto chunk_gp = [&](int64_t t0, typename VT::Raw xraw, typename VT::Raw graw, float (&gp)[8]) {
+    float xe[11], gv[8];
+    {
+      float cx[8];
+      VT::unpack(xraw, cx);
+      VT::unpack(graw, gv);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) xe[3 + u] = cx[u];
+    }
+#pragma unroll
+    for (int i = 0; i < kState; ++i) {
+      const float px = __shfl_up_sync(kAll, xe[3 + 8 - kState + i], 1);
+      xe[i] = lane == 0 ? carry[i] : px;
+      carry[i] = __shfl_sync(kAll, xe[3 + 8 - kState + i], 31);
+    }
     const bool valid = t0 < T;
-    const typename VT::Raw xcur = xn, gcur = gn;
-    if (t0 + 256 < T) { xn = VT::ld(xr + t0 + 256); gn = VT::ld(gr + t0 + 256); }
-    // xe[t0 - 3 .. t0 + 10] and grad_out[t0 .. t0 + 10]
-    float xe[14], gv[11];
-    {
-      float cx[8], cg[8];
-      VT::unpack(xcur, cx);
-      VT::unpack(gcur, cg);
 #pragma unroll
-      for (int u = 0; u < 8; ++u) { xe[3 + u] = cx[u]; gv[u] = cg[u]; }
-    }
-    {
-      float nx[8], ng[8];  // lane 0's next chunk, for lane 31
-      VT::unpack(xn, nx);
-      VT::unpack(gn, ng);
-#pragma unroll
-      for (int i = 0; i < kState; ++i) {
-        const float px = __shfl_up_sync(kAll, xe[3 + 8 - kState + i], 1);
-        xe[i] = lane == 0 ? carry[i] : px;
-        const float dxv = __shfl_down_sync(kAll, xe[3 + i], 1);
-        const float dgv = __shfl_down_sync(kAll, gv[i], 1);
-        const float lx = __shfl_sync(kAll, nx[i], 0);
-        const float lg = __shfl_sync(kAll, ng[i], 0);
-        const bool more = t0 + 8 < T;  // the row goes on after this chunk
-        xe[11 + i] = !more ? 0.0f : lane == 31 ? lx : dxv;
-        gv[8 + i] = !more ? 0.0f : lane == 31 ? lg : dgv;
-      }
-    }
-    // gp2 for tokens t0 .. t0 + 10 (beyond the row: zero)
-    float gp[11];
-#pragma unroll
-    for (int u = 0; u < 11; ++u) {
+    for (int u = 0; u < 8; ++u) {
       float p = b[0];
       p = fmaf(w0, xe[u], p);
       p = fmaf(w1, xe[u + 1], p);
       p = fmaf(w2, xe[u + 2], p);
       p = fmaf(w3, xe[u + 3], p);
-      gp[u] = act_bwd<ACT>(p, gv[u]);
-    }
-    if (t0 + 8 >= T) {
-#pragma unroll
-      for (int u = 8; u < 11; ++u) gp[u] = 0.0f;
+      gp[u] = valid ? act_bwd<ACT>(p, gv[u]) : 0.0f;
     }
     if (valid) {
 #pragma unroll
@@ -706,14 +687,40 @@ __global__ void __launch_bounds__(256) bwd_bdt8_kernel(BwdArgs a) {
         aw[3] = fmaf(gp[u], xe[u + 3], aw[3]);
         ab += gp[u];
       }
+    }
+  };
+
+  const typename VT::Raw zero = make_uint4(0, 0, 0, 0);
+  auto ld = [&](const uint16_t* r, int64_t t) { return t < T ? VT::ld(r + t) : zero; };
+  float gp_cur[8];
+  chunk_gp(lane * 8, ld(xr, lane * 8), ld(gr, lane * 8), gp_cur);
+  typename VT::Raw xn = ld(xr, 256 + lane * 8), gn = ld(gr, 256 + lane * 8);
+  for (int64_t base = 0; base < T; base += 256) {
+    const int64_t t0 = base + lane * 8;
+    const typename VT::Raw xnn = ld(xr, t0 + 512), gnn = ld(gr, t0 + 512);  // two chunks ahead
+    float gp_next[8];
+    chunk_gp(t0 + 256, xn, gn, gp_next);
+    xn = xnn;
+    gn = gnn;
+    // gp2 of the three tokens after this lane's chunk
+    float ga[kState];
+#pragma unroll
+    for (int i = 0; i < kState; ++i) {
+      const float down = __shfl_down_sync(kAll, gp_cur[i], 1);
+      const float wrap = __shfl_sync(kAll, gp_next[i], 0);
+      ga[i] = lane == 31 ? wrap : down;
+    }
+    if (t0 < T) {
+      const float g11[11] = {gp_cur[0], gp_cur[1], gp_cur[2], gp_cur[3], gp_cur[4], gp_cur[5],
+                             gp_cur[6], gp_cur[7], ga[0], ga[1], ga[2]};
       // dx[t0 + u] = w3 gp[u] + w2 gp[u+1] + w1 gp[u+2] + w0 gp[u+3] (halved weights)
       float v[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        float acc = w3 * gp[u];
-        acc = fmaf(w2, gp[u + 1], acc);
-        acc = fmaf(w1, gp[u + 2], acc);
-        acc = fmaf(w0, gp[u + 3], acc);
+        float acc = w3 * g11[u];
+        acc = fmaf(w2, g11[u + 1], acc);
+        acc = fmaf(w1, g11[u + 2], acc);
+        acc = fmaf(w0, g11[u + 3], acc);
         v[u] = acc;
       }
       if (a.dfin && t0 + 8 == T) {  // the last three positions take dfinal_states
@@ -725,7 +732,7 @@ __global__ void __launch_bounds__(256) bwd_bdt8_kernel(BwdArgs a) {
       }
       VT::st(dxr + t0, VT::pack(v));
       if (t0 == 0 && a.dinit) {  // dinit[j + 3] = dxe[j], j = -3 .. -1 (gp before 0 is zero)
-        const float g3[kState + 3] = {0.0f, 0.0f, 0.0f, gp[0], gp[1], gp[2]};
+        const float g3[kState + 3] = {0.0f, 0.0f, 0.0f, gp_cur[0], gp_cur[1], gp_cur[2]};
 #pragma unroll
         for (int i = 0; i < kState; ++i) {
           float acc = w3 * g3[i];
@@ -738,7 +745,7 @@ __global__ void __launch_bounds__(256) bwd_bdt8_kernel(BwdArgs a) {
       }
     }
 #pragma unroll
-    for (int i = 0; i < kState; ++i) carry[i] = __shfl_sync(kAll, xe[3 + 8 - kState + i], 31);
+    for (int u = 0; u < 8; ++u) gp_cur[u] = gp_next[u];
   }
   pdl_release();
   // the sums are of gp2 = 2 gp: halve them (exact)
