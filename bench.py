@@ -667,6 +667,10 @@ def main():
               bench_conv_workload("packed_varlen", workloads.packed_varlen(), device, stream, peak,
                                   True),
               bench_update(device, stream, peak)]
+        # the same dense step on a contiguous [B, D, T] tensor (time-contiguous)
+        tc = workloads.make_inputs(4, 1536, 2048, seed=0, initial_states=True, grad=True,
+                                   channel_last=False)
+        bd.append(bench_conv_workload("dense_state_time_contiguous", tc, device, stream, peak, False))
         # the same dense step with a width-three filter (weight [D, 3], states [., D, 2])
         w3 = workloads.make_inputs(4, 1536, 2048, seed=0, initial_states=True, grad=True, width=3)
         bd.append(bench_conv_workload("dense_state_width3", w3, device, stream, peak, False))
