@@ -429,6 +429,25 @@ def time_e2e(inp: workloads.ConvInputs, device, steps, warmup, stream):
 
 # ---- CPU oracle ---------------------------------------------------------------------
 
+def host_cpu_model() -> str:
+    """The host CPU's name as /proc/cpuinfo gives it (best effort)."""
+    try:
+        fields = {}
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                if ":" in ln:
+                    k, v = ln.split(":", 1)
+                    fields.setdefault(k.strip(), v.strip())
+        for k in ("model name", "Model", "CPU part"):
+            if k in fields:
+                impl = fields.get("CPU implementer", "")
+                return fields[k] if k != "CPU part" else f"implementer {impl} part {fields[k]}"
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
 def oracle_threads() -> int:
     """Host cores this process may run on (the oracle is split over them)."""
     try:
@@ -683,11 +702,15 @@ def main():
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         threads = oracle_threads()
         s, nb, reps, shape = oracle_step_seconds(inp, 1.5, 200, None, threads)
+        s1, nb1, reps1, _ = oracle_step_seconds(inp, 1.0, 5, None, 1)
         line["cpu_baseline"] = {"value": round(nb / s / 1e9, 4), "unit": UNIT, "cores": threads,
-                                "kind": "oracle",
+                                "kind": "oracle", "cpu": host_cpu_model(),
                                 "sample": f"whole dense_state workload fwd+bwd, channels split over "
                                           f"{threads} threads, {reps} reps, {s:.3f} s each "
-                                          f"({reps * s * threads:.0f} core-seconds)"}
+                                          f"({reps * s * threads:.0f} core-seconds)",
+                                "single_thread": {"value": round(nb1 / s1 / 1e9, 4), "cores": 1,
+                                                  "sample": f"the same, one thread, {reps1} reps, "
+                                                            f"{s1:.2f} s each"}}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if pg is not None:
