@@ -303,8 +303,16 @@ FwdPlan plan_fwd(int kind, int vec, int64_t Q, int D, int64_t rows, int sm_count
     return p;
   }
   // segments of a multiple of six tokens: the vector kernel's ring groups then
-  // cover a segment inside a sequence exactly
-  return plan_cl(vec, Q, D, sm_count, fwd_blocks_per_sm(vec), 1, 12, 256, vec == 4 ? 6 : 1);
+  // cover a segment inside a sequence exactly.  Long per-thread ranges run in
+  // several waves of shorter segments, one wave per 64 tokens a thread would
+  // get in one wave, up to eight (measured: 4x2048x1536 best in one wave,
+  // packed 16 x U[1,4096] x 2048 in two, 8x8192x5120 in eight).
+  const int bps = fwd_blocks_per_sm(vec);
+  const int64_t groups = ceil_div(D, vec);
+  const int64_t threads = int64_t(sm_count) * std::max(1, bps) * 256;
+  const int64_t per_thread = ceil_div(std::max<int64_t>(Q, 1) * groups, std::max<int64_t>(threads, 1));
+  const int waves = int(std::min<int64_t>(8, std::max<int64_t>(1, per_thread / 64)));
+  return plan_cl(vec, Q, D, sm_count, bps, waves, 12, 256, vec == 4 ? 6 : 1);
 }
 
 BwdPlan plan_bwd(int kind, int vec, int64_t Q, int D, int64_t rows, int sm_count) {
