@@ -349,6 +349,18 @@ __global__ void __launch_bounds__(kBwdThreads, V == 8 ? CCC_BWD_MIN_BLOCKS : 4)
       const uint16_t* gq = a.g + (dense ? n * a.g_sb + (a0 - lo) * gst : a0 * gst) + d0;
       uint16_t* dp = a.dx + (dense ? n * a.dx_sb + (a0 - lo) * dst : a0 * dst) + d0;
       const int64_t m_end = e + kState;  // tokens stepped: [a0, e + 3)
+      // rows the general steps may read at the piece's two ends: into L2 now
+      {
+        const int64_t r_end = m_end < hi ? m_end : hi;
+        for (int64_t t = a0; t < a0 + kState && t < r_end; ++t) {
+          prefetch_l2(xp + (t - a0) * xst);
+          prefetch_l2(gq + (t - a0) * gst);
+        }
+        for (int64_t t = (e - 2 > a0 + kState ? e - 2 : a0 + kState); t < r_end; ++t) {
+          prefetch_l2(xp + (t - a0) * xst);
+          prefetch_l2(gq + (t - a0) * gst);
+        }
+      }
 
       float2 X[kState][H], G[kState][H];  // xe[m-3 .. m-1], gp[m-3 .. m-1]
       {
