@@ -300,6 +300,7 @@ __global__ void __launch_bounds__(kBwdThreads, V == 8 ? CCC_BWD_MIN_BLOCKS : 4)
   constexpr int H = V / 2;  // channel pairs
   constexpr int RB = int(sizeof(Raw));
   __shared__ __align__(16) float wsm[(kWidth + 1) * kMaxBlockChannels];
+  if (blockDim.x * blockDim.y * blockDim.z != kBwdThreads) return;  // the ring layout assumes it
   pdl_wait();  // inputs may come from the previous kernel in the stream
   if (block_rejects_cu_seqlens(a.seqs, a.status)) return;
   const int n_blk = blockDim.x * V;
@@ -319,13 +320,13 @@ __global__ void __launch_bounds__(kBwdThreads, V == 8 ? CCC_BWD_MIN_BLOCKS : 4)
     if (a.wr.w_vec) weights_direct2<V>(a.wr, d0, w, b);
     else weights_from_smem2<V>(wsm, n_blk, threadIdx.x * V, w, b);
     // this thread's ring: slot (stage, row u, tensor t) at byte
-    // (((stage * 3 + u) * 2 + t) * threads + tid) * RB past the ring base
-    const int nthr = blockDim.x * blockDim.y;
+    // (((stage * 3 + u) * 2 + t) * kBwdThreads + tid) * RB past the ring base: the
+    // block size is a compile-time constant, so every offset is an immediate
     const int tid = threadIdx.y * blockDim.x + threadIdx.x;
-    const char* ring = reinterpret_cast<const char*>(bwd_dyn_smem) + bwd_red_bytes<V>(nthr) +
+    const char* ring = reinterpret_cast<const char*>(bwd_dyn_smem) + bwd_red_bytes<V>(kBwdThreads) +
                        size_t(tid) * RB;
     const uint32_t ring_s = smem_u32(ring);
-    const uint32_t slot = uint32_t(nthr) * RB;
+    constexpr uint32_t slot = uint32_t(kBwdThreads) * RB;
 
     int64_t q = seg * a.seg_len;
     const int64_t q_end = q + a.seg_len < a.seqs.Q ? q + a.seg_len : a.seqs.Q;
@@ -533,7 +534,7 @@ __global__ void __launch_bounds__(kBwdThreads, V == 8 ? CCC_BWD_MIN_BLOCKS : 4)
           gi += 3 * gst;
         }
         ++ki;
-        si = si + 1 == kBwdRing ? 0 : si + 1;
+        si = (si + 1) % kBwdRing;
         cp_async_commit();
       };
       int st = 0;  // stage of the group being taken
@@ -546,7 +547,7 @@ __global__ void __launch_bounds__(kBwdThreads, V == 8 ? CCC_BWD_MIN_BLOCKS : 4)
           xr[u] = *reinterpret_cast<const Raw*>(s0 + size_t(2 * u) * slot);
           gr[u] = *reinterpret_cast<const Raw*>(s0 + size_t(2 * u + 1) * slot);
         }
-        st = st + 1 == kBwdRing ? 0 : st + 1;
+        st = (st + 1) % kBwdRing;
       };
 #pragma unroll
       for (int j = 0; j < kBwdRing - 1; ++j) issue_next();

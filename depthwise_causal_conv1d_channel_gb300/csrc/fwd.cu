@@ -157,6 +157,7 @@ extern __shared__ __align__(16) char fwd_dyn_smem[];
 
 template <int V, int ACT>
 __global__ void __launch_bounds__(kFwdThreads, 3) fwd_clv_kernel(FwdArgs a) {
+  if (blockDim.x * blockDim.y * blockDim.z != kFwdThreads) return;  // the ring layout assumes it
   pdl_wait();     // inputs may come from the previous kernel in the stream
   pdl_release();
   using VT = Vec<V>;
@@ -174,12 +175,12 @@ __global__ void __launch_bounds__(kFwdThreads, 3) fwd_clv_kernel(FwdArgs a) {
   float2 w[H][kWidth], b[H];
   if (a.wr.w_vec) weights_direct2<V>(a.wr, d0, w, b);
   else weights_from_smem2<V>(ws, n_blk, threadIdx.x * V, w, b);
-  // this thread's ring: slot (stage, row u) at byte ((stage * G + u) * threads + tid) * RB
-  const int nthr = blockDim.x * blockDim.y;
+  // this thread's ring: slot (stage, row u) at byte ((stage * G + u) * kFwdThreads + tid) * RB
+  // (a compile-time block size: the offsets are immediates)
   const int tid = threadIdx.y * blockDim.x + threadIdx.x;
   const char* ring = fwd_dyn_smem + size_t(tid) * RB;
   const uint32_t ring_s = smem_u32(ring);
-  const uint32_t slot = uint32_t(nthr) * RB;
+  constexpr uint32_t slot = uint32_t(kFwdThreads) * RB;
 
   int64_t q = seg * a.seg_len;
   const int64_t q_end = q + a.seg_len < a.seqs.Q ? q + a.seg_len : a.seqs.Q;
