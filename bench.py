@@ -314,6 +314,27 @@ def _rate(nbytes, ms, tokens, peak):
             "frac_of_peak": round(gbs / peak, 4), "tokens_per_s": round(tokens / (ms * 1e-3))}
 
 
+def bench_stream_floor(inp: workloads.ConvInputs, device, stream, peak):
+    """Context for the dense workloads, not a roofline: PyTorch's own
+    elementwise kernels moving the bytes of the dense forward (read x, write
+    out: neg) and backward (read x and grad_out, write dx: add) on contiguous
+    BF16 tensors of x's size, timed like the conv calls (a graph of 20 calls
+    over rotating buffer sets, cold in L2)."""
+    n = inp.x.numel()
+    nbytes = 2 * n
+    sets = max(1, -(-3 * L2_BYTES // (3 * nbytes)))
+    gen = torch.Generator(device=device).manual_seed(0)
+    a = [torch.randn(n, device=device, generator=gen).to(torch.bfloat16) for _ in range(sets)]
+    b = [torch.randn(n, device=device, generator=gen).to(torch.bfloat16) for _ in range(sets)]
+    o = [torch.empty_like(t) for t in a]
+    neg_ms = _per_call_ms(lambda i, s: torch.neg(a[i % sets], out=o[i % sets]), sets, device, stream)
+    add_ms = _per_call_ms(lambda i, s: torch.add(a[i % sets], b[i % sets], out=o[i % sets]), sets,
+                          device, stream)
+    return {"workload": "torch_elementwise_same_bytes", "elements": n, "rotating_sets": sets,
+            "neg_1read_1write": _rate(2 * nbytes, neg_ms, inp.tokens, peak),
+            "add_2read_1write": _rate(3 * nbytes, add_ms, inp.tokens, peak)}
+
+
 def bench_update(device, stream, peak, iters=50):
     from depthwise_causal_conv1d_channel_gb300 import _abi
 
@@ -683,6 +704,7 @@ def main():
         bd = [bench_conv_workload("dense_small", workloads.dense_small(), device, stream, peak,
                                   False, do_bwd=False),
               bench_conv_workload("dense_state", inp, device, stream, peak, False),
+              bench_stream_floor(inp, device, stream, peak),
               bench_conv_workload("packed_varlen", workloads.packed_varlen(), device, stream, peak,
                                   True),
               bench_update(device, stream, peak)]

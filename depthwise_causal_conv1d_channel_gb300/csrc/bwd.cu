@@ -317,8 +317,7 @@ __global__ void __launch_bounds__(kBwdThreads, V == 8 ? CCC_BWD_MIN_BLOCKS : 4)
   }
   if (active) {
     float2 w[H][kWidth], b[H];
-    if (a.wr.w_vec) weights_direct2<V>(a.wr, d0, w, b);
-    else weights_from_smem2<V>(wsm, n_blk, threadIdx.x * V, w, b);
+    bool have_w = false;  // the weights are loaded once the first ring groups are in flight
     // this thread's ring: slot (stage, row u, tensor t) at byte
     // (((stage * 3 + u) * 2 + t) * kBwdThreads + tid) * RB past the ring base: the
     // block size is a compile-time constant, so every offset is an immediate
@@ -350,6 +349,58 @@ __global__ void __launch_bounds__(kBwdThreads, V == 8 ? CCC_BWD_MIN_BLOCKS : 4)
       const uint16_t* gq = a.g + (dense ? n * a.g_sb + (a0 - lo) * gst : a0 * gst) + d0;
       uint16_t* dp = a.dx + (dense ? n * a.dx_sb + (a0 - lo) * dst : a0 * dst) + d0;
       const int64_t m_end = e + kState;  // tokens stepped: [a0, e + 3)
+      // The ring's groups: rows r0 + 3k .. r0 + 3k + 2 for k < n_total.  With a
+      // head (the window came from x rows and a0 .. a0+2 are own) r0 = a0 and
+      // group 0 computes own tokens whose emissions are the previous piece's
+      // rows; otherwise the first three tokens take the general step and
+      // r0 = a0 + 3.  Then the groups of own tokens emitting own rows; then,
+      // when those end on e with three more rows in the sequence, the tail
+      // group, which emits the last own rows; else the general step finishes.
+      // The first groups are issued before anything else of the piece is read.
+      const bool head = a0 - kState >= lo && a0 + 3 <= e;
+      const int64_t r0 = head ? a0 : (a0 + kState < m_end ? a0 + kState : m_end);
+      const int n_main = e > r0 ? int((e - r0) / 3) : 0;  // a segment's groups: below 2^31
+      const bool tail = e > r0 && (e - r0) % 3 == 0 && e + kState <= hi && e - a0 >= kState;
+      const int n_total = n_main + (tail ? 1 : 0);
+      // running pointers: the next group to issue (rows and ring stage), the
+      // group being taken (stage, dx rows)
+      const uint16_t* xi = xp + (r0 - a0) * xst;
+      const uint16_t* gi = gq + (r0 - a0) * gst;
+      int ki = 0, si = 0;  // next group to issue, its stage
+      auto issue_next = [&]() {
+        if (ki < n_total) {
+          const uint32_t s0 = ring_s + uint32_t(si * 6) * slot;
+#pragma unroll
+          for (int u = 0; u < 3; ++u) {
+            cp_async<RB>(s0 + uint32_t(2 * u) * slot, xi + u * xst);
+            cp_async<RB>(s0 + uint32_t(2 * u + 1) * slot, gi + u * gst);
+          }
+          xi += 3 * xst;
+          gi += 3 * gst;
+        }
+        ++ki;
+        si = (si + 1) % kBwdRing;
+        cp_async_commit();
+      };
+      int st = 0;  // stage of the group being taken
+      auto take = [&](Raw (&xr)[3], Raw (&gr)[3]) {
+        issue_next();
+        cp_async_wait<kBwdRing - 1>();  // the group being taken has landed
+        const char* s0 = ring + size_t(st * 6) * slot;
+#pragma unroll
+        for (int u = 0; u < 3; ++u) {
+          xr[u] = *reinterpret_cast<const Raw*>(s0 + size_t(2 * u) * slot);
+          gr[u] = *reinterpret_cast<const Raw*>(s0 + size_t(2 * u + 1) * slot);
+        }
+        st = (st + 1) % kBwdRing;
+      };
+#pragma unroll
+      for (int j = 0; j < kBwdRing - 1; ++j) issue_next();
+      if (!have_w) {
+        if (a.wr.w_vec) weights_direct2<V>(a.wr, d0, w, b);
+        else weights_from_smem2<V>(wsm, n_blk, threadIdx.x * V, w, b);
+        have_w = true;
+      }
       // rows the general steps may read at the piece's two ends: into L2 now
       {
         const int64_t r_end = m_end < hi ? m_end : hi;
@@ -500,57 +551,10 @@ __global__ void __launch_bounds__(kBwdThreads, V == 8 ? CCC_BWD_MIN_BLOCKS : 4)
         fast(P2{}, acc_flag, store_flag, xr[2], gr[2], drow + 2 * dst);
       };
 
-      // The ring's groups: rows r0 + 3k .. r0 + 3k + 2 for k < n_total.  With a
-      // head (the window came from x rows and a0 .. a0+2 are own) r0 = a0 and
-      // group 0 computes own tokens whose emissions are the previous piece's
-      // rows; otherwise the first three tokens take the general step and
-      // r0 = a0 + 3.  Then the groups of own tokens emitting own rows; then,
-      // when those end on e with three more rows in the sequence, the tail
-      // group, which emits the last own rows; else the general step finishes.
-      int64_t m = a0;
-      const bool head = a0 - kState >= lo && a0 + 3 <= e;
+      int64_t m = a0;  // general steps before the ring's first group
       if (!head) {
-        const int64_t pro_end = a0 + kState < m_end ? a0 + kState : m_end;
-        for (; m < pro_end; ++m) slow(m);
+        for (; m < r0; ++m) slow(m);
       }
-      const int64_t r0 = m;
-      const int n_main = e > r0 ? int((e - r0) / 3) : 0;  // a segment's groups: below 2^31
-      const bool tail = e > r0 && (e - r0) % 3 == 0 && e + kState <= hi && e - a0 >= kState;
-      const int n_total = n_main + (tail ? 1 : 0);
-      // running pointers: the next group to issue (rows and ring stage), the
-      // group being taken (stage, dx rows)
-      const uint16_t* xi = xp + (r0 - a0) * xst;
-      const uint16_t* gi = gq + (r0 - a0) * gst;
-      int ki = 0, si = 0;  // next group to issue, its stage
-      auto issue_next = [&]() {
-        if (ki < n_total) {
-          const uint32_t s0 = ring_s + uint32_t(si * 6) * slot;
-#pragma unroll
-          for (int u = 0; u < 3; ++u) {
-            cp_async<RB>(s0 + uint32_t(2 * u) * slot, xi + u * xst);
-            cp_async<RB>(s0 + uint32_t(2 * u + 1) * slot, gi + u * gst);
-          }
-          xi += 3 * xst;
-          gi += 3 * gst;
-        }
-        ++ki;
-        si = (si + 1) % kBwdRing;
-        cp_async_commit();
-      };
-      int st = 0;  // stage of the group being taken
-      auto take = [&](Raw (&xr)[3], Raw (&gr)[3]) {
-        issue_next();
-        cp_async_wait<kBwdRing - 1>();  // the group being taken has landed
-        const char* s0 = ring + size_t(st * 6) * slot;
-#pragma unroll
-        for (int u = 0; u < 3; ++u) {
-          xr[u] = *reinterpret_cast<const Raw*>(s0 + size_t(2 * u) * slot);
-          gr[u] = *reinterpret_cast<const Raw*>(s0 + size_t(2 * u + 1) * slot);
-        }
-        st = (st + 1) % kBwdRing;
-      };
-#pragma unroll
-      for (int j = 0; j < kBwdRing - 1; ++j) issue_next();
       Raw xr[3], gr[3];
       int k = 0;
       uint16_t* drow = dp + (r0 - kState - a0) * dst;  // dx rows of group k

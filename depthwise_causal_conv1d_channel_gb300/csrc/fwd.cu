@@ -173,8 +173,7 @@ __global__ void __launch_bounds__(kFwdThreads, 3) fwd_clv_kernel(FwdArgs a) {
   if (!a.wr.w_vec) stage_weights(a.wr, blockIdx.x * n_blk, n_blk, a.D, ws);  // block-uniform
   if (d0 >= a.D || seg >= a.n_seg) return;
   float2 w[H][kWidth], b[H];
-  if (a.wr.w_vec) weights_direct2<V>(a.wr, d0, w, b);
-  else weights_from_smem2<V>(ws, n_blk, threadIdx.x * V, w, b);
+  bool have_w = false;  // the weights are loaded once the first ring groups are in flight
   // this thread's ring: slot (stage, row u) at byte ((stage * G + u) * kFwdThreads + tid) * RB
   // (a compile-time block size: the offsets are immediates)
   const int tid = threadIdx.y * blockDim.x + threadIdx.x;
@@ -218,6 +217,11 @@ __global__ void __launch_bounds__(kFwdThreads, 3) fwd_clv_kernel(FwdArgs a) {
     for (int k = 0; k < kFwdRing - 1; ++k) {
       if (k < n_grp) issue(k);
       cp_async_commit();
+    }
+    if (!have_w) {
+      if (a.wr.w_vec) weights_direct2<V>(a.wr, d0, w, b);
+      else weights_from_smem2<V>(ws, n_blk, threadIdx.x * V, w, b);
+      have_w = true;
     }
 
     // W[j] = xe[q - 3 + j]
