@@ -147,7 +147,6 @@ __global__ void __launch_bounds__(32 * TY) update_w8_kernel(UpdArgs a) {
   const int b0 = (blockIdx.y * blockDim.y + wy) * R;
   if (b0 >= a.B) return;  // the whole warp: it shares b0
   float2 w[4][kWidth], bias[4];
-  if (valid) weights_direct2<8>(a.wr, d0, w, bias);
   uint4 sr[R][kState], xr[R];
 #pragma unroll
   for (int r = 0; r < R; ++r) {
@@ -159,6 +158,7 @@ __global__ void __launch_bounds__(32 * TY) update_w8_kernel(UpdArgs a) {
       if (valid) xr[r] = Vec<8>::ld(a.x + int64_t(b0 + r) * a.x_sb + d0);
     }
   }
+  if (valid) weights_direct2<8>(a.wr, d0, w, bias);  // after the state loads are in flight
 #pragma unroll
   for (int r = 0; r < R; ++r)
     if (b0 + r < a.B)
