@@ -47,8 +47,8 @@ L2_BYTES = 129 * 2 ** 20
 # per launch.  Valid only for the kernel sources whose digest is recorded here.
 # The capture flushes caches before each launch; the 25 MB dx written to L2 is
 # mostly not yet written back when the kernel ends, so writes are undercounted.
-TRAFFIC = {"sources_sha256": "e0879d9d78d1fe57528136aefbfa99cfed6066c9e893a314f0cba65c8d267de5",
-           "bytes_per_launch": (50439936 + 998912) + (1512960 + 0)}
+TRAFFIC = {"sources_sha256": "86fdfe1441f9fc21028fc18819adb2ed803d55070538a2d01ac63899c6f36256",
+           "bytes_per_launch": (50440704 + 883456) + (1512960 + 0)}
 
 
 def kernel_sources_digest() -> str:
