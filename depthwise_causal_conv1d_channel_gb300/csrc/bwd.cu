@@ -784,6 +784,8 @@ __global__ void __launch_bounds__(256) bwd_bdt8_kernel(BwdArgs a) {
 constexpr int kFinClasses = 8;
 __global__ void __launch_bounds__(32 * kFinClasses) wgrad_finalize_kernel(const float* ws, int64_t R,
                                                                           int D, WgradOut o) {
+  // No early griddepcontrol.launch_dependents here: a following backward
+  // launched into this kernel's tail measured slower than one launched at its end.
   pdl_wait();  // the backward kernel's sums
   __shared__ float part[kFinClasses][32];
   const int tx = threadIdx.x & 31, c = threadIdx.x >> 5;
