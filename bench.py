@@ -47,7 +47,7 @@ L2_BYTES = 129 * 2 ** 20
 # per launch.  Valid only for the kernel sources whose digest is recorded here.
 # The capture flushes caches before each launch; the 25 MB dx written to L2 is
 # mostly not yet written back when the kernel ends, so writes are undercounted.
-TRAFFIC = {"sources_sha256": "86fdfe1441f9fc21028fc18819adb2ed803d55070538a2d01ac63899c6f36256",
+TRAFFIC = {"sources_sha256": "a3df385e7854fe44bd2bd48c8a652e035ad459c0dad4487f72fb82db3890eeae",
            "bytes_per_launch": (50440704 + 883456) + (1512960 + 0)}
 
 
