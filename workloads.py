@@ -189,6 +189,16 @@ WORKLOADS = {
 
 # ---- marshalling helpers (bit patterns, no arithmetic) ----------------------
 
+def device_activations(B: int, D: int, T: int, device, seed: int, channel_last: bool = True):
+    """A seeded N(0, 1) BF16 activation tensor drawn on the device, for sizes
+    too large to draw on the host: [B, T, D] storage seen as its [B, D, T]
+    transpose when ``channel_last``, else contiguous [B, D, T]."""
+    gen = torch.Generator(device=device).manual_seed(seed)
+    shape = (B, T, D) if channel_last else (B, D, T)
+    t = torch.randn(shape, generator=gen, device=device, dtype=BF16)
+    return t.transpose(1, 2) if channel_last else t
+
+
 def bits(t: Optional[torch.Tensor]):
     """BF16 tensor -> numpy uint16 bit patterns (logical shape kept); float32 and
     int32 tensors are returned as numpy arrays of their own dtype."""
