@@ -1,7 +1,7 @@
-"""Depthwise causal conv1d for GB300 (sm_103a): BF16 activations, width four,
-SiLU, W-1 initial/final state, cu_seqlens packing, backward, and the
-single-token update -- as hand-written CUDA kernels behind a C ABI
-(include/ccc_conv1d.h, libccc_conv1d.so).
+"""Depthwise causal conv1d for GB300 (sm_103a): BF16 activations, filter
+widths 2..4, SiLU, W-1 initial/final state, cu_seqlens packing, backward, and
+the in-place decode update of one or several tokens -- as hand-written CUDA
+kernels behind a C ABI (include/ccc_conv1d.h, libccc_conv1d.so).
 
 ``causal_conv1d`` and ``causal_conv1d_update`` are the model-facing calls;
 ``_abi`` holds the ctypes binding with the C function names.  Importing this
