@@ -47,7 +47,7 @@ L2_BYTES = 129 * 2 ** 20
 # per launch.  Valid only for the kernel sources whose digest is recorded here.
 # The capture flushes caches before each launch; the 25 MB dx written to L2 is
 # mostly not yet written back when the kernel ends, so writes are undercounted.
-TRAFFIC = {"sources_sha256": "a3df385e7854fe44bd2bd48c8a652e035ad459c0dad4487f72fb82db3890eeae",
+TRAFFIC = {"sources_sha256": "197c6484be887a960c65ca9d9ccafdb67c4952b85783ff71260ef862ac1159bd",
            "bytes_per_launch": (50440704 + 883456) + (1512960 + 0)}
 
 

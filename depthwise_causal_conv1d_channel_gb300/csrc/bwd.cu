@@ -276,7 +276,8 @@ __global__ void __launch_bounds__(256) bwd_cl_kernel(BwdArgs a) {
 // registers for loads in flight.  The ring's first group is the head (own
 // tokens whose dx rows belong to the previous piece) and its last the tail
 // (the three tokens after the piece, which emit its last dx rows); the few
-// tokens at sequence edges take the general step, their rows loaded together.
+// tokens at sequence edges take the general step, loading their rows directly
+// (prefetched into L2 when the piece starts).
 // 128-thread blocks (two resident per SM for V = 8, four for V = 4).
 #ifndef CCC_BWD_MIN_BLOCKS
 #define CCC_BWD_MIN_BLOCKS 2

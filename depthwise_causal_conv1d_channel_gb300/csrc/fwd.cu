@@ -131,8 +131,8 @@ __global__ void __launch_bounds__(256) fwd_cl_kernel(FwdArgs a) {
 }
 
 // Channel-last x with vectors of V = 4 channels, computed as two channel
-// pairs of scalar instructions (the fast path; eight channels a thread
-// measured no faster, paired instructions 1-2% slower).  Same
+// pairs of scalar instructions (the fast path; eight channels a thread, two
+// blocks per SM, measured slower, paired instructions 1-2% slower).  Same
 // walk as fwd_walk, specialised: the three-token window lives in three register
 // slots that rotate (the newest token overwrites the oldest slot), so full
 // groups of kFwdGroup tokens (a multiple of three) need no register copies.
