@@ -12,9 +12,9 @@
  *
  *   out[b,d,t] = act(bias[d] + sum_{k<W} weight[d,k] * xe[b,d,t-(W-1)+k])
  *
- * where xe is x extended on the left by the three entries of initial_states
+ * where xe is x extended on the left by the W - 1 entries of initial_states
  * (zeros when none are given); index 0 of the state axis is the oldest entry.
- * Tap 3 multiplies the current token (POPCORNBENCH conv1d page, the reasoning
+ * Tap W - 1 multiplies the current token (POPCORNBENCH conv1d page, the reasoning
  * section's causal-padding derivation: tap k reads position t + k - (K-1)).
  * act is SiLU, p * sigmoid(p), or the identity.
  *
