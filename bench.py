@@ -574,8 +574,8 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
-PROFILE_WORKLOADS = ("dense_small", "dense_state", "packed_varlen", "decode_update",
-                     "dense_large_bias", "dense_large_det")
+PROFILE_WORKLOADS = ("dense_small", "dense_state", "dense_state_time_contiguous", "packed_varlen",
+                     "decode_update", "dense_large_bias", "dense_large_det")
 
 
 def run_profile(name: str, calls: int):
@@ -599,6 +599,9 @@ def run_profile(name: str, calls: int):
             inp = workloads.dense_small()
         elif name == "dense_state":
             inp = workloads.dense_state()
+        elif name == "dense_state_time_contiguous":
+            inp = workloads.make_inputs(4, 1536, 2048, seed=0, initial_states=True, grad=True,
+                                        channel_last=False)
         elif name == "packed_varlen":
             inp = workloads.packed_varlen()
         else:
