@@ -78,10 +78,15 @@ DENSE_CASES = [
     (2, 40, 300, False, dict(initial_states=True, grad=True, dfinal_states=True)),     # [B, D, T]
     (2, 64, 128, False, dict(grad=True)),
     (1, 33, 7, False, dict(initial_states=True, grad=True, bias=False, weight_dtype=torch.float32)),
-    # time-contiguous rows of a multiple of 8 tokens: 8 tokens a lane, warp steps of 256
+    # time-contiguous rows of a multiple of 8 tokens: 8 tokens a lane, warp steps of 256;
+    # an even D takes two channel rows a warp (the last block ragged for 3 x 10)
     (3, 24, 264, False, dict(initial_states=True, grad=True, dfinal_states=True)),
     (2, 16, 512, False, dict(initial_states=True, grad=True)),
     (1, 8, 2056, False, dict(grad=True, activation=None)),
+    (3, 10, 520, False, dict(initial_states=True, grad=True, dfinal_states=True)),
+    # an odd D: one channel row a warp
+    (2, 25, 264, False, dict(initial_states=True, grad=True, dfinal_states=True)),
+    (1, 7, 512, False, dict(initial_states=True, grad=True, bias=False, weight_dtype=torch.float32)),
 ]
 
 
