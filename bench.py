@@ -47,8 +47,8 @@ L2_BYTES = 129 * 2 ** 20
 # per launch.  Valid only for the kernel sources whose digest is recorded here.
 # The capture flushes caches before each launch; the 25 MB dx written to L2 is
 # mostly not yet written back when the kernel ends, so writes are undercounted.
-TRAFFIC = {"sources_sha256": "197c6484be887a960c65ca9d9ccafdb67c4952b85783ff71260ef862ac1159bd",
-           "bytes_per_launch": (50440704 + 883456) + (1512960 + 0)}
+TRAFFIC = {"sources_sha256": "25ecb81c803852ccc2c513bb9c615ea425a246f5075e749d358c71c7b78bf76a",
+           "bytes_per_launch": (50443520 + 836864) + (1512960 + 0)}
 
 
 def kernel_sources_digest() -> str:
