@@ -47,8 +47,8 @@ L2_BYTES = 129 * 2 ** 20
 # per launch.  Valid only for the kernel sources whose digest is recorded here.
 # The capture flushes caches before each launch; the 25 MB dx written to L2 is
 # mostly not yet written back when the kernel ends, so writes are undercounted.
-TRAFFIC = {"sources_sha256": "25ecb81c803852ccc2c513bb9c615ea425a246f5075e749d358c71c7b78bf76a",
-           "bytes_per_launch": (50443520 + 836864) + (1512960 + 0)}
+TRAFFIC = {"sources_sha256": "a047e853aea0a4df653109e55b0d0af5c091a744cd6386e3c3fa6d1189d6cf20",
+           "bytes_per_launch": (50439168 + 1000448) + (1512960 + 0)}
 
 
 def kernel_sources_digest() -> str:

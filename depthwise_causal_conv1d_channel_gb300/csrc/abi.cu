@@ -219,6 +219,14 @@ bool bdt_vec_ok(const Problem& pb, std::initializer_list<const ccc_tensor*> acts
   return true;
 }
 
+// Time-contiguous backward: 16-byte token chunks over pairs of channel rows
+// (vec 16) for an even D and rows of at least kBdtPairMinTokens tokens, one
+// row a warp (vec 8) for other aligned rows, else the per-token kernel (1).
+int bdt_bwd_vec(const Problem& pb, std::initializer_list<const ccc_tensor*> acts) {
+  if (!bdt_vec_ok(pb, acts)) return 1;
+  return pb.D % 2 == 0 && pb.T >= ccc::kBdtPairMinTokens ? 16 : 8;
+}
+
 // Channels per thread: the preferred width when the tensors allow it, else 4,
 // else 1 (scalar).
 int pick_vec(int preferred, const Problem& pb, std::initializer_list<const ccc_tensor*> acts,
@@ -317,6 +325,16 @@ FwdPlan plan_fwd(int kind, int vec, int64_t Q, int D, int64_t rows, int sm_count
 
 BwdPlan plan_bwd(int kind, int vec, int64_t Q, int D, int64_t rows, int sm_count) {
   if (kind == kLayoutTimeContiguous) {
+    if (vec == 16) {  // a warp per pair of channel rows
+      BwdPlan p{};
+      p.kind = kLayoutTimeContiguous;
+      p.vec = 16;
+      p.tx = kBdtPairThreads;
+      p.ty = 1;
+      p.gx = unsigned(ceil_div(std::max<int64_t>(rows / 2, 1), kBdtPairThreads / 32));
+      p.gy = 1;
+      return p;
+    }
     BwdPlan p = plan_bdt(rows);
     p.vec = vec;  // 8: 16-byte token chunks per lane
     return p;
@@ -474,7 +492,7 @@ ccc_status ccc_conv1d_bwd(const ccc_tensor* x, const ccc_tensor* weight, const c
   if (sms <= 0) return CCC_ERR_CUDA;
   const int64_t Q = pb.packed ? pb.T : int64_t(pb.B) * pb.T;
   const int vec = pb.layout == ccc::kLayoutTimeContiguous
-                      ? (bdt_vec_ok(pb, {x, dout, dx}) ? 8 : 1)
+                      ? bdt_bwd_vec(pb, {x, dout, dx})
                       : pick_vec(bwd_preferred_vec(Q, pb.D, sms), pb, {x, dout, dx},
                                  {initial_states, dfinal_states, dinitial_states});
   ccc::BwdPlan p{};

@@ -777,6 +777,183 @@ __global__ void __launch_bounds__(256) bwd_bdt8_kernel(BwdArgs a) {
   }
 }
 
+// bwd_bdt8_kernel's pipelined walk over two adjacent channel rows (d, d + 1)
+// of one batch at once (D even): each lane loads 8 tokens of x and grad_out
+// of both rows per step and computes the two channels as the two halves of
+// paired FP32 instructions, so one instruction serves two channels and the
+// per-step addresses, halo shuffles and loop are shared.  Per channel the
+// operations and their order are bwd_bdt8_kernel's, and so are the results.
+// Capped at 124 registers (four 128-thread blocks per SM).  Measured: faster
+// on long rows (8 x 5120 x 8192: 386 -> 368 us), slower on short ones (4 x
+// 1536 x 2048: 23.8 -> 24.2 us), so the call takes it for rows of at least
+// kBdtPairMinTokens tokens.
+template <int ACT>
+__global__ void __launch_bounds__(kBdtPairThreads, 4) bwd_bdt8x2_kernel(BwdArgs a) {
+  pdl_wait();  // inputs may come from the previous kernel in the stream
+  using VT = Vec<8>;
+  using Raw = typename VT::Raw;
+  const unsigned kAll = 0xffffffffu;
+  const int lane = threadIdx.x & 31;
+  const int64_t pr = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (pr >= int64_t(a.B) * (a.D / 2)) return;  // the whole warp shares the row pair
+  const int64_t row = 2 * pr;                   // rows row, row + 1 of one batch
+  const int bb = int(row / a.D), d = int(row % a.D);
+  float2 w[kWidth], b;
+  {
+    float wa[1][kWidth], ba[1], wb[1][kWidth], bq[1];
+    load_weights_1(a.wr, d, wa, ba);
+    load_weights_1(a.wr, d + 1, wb, bq);
+#pragma unroll
+    for (int k = 0; k < kWidth; ++k) w[k] = make_float2(wa[0][k], wb[0][k]);
+    b = make_float2(ba[0], bq[0]);
+  }
+  const int64_t T = a.seqs.T;
+  const uint16_t* xa = a.x + bb * a.x_sb + d * a.x_sd;
+  const uint16_t* xb = xa + a.x_sd;
+  const uint16_t* ga = a.g + bb * a.g_sb + d * a.g_sd;
+  const uint16_t* gb = ga + a.g_sd;
+  uint16_t* da = a.dx + bb * a.dx_sb + d * a.dx_sd;
+  uint16_t* db = da + a.dx_sd;
+  float2 carry[kState];  // for lane 0: xe of the three tokens before its next chunk
+  {
+    float ia[kState][1] = {{0.0f}, {0.0f}, {0.0f}}, ib[kState][1] = {{0.0f}, {0.0f}, {0.0f}};
+    if (a.init) {
+      load_state<1>(a.init, row, a.sw, ia);
+      load_state<1>(a.init, row + 1, a.sw, ib);
+    }
+#pragma unroll
+    for (int i = 0; i < kState; ++i) carry[i] = make_float2(ia[i][0], ib[i][0]);
+  }
+  float2 aw[kWidth] = {splat2(0.0f), splat2(0.0f), splat2(0.0f), splat2(0.0f)};
+  float2 ab = splat2(0.0f);
+  // gp2 of the chunk at t0 (zero for t0 >= T); accumulates the weight sums
+  auto chunk_gp = [&](int64_t t0, Raw xra, Raw xrb, Raw gra, Raw grb, float2 (&gp)[8]) {
+    float2 xe[11], gv[8];
+    {
+      float fa[8], fb[8], ha[8], hb[8];
+      VT::unpack(xra, fa);
+      VT::unpack(xrb, fb);
+      VT::unpack(gra, ha);
+      VT::unpack(grb, hb);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        xe[3 + u] = make_float2(fa[u], fb[u]);
+        gv[u] = make_float2(ha[u], hb[u]);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kState; ++i) {
+      const float2 last = xe[3 + 8 - kState + i];
+      const float2 px = make_float2(__shfl_up_sync(kAll, last.x, 1), __shfl_up_sync(kAll, last.y, 1));
+      xe[i] = lane == 0 ? carry[i] : px;
+      carry[i] = make_float2(__shfl_sync(kAll, last.x, 31), __shfl_sync(kAll, last.y, 31));
+    }
+    const bool valid = t0 < T;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      float2 p = b;
+      p = ffma2(w[0], xe[u], p);
+      p = ffma2(w[1], xe[u + 1], p);
+      p = ffma2(w[2], xe[u + 2], p);
+      p = ffma2(w[3], xe[u + 3], p);
+      gp[u] = valid ? act_bwd2<ACT>(p, gv[u]) : splat2(0.0f);
+    }
+    if (valid) {
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        aw[0] = ffma2(gp[u], xe[u], aw[0]);
+        aw[1] = ffma2(gp[u], xe[u + 1], aw[1]);
+        aw[2] = ffma2(gp[u], xe[u + 2], aw[2]);
+        aw[3] = ffma2(gp[u], xe[u + 3], aw[3]);
+        ab = fadd2(ab, gp[u]);
+      }
+    }
+  };
+  const Raw zero = make_uint4(0, 0, 0, 0);
+  auto ld = [&](const uint16_t* r, int64_t t) { return t < T ? VT::ld(r + t) : zero; };
+  float2 gp_cur[8];
+  chunk_gp(lane * 8, ld(xa, lane * 8), ld(xb, lane * 8), ld(ga, lane * 8), ld(gb, lane * 8), gp_cur);
+  Raw nxa = ld(xa, 256 + lane * 8), nxb = ld(xb, 256 + lane * 8);
+  Raw nga = ld(ga, 256 + lane * 8), ngb = ld(gb, 256 + lane * 8);
+  for (int64_t base = 0; base < T; base += 256) {
+    const int64_t t0 = base + lane * 8;
+    const Raw mxa = ld(xa, t0 + 512), mxb = ld(xb, t0 + 512);  // two chunks ahead
+    const Raw mga = ld(ga, t0 + 512), mgb = ld(gb, t0 + 512);
+    float2 gp_next[8];
+    chunk_gp(t0 + 256, nxa, nxb, nga, ngb, gp_next);
+    nxa = mxa;
+    nxb = mxb;
+    nga = mga;
+    ngb = mgb;
+    // gp2 of the three tokens after this lane's chunk
+    float2 gaft[kState];
+#pragma unroll
+    for (int i = 0; i < kState; ++i) {
+      const float2 down = make_float2(__shfl_down_sync(kAll, gp_cur[i].x, 1),
+                                      __shfl_down_sync(kAll, gp_cur[i].y, 1));
+      const float2 wrap = make_float2(__shfl_sync(kAll, gp_next[i].x, 0),
+                                      __shfl_sync(kAll, gp_next[i].y, 0));
+      gaft[i] = lane == 31 ? wrap : down;
+    }
+    if (t0 < T) {
+      const float2 g11[11] = {gp_cur[0], gp_cur[1], gp_cur[2], gp_cur[3], gp_cur[4], gp_cur[5],
+                              gp_cur[6], gp_cur[7], gaft[0], gaft[1], gaft[2]};
+      // dx[t0 + u] = w3 gp[u] + w2 gp[u+1] + w1 gp[u+2] + w0 gp[u+3] (halved weights)
+      float va[8], vb[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        float2 acc = fmul2(w[3], g11[u]);
+        acc = ffma2(w[2], g11[u + 1], acc);
+        acc = ffma2(w[1], g11[u + 2], acc);
+        acc = ffma2(w[0], g11[u + 3], acc);
+        va[u] = acc.x;
+        vb[u] = acc.y;
+      }
+      if (a.dfin && t0 + 8 == T) {  // the last three positions take dfinal_states
+#pragma unroll
+        for (int i = 0; i < kState; ++i) {
+          const int64_t ka = state_slot(row, i, a.sw), kb = state_slot(row + 1, i, a.sw);
+          if (ka >= 0) va[8 - kState + i] += bf16_to_f32(__ldg(a.dfin + ka));
+          if (kb >= 0) vb[8 - kState + i] += bf16_to_f32(__ldg(a.dfin + kb));
+        }
+      }
+      VT::st(da + t0, VT::pack(va));
+      VT::st(db + t0, VT::pack(vb));
+      if (t0 == 0 && a.dinit) {  // dinit[j + 3] = dxe[j], j = -3 .. -1 (gp before 0 is zero)
+        const float2 g3[kState + 3] = {splat2(0.0f), splat2(0.0f), splat2(0.0f),
+                                       gp_cur[0], gp_cur[1], gp_cur[2]};
+#pragma unroll
+        for (int i = 0; i < kState; ++i) {
+          float2 acc = fmul2(w[3], g3[i]);
+          acc = ffma2(w[2], g3[i + 1], acc);
+          acc = ffma2(w[1], g3[i + 2], acc);
+          acc = ffma2(w[0], g3[i + 3], acc);
+          const int64_t ka = state_slot(row, i, a.sw), kb = state_slot(row + 1, i, a.sw);
+          if (ka >= 0) a.dinit[ka] = f32_to_bf16(acc.x);
+          if (kb >= 0) a.dinit[kb] = f32_to_bf16(acc.y);
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) gp_cur[u] = gp_next[u];
+  }
+  pdl_release();
+  // the sums are of gp2 = 2 gp: halve them (exact); one butterfly per channel
+  float vs[2][kWidth + 1] = {{0.5f * aw[0].x, 0.5f * aw[1].x, 0.5f * aw[2].x, 0.5f * aw[3].x, 0.5f * ab.x},
+                             {0.5f * aw[0].y, 0.5f * aw[1].y, 0.5f * aw[2].y, 0.5f * aw[3].y, 0.5f * ab.y}};
+#pragma unroll
+  for (int c = 0; c < 2; ++c)
+#pragma unroll
+    for (int k = 0; k < kWidth + 1; ++k)
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) vs[c][k] += __shfl_xor_sync(kAll, vs[c][k], off);
+  if (lane == 0) {
+    for (int c = 0; c < 2; ++c)
+      for (int k = 0; k < kWidth + 1; ++k)
+        a.ws[(int64_t(bb) * a.D + d + c) * (kWidth + 1) + k] = vs[c][k];
+  }
+}
+
 // dweight/dbias from R rows of FP32 partial sums ws[r][D][5].  A block takes
 // 32 consecutive values in eight row classes: thread (value v, class c) adds
 // rows c, c + 8, c + 16, ... in increasing order (loads issued eight at a
@@ -889,6 +1066,8 @@ static cudaError_t launch_bwd_act(const BwdArgs& a, const BwdPlan& p, bool pdl,
     if (p.vec == 4) return launch_kernel(bwd_clv_kernel<4, ACT>, grid, block, smem, stream, pdl, a);
     return launch_kernel(bwd_cl_kernel<1, ACT>, grid, block, smem, stream, pdl, a);
   }
+  if (p.vec == 16)
+    return launch_kernel(bwd_bdt8x2_kernel<ACT>, dim3(p.gx), dim3(kBdtPairThreads), 0, stream, pdl, a);
   if (p.vec == 8) return launch_kernel(bwd_bdt8_kernel<ACT>, dim3(p.gx), dim3(256), 0, stream, pdl, a);
   return launch_kernel(bwd_bdt_kernel<ACT>, dim3(p.gx), dim3(256), 0, stream, pdl, a);
 }

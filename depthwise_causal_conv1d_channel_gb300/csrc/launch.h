@@ -29,6 +29,11 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
 
 enum Layout { kLayoutChannelLast = 0, kLayoutTimeContiguous = 1 };
 
+// Time-contiguous backward over pairs of channel rows (vec 16): threads per
+// block, and the shortest rows that take it.
+constexpr int kBdtPairThreads = 128;
+constexpr int64_t kBdtPairMinTokens = 4096;
+
 struct FwdArgs {
   const uint16_t* x;
   uint16_t* out;

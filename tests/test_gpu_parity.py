@@ -87,6 +87,11 @@ DENSE_CASES = [
     # an odd D: one channel row a warp
     (2, 25, 264, False, dict(initial_states=True, grad=True, dfinal_states=True)),
     (1, 7, 512, False, dict(initial_states=True, grad=True, bias=False, weight_dtype=torch.float32)),
+    # rows of 4096 tokens or more: the backward takes two channel rows a warp for an even D
+    (2, 6, 4096, False, dict(initial_states=True, grad=True, dfinal_states=True)),
+    (1, 10, 4104, False, dict(grad=True, bias=False, weight_dtype=torch.float32)),
+    (1, 4, 4096, False, dict(initial_states=True, grad=True, activation=None)),
+    (1, 5, 4096, False, dict(initial_states=True, grad=True)),
 ]
 
 
