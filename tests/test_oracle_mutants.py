@@ -39,6 +39,9 @@ MUTANTS = {
     "bf16_truncates": ("double r = rint(ldexp(a, -qexp));", "double r = floor(ldexp(a, -qexp));"),
     "bias_dropped": ("double p = b;\n    for (int k = 0; k < W; ++k)\n        p += w[k]",
                      "double p = 0.0 * b;\n    for (int k = 0; k < W; ++k)\n        p += w[k]"),
+    "dw_abs_shifted_tap": ("sdw_abs[k] += fabs(term);", "sdw_abs[(k + 1) % W] += fabs(term);"),
+    "dw_abs_doubled": ("sdw_abs[k] += fabs(term);", "sdw_abs[k] += 2.0 * fabs(term);"),
+    "db_abs_without_act_grad": ("sdb_abs += fabs(gp[t]);", "sdb_abs += fabs(gs[t]);"),
     "width_state_offset": ("const double *is = init ? init + ((int64_t)n * D + d) * S : NULL;\n            for (int64_t t = 0; t < len; ++t) {",
                            "const double *is = init ? init + ((int64_t)n * D + d) * 3 : NULL;\n            for (int64_t t = 0; t < len; ++t) {"),
 }
