@@ -1,9 +1,10 @@
 """Throughput of the depthwise causal conv1d on GB300: forward + backward of the
-dense channel-last workload with state (x stored [4, 2048, 1536] BF16, BF16
-weight/bias, initial/final state, grad_out), as achieved HBM GB/s
-(algorithmic bytes / time) and tokens/s, with the other workloads (dense
-[2, 64, 128] forward, packed varlen, decode update, large dense) reported per
-kernel under "breakdown".
+large dense channel-last workload (x stored [8, 8192, 5120] BF16, BF16
+weight/bias, initial/final state, grad_out) -- the largest of the workloads,
+all of which fit one GPU -- as achieved HBM GB/s (algorithmic bytes / time)
+and tokens/s, with the other workloads (dense [2, 64, 128] forward, dense
+[4, 2048, 1536] with state, packed varlen, decode update, the large dense
+workload bias-free and deterministic) reported per kernel under "breakdown".
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -42,13 +43,11 @@ FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 2 ** 20
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the dominant
-# call -- the backward on the dense_state workload: backward kernel plus the
-# finalize kernel -- from one ncu --set full capture (profiles/kernels_dense_state.md),
-# per launch.  Valid only for the kernel sources whose digest is recorded here.
-# The capture flushes caches before each launch; the 25 MB dx written to L2 is
-# mostly not yet written back when the kernel ends, so writes are undercounted.
-TRAFFIC = {"sources_sha256": "a047e853aea0a4df653109e55b0d0af5c091a744cd6386e3c3fa6d1189d6cf20",
-           "bytes_per_launch": (50439168 + 1000448) + (1512960 + 0)}
+# call -- the backward on the large dense workload: backward kernel plus the
+# finalize kernel -- from one ncu capture of those two kernels
+# (profiles/traffic_dense_large_backward.md), per launch.  Valid only for the
+# kernel sources whose digest is recorded here (null otherwise).
+TRAFFIC = {"sources_sha256": None, "bytes_per_launch": None}
 
 
 def kernel_sources_digest() -> str:
@@ -545,9 +544,9 @@ def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    inp = workloads.dense_state()
+    inp = workloads.dense_large(bias=True)
     D = inp.x.shape[1]
-    channels = list(range(0, D, 16))  # a 1/16 sample of the channels, every token
+    channels = list(range(0, D, 64))  # a 1/64 sample of the channels, every token
     threads = oracle_threads()
     ms = []
     for _ in range(args.warmup):
@@ -557,14 +556,15 @@ def run_reference(args):
         ms.append(s * 1e3)
     per = statistics.mean(ms)
     value = nb / (per * 1e-3) / 1e9
-    sample = (f"dense_state workload, forward+backward on {len(channels)} of {D} channels "
-              f"(every 16th), all {inp.tokens} tokens, per step, split over {threads} threads")
+    sample = (f"dense_large workload, forward+backward on {len(channels)} of {D} channels "
+              f"(every 64th), all {inp.tokens} tokens, per step, split over {threads} threads")
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(per, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "dense_state", "x": [4, 2048, 1536], "layout": "channel-last",
+        "config": {"workload": "dense_large", "x": [8, 5120, 8192],
+                   "layout": "channel-last ([8, 8192, 5120] storage)",
                    "sample_channels": len(channels)},
         "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
                          "sample": sample},
@@ -575,7 +575,8 @@ def run_reference(args):
 
 
 PROFILE_WORKLOADS = ("dense_small", "dense_state", "dense_state_time_contiguous", "packed_varlen",
-                     "decode_update", "dense_large_bias", "dense_large_det")
+                     "decode_update", "dense_large_bias", "dense_large_det",
+                     "dense_large_quarter")
 
 
 def run_profile(name: str, calls: int):
@@ -604,6 +605,11 @@ def run_profile(name: str, calls: int):
                                         channel_last=False)
         elif name == "packed_varlen":
             inp = workloads.packed_varlen()
+        elif name == "dense_large_quarter":
+            # the large workload's shape with a quarter of its tokens (x and
+            # grad_out 168 MB each, still above L2): the small case for
+            # multi-pass ncu captures of its kernels
+            inp = workloads.make_inputs(8, 5120, 2048, seed=0, initial_states=True, grad=True)
         else:
             inp = workloads.dense_large(bias=name == "dense_large_bias")
         step = DenseStep(inp, device, deterministic=inp.deterministic, sets=1)
@@ -649,8 +655,10 @@ def main():
 
     stream = torch.cuda.current_stream(device)
     peak, peak_kind = measured_peak()
-    inp = workloads.dense_state()
-    step = DenseStep(inp, device)
+    # the largest workload: x and grad_out are 671 MB each, larger than L2, so
+    # one buffer set serves every step cold
+    inp = workloads.dense_large(bias=True)
+    step = DenseStep(inp, device, sets=1)
 
     def barrier():
         if pg is not None:
@@ -671,7 +679,7 @@ def main():
     achieved = dominant[2] / (dominant[1] * 1e-3) / 1e9
     traffic = TRAFFIC["bytes_per_launch"] if TRAFFIC["sources_sha256"] == kernel_sources_digest() else None
 
-    e2e_ms, h2d, d2h = time_e2e(inp, device, max(5, args.steps // 5), 3, stream)
+    e2e_ms, h2d, d2h = time_e2e(inp, device, args.steps, args.warmup, stream)
     e2e_value = world * step_bytes / (e2e_ms * 1e-3) / 1e9
 
     line = {
@@ -679,18 +687,19 @@ def main():
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": "dense_state", "x": [4, 2048, 1536], "layout": "channel-last",
+        "config": {"workload": "dense_large", "x": [8, 5120, 8192],
+                   "layout": "channel-last ([8, 8192, 5120] storage)",
                    "weight": "bf16", "bias": True, "initial_states": True,
                    "final_states": True, "dweight": "fp32-partials",
                    "step": "forward + backward", "parallelism": f"replicas{world}",
-                   "l2": f"rotating {step.sets} buffer sets, "
-                         f"{step.sets * 4 * act_bytes(step.x[0]) / 2**20:.0f} MiB > L2"},
+                   "l2": f"inputs larger than L2: x and grad_out {act_bytes(step.x[0]) / 1e6:.0f} MB "
+                         f"each, one buffer set"},
         "tokens_per_s": round(tokens_per_s),
         "fwd_us": round(f_ms * 1e3, 2), "bwd_us": round(b_ms * 1e3, 2),
         "gpu_launches": args.steps * (step.launches_fwd + step.launches_bwd),
         "timing": "K forward calls then K backward calls, each as one CUDA graph replay "
                   "(after an untimed upload replay); events before, between and after",
-        "roofline": {"bound": "hbm", "kernel": f"{dominant[0]} call (dense_state)",
+        "roofline": {"bound": "hbm", "kernel": f"{dominant[0]} call (dense_large)",
                      "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                      "bytes_per_launch": dominant[2]},
@@ -704,10 +713,13 @@ def main():
     }
 
     if not args.no_breakdown:
+        del step
+        torch.cuda.empty_cache()
+        ds = workloads.dense_state()
         bd = [bench_conv_workload("dense_small", workloads.dense_small(), device, stream, peak,
                                   False, do_bwd=False),
-              bench_conv_workload("dense_state", inp, device, stream, peak, False),
-              bench_stream_floor(inp, device, stream, peak),
+              bench_conv_workload("dense_state", ds, device, stream, peak, False),
+              bench_stream_floor(ds, device, stream, peak),
               bench_conv_workload("packed_varlen", workloads.packed_varlen(), device, stream, peak,
                                   True),
               bench_update(device, stream, peak)]
@@ -718,23 +730,26 @@ def main():
         # the same dense step with a width-three filter (weight [D, 3], states [., D, 2])
         w3 = workloads.make_inputs(4, 1536, 2048, seed=0, initial_states=True, grad=True, width=3)
         bd.append(bench_conv_workload("dense_state_width3", w3, device, stream, peak, False))
-        large = workloads.dense_large(bias=True)
-        bd.append(bench_conv_workload("dense_large_bias", large, device, stream, peak, False))
-        large = dataclasses.replace(large, bias=None, deterministic=True)
+        bd.append(bench_conv_workload("dense_large_bias", inp, device, stream, peak, False))
+        large = dataclasses.replace(inp, bias=None, deterministic=True)
         bd.append(bench_conv_workload("dense_large_det", large, device, stream, peak, True))
         line["breakdown"] = bd
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         threads = oracle_threads()
-        s, nb, reps, shape = oracle_step_seconds(inp, 1.5, 200, None, threads)
-        s1, nb1, reps1, _ = oracle_step_seconds(inp, 1.0, 5, None, 1)
+        D = inp.x.shape[1]
+        chans = list(range(0, D, 32))  # every 32nd channel, all tokens
+        s, nb, reps, shape = oracle_step_seconds(inp, 1.5, 200, chans, threads)
+        s1, nb1, reps1, _ = oracle_step_seconds(inp, 1.0, 5, chans[:len(chans) // 8], 1)
         line["cpu_baseline"] = {"value": round(nb / s / 1e9, 4), "unit": UNIT, "cores": threads,
                                 "kind": "oracle", "cpu": host_cpu_model(),
-                                "sample": f"whole dense_state workload fwd+bwd, channels split over "
-                                          f"{threads} threads, {reps} reps, {s:.3f} s each "
-                                          f"({reps * s * threads:.0f} core-seconds)",
+                                "sample": f"dense_large workload fwd+bwd on {len(chans)} of {D} "
+                                          f"channels (every 32nd), all {inp.tokens} tokens; "
+                                          f"channels split over {threads} threads, {reps} reps, "
+                                          f"{s:.3f} s each ({reps * s * threads:.0f} core-seconds)",
                                 "single_thread": {"value": round(nb1 / s1 / 1e9, 4), "cores": 1,
-                                                  "sample": f"the same, one thread, {reps1} reps, "
+                                                  "sample": f"{len(chans) // 8} of those channels, "
+                                                            f"one thread, {reps1} reps, "
                                                             f"{s1:.2f} s each"}}
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -17,7 +17,6 @@
 // The kernels work with the halved weights and gp2 = 2 gp (see the activation
 // section of common.cuh), which leaves dxe unchanged and doubles the sums,
 // halved once before they are written.
-#include <atomic>
 #include <type_traits>
 
 #include "common.cuh"
@@ -202,9 +201,10 @@ __host__ __device__ constexpr size_t bwd_red_bytes(int threads) {
 }
 
 // Block-wide sum of the per-thread weight/bias sums (sums of gp2 = 2 gp, halved
-// here) over threadIdx.y (threads
-// with equal threadIdx.x own the same channels), in a fixed order, then either
-// FP32 atomics into ws[0] or a store into this block row's partial ws[blockIdx.y].
+// here) over threadIdx.y (threads with equal threadIdx.x own the same
+// channels), in a fixed order, stored into this block row's own partial row
+// ws[blockIdx.y].  No atomics: every value of the row is written, so the
+// workspace needs no zeroing and its contents on entry are never read.
 template <int V>
 __device__ __forceinline__ void block_wgrad_out(const BwdArgs& a, int d0, bool active,
                                                 const float (&aw)[V][kWidth], const float (&ab)[V]) {
@@ -1019,37 +1019,40 @@ static size_t bwd_smem_bytes(int vec, int threads) {
   return bwd_red_bytes<1>(threads);
 }
 
-// Opt the vector kernels in to more than 48 KB of dynamic shared memory (once).
+// Opt the vector kernels in to more than 48 KB of dynamic shared memory (once
+// per context: the attribute belongs to the module loaded in a context).
+static ContextCache g_bwd_attr_done;
 static cudaError_t bwd_smem_attributes() {
-  static std::atomic<int> done{0};
-  if (done.load(std::memory_order_acquire)) return cudaSuccess;
+  long long done = 0;
+  if (g_bwd_attr_done.get(&done) && done) return cudaSuccess;
   cudaError_t err = cudaSuccess;
   const int b8 = int(bwd_smem_bytes(8, kBwdThreads)), b4 = int(bwd_smem_bytes(4, kBwdThreads));
   for (auto f : {bwd_clv_kernel<8, kActSilu>, bwd_clv_kernel<8, kActNone>})
     if (err == cudaSuccess) err = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, b8);
   for (auto f : {bwd_clv_kernel<4, kActSilu>, bwd_clv_kernel<4, kActNone>})
     if (err == cudaSuccess) err = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, b4);
-  if (err == cudaSuccess) done.store(1, std::memory_order_release);
+  if (err == cudaSuccess) g_bwd_attr_done.put(1);
   return err;
 }
 
+static ContextCache g_bwd_occupancy[3];
 int bwd_blocks_per_sm(int vec) {
-  static std::atomic<int> cache[3];
-  const int i = vec == 8 ? 0 : vec == 4 ? 1 : 2;
-  int v = cache[i].load(std::memory_order_relaxed);
-  if (v == 0) {
-    int n = 0;
-    const int threads = bwd_block_threads(vec);
-    const size_t smem = bwd_smem_bytes(vec, threads);
-    bwd_smem_attributes();
-    const cudaError_t err =
-        vec == 8   ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, bwd_clv_kernel<8, kActSilu>, threads, smem)
-        : vec == 4 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, bwd_clv_kernel<4, kActSilu>, threads, smem)
-                   : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, bwd_cl_kernel<1, kActSilu>, threads, smem);
-    v = (err == cudaSuccess && n > 0) ? n : 1;
-    cache[i].store(v, std::memory_order_relaxed);
+  ContextCache& cache = g_bwd_occupancy[vec == 8 ? 0 : vec == 4 ? 1 : 2];
+  long long v = 0;
+  if (cache.get(&v) && v > 0) return int(v);
+  int n = 0;
+  const int threads = bwd_block_threads(vec);
+  const size_t smem = bwd_smem_bytes(vec, threads);
+  bwd_smem_attributes();
+  const cudaError_t err =
+      vec == 8   ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, bwd_clv_kernel<8, kActSilu>, threads, smem)
+      : vec == 4 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, bwd_clv_kernel<4, kActSilu>, threads, smem)
+                 : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, bwd_cl_kernel<1, kActSilu>, threads, smem);
+  if (err == cudaSuccess && n > 0) {
+    cache.put(n);
+    return n;
   }
-  return v;
+  return 1;
 }
 
 template <int ACT>

@@ -9,7 +9,6 @@
 // about one FLOP per byte, bound by HBM bandwidth, not a contraction.  The
 // weights are held halved, so the sums below are h = pre / 2 (see the
 // activation section of common.cuh).
-#include <atomic>
 #include <type_traits>
 
 #include "common.cuh"
@@ -423,35 +422,38 @@ __global__ void fwd_empty_kernel(const uint16_t* init, uint16_t* fin, int64_t n)
 
 // ---- host launchers ------------------------------------------------------------
 
-// Opt the vector kernel in to its ring's dynamic shared memory (once).
+// Opt the vector kernel in to its ring's dynamic shared memory (once per
+// context: the attribute belongs to the module loaded in a context).
+static ContextCache g_fwd_attr_done;
 static cudaError_t fwd_smem_attributes() {
-  static std::atomic<int> done{0};
-  if (done.load(std::memory_order_acquire)) return cudaSuccess;
+  long long done = 0;
+  if (g_fwd_attr_done.get(&done) && done) return cudaSuccess;
   const int bytes = int(fwd_ring_bytes<4>(kFwdThreads));
   cudaError_t err = cudaFuncSetAttribute(fwd_clv_kernel<4, kActSilu>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (err == cudaSuccess)
     err = cudaFuncSetAttribute(fwd_clv_kernel<4, kActNone>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (err == cudaSuccess) done.store(1, std::memory_order_release);
+  if (err == cudaSuccess) g_fwd_attr_done.put(1);
   return err;
 }
 
+static ContextCache g_fwd_occupancy[2];
 int fwd_blocks_per_sm(int vec) {
-  static std::atomic<int> cache[2];
-  const int i = vec == 4 ? 0 : 1;
-  int v = cache[i].load(std::memory_order_relaxed);
-  if (v == 0) {
-    int n = 0;
-    fwd_smem_attributes();
-    const cudaError_t err =
-        vec == 4 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fwd_clv_kernel<4, kActSilu>, 256,
-                                                                 fwd_ring_bytes<4>(256))
-                 : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fwd_cl_kernel<1, kActSilu>, 256, 0);
-    v = (err == cudaSuccess && n > 0) ? n : 1;
-    cache[i].store(v, std::memory_order_relaxed);
+  ContextCache& cache = g_fwd_occupancy[vec == 4 ? 0 : 1];
+  long long v = 0;
+  if (cache.get(&v) && v > 0) return int(v);
+  int n = 0;
+  fwd_smem_attributes();
+  const cudaError_t err =
+      vec == 4 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fwd_clv_kernel<4, kActSilu>, 256,
+                                                               fwd_ring_bytes<4>(256))
+               : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fwd_cl_kernel<1, kActSilu>, 256, 0);
+  if (err == cudaSuccess && n > 0) {
+    cache.put(n);
+    return n;
   }
-  return v;
+  return 1;
 }
 
 template <int ACT>

@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "common.cuh"
 
 namespace ccc {
@@ -26,6 +28,28 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
   cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
+
+// ---- per-context caches (context.cu) ---------------------------------------------
+
+constexpr int kMaxDevices = 64;
+
+// The current device and the CUDA context current on this thread (nullptr
+// before the runtime has made one current).
+cudaError_t current_device_context(int* dev, void** ctx);
+
+// One value per (device, context).  get() succeeds only when the stored value
+// was computed in the context current now; put() stores a value computed in
+// the current context (call it after the runtime call that computed it).
+class ContextCache {
+ public:
+  bool get(long long* value);
+  void put(long long value);
+
+ private:
+  std::mutex mu_;
+  void* ctx_[kMaxDevices] = {};
+  long long value_[kMaxDevices] = {};
+};
 
 enum Layout { kLayoutChannelLast = 0, kLayoutTimeContiguous = 1 };
 

@@ -9,17 +9,17 @@
 // from a fixed scratch array compiled into this library.
 //
 // The scratch array lives in device memory on every GPU that loads the
-// library, for as long as the library stays loaded.  Its address is looked up
-// once per device, on the first call made with that device current.  All calls
-// on a device share the one array: calls whose work overlaps on the GPU (for
-// example on two streams at once) race on it; calls on one stream are ordered
-// and safe.  The backward fully writes every per-block partial row before the
-// finalize kernel reads it, so stale contents from an earlier call are never
-// used.
-#include <atomic>
-#include <mutex>
-
+// library, for as long as the library stays loaded.  Its device address is
+// looked up with cudaGetSymbolAddress on the first call made in a CUDA context
+// (the array belongs to the module loaded in that context, so a new context
+// on the same device -- after cudaDeviceReset, say -- gets its own lookup).
+// All calls in a context share the one array: calls whose work overlaps on
+// the GPU (for example on two streams at once) race on it; calls on one stream
+// are ordered and safe.  The backward fully writes every per-block partial row
+// before the finalize kernel reads it, so stale contents from an earlier call
+// are never used.
 #include "ccc_conv1d.h"
+#include "launch.h"
 
 namespace {
 
@@ -28,28 +28,23 @@ constexpr size_t kScratchBytes = CCC_CONV1D_NOALLOC_SCRATCH_BYTES;
 
 static __device__ __align__(256) float g_bwd_scratch[kScratchBytes / sizeof(float)];
 
-constexpr int kMaxDevices = 64;
-std::atomic<void*> g_scratch_addr[kMaxDevices];
-std::mutex g_setup_mutex;
+// Device address of g_bwd_scratch, per (device, context).
+ccc::ContextCache g_scratch_addr;
 
-// Device address of g_bwd_scratch on the current device (looked up once).
+// Device address of g_bwd_scratch in the current context.  In host code the
+// array's name is only a host-side stand-in; the device address comes from the
+// runtime, checked before use.
 ccc_status scratch_address(void** out) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess) return CCC_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxDevices) return CCC_ERR_UNSUPPORTED;
-  void* p = g_scratch_addr[dev].load(std::memory_order_acquire);
-  if (p == nullptr) {
-    std::lock_guard<std::mutex> lock(g_setup_mutex);
-    p = g_scratch_addr[dev].load(std::memory_order_acquire);
-    if (p == nullptr) {
-      void* addr = nullptr;
-      if (cudaGetSymbolAddress(&addr, g_bwd_scratch) != cudaSuccess || addr == nullptr)
-        return CCC_ERR_CUDA;
-      g_scratch_addr[dev].store(addr, std::memory_order_release);
-      p = addr;
-    }
+  long long cached = 0;
+  if (g_scratch_addr.get(&cached) && cached != 0) {
+    *out = reinterpret_cast<void*>(static_cast<uintptr_t>(cached));
+    return CCC_OK;
   }
-  *out = p;
+  void* addr = nullptr;
+  if (cudaGetSymbolAddress(&addr, g_bwd_scratch) != cudaSuccess || addr == nullptr)
+    return CCC_ERR_CUDA;
+  g_scratch_addr.put(static_cast<long long>(reinterpret_cast<uintptr_t>(addr)));
+  *out = addr;
   return CCC_OK;
 }
 

@@ -4,7 +4,8 @@
  *
  * C ABI of the CUDA library (libccc_conv1d.so).  All tensor memory is owned by
  * the caller and the library allocates nothing.  Its only global state is a
- * cache of per-device launch limits and the built-in scratch array of
+ * cache of launch facts kept per (device, CUDA context) -- kernel attributes,
+ * occupancy figures -- and the built-in scratch array of
  * ccc_conv1d_bwd_noalloc; every other call may run concurrently with others on
  * different streams (on disjoint outputs).
  *
@@ -166,9 +167,11 @@ ccc_status ccc_conv1d_bwd(const ccc_tensor *x, const ccc_tensor *weight, const c
  * library is unloaded.  Nothing is allocated (no cudaMalloc, no cudaFree, no
  * allocating library routine).
  *
- *   - The first call on a device, with that device current, looks up the
- *     array's device address (cudaGetSymbolAddress); make that first call
- *     before any stream capture.
+ *   - The first call in a CUDA context (normally the device's primary
+ *     context), with that device current, looks up the array's device
+ *     address (cudaGetSymbolAddress); make that first call before any stream
+ *     capture.  A new context on the same device (after cudaDeviceReset, for
+ *     example) gets its own lookup on its first call.
  *   - A problem whose workspace (ccc_conv1d_bwd_workspace_size) exceeds the
  *     scratch returns CCC_ERR_SCRATCH_LIMIT and enqueues nothing.
  *   - All calls on a device share the array.  Calls whose work overlaps on
