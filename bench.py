@@ -540,6 +540,19 @@ def dist_env():
     return rank, world, local
 
 
+def headline_config(world: int) -> dict:
+    """The timed workload, shared by both arms: forward + backward of the large
+    dense workload (BF16 x stored [8, 8192, 5120], seen as [8, 5120, 8192])."""
+    B, D, T = 8, 5120, 8192
+    act_mb = B * T * D * 2 / 1e6
+    return {"workload": "dense_large", "x": [B, D, T],
+            "layout": f"channel-last ([{B}, {T}, {D}] storage)",
+            "weight": "bf16", "bias": True, "initial_states": True,
+            "final_states": True, "dweight": "fp32-partials",
+            "step": "forward + backward", "parallelism": f"replicas{world}",
+            "l2": f"inputs larger than L2: x and grad_out {act_mb:.0f} MB each, one buffer set"}
+
+
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
@@ -563,9 +576,7 @@ def run_reference(args):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(per, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "dense_large", "x": [8, 5120, 8192],
-                   "layout": "channel-last ([8, 8192, 5120] storage)",
-                   "sample_channels": len(channels)},
+        "config": headline_config(world),
         "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -687,13 +698,7 @@ def main():
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": "dense_large", "x": [8, 5120, 8192],
-                   "layout": "channel-last ([8, 8192, 5120] storage)",
-                   "weight": "bf16", "bias": True, "initial_states": True,
-                   "final_states": True, "dweight": "fp32-partials",
-                   "step": "forward + backward", "parallelism": f"replicas{world}",
-                   "l2": f"inputs larger than L2: x and grad_out {act_bytes(step.x[0]) / 1e6:.0f} MB "
-                         f"each, one buffer set"},
+        "config": headline_config(world),
         "tokens_per_s": round(tokens_per_s),
         "fwd_us": round(f_ms * 1e3, 2), "bwd_us": round(b_ms * 1e3, 2),
         "gpu_launches": args.steps * (step.launches_fwd + step.launches_bwd),

@@ -38,6 +38,7 @@ _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 
 ACTIVATIONS = {"silu": 1, None: 0, "none": 0, "identity": 0}
 BAD_CU_SEQLENS = 7
+BAD_SEQ_IDX = 102
 
 _lib = None
 
@@ -62,9 +63,9 @@ def _load():
         # broken copy; nothing else sets it.
         lib = ctypes.CDLL(os.environ.get("CCC_ORACLE_LIB") or build())
         P, I64, I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
-        lib.oracle_fwd.argtypes = [P, I64, I64, I64, P, I, P, P, I, P, I, P, P, P]
+        lib.oracle_fwd.argtypes = [P, I64, I64, I64, P, I, P, P, I, P, P, I, P, P, P]
         lib.oracle_fwd.restype = I
-        lib.oracle_bwd.argtypes = [P, I64, I64, I64, P, I, P, P, I, P, I, P, P, P, P, P, P, P, P]
+        lib.oracle_bwd.argtypes = [P, I64, I64, I64, P, I, P, P, I, P, P, I, P, P, P, P, P, P, P, P]
         lib.oracle_bwd.restype = I
         lib.oracle_update.argtypes = [P, I64, I64, P, I, P, I, P, P]
         lib.oracle_update.restype = I
@@ -90,6 +91,16 @@ def _act(activation):
     if activation not in ACTIVATIONS:
         raise ValueError(f"activation {activation!r} not supported")
     return ACTIVATIONS[activation]
+
+
+def _seq_idx(x_shape, seq_idx):
+    """Per-token sequence ids [B, T] as contiguous int32 (or None)."""
+    if seq_idx is None:
+        return None
+    ids = np.ascontiguousarray(seq_idx, dtype=np.int32)
+    if ids.shape != (x_shape[0], x_shape[2]):
+        raise ValueError(f"seq_idx must be [B, T] = {(x_shape[0], x_shape[2])}, got {ids.shape}")
+    return ids
 
 
 def _cu(B, cu_seqlens):
@@ -146,27 +157,38 @@ def check_cu_seqlens(cu_seqlens, total: int) -> bool:
 
 # ---- fp64 core ---------------------------------------------------------------
 
-def fwd_f64(x, weight, bias=None, cu_seqlens=None, initial_states=None, activation="silu"):
-    """Returns dict(out, pre: [B,D,T], final: [S,D,W-1]) in float64."""
+def _check_rc(rc, what):
+    if rc == BAD_CU_SEQLENS:
+        raise ValueError(f"malformed cu_seqlens (oracle status {rc})")
+    if rc == BAD_SEQ_IDX:
+        raise ValueError("seq_idx excludes cu_seqlens, initial states and final states")
+    if rc != 0:
+        raise ValueError(f"oracle {what} failed (status {rc})")
+
+
+def fwd_f64(x, weight, bias=None, cu_seqlens=None, initial_states=None, activation="silu",
+            seq_idx=None):
+    """Returns dict(out, pre: [B,D,T], final: [S,D,W-1]) in float64 (final is None
+    with seq_idx, which defines no state)."""
     lib = _load()
     x = _f64(x)
     B, D, T = x.shape
     w = _f64(weight)
     W = _width(w)
     cu, S = _cu(B, cu_seqlens)
+    ids = _seq_idx(x.shape, seq_idx)
     out = np.empty((B, D, T))
     pre = np.empty((B, D, T))
-    fin = np.empty((S, D, W - 1))
-    rc = lib.oracle_fwd(_ptr(x), B, D, T, _ptr(w), W, _ptr(_f64(bias)), _ptr(cu), S,
+    fin = np.empty((S, D, W - 1)) if ids is None else None
+    rc = lib.oracle_fwd(_ptr(x), B, D, T, _ptr(w), W, _ptr(_f64(bias)), _ptr(cu), S, _ptr(ids),
                         _ptr(_f64(initial_states)), _act(activation), _ptr(out), _ptr(pre),
                         _ptr(fin))
-    if rc != 0:
-        raise ValueError(f"malformed cu_seqlens (oracle status {rc})")
+    _check_rc(rc, "forward")
     return dict(out=out, pre=pre, final=fin)
 
 
 def bwd_f64(x, weight, g, bias=None, cu_seqlens=None, initial_states=None, dfinal_states=None,
-            activation="silu"):
+            activation="silu", seq_idx=None):
     """Returns dict(dx [B,D,T], dinit [S,D,W-1], dw, dw_abs [D,W], db, db_abs [D]) in
     float64.  ``dinit`` is the gradient at the W - 1 positions before each
     sequence, given whether or not initial states were passed."""
@@ -179,18 +201,18 @@ def bwd_f64(x, weight, g, bias=None, cu_seqlens=None, initial_states=None, dfina
     if g.shape != x.shape:
         raise ValueError("g must have the shape of x")
     cu, S = _cu(B, cu_seqlens)
+    ids = _seq_idx(x.shape, seq_idx)
     dx = np.empty((B, D, T))
     dinit = np.empty((S, D, W - 1))
     dw = np.empty((D, W))
     dw_abs = np.empty((D, W))
     db = np.empty((D,))
     db_abs = np.empty((D,))
-    rc = lib.oracle_bwd(_ptr(x), B, D, T, _ptr(w), W, _ptr(_f64(bias)), _ptr(cu), S,
+    rc = lib.oracle_bwd(_ptr(x), B, D, T, _ptr(w), W, _ptr(_f64(bias)), _ptr(cu), S, _ptr(ids),
                         _ptr(_f64(initial_states)), _act(activation), _ptr(g),
                         _ptr(_f64(dfinal_states)), _ptr(dx), _ptr(dinit), _ptr(dw),
                         _ptr(dw_abs), _ptr(db), _ptr(db_abs))
-    if rc != 0:
-        raise ValueError(f"oracle backward failed (status {rc})")
+    _check_rc(rc, "backward")
     return dict(dx=dx, dinit=dinit, dw=dw, dw_abs=dw_abs, db=db, db_abs=db_abs)
 
 
@@ -212,23 +234,26 @@ def update_f64(x, conv_state, weight, bias=None, activation="silu"):
 
 # ---- BF16 interface ----------------------------------------------------------
 
-def fwd(x, weight, bias=None, cu_seqlens=None, initial_states=None, activation="silu"):
-    """BF16 forward.  Returns dict(out, final: uint16 bits; out64, pre64, final64: float64)."""
+def fwd(x, weight, bias=None, cu_seqlens=None, initial_states=None, activation="silu",
+        seq_idx=None):
+    """BF16 forward.  Returns dict(out, final: uint16 bits; out64, pre64, final64:
+    float64); final and final64 are None with seq_idx."""
     w, _ = _weight_f64(weight)
     r = fwd_f64(bf16_decode(x), w, bf16_decode(bias), cu_seqlens, bf16_decode(initial_states),
-                activation)
-    return dict(out=bf16_encode(r["out"]), out64=r["out"], pre64=r["pre"],
-                final=bf16_encode(r["final"]), final64=r["final"])
+                activation, seq_idx)
+    fin = None if r["final"] is None else bf16_encode(r["final"])
+    return dict(out=bf16_encode(r["out"]), out64=r["out"], pre64=r["pre"], final=fin,
+                final64=r["final"])
 
 
 def bwd(x, weight, g, bias=None, cu_seqlens=None, initial_states=None, dfinal_states=None,
-        activation="silu"):
+        activation="silu", seq_idx=None):
     """BF16 backward.  Returns dict(dx, dinit, db: uint16 bits; dw: uint16 bits for a
     BF16 weight or float32 for an FP32 weight; dx64, dinit64, dw64, db64, dw_abs,
     db_abs: float64)."""
     w, w_f32 = _weight_f64(weight)
     r = bwd_f64(bf16_decode(x), w, bf16_decode(g), bf16_decode(bias), cu_seqlens,
-                bf16_decode(initial_states), bf16_decode(dfinal_states), activation)
+                bf16_decode(initial_states), bf16_decode(dfinal_states), activation, seq_idx)
     dw = r["dw"].astype(np.float32) if w_f32 else bf16_encode(r["dw"])
     return dict(dx=bf16_encode(r["dx"]), dinit=bf16_encode(r["dinit"]), dw=dw,
                 db=bf16_encode(r["db"]), dx64=r["dx"], dinit64=r["dinit"], dw64=r["dw"],

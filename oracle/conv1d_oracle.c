@@ -24,6 +24,13 @@
  * packed call (each with its own initial/final state, nothing crosses a
  * boundary).
  *
+ * Per-token sequence ids (the cuDNN page's seq_idx[B, T] keyword, mutually
+ * exclusive with cu_seqlens): tokens of a dense row that carry the same id
+ * form one sequence, so tap k of token t reads xe[t - S + k] only when that
+ * token carries the id of token t, and reads zero otherwise.  The pages fix
+ * nothing more; initial and final states are not defined with seq_idx and are
+ * rejected in combination with it.
+ *
  * Backward (gradients of L with g = dL/dout and gf = dL/dfinal):
  *   gp[t]    = g[t] * silu'(pre[t]),   silu'(p) = s(p) * (1 + p * (1 - s(p)))
  *   dxe[j]   = sum_k w[k] * gp[j + S - k]   (only terms with 0 <= j+S-k < len)
@@ -47,7 +54,8 @@
 
 #define CONV_WMAX 4 /* widths 2..4 */
 
-enum { ORC_OK = 0, ORC_BAD_CU_SEQLENS = 7, ORC_NO_MEMORY = 100, ORC_BAD_WIDTH = 101 };
+enum { ORC_OK = 0, ORC_BAD_CU_SEQLENS = 7, ORC_NO_MEMORY = 100, ORC_BAD_WIDTH = 101,
+       ORC_BAD_SEQ_IDX = 102 };
 
 /* ---- BF16 rounding ------------------------------------------------------ */
 
@@ -137,13 +145,28 @@ static double xe(const double *x, const double *init, int S, int64_t j)
     return init ? init[j + S] : 0.0;
 }
 
-static double pre_activation(const double *x, const double *init, const double *w, int W,
-                             double b, int64_t t)
+/* Whether input position j (of the same row) feeds token t: always without
+ * per-token ids (positions before the row read the initial state or zero);
+ * with ids, only positions carrying the id of token t. */
+static int same_seq(const int32_t *ids, int64_t j, int64_t t)
+{
+    return !ids || j < 0 || ids[j] == ids[t];
+}
+
+static double pre_activation(const double *x, const double *init, const int32_t *ids,
+                             const double *w, int W, double b, int64_t t)
 {
     double p = b;
     for (int k = 0; k < W; ++k)
-        p += w[k] * xe(x, init, W - 1, t - (W - 1) + k);
+        if (same_seq(ids, t - (W - 1) + k, t))
+            p += w[k] * xe(x, init, W - 1, t - (W - 1) + k);
     return p;
+}
+
+/* seq_idx excludes cu_seqlens and the states (see the header comment). */
+static int seq_idx_ok(const int32_t *seq_idx, const int32_t *cu, const void *init, const void *fin)
+{
+    return !seq_idx || (!cu && !init && !fin);
 }
 
 /* ---- forward ------------------------------------------------------------ */
@@ -152,16 +175,20 @@ static double pre_activation(const double *x, const double *init, const double *
  * x:     [B][D][T] (packed: B == 1 and T == token total)
  * w:     [D][W], 2 <= W <= 4;  bias: [D] or NULL
  * cu:    [n_seq + 1] or NULL (dense: n_seq is taken as B)
+ * seq_idx: [B][T] per-token sequence ids or NULL (dense only, no states)
  * init:  [n_seq][D][W-1] or NULL
  * out, pre: [B][D][T] (pre may be NULL);  fin: [n_seq][D][W-1] or NULL
  */
 int oracle_fwd(const double *x, int64_t B, int64_t D, int64_t T,
                const double *w, int W, const double *bias, const int32_t *cu, int n_seq,
-               const double *init, int act, double *out, double *pre, double *fin)
+               const int32_t *seq_idx, const double *init, int act, double *out, double *pre,
+               double *fin)
 {
     if (W < 2 || W > CONV_WMAX)
         return ORC_BAD_WIDTH;
     const int S = W - 1;
+    if (!seq_idx_ok(seq_idx, cu, init, fin))
+        return ORC_BAD_SEQ_IDX;
     if (cu && oracle_check_cu_seqlens(cu, n_seq, T))
         return ORC_BAD_CU_SEQLENS;
     if (!cu)
@@ -175,8 +202,9 @@ int oracle_fwd(const double *x, int64_t B, int64_t D, int64_t T,
             int64_t base = (row * D + d) * T + start;
             const double *xs = x + base;
             const double *is = init ? init + ((int64_t)n * D + d) * S : NULL;
+            const int32_t *ids = seq_idx ? seq_idx + row * T + start : NULL;
             for (int64_t t = 0; t < len; ++t) {
-                double p = pre_activation(xs, is, wd, W, b, t);
+                double p = pre_activation(xs, is, ids, wd, W, b, t);
                 out[base + t] = activate(p, act);
                 if (pre)
                     pre[base + t] = p;
@@ -203,12 +231,15 @@ int oracle_fwd(const double *x, int64_t B, int64_t D, int64_t T,
  */
 int oracle_bwd(const double *x, int64_t B, int64_t D, int64_t T,
                const double *w, int W, const double *bias, const int32_t *cu, int n_seq,
-               const double *init, int act, const double *g, const double *gfin,
-               double *dx, double *dinit, double *dw, double *dw_abs, double *db, double *db_abs)
+               const int32_t *seq_idx, const double *init, int act, const double *g,
+               const double *gfin, double *dx, double *dinit, double *dw, double *dw_abs,
+               double *db, double *db_abs)
 {
     if (W < 2 || W > CONV_WMAX)
         return ORC_BAD_WIDTH;
     const int S = W - 1;
+    if (!seq_idx_ok(seq_idx, cu, init, gfin))
+        return ORC_BAD_SEQ_IDX;
     if (cu && oracle_check_cu_seqlens(cu, n_seq, T))
         return ORC_BAD_CU_SEQLENS;
     if (!cu)
@@ -229,11 +260,14 @@ int oracle_bwd(const double *x, int64_t B, int64_t D, int64_t T,
             const double *gs = g + base;
             const double *is = init ? init + ((int64_t)n * D + d) * S : NULL;
             const double *gfs = gfin ? gfin + ((int64_t)n * D + d) * S : NULL;
+            const int32_t *ids = seq_idx ? seq_idx + row * T + start : NULL;
             /* gradient at the pre-activation; weight and bias sums */
             for (int64_t t = 0; t < len; ++t) {
-                gp[t] = gs[t] * activate_grad(pre_activation(xs, is, wd, W, b, t), act);
+                gp[t] = gs[t] * activate_grad(pre_activation(xs, is, ids, wd, W, b, t), act);
                 for (int k = 0; k < W; ++k) {
                     double term = gp[t] * xe(xs, is, S, t - (W - 1) + k);
+                    if (!same_seq(ids, t - (W - 1) + k, t))
+                        term = 0.0; /* tap reads another sequence: zero */
                     sdw[k] += term;
                     sdw_abs[k] += fabs(term);
                 }
@@ -245,7 +279,7 @@ int oracle_bwd(const double *x, int64_t B, int64_t D, int64_t T,
                 double acc = 0.0;
                 for (int k = 0; k < W; ++k) {
                     int64_t t = j + (W - 1) - k; /* the output that tap k reads xe[j] for */
-                    if (t >= 0 && t < len)
+                    if (t >= 0 && t < len && same_seq(ids, j, t))
                         acc += wd[k] * gp[t];
                 }
                 if (gfs && j >= len - S)

@@ -37,13 +37,18 @@ MUTANTS = {
     "update_drops_bias": ("double p = bias ? bias[d] : 0.0;\n            for (int k = 0; k < W; ++k)\n                p += wd[k] * ext[k];",
                           "double p = 0.0;\n            for (int k = 0; k < W; ++k)\n                p += wd[k] * ext[k];"),
     "bf16_truncates": ("double r = rint(ldexp(a, -qexp));", "double r = floor(ldexp(a, -qexp));"),
-    "bias_dropped": ("double p = b;\n    for (int k = 0; k < W; ++k)\n        p += w[k]",
-                     "double p = 0.0 * b;\n    for (int k = 0; k < W; ++k)\n        p += w[k]"),
+    "bias_dropped": ("double p = b;\n    for (int k = 0; k < W; ++k)\n        if (same_seq",
+                     "double p = 0.0 * b;\n    for (int k = 0; k < W; ++k)\n        if (same_seq"),
     "dw_abs_shifted_tap": ("sdw_abs[k] += fabs(term);", "sdw_abs[(k + 1) % W] += fabs(term);"),
     "dw_abs_doubled": ("sdw_abs[k] += fabs(term);", "sdw_abs[k] += 2.0 * fabs(term);"),
     "db_abs_without_act_grad": ("sdb_abs += fabs(gp[t]);", "sdb_abs += fabs(gs[t]);"),
-    "width_state_offset": ("const double *is = init ? init + ((int64_t)n * D + d) * S : NULL;\n            for (int64_t t = 0; t < len; ++t) {",
-                           "const double *is = init ? init + ((int64_t)n * D + d) * 3 : NULL;\n            for (int64_t t = 0; t < len; ++t) {"),
+    "seq_idx_ordered_not_equal": ("return !ids || j < 0 || ids[j] == ids[t];",
+                                  "return !ids || j < 0 || ids[j] <= ids[t];"),
+    "seq_idx_dx_unmasked": ("if (t >= 0 && t < len && same_seq(ids, j, t))", "if (t >= 0 && t < len)"),
+    "seq_idx_dw_unmasked": ("if (!same_seq(ids, t - (W - 1) + k, t))\n                        term = 0.0;",
+                            "if (0)\n                        term = 0.0;"),
+    "width_state_offset": ("const double *is = init ? init + ((int64_t)n * D + d) * S : NULL;\n            const int32_t *ids",
+                           "const double *is = init ? init + ((int64_t)n * D + d) * 3 : NULL;\n            const int32_t *ids"),
 }
 
 

@@ -611,3 +611,176 @@ def test_widths_outside_two_to_four_are_rejected():
         oracle.fwd_f64(np.zeros((1, 2, 3)), np.zeros((2, 5)))
     with pytest.raises(ValueError):
         oracle.fwd_f64(np.zeros((1, 2, 3)), np.zeros((2, 1)))
+
+
+# ---- per-token sequence ids (the cuDNN page's seq_idx[B, T] keyword) ------------
+#
+# Reading: tokens of a row carrying the same id form one sequence; a tap reads
+# another sequence's token as zero.  The pins below do not depend on that
+# reading's implementation in the oracle: a masked banded matrix, packed
+# cu_seqlens calls and per-run dense calls, finite differences and autograd.
+
+
+def _masked_band_pre(x, w, b, ids):
+    """Brute force: per row and channel, the T x T matrix whose entry (t, j) is
+    w[j - t + S] when 0 <= t - j <= S and tokens j and t carry the same id."""
+    B, D, T = x.shape
+    W = w.shape[1]
+    S = W - 1
+    pre = np.zeros((B, D, T))
+    for bb in range(B):
+        M = np.zeros((D, T, T))
+        for t in range(T):
+            for j in range(max(0, t - S), t + 1):
+                if ids[bb, j] == ids[bb, t]:
+                    M[:, t, j] = w[:, j - t + S]
+        for d in range(D):
+            pre[bb, d] = M[d] @ x[bb, d] + (b[d] if b is not None else 0.0)
+    return pre
+
+
+def _runs(lengths, first=0, step=1):
+    return np.repeat(first + step * np.arange(len(lengths)), lengths).astype(np.int32)
+
+
+@pytest.mark.parametrize("W", [2, 3, 4])
+@pytest.mark.parametrize("kind", ["runs", "random"])
+def test_seq_idx_matches_masked_band_matrix(W, kind):
+    rng = np.random.default_rng(40 + W)
+    B, D, T = 2, 3, 19
+    x = rng.standard_normal((B, D, T))
+    w = rng.uniform(-0.5, 0.5, (D, W))
+    b = rng.uniform(-0.1, 0.1, D)
+    if kind == "runs":
+        ids = np.stack([_runs([4, 1, 6, 8]), _runs([1, 1, 17], first=7, step=3)])
+    else:  # ids need not form runs: equality alone decides
+        ids = rng.integers(0, 3, (B, T)).astype(np.int32)
+    ref = _masked_band_pre(x, w, b, ids)
+    for act in ("silu", None):
+        r = oracle.fwd_f64(x, w, b, None, None, act, seq_idx=ids)
+        np.testing.assert_allclose(r["pre"], ref, rtol=1e-13, atol=1e-14)
+        np.testing.assert_allclose(r["out"], _silu(ref) if act else ref, rtol=1e-13, atol=1e-14)
+        assert r["final"] is None
+
+
+@pytest.mark.parametrize("lengths", [[1], [3, 1, 5, 2, 7], [2, 2, 2, 2], [1, 1, 1, 9]])
+def test_seq_idx_runs_equal_packed_cu_seqlens(lengths):
+    D = 3
+    T = sum(lengths)
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    ids = _runs(lengths, first=-5, step=4)[None]  # any int32 values
+    x = _rand_bf16((1, D, T))
+    g = _rand_bf16((1, D, T))
+    w = _rand_bf16((D, 4), 0.3)
+    b = _rand_bf16((D,), 0.05)
+    pf = oracle.fwd(x, w, b, cu)
+    sf = oracle.fwd(x, w, b, seq_idx=ids)
+    assert np.array_equal(sf["out"], pf["out"])
+    pb = oracle.bwd(x, w, g, b, cu)
+    sb = oracle.bwd(x, w, g, b, seq_idx=ids)
+    assert np.array_equal(sb["dx"], pb["dx"])
+    np.testing.assert_allclose(sb["dw64"], pb["dw64"], rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(sb["db64"], pb["db64"], rtol=1e-13, atol=1e-13)
+
+
+def test_seq_idx_rows_equal_per_run_dense_calls():
+    D = 4
+    rows = [[5, 2, 9], [16], [1, 15]]
+    T = 16
+    ids = np.stack([_runs(r, first=10 * i) for i, r in enumerate(rows)])
+    x = _rand_bf16((len(rows), D, T))
+    g = _rand_bf16((len(rows), D, T))
+    w = _rand_bf16((D, 4), 0.3)
+    b = _rand_bf16((D,), 0.05)
+    sf = oracle.fwd(x, w, b, seq_idx=ids)
+    sb = oracle.bwd(x, w, g, b, seq_idx=ids)
+    dw = np.zeros((D, 4))
+    for bb, lens in enumerate(rows):
+        s0 = 0
+        for L in lens:
+            sl = slice(s0, s0 + L)
+            xs = np.ascontiguousarray(x[bb:bb + 1, :, sl])
+            gs = np.ascontiguousarray(g[bb:bb + 1, :, sl])
+            assert np.array_equal(sf["out"][bb:bb + 1, :, sl], oracle.fwd(xs, w, b)["out"])
+            rb = oracle.bwd(xs, w, gs, b)
+            assert np.array_equal(sb["dx"][bb:bb + 1, :, sl], rb["dx"])
+            dw += rb["dw64"]
+            s0 += L
+    np.testing.assert_allclose(sb["dw64"], dw, rtol=1e-12, atol=1e-12)
+
+
+def test_seq_idx_constant_equals_dense():
+    B, D, T = 2, 3, 12
+    x = _rand_bf16((B, D, T))
+    g = _rand_bf16((B, D, T))
+    w = _rand_bf16((D, 4), 0.3)
+    b = _rand_bf16((D,), 0.05)
+    ids = np.full((B, T), 3, np.int32)
+    assert np.array_equal(oracle.fwd(x, w, b, seq_idx=ids)["out"], oracle.fwd(x, w, b)["out"])
+    sb, db = oracle.bwd(x, w, g, b, seq_idx=ids), oracle.bwd(x, w, g, b)
+    assert np.array_equal(sb["dx"], db["dx"])
+    assert np.array_equal(sb["dw64"], db["dw64"])
+
+
+@pytest.mark.parametrize("kind", ["runs", "random"])
+def test_seq_idx_bwd_matches_central_finite_differences(kind):
+    rng = np.random.default_rng(55)
+    B, D, T = 2, 2, 11
+    x = rng.standard_normal((B, D, T))
+    g = rng.standard_normal((B, D, T))
+    w = rng.uniform(-0.8, 0.8, (D, 4))
+    b = rng.uniform(-0.3, 0.3, D)
+    ids = (np.stack([_runs([3, 1, 7]), _runs([6, 5])]) if kind == "runs"
+           else rng.integers(0, 2, (B, T)).astype(np.int32))
+
+    def L():
+        return float((oracle.fwd_f64(x, w, b, None, None, "silu", seq_idx=ids)["out"] * g).sum())
+
+    r = oracle.bwd_f64(x, w, g, b, None, None, None, "silu", seq_idx=ids)
+    tol = dict(rtol=1e-6, atol=1e-7)
+    np.testing.assert_allclose(r["dx"], _central_diff(L, x), **tol)
+    np.testing.assert_allclose(r["dw"], _central_diff(L, w), **tol)
+    np.testing.assert_allclose(r["db"], _central_diff(L, b), **tol)
+
+
+def test_seq_idx_bwd_matches_torch_autograd_float64():
+    """Autograd through the taps written with a per-tap id mask."""
+    rng = np.random.default_rng(77)
+    B, D, T, W = 2, 3, 14, 4
+    S = W - 1
+    x = rng.standard_normal((B, D, T))
+    g = rng.standard_normal((B, D, T))
+    w = rng.uniform(-0.5, 0.5, (D, W))
+    b = rng.uniform(-0.1, 0.1, D)
+    ids = np.stack([_runs([2, 5, 7]), rng.integers(0, 3, T).astype(np.int32)])
+    tx, tw, tb = (torch.tensor(a, requires_grad=True) for a in (x, w, b))
+    pre = tb[None, :, None].expand(B, D, T).clone()
+    for k in range(W):
+        sh = S - k  # tap k reads position t - sh
+        xs = F.pad(tx, (sh, 0))[:, :, :T]
+        m = np.zeros((B, T))
+        for bb in range(B):
+            for t in range(sh, T):
+                m[bb, t] = ids[bb, t - sh] == ids[bb, t]
+        pre = pre + tw[None, :, k:k + 1] * xs * torch.from_numpy(m)[:, None, :]
+    (F.silu(pre) * torch.from_numpy(g)).sum().backward()
+    r = oracle.bwd_f64(x, w, g, b, None, None, None, "silu", seq_idx=ids)
+    np.testing.assert_allclose(r["dx"], tx.grad.numpy(), rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(r["dw"], tw.grad.numpy(), rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(r["db"], tb.grad.numpy(), rtol=1e-12, atol=1e-13)
+
+
+def test_seq_idx_declines_packed_and_states():
+    """The page makes seq_idx and cu_seqlens mutually exclusive; no state is
+    defined with seq_idx."""
+    x = np.zeros((1, 2, 4))
+    w = np.zeros((2, 4))
+    ids = np.zeros((1, 4), np.int32)
+    with pytest.raises(ValueError):
+        oracle.fwd_f64(x, w, None, np.array([0, 4], np.int32), None, "silu", seq_idx=ids)
+    with pytest.raises(ValueError):
+        oracle.fwd_f64(x, w, None, None, np.zeros((1, 2, 3)), "silu", seq_idx=ids)
+    with pytest.raises(ValueError):
+        oracle.bwd_f64(x, w, x, None, None, None, np.zeros((1, 2, 3)), "silu", seq_idx=ids)
+    with pytest.raises(ValueError):
+        oracle.fwd_f64(x, w, None, None, None, "silu", seq_idx=np.zeros((1, 3), np.int32))
