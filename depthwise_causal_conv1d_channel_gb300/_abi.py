@@ -30,7 +30,7 @@ CCC_ERR_SCRATCH_LIMIT = 8
 CCC_BF16, CCC_F32, CCC_I32 = 0, 1, 2
 CCC_ACT_NONE, CCC_ACT_SILU = 0, 1
 
-ABI_VERSION = 1
+ABI_VERSION = 2
 
 EXPORTED = (
     "ccc_conv1d_fwd",
@@ -74,11 +74,11 @@ def _load():
     P = ctypes.POINTER(ccc_tensor)
     V = ctypes.c_void_p
     I = ctypes.c_int
-    lib.ccc_conv1d_fwd.argtypes = [P, P, P, P, P, P, P, I, V, V]
+    lib.ccc_conv1d_fwd.argtypes = [P, P, P, P, P, P, P, P, I, V, V]
     lib.ccc_conv1d_fwd.restype = I
     lib.ccc_conv1d_bwd_workspace_size.argtypes = [P, I]
     lib.ccc_conv1d_bwd_workspace_size.restype = ctypes.c_size_t
-    lib.ccc_conv1d_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, P, I, I, V, ctypes.c_size_t, V, V]
+    lib.ccc_conv1d_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, I, I, V, ctypes.c_size_t, V, V]
     lib.ccc_conv1d_bwd.restype = I
     lib.ccc_conv1d_bwd_noalloc.argtypes = [P, P, P, P, P, P, P, P, P, P, P, I, I, V, V]
     lib.ccc_conv1d_bwd_noalloc.restype = I
@@ -147,8 +147,9 @@ def _status_ptr(status):
 
 
 def ccc_conv1d_fwd(x, weight, bias, cu_seqlens, initial_states, out, final_states,
-                   activation: int, status=None, stream=None) -> int:
-    ds = [desc(t) for t in (x, weight, bias, cu_seqlens, initial_states, out, final_states)]
+                   activation: int, status=None, stream=None, seq_idx=None) -> int:
+    ds = [desc(t) for t in (x, weight, bias, cu_seqlens, seq_idx, initial_states, out,
+                            final_states)]
     return lib.ccc_conv1d_fwd(*[_ref(d) for d in ds], int(activation), _status_ptr(status),
                               _stream(stream))
 
@@ -159,9 +160,9 @@ def ccc_conv1d_bwd_workspace_size(x, deterministic: bool) -> int:
 
 def ccc_conv1d_bwd(x, weight, bias, cu_seqlens, initial_states, dout, dfinal_states, dx,
                    dweight, dbias, dinitial_states, activation: int, deterministic: bool,
-                   workspace, status=None, stream=None) -> int:
-    ds = [desc(t) for t in (x, weight, bias, cu_seqlens, initial_states, dout, dfinal_states,
-                            dx, dweight, dbias, dinitial_states)]
+                   workspace, status=None, stream=None, seq_idx=None) -> int:
+    ds = [desc(t) for t in (x, weight, bias, cu_seqlens, seq_idx, initial_states, dout,
+                            dfinal_states, dx, dweight, dbias, dinitial_states)]
     ws_ptr = workspace.data_ptr() if workspace is not None and workspace.numel() > 0 else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     return lib.ccc_conv1d_bwd(*[_ref(d) for d in ds], int(activation), int(bool(deterministic)),

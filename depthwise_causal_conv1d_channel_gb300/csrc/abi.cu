@@ -128,10 +128,12 @@ struct Problem {
   int w_f32 = 0;
   int W = kWidth;  // filter width, 2..4 (four on the optimized route)
   int sw = kState; // state entries per channel, W - 1
+  bool ids = false; // per-token sequence ids given
 };
 
 ccc_status check_common(const ccc_tensor* x, const ccc_tensor* weight, const ccc_tensor* bias,
-                        const ccc_tensor* cu, const ccc_tensor* init, int activation, Problem& pb) {
+                        const ccc_tensor* cu, const ccc_tensor* ids, const ccc_tensor* init,
+                        int activation, Problem& pb) {
   if (!well_formed(x, 3) || x->dtype != CCC_BF16) return CCC_ERR_INVALID_ARG;
   if (x->shape[1] < 1) return CCC_ERR_INVALID_ARG;
   if (x->shape[0] > INT32_MAX || x->shape[1] > INT32_MAX) return CCC_ERR_UNSUPPORTED;
@@ -165,6 +167,16 @@ ccc_status check_common(const ccc_tensor* x, const ccc_tensor* weight, const ccc
     pb.n_seq = int(cu->shape[0] - 1);
   } else {
     pb.n_seq = pb.B;
+  }
+  if (ids) {
+    // per-token sequence ids [B, T] int32, any non-negative strides; the page
+    // makes them mutually exclusive with cu_seqlens, and no state is defined
+    // with them
+    if (!well_formed(ids, 2) || ids->dtype != CCC_I32 || !shape_is(ids, pb.B, pb.T))
+      return CCC_ERR_INVALID_ARG;
+    if (pb.packed) return CCC_ERR_INVALID_ARG;
+    if (init) return CCC_ERR_UNSUPPORTED;
+    pb.ids = true;
   }
   if (init && !state_ok(init, pb.n_seq, pb.D, pb.sw)) return CCC_ERR_INVALID_ARG;
   return CCC_OK;
@@ -251,6 +263,12 @@ ccc::WeightRef weight_ref(const ccc_tensor* weight, const ccc_tensor* bias) {
   return r;
 }
 
+// Element strides of the [B, T] ids (size-1 dims contribute nothing).
+void ids_strides(const ccc_tensor* ids, int64_t& sb, int64_t& st) {
+  sb = ids && ids->shape[0] > 1 ? ids->stride[0] : 0;
+  st = ids && ids->shape[1] > 1 ? ids->stride[1] : 0;
+}
+
 ccc::Seqs seqs_of(const Problem& pb, const ccc_tensor* cu) {
   ccc::Seqs s{};
   s.cu = pb.packed ? static_cast<const int*>(cu->data) : nullptr;
@@ -304,7 +322,15 @@ static FwdPlan plan_bdt(int64_t rows) {
   return p;
 }
 
-FwdPlan plan_fwd(int kind, int vec, int64_t Q, int D, int64_t rows, int sm_count) {
+FwdPlan plan_fwd(int kind, int vec, int64_t Q, int D, int64_t rows, int sm_count, bool ids) {
+  if (ids) {  // the general kernels with id masks: vec 4 or 1
+    FwdPlan p = kind == kLayoutTimeContiguous
+                    ? plan_bdt(rows)
+                    : plan_cl(vec, Q, D, sm_count, fwd_ids_blocks_per_sm(vec), 1, 12, kGeneralThreads);
+    p.ids = 1;
+    if (kind == kLayoutTimeContiguous) p.vec = 1;
+    return p;
+  }
   if (kind == kLayoutTimeContiguous) {
     FwdPlan p = plan_bdt(rows);
     p.vec = vec;  // 8: 16-byte token chunks per lane
@@ -323,7 +349,15 @@ FwdPlan plan_fwd(int kind, int vec, int64_t Q, int D, int64_t rows, int sm_count
   return plan_cl(vec, Q, D, sm_count, bps, waves, 12, 256, vec == 4 ? 6 : 1);
 }
 
-BwdPlan plan_bwd(int kind, int vec, int64_t Q, int D, int64_t rows, int sm_count) {
+BwdPlan plan_bwd(int kind, int vec, int64_t Q, int D, int64_t rows, int sm_count, bool ids) {
+  if (ids) {  // the general kernels with id masks: vec 4 or 1
+    BwdPlan p = kind == kLayoutTimeContiguous
+                    ? plan_bdt(rows)
+                    : plan_cl(vec, Q, D, sm_count, bwd_ids_blocks_per_sm(vec), 1, 18, kGeneralThreads);
+    p.ids = 1;
+    if (kind == kLayoutTimeContiguous) p.vec = 1;
+    return p;
+  }
   if (kind == kLayoutTimeContiguous) {
     if (vec == 16) {  // a warp per pair of channel rows
       BwdPlan p{};
@@ -371,18 +405,20 @@ const char* ccc_status_string(int status) {
 }
 
 ccc_status ccc_conv1d_fwd(const ccc_tensor* x, const ccc_tensor* weight, const ccc_tensor* bias,
-                          const ccc_tensor* cu_seqlens, const ccc_tensor* initial_states,
-                          const ccc_tensor* out, const ccc_tensor* final_states, int activation,
-                          int* d_status, cudaStream_t stream) {
+                          const ccc_tensor* cu_seqlens, const ccc_tensor* seq_idx,
+                          const ccc_tensor* initial_states, const ccc_tensor* out,
+                          const ccc_tensor* final_states, int activation, int* d_status,
+                          cudaStream_t stream) {
   Problem pb;
-  ccc_status st = check_common(x, weight, bias, cu_seqlens, initial_states, activation, pb);
+  ccc_status st = check_common(x, weight, bias, cu_seqlens, seq_idx, initial_states, activation, pb);
   if (st != CCC_OK) return st;
   if (!same_act_shape(out, pb)) return CCC_ERR_INVALID_ARG;
   if (layout_of(out) != pb.layout || !self_disjoint(out)) return CCC_ERR_UNSUPPORTED;
   if (final_states && !state_ok(final_states, pb.n_seq, pb.D, pb.sw)) return CCC_ERR_INVALID_ARG;
+  if (final_states && pb.ids) return CCC_ERR_UNSUPPORTED;  // no state with seq_idx
   // final_states must not share memory with the inputs (cuDNN page, aliasing rule);
   // neither may out.
-  for (const ccc_tensor* in : {x, weight, bias, cu_seqlens, initial_states}) {
+  for (const ccc_tensor* in : {x, weight, bias, cu_seqlens, seq_idx, initial_states}) {
     if (!in) continue;
     if ((final_states && overlaps(final_states, in)) || overlaps(out, in)) return CCC_ERR_ALIAS;
   }
@@ -400,27 +436,29 @@ ccc_status ccc_conv1d_fwd(const ccc_tensor* x, const ccc_tensor* weight, const c
   a.fin = final_states ? static_cast<uint16_t*>(final_states->data) : nullptr;
   a.sw = pb.sw;
   a.seqs = seqs_of(pb, cu_seqlens);
+  a.ids = pb.ids ? static_cast<const int*>(seq_idx->data) : nullptr;
+  ids_strides(pb.ids ? seq_idx : nullptr, a.ids_sb, a.ids_st);
   a.B = pb.B;
   a.D = pb.D;
   a.status = d_status;
   if (pb.n_seq == 0) return CCC_OK;
-  const int vec = pb.layout == ccc::kLayoutTimeContiguous ? (bdt_vec_ok(pb, {x, out}) ? 8 : 1)
-                                                          : pick_vec(4, pb, {x, out}, {initial_states, final_states});
+  const int vec = pb.layout == ccc::kLayoutTimeContiguous
+                      ? (bdt_vec_ok(pb, {x, out}) && !pb.ids ? 8 : 1)
+                      : pick_vec(4, pb, {x, out}, {initial_states, final_states});
   const int64_t rows = pb.packed ? pb.D : int64_t(pb.B) * pb.D;
-  const ccc::FwdPlan p = ccc::plan_fwd(pb.layout, vec, a.seqs.Q, pb.D, rows, sms);
+  const ccc::FwdPlan p = ccc::plan_fwd(pb.layout, vec, a.seqs.Q, pb.D, rows, sms, pb.ids);
   a.seg_len = p.seg_len;
   a.n_seg = p.n_seg;
   return ccc::launch_fwd(a, p, activation, stream) == cudaSuccess ? CCC_OK : CCC_ERR_CUDA;
 }
 
 // Shared by the size query and the call itself, so both agree.
-static bool bwd_plan_for(const ccc_tensor* x, const Problem& pb, int vec, ccc::BwdPlan& p) {
+static bool bwd_plan_for(const Problem& pb, int vec, bool ids, ccc::BwdPlan& p) {
   const int sms = device_sm_count();
   if (sms <= 0) return false;
   const int64_t Q = pb.packed ? pb.T : int64_t(pb.B) * pb.T;
   const int64_t rows = pb.packed ? pb.D : int64_t(pb.B) * pb.D;
-  (void)x;
-  p = ccc::plan_bwd(pb.layout, vec, Q, pb.D, rows, sms);
+  p = ccc::plan_bwd(pb.layout, vec, Q, pb.D, rows, sms, ids);
   return true;
 }
 
@@ -440,30 +478,36 @@ size_t ccc_conv1d_bwd_workspace_size(const ccc_tensor* x, int deterministic) {
   pb.layout = layout_of(x);
   if (pb.layout < 0) return 0;
   // The call picks its vector width from the alignment of all its tensors, and
-  // a packed call needs no more than a dense one: cover every width.
+  // a packed call needs no more than a dense one: cover every width, with and
+  // without per-token sequence ids.
   size_t n = 0;
   for (int vec : {8, 4, 1}) {
     ccc::BwdPlan p{};
-    if (!bwd_plan_for(x, pb, vec, p)) return 0;
+    if (!bwd_plan_for(pb, vec, false, p)) return 0;
+    n = std::max(n, bwd_ws_bytes(p, pb, deterministic));
+    if (vec == 8) continue;
+    if (!bwd_plan_for(pb, vec, true, p)) return 0;
     n = std::max(n, bwd_ws_bytes(p, pb, deterministic));
   }
   return (n + 255) / 256 * 256;
 }
 
 ccc_status ccc_conv1d_bwd(const ccc_tensor* x, const ccc_tensor* weight, const ccc_tensor* bias,
-                          const ccc_tensor* cu_seqlens, const ccc_tensor* initial_states,
-                          const ccc_tensor* dout, const ccc_tensor* dfinal_states,
-                          const ccc_tensor* dx, const ccc_tensor* dweight, const ccc_tensor* dbias,
+                          const ccc_tensor* cu_seqlens, const ccc_tensor* seq_idx,
+                          const ccc_tensor* initial_states, const ccc_tensor* dout,
+                          const ccc_tensor* dfinal_states, const ccc_tensor* dx,
+                          const ccc_tensor* dweight, const ccc_tensor* dbias,
                           const ccc_tensor* dinitial_states, int activation, int deterministic,
                           void* workspace, size_t workspace_bytes, int* d_status,
                           cudaStream_t stream) {
   Problem pb;
-  ccc_status st = check_common(x, weight, bias, cu_seqlens, initial_states, activation, pb);
+  ccc_status st = check_common(x, weight, bias, cu_seqlens, seq_idx, initial_states, activation, pb);
   if (st != CCC_OK) return st;
   if (!same_act_shape(dout, pb) || !same_act_shape(dx, pb)) return CCC_ERR_INVALID_ARG;
   if (layout_of(dout) != pb.layout || layout_of(dx) != pb.layout || !self_disjoint(dx))
     return CCC_ERR_UNSUPPORTED;
   if (dfinal_states && !state_ok(dfinal_states, pb.n_seq, pb.D, pb.sw)) return CCC_ERR_INVALID_ARG;
+  if (dfinal_states && pb.ids) return CCC_ERR_UNSUPPORTED;  // no state with seq_idx
   if (!dweight || !well_formed(dweight, 2) || !shape_is(dweight, pb.D, pb.W) ||
       dweight->dtype != weight->dtype || !self_disjoint(dweight))
     return CCC_ERR_INVALID_ARG;
@@ -477,7 +521,7 @@ ccc_status ccc_conv1d_bwd(const ccc_tensor* x, const ccc_tensor* weight, const c
   if (deterministic && bias) return CCC_ERR_NONDETERMINISTIC;
 
   // outputs vs inputs, and outputs vs each other
-  const ccc_tensor* ins[] = {x, weight, bias, cu_seqlens, initial_states, dout, dfinal_states};
+  const ccc_tensor* ins[] = {x, weight, bias, cu_seqlens, seq_idx, initial_states, dout, dfinal_states};
   const ccc_tensor* outs[] = {dx, dweight, dbias, dinitial_states};
   for (const ccc_tensor* o : outs) {
     if (!o) continue;
@@ -491,12 +535,16 @@ ccc_status ccc_conv1d_bwd(const ccc_tensor* x, const ccc_tensor* weight, const c
   const int sms = device_sm_count();
   if (sms <= 0) return CCC_ERR_CUDA;
   const int64_t Q = pb.packed ? pb.T : int64_t(pb.B) * pb.T;
-  const int vec = pb.layout == ccc::kLayoutTimeContiguous
-                      ? bdt_bwd_vec(pb, {x, dout, dx})
-                      : pick_vec(bwd_preferred_vec(Q, pb.D, sms), pb, {x, dout, dx},
-                                 {initial_states, dfinal_states, dinitial_states});
+  int vec = 1;
+  if (pb.ids)  // the general kernels: four channels a thread when aligned, else one
+    vec = pb.layout == ccc::kLayoutTimeContiguous ? 1 : pick_vec(4, pb, {x, dout, dx}, {});
+  else if (pb.layout == ccc::kLayoutTimeContiguous)
+    vec = bdt_bwd_vec(pb, {x, dout, dx});
+  else
+    vec = pick_vec(bwd_preferred_vec(Q, pb.D, sms), pb, {x, dout, dx},
+                   {initial_states, dfinal_states, dinitial_states});
   ccc::BwdPlan p{};
-  if (!bwd_plan_for(x, pb, vec, p)) return CCC_ERR_CUDA;
+  if (!bwd_plan_for(pb, vec, pb.ids, p)) return CCC_ERR_CUDA;
   const size_t need = bwd_ws_bytes(p, pb, deterministic);
   if (!workspace || workspace_bytes < need || !aligned16(workspace)) return CCC_ERR_WORKSPACE;
   {
@@ -521,6 +569,8 @@ ccc_status ccc_conv1d_bwd(const ccc_tensor* x, const ccc_tensor* weight, const c
   a.dinit = dinitial_states ? static_cast<uint16_t*>(dinitial_states->data) : nullptr;
   a.sw = pb.sw;
   a.seqs = seqs_of(pb, cu_seqlens);
+  a.ids = pb.ids ? static_cast<const int*>(seq_idx->data) : nullptr;
+  ids_strides(pb.ids ? seq_idx : nullptr, a.ids_sb, a.ids_st);
   a.B = pb.B;
   a.D = pb.D;
   a.seg_len = p.seg_len;

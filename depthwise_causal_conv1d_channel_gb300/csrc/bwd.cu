@@ -24,7 +24,7 @@
 
 namespace ccc {
 
-template <int V, int ACT, int U, int P>
+template <int V, int ACT, int U, int P, bool IDS = false>
 __device__ __forceinline__ void bwd_walk(const BwdArgs& a, const Seqs& seqs, const Stream& xs,
                                          const Stream& gs, const Stream& ds, int n_base, int d0,
                                          const float (&w)[V][kWidth], const float (&b)[V],
@@ -44,6 +44,12 @@ __device__ __forceinline__ void bwd_walk(const BwdArgs& a, const Seqs& seqs, con
     float gw[kState][V];  // gp[m-3 .. m-1]; entries before a0 are never emitted from,
                           // except before a sequence start, where gp is zero
     float di[kState][V];  // dinit entries of this sequence (only when starts)
+    // With IDS (per-token sequence ids, cuDNN page seq_idx[B, T]): iw = ids of
+    // tokens m-3 .. m-1 (any value before the row start, where x and gp are
+    // zero); token t's id is at id_off + t * ids_st.  A tap joins two tokens
+    // only when their ids are equal.
+    int iw[kState] = {0, 0, 0};
+    const int64_t id_off = IDS ? (int64_t(n_base) + n) * a.ids_sb - lo * a.ids_st : 0;
     {
       float init[kState][V];
       if (a0 - kState < lo && a.init) {
@@ -59,6 +65,7 @@ __device__ __forceinline__ void bwd_walk(const BwdArgs& a, const Seqs& seqs, con
         const int64_t tok = a0 - kState + j;
         if (tok >= lo) {
           VT::unpack(VT::ld(a.x + xs.at(n, tok)), xw[j]);
+          if constexpr (IDS) iw[j] = __ldg(a.ids + id_off + tok * a.ids_st);
         } else {
           const int64_t i = tok - lo + kState;
 #pragma unroll
@@ -69,6 +76,8 @@ __device__ __forceinline__ void bwd_walk(const BwdArgs& a, const Seqs& seqs, con
         for (int c = 0; c < V; ++c) { gw[j][c] = 0.0f; di[j][c] = 0.0f; }
       }
     }
+    // id of token m (IDS), read once per step by grad_at and emit
+    int cid = 0;
 
     // gp at token m from its inputs; accumulate the weight/bias sums when m is
     // one of this thread's tokens; shift the input window.
@@ -76,18 +85,26 @@ __device__ __forceinline__ void bwd_walk(const BwdArgs& a, const Seqs& seqs, con
       float xc[V], gc[V];
       VT::unpack(xr, xc);
       VT::unpack(gr, gc);
+      bool m0 = true, m1 = true, m2 = true;  // window token k feeds token m
+      if constexpr (IDS) {
+        m0 = iw[0] == cid;
+        m1 = iw[1] == cid;
+        m2 = iw[2] == cid;
+      }
 #pragma unroll
       for (int c = 0; c < V; ++c) {
+        const float x0 = m0 ? xw[0][c] : 0.0f, x1 = m1 ? xw[1][c] : 0.0f,
+                    x2 = m2 ? xw[2][c] : 0.0f;
         float p = b[c];
-        p = fmaf(w[c][0], xw[0][c], p);
-        p = fmaf(w[c][1], xw[1][c], p);
-        p = fmaf(w[c][2], xw[2][c], p);
+        p = fmaf(w[c][0], x0, p);
+        p = fmaf(w[c][1], x1, p);
+        p = fmaf(w[c][2], x2, p);
         p = fmaf(w[c][3], xc[c], p);
         gp[c] = act_bwd<ACT>(p, gc[c]);
         if (own) {
-          aw[c][0] = fmaf(gp[c], xw[0][c], aw[c][0]);
-          aw[c][1] = fmaf(gp[c], xw[1][c], aw[c][1]);
-          aw[c][2] = fmaf(gp[c], xw[2][c], aw[c][2]);
+          aw[c][0] = fmaf(gp[c], x0, aw[c][0]);
+          aw[c][1] = fmaf(gp[c], x1, aw[c][1]);
+          aw[c][2] = fmaf(gp[c], x2, aw[c][2]);
           aw[c][3] = fmaf(gp[c], xc[c], aw[c][3]);
           ab[c] += gp[c];
         }
@@ -96,14 +113,23 @@ __device__ __forceinline__ void bwd_walk(const BwdArgs& a, const Seqs& seqs, con
         xw[2][c] = xc[c];
       }
     };
-    // dxe[m - 3] from gp[m] and the window gp[m-3 .. m-1]; shift the window.
+    // dxe[m - 3] from gp[m] and the window gp[m-3 .. m-1]; shift the windows.
     auto emit = [&](const float (&gp)[V], float (&v)[V]) {
+      bool e2 = true, e1 = true, e0 = true;  // token m-3 feeds the tap of token m-2, m-1, m
+      if constexpr (IDS) {
+        e2 = iw[0] == iw[1];
+        e1 = iw[0] == iw[2];
+        e0 = iw[0] == cid;
+        iw[0] = iw[1];
+        iw[1] = iw[2];
+        iw[2] = cid;
+      }
 #pragma unroll
       for (int c = 0; c < V; ++c) {
         float s = w[c][3] * gw[0][c];  // oldest first: gp[m] enters last
-        s = fmaf(w[c][2], gw[1][c], s);
-        s = fmaf(w[c][1], gw[2][c], s);
-        s = fmaf(w[c][0], gp[c], s);
+        s = fmaf(w[c][2], e2 ? gw[1][c] : 0.0f, s);
+        s = fmaf(w[c][1], e1 ? gw[2][c] : 0.0f, s);
+        s = fmaf(w[c][0], e0 ? gp[c] : 0.0f, s);
         v[c] = s;
         gw[0][c] = gw[1][c];
         gw[1][c] = gw[2][c];
@@ -115,6 +141,7 @@ __device__ __forceinline__ void bwd_walk(const BwdArgs& a, const Seqs& seqs, con
     auto slow = [&](int64_t m) {
       float gp[V], v[V];
       if (m < hi) {
+        if constexpr (IDS) cid = __ldg(a.ids + id_off + m * a.ids_st);
         grad_at(VT::ld(a.x + xs.at(n, m)), VT::ld(a.g + gs.at(n, m)), m < e, gp);
       } else {
 #pragma unroll
@@ -179,6 +206,7 @@ __device__ __forceinline__ void bwd_walk(const BwdArgs& a, const Seqs& seqs, con
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         float gp[V], v[V];
+        if constexpr (IDS) cid = __ldg(a.ids + id_off + (m + u) * a.ids_st);
         grad_at(xr[u], gr[u], true, gp);
         emit(gp, v);
         VT::st(a.dx + ds.at(n, m + u - kState), VT::pack(v));
@@ -234,8 +262,8 @@ __device__ __forceinline__ void block_wgrad_out(const BwdArgs& a, int d0, bool a
   }
 }
 
-template <int V, int ACT>
-__global__ void __launch_bounds__(256) bwd_cl_kernel(BwdArgs a) {
+template <int V, int ACT, bool IDS = false>
+__global__ void __launch_bounds__(kGeneralThreads) bwd_cl_kernel(BwdArgs a) {
   __shared__ __align__(16) float wsm[(kWidth + 1) * kMaxBlockChannels];
   pdl_wait();  // inputs may come from the previous kernel in the stream
   if (block_rejects_cu_seqlens(a.seqs, a.status)) return;
@@ -260,7 +288,7 @@ __global__ void __launch_bounds__(256) bwd_cl_kernel(BwdArgs a) {
     const Stream xs{d0, dense ? a.x_sb - a.seqs.T * a.x_st : 0, a.x_st};
     const Stream gs{d0, dense ? a.g_sb - a.seqs.T * a.g_st : 0, a.g_st};
     const Stream ds{d0, dense ? a.dx_sb - a.seqs.T * a.dx_st : 0, a.dx_st};
-    bwd_walk<V, ACT, 4, (V == 8 ? 16 : 0)>(a, a.seqs, xs, gs, ds, 0, d0, w, b, q0, q1, aw, ab);
+    bwd_walk<V, ACT, 4, (V == 8 ? 16 : 0), IDS>(a, a.seqs, xs, gs, ds, 0, d0, w, b, q0, q1, aw, ab);
   }
   pdl_release();
   block_wgrad_out<V>(a, d0, active, aw, ab);
@@ -597,7 +625,7 @@ __global__ void __launch_bounds__(kBwdThreads, V == 8 ? CCC_BWD_MIN_BLOCKS : 4)
 // Time-contiguous layout: one warp per (batch, channel) row, lane l walks
 // tokens [8l + 256i, 8l + 256i + 8).  The row's sums are reduced across the
 // warp in a fixed butterfly order; partial row = batch index.
-template <int ACT>
+template <int ACT, bool IDS = false>
 __global__ void __launch_bounds__(256) bwd_bdt_kernel(BwdArgs a) {
   pdl_wait();  // inputs may come from the previous kernel in the stream
   if (block_rejects_cu_seqlens(a.seqs, a.status)) return;
@@ -618,7 +646,7 @@ __global__ void __launch_bounds__(256) bwd_bdt_kernel(BwdArgs a) {
   float aw[1][kWidth] = {{0.0f, 0.0f, 0.0f, 0.0f}}, ab[1] = {0.0f};
   for (int64_t q0 = int64_t(lane) * 8; q0 < rs.Q; q0 += 256) {
     const int64_t q1 = q0 + 8 < rs.Q ? q0 + 8 : rs.Q;
-    bwd_walk<1, ACT, 4, 0>(a, rs, xs, gs, ds, dense ? bb : 0, d, w, b, q0, q1, aw, ab);
+    bwd_walk<1, ACT, 4, 0, IDS>(a, rs, xs, gs, ds, dense ? bb : 0, d, w, b, q0, q1, aw, ab);
   }
   pdl_release();
   // the sums are of gp2 = 2 gp: halve them (exact)
@@ -1055,9 +1083,42 @@ int bwd_blocks_per_sm(int vec) {
   return 1;
 }
 
+static ContextCache g_bwd_ids_occupancy[2];
+int bwd_ids_blocks_per_sm(int vec) {
+  ContextCache& cache = g_bwd_ids_occupancy[vec == 4 ? 0 : 1];
+  long long v = 0;
+  if (cache.get(&v) && v > 0) return int(v);
+  int n = 0;
+  const cudaError_t err =
+      vec == 4 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                     &n, bwd_cl_kernel<4, kActSilu, true>, kGeneralThreads, bwd_red_bytes<4>(kGeneralThreads))
+               : cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                     &n, bwd_cl_kernel<1, kActSilu, true>, kGeneralThreads, bwd_red_bytes<1>(kGeneralThreads));
+  if (err == cudaSuccess && n > 0) {
+    cache.put(n);
+    return n;
+  }
+  return 1;
+}
+
+// Calls with per-token sequence ids: the general kernels with id masks.
+template <int ACT>
+static cudaError_t launch_bwd_ids(const BwdArgs& a, const BwdPlan& p, bool pdl, cudaStream_t stream) {
+  if (p.kind == kLayoutChannelLast) {
+    dim3 block(p.tx, p.ty), grid(p.gx, p.gy);
+    if (p.vec == 4)
+      return launch_kernel(bwd_cl_kernel<4, ACT, true>, grid, block, bwd_red_bytes<4>(p.tx * p.ty),
+                           stream, pdl, a);
+    return launch_kernel(bwd_cl_kernel<1, ACT, true>, grid, block, bwd_red_bytes<1>(p.tx * p.ty),
+                         stream, pdl, a);
+  }
+  return launch_kernel(bwd_bdt_kernel<ACT, true>, dim3(p.gx), dim3(256), 0, stream, pdl, a);
+}
+
 template <int ACT>
 static cudaError_t launch_bwd_act(const BwdArgs& a, const BwdPlan& p, bool pdl,
                                   cudaStream_t stream) {
+  if (p.ids) return launch_bwd_ids<ACT>(a, p, pdl, stream);
   if (p.kind == kLayoutChannelLast) {
     dim3 block(p.tx, p.ty), grid(p.gx, p.gy);
     const size_t smem = bwd_smem_bytes(p.vec, p.tx * p.ty);

@@ -19,8 +19,10 @@ namespace ccc {
 // One thread: channels [d0, d0 + V), tokens [q, q_end) of one token stream.
 // `n_base` is the state index of the stream's sequence 0.  U token loads are
 // in flight per step; rows P tokens further on are prefetched into L2 (P = 0:
-// none), so the bytes in flight do not depend on registers.
-template <int V, int ACT, int U, int P>
+// none), so the bytes in flight do not depend on registers.  With IDS, every
+// token carries a sequence id (cuDNN page, seq_idx[B, T]): a tap reads a window
+// token of another id as zero.
+template <int V, int ACT, int U, int P, bool IDS = false>
 __device__ __forceinline__ void fwd_walk(const FwdArgs& a, const Seqs& seqs, const Stream& xs,
                                          const Stream& os, int n_base, int d0,
                                          const float (&w)[V][kWidth], const float (&b)[V],
@@ -36,6 +38,10 @@ __device__ __forceinline__ void fwd_walk(const FwdArgs& a, const Seqs& seqs, con
     // win[j] = xe[q - 3 + j]: from x, or from the initial state before the
     // sequence start, or zero.
     float win[kState][V];
+    // ids of the window tokens (IDS; before the row start the window is zero,
+    // so any id serves), and the element offset of token t's id: id_off + t * ids_st
+    int iw[kState] = {0, 0, 0};
+    const int64_t id_off = IDS ? (int64_t(n_base) + n) * a.ids_sb - lo * a.ids_st : 0;
     {
       float init[kState][V];
       if (q - kState < lo && a.init) {
@@ -51,6 +57,7 @@ __device__ __forceinline__ void fwd_walk(const FwdArgs& a, const Seqs& seqs, con
         const int64_t tok = q - kState + j;
         if (tok >= lo) {
           VT::unpack(VT::ld(a.x + xs.at(n, tok)), win[j]);
+          if constexpr (IDS) iw[j] = __ldg(a.ids + id_off + tok * a.ids_st);
         } else {
           const int64_t i = tok - lo + kState;  // 0..2
 #pragma unroll
@@ -63,12 +70,22 @@ __device__ __forceinline__ void fwd_walk(const FwdArgs& a, const Seqs& seqs, con
     auto step = [&](typename VT::Raw raw, int64_t t) {
       float cur[V], y[V];
       VT::unpack(raw, cur);
+      bool m0 = true, m1 = true, m2 = true;  // window token k feeds token t
+      if constexpr (IDS) {
+        const int cid = __ldg(a.ids + id_off + t * a.ids_st);
+        m0 = iw[0] == cid;
+        m1 = iw[1] == cid;
+        m2 = iw[2] == cid;
+        iw[0] = iw[1];
+        iw[1] = iw[2];
+        iw[2] = cid;
+      }
 #pragma unroll
       for (int c = 0; c < V; ++c) {
         float p = b[c];
-        p = fmaf(w[c][0], win[0][c], p);
-        p = fmaf(w[c][1], win[1][c], p);
-        p = fmaf(w[c][2], win[2][c], p);
+        p = fmaf(w[c][0], m0 ? win[0][c] : 0.0f, p);
+        p = fmaf(w[c][1], m1 ? win[1][c] : 0.0f, p);
+        p = fmaf(w[c][2], m2 ? win[2][c] : 0.0f, p);
         p = fmaf(w[c][3], cur[c], p);
         y[c] = act_fwd<ACT>(p);
         win[0][c] = win[1][c];
@@ -108,8 +125,8 @@ __device__ __forceinline__ void fwd_walk(const FwdArgs& a, const Seqs& seqs, con
 // Block (TX, TY): threadIdx.x runs over groups of V channels, threadIdx.y over
 // token ranges of seg_len tokens.  A warp reads 32 * V * 2 contiguous bytes
 // per token.
-template <int V, int ACT>
-__global__ void __launch_bounds__(256) fwd_cl_kernel(FwdArgs a) {
+template <int V, int ACT, bool IDS = false>
+__global__ void __launch_bounds__(kGeneralThreads) fwd_cl_kernel(FwdArgs a) {
   pdl_wait();     // inputs may come from the previous kernel in the stream
   pdl_release();
   __shared__ __align__(16) float ws[(kWidth + 1) * kMaxBlockChannels];
@@ -126,7 +143,7 @@ __global__ void __launch_bounds__(256) fwd_cl_kernel(FwdArgs a) {
   const bool dense = a.seqs.cu == nullptr;
   const Stream xs{d0, dense ? a.x_sb - a.seqs.T * a.x_st : 0, a.x_st};
   const Stream os{d0, dense ? a.o_sb - a.seqs.T * a.o_st : 0, a.o_st};
-  fwd_walk<V, ACT, 4, (V == 8 ? 16 : 0)>(a, a.seqs, xs, os, 0, d0, w, b, q0, q1);
+  fwd_walk<V, ACT, 4, (V == 8 ? 16 : 0), IDS>(a, a.seqs, xs, os, 0, d0, w, b, q0, q1);
 }
 
 // Channel-last x with vectors of V = 4 channels, computed as two channel
@@ -389,7 +406,7 @@ __global__ void __launch_bounds__(256) fwd_bdt8_kernel(FwdArgs a) {
 
 // Time-contiguous x (stride of T is 1).  One warp per (batch, channel) row;
 // lane l walks tokens [8l + 256i, 8l + 256i + 8).
-template <int ACT>
+template <int ACT, bool IDS = false>
 __global__ void __launch_bounds__(256) fwd_bdt_kernel(FwdArgs a) {
   pdl_wait();     // inputs may come from the previous kernel in the stream
   pdl_release();
@@ -410,7 +427,7 @@ __global__ void __launch_bounds__(256) fwd_bdt_kernel(FwdArgs a) {
   const Stream os{bb * a.o_sb + d * a.o_sd, 0, 1};
   for (int64_t q0 = int64_t(lane) * 8; q0 < rs.Q; q0 += 256) {
     const int64_t q1 = q0 + 8 < rs.Q ? q0 + 8 : rs.Q;
-    fwd_walk<1, ACT, 4, 0>(a, rs, xs, os, dense ? bb : 0, d, w, b, q0, q1);
+    fwd_walk<1, ACT, 4, 0, IDS>(a, rs, xs, os, dense ? bb : 0, d, w, b, q0, q1);
   }
 }
 
@@ -456,8 +473,38 @@ int fwd_blocks_per_sm(int vec) {
   return 1;
 }
 
+static ContextCache g_fwd_ids_occupancy[2];
+int fwd_ids_blocks_per_sm(int vec) {
+  ContextCache& cache = g_fwd_ids_occupancy[vec == 4 ? 0 : 1];
+  long long v = 0;
+  if (cache.get(&v) && v > 0) return int(v);
+  int n = 0;
+  const cudaError_t err =
+      vec == 4 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fwd_cl_kernel<4, kActSilu, true>,
+                                                               kGeneralThreads, 0)
+               : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fwd_cl_kernel<1, kActSilu, true>,
+                                                               kGeneralThreads, 0);
+  if (err == cudaSuccess && n > 0) {
+    cache.put(n);
+    return n;
+  }
+  return 1;
+}
+
+// Calls with per-token sequence ids: the general kernels with id masks.
+template <int ACT>
+static cudaError_t launch_fwd_ids(const FwdArgs& a, const FwdPlan& p, cudaStream_t stream) {
+  if (p.kind == kLayoutChannelLast) {
+    dim3 block(p.tx, p.ty), grid(p.gx, p.gy);
+    if (p.vec == 4) return launch_kernel(fwd_cl_kernel<4, ACT, true>, grid, block, 0, stream, true, a);
+    return launch_kernel(fwd_cl_kernel<1, ACT, true>, grid, block, 0, stream, true, a);
+  }
+  return launch_kernel(fwd_bdt_kernel<ACT, true>, dim3(p.gx), dim3(256), 0, stream, true, a);
+}
+
 template <int ACT>
 static cudaError_t launch_fwd_act(const FwdArgs& a, const FwdPlan& p, cudaStream_t stream) {
+  if (p.ids) return launch_fwd_ids<ACT>(a, p, stream);
   if (p.kind == kLayoutChannelLast) {
     dim3 block(p.tx, p.ty), grid(p.gx, p.gy);
     if (p.vec == 4) {

@@ -68,6 +68,8 @@ struct FwdArgs {
   uint16_t* fin;         // [S, D, sw] contiguous or nullptr
   int sw;                // state entries per channel: W - 1
   Seqs seqs;
+  const int* ids;        // per-token sequence ids [B, T] (dense only) or nullptr
+  int64_t ids_sb, ids_st;
   int B, D;
   int64_t seg_len, n_seg;  // channel-last: tokens per thread range, number of ranges
   int* status;
@@ -95,6 +97,8 @@ struct BwdArgs {
   uint16_t* dinit;        // [S, D, sw] or nullptr
   int sw;                 // state entries per channel: W - 1
   Seqs seqs;
+  const int* ids;         // per-token sequence ids [B, T] (dense only) or nullptr
+  int64_t ids_sb, ids_st;
   int B, D;
   int64_t seg_len, n_seg;
   float* ws;              // FP32 weight/bias-gradient partial sums, [R, D, 5]: block row r writes ws[r]
@@ -105,6 +109,7 @@ struct BwdArgs {
 // Launch shape of one call, chosen on the host from the sizes and the SM count.
 struct FwdPlan {
   int kind;      // Layout
+  int ids;       // per-token sequence ids: the general kernels with id masks
   int vec;       // channels per thread (channel-last): 8 or 1
   int tx, ty;    // block shape (channel-last)
   unsigned gx, gy;
@@ -126,14 +131,21 @@ struct UpdArgs {
 };
 
 
-FwdPlan plan_fwd(int kind, int vec_ok, int64_t Q, int D, int64_t rows, int sm_count);
-BwdPlan plan_bwd(int kind, int vec_ok, int64_t Q, int D, int64_t rows, int sm_count);
+FwdPlan plan_fwd(int kind, int vec_ok, int64_t Q, int D, int64_t rows, int sm_count,
+                 bool ids = false);
+BwdPlan plan_bwd(int kind, int vec_ok, int64_t Q, int D, int64_t rows, int sm_count,
+                 bool ids = false);
 // Rows of FP32 partial sums the backward writes.
 int64_t bwd_partial_rows(const BwdPlan& p, int B, bool packed);
 
 // Resident blocks per SM of the channel-last kernels (SiLU instance), cached.
 int fwd_blocks_per_sm(int vec);
 int bwd_blocks_per_sm(int vec);
+// The same for the general channel-last kernels with id masks (vec 4 or 1).
+int fwd_ids_blocks_per_sm(int vec);
+int bwd_ids_blocks_per_sm(int vec);
+// Threads per block of the general channel-last kernels.
+constexpr int kGeneralThreads = 256;
 // Threads per block of the channel-last backward kernel for this vector width.
 int bwd_block_threads(int vec);
 

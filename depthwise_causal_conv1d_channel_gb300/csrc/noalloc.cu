@@ -65,8 +65,8 @@ ccc_status ccc_conv1d_bwd_noalloc(const ccc_tensor* x, const ccc_tensor* weight,
   void* scratch = nullptr;
   const ccc_status st = scratch_address(&scratch);
   if (st != CCC_OK) return st;
-  return ccc_conv1d_bwd(x, weight, bias, cu_seqlens, initial_states, dout, dfinal_states, dx,
-                        dweight, dbias, dinitial_states, activation, deterministic, scratch,
+  return ccc_conv1d_bwd(x, weight, bias, cu_seqlens, nullptr, initial_states, dout, dfinal_states,
+                        dx, dweight, dbias, dinitial_states, activation, deterministic, scratch,
                         kScratchBytes, d_status, stream);
 }
 

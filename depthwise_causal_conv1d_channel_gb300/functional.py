@@ -3,9 +3,10 @@
 The argument lists follow the cuDNN frontend "Causal Conv1d" page (the
 commonly consumed causal-conv1d interface): x [B, D, T] -- or the
 transpose(1, 2) view of [B, T, D] storage, read in place --, weight [D, 4],
-optional bias [D], the reserved seq_idx keyword (only None), optional packed
-cu_seqlens [N + 1], optional initial_states and returned final_states of width
-W - 1 = 3, and a SiLU activation.  Every step runs in the CUDA library through
+optional bias [D], optional per-token sequence ids seq_idx [B, T], optional
+packed cu_seqlens [N + 1] (mutually exclusive with seq_idx), optional
+initial_states and returned final_states of width W - 1 = 3, and a SiLU
+activation.  Every step runs in the CUDA library through
 the C ABI; this module allocates outputs, picks the determinism mode and maps
 status codes to Python exceptions.
 """
@@ -101,8 +102,8 @@ def _deterministic_mode(has_bias: bool, deterministic: Optional[bool]) -> bool:
 
 class _CausalConv1dFn(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, x, weight, bias, cu_seqlens, initial_states, final_states_out, want_final,
-                act, deterministic):
+    def forward(ctx, x, weight, bias, cu_seqlens, seq_idx, initial_states, final_states_out,
+                want_final, act, deterministic):
         out = torch.empty_like(x)  # same strides as x: channel-last in, channel-last out
         S = x.shape[0] if cu_seqlens is None else cu_seqlens.numel() - 1
         final = None
@@ -110,10 +111,11 @@ class _CausalConv1dFn(torch.autograd.Function):
             final = final_states_out if final_states_out is not None else torch.empty(
                 (S, x.shape[1], weight.shape[1] - 1), dtype=x.dtype, device=x.device)
         st = _abi.ccc_conv1d_fwd(x, weight, bias, cu_seqlens, initial_states, out, final, act,
-                                 status_word(x.device), torch.cuda.current_stream(x.device))
+                                 status_word(x.device), torch.cuda.current_stream(x.device),
+                                 seq_idx=seq_idx)
         _raise(st, "causal_conv1d")
         _debug_check(x.device)
-        ctx.save_for_backward(x, weight, bias, cu_seqlens, initial_states)
+        ctx.save_for_backward(x, weight, bias, cu_seqlens, seq_idx, initial_states)
         ctx.act = act
         ctx.deterministic = deterministic
         if final_states_out is not None:
@@ -122,7 +124,7 @@ class _CausalConv1dFn(torch.autograd.Function):
 
     @staticmethod
     def backward(ctx, dout, dfinal):
-        x, weight, bias, cu_seqlens, initial_states = ctx.saved_tensors
+        x, weight, bias, cu_seqlens, seq_idx, initial_states = ctx.saved_tensors
         det = _deterministic_mode(bias is not None, ctx.deterministic)
         if dout is None:
             dout = torch.zeros_like(x)
@@ -133,16 +135,16 @@ class _CausalConv1dFn(torch.autograd.Function):
         dweight = torch.empty_like(weight, memory_format=torch.contiguous_format)
         dbias = torch.empty_like(bias) if bias is not None else None
         dinit = None
-        if initial_states is not None and ctx.needs_input_grad[4]:
+        if initial_states is not None and ctx.needs_input_grad[5]:
             dinit = torch.empty_like(initial_states)
         ws = torch.empty(_abi.ccc_conv1d_bwd_workspace_size(x, det), dtype=torch.uint8,
                          device=x.device)
         st = _abi.ccc_conv1d_bwd(x, weight, bias, cu_seqlens, initial_states, dout, dfinal, dx,
                                  dweight, dbias, dinit, ctx.act, det, ws, status_word(x.device),
-                                 torch.cuda.current_stream(x.device))
+                                 torch.cuda.current_stream(x.device), seq_idx=seq_idx)
         _raise(st, "causal_conv1d backward")
         _debug_check(x.device)
-        return dx, dweight, dbias, None, dinit, None, None, None, None
+        return dx, dweight, dbias, None, None, dinit, None, None, None, None
 
 
 def causal_conv1d(x: torch.Tensor, weight: torch.Tensor, bias: Optional[torch.Tensor] = None,
@@ -157,18 +159,28 @@ def causal_conv1d(x: torch.Tensor, weight: torch.Tensor, bias: Optional[torch.Te
     xe is x preceded by the W - 1 initial-state entries (zeros when none);
     initial_states and final_states are [B or N, D, W - 1].
 
+    ``seq_idx`` [B, T] int32 gives every token a sequence id: tokens of a row
+    with the same id form one sequence, and a tap reads a token of another id as
+    zero.  It excludes cu_seqlens (ValueError) and has no initial or final
+    state (NotImplementedError).
+
     Returns ``out`` (same shape and strides as x) or ``(out, final_states)`` when
     ``return_final_states`` is set or ``final_states_out`` is given.  Differentiable
     in x, weight, bias and initial_states.  ``deterministic`` (default: follow
     ``torch.use_deterministic_algorithms``) selects the reproducible dweight route.
     """
-    if seq_idx is not None:
-        raise NotImplementedError("seq_idx is reserved; only None is accepted")
     if cu_seqlens is not None and cu_seqlens.dtype != torch.int32:
         raise ValueError("cu_seqlens must be int32")
+    if seq_idx is not None:
+        if seq_idx.dtype != torch.int32:
+            raise ValueError("seq_idx must be int32")
+        if cu_seqlens is not None:
+            raise ValueError("seq_idx and cu_seqlens are mutually exclusive")
+        if initial_states is not None or return_final_states or final_states_out is not None:
+            raise NotImplementedError("seq_idx defines no initial or final state")
     act = _activation_code(activation)
     want_final = bool(return_final_states) or final_states_out is not None
-    out, final = _CausalConv1dFn.apply(x, weight, bias, cu_seqlens, initial_states,
+    out, final = _CausalConv1dFn.apply(x, weight, bias, cu_seqlens, seq_idx, initial_states,
                                        final_states_out, want_final, act, deterministic)
     return (out, final) if want_final else out
 

@@ -46,7 +46,7 @@
 extern "C" {
 #endif
 
-#define CCC_CONV1D_ABI_VERSION 1
+#define CCC_CONV1D_ABI_VERSION 2
 #define CCC_CONV1D_WIDTH 4
 
 typedef enum {
@@ -95,6 +95,14 @@ typedef struct {
  *                   N sequences back to back along T; no tap reads across a
  *                   boundary.  Validated on the device (see above): offsets
  *                   start at 0, end at T, and strictly increase.
+ *   seq_idx         [B, T] int32 or NULL, any non-negative strides: per-token
+ *                   sequence ids (the page's seq_idx[B, T] keyword).  Tokens of
+ *                   a row that carry the same id form one sequence: a tap of
+ *                   token t reads a token of another id as zero.  The page makes
+ *                   it mutually exclusive with cu_seqlens (both given:
+ *                   CCC_ERR_INVALID_ARG); the page defines no state for it, so
+ *                   initial_states or final_states with seq_idx return
+ *                   CCC_ERR_UNSUPPORTED.
  *   initial_states  [S, D, W-1] BF16 contiguous or NULL; S = B (dense) or N (packed).
  *   out             [B, D, T] BF16, same layout kind as x (its own strides).
  *   final_states    [S, D, W-1] BF16 contiguous or NULL: xe[T-W+1 .. T-1] of
@@ -108,9 +116,10 @@ typedef struct {
  * T == 0 is allowed (final_states then equals initial_states, or zeros).
  */
 ccc_status ccc_conv1d_fwd(const ccc_tensor *x, const ccc_tensor *weight, const ccc_tensor *bias,
-                          const ccc_tensor *cu_seqlens, const ccc_tensor *initial_states,
-                          const ccc_tensor *out, const ccc_tensor *final_states, int activation,
-                          int *d_status, cudaStream_t stream);
+                          const ccc_tensor *cu_seqlens, const ccc_tensor *seq_idx,
+                          const ccc_tensor *initial_states, const ccc_tensor *out,
+                          const ccc_tensor *final_states, int activation, int *d_status,
+                          cudaStream_t stream);
 
 /*
  * Workspace bytes that ccc_conv1d_bwd needs for this x (shape and layout) and
@@ -125,7 +134,8 @@ size_t ccc_conv1d_bwd_workspace_size(const ccc_tensor *x, int deterministic);
  * route; the paragraph on determinism).  The pre-activation is recomputed
  * from x; nothing from the forward is needed.
  *
- *   x, weight, bias, cu_seqlens, initial_states   as in ccc_conv1d_fwd.
+ *   x, weight, bias, cu_seqlens, seq_idx, initial_states   as in ccc_conv1d_fwd
+ *                   (with seq_idx, dfinal_states and dinitial_states must be NULL).
  *   dout            [B, D, T] BF16, same layout kind as x: dL/dout.
  *   dfinal_states   [S, D, W-1] BF16 contiguous or NULL (NULL = zero gradient).
  *   dx              [B, D, T] BF16, same layout kind as x.
@@ -146,9 +156,10 @@ size_t ccc_conv1d_bwd_workspace_size(const ccc_tensor *x, int deterministic);
  * Outputs must not overlap each other or any input (CCC_ERR_ALIAS).
  */
 ccc_status ccc_conv1d_bwd(const ccc_tensor *x, const ccc_tensor *weight, const ccc_tensor *bias,
-                          const ccc_tensor *cu_seqlens, const ccc_tensor *initial_states,
-                          const ccc_tensor *dout, const ccc_tensor *dfinal_states,
-                          const ccc_tensor *dx, const ccc_tensor *dweight, const ccc_tensor *dbias,
+                          const ccc_tensor *cu_seqlens, const ccc_tensor *seq_idx,
+                          const ccc_tensor *initial_states, const ccc_tensor *dout,
+                          const ccc_tensor *dfinal_states, const ccc_tensor *dx,
+                          const ccc_tensor *dweight, const ccc_tensor *dbias,
                           const ccc_tensor *dinitial_states, int activation, int deterministic,
                           void *workspace, size_t workspace_bytes, int *d_status,
                           cudaStream_t stream);
@@ -161,7 +172,8 @@ ccc_status ccc_conv1d_bwd(const ccc_tensor *x, const ccc_tensor *weight, const c
  * over only the operation's own tensors): they cannot provide the workspace
  * ccc_conv1d_bwd asks for.
  *
- * Same arguments and results as ccc_conv1d_bwd, minus the workspace: the FP32
+ * Same arguments and results as ccc_conv1d_bwd without seq_idx (it takes no
+ * per-token sequence ids), minus the workspace: the FP32
  * sums live in a scratch array of CCC_CONV1D_NOALLOC_SCRATCH_BYTES built into
  * the library, present in device memory on every GPU that loads it, until the
  * library is unloaded.  Nothing is allocated (no cudaMalloc, no cudaFree, no

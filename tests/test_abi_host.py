@@ -85,15 +85,16 @@ def cl(off, B, D, Tn):
 MB = 1 << 20
 
 
-def fwd(x, w, b=None, cu=None, init=None, out=None, fin=None, act=1):
+def fwd(x, w, b=None, cu=None, init=None, out=None, fin=None, act=1, ids=None):
     r = lambda d: None if d is None else ctypes.byref(d)
-    return _abi.lib.ccc_conv1d_fwd(r(x), r(w), r(b), r(cu), r(init), r(out), r(fin), act, None, None)
+    return _abi.lib.ccc_conv1d_fwd(r(x), r(w), r(b), r(cu), r(ids), r(init), r(out), r(fin), act,
+                                   None, None)
 
 
-def bwd(x, w, b, cu, init, g, gf, dx, dw, db, dinit, det=0, act=1, ws=None, ws_bytes=0):
+def bwd(x, w, b, cu, init, g, gf, dx, dw, db, dinit, det=0, act=1, ws=None, ws_bytes=0, ids=None):
     r = lambda d: None if d is None else ctypes.byref(d)
-    return _abi.lib.ccc_conv1d_bwd(r(x), r(w), r(b), r(cu), r(init), r(g), r(gf), r(dx), r(dw),
-                                   r(db), r(dinit), act, det, ws, ws_bytes, None, None)
+    return _abi.lib.ccc_conv1d_bwd(r(x), r(w), r(b), r(cu), r(ids), r(init), r(g), r(gf), r(dx),
+                                   r(dw), r(db), r(dinit), act, det, ws, ws_bytes, None, None)
 
 
 B_, D_, T_ = 2, 16, 32
@@ -183,6 +184,33 @@ def test_bwd_rejects_bad_arguments_on_host():
                det=2) == _abi.CCC_ERR_INVALID_ARG
 
 
+def test_seq_idx_host_checks():
+    """seq_idx [B, T] int32: mutually exclusive with cu_seqlens (cuDNN page),
+    no state with it, outputs may not overlap it."""
+    g = good()
+    ids = T(80 * MB, I32, (B_, T_))
+    dout = cl(50 * MB, B_, D_, T_)
+    dx = cl(60 * MB, B_, D_, T_)
+    dw = T(70 * MB, BF16, (D_, 4))
+    db = T(71 * MB, BF16, (D_,))
+    # wrong shape or dtype
+    assert fwd(g["x"], g["w"], g["b"], out=g["out"], ids=T(80 * MB, I32, (B_, T_ + 1))) == _abi.CCC_ERR_INVALID_ARG
+    assert fwd(g["x"], g["w"], g["b"], out=g["out"], ids=T(80 * MB, BF16, (B_, T_))) == _abi.CCC_ERR_INVALID_ARG
+    # with cu_seqlens
+    x1, out1 = cl(0, 1, D_, T_), cl(20 * MB, 1, D_, T_)
+    assert fwd(x1, g["w"], g["b"], cu=T(40 * MB, I32, (3,)), out=out1,
+               ids=T(80 * MB, I32, (1, T_))) == _abi.CCC_ERR_INVALID_ARG
+    # no state with seq_idx
+    assert fwd(g["x"], g["w"], g["b"], init=g["init"], out=g["out"], ids=ids) == _abi.CCC_ERR_UNSUPPORTED
+    assert fwd(g["x"], g["w"], g["b"], out=g["out"], fin=g["fin"], ids=ids) == _abi.CCC_ERR_UNSUPPORTED
+    assert bwd(g["x"], g["w"], g["b"], None, None, dout, T(90 * MB, BF16, (B_, D_, 3)), dx, dw, db,
+               None, ids=ids) == _abi.CCC_ERR_UNSUPPORTED
+    # outputs overlapping the ids
+    assert fwd(g["x"], g["w"], g["b"], out=cl(80 * MB, B_, D_, T_), ids=ids) == _abi.CCC_ERR_ALIAS
+    assert bwd(g["x"], g["w"], g["b"], None, None, dout, None, cl(80 * MB, B_, D_, T_), dw, db,
+               None, ids=ids) == _abi.CCC_ERR_ALIAS
+
+
 def test_update_rejects_bad_arguments_on_host():
     r = lambda d: None if d is None else ctypes.byref(d)
     x = T(0, BF16, (4, D_))
@@ -224,12 +252,19 @@ def test_multi_token_update_host_checks():
     assert upd(cl3(0, 0), st, w, b, cl3(4 * MB, 0)) == _abi.CCC_OK
 
 
-def test_python_api_rejects_seq_idx_and_bad_activation():
+def test_python_api_seq_idx_rules_and_bad_activation():
     import torch
 
     x = torch.zeros(1, 8, 4, dtype=torch.bfloat16)
     w = torch.zeros(8, 4, dtype=torch.bfloat16)
+    ids = torch.zeros(1, 4, dtype=torch.int32)
+    with pytest.raises(ValueError):       # int32 only
+        ccc.causal_conv1d(x, w, seq_idx=ids.long())
+    with pytest.raises(ValueError):       # mutually exclusive with cu_seqlens
+        ccc.causal_conv1d(x, w, seq_idx=ids, cu_seqlens=torch.tensor([0, 4], dtype=torch.int32))
+    with pytest.raises(NotImplementedError):  # no state with seq_idx
+        ccc.causal_conv1d(x, w, seq_idx=ids, initial_states=torch.zeros(1, 8, 3, dtype=torch.bfloat16))
     with pytest.raises(NotImplementedError):
-        ccc.causal_conv1d(x, w, seq_idx=torch.zeros(1, 4, dtype=torch.int32))
+        ccc.causal_conv1d(x, w, seq_idx=ids, return_final_states=True)
     with pytest.raises(ValueError):
         ccc.causal_conv1d(x, w, activation="gelu")

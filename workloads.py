@@ -213,3 +213,27 @@ def bits(t: Optional[torch.Tensor]):
 def from_bits(a: np.ndarray) -> torch.Tensor:
     """numpy uint16 bit patterns -> BF16 tensor."""
     return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(BF16)
+
+
+def seq_ids(B: int, T: int, seed: int, kind: str = "runs", max_run: int = 64,
+            n_ids: int = 3) -> torch.Tensor:
+    """Per-token sequence ids [B, T] int32 (the seq_idx keyword of the cuDNN page).
+
+    ``runs``: every row is cut into consecutive runs of U[1, max_run] tokens,
+    numbered upward from a per-row offset (the usual packed-in-a-row layout);
+    ``random``: every token draws an id from U{0, .., n_ids - 1}, so equal ids
+    need not be adjacent."""
+    gen = torch.Generator().manual_seed(seed)
+    if kind == "random":
+        return torch.randint(0, n_ids, (B, T), generator=gen, dtype=torch.int32)
+    if kind != "runs":
+        raise ValueError(f"unknown id layout {kind!r}")
+    ids = torch.empty(B, T, dtype=torch.int32)
+    for b in range(B):
+        t, cur = 0, int(torch.randint(-100, 100, (1,), generator=gen))
+        while t < T:
+            n = int(torch.randint(1, max_run + 1, (1,), generator=gen))
+            ids[b, t:t + n] = cur
+            t += n
+            cur += 1
+    return ids
