@@ -71,6 +71,8 @@ def _load():
         lib.oracle_update.restype = I
         lib.oracle_check_cu_seqlens.argtypes = [P, I, I64]
         lib.oracle_check_cu_seqlens.restype = I
+        lib.oracle_fullconv_fwd.argtypes = [P, I64, I64, I64, P, I64, I, I, P, P, P]
+        lib.oracle_fullconv_fwd.restype = I
         lib.oracle_bf16_encode.argtypes = [ctypes.c_double]
         lib.oracle_bf16_encode.restype = ctypes.c_uint16
         lib.oracle_bf16_encode_array.argtypes = [P, I64, P]
@@ -265,3 +267,34 @@ def update(x, conv_state, weight, bias=None, activation="silu"):
     w, _ = _weight_f64(weight)
     r = update_f64(bf16_decode(x), bf16_decode(conv_state), w, bf16_decode(bias), activation)
     return dict(out=bf16_encode(r["out"]), out64=r["out"], state=bf16_encode(r["state"]))
+
+
+# ---- full-channel dilated causal conv1d (POPCORNBENCH conv1d page) -----------
+
+def fullconv_f64(x, weight, bias=None, dilation=1):
+    """x [B, Cin, T], weight [Cout, Cin, K], bias [Cout] or None (any real values).
+    Returns dict(out [B, Cout, T], abs_sum [B, Cout, T]) in float64."""
+    lib = _load()
+    x = _f64(x)
+    w = _f64(weight)
+    B, Cin, T = x.shape
+    Cout, Cin_w, K = w.shape
+    if Cin_w != Cin:
+        raise ValueError("weight must be [Cout, Cin, K] with the Cin of x")
+    out = np.empty((B, Cout, T))
+    abs_sum = np.empty((B, Cout, T))
+    rc = lib.oracle_fullconv_fwd(_ptr(x), B, Cin, T, _ptr(w), Cout, int(K), int(dilation),
+                                 _ptr(_f64(bias)), _ptr(out), _ptr(abs_sum))
+    if rc != 0:
+        raise ValueError(f"kernel size and dilation must be >= 1 (oracle status {rc})")
+    return dict(out=out, abs_sum=abs_sum)
+
+
+def fullconv(x, weight, bias=None, dilation=1):
+    """BF16 inputs (uint16 bit patterns; weight and bias may be float32 instead).
+    Returns dict(out: BF16 bits, out64, abs_sum: float64)."""
+    w = bf16_decode(weight) if np.asarray(weight).dtype == np.uint16 else _f64(weight)
+    b = None if bias is None else (bf16_decode(bias) if np.asarray(bias).dtype == np.uint16
+                                   else _f64(bias))
+    r = fullconv_f64(bf16_decode(x), w, b, dilation)
+    return dict(out=bf16_encode(r["out"]), out64=r["out"], abs_sum=r["abs_sum"])

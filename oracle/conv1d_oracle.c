@@ -338,3 +338,49 @@ int oracle_update(const double *x, int64_t B, int64_t D, const double *w, int W,
     }
     return ORC_OK;
 }
+
+/* ---- full-channel dilated causal conv1d ---------------------------------- */
+
+/*
+ * POPCORNBENCH conv1d page (the reasoning section and both listings): a Conv1d
+ * over all input channels with dilation, made causal by left padding
+ * P = (K-1)*dil; tap k reads input position t + k*dil - P, and positions before
+ * 0 read zero:
+ *
+ *   out[b,oc,t] = bias[oc] + sum_{ic<Cin} sum_{k<K} w[oc,ic,k] * x[b,ic,t + k*dil - P]
+ *
+ * x [B][Cin][T], w [Cout][Cin][K], bias [Cout] or NULL, out [B][Cout][T];
+ * abs_sum (or NULL) [B][Cout][T] receives |bias| + sum |w * x| over the same
+ * terms (the scale of the rounding error of any summation order).  The sum runs
+ * over ic, then k, in ascending order, in one double accumulator.
+ */
+int oracle_fullconv_fwd(const double *x, int64_t B, int64_t Cin, int64_t T, const double *w,
+                        int64_t Cout, int K, int dil, const double *bias, double *out,
+                        double *abs_sum)
+{
+    if (K < 1 || dil < 1)
+        return ORC_BAD_WIDTH;
+    const int64_t P = (int64_t)(K - 1) * dil;
+    for (int64_t b = 0; b < B; ++b) {
+        for (int64_t oc = 0; oc < Cout; ++oc) {
+            for (int64_t t = 0; t < T; ++t) {
+                double s = bias ? bias[oc] : 0.0;
+                double a = bias ? fabs(bias[oc]) : 0.0;
+                for (int64_t ic = 0; ic < Cin; ++ic) {
+                    for (int k = 0; k < K; ++k) {
+                        int64_t pos = t + (int64_t)k * dil - P;
+                        if (pos < 0)
+                            continue; /* the causal padding */
+                        double term = w[(oc * Cin + ic) * K + k] * x[(b * Cin + ic) * T + pos];
+                        s += term;
+                        a += fabs(term);
+                    }
+                }
+                out[(b * Cout + oc) * T + t] = s;
+                if (abs_sum)
+                    abs_sum[(b * Cout + oc) * T + t] = a;
+            }
+        }
+    }
+    return ORC_OK;
+}

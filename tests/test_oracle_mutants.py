@@ -2,8 +2,9 @@
 
 Each case plants one mistake in a copy of conv1d_oracle.c (a wrong tap offset,
 reversed state order, a sign flip in the SiLU derivative, transposed taps in
-the input gradient, ...), compiles it, and runs the pin suite against it in a
-subprocess: the suite has to fail.  Every planted mistake keeps all memory
+the input gradient, a transposed full-channel weight, ...), compiles it, and
+runs the pin suites (depthwise and full-channel) against it in a subprocess:
+the suites have to fail.  Every planted mistake keeps all memory
 accesses in bounds.
 """
 
@@ -47,6 +48,12 @@ MUTANTS = {
     "seq_idx_dx_unmasked": ("if (t >= 0 && t < len && same_seq(ids, j, t))", "if (t >= 0 && t < len)"),
     "seq_idx_dw_unmasked": ("if (!same_seq(ids, t - (W - 1) + k, t))\n                        term = 0.0;",
                             "if (0)\n                        term = 0.0;"),
+    "fullconv_padding_sign": ("int64_t pos = t + (int64_t)k * dil - P;", "int64_t pos = t - (int64_t)k * dil;"),
+    "fullconv_no_dilation": ("int64_t pos = t + (int64_t)k * dil - P;", "int64_t pos = t + (int64_t)k - P;"),
+    "fullconv_weight_transposed": ("double term = w[(oc * Cin + ic) * K + k] * x[(b * Cin + ic) * T + pos];",
+                                   "double term = w[(ic * Cout + oc) * K + k] * x[(b * Cin + ic) * T + pos];"),
+    "fullconv_bias_dropped": ("double s = bias ? bias[oc] : 0.0;", "double s = 0.0;"),
+    "fullconv_abs_without_bias": ("double a = bias ? fabs(bias[oc]) : 0.0;", "double a = 0.0;"),
     "width_state_offset": ("const double *is = init ? init + ((int64_t)n * D + d) * S : NULL;\n            const int32_t *ids",
                            "const double *is = init ? init + ((int64_t)n * D + d) * 3 : NULL;\n            const int32_t *ids"),
 }
@@ -66,6 +73,7 @@ def test_pins_reject_planted_mistake(name):
                                msrc, "-o", lib, "-lm"])
         env = dict(os.environ, CCC_ORACLE_LIB=lib)
         r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
-                            os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                            os.path.join(ROOT, "tests", "test_oracle_pins.py"),
+                            os.path.join(ROOT, "tests", "test_oracle_pins_fullconv.py")],
                            cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
         assert r.returncode != 0, f"pins did not catch mutant {name}:\n{r.stdout[-2000:]}"
