@@ -26,6 +26,7 @@ CCC_ERR_WORKSPACE = 5
 CCC_ERR_CUDA = 6
 CCC_ERR_BAD_CU_SEQLENS = 7
 CCC_ERR_SCRATCH_LIMIT = 8
+CCC_ERR_DEVICE_TIMEOUT = 9
 
 CCC_BF16, CCC_F32, CCC_I32 = 0, 1, 2
 CCC_ACT_NONE, CCC_ACT_SILU = 0, 1
@@ -38,6 +39,8 @@ EXPORTED = (
     "ccc_conv1d_bwd",
     "ccc_conv1d_bwd_noalloc",
     "ccc_conv1d_update",
+    "ccc_fullconv1d_pack_weight",
+    "ccc_fullconv1d_fwd",
     "ccc_read_status",
     "ccc_status_string",
     "ccc_conv1d_abi_version",
@@ -84,6 +87,10 @@ def _load():
     lib.ccc_conv1d_bwd_noalloc.restype = I
     lib.ccc_conv1d_update.argtypes = [P, P, P, P, P, I, V]
     lib.ccc_conv1d_update.restype = I
+    lib.ccc_fullconv1d_pack_weight.argtypes = [P, P, V]
+    lib.ccc_fullconv1d_pack_weight.restype = I
+    lib.ccc_fullconv1d_fwd.argtypes = [P, P, P, I, P, V, V]
+    lib.ccc_fullconv1d_fwd.restype = I
     lib.ccc_read_status.argtypes = [V, V]
     lib.ccc_read_status.restype = I
     lib.ccc_status_string.argtypes = [I]
@@ -184,6 +191,16 @@ def ccc_conv1d_bwd_noalloc(x, weight, bias, cu_seqlens, initial_states, dout, df
 def ccc_conv1d_update(x, conv_state, weight, bias, out, activation: int, stream=None) -> int:
     ds = [desc(t) for t in (x, conv_state, weight, bias, out)]
     return lib.ccc_conv1d_update(*[_ref(d) for d in ds], int(activation), _stream(stream))
+
+
+def ccc_fullconv1d_pack_weight(weight, packed, stream=None) -> int:
+    return lib.ccc_fullconv1d_pack_weight(_ref(desc(weight)), _ref(desc(packed)), _stream(stream))
+
+
+def ccc_fullconv1d_fwd(x, packed_weight, bias, dilation: int, out, status=None, stream=None) -> int:
+    ds = [desc(t) for t in (x, packed_weight, bias)]
+    return lib.ccc_fullconv1d_fwd(*[_ref(d) for d in ds], int(dilation), _ref(desc(out)),
+                                  _status_ptr(status), _stream(stream))
 
 
 def ccc_read_status(status, stream=None) -> int:

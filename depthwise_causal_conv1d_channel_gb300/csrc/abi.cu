@@ -400,6 +400,7 @@ const char* ccc_status_string(int status) {
     case CCC_ERR_CUDA: return "CUDA error";
     case CCC_ERR_BAD_CU_SEQLENS: return "malformed cu_seqlens";
     case CCC_ERR_SCRATCH_LIMIT: return "problem exceeds the built-in scratch of ccc_conv1d_bwd_noalloc";
+    case CCC_ERR_DEVICE_TIMEOUT: return "a bounded wait inside a kernel ran out";
     default: return "unknown status";
   }
 }
@@ -663,6 +664,86 @@ ccc_status ccc_read_status(int* d_status, cudaStream_t stream) {
   if (cudaMemcpy(&h, d_status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return CCC_ERR_CUDA;
   if (h != 0 && cudaMemset(d_status, 0, sizeof(int)) != cudaSuccess) return CCC_ERR_CUDA;
   return static_cast<ccc_status>(h);
+}
+
+// ---- full-channel dilated causal conv1d -------------------------------------------
+
+ccc_status ccc_fullconv1d_pack_weight(const ccc_tensor* weight, const ccc_tensor* packed,
+                                      cudaStream_t stream) {
+  if (!well_formed(weight, 3) || (weight->dtype != CCC_BF16 && weight->dtype != CCC_F32))
+    return CCC_ERR_INVALID_ARG;
+  const int64_t Cout = weight->shape[0], Cin = weight->shape[1], K = weight->shape[2];
+  if (!well_formed(packed, 3) || packed->dtype != CCC_BF16 || !shape_is(packed, K, Cout, Cin))
+    return CCC_ERR_INVALID_ARG;
+  const int64_t n = K * Cout * Cin;
+  if (n > 0 && !((Cin <= 1 || packed->stride[2] == 1) && (Cout <= 1 || packed->stride[1] == Cin) &&
+                 (K <= 1 || packed->stride[0] == Cout * Cin)))
+    return CCC_ERR_UNSUPPORTED;  // the packed weight is contiguous
+  if (overlaps(weight, packed)) return CCC_ERR_ALIAS;
+  if (n == 0) return CCC_OK;
+  return ccc::launch_pack_weight(weight->data, weight->dtype == CCC_F32, weight->stride[0],
+                                 weight->stride[1], weight->stride[2],
+                                 static_cast<uint16_t*>(packed->data), Cout, Cin, K, stream) == cudaSuccess
+             ? CCC_OK
+             : CCC_ERR_CUDA;
+}
+
+ccc_status ccc_fullconv1d_fwd(const ccc_tensor* x, const ccc_tensor* packed_weight,
+                              const ccc_tensor* bias, int dilation, const ccc_tensor* out,
+                              int* d_status, cudaStream_t stream) {
+  if (!well_formed(x, 3) || x->dtype != CCC_BF16) return CCC_ERR_INVALID_ARG;
+  if (!well_formed(packed_weight, 3) || packed_weight->dtype != CCC_BF16) return CCC_ERR_INVALID_ARG;
+  const int64_t B = x->shape[0], Cin = x->shape[1], T = x->shape[2];
+  const int64_t K = packed_weight->shape[0], Cout = packed_weight->shape[1];
+  if (packed_weight->shape[2] != Cin || K < 1 || Cin < 1 || Cout < 1) return CCC_ERR_INVALID_ARG;
+  if (dilation < 1) return CCC_ERR_INVALID_ARG;
+  if (!well_formed(out, 3) || out->dtype != CCC_BF16 || !shape_is(out, B, Cout, T))
+    return CCC_ERR_INVALID_ARG;
+  if (bias && (!well_formed(bias, 1) || (bias->dtype != CCC_BF16 && bias->dtype != CCC_F32) ||
+               !shape_is(bias, Cout)))
+    return CCC_ERR_INVALID_ARG;
+  // what the tensor-memory GEMM reads: channel-last x and out with rows on
+  // 16-byte boundaries, a contiguous packed weight, sizes that fit its grid
+  if (Cin % 8 != 0 || Cout % 8 != 0) return CCC_ERR_UNSUPPORTED;
+  if (K > 1024 || (K - 1) * int64_t(dilation) > INT32_MAX / 2 || T > INT32_MAX / 2 ||
+      B > 65535 || (Cout + 255) / 256 > 65535 || Cin > (int64_t(1) << 24))
+    return CCC_ERR_UNSUPPORTED;
+  for (const ccc_tensor* t : {x, out}) {
+    const int64_t sb = t->shape[0] > 1 ? t->stride[0] : 0;
+    const int64_t st = t->shape[2] > 1 ? t->stride[2] : 0;
+    if (t->shape[1] > 1 && t->stride[1] != 1) return CCC_ERR_UNSUPPORTED;
+    if (sb % 8 != 0 || st % 8 != 0 || !aligned16(t->data)) return CCC_ERR_UNSUPPORTED;
+    if (T > 1 && st < t->shape[1]) return CCC_ERR_UNSUPPORTED;
+  }
+  if (!((Cin <= 1 || packed_weight->stride[2] == 1) &&
+        (Cout <= 1 || packed_weight->stride[1] == Cin) &&
+        (K <= 1 || packed_weight->stride[0] == Cout * Cin)) ||
+      !aligned16(packed_weight->data))
+    return CCC_ERR_UNSUPPORTED;
+  if (!self_disjoint(out)) return CCC_ERR_UNSUPPORTED;
+  for (const ccc_tensor* in : {x, packed_weight, bias})
+    if (in && overlaps(out, in)) return CCC_ERR_ALIAS;
+  if (B == 0 || T == 0) return CCC_OK;
+
+  ccc::FullConvArgs f{};
+  f.x = static_cast<const uint16_t*>(x->data);
+  f.x_sb = B > 1 ? x->stride[0] : 0;
+  f.x_st = T > 1 ? x->stride[2] : Cin + (8 - Cin % 8) % 8;
+  f.w = static_cast<const uint16_t*>(packed_weight->data);
+  f.bias = bias ? bias->data : nullptr;
+  f.bias_f32 = bias && bias->dtype == CCC_F32;
+  f.bias_s = bias ? bias->stride[0] : 0;
+  f.out = static_cast<uint16_t*>(out->data);
+  f.o_sb = B > 1 ? out->stride[0] : 0;
+  f.o_st = T > 1 ? out->stride[2] : 0;
+  f.B = B;
+  f.T = T;
+  f.Cin = int(Cin);
+  f.Cout = int(Cout);
+  f.K = int(K);
+  f.dil = dilation;
+  f.status = d_status;
+  return ccc::launch_fullconv(f, stream) == cudaSuccess ? CCC_OK : CCC_ERR_CUDA;
 }
 
 }  // extern "C"

@@ -1,0 +1,411 @@
+// Full-channel dilated causal conv1d on the 5th-generation tensor cores
+// (POPCORNBENCH conv1d page: a Conv1d over all input channels with dilation,
+// left-padded by P = (K-1)*dil so that tap k reads input position
+// t + k*dil - P, zero before 0).  With channel-last activations and the
+// weight packed tap-major as Wk[oc, ic] = W[oc, ic, k]:
+//
+//   out[b, t, oc] = bias[oc] + sum_k sum_ic x[b, t - (K-1-k)*dil, ic] * Wk[oc, ic]
+//
+// a sum of K GEMMs whose A operand is x shifted along tokens.  This is a dense
+// contraction (2 * Cin * K FLOPs per output), so it runs as an implicit GEMM
+// on tcgen05: one CTA per output tile of 128 tokens x 256 output channels of
+// one batch row.  For each (tap, block of 64 input channels) a TMA load brings
+// the 128 x 64 slice of x starting at token t0 - (K-1-k)*dil (coordinates
+// before token 0 read as zeros: the causal padding needs no padded copy) and
+// the 256 x 64 slice of Wk into a 4-stage ring of 128-byte-swizzled shared
+// memory; one thread issues four tcgen05.mma (M 128, N 256, K 16, BF16 in,
+// FP32 accumulate) into a 128 x 256 FP32 accumulator in tensor memory; after
+// the last block the four warps read the accumulator back with tcgen05.ld,
+// add the bias, round to BF16 and store.
+//
+// Every wait on an mbarrier is bounded (by the global timer): when one runs
+// out, the kernel records CCC_ERR_DEVICE_TIMEOUT in the status word, waits
+// (bounded again) for its own copies and MMAs in flight, frees its tensor
+// memory and returns, so the context stays usable.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+
+#include "ccc_conv1d.h"
+#include "launch.h"
+
+namespace ccc {
+namespace fullconv {
+
+constexpr int BM = 128;  // tokens per tile (MMA M, TMEM lanes)
+constexpr int BN = 256;  // output channels per tile (MMA N, TMEM columns)
+constexpr int BK = 64;   // input channels per stage: one 128-byte swizzle row of BF16
+constexpr int UK = 16;   // K of one kind::f16 MMA
+constexpr int kStages = 4;
+constexpr int kThreads = 128;
+constexpr uint32_t kABytes = BM * BK * 2;  // 16 KB
+constexpr uint32_t kBBytes = BN * BK * 2;  // 32 KB
+constexpr uint32_t kStageBytes = kABytes + kBBytes;
+constexpr uint32_t kTmemCols = BN;  // FP32 accumulator: one column per output channel
+// ring + barriers (2 per stage + 1) + TMEM address + abort flag, plus slack to
+// align the ring to 1024 bytes (the 128-byte swizzle repeats every 8 rows)
+constexpr size_t kSmemBytes = 1024 + size_t(kStages) * kStageBytes + 8 * (2 * kStages + 1) + 16;
+constexpr int kStatusTimeout = 9;  // == CCC_ERR_DEVICE_TIMEOUT
+constexpr uint64_t kWaitLimitNs = 500ull * 1000 * 1000;
+
+// Instruction descriptor of tcgen05.mma kind::f16: D FP32 (bits 4-5 = 1), A and
+// B BF16 (bits 7-9 = 1, 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 at
+// bits 17-22, M >> 4 at bits 24-28.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(BN >> 3) << 17) |
+                            (uint32_t(BM >> 4) << 24);
+
+// Shared-memory matrix descriptor of a K-major tile stored as TMA writes it
+// with 128-byte swizzling: rows of 64 BF16 (128 bytes), 8-row groups 1024 bytes
+// apart.  Start address >> 4 at bits 0-13; leading byte offset (unused for
+// swizzled K-major tiles) 16 >> 4 at bits 16-29; stride byte offset
+// 1024 >> 4 at bits 32-45; descriptor version 1 at bits 46-47; base offset 0
+// (tiles are 1024-byte aligned); layout SWIZZLE_128B = 2 at bits 61-63.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  return uint64_t((saddr & 0x3FFFFu) >> 4) | (uint64_t(1) << 16) | (uint64_t(1024 >> 4) << 32) |
+         (uint64_t(1) << 46) | (uint64_t(2) << 61);
+}
+
+// ---- PTX wrappers ----------------------------------------------------------------
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.b32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Waits for the phase of `bar` with the given parity to complete; false when
+// kWaitLimitNs pass first (or after 2^26 polls, should the timer stall).
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 0; i < (1u << 26); ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (global_ns() - t0 > kWaitLimitNs) return false;
+  }
+  return false;
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// D[tmem] (+)= A[smem] * B[smem]^T, M 128 x N 256 x K 16.
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(kIdesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive on `bar` once every MMA this thread issued so far has completed.
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+// 32 consecutive FP32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+      "%12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
+      "%30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld_wait() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+struct Args {
+  uint16_t* out;      // [B, T, Cout] storage (channel stride 1)
+  int64_t o_sb, o_st;
+  const void* bias;   // [Cout] BF16 or FP32, or nullptr
+  int bias_f32;
+  int64_t bias_s;
+  int T, Cout, K, dil;
+  int n_kblk;         // blocks of 64 input channels
+  int* status;
+};
+
+extern __shared__ __align__(1024) uint8_t fc_smem[];
+
+__global__ void __launch_bounds__(kThreads, 1)
+    fullconv_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
+                    Args a) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t0 = blockIdx.x * BM, n0 = blockIdx.y * BN, bb = blockIdx.z;
+  const int n_iter = a.K * a.n_kblk;
+
+  // shared layout: A stages, B stages (1024-aligned), then the barriers
+  const uint32_t raw = smem_u32(fc_smem);
+  const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+  const uint32_t sA = raw + pad;
+  const uint32_t sB = sA + kStages * kABytes;
+  const uint32_t bars = sB + kStages * kBBytes;
+  auto full_bar = [&](int s) { return bars + 8u * s; };
+  auto empty_bar = [&](int s) { return bars + 8u * (kStages + s); };
+  const uint32_t acc_bar = bars + 8u * (2 * kStages);
+  const uint32_t tmem_slot = acc_bar + 8;
+  uint8_t* gbase = fc_smem + pad + (bars - sA) + 8 * (2 * kStages + 1);  // generic view of the slot
+  volatile uint32_t* tmem_slot_p = reinterpret_cast<volatile uint32_t*>(gbase);
+  volatile int* abort_p = reinterpret_cast<volatile int*>(gbase + 4);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    mbar_init(acc_bar, 1);
+    *abort_p = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    prefetch_map(&map_x);
+    prefetch_map(&map_w);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot_p;
+
+  auto fail = [&]() {
+    *abort_p = 1;
+    if (a.status) atomicCAS(a.status, 0, kStatusTimeout);
+  };
+
+  if (warp == 0 && lane == 0) {
+    // producer: TMA loads of the (tap, channel block) stages
+    int issued = 0;
+    for (int i = 0; i < n_iter; ++i) {
+      const int s = i % kStages;
+      const uint32_t ph = uint32_t(i / kStages) & 1u;
+      if (!mbar_wait(empty_bar(s), ph ^ 1u)) {  // the MMAs have released the stage
+        fail();
+        break;
+      }
+      if (*abort_p) break;
+      const int k = i / a.n_kblk, kb = i - k * a.n_kblk;
+      mbar_expect_tx(full_bar(s), kStageBytes);
+      tma_load_3d(sA + s * kABytes, &map_x, full_bar(s), kb * BK, t0 - (a.K - 1 - k) * a.dil, bb);
+      tma_load_3d(sB + s * kBBytes, &map_w, full_bar(s), kb * BK, n0, k);
+      ++issued;
+    }
+    if (*abort_p) {  // let the loads in flight land before the CTA leaves
+      for (int i = issued - kStages < 0 ? 0 : issued - kStages; i < issued; ++i)
+        mbar_wait(full_bar(i % kStages), uint32_t(i / kStages) & 1u);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // MMA issuer
+    for (int i = 0; i < n_iter; ++i) {
+      const int s = i % kStages;
+      const uint32_t ph = uint32_t(i / kStages) & 1u;
+      if (!mbar_wait(full_bar(s), ph)) {  // both tiles of the stage have landed
+        fail();
+        break;
+      }
+      if (*abort_p) break;
+      tc_fence_after();
+      const uint64_t ad = sw128_desc(sA + s * kABytes), bd = sw128_desc(sB + s * kBBytes);
+#pragma unroll
+      for (int j = 0; j < BK / UK; ++j)  // +32 bytes along K per MMA: +2 in the address field
+        mma_bf16(tmem, ad + 2 * j, bd + 2 * j, (i > 0 || j > 0) ? 1u : 0u);
+      mma_commit(empty_bar(s));
+    }
+    mma_commit(acc_bar);  // all MMAs above complete (also on the abort path)
+  }
+  __syncwarp();
+
+  // epilogue: warp w owns TMEM lanes 32w .. 32w+31, i.e. tokens t0 + 32w + lane
+  const bool acc_ok = mbar_wait(acc_bar, 0);
+  tc_fence_after();
+  if (!acc_ok && lane == 0) fail();
+  __syncwarp();
+  if (acc_ok && !*abort_p) {
+    const int t = t0 + warp * 32 + lane;
+    uint16_t* orow = a.out + int64_t(bb) * a.o_sb + int64_t(t) * a.o_st;
+    for (int c0 = 0; c0 < BN && n0 + c0 < a.Cout; c0 += 32) {  // warp-uniform bound
+      uint32_t r[32];
+      tmem_ld32(tmem + (uint32_t(warp * 32) << 16) + uint32_t(c0), r);
+      tmem_ld_wait();
+      if (t < a.T) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int oc = n0 + c0 + 8 * q;
+          if (oc >= a.Cout) break;  // Cout is a multiple of 8
+          float v[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            float bj = 0.0f;
+            if (a.bias)
+              bj = a.bias_f32 ? __ldg(static_cast<const float*>(a.bias) + int64_t(oc + j) * a.bias_s)
+                              : bf16_to_f32(__ldg(static_cast<const uint16_t*>(a.bias) +
+                                                  int64_t(oc + j) * a.bias_s));
+            v[j] = __uint_as_float(r[8 * q + j]) + bj;
+          }
+          const uint4 pk = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                                      pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+          *reinterpret_cast<uint4*>(orow + oc) = pk;
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// weight [Cout, Cin, K] (any strides, BF16 or FP32) -> packed [K, Cout, Cin] BF16
+// (nearest-even for FP32); consecutive threads write consecutive input channels.
+__global__ void pack_weight_kernel(const void* w, int w_f32, int64_t s_oc, int64_t s_ic, int64_t s_k,
+                                   uint16_t* packed, int64_t Cout, int64_t Cin, int64_t K) {
+  const int64_t n = K * Cout * Cin;
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t ic = i % Cin, r = i / Cin, oc = r % Cout, k = r / Cout;
+    const int64_t o = oc * s_oc + ic * s_ic + k * s_k;
+    packed[i] = w_f32 ? f32_to_bf16(__ldg(static_cast<const float*>(w) + o))
+                      : __ldg(static_cast<const uint16_t*>(w) + o);
+  }
+}
+
+// ---- host side --------------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }();
+  return fn;
+}
+
+// A 3-D BF16 tensor map (innermost dimension contiguous) with a box of
+// (64, box1, 1) elements and 128-byte swizzling; out-of-range elements read 0.
+bool make_map(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+              uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box1) {
+  const PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
+  const cuuint32_t box[3] = {uint32_t(BK), box1, 1};
+  const cuuint32_t estride[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+            estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+ContextCache g_attr_done;
+
+cudaError_t smem_attribute() {
+  long long done = 0;
+  if (g_attr_done.get(&done) && done) return cudaSuccess;
+  const cudaError_t err = cudaFuncSetAttribute(fullconv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               int(kSmemBytes));
+  if (err == cudaSuccess) g_attr_done.put(1);
+  return err;
+}
+
+}  // namespace fullconv
+
+cudaError_t launch_fullconv(const FullConvArgs& f, cudaStream_t stream) {
+  using namespace fullconv;
+  CUtensorMap mx, mw;
+  // x: dims (Cin, T, B), row strides in bytes (the batch stride of a single
+  // batch row is never used; any legal value serves)
+  const uint64_t xs_t = uint64_t(f.x_st) * 2;
+  const uint64_t xs_b = f.B > 1 ? uint64_t(f.x_sb) * 2 : xs_t * uint64_t(f.T > 0 ? f.T : 1);
+  if (!make_map(&mx, f.x, uint64_t(f.Cin), uint64_t(f.T), uint64_t(f.B), xs_t, xs_b, BM))
+    return cudaErrorInvalidValue;
+  // packed weight: dims (Cin, Cout, K), contiguous
+  if (!make_map(&mw, f.w, uint64_t(f.Cin), uint64_t(f.Cout), uint64_t(f.K), uint64_t(f.Cin) * 2,
+                uint64_t(f.Cin) * 2 * uint64_t(f.Cout), BN))
+    return cudaErrorInvalidValue;
+  const cudaError_t err = smem_attribute();
+  if (err != cudaSuccess) return err;
+  Args a{};
+  a.out = f.out;
+  a.o_sb = f.o_sb;
+  a.o_st = f.o_st;
+  a.bias = f.bias;
+  a.bias_f32 = f.bias_f32;
+  a.bias_s = f.bias_s;
+  a.T = int(f.T);
+  a.Cout = f.Cout;
+  a.K = f.K;
+  a.dil = f.dil;
+  a.n_kblk = (f.Cin + BK - 1) / BK;
+  a.status = f.status;
+  const dim3 grid(unsigned((f.T + BM - 1) / BM), unsigned((f.Cout + BN - 1) / BN), unsigned(f.B));
+  return launch_kernel(fullconv_kernel, grid, dim3(kThreads), kSmemBytes, stream, false, mx, mw, a);
+}
+
+cudaError_t launch_pack_weight(const void* w, int w_f32, int64_t s_oc, int64_t s_ic, int64_t s_k,
+                               uint16_t* packed, int64_t Cout, int64_t Cin, int64_t K,
+                               cudaStream_t stream) {
+  const int64_t n = K * Cout * Cin;
+  const unsigned blocks = unsigned(std::min<int64_t>((n + 255) / 256, 152 * 8));
+  fullconv::pack_weight_kernel<<<blocks, 256, 0, stream>>>(w, w_f32, s_oc, s_ic, s_k, packed, Cout,
+                                                           Cin, K);
+  return cudaGetLastError();
+}
+
+}  // namespace ccc

@@ -154,4 +154,23 @@ cudaError_t launch_bwd(const BwdArgs& a, const BwdPlan& p, int act, const WgradO
                        int64_t partial_rows, cudaStream_t stream);
 cudaError_t launch_update(const UpdArgs& a, int vec, int act, cudaStream_t stream);
 
+// Full-channel dilated causal conv1d (fullconv.cu).
+struct FullConvArgs {
+  const uint16_t* x;     // [B, T, Cin] storage: channel stride 1
+  int64_t x_sb, x_st;    // element strides (multiples of 8)
+  const uint16_t* w;     // packed [K, Cout, Cin] BF16, contiguous
+  const void* bias;      // [Cout] BF16 or FP32, or nullptr
+  int bias_f32;
+  int64_t bias_s;
+  uint16_t* out;         // [B, T, Cout] storage: channel stride 1
+  int64_t o_sb, o_st;
+  int64_t B, T;
+  int Cin, Cout, K, dil;
+  int* status;
+};
+cudaError_t launch_fullconv(const FullConvArgs& f, cudaStream_t stream);
+cudaError_t launch_pack_weight(const void* w, int w_f32, int64_t s_oc, int64_t s_ic, int64_t s_k,
+                               uint16_t* packed, int64_t Cout, int64_t Cin, int64_t K,
+                               cudaStream_t stream);
+
 }  // namespace ccc

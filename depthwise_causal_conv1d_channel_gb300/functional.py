@@ -208,3 +208,48 @@ def causal_conv1d_update(x: torch.Tensor, conv_state: torch.Tensor, weight: torc
                                 torch.cuda.current_stream(x.device))
     _raise(st, "causal_conv1d_update")
     return out
+
+
+def pack_full_conv_weight(weight: torch.Tensor, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """The full-channel conv's weight [Cout, Cin, K] (BF16, or FP32 rounded to
+    BF16) copied tap-major into the [K, Cout, Cin] BF16 layout that
+    full_causal_conv1d's kernel reads; pack once per weight update."""
+    K, Cout, Cin = weight.shape[2], weight.shape[0], weight.shape[1]
+    if out is None:
+        out = torch.empty(K, Cout, Cin, dtype=torch.bfloat16, device=weight.device)
+    st = _abi.ccc_fullconv1d_pack_weight(weight, out, torch.cuda.current_stream(weight.device))
+    _raise(st, "pack_full_conv_weight")
+    return out
+
+
+def full_causal_conv1d(x: torch.Tensor, weight: Optional[torch.Tensor] = None,
+                       bias: Optional[torch.Tensor] = None, dilation: int = 1,
+                       packed_weight: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Full-channel dilated causal conv1d (the POPCORNBENCH conv1d page's
+    operation), forward only:
+
+        out[b, oc, t] = bias[oc] + sum_{ic, k} weight[oc, ic, k] * x[b, ic, t + k*dilation - P]
+
+    with P = (K - 1) * dilation and x read as zero before position 0.  x is
+    [B, Cin, T] BF16; the kernel reads channel-last storage ([B, T, Cin] seen
+    as its transpose), so another layout is restrided first (a copy).  Pass
+    ``weight`` [Cout, Cin, K] or its ``packed_weight`` from
+    pack_full_conv_weight.  Returns out [B, Cout, T] BF16 with channel-last
+    storage.  Runs on the tensor cores (BF16 operands, FP32 accumulation)."""
+    if torch.is_grad_enabled() and (x.requires_grad or (weight is not None and weight.requires_grad)
+                                    or (bias is not None and bias.requires_grad)):
+        raise NotImplementedError("full_causal_conv1d is forward only")
+    if packed_weight is None:
+        if weight is None:
+            raise ValueError("pass weight or packed_weight")
+        packed_weight = pack_full_conv_weight(weight)
+    if x.dim() == 3 and x.shape[1] > 1 and x.stride(1) != 1:
+        x = x.transpose(1, 2).contiguous().transpose(1, 2)
+    B, T = x.shape[0], x.shape[2]
+    Cout = packed_weight.shape[1]
+    out = torch.empty(B, T, Cout, dtype=torch.bfloat16, device=x.device).transpose(1, 2)
+    st = _abi.ccc_fullconv1d_fwd(x, packed_weight, bias, int(dilation), out, status_word(x.device),
+                                 torch.cuda.current_stream(x.device))
+    _raise(st, "full_causal_conv1d")
+    _debug_check(x.device)
+    return out

@@ -59,8 +59,10 @@ typedef enum {
     CCC_ERR_WORKSPACE = 5,        /* workspace NULL, too small or not 16-byte aligned */
     CCC_ERR_CUDA = 6,             /* a CUDA runtime call or launch failed */
     CCC_ERR_BAD_CU_SEQLENS = 7,   /* device-detected malformed cu_seqlens (via d_status) */
-    CCC_ERR_SCRATCH_LIMIT = 8     /* ccc_conv1d_bwd_noalloc: the problem needs more scratch
+    CCC_ERR_SCRATCH_LIMIT = 8,    /* ccc_conv1d_bwd_noalloc: the problem needs more scratch
                                      than CCC_CONV1D_NOALLOC_SCRATCH_BYTES */
+    CCC_ERR_DEVICE_TIMEOUT = 9    /* ccc_fullconv1d_fwd: a bounded wait on the device ran out
+                                     (via d_status); the call's output is unspecified */
 } ccc_status;
 
 typedef enum { CCC_BF16 = 0, CCC_F32 = 1, CCC_I32 = 2 } ccc_dtype;
@@ -226,6 +228,51 @@ ccc_status ccc_conv1d_bwd_noalloc(const ccc_tensor *x, const ccc_tensor *weight,
 ccc_status ccc_conv1d_update(const ccc_tensor *x, const ccc_tensor *conv_state,
                              const ccc_tensor *weight, const ccc_tensor *bias,
                              const ccc_tensor *out, int activation, cudaStream_t stream);
+
+/*
+ * Full-channel dilated causal conv1d (POPCORNBENCH conv1d page: a Conv1d over
+ * all input channels with dilation, left-padded by P = (K-1)*dilation; the
+ * reasoning section derives that tap k reads input position t + k*dilation - P
+ * and the listing adds an optional bias):
+ *
+ *   out[b,oc,t] = bias[oc] + sum_{ic<Cin} sum_{k<K} W[oc,ic,k] * x[b,ic,t + k*dilation - P]
+ *
+ * with x read as zero at negative positions.  A dense contraction over input
+ * channels and taps, computed on the tensor cores: BF16 operands, FP32
+ * accumulation, BF16 output (rounded to nearest even).  Forward only.
+ *
+ * ccc_fullconv1d_pack_weight copies W into the tap-major layout the kernel
+ * reads (do it once per weight update; the weight is not read otherwise):
+ *
+ *   weight   [Cout, Cin, K] BF16 or FP32 (rounded to BF16), any strides.
+ *   packed   [K, Cout, Cin] BF16, contiguous; packed[k, oc, ic] = W[oc, ic, k].
+ *            Must not overlap weight (CCC_ERR_ALIAS).
+ *
+ * ccc_fullconv1d_fwd:
+ *
+ *   x              [B, Cin, T] BF16, channel-last: stride[1] == 1 (the
+ *                  transpose view of [B, T, Cin] storage); the token and batch
+ *                  strides multiples of 8 elements, data 16-byte aligned,
+ *                  Cin a multiple of 8.  Other layouts: CCC_ERR_UNSUPPORTED.
+ *   packed_weight  [K, Cout, Cin] BF16 from ccc_fullconv1d_pack_weight
+ *                  (contiguous, 16-byte aligned); Cout a multiple of 8.
+ *   bias           [Cout] BF16 or FP32 (added in FP32), any stride, or NULL.
+ *   dilation       >= 1.
+ *   out            [B, Cout, T] BF16, channel-last like x (same rules).
+ *                  Must not overlap x, packed_weight or bias (CCC_ERR_ALIAS).
+ *   d_status       device int or NULL: a wait inside the kernel that runs out
+ *                  (it cannot in a working GPU) records CCC_ERR_DEVICE_TIMEOUT.
+ *
+ * B == 0 or T == 0 computes nothing.  Limits (else CCC_ERR_UNSUPPORTED): B and
+ * ceil(Cout / 256) at most 65535, K at most 1024, (K-1)*dilation and T below
+ * 2^30.
+ */
+ccc_status ccc_fullconv1d_pack_weight(const ccc_tensor *weight, const ccc_tensor *packed,
+                                      cudaStream_t stream);
+
+ccc_status ccc_fullconv1d_fwd(const ccc_tensor *x, const ccc_tensor *packed_weight,
+                              const ccc_tensor *bias, int dilation, const ccc_tensor *out,
+                              int *d_status, cudaStream_t stream);
 
 /*
  * Synchronise `stream`, read the device status word written by the kernels

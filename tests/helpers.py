@@ -8,6 +8,10 @@ Tolerances (stated once, used everywhere):
 * dweight / dbias: |gpu - ref64| <= 1e-3 * sum|terms| (+ 2^-8 * |ref64| when the
   output is BF16: one BF16 rounding of the result, which the relative bound on
   the sum cannot absorb when the terms do not cancel).
+* full-channel conv output: the same form, |gpu - ref64| <= 1e-3 * sum|terms| +
+  2^-8 * |ref64|: the operands are BF16 (their products exact in FP32), the
+  tensor cores accumulate Cin * K products in FP32 in an order of their own,
+  and the result is rounded once to BF16.
 """
 
 from __future__ import annotations
@@ -92,3 +96,14 @@ def oracle_bwd(inp, channels=None):
     return oracle.bwd(bits(x), bits(w), bits(g), bits(b),
                       None if inp.cu_seqlens is None else inp.cu_seqlens.numpy(),
                       bits(init), bits(gf), inp.activation)
+
+
+def assert_fullconv_close(gpu_bits, ref64, abs_sum, what="full conv out"):
+    g = decode(gpu_bits)
+    err = np.abs(g - ref64)
+    bound = WG_REL * abs_sum + BF16_HALF_ULP_REL * np.abs(ref64) + 1e-30
+    bad = err > bound
+    if bad.any():
+        i = np.unravel_index(np.argmax(err / bound), err.shape)
+        raise AssertionError(f"{what}: {bad.sum()} of {bad.size} out of tolerance; worst at {i}: "
+                             f"gpu={g[i]} ref={ref64[i]} sum|terms|={abs_sum[i]}")

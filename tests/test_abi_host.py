@@ -51,7 +51,7 @@ def test_header_compiles_as_c():
 
 def test_abi_version_and_status_strings():
     assert _abi.lib.ccc_conv1d_abi_version() == _abi.ABI_VERSION
-    for code in range(9):
+    for code in range(10):
         assert _abi.status_string(code) != "unknown status"
     assert _abi.status_string(99) == "unknown status"
 

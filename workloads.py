@@ -237,3 +237,42 @@ def seq_ids(B: int, T: int, seed: int, kind: str = "runs", max_run: int = 64,
             t += n
             cur += 1
     return ids
+
+
+# ---- full-channel dilated causal conv1d (POPCORNBENCH conv1d page) -------------
+
+@dataclasses.dataclass
+class FullConvInputs:
+    x: torch.Tensor                 # [B, Cin, T] BF16 (channel-last storage: [B, T, Cin])
+    weight: torch.Tensor            # [Cout, Cin, K] BF16 or FP32
+    bias: Optional[torch.Tensor]    # [Cout] BF16 or FP32, or None
+    dilation: int
+
+    def to(self, device) -> "FullConvInputs":
+        return dataclasses.replace(
+            self, x=self.x.transpose(1, 2).contiguous().to(device).transpose(1, 2),
+            weight=self.weight.to(device), bias=None if self.bias is None else self.bias.to(device))
+
+
+def fullconv_inputs(B: int, Cin: int, Cout: int, T: int, K: int, dilation: int, seed: int = 0,
+                    bias: bool = True, weight_dtype=BF16, bias_dtype=BF16) -> FullConvInputs:
+    """x ~ N(0, 1) stored [B, T, Cin]; weight and bias ~ U(-1/sqrt(Cin*K), +1/sqrt(Cin*K))
+    (the bound of the page's listing's initialisation, fan-in Cin*K).  Draw
+    order: x, weight, bias."""
+    gen = torch.Generator().manual_seed(seed)
+    x = _normal(gen, (B, T, Cin)).to(BF16).transpose(1, 2)
+    bound = 1.0 / float(Cin * K) ** 0.5
+    w = _uniform(gen, (Cout, Cin, K), -bound, bound)
+    w = w if weight_dtype == torch.float32 else w.to(BF16)
+    b = None
+    if bias:
+        b = _uniform(gen, (Cout,), -bound, bound)
+        b = b if bias_dtype == torch.float32 else b.to(BF16)
+    return FullConvInputs(x=x, weight=w, bias=b, dilation=dilation)
+
+
+def fullconv_dilated(seed: int = 0) -> FullConvInputs:
+    """The full-channel workload measured here: B = 8 rows of T = 4096 tokens,
+    Cin = Cout = 1024, kernel size 4, dilation 2, BF16 bias (the page prints no
+    sizes; this is a mid-size dilated causal layer)."""
+    return fullconv_inputs(8, 1024, 1024, 4096, 4, 2, seed=seed)
