@@ -149,14 +149,17 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
-def measured_peak():
+def measured_peak(key="hbm_gbs", fallback=FALLBACK_HBM_GBS):
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(path) as f:
-            v = float(json.load(f)["hbm_gbs"])
+            v = float(json.load(f)[key])
         return v, "measured"
     except (OSError, KeyError, ValueError):
-        return FALLBACK_HBM_GBS, "fallback"
+        return fallback, "fallback"
+
+
+FALLBACK_BF16_TFLOPS = 1900.0
 
 
 # ---- the timed step ---------------------------------------------------------------
@@ -365,6 +368,67 @@ def bench_update(device, stream, peak, iters=50):
     torch.cuda.synchronize()
     r["graph_chain_1000"] = {"us_per_step": round(a.elapsed_time(c) * 1e3 / 1000, 3),
                              "note": "one state, L2-resident, CUDA graph; not an HBM figure"}
+    return r
+
+
+def fullconv_flops(B, T, Cin, Cout, K):
+    """Dense count of the full-channel conv: 2 * Cin * K multiply-adds per output
+    (the taps that read the causal padding included)."""
+    return 2 * B * T * Cout * Cin * K
+
+
+class FullConvStep:
+    """The full-channel dilated conv forward through the C ABI on the packed
+    weight (packed once, outside the timed region)."""
+
+    def __init__(self, inp: "workloads.FullConvInputs", device, sets=2):
+        from depthwise_causal_conv1d_channel_gb300 import _abi
+        import depthwise_causal_conv1d_channel_gb300 as ccc
+
+        self.abi = _abi
+        d = inp.to(device)
+        self.dil = inp.dilation
+        self.B, self.Cin, self.T = d.x.shape
+        self.Cout, _, self.K = d.weight.shape
+        self.packed = ccc.pack_full_conv_weight(d.weight)
+        self.bias = d.bias
+        self.sets = sets
+        self.x = [d.x] + [d.x.transpose(1, 2).clone().transpose(1, 2) for _ in range(sets - 1)]
+        self.out = [torch.empty(self.B, self.T, self.Cout, dtype=torch.bfloat16,
+                                device=device).transpose(1, 2) for _ in range(sets)]
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        self.flops = fullconv_flops(self.B, self.T, self.Cin, self.Cout, self.K)
+
+    def fwd(self, i, stream):
+        k = i % self.sets
+        rc = self.abi.ccc_fullconv1d_fwd(self.x[k], self.packed, self.bias, self.dil, self.out[k],
+                                         self.status, stream)
+        assert rc == 0, self.abi.status_string(rc)
+
+    def check_status(self, stream):
+        rc = self.abi.ccc_read_status(self.status, stream)
+        assert rc == 0, self.abi.status_string(rc)
+
+
+def bench_fullconv(device, stream):
+    """The full-channel dilated causal conv (8 x 4096 tokens, 1024 -> 1024
+    channels, K 4, dilation 2): TFLOP/s against the measured dense BF16 peak."""
+    peak, kind = measured_peak("bf16_tflops", FALLBACK_BF16_TFLOPS)
+    sustained, _ = measured_peak("bf16_tflops_sustained", FALLBACK_BF16_TFLOPS)
+    st = FullConvStep(workloads.fullconv_dilated(), device)
+    ms = _per_call_ms(st.fwd, st.sets, device, stream)
+    st.check_status(stream)
+    tflops = st.flops / (ms * 1e-3) / 1e12
+    r = {"workload": "fullconv_dilated", "B": st.B, "T": st.T, "Cin": st.Cin, "Cout": st.Cout,
+         "K": st.K, "dilation": st.dil,
+         "fwd": {"us": round(ms * 1e3, 2), "flops": st.flops, "TFLOP/s": round(tflops, 1),
+                 "tokens_per_s": round(st.B * st.T / (ms * 1e-3))},
+         "roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": peak,
+                      "peak_kind": f"{kind} bf16 burst", "unit": "TFLOP/s",
+                      "frac": round(tflops / peak, 4),
+                      "frac_of_sustained": round(tflops / sustained, 4)}}
+    del st
+    torch.cuda.empty_cache()
     return r
 
 
@@ -587,7 +651,7 @@ def run_reference(args):
 
 PROFILE_WORKLOADS = ("dense_small", "dense_state", "dense_state_time_contiguous", "packed_varlen",
                      "decode_update", "dense_large_bias", "dense_large_det",
-                     "dense_large_quarter")
+                     "dense_large_quarter", "fullconv_dilated")
 
 
 def run_profile(name: str, calls: int):
@@ -598,6 +662,14 @@ def run_profile(name: str, calls: int):
     from depthwise_causal_conv1d_channel_gb300 import _abi
 
     stream = torch.cuda.current_stream(device)
+    if name == "fullconv_dilated":
+        st = FullConvStep(workloads.fullconv_dilated(), device, sets=1)
+        for _ in range(calls):
+            st.fwd(0, stream)
+        st.check_status(stream)
+        torch.cuda.synchronize()
+        print(json.dumps({"profile": name, "calls": calls}))
+        return
     if name == "decode_update":
         wl = workloads.decode_update(steps=calls)
         st = wl.conv_state.to(device)
@@ -738,6 +810,7 @@ def main():
         bd.append(bench_conv_workload("dense_large_bias", inp, device, stream, peak, False))
         large = dataclasses.replace(inp, bias=None, deterministic=True)
         bd.append(bench_conv_workload("dense_large_det", large, device, stream, peak, True))
+        bd.append(bench_fullconv(device, stream))
         line["breakdown"] = bd
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -49,18 +49,24 @@ constexpr size_t kSmemBytes = 1024 + size_t(kStages) * kStageBytes + 8 * (2 * kS
 constexpr int kStatusTimeout = 9;  // == CCC_ERR_DEVICE_TIMEOUT
 constexpr uint64_t kWaitLimitNs = 500ull * 1000 * 1000;
 
-// Instruction descriptor of tcgen05.mma kind::f16: D FP32 (bits 4-5 = 1), A and
-// B BF16 (bits 7-9 = 1, 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 at
-// bits 17-22, M >> 4 at bits 24-28.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(BN >> 3) << 17) |
-                            (uint32_t(BM >> 4) << 24);
+// Instruction descriptor of tcgen05.mma kind::f16 for M 128 and the given N:
+// D FP32 (bits 4-5 = 1), A and B BF16 (bits 7-9 = 1, 10-12 = 1), both K-major
+// (bits 15, 16 = 0), N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_m128(int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(n >> 3) << 17) | (uint32_t(128 >> 4) << 24);
+}
 
 // Shared-memory matrix descriptor of a K-major tile stored as TMA writes it
 // with 128-byte swizzling: rows of 64 BF16 (128 bytes), 8-row groups 1024 bytes
-// apart.  Start address >> 4 at bits 0-13; leading byte offset (unused for
-// swizzled K-major tiles) 16 >> 4 at bits 16-29; stride byte offset
-// 1024 >> 4 at bits 32-45; descriptor version 1 at bits 46-47; base offset 0
-// (tiles are 1024-byte aligned); layout SWIZZLE_128B = 2 at bits 61-63.
+// apart, the 16-byte chunks of a row permuted by address bits 7-9 (the row's
+// place in its 1024-byte group).  Start address >> 4 at bits 0-13; leading
+// byte offset (unused for swizzled K-major tiles) 16 >> 4 at bits 16-29;
+// stride byte offset 1024 >> 4 at bits 32-45; descriptor version 1 at bits
+// 46-48; base offset 0 at bits 49-51; layout SWIZZLE_128B = 2 at bits 61-63.
+// The tensor cores apply the permutation to the addresses they form, like the
+// TMA unit does, so a matrix may start at any row of a swizzled tile (row r:
+// start + 128 r) with the base offset left at 0 -- measured on sm_103a with
+// an own probe over row offsets 0..16, exact for every offset.
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   return uint64_t((saddr & 0x3FFFFu) >> 4) | (uint64_t(1) << 16) | (uint64_t(1024 >> 4) << 32) |
          (uint64_t(1) << 46) | (uint64_t(2) << 61);
@@ -133,14 +139,14 @@ __device__ __forceinline__ void tc_fence_before() {
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
-// D[tmem] (+)= A[smem] * B[smem]^T, M 128 x N 256 x K 16.
+// D[tmem] (+)= A[smem] * B[smem]^T, M 128 x N x K 16 (N from the descriptor).
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                         uint32_t accumulate) {
+                                         uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(kIdesc), "r"(accumulate)
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 // Arrive on `bar` once every MMA this thread issued so far has completed.
@@ -224,6 +230,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_p = 1;
     if (a.status) atomicCAS(a.status, 0, kStatusTimeout);
   };
+  // Tiles start their walk over the channel blocks at different blocks, so the
+  // CTAs running at once read different weight slices instead of all asking
+  // L2 for the same lines (the sum's order is fixed per tile).
+  const int rot = int((blockIdx.x + blockIdx.y + blockIdx.z) % unsigned(a.n_kblk));
 
   if (warp == 0 && lane == 0) {
     // producer: TMA loads of the (tap, channel block) stages
@@ -236,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       if (*abort_p) break;
-      const int k = i / a.n_kblk, kb = i - k * a.n_kblk;
+      const int k = i / a.n_kblk, kb = (i - k * a.n_kblk + rot) % a.n_kblk;
       mbar_expect_tx(full_bar(s), kStageBytes);
       tma_load_3d(sA + s * kABytes, &map_x, full_bar(s), kb * BK, t0 - (a.K - 1 - k) * a.dil, bb);
       tma_load_3d(sB + s * kBBytes, &map_w, full_bar(s), kb * BK, n0, k);
@@ -260,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t ad = sw128_desc(sA + s * kABytes), bd = sw128_desc(sB + s * kBBytes);
 #pragma unroll
       for (int j = 0; j < BK / UK; ++j)  // +32 bytes along K per MMA: +2 in the address field
-        mma_bf16(tmem, ad + 2 * j, bd + 2 * j, (i > 0 || j > 0) ? 1u : 0u);
+        mma_bf16(tmem, ad + 2 * j, bd + 2 * j, idesc_m128(BN), (i > 0 || j > 0) ? 1u : 0u);
       mma_commit(empty_bar(s));
     }
     mma_commit(acc_bar);  // all MMAs above complete (also on the abort path)
@@ -309,6 +319,197 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ---- one x tile shared by all taps --------------------------------------------------
+//
+// The taps of one output tile read the same x rows shifted by multiples of the
+// dilation, so instead of one 128-row x slice per tap, the kernel below loads
+// per block of 64 input channels ONE slice of RA = 256 + pad rows (tokens
+// t0 - pad .. t0 + 255, pad >= (K-1)*dil rounded up to 16) and lets tap k read
+// it from row pad - (K-1-k)*dil on: the MMA's A descriptor simply starts at that
+// row (see sw128_desc).  A tile
+// is 256 tokens -- two M-128 accumulators sharing each weight slice -- by N
+// output channels, so per (channel block, tap) the tensor cores do 2 x 128 x N
+// x 64 multiply-adds for N x 128 bytes of weight plus a quarter of the x slice:
+// about half the bytes per FLOP of the per-tap kernel above.  x slices take two
+// ring slots, weight slices a ring of NB stages.
+
+struct SharedPlan {
+  int ra;    // rows of an x slot (multiple of 16, at most 512)
+  int pad;   // ra - 256: rows before t0
+  int nb;    // weight stages
+};
+
+template <int N>
+__global__ void __launch_bounds__(kThreads, 1)
+    fullconv_shared_kernel(const __grid_constant__ CUtensorMap map_x,
+                           const __grid_constant__ CUtensorMap map_w, Args a, SharedPlan sp) {
+  constexpr uint32_t kBStage = uint32_t(N) * BK * 2;
+  constexpr uint32_t kCols = 2 * N;  // two accumulators of N FP32 columns
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t0 = blockIdx.x * 256, n0 = blockIdx.y * N, bb = blockIdx.z;
+  const uint32_t slot_a = uint32_t(sp.ra) * 128;
+
+  const uint32_t raw = smem_u32(fc_smem);
+  const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+  const uint32_t sA = raw + pad;
+  const uint32_t sB = sA + 2 * slot_a;
+  const uint32_t bars = sB + uint32_t(sp.nb) * kBStage;
+  auto a_full = [&](int i) { return bars + 8u * i; };
+  auto a_empty = [&](int i) { return bars + 8u * (2 + i); };
+  auto b_full = [&](int i) { return bars + 8u * (4 + i); };
+  auto b_empty = [&](int i) { return bars + 8u * (4 + sp.nb + i); };
+  const uint32_t acc_bar = bars + 8u * (4 + 2 * sp.nb);
+  const uint32_t tmem_slot = acc_bar + 8;
+  uint8_t* gslot = fc_smem + pad + (tmem_slot - sA);
+  volatile uint32_t* tmem_slot_p = reinterpret_cast<volatile uint32_t*>(gslot);
+  volatile int* abort_p = reinterpret_cast<volatile int*>(gslot + 4);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(a_full(i), 1);
+      mbar_init(a_empty(i), 1);
+    }
+    for (int i = 0; i < sp.nb; ++i) {
+      mbar_init(b_full(i), 1);
+      mbar_init(b_empty(i), 1);
+    }
+    mbar_init(acc_bar, 1);
+    *abort_p = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    prefetch_map(&map_x);
+    prefetch_map(&map_w);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot_p;
+
+  auto fail = [&]() {
+    *abort_p = 1;
+    if (a.status) atomicCAS(a.status, 0, kStatusTimeout);
+  };
+
+  // Tiles start their walk over the channel blocks at different blocks, so the
+  // CTAs running at once read different weight slices instead of all asking
+  // L2 for the same lines (the sum's order is fixed per tile).
+  const int rot = int((blockIdx.x + blockIdx.y + blockIdx.z) % unsigned(a.n_kblk));
+
+  if (warp == 0 && lane == 0) {
+    // producer: per channel block one x slice (two boxes of ra / 2 rows),
+    // then the K weight slices
+    int ia = 0, ib = 0;
+    for (int kb = 0; kb < a.n_kblk && !*abort_p; ++kb) {
+      const int sa = kb & 1;
+      const int cb = (kb + rot) % a.n_kblk;  // the channel block
+      if (!mbar_wait(a_empty(sa), (uint32_t(kb >> 1) & 1u) ^ 1u)) {
+        fail();
+        break;
+      }
+      mbar_expect_tx(a_full(sa), slot_a);
+      const uint32_t dst = sA + sa * slot_a;
+      tma_load_3d(dst, &map_x, a_full(sa), cb * BK, t0 - sp.pad, bb);
+      tma_load_3d(dst + slot_a / 2, &map_x, a_full(sa), cb * BK, t0 - sp.pad + sp.ra / 2, bb);
+      ++ia;
+      for (int k = 0; k < a.K; ++k, ++ib) {
+        const int s = ib % sp.nb;
+        if (!mbar_wait(b_empty(s), (uint32_t(ib / sp.nb) & 1u) ^ 1u)) {
+          fail();
+          break;
+        }
+        mbar_expect_tx(b_full(s), kBStage);
+        tma_load_3d(sB + s * kBStage, &map_w, b_full(s), cb * BK, n0, k);
+      }
+    }
+    if (*abort_p) {  // let the loads in flight land before the CTA leaves
+      for (int i = ia - 2 < 0 ? 0 : ia - 2; i < ia; ++i) mbar_wait(a_full(i & 1), uint32_t(i >> 1) & 1u);
+      for (int i = ib - sp.nb < 0 ? 0 : ib - sp.nb; i < ib; ++i)
+        mbar_wait(b_full(i % sp.nb), uint32_t(i / sp.nb) & 1u);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // MMA issuer
+    int ib = 0;
+    constexpr uint32_t idesc = idesc_m128(N);
+    for (int kb = 0; kb < a.n_kblk && !*abort_p; ++kb) {
+      const int sa = kb & 1;
+      if (!mbar_wait(a_full(sa), uint32_t(kb >> 1) & 1u)) {
+        fail();
+        break;
+      }
+      const uint32_t xa = sA + sa * slot_a;
+      for (int k = 0; k < a.K; ++k, ++ib) {
+        const int s = ib % sp.nb;
+        if (!mbar_wait(b_full(s), uint32_t(ib / sp.nb) & 1u)) {
+          fail();
+          break;
+        }
+        tc_fence_after();
+        const int sh = sp.pad - (a.K - 1 - k) * a.dil;  // x slot row of the tile's first token
+        const uint64_t bd = sw128_desc(sB + s * kBStage);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint64_t ad = sw128_desc(xa + uint32_t(128 * h + sh) * 128u);
+#pragma unroll
+          for (int j = 0; j < BK / UK; ++j)
+            mma_bf16(tmem + uint32_t(h * N), ad + 2 * j, bd + 2 * j, idesc,
+                     (kb > 0 || k > 0 || j > 0) ? 1u : 0u);
+        }
+        mma_commit(b_empty(s));
+      }
+      mma_commit(a_empty(sa));
+    }
+    mma_commit(acc_bar);
+  }
+  __syncwarp();
+
+  // epilogue: warp w reads TMEM lanes 32w .. 32w+31 of both accumulators
+  const bool acc_ok = mbar_wait(acc_bar, 0);
+  tc_fence_after();
+  if (!acc_ok && lane == 0) fail();
+  __syncwarp();
+  if (acc_ok && !*abort_p) {
+#pragma unroll 1
+    for (int h = 0; h < 2; ++h) {
+      const int t = t0 + 128 * h + warp * 32 + lane;
+      uint16_t* orow = a.out + int64_t(bb) * a.o_sb + int64_t(t) * a.o_st;
+      for (int c0 = 0; c0 < N && n0 + c0 < a.Cout; c0 += 32) {  // warp-uniform bound
+        uint32_t r[32];
+        tmem_ld32(tmem + (uint32_t(warp * 32) << 16) + uint32_t(h * N + c0), r);
+        tmem_ld_wait();
+        if (t < a.T) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int oc = n0 + c0 + 8 * q;
+            if (oc >= a.Cout) break;  // Cout is a multiple of 8
+            float v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              float bj = 0.0f;
+              if (a.bias)
+                bj = a.bias_f32 ? __ldg(static_cast<const float*>(a.bias) + int64_t(oc + j) * a.bias_s)
+                                : bf16_to_f32(__ldg(static_cast<const uint16_t*>(a.bias) +
+                                                    int64_t(oc + j) * a.bias_s));
+              v[j] = __uint_as_float(r[8 * q + j]) + bj;
+            }
+            *reinterpret_cast<uint4*>(orow + oc) =
+                make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                           pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kCols);
+  }
+}
+
 // weight [Cout, Cin, K] (any strides, BF16 or FP32) -> packed [K, Cout, Cin] BF16
 // (nearest-even for FP32); consecutive threads write consecutive input channels.
 __global__ void pack_weight_kernel(const void* w, int w_f32, int64_t s_oc, int64_t s_ic, int64_t s_k,
@@ -353,33 +554,48 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+#ifndef CCC_FULLCONV_N
+#define CCC_FULLCONV_N 256  // output channels per tile of the shared-x kernel
+#endif
+constexpr int kSharedN = CCC_FULLCONV_N;
+static_assert(kSharedN == 128 || kSharedN == 256, "N of the shared-x tile");
+constexpr size_t kMaxSmem = 232448;  // 227 KB: the per-block opt-in limit
+
 ContextCache g_attr_done;
 
-cudaError_t smem_attribute() {
+cudaError_t smem_attributes() {
   long long done = 0;
   if (g_attr_done.get(&done) && done) return cudaSuccess;
-  const cudaError_t err = cudaFuncSetAttribute(fullconv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               int(kSmemBytes));
+  cudaError_t err = cudaFuncSetAttribute(fullconv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(kSmemBytes));
+  if (err == cudaSuccess)
+    err = cudaFuncSetAttribute(fullconv_shared_kernel<kSharedN>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, int(kMaxSmem));
   if (err == cudaSuccess) g_attr_done.put(1);
   return err;
+}
+
+// Shared-x plan for this receptive field, or false when the x slot would not
+// fit (then the per-tap kernel serves the call).
+bool shared_plan(int64_t K, int64_t dil, SharedPlan& sp, size_t& smem) {
+  const int64_t P = (K - 1) * dil;
+  const int64_t padr = (P + 15) / 16 * 16;
+  if (padr > 256) return false;
+  sp.pad = int(padr);
+  sp.ra = 256 + sp.pad;
+  const size_t fixed = 1024 + 2 * size_t(sp.ra) * 128 + 256;
+  const size_t bstage = size_t(kSharedN) * BK * 2;
+  if (fixed + 2 * bstage > kMaxSmem) return false;
+  sp.nb = int(std::min<size_t>(8, (kMaxSmem - fixed) / bstage));
+  smem = fixed + size_t(sp.nb) * bstage;
+  return true;
 }
 
 }  // namespace fullconv
 
 cudaError_t launch_fullconv(const FullConvArgs& f, cudaStream_t stream) {
   using namespace fullconv;
-  CUtensorMap mx, mw;
-  // x: dims (Cin, T, B), row strides in bytes (the batch stride of a single
-  // batch row is never used; any legal value serves)
-  const uint64_t xs_t = uint64_t(f.x_st) * 2;
-  const uint64_t xs_b = f.B > 1 ? uint64_t(f.x_sb) * 2 : xs_t * uint64_t(f.T > 0 ? f.T : 1);
-  if (!make_map(&mx, f.x, uint64_t(f.Cin), uint64_t(f.T), uint64_t(f.B), xs_t, xs_b, BM))
-    return cudaErrorInvalidValue;
-  // packed weight: dims (Cin, Cout, K), contiguous
-  if (!make_map(&mw, f.w, uint64_t(f.Cin), uint64_t(f.Cout), uint64_t(f.K), uint64_t(f.Cin) * 2,
-                uint64_t(f.Cin) * 2 * uint64_t(f.Cout), BN))
-    return cudaErrorInvalidValue;
-  const cudaError_t err = smem_attribute();
+  const cudaError_t err = smem_attributes();
   if (err != cudaSuccess) return err;
   Args a{};
   a.out = f.out;
@@ -394,6 +610,28 @@ cudaError_t launch_fullconv(const FullConvArgs& f, cudaStream_t stream) {
   a.dil = f.dil;
   a.n_kblk = (f.Cin + BK - 1) / BK;
   a.status = f.status;
+  // x: dims (Cin, T, B), row strides in bytes (the batch stride of a single
+  // batch row is never used; any legal value serves); packed weight: dims
+  // (Cin, Cout, K), contiguous
+  const uint64_t xs_t = uint64_t(f.x_st) * 2;
+  const uint64_t xs_b = f.B > 1 ? uint64_t(f.x_sb) * 2 : xs_t * uint64_t(f.T > 0 ? f.T : 1);
+  const uint64_t ws_o = uint64_t(f.Cin) * 2, ws_k = ws_o * uint64_t(f.Cout);
+  CUtensorMap mx, mw;
+  SharedPlan sp{};
+  size_t smem = 0;
+  if (shared_plan(f.K, f.dil, sp, smem)) {
+    if (!make_map(&mx, f.x, uint64_t(f.Cin), uint64_t(f.T), uint64_t(f.B), xs_t, xs_b,
+                  uint32_t(sp.ra / 2)) ||
+        !make_map(&mw, f.w, uint64_t(f.Cin), uint64_t(f.Cout), uint64_t(f.K), ws_o, ws_k, kSharedN))
+      return cudaErrorInvalidValue;
+    const dim3 grid(unsigned((f.T + 255) / 256), unsigned((f.Cout + kSharedN - 1) / kSharedN),
+                    unsigned(f.B));
+    return launch_kernel(fullconv_shared_kernel<kSharedN>, grid, dim3(kThreads), smem, stream, false,
+                         mx, mw, a, sp);
+  }
+  if (!make_map(&mx, f.x, uint64_t(f.Cin), uint64_t(f.T), uint64_t(f.B), xs_t, xs_b, BM) ||
+      !make_map(&mw, f.w, uint64_t(f.Cin), uint64_t(f.Cout), uint64_t(f.K), ws_o, ws_k, BN))
+    return cudaErrorInvalidValue;
   const dim3 grid(unsigned((f.T + BM - 1) / BM), unsigned((f.Cout + BN - 1) / BN), unsigned(f.B));
   return launch_kernel(fullconv_kernel, grid, dim3(kThreads), kSmemBytes, stream, false, mx, mw, a);
 }

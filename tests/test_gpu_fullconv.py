@@ -4,7 +4,9 @@ page) on the tensor cores, against the fp64 oracle on the same seeded inputs.
 Tolerance (helpers.assert_fullconv_close): |gpu - ref| <= 1e-3 * sum|terms| +
 2^-8 * |ref|.  Cases span several output tiles along tokens and channels with
 ragged tails (T, Cout, and Cin not multiples of the 128 / 256 / 64 tile),
-receptive fields longer than the sequence, K = 1, FP32 weights and biases
+receptive fields longer than the sequence, receptive fields up to the widest
+x slice the shared-slice kernel holds and beyond it (the per-tap kernel), K = 1,
+FP32 weights and biases
 (the pack rounds the weight to BF16; the oracle takes the rounded weight),
 strided inputs, and the full-size workload on sampled output channels.
 """
@@ -52,6 +54,8 @@ CASES = [
     (2, 256, 512, 256, 1, 1, dict(bias=False)),    # K = 1: a plain matrix product
     (1, 72, 40, 1000, 2, 97, dict(weight_dtype=torch.float32, bias=False)),
     (2, 512, 128, 384, 4, 1, {}),
+    (1, 128, 256, 700, 5, 64, {}),                 # receptive field 256: the widest shared x slice
+    (2, 64, 136, 600, 3, 200, {}),                 # receptive field 400: one x slice per tap
 ]
 
 
