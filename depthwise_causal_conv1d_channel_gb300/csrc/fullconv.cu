@@ -43,9 +43,11 @@ constexpr uint32_t kABytes = BM * BK * 2;  // 16 KB
 constexpr uint32_t kBBytes = BN * BK * 2;  // 32 KB
 constexpr uint32_t kStageBytes = kABytes + kBBytes;
 constexpr uint32_t kTmemCols = BN;  // FP32 accumulator: one column per output channel
-// ring + barriers (2 per stage + 1) + TMEM address + abort flag, plus slack to
-// align the ring to 1024 bytes (the 128-byte swizzle repeats every 8 rows)
-constexpr size_t kSmemBytes = 1024 + size_t(kStages) * kStageBytes + 8 * (2 * kStages + 1) + 16;
+// ring + barriers (2 per stage + 1) + TMEM address + abort flag + the tile's
+// bias, plus slack to align the ring to 1024 bytes (the 128-byte swizzle
+// repeats every 8 rows)
+constexpr size_t kSmemBytes =
+    1024 + size_t(kStages) * kStageBytes + 8 * (2 * kStages + 1) + 16 + size_t(BN) * 4;
 constexpr int kStatusTimeout = 9;  // == CCC_ERR_DEVICE_TIMEOUT
 constexpr uint64_t kWaitLimitNs = 500ull * 1000 * 1000;
 
@@ -92,18 +94,32 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// try_wait that may suspend the thread until the phase completes or `ns`
+// nanoseconds pass: a waiting thread sleeps instead of polling, so it takes no
+// issue slots or shared-memory bandwidth from the producer and MMA threads.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.b32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
 __device__ __forceinline__ uint64_t global_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
 // Waits for the phase of `bar` with the given parity to complete; false when
-// kWaitLimitNs pass first (or after 2^26 polls, should the timer stall).
+// kWaitLimitNs pass first (or after 2^20 sleeps, should the timer stall).
 __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
-  for (uint32_t i = 0; i < (1u << 26); ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
+  for (uint32_t i = 0; i < (1u << 20); ++i) {
+    if (mbar_try_wait_sleep(bar, parity, 1000000u)) return true;
     if (global_ns() - t0 > kWaitLimitNs) return false;
   }
   return false;
@@ -185,6 +201,66 @@ struct Args {
 
 extern __shared__ __align__(1024) uint8_t fc_smem[];
 
+// Bias of the tile's output channels n0 .. n0+N-1 as FP32 in shared memory
+// (zero past Cout or without a bias); every thread of the block calls it.
+template <int N>
+__device__ __forceinline__ void stage_bias(const Args& a, int n0, float* bias_s) {
+  for (int i = threadIdx.x; i < N; i += blockDim.x) {
+    const int oc = n0 + i;
+    float v = 0.0f;
+    if (a.bias && oc < a.Cout)
+      v = a.bias_f32 ? __ldg(static_cast<const float*>(a.bias) + int64_t(oc) * a.bias_s)
+                     : bf16_to_f32(__ldg(static_cast<const uint16_t*>(a.bias) + int64_t(oc) * a.bias_s));
+    bias_s[i] = v;
+  }
+}
+
+// Epilogue of one 128-row accumulator (TMEM columns col0 .. col0+N-1, rows =
+// tokens t_first .. t_first+127): warp w takes TMEM lanes 32w .. 32w+31.  Each
+// thread reads its row's FP32 sums 64 columns at a time (two loads in flight
+// per wait), adds the bias, rounds to BF16 and writes the row piece into the
+// warp's staging rows in shared memory (row stride N*2 + 16 bytes, so the
+// 16-byte writes of the 32 rows spread over all banks); then the warp writes
+// its 32 rows to global memory one row at a time, each row one coalesced
+// N*2-byte store.  `stage` is this warp's 32 staging rows.
+template <int N>
+__device__ __forceinline__ void store_accumulator(const Args& a, uint32_t tmem, uint32_t col0,
+                                                  int t_first, int n0, int bb, const float* bias_s,
+                                                  uint8_t* stage) {
+  constexpr int kRowBytes = N * 2 + 16;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ncols = a.Cout - n0 < N ? a.Cout - n0 : N;  // a multiple of 8
+  for (int c0 = 0; c0 < N && c0 < ncols; c0 += 64) {  // warp-uniform bounds
+    uint32_t r0[32], r1[32];
+    const uint32_t taddr = tmem + (uint32_t(warp * 32) << 16) + col0 + uint32_t(c0);
+    tmem_ld32(taddr, r0);
+    tmem_ld32(taddr + 32, r1);
+    tmem_ld_wait();
+    uint8_t* row = stage + lane * kRowBytes + c0 * 2;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const uint32_t* r = q < 4 ? r0 + 8 * q : r1 + 8 * (q - 4);
+      const float* bq = bias_s + c0 + 8 * q;
+      float v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = __uint_as_float(r[j]) + bq[j];
+      *reinterpret_cast<uint4*>(row + 16 * q) =
+          make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                     pack_bf16x2(v[6], v[7]));
+    }
+  }
+  __syncwarp();
+  for (int rr = 0; rr < 32; ++rr) {
+    const int t = t_first + warp * 32 + rr;
+    if (t >= a.T) break;  // rows past T are the tile's tail
+    uint16_t* orow = a.out + int64_t(bb) * a.o_sb + int64_t(t) * a.o_st + n0;
+    const uint8_t* srow = stage + rr * kRowBytes;
+    for (int cc = lane * 8; cc < ncols; cc += 256)
+      *reinterpret_cast<uint4*>(orow + cc) = *reinterpret_cast<const uint4*>(srow + cc * 2);
+  }
+  __syncwarp();
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     fullconv_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
                     Args a) {
@@ -205,6 +281,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* gbase = fc_smem + pad + (bars - sA) + 8 * (2 * kStages + 1);  // generic view of the slot
   volatile uint32_t* tmem_slot_p = reinterpret_cast<volatile uint32_t*>(gbase);
   volatile int* abort_p = reinterpret_cast<volatile int*>(gbase + 4);
+  float* bias_s = reinterpret_cast<float*>(gbase + 16);  // BN floats
+  stage_bias<BN>(a, n0, bias_s);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -277,40 +355,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncwarp();
 
-  // epilogue: warp w owns TMEM lanes 32w .. 32w+31, i.e. tokens t0 + 32w + lane
+  // epilogue: the ring is idle now; warp w stages its rows at the ring's start
   const bool acc_ok = mbar_wait(acc_bar, 0);
   tc_fence_after();
   if (!acc_ok && lane == 0) fail();
   __syncwarp();
-  if (acc_ok && !*abort_p) {
-    const int t = t0 + warp * 32 + lane;
-    uint16_t* orow = a.out + int64_t(bb) * a.o_sb + int64_t(t) * a.o_st;
-    for (int c0 = 0; c0 < BN && n0 + c0 < a.Cout; c0 += 32) {  // warp-uniform bound
-      uint32_t r[32];
-      tmem_ld32(tmem + (uint32_t(warp * 32) << 16) + uint32_t(c0), r);
-      tmem_ld_wait();
-      if (t < a.T) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int oc = n0 + c0 + 8 * q;
-          if (oc >= a.Cout) break;  // Cout is a multiple of 8
-          float v[8];
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            float bj = 0.0f;
-            if (a.bias)
-              bj = a.bias_f32 ? __ldg(static_cast<const float*>(a.bias) + int64_t(oc + j) * a.bias_s)
-                              : bf16_to_f32(__ldg(static_cast<const uint16_t*>(a.bias) +
-                                                  int64_t(oc + j) * a.bias_s));
-            v[j] = __uint_as_float(r[8 * q + j]) + bj;
-          }
-          const uint4 pk = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
-                                      pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
-          *reinterpret_cast<uint4*>(orow + oc) = pk;
-        }
-      }
-    }
-  }
+  if (acc_ok && !*abort_p)
+    store_accumulator<BN>(a, tmem, 0, t0, n0, bb, bias_s, fc_smem + pad + warp * 32 * (BN * 2 + 16));
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -363,6 +414,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* gslot = fc_smem + pad + (tmem_slot - sA);
   volatile uint32_t* tmem_slot_p = reinterpret_cast<volatile uint32_t*>(gslot);
   volatile int* abort_p = reinterpret_cast<volatile int*>(gslot + 4);
+  float* bias_s = reinterpret_cast<float*>(gslot + 16);  // N floats
+  stage_bias<N>(a, n0, bias_s);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
@@ -465,42 +518,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncwarp();
 
-  // epilogue: warp w reads TMEM lanes 32w .. 32w+31 of both accumulators
+  // epilogue: the ring is idle now (every load was consumed by an MMA that
+  // has completed); warp w stages its rows at the ring's start
   const bool acc_ok = mbar_wait(acc_bar, 0);
   tc_fence_after();
   if (!acc_ok && lane == 0) fail();
   __syncwarp();
   if (acc_ok && !*abort_p) {
-#pragma unroll 1
-    for (int h = 0; h < 2; ++h) {
-      const int t = t0 + 128 * h + warp * 32 + lane;
-      uint16_t* orow = a.out + int64_t(bb) * a.o_sb + int64_t(t) * a.o_st;
-      for (int c0 = 0; c0 < N && n0 + c0 < a.Cout; c0 += 32) {  // warp-uniform bound
-        uint32_t r[32];
-        tmem_ld32(tmem + (uint32_t(warp * 32) << 16) + uint32_t(h * N + c0), r);
-        tmem_ld_wait();
-        if (t < a.T) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int oc = n0 + c0 + 8 * q;
-            if (oc >= a.Cout) break;  // Cout is a multiple of 8
-            float v[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              float bj = 0.0f;
-              if (a.bias)
-                bj = a.bias_f32 ? __ldg(static_cast<const float*>(a.bias) + int64_t(oc + j) * a.bias_s)
-                                : bf16_to_f32(__ldg(static_cast<const uint16_t*>(a.bias) +
-                                                    int64_t(oc + j) * a.bias_s));
-              v[j] = __uint_as_float(r[8 * q + j]) + bj;
-            }
-            *reinterpret_cast<uint4*>(orow + oc) =
-                make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
-                           pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
-          }
-        }
-      }
-    }
+    uint8_t* stage = fc_smem + pad + warp * 32 * (N * 2 + 16);
+    store_accumulator<N>(a, tmem, 0, t0, n0, bb, bias_s, stage);
+    store_accumulator<N>(a, tmem, uint32_t(N), t0 + 128, n0, bb, bias_s, stage);
   }
   tc_fence_before();
   __syncthreads();
@@ -583,12 +610,14 @@ bool shared_plan(int64_t K, int64_t dil, SharedPlan& sp, size_t& smem) {
   if (padr > 256) return false;
   sp.pad = int(padr);
   sp.ra = 256 + sp.pad;
-  const size_t fixed = 1024 + 2 * size_t(sp.ra) * 128 + 256;
+  // slack to align the ring, the x slots, barriers and TMEM address, the bias
+  const size_t fixed = 1024 + 2 * size_t(sp.ra) * 128 + 256 + size_t(kSharedN) * 4;
   const size_t bstage = size_t(kSharedN) * BK * 2;
   if (fixed + 2 * bstage > kMaxSmem) return false;
   sp.nb = int(std::min<size_t>(8, (kMaxSmem - fixed) / bstage));
   smem = fixed + size_t(sp.nb) * bstage;
-  return true;
+  // the epilogue stages 128 rows of N*2 + 16 bytes in the ring
+  return 2 * size_t(sp.ra) * 128 + size_t(sp.nb) * bstage >= size_t(128) * (kSharedN * 2 + 16);
 }
 
 }  // namespace fullconv
