@@ -708,6 +708,8 @@ ccc_status ccc_fullconv1d_fwd(const ccc_tensor* x, const ccc_tensor* packed_weig
   if (K > 1024 || (K - 1) * int64_t(dilation) > INT32_MAX / 2 || T > INT32_MAX / 2 ||
       B > 65535 || (Cout + 255) / 256 > 65535 || Cin > (int64_t(1) << 24))
     return CCC_ERR_UNSUPPORTED;
+  // the persistent kernel numbers its 256 x 256 tiles with int
+  if (B * ((T + 255) / 256) * ((Cout + 255) / 256) > INT32_MAX / 2) return CCC_ERR_UNSUPPORTED;
   for (const ccc_tensor* t : {x, out}) {
     const int64_t sb = t->shape[0] > 1 ? t->stride[0] : 0;
     const int64_t st = t->shape[2] > 1 ? t->stride[2] : 0;

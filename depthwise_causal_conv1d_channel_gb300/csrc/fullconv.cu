@@ -8,7 +8,10 @@
 //
 // a sum of K GEMMs whose A operand is x shifted along tokens.  This is a dense
 // contraction (2 * Cin * K FLOPs per output), so it runs as an implicit GEMM
-// on tcgen05: one CTA per output tile of 128 tokens x 256 output channels of
+// on tcgen05.  Two kernels: the persistent kernel further below serves
+// receptive fields up to 256 tokens, loading one x slice per block of input
+// channels for all taps; the per-tap kernel first, for longer receptive
+// fields, runs one CTA per output tile of 128 tokens x 256 output channels of
 // one batch row.  For each (tap, block of 64 input channels) a TMA load brings
 // the 128 x 64 slice of x starting at token t0 - (K-1-k)*dil (coordinates
 // before token 0 read as zeros: the causal padding needs no padded copy) and
@@ -115,7 +118,10 @@ __device__ __forceinline__ uint64_t global_ns() {
 }
 // Waits for the phase of `bar` with the given parity to complete; false when
 // kWaitLimitNs pass first (or after 2^20 sleeps, should the timer stall).
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// Inlined: as an out-of-line call it made the producer and MMA threads save
+// and restore registers around every wait, which slowed the MMA stream of a
+// 256 x 256 tile from 43 to 51 us.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (uint32_t i = 0; i < (1u << 20); ++i) {
@@ -355,12 +361,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncwarp();
 
-  // epilogue: the ring is idle now; warp w stages its rows at the ring's start
-  const bool acc_ok = mbar_wait(acc_bar, 0);
+  // epilogue: the ring is idle now; warp w stages its rows at the ring's start.
+  // Lane 0 waits and tells the warp, so the warp-wide tcgen05.ld is reached by
+  // all lanes or by none.
+  int st = 0;
+  if (lane == 0) {
+    st = mbar_wait(acc_bar, 0) ? (*abort_p ? 1 : 0) : 2;
+    if (st == 2) fail();
+  }
+  st = __shfl_sync(0xffffffffu, st, 0);
   tc_fence_after();
-  if (!acc_ok && lane == 0) fail();
-  __syncwarp();
-  if (acc_ok && !*abort_p)
+  if (st == 0)
     store_accumulator<BN>(a, tmem, 0, t0, n0, bb, bias_s, fc_smem + pad + warp * 32 * (BN * 2 + 16));
   tc_fence_before();
   __syncthreads();
@@ -370,19 +381,32 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// ---- one x tile shared by all taps --------------------------------------------------
+// ---- persistent kernel: one x slice per channel block shared by all taps -----------
 //
 // The taps of one output tile read the same x rows shifted by multiples of the
-// dilation, so instead of one 128-row x slice per tap, the kernel below loads
-// per block of 64 input channels ONE slice of RA = 256 + pad rows (tokens
-// t0 - pad .. t0 + 255, pad >= (K-1)*dil rounded up to 16) and lets tap k read
-// it from row pad - (K-1-k)*dil on: the MMA's A descriptor simply starts at that
-// row (see sw128_desc).  A tile
-// is 256 tokens -- two M-128 accumulators sharing each weight slice -- by N
-// output channels, so per (channel block, tap) the tensor cores do 2 x 128 x N
-// x 64 multiply-adds for N x 128 bytes of weight plus a quarter of the x slice:
-// about half the bytes per FLOP of the per-tap kernel above.  x slices take two
-// ring slots, weight slices a ring of NB stages.
+// dilation, so instead of one x slice per tap, the kernel below loads per block
+// of 64 input channels ONE slice of RA = 256 + pad rows (tokens t0 - pad ..
+// t0 + 255, pad >= (K-1)*dil rounded up to 16) and lets tap k read it from row
+// pad - (K-1-k)*dil on: the MMA's A descriptor simply starts at that row (see
+// sw128_desc).  A tile is 256 tokens -- two M-128 accumulators sharing each
+// weight slice -- by N output channels, so per (channel block, tap) the tensor
+// cores do 2 x 128 x N x 64 multiply-adds for N x 128 bytes of weight plus a
+// quarter of the x slice: about half the bytes per FLOP of the per-tap kernel.
+//
+// One CTA runs per SM and walks a static list of work items: whole tiles, then,
+// when the tiles do not fill the last wave, the remaining tiles cut into halves
+// of 128 tokens (one accumulator each), so the last wave is shorter.  (A half
+// keeps all of the tile's weight bytes for half the MMAs, so it takes about
+// three quarters of a tile's time, bound by L2 reads; halves of N / 2 output
+// channels measured slower still, the N / 2 MMAs running below the tensor
+// cores' rate.)
+//
+// Warp 0 issues the TMA loads, warp 1 the MMAs, warps 2-9 drain the
+// accumulators: warp w reads TMEM lanes 32 (w % 4) .. +31 of accumulator
+// (w - 2) / 4, adds the bias, keeps the row as packed BF16 in registers and
+// releases the tensor memory before it stores, so the next item's MMAs run
+// while the rows go out.  The loads of the next item fill the ring while the
+// MMAs of this one finish.
 
 struct SharedPlan {
   int ra;    // rows of an x slot (multiple of 16, at most 512)
@@ -390,32 +414,78 @@ struct SharedPlan {
   int nb;    // weight stages
 };
 
+// Work items: [0, n_main) whole tiles (tile = item), [n_main, n_items) half
+// tiles (tile n_main + j / 2, tokens 128 (j % 2) on; j = item - n_main).
+// Tiles are numbered token tile fastest, then output-channel tile, then row.
+struct Sched {
+  int n_tb, n_ob;
+  int n_main, n_items;
+};
+
+struct Item {
+  int t0, n0, bb, nh;  // first token, first output channel, batch row, accumulators (M-128 halves)
+};
+
 template <int N>
-__global__ void __launch_bounds__(kThreads, 1)
-    fullconv_shared_kernel(const __grid_constant__ CUtensorMap map_x,
-                           const __grid_constant__ CUtensorMap map_w, Args a, SharedPlan sp) {
+__device__ __forceinline__ Item item_at(const Sched& sc, int w) {
+  int tile = w, t_off = 0, nh = 2;
+  if (w >= sc.n_main) {
+    const int j = w - sc.n_main;
+    tile = sc.n_main + (j >> 1);
+    t_off = 128 * (j & 1);
+    nh = 1;
+  }
+  const int tb = tile % sc.n_tb, r = tile / sc.n_tb;
+  return Item{tb * 256 + t_off, (r % sc.n_ob) * N, r / sc.n_ob, nh};
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+constexpr int kPThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue
+constexpr int kEpiWarps = 8;
+constexpr int kChunk = 32;                            // columns per staged store round
+constexpr uint32_t kStageRow = kChunk * 2 + 16;       // staging row stride: banks spread
+constexpr uint32_t kStageWarp = 32 * kStageRow;       // one warp's staging rows
+
+template <int N>
+constexpr size_t persistent_fixed_smem(int ra) {
+  // align slack, two x slots, epilogue staging, per-warp bias copies,
+  // barriers + TMEM address + abort flag
+  return 1024 + 2 * size_t(ra) * 128 + kEpiWarps * size_t(kStageWarp) + kEpiWarps * size_t(N) * 4 + 256;
+}
+
+template <int N>
+__global__ void __launch_bounds__(kPThreads, 1)
+    fullconv_persistent_kernel(const __grid_constant__ CUtensorMap map_x,
+                               const __grid_constant__ CUtensorMap map_w, Args a, SharedPlan sp,
+                               Sched sc) {
   constexpr uint32_t kBStage = uint32_t(N) * BK * 2;
   constexpr uint32_t kCols = 2 * N;  // two accumulators of N FP32 columns
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t0 = blockIdx.x * 256, n0 = blockIdx.y * N, bb = blockIdx.z;
   const uint32_t slot_a = uint32_t(sp.ra) * 128;
 
+  // shared layout: x slots, weight stages, staging rows, bias copies, barriers
   const uint32_t raw = smem_u32(fc_smem);
   const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
   const uint32_t sA = raw + pad;
   const uint32_t sB = sA + 2 * slot_a;
-  const uint32_t bars = sB + uint32_t(sp.nb) * kBStage;
+  const uint32_t sStage = sB + uint32_t(sp.nb) * kBStage;
+  const uint32_t sBias = sStage + kEpiWarps * kStageWarp;
+  const uint32_t bars = sBias + kEpiWarps * N * 4;
   auto a_full = [&](int i) { return bars + 8u * i; };
   auto a_empty = [&](int i) { return bars + 8u * (2 + i); };
   auto b_full = [&](int i) { return bars + 8u * (4 + i); };
   auto b_empty = [&](int i) { return bars + 8u * (4 + sp.nb + i); };
-  const uint32_t acc_bar = bars + 8u * (4 + 2 * sp.nb);
-  const uint32_t tmem_slot = acc_bar + 8;
-  uint8_t* gslot = fc_smem + pad + (tmem_slot - sA);
-  volatile uint32_t* tmem_slot_p = reinterpret_cast<volatile uint32_t*>(gslot);
-  volatile int* abort_p = reinterpret_cast<volatile int*>(gslot + 4);
-  float* bias_s = reinterpret_cast<float*>(gslot + 16);  // N floats
-  stage_bias<N>(a, n0, bias_s);
+  const uint32_t acc_full = bars + 8u * (4 + 2 * sp.nb);
+  const uint32_t acc_empty = acc_full + 8;
+  const uint32_t mma_done = acc_full + 16;
+  const uint32_t tmem_slot = acc_full + 24;
+  uint8_t* const gsm = fc_smem + pad;  // generic view of sA
+  auto generic = [&](uint32_t s) { return gsm + (s - sA); };
+  volatile uint32_t* tmem_slot_p = reinterpret_cast<volatile uint32_t*>(generic(tmem_slot));
+  volatile int* abort_p = reinterpret_cast<volatile int*>(generic(tmem_slot) + 4);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
@@ -426,7 +496,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(b_full(i), 1);
       mbar_init(b_empty(i), 1);
     }
-    mbar_init(acc_bar, 1);
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, kEpiWarps);
+    mbar_init(mma_done, 1);
     *abort_p = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     prefetch_map(&map_x);
@@ -446,89 +518,169 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (a.status) atomicCAS(a.status, 0, kStatusTimeout);
   };
 
-  // Tiles start their walk over the channel blocks at different blocks, so the
-  // CTAs running at once read different weight slices instead of all asking
-  // L2 for the same lines (the sum's order is fixed per tile).
-  const int rot = int((blockIdx.x + blockIdx.y + blockIdx.z) % unsigned(a.n_kblk));
-
   if (warp == 0 && lane == 0) {
     // producer: per channel block one x slice (two boxes of ra / 2 rows),
-    // then the K weight slices
+    // then the K weight slices; runs ahead across items as far as the ring allows
     int ia = 0, ib = 0;
-    for (int kb = 0; kb < a.n_kblk && !*abort_p; ++kb) {
-      const int sa = kb & 1;
-      const int cb = (kb + rot) % a.n_kblk;  // the channel block
-      if (!mbar_wait(a_empty(sa), (uint32_t(kb >> 1) & 1u) ^ 1u)) {
-        fail();
-        break;
-      }
-      mbar_expect_tx(a_full(sa), slot_a);
-      const uint32_t dst = sA + sa * slot_a;
-      tma_load_3d(dst, &map_x, a_full(sa), cb * BK, t0 - sp.pad, bb);
-      tma_load_3d(dst + slot_a / 2, &map_x, a_full(sa), cb * BK, t0 - sp.pad + sp.ra / 2, bb);
-      ++ia;
-      for (int k = 0; k < a.K; ++k, ++ib) {
-        const int s = ib % sp.nb;
-        if (!mbar_wait(b_empty(s), (uint32_t(ib / sp.nb) & 1u) ^ 1u)) {
-          fail();
+    bool ok = true;
+    for (int w = blockIdx.x; ok && w < sc.n_items; w += gridDim.x) {
+      const Item it = item_at<N>(sc, w);
+      for (int kb = 0; ok && kb < a.n_kblk; ++kb) {
+        const int sa = ia & 1;
+        if (!mbar_wait(a_empty(sa), (uint32_t(ia >> 1) & 1u) ^ 1u) || *abort_p) {
+          ok = false;
           break;
         }
-        mbar_expect_tx(b_full(s), kBStage);
-        tma_load_3d(sB + s * kBStage, &map_w, b_full(s), cb * BK, n0, k);
+        mbar_expect_tx(a_full(sa), slot_a);
+        const uint32_t dst = sA + sa * slot_a;
+        tma_load_3d(dst, &map_x, a_full(sa), kb * BK, it.t0 - sp.pad, it.bb);
+        tma_load_3d(dst + slot_a / 2, &map_x, a_full(sa), kb * BK, it.t0 - sp.pad + sp.ra / 2, it.bb);
+        ++ia;
+        for (int k = 0; k < a.K; ++k) {
+          const int s = ib % sp.nb;
+          if (!mbar_wait(b_empty(s), (uint32_t(ib / sp.nb) & 1u) ^ 1u) || *abort_p) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(b_full(s), kBStage);
+          tma_load_3d(sB + s * kBStage, &map_w, b_full(s), kb * BK, it.n0, k);
+          ++ib;
+        }
       }
     }
-    if (*abort_p) {  // let the loads in flight land before the CTA leaves
+    if (!ok) {  // let the loads in flight land before the CTA leaves
+      if (!*abort_p) fail();
       for (int i = ia - 2 < 0 ? 0 : ia - 2; i < ia; ++i) mbar_wait(a_full(i & 1), uint32_t(i >> 1) & 1u);
       for (int i = ib - sp.nb < 0 ? 0 : ib - sp.nb; i < ib; ++i)
         mbar_wait(b_full(i % sp.nb), uint32_t(i / sp.nb) & 1u);
     }
   } else if (warp == 1 && lane == 0) {
     // MMA issuer
-    int ib = 0;
     constexpr uint32_t idesc = idesc_m128(N);
-    for (int kb = 0; kb < a.n_kblk && !*abort_p; ++kb) {
-      const int sa = kb & 1;
-      if (!mbar_wait(a_full(sa), uint32_t(kb >> 1) & 1u)) {
-        fail();
+    int ia = 0, ib = 0, n = 0;
+    bool ok = true;
+    for (int w = blockIdx.x; ok && w < sc.n_items; w += gridDim.x, ++n) {
+      const Item it = item_at<N>(sc, w);
+      // the epilogue has read the previous item's accumulators out
+      if (!mbar_wait(acc_empty, (uint32_t(n) & 1u) ^ 1u) || *abort_p) {
+        ok = false;
         break;
       }
-      const uint32_t xa = sA + sa * slot_a;
-      for (int k = 0; k < a.K; ++k, ++ib) {
-        const int s = ib % sp.nb;
-        if (!mbar_wait(b_full(s), uint32_t(ib / sp.nb) & 1u)) {
-          fail();
+      tc_fence_after();
+      for (int kb = 0; ok && kb < a.n_kblk; ++kb) {
+        const int sa = ia & 1;
+        if (!mbar_wait(a_full(sa), uint32_t(ia >> 1) & 1u) || *abort_p) {
+          ok = false;
           break;
         }
-        tc_fence_after();
-        const int sh = sp.pad - (a.K - 1 - k) * a.dil;  // x slot row of the tile's first token
-        const uint64_t bd = sw128_desc(sB + s * kBStage);
+        const uint32_t xa = sA + sa * slot_a;
+        for (int k = 0; k < a.K; ++k) {
+          const int s = ib % sp.nb;
+          if (!mbar_wait(b_full(s), uint32_t(ib / sp.nb) & 1u) || *abort_p) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const int sh = sp.pad - (a.K - 1 - k) * a.dil;  // x slot row of the item's first token
+          const uint64_t bd = sw128_desc(sB + s * kBStage);
+          for (int h = 0; h < it.nh; ++h) {
+            const uint64_t ad = sw128_desc(xa + uint32_t(128 * h + sh) * 128u);
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const uint64_t ad = sw128_desc(xa + uint32_t(128 * h + sh) * 128u);
-#pragma unroll
-          for (int j = 0; j < BK / UK; ++j)
-            mma_bf16(tmem + uint32_t(h * N), ad + 2 * j, bd + 2 * j, idesc,
-                     (kb > 0 || k > 0 || j > 0) ? 1u : 0u);
+            for (int j = 0; j < BK / UK; ++j)
+              mma_bf16(tmem + uint32_t(h * N), ad + 2 * j, bd + 2 * j, idesc,
+                       (kb > 0 || k > 0 || j > 0) ? 1u : 0u);
+          }
+          mma_commit(b_empty(s));
+          ++ib;
         }
-        mma_commit(b_empty(s));
+        if (!ok) break;
+        mma_commit(a_empty(sa));
+        ++ia;
       }
-      mma_commit(a_empty(sa));
+      if (ok) mma_commit(acc_full);
     }
-    mma_commit(acc_bar);
+    if (!ok && !*abort_p) fail();
+    // every MMA issued above completes before the tensor memory is freed
+    mma_commit(mma_done);
+    if (!mbar_wait(mma_done, 0)) fail();
+  } else if (warp >= 2) {
+    // epilogue: warp w drains TMEM lanes 32 (w % 4) .. +31 of accumulator (w - 2) / 4
+    const int e = warp - 2, q = warp & 3, h = e >> 2;
+    uint8_t* const stage = generic(sStage) + e * kStageWarp;
+    float* const bias_w = reinterpret_cast<float*>(generic(sBias)) + e * N;
+    int n = 0;
+    for (int w = blockIdx.x; w < sc.n_items; w += gridDim.x, ++n) {
+      const Item it = item_at<N>(sc, w);
+      // this warp's copy of the item's bias (zero past Cout or without one)
+      __syncwarp();
+      for (int i = lane; i < N; i += 32) {
+        const int oc = it.n0 + i;
+        float v = 0.0f;
+        if (a.bias && oc < a.Cout)
+          v = a.bias_f32 ? __ldg(static_cast<const float*>(a.bias) + int64_t(oc) * a.bias_s)
+                         : bf16_to_f32(__ldg(static_cast<const uint16_t*>(a.bias) + int64_t(oc) * a.bias_s));
+        bias_w[i] = v;
+      }
+      __syncwarp();
+      // lane 0 waits and tells the warp, so the warp-wide tcgen05.ld below is
+      // reached by all lanes or by none
+      int st = 0;
+      if (lane == 0) {
+        st = mbar_wait(acc_full, uint32_t(n) & 1u) ? (*abort_p ? 1 : 0) : 2;
+        if (st == 2) fail();
+      }
+      st = __shfl_sync(0xffffffffu, st, 0);
+      if (st) break;
+      tc_fence_after();
+      uint32_t pk[N / 2];  // the row as packed BF16
+      if (h < it.nh) {
+        const uint32_t taddr = tmem + (uint32_t(q * 32) << 16) + uint32_t(h * N);
+#pragma unroll
+        for (int c = 0; c < N; c += 32) {
+          uint32_t r[32];
+          tmem_ld32(taddr + uint32_t(c), r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            pk[c / 2 + j] = pack_bf16x2(__uint_as_float(r[2 * j]) + bias_w[c + 2 * j],
+                                        __uint_as_float(r[2 * j + 1]) + bias_w[c + 2 * j + 1]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty);  // the accumulators may be overwritten
+      if (h >= it.nh) continue;
+      // rows t_row .. t_row + 31, kChunk columns per round through the staging
+      // rows: each lane writes its row piece, then every store instruction
+      // writes 8 whole row pieces of kChunk * 2 bytes
+      const int t_row = it.t0 + h * 128 + q * 32;
+      const int ncols = a.Cout - it.n0 < N ? a.Cout - it.n0 : N;  // a multiple of 8
+      uint16_t* const obase = a.out + int64_t(it.bb) * a.o_sb + it.n0;
+#pragma unroll
+      for (int c = 0; c < N; c += kChunk) {
+        if (c >= ncols) break;
+        uint8_t* row = stage + lane * kStageRow;
+#pragma unroll
+        for (int p = 0; p < kChunk / 8; ++p)
+          *reinterpret_cast<uint4*>(row + 16 * p) =
+              make_uint4(pk[c / 2 + 4 * p], pk[c / 2 + 4 * p + 1], pk[c / 2 + 4 * p + 2],
+                         pk[c / 2 + 4 * p + 3]);
+        __syncwarp();
+        constexpr int kPieces = kChunk / 8;        // 16-byte pieces per row piece
+        constexpr int kRowsPerStore = 32 / kPieces;
+#pragma unroll
+        for (int i = 0; i < 32 / kRowsPerStore; ++i) {
+          const int rr = i * kRowsPerStore + lane / kPieces, pc = lane % kPieces;
+          const int t = t_row + rr, col = c + pc * 8;
+          if (t < a.T && col < ncols)
+            *reinterpret_cast<uint4*>(obase + int64_t(t) * a.o_st + col) =
+                *reinterpret_cast<const uint4*>(stage + rr * kStageRow + pc * 16);
+        }
+        __syncwarp();
+      }
+    }
   }
   __syncwarp();
-
-  // epilogue: the ring is idle now (every load was consumed by an MMA that
-  // has completed); warp w stages its rows at the ring's start
-  const bool acc_ok = mbar_wait(acc_bar, 0);
-  tc_fence_after();
-  if (!acc_ok && lane == 0) fail();
-  __syncwarp();
-  if (acc_ok && !*abort_p) {
-    uint8_t* stage = fc_smem + pad + warp * 32 * (N * 2 + 16);
-    store_accumulator<N>(a, tmem, 0, t0, n0, bb, bias_s, stage);
-    store_accumulator<N>(a, tmem, uint32_t(N), t0 + 128, n0, bb, bias_s, stage);
-  }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -582,13 +734,14 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64
 }
 
 #ifndef CCC_FULLCONV_N
-#define CCC_FULLCONV_N 256  // output channels per tile of the shared-x kernel
+#define CCC_FULLCONV_N 256  // output channels per tile of the persistent kernel
 #endif
 constexpr int kSharedN = CCC_FULLCONV_N;
-static_assert(kSharedN == 128 || kSharedN == 256, "N of the shared-x tile");
+static_assert(kSharedN == 128 || kSharedN == 256, "N of the persistent kernel's tile");
 constexpr size_t kMaxSmem = 232448;  // 227 KB: the per-block opt-in limit
 
 ContextCache g_attr_done;
+ContextCache g_sm_count;
 
 cudaError_t smem_attributes() {
   long long done = 0;
@@ -596,28 +749,57 @@ cudaError_t smem_attributes() {
   cudaError_t err = cudaFuncSetAttribute(fullconv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(kSmemBytes));
   if (err == cudaSuccess)
-    err = cudaFuncSetAttribute(fullconv_shared_kernel<kSharedN>,
+    err = cudaFuncSetAttribute(fullconv_persistent_kernel<kSharedN>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, int(kMaxSmem));
   if (err == cudaSuccess) g_attr_done.put(1);
   return err;
 }
 
-// Shared-x plan for this receptive field, or false when the x slot would not
-// fit (then the per-tap kernel serves the call).
+cudaError_t sm_count(int* n) {
+  long long v = 0;
+  if (g_sm_count.get(&v) && v > 0) {
+    *n = int(v);
+    return cudaSuccess;
+  }
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err == cudaSuccess) err = cudaDeviceGetAttribute(n, cudaDevAttrMultiProcessorCount, dev);
+  if (err == cudaSuccess) g_sm_count.put(*n);
+  return err;
+}
+
+// Persistent-kernel plan for this receptive field, or false when the x slots
+// and at least two weight stages would not fit (then the per-tap kernel
+// serves the call).
 bool shared_plan(int64_t K, int64_t dil, SharedPlan& sp, size_t& smem) {
   const int64_t P = (K - 1) * dil;
   const int64_t padr = (P + 15) / 16 * 16;
   if (padr > 256) return false;
   sp.pad = int(padr);
   sp.ra = 256 + sp.pad;
-  // slack to align the ring, the x slots, barriers and TMEM address, the bias
-  const size_t fixed = 1024 + 2 * size_t(sp.ra) * 128 + 256 + size_t(kSharedN) * 4;
+  const size_t fixed = persistent_fixed_smem<kSharedN>(sp.ra);
   const size_t bstage = size_t(kSharedN) * BK * 2;
   if (fixed + 2 * bstage > kMaxSmem) return false;
   sp.nb = int(std::min<size_t>(8, (kMaxSmem - fixed) / bstage));
   smem = fixed + size_t(sp.nb) * bstage;
-  // the epilogue stages 128 rows of N*2 + 16 bytes in the ring
-  return 2 * size_t(sp.ra) * 128 + size_t(sp.nb) * bstage >= size_t(128) * (kSharedN * 2 + 16);
+  return true;
+}
+
+// Whole tiles fill full waves of `grid_max` CTAs; when the rest would fill at
+// most half a wave, it is cut into half tiles that all run in one last round.
+Sched make_sched(int64_t T, int64_t Cout, int64_t B, int grid_max) {
+  Sched sc{};
+  sc.n_tb = int((T + 255) / 256);
+  sc.n_ob = int((Cout + kSharedN - 1) / kSharedN);
+  const int64_t n_tiles = int64_t(sc.n_tb) * sc.n_ob * B;
+  const int64_t r = n_tiles % grid_max;
+  if (r != 0 && 2 * r <= grid_max) {
+    sc.n_main = int(n_tiles - r);
+    sc.n_items = int(n_tiles + r);
+  } else {
+    sc.n_main = sc.n_items = int(n_tiles);
+  }
+  return sc;
 }
 
 }  // namespace fullconv
@@ -653,10 +835,13 @@ cudaError_t launch_fullconv(const FullConvArgs& f, cudaStream_t stream) {
                   uint32_t(sp.ra / 2)) ||
         !make_map(&mw, f.w, uint64_t(f.Cin), uint64_t(f.Cout), uint64_t(f.K), ws_o, ws_k, kSharedN))
       return cudaErrorInvalidValue;
-    const dim3 grid(unsigned((f.T + 255) / 256), unsigned((f.Cout + kSharedN - 1) / kSharedN),
-                    unsigned(f.B));
-    return launch_kernel(fullconv_shared_kernel<kSharedN>, grid, dim3(kThreads), smem, stream, false,
-                         mx, mw, a, sp);
+    int nsm = 0;
+    const cudaError_t e2 = sm_count(&nsm);
+    if (e2 != cudaSuccess) return e2;
+    const Sched sc = make_sched(f.T, f.Cout, f.B, nsm);
+    const unsigned grid = unsigned(std::min(nsm, sc.n_items));
+    return launch_kernel(fullconv_persistent_kernel<kSharedN>, dim3(grid), dim3(kPThreads), smem, stream,
+                         false, mx, mw, a, sp, sc);
   }
   if (!make_map(&mx, f.x, uint64_t(f.Cin), uint64_t(f.T), uint64_t(f.B), xs_t, xs_b, BM) ||
       !make_map(&mw, f.w, uint64_t(f.Cin), uint64_t(f.Cout), uint64_t(f.K), ws_o, ws_k, BN))

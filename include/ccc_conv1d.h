@@ -265,7 +265,11 @@ ccc_status ccc_conv1d_update(const ccc_tensor *x, const ccc_tensor *conv_state,
  *
  * B == 0 or T == 0 computes nothing.  Limits (else CCC_ERR_UNSUPPORTED): B and
  * ceil(Cout / 256) at most 65535, K at most 1024, (K-1)*dilation and T below
- * 2^30.
+ * 2^30, B * ceil(T / 256) * ceil(Cout / 256) below 2^30.
+ *
+ * The call launches one CTA per SM (receptive field (K-1)*dilation up to 256
+ * tokens; longer ones take one CTA per tile of 128 tokens x 256 channels), so
+ * it occupies the whole GPU while it runs.
  */
 ccc_status ccc_fullconv1d_pack_weight(const ccc_tensor *weight, const ccc_tensor *packed,
                                       cudaStream_t stream);

@@ -5,7 +5,8 @@ Tolerance (helpers.assert_fullconv_close): |gpu - ref| <= 1e-3 * sum|terms| +
 2^-8 * |ref|.  Cases span several output tiles along tokens and channels with
 ragged tails (T, Cout, and Cin not multiples of the 128 / 256 / 64 tile),
 receptive fields longer than the sequence, receptive fields up to the widest
-x slice the shared-slice kernel holds and beyond it (the per-tap kernel), K = 1,
+x slice the persistent kernel holds and beyond it (the per-tap kernel), K = 1,
+calls of hundreds of tiles (several per CTA, whole and half tiles),
 FP32 weights and biases
 (the pack rounds the weight to BF16; the oracle takes the rounded weight),
 strided inputs, and the full-size workload on sampled output channels.
@@ -54,7 +55,7 @@ CASES = [
     (2, 256, 512, 256, 1, 1, dict(bias=False)),    # K = 1: a plain matrix product
     (1, 72, 40, 1000, 2, 97, dict(weight_dtype=torch.float32, bias=False)),
     (2, 512, 128, 384, 4, 1, {}),
-    (1, 128, 256, 700, 5, 64, {}),                 # receptive field 256: the widest shared x slice
+    (1, 128, 256, 700, 5, 64, {}),                 # receptive field 256: the widest x slice
     (2, 64, 136, 600, 3, 200, {}),                 # receptive field 400: one x slice per tap
 ]
 
@@ -67,6 +68,30 @@ def test_fullconv_parity(case, cuda_device):
     assert out.shape == (B, Cout, T) and out.stride(1) == 1
     ref = oracle.fullconv(bits(inp.x), _weight_bits_as_packed(inp.weight), _bias_np(inp.bias), dil)
     assert_fullconv_close(bits(out.cpu()), ref["out64"], ref["abs_sum"])
+
+
+SCHEDULE_CASES = [
+    # (B, Cin, Cout, T, K, dilation): many 256 x 256 tiles per call, so that a
+    # CTA takes several of them in turn
+    (1, 64, 256, 256 * 250, 4, 2),    # 250 tiles: the last wave is more than half full
+    (2, 64, 256, 25500, 3, 7),        # 200 tiles: one wave, then halves (ragged token tail)
+    (1, 128, 512, 256 * 160, 2, 1),   # 320 tiles: two waves, then halves
+]
+
+
+@pytest.mark.parametrize("case", SCHEDULE_CASES, ids=lambda c: f"B{c[0]}Co{c[2]}T{c[3]}")
+def test_fullconv_persistent_schedule(case, cuda_device):
+    """Calls of hundreds of tiles, which each CTA of the persistent kernel
+    walks several of (whole tiles and, where the last wave is at most half
+    full, half tiles).  Output channels are independent given x, so a sample
+    of whole channels from every channel tile is checked element by element."""
+    B, Cin, Cout, T, K, dil = case
+    inp = fullconv_inputs(B, Cin, Cout, T, K, dil, seed=T + Cout)
+    out = gpu_fullconv(inp, cuda_device).cpu()
+    chans = sorted({c for base in range(0, Cout, 256) for c in (base, base + 1, base + 130, base + 255)
+                    if c < Cout})
+    ref = oracle.fullconv(bits(inp.x), bits(inp.weight[chans]), bits(inp.bias[chans]), dil)
+    assert_fullconv_close(bits(out[:, chans]), ref["out64"], ref["abs_sum"])
 
 
 def test_fullconv_pack_weight_is_tap_major_and_rounds_to_bf16(cuda_device):
@@ -111,7 +136,8 @@ def test_fullconv_workload_sampled_channels(cuda_device):
     whole sampled channels of sampled rows are checked element by element."""
     inp = fullconv_dilated()
     out = gpu_fullconv(inp, cuda_device).cpu()
-    for b in (0, 5):
+    # row 7 holds the tiles that the last wave cuts into halves of 128 tokens
+    for b in (0, 5, 7):
         chans = [0, 1, 255, 256, 511, 700, 1023]
         xb = bits(inp.x[b:b + 1])
         ref = oracle.fullconv(xb, bits(inp.weight[chans]), bits(inp.bias[chans]), inp.dilation)
