@@ -175,7 +175,8 @@ class DenseStep:
     `sets` copies of the activations rotate so that no step finds its inputs
     in L2 (total footprint well above the L2 size)."""
 
-    def __init__(self, inp: workloads.ConvInputs, device, deterministic=False, sets=None):
+    def __init__(self, inp: workloads.ConvInputs, device, deterministic=False, sets=None,
+                 seq_idx=None):
         from depthwise_causal_conv1d_channel_gb300 import _abi
 
         self.abi = _abi
@@ -208,8 +209,10 @@ class DenseStep:
         self.ws = torch.empty(_abi.ccc_conv1d_bwd_workspace_size(d.x, deterministic),
                               dtype=torch.uint8, device=device)
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
-        self.fwd_bytes = fwd_bytes(d.x, self.w, self.b, self.init, self.fin)
-        self.bwd_bytes = bwd_bytes(d.x, self.w, self.b, self.init, self.dfin, self.dinit)
+        self.ids = None if seq_idx is None else seq_idx.to(device)
+        ids_bytes = 0 if seq_idx is None else act_bytes(seq_idx)
+        self.fwd_bytes = fwd_bytes(d.x, self.w, self.b, self.init, self.fin) + ids_bytes
+        self.bwd_bytes = bwd_bytes(d.x, self.w, self.b, self.init, self.dfin, self.dinit) + ids_bytes
         self.tokens = inp.tokens if inp.cu_seqlens is None else d.x.shape[2]
         self.launches_fwd = 1
         # backward kernel + the fixed-order finalize kernel
@@ -218,14 +221,14 @@ class DenseStep:
     def fwd(self, i, stream):
         k = i % self.sets
         rc = self.abi.ccc_conv1d_fwd(self.x[k], self.w, self.b, self.cu, self.init, self.out[k],
-                                     self.fin, self.act, self.status, stream)
+                                     self.fin, self.act, self.status, stream, seq_idx=self.ids)
         assert rc == 0, self.abi.status_string(rc)
 
     def bwd(self, i, stream):
         k = i % self.sets
         rc = self.abi.ccc_conv1d_bwd(self.x[k], self.w, self.b, self.cu, self.init, self.g[k],
                                      self.dfin, self.dx[k], self.dw, self.db, self.dinit, self.act,
-                                     self.det, self.ws, self.status, stream)
+                                     self.det, self.ws, self.status, stream, seq_idx=self.ids)
         assert rc == 0, self.abi.status_string(rc)
 
     def check_status(self, stream):
@@ -302,8 +305,8 @@ def _per_call_ms(call, sets, device, stream, per=20, reps=5):
     return statistics.median(out)
 
 
-def bench_conv_workload(name, inp, device, stream, peak, deterministic, do_bwd=True):
-    st = DenseStep(inp, device, deterministic=deterministic)
+def bench_conv_workload(name, inp, device, stream, peak, deterministic, do_bwd=True, seq_idx=None):
+    st = DenseStep(inp, device, deterministic=deterministic, seq_idx=seq_idx)
     r = {"workload": name, "tokens": st.tokens, "rotating_sets": st.sets}
     f_ms = _per_call_ms(st.fwd, st.sets, device, stream)
     r["fwd"] = _rate(st.fwd_bytes, f_ms, st.tokens, peak)
@@ -375,6 +378,35 @@ def bench_update(device, stream, peak, iters=50):
     r["graph_chain_1000"] = {"us_per_step": round(a.elapsed_time(c) * 1e3 / 1000, 3),
                              "note": "one state, L2-resident, CUDA graph; not an HBM figure"}
     return r
+
+
+def bench_update_multi(device, stream, peak, L=4):
+    """The update with L new tokens a row ([B, D, L], the multi-token form):
+    B 256, D 4096, as the decode workload.  Bytes: state read and write, L
+    tokens of x read and of out written, weight and bias."""
+    from depthwise_causal_conv1d_channel_gb300 import _abi
+
+    gen = torch.Generator(device=device).manual_seed(1)
+    B, D = 256, 4096
+    per = B * D * 3 * 2 + 2 * B * D * L * 2
+    sets = max(1, -(-3 * L2_BYTES // per))
+    state = [torch.randn(B, D, 3, device=device, generator=gen).to(torch.bfloat16) for _ in range(sets)]
+    x = [torch.randn(B, L, D, device=device, generator=gen).to(torch.bfloat16).transpose(1, 2)
+         for _ in range(sets)]
+    out = [torch.empty(B, L, D, dtype=torch.bfloat16, device=device).transpose(1, 2)
+           for _ in range(sets)]
+    w = (torch.rand(D, 4, device=device, generator=gen) - 0.5).to(torch.bfloat16)
+    b = ((torch.rand(D, device=device, generator=gen) - 0.5) * 0.2).to(torch.bfloat16)
+
+    def upd(i, s):
+        k = i % sets
+        rc = _abi.ccc_conv1d_update(x[k], state[k], w, b, out[k], _abi.CCC_ACT_SILU, s)
+        assert rc == 0
+
+    ms = _per_call_ms(upd, sets, device, stream, per=40)
+    nbytes = update_bytes(B, D, w, b) + 2 * B * D * (L - 1) * 2
+    return {"workload": "decode_update_multi_token", "batch": B, "dim": D, "tokens_per_row": L,
+            "rotating_sets": sets, "update": _rate(nbytes, ms, B * L, peak)}
 
 
 def fullconv_flops(B, T, Cin, Cout, K):
@@ -813,6 +845,12 @@ def main():
         # the same dense step with a width-three filter (weight [D, 3], states [., D, 2])
         w3 = workloads.make_inputs(4, 1536, 2048, seed=0, initial_states=True, grad=True, width=3)
         bd.append(bench_conv_workload("dense_state_width3", w3, device, stream, peak, False))
+        # the dense_state shape (no states) with per-token sequence ids: runs of
+        # U[1, 512] tokens in every row
+        si = workloads.make_inputs(4, 1536, 2048, seed=0, grad=True)
+        bd.append(bench_conv_workload("dense_state_seq_idx", si, device, stream, peak, False,
+                                      seq_idx=workloads.seq_ids(4, 2048, seed=0, max_run=512)))
+        bd.append(bench_update_multi(device, stream, peak))
         bd.append(bench_conv_workload("dense_large_bias", inp, device, stream, peak, False))
         large = dataclasses.replace(inp, bias=None, deterministic=True)
         bd.append(bench_conv_workload("dense_large_det", large, device, stream, peak, True))

@@ -116,7 +116,16 @@ __device__ __forceinline__ void fwd_walk(const FwdArgs& a, const Seqs& seqs, con
     for (; q < e; ++q) step(VT::ld(a.x + xs.at(n, q)), q);
 
     // the thread that finishes a sequence writes its final state: xe[len-3 .. len-1]
-    if (e == hi && a.fin) store_state<V>(a.fin, state_row, a.sw, win);
+    // (from a copy: the window's own address never leaves this function, so it
+    // stays in registers, though narrow states go through an out-of-line store)
+    if (e == hi && a.fin) {
+      float fin[kState][V];
+#pragma unroll
+      for (int i = 0; i < kState; ++i)
+#pragma unroll
+        for (int c = 0; c < V; ++c) fin[i][c] = win[i][c];
+      store_state<V>(a.fin, state_row, a.sw, fin);
+    }
     ++n;
   }
 }
