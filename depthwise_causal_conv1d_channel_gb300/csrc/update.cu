@@ -131,8 +131,11 @@ __global__ void __launch_bounds__(256) update_kernel(UpdArgs a) {
 // eight distinct 16-byte bank groups, so the exchange is conflict-free).
 // Read with per-lane 48-byte strides instead, every load instruction would
 // touch twice the sectors it uses.
+#ifndef CCC_UPDATE_MULTI_BLOCKS
+#define CCC_UPDATE_MULTI_BLOCKS 4  // resident blocks an SM asked of the L-token instance
+#endif
 template <int ACT, int TY, int R, bool MULTI>
-__global__ void __launch_bounds__(32 * TY) update_w8_kernel(UpdArgs a) {
+__global__ void __launch_bounds__(32 * TY, MULTI ? CCC_UPDATE_MULTI_BLOCKS : 1) update_w8_kernel(UpdArgs a) {
   pdl_wait();
   pdl_release();
   constexpr int kChunks = 32 * kState;  // 16-byte chunks of one warp-row of state
@@ -148,6 +151,10 @@ __global__ void __launch_bounds__(32 * TY) update_w8_kernel(UpdArgs a) {
   if (b0 >= a.B) return;  // the whole warp: it shares b0
   float2 w[4][kWidth], bias[4];
   uint4 sr[R][kState], xr[R];
+  // L tokens a row: tokens are taken kTokChunk at a time, all loads of a chunk
+  // in flight at once; the first chunk's go out with the state's
+  constexpr int kTokChunk = 4;
+  uint4 xq[kTokChunk - 1] = {};  // tokens 1 .. kTokChunk - 1 of row b0 (MULTI, R == 1)
 #pragma unroll
   for (int r = 0; r < R; ++r) {
     if (b0 + r < a.B) {
@@ -157,6 +164,12 @@ __global__ void __launch_bounds__(32 * TY) update_w8_kernel(UpdArgs a) {
         if (lane + 32 * j < n_chunks) sr[r][j] = run[lane + 32 * j];
       if (valid) xr[r] = Vec<8>::ld(a.x + int64_t(b0 + r) * a.x_sb + d0);
     }
+  }
+  if constexpr (MULTI) {
+    static_assert(!MULTI || R == 1, "one row a warp with L tokens");
+#pragma unroll
+    for (int j = 1; j < kTokChunk; ++j)
+      if (valid && j < a.L) xq[j - 1] = Vec<8>::ld(a.x + int64_t(b0) * a.x_sb + int64_t(j) * a.x_sl + d0);
   }
   if (valid) weights_direct2<8>(a.wr, d0, w, bias);  // after the state loads are in flight
 #pragma unroll
@@ -222,27 +235,39 @@ __global__ void __launch_bounds__(32 * TY) update_w8_kernel(UpdArgs a) {
         win[i][h] = make_float2(bf16_to_f32(u.h[(2 * h) * 3 + i]), bf16_to_f32(u.h[(2 * h + 1) * 3 + i]));
     const uint16_t* xrow = a.x + int64_t(b0 + r) * a.x_sb + d0;
     uint16_t* orow = a.out + int64_t(b0 + r) * a.o_sb + d0;
-    uint4 cur = xr[r];
-    for (int l = 0; l < a.L; ++l) {
-      // the next token's load is in flight while this one is computed
-      uint4 nxt = cur;
-      if (l + 1 < a.L) nxt = Vec<8>::ld(xrow + int64_t(l + 1) * a.x_sl);
-      float2 xc[4], y[4];
-      Vec<8>::unpack2(cur, xc);
+    uint4 xs[kTokChunk];
+    xs[0] = xr[r];
 #pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        float2 p = bias[h];
-        p = ffma2(w[h][0], win[0][h], p);
-        p = ffma2(w[h][1], win[1][h], p);
-        p = ffma2(w[h][2], win[2][h], p);
-        p = ffma2(w[h][3], xc[h], p);
-        y[h] = act_fwd2<ACT>(p);
-        win[0][h] = win[1][h];
-        win[1][h] = win[2][h];
-        win[2][h] = xc[h];
+    for (int j = 1; j < kTokChunk; ++j) xs[j] = xq[j - 1];
+    for (int l0 = 0; l0 < a.L; l0 += kTokChunk) {
+      // the next chunk's loads are in flight while this one is computed
+      uint4 nx[kTokChunk] = {};
+#pragma unroll
+      for (int j = 0; j < kTokChunk; ++j) {
+        const int l = l0 + kTokChunk + j;
+        if (l < a.L) nx[j] = Vec<8>::ld(xrow + int64_t(l) * a.x_sl);
       }
-      Vec<8>::st(orow + int64_t(l) * a.o_sl, Vec<8>::pack2(y));
-      cur = nxt;
+#pragma unroll
+      for (int j = 0; j < kTokChunk; ++j) {
+        if (l0 + j >= a.L) break;
+        float2 xc[4], y[4];
+        Vec<8>::unpack2(xs[j], xc);
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          float2 p = bias[h];
+          p = ffma2(w[h][0], win[0][h], p);
+          p = ffma2(w[h][1], win[1][h], p);
+          p = ffma2(w[h][2], win[2][h], p);
+          p = ffma2(w[h][3], xc[h], p);
+          y[h] = act_fwd2<ACT>(p);
+          win[0][h] = win[1][h];
+          win[1][h] = win[2][h];
+          win[2][h] = xc[h];
+        }
+        Vec<8>::st(orow + int64_t(l0 + j) * a.o_sl, Vec<8>::pack2(y));
+      }
+#pragma unroll
+      for (int j = 0; j < kTokChunk; ++j) xs[j] = nx[j];
     }
     // new state: the last three extended inputs, BF16 values held exactly in FP32
 #pragma unroll

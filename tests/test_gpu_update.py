@@ -101,7 +101,7 @@ def _multi_inputs(B, D, L, seed, channel_last=True, weight_dtype=torch.bfloat16,
 
 
 @pytest.mark.parametrize("B,D,L", [(3, 264, 5), (2, 100, 7), (4, 4096, 3), (1, 8, 1), (5, 36, 64),
-                                   (2, 1, 4)])
+                                   (2, 1, 4), (2, 512, 4), (3, 520, 8), (2, 264, 9), (1, 256, 2)])
 @pytest.mark.parametrize("act", ["silu", None])
 def test_multi_token_update_parity(B, D, L, act, cuda_device):
     """Each row's L tokens in one call: out equals the oracle's forward over
