@@ -323,10 +323,11 @@ static FwdPlan plan_bdt(int64_t rows) {
 }
 
 FwdPlan plan_fwd(int kind, int vec, int64_t Q, int D, int64_t rows, int sm_count, bool ids) {
-  if (ids) {  // the general kernels with id masks: vec 4 or 1
-    FwdPlan p = kind == kLayoutTimeContiguous
-                    ? plan_bdt(rows)
-                    : plan_cl(vec, Q, D, sm_count, fwd_ids_blocks_per_sm(vec), 1, 12, kGeneralThreads);
+  if (ids) {  // kernels with id masks: the ring kernel (vec 4) or the general ones
+    FwdPlan p = kind == kLayoutTimeContiguous ? plan_bdt(rows)
+                : vec == 4 ? plan_cl(4, Q, D, sm_count, fwd_ids_blocks_per_sm(4), 1, 12, 256, 6)
+                           : plan_cl(vec, Q, D, sm_count, fwd_ids_blocks_per_sm(vec), 1, 12,
+                                     kGeneralThreads);
     p.ids = 1;
     if (kind == kLayoutTimeContiguous) p.vec = 1;
     return p;
@@ -350,10 +351,12 @@ FwdPlan plan_fwd(int kind, int vec, int64_t Q, int D, int64_t rows, int sm_count
 }
 
 BwdPlan plan_bwd(int kind, int vec, int64_t Q, int D, int64_t rows, int sm_count, bool ids) {
-  if (ids) {  // the general kernels with id masks: vec 4 or 1
-    BwdPlan p = kind == kLayoutTimeContiguous
-                    ? plan_bdt(rows)
-                    : plan_cl(vec, Q, D, sm_count, bwd_ids_blocks_per_sm(vec), 1, 18, kGeneralThreads);
+  if (ids) {  // kernels with id masks: the ring kernel (vec 4) or the general ones
+    BwdPlan p = kind == kLayoutTimeContiguous ? plan_bdt(rows)
+                : vec == 4 ? plan_cl(4, Q, D, sm_count, bwd_ids_blocks_per_sm(4), 1, 18,
+                                     bwd_block_threads(4), 3)
+                           : plan_cl(vec, Q, D, sm_count, bwd_ids_blocks_per_sm(vec), 1, 18,
+                                     kGeneralThreads);
     p.ids = 1;
     if (kind == kLayoutTimeContiguous) p.vec = 1;
     return p;

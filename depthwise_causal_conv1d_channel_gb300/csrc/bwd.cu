@@ -321,8 +321,17 @@ constexpr size_t bwd_ring_bytes(int threads) {
 }
 constexpr int kBwdThreads = 128;
 
-template <int V, int ACT>
-__global__ void __launch_bounds__(kBwdThreads, V == 8 ? CCC_BWD_MIN_BLOCKS : 4)
+// With IDS (V = 4; dense calls without states), every token carries a sequence
+// id (cuDNN page, seq_idx[B, T]): a tap joins two tokens only when their ids
+// are equal.  A ring group whose three tokens and the three before them share
+// one id (all but the groups at an id change, for ids that form runs) takes
+// the fast steps; any other takes the general step, which masks every tap by
+// the ids.  Both leave the windows at phase 0 after a group.
+#ifndef CCC_BWD_IDS_BLOCKS
+#define CCC_BWD_IDS_BLOCKS 3  // resident blocks an SM asked of the id instance
+#endif
+template <int V, int ACT, bool IDS = false>
+__global__ void __launch_bounds__(kBwdThreads, V == 8 ? CCC_BWD_MIN_BLOCKS : (IDS ? CCC_BWD_IDS_BLOCKS : 4))
     bwd_clv_kernel(BwdArgs a) {
   using VT = Vec<V>;
   using Raw = typename VT::Raw;
@@ -373,6 +382,11 @@ __global__ void __launch_bounds__(kBwdThreads, V == 8 ? CCC_BWD_MIN_BLOCKS : 4)
       const bool starts = a0 == lo;
       const int64_t state_row = int64_t(n) * a.D + d0;
       const int64_t xst = a.x_st, gst = a.g_st, dst = a.dx_st;
+      // IW: ids of tokens m-3 .. m-1 (IDS; any value before the row start,
+      // where x and gp are zero); token t's id is at id_off + t * ids_st
+      int IW[kState] = {0, 0, 0};
+      const int64_t id_off = IDS ? int64_t(n) * a.ids_sb - lo * a.ids_st : 0;
+      auto id_at = [&](int64_t t) { return __ldg(a.ids + id_off + t * a.ids_st); };
       // pointers at token a0
       const uint16_t* xp = a.x + (dense ? n * a.x_sb + (a0 - lo) * xst : a0 * xst) + d0;
       const uint16_t* gq = a.g + (dense ? n * a.g_sb + (a0 - lo) * gst : a0 * gst) + d0;
@@ -412,8 +426,16 @@ __global__ void __launch_bounds__(kBwdThreads, V == 8 ? CCC_BWD_MIN_BLOCKS : 4)
         cp_async_commit();
       };
       int st = 0;  // stage of the group being taken
-      auto take = [&](Raw (&xr)[3], Raw (&gr)[3]) {
+      // takes the group of tokens m0 .. m0 + 2; true when they and the three
+      // tokens before them share one id (always without IDS)
+      auto take = [&](Raw (&xr)[3], Raw (&gr)[3], int64_t m0) {
         issue_next();
+        bool uniform = true;
+        if constexpr (IDS) {
+          uniform = IW[0] == IW[1] && IW[1] == IW[2];
+#pragma unroll
+          for (int u = 0; u < 3; ++u) uniform = uniform && id_at(m0 + u) == IW[2];
+        }
         cp_async_wait<kBwdRing - 1>();  // the group being taken has landed
         const char* s0 = ring + size_t(st * 6) * slot;
 #pragma unroll
@@ -422,6 +444,7 @@ __global__ void __launch_bounds__(kBwdThreads, V == 8 ? CCC_BWD_MIN_BLOCKS : 4)
           gr[u] = *reinterpret_cast<const Raw*>(s0 + size_t(2 * u + 1) * slot);
         }
         st = (st + 1) % kBwdRing;
+        return uniform;
       };
 #pragma unroll
       for (int j = 0; j < kBwdRing - 1; ++j) issue_next();
@@ -444,6 +467,11 @@ __global__ void __launch_bounds__(kBwdThreads, V == 8 ? CCC_BWD_MIN_BLOCKS : 4)
       }
 
       float2 X[kState][H], G[kState][H];  // xe[m-3 .. m-1], gp[m-3 .. m-1]
+      if constexpr (IDS) {
+#pragma unroll
+        for (int j = 0; j < kState; ++j)
+          if (a0 - kState + j >= lo) IW[j] = id_at(a0 - kState + j);
+      }
       {
         float2 init[kState][H];
         if (a0 - kState < lo && a.init) {
@@ -473,6 +501,24 @@ __global__ void __launch_bounds__(kBwdThreads, V == 8 ? CCC_BWD_MIN_BLOCKS : 4)
       // general step at token m, windows at phase 0 (physical shifts)
       auto slow = [&](int64_t m) {
         float2 gp[H], v[H];
+        // IDS: the forward taps read window token k only when its id is token
+        // m's (f0..f2); dx[m-3] takes gp of m-2, m-1, m only when their ids are
+        // token m-3's (e1, e2, e3)
+        int cid = 0;
+        bool f0 = true, f1 = true, f2 = true, e1 = true, e2 = true, e3 = true;
+        if constexpr (IDS) {
+          if (m < hi) cid = id_at(m);
+          f0 = IW[0] == cid;
+          f1 = IW[1] == cid;
+          f2 = IW[2] == cid;
+          e1 = IW[1] == IW[0];
+          e2 = IW[2] == IW[0];
+          e3 = cid == IW[0];
+          IW[0] = IW[1];
+          IW[1] = IW[2];
+          IW[2] = cid;
+        }
+        const float2 zero2 = splat2(0.0f);
         if (m < hi) {
           float2 xc[H], gc[H];
           VT::unpack2(VT::ld(xp + (m - a0) * xst), xc);
@@ -480,16 +526,18 @@ __global__ void __launch_bounds__(kBwdThreads, V == 8 ? CCC_BWD_MIN_BLOCKS : 4)
           const bool own = m < e;
 #pragma unroll
           for (int h = 0; h < H; ++h) {
+            const float2 x0 = f0 ? X[0][h] : zero2, x1 = f1 ? X[1][h] : zero2,
+                         x2 = f2 ? X[2][h] : zero2;
             float2 p = b[h];
-            p = ffma2(w[h][0], X[0][h], p);
-            p = ffma2(w[h][1], X[1][h], p);
-            p = ffma2(w[h][2], X[2][h], p);
+            p = ffma2(w[h][0], x0, p);
+            p = ffma2(w[h][1], x1, p);
+            p = ffma2(w[h][2], x2, p);
             p = ffma2(w[h][3], xc[h], p);
             gp[h] = act_bwd2<ACT>(p, gc[h]);
             if (own) {
-              aw[h][0] = ffma2(gp[h], X[0][h], aw[h][0]);
-              aw[h][1] = ffma2(gp[h], X[1][h], aw[h][1]);
-              aw[h][2] = ffma2(gp[h], X[2][h], aw[h][2]);
+              aw[h][0] = ffma2(gp[h], x0, aw[h][0]);
+              aw[h][1] = ffma2(gp[h], x1, aw[h][1]);
+              aw[h][2] = ffma2(gp[h], x2, aw[h][2]);
               aw[h][3] = ffma2(gp[h], xc[h], aw[h][3]);
               ab[h] = fadd2(ab[h], gp[h]);
             }
@@ -499,14 +547,14 @@ __global__ void __launch_bounds__(kBwdThreads, V == 8 ? CCC_BWD_MIN_BLOCKS : 4)
           }
         } else {
 #pragma unroll
-          for (int h = 0; h < H; ++h) gp[h] = splat2(0.0f);
+          for (int h = 0; h < H; ++h) gp[h] = zero2;
         }
 #pragma unroll
         for (int h = 0; h < H; ++h) {
           float2 acc = fmul2(w[h][3], G[0][h]);
-          acc = ffma2(w[h][2], G[1][h], acc);
-          acc = ffma2(w[h][1], G[2][h], acc);
-          acc = ffma2(w[h][0], gp[h], acc);
+          acc = ffma2(w[h][2], e1 ? G[1][h] : zero2, acc);
+          acc = ffma2(w[h][1], e2 ? G[2][h] : zero2, acc);
+          acc = ffma2(w[h][0], e3 ? gp[h] : zero2, acc);
           v[h] = acc;
           G[0][h] = G[1][h];
           G[1][h] = G[2][h];
@@ -587,21 +635,28 @@ __global__ void __launch_bounds__(kBwdThreads, V == 8 ? CCC_BWD_MIN_BLOCKS : 4)
       Raw xr[3], gr[3];
       int k = 0;
       uint16_t* drow = dp + (r0 - kState - a0) * dst;  // dx rows of group k
+      // a group of other ids than its window's takes the general steps
+      auto mixed = [&](int64_t m0) {
+        slow(m0);
+        slow(m0 + 1);
+        slow(m0 + 2);
+      };
       if (head) {
-        take(xr, gr);
-        group(Yes{}, No{}, xr, gr, drow);
+        if (take(xr, gr, r0)) group(Yes{}, No{}, xr, gr, drow);
+        else mixed(r0);
         k = 1;
         drow += 3 * dst;
       }
       for (; k < n_main; ++k) {
-        take(xr, gr);
-        group(Yes{}, Yes{}, xr, gr, drow);
+        const int64_t m0 = r0 + 3 * int64_t(k);
+        if (take(xr, gr, m0)) group(Yes{}, Yes{}, xr, gr, drow);
+        else mixed(m0);
         drow += 3 * dst;
       }
       m = r0 + 3 * int64_t(n_main);
       if (tail) {
-        take(xr, gr);
-        group(No{}, Yes{}, xr, gr, drow);
+        if (take(xr, gr, m)) group(No{}, Yes{}, xr, gr, drow);
+        else mixed(m);
       } else {
         for (; m < m_end; ++m) slow(m);
       }
@@ -1057,7 +1112,8 @@ static cudaError_t bwd_smem_attributes() {
   const int b8 = int(bwd_smem_bytes(8, kBwdThreads)), b4 = int(bwd_smem_bytes(4, kBwdThreads));
   for (auto f : {bwd_clv_kernel<8, kActSilu>, bwd_clv_kernel<8, kActNone>})
     if (err == cudaSuccess) err = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, b8);
-  for (auto f : {bwd_clv_kernel<4, kActSilu>, bwd_clv_kernel<4, kActNone>})
+  for (auto f : {bwd_clv_kernel<4, kActSilu>, bwd_clv_kernel<4, kActNone>, bwd_clv_kernel<4, kActSilu, true>,
+                 bwd_clv_kernel<4, kActNone, true>})
     if (err == cudaSuccess) err = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, b4);
   if (err == cudaSuccess) g_bwd_attr_done.put(1);
   return err;
@@ -1089,9 +1145,10 @@ int bwd_ids_blocks_per_sm(int vec) {
   long long v = 0;
   if (cache.get(&v) && v > 0) return int(v);
   int n = 0;
+  bwd_smem_attributes();
   const cudaError_t err =
-      vec == 4 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                     &n, bwd_cl_kernel<4, kActSilu, true>, kGeneralThreads, bwd_red_bytes<4>(kGeneralThreads))
+      vec == 4 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, bwd_clv_kernel<4, kActSilu, true>, kBwdThreads,
+                                                               bwd_smem_bytes(4, kBwdThreads))
                : cudaOccupancyMaxActiveBlocksPerMultiprocessor(
                      &n, bwd_cl_kernel<1, kActSilu, true>, kGeneralThreads, bwd_red_bytes<1>(kGeneralThreads));
   if (err == cudaSuccess && n > 0) {
@@ -1101,14 +1158,18 @@ int bwd_ids_blocks_per_sm(int vec) {
   return 1;
 }
 
-// Calls with per-token sequence ids: the general kernels with id masks.
+// Calls with per-token sequence ids: the ring kernel (4 channels a thread) or
+// the general kernels, with id masks.
 template <int ACT>
 static cudaError_t launch_bwd_ids(const BwdArgs& a, const BwdPlan& p, bool pdl, cudaStream_t stream) {
   if (p.kind == kLayoutChannelLast) {
     dim3 block(p.tx, p.ty), grid(p.gx, p.gy);
-    if (p.vec == 4)
-      return launch_kernel(bwd_cl_kernel<4, ACT, true>, grid, block, bwd_red_bytes<4>(p.tx * p.ty),
+    if (p.vec == 4) {
+      const cudaError_t err = bwd_smem_attributes();
+      if (err != cudaSuccess) return err;
+      return launch_kernel(bwd_clv_kernel<4, ACT, true>, grid, block, bwd_smem_bytes(4, p.tx * p.ty),
                            stream, pdl, a);
+    }
     return launch_kernel(bwd_cl_kernel<1, ACT, true>, grid, block, bwd_red_bytes<1>(p.tx * p.ty),
                          stream, pdl, a);
   }

@@ -180,8 +180,19 @@ constexpr size_t fwd_ring_bytes(int threads) {
 }
 extern __shared__ __align__(16) char fwd_dyn_smem[];
 
-template <int V, int ACT>
-__global__ void __launch_bounds__(kFwdThreads, 3) fwd_clv_kernel(FwdArgs a) {
+// With IDS, every token carries a sequence id (cuDNN page, seq_idx[B, T]; dense
+// calls without states): a tap reads a window token of another id as zero.
+// The ids of a ring group are loaded (one 4-byte load per token, the same
+// address for all lanes of a warp) before the wait for the group's rows.  A
+// group whose tokens and the three before them share one id (all but the
+// groups at an id change, for ids that form runs) takes the unmasked steps;
+// any other takes the masked step with physical shifts.  A group is a whole
+// number of window periods, so both leave the window at phase 0.
+#ifndef CCC_FWD_IDS_BLOCKS
+#define CCC_FWD_IDS_BLOCKS 2  // resident blocks an SM asked of the id instance
+#endif
+template <int V, int ACT, bool IDS = false>
+__global__ void __launch_bounds__(kFwdThreads, IDS ? CCC_FWD_IDS_BLOCKS : 3) fwd_clv_kernel(FwdArgs a) {
   if (blockDim.x * blockDim.y * blockDim.z != kFwdThreads) return;  // the ring layout assumes it
   pdl_wait();     // inputs may come from the previous kernel in the stream
   pdl_release();
@@ -249,8 +260,11 @@ __global__ void __launch_bounds__(kFwdThreads, 3) fwd_clv_kernel(FwdArgs a) {
       have_w = true;
     }
 
-    // W[j] = xe[q - 3 + j]
+    // W[j] = xe[q - 3 + j]; IW[j] = its id (IDS; any value before the row
+    // start, where the window is zero)
     float2 W[kState][H];
+    int IW[kState] = {0, 0, 0};
+    const int64_t id_off = IDS ? int64_t(n) * a.ids_sb - lo * a.ids_st : 0;
     {
       float2 init[kState][H];
       if (q - kState < lo && a.init) {
@@ -266,6 +280,7 @@ __global__ void __launch_bounds__(kFwdThreads, 3) fwd_clv_kernel(FwdArgs a) {
         const int64_t tok = q - kState + j;
         if (tok >= lo) {
           VT::unpack2(VT::ld(xp - (kState - j) * xst), W[j]);
+          if constexpr (IDS) IW[j] = __ldg(a.ids + id_off + tok * a.ids_st);
         } else {
           const int64_t i = tok - lo + kState;
 #pragma unroll
@@ -274,6 +289,7 @@ __global__ void __launch_bounds__(kFwdThreads, 3) fwd_clv_kernel(FwdArgs a) {
         }
       }
     }
+    const float2 zero2 = splat2(0.0f);
 
     // one token at window phase J: taps W[J], W[J+1], W[J+2] (mod 3), then the
     // new token replaces W[J]
@@ -293,16 +309,26 @@ __global__ void __launch_bounds__(kFwdThreads, 3) fwd_clv_kernel(FwdArgs a) {
       }
       VT::st(dst, VT::pack2(y));
     };
-    // one token with a physical shift (keeps the window at phase 0)
-    auto shift_step = [&](Raw raw, uint16_t* dst) {
+    // one token with a physical shift (keeps the window at phase 0); cid is
+    // its id (IDS)
+    auto shift_step = [&](Raw raw, int cid, uint16_t* dst) {
+      bool m0 = true, m1 = true, m2 = true;
+      if constexpr (IDS) {
+        m0 = IW[0] == cid;
+        m1 = IW[1] == cid;
+        m2 = IW[2] == cid;
+        IW[0] = IW[1];
+        IW[1] = IW[2];
+        IW[2] = cid;
+      }
       float2 cur[H], y[H];
       VT::unpack2(raw, cur);
 #pragma unroll
       for (int h = 0; h < H; ++h) {
         float2 p = b[h];
-        p = ffma2_split(w[h][0], W[0][h], p);
-        p = ffma2_split(w[h][1], W[1][h], p);
-        p = ffma2_split(w[h][2], W[2][h], p);
+        p = ffma2_split(w[h][0], m0 ? W[0][h] : zero2, p);
+        p = ffma2_split(w[h][1], m1 ? W[1][h] : zero2, p);
+        p = ffma2_split(w[h][2], m2 ? W[2][h] : zero2, p);
         p = ffma2_split(w[h][3], cur[h], p);
         y[h] = act_fwd2<ACT, true>(p);
         W[0][h] = W[1][h];
@@ -315,13 +341,23 @@ __global__ void __launch_bounds__(kFwdThreads, 3) fwd_clv_kernel(FwdArgs a) {
     for (int k = 0; k < n_grp; ++k) {
       if (k + kFwdRing - 1 < n_grp) issue(k + kFwdRing - 1);
       cp_async_commit();
+      // one id over the group and the window before it (IDS)?
+      bool uniform = true;
+      if constexpr (IDS) {
+        uniform = IW[0] == IW[1] && IW[1] == IW[2];
+#pragma unroll
+        for (int u = 0; u < G; ++u) {
+          const int64_t t = q + int64_t(k) * G + u;
+          if (t < e) uniform = uniform && __ldg(a.ids + id_off + t * a.ids_st) == IW[2];
+        }
+      }
       cp_async_wait<kFwdRing - 1>();  // group k has landed
       const char* s0 = ring + size_t((k % kFwdRing) * G) * slot;
       Raw r[G];
 #pragma unroll
       for (int u = 0; u < G; ++u) r[u] = *reinterpret_cast<const Raw*>(s0 + size_t(u) * slot);
       uint16_t* om = op + int64_t(k) * G * ost;
-      if (k * G + G <= n_tok) {
+      if (k * G + G <= n_tok && uniform) {
 #pragma unroll
         for (int u = 0; u < G; u += 3) {
           step(P0{}, r[u], om + u * ost);
@@ -331,7 +367,9 @@ __global__ void __launch_bounds__(kFwdThreads, 3) fwd_clv_kernel(FwdArgs a) {
       } else {
 #pragma unroll
         for (int u = 0; u < G; ++u)
-          if (k * G + u < n_tok) shift_step(r[u], om + u * ost);
+          if (k * G + u < n_tok)
+            shift_step(r[u], IDS ? __ldg(a.ids + id_off + (q + int64_t(k) * G + u) * a.ids_st) : 0,
+                       om + u * ost);
       }
     }
     if (e == hi && a.fin) store_state2<V>(a.fin, state_row, a.sw, W);
@@ -455,11 +493,10 @@ static cudaError_t fwd_smem_attributes() {
   long long done = 0;
   if (g_fwd_attr_done.get(&done) && done) return cudaSuccess;
   const int bytes = int(fwd_ring_bytes<4>(kFwdThreads));
-  cudaError_t err = cudaFuncSetAttribute(fwd_clv_kernel<4, kActSilu>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (err == cudaSuccess)
-    err = cudaFuncSetAttribute(fwd_clv_kernel<4, kActNone>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  cudaError_t err = cudaSuccess;
+  for (auto f : {fwd_clv_kernel<4, kActSilu>, fwd_clv_kernel<4, kActNone>,
+                 fwd_clv_kernel<4, kActSilu, true>, fwd_clv_kernel<4, kActNone, true>})
+    if (err == cudaSuccess) err = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (err == cudaSuccess) g_fwd_attr_done.put(1);
   return err;
 }
@@ -488,9 +525,10 @@ int fwd_ids_blocks_per_sm(int vec) {
   long long v = 0;
   if (cache.get(&v) && v > 0) return int(v);
   int n = 0;
+  fwd_smem_attributes();
   const cudaError_t err =
-      vec == 4 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fwd_cl_kernel<4, kActSilu, true>,
-                                                               kGeneralThreads, 0)
+      vec == 4 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fwd_clv_kernel<4, kActSilu, true>,
+                                                               kFwdThreads, fwd_ring_bytes<4>(kFwdThreads))
                : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fwd_cl_kernel<1, kActSilu, true>,
                                                                kGeneralThreads, 0);
   if (err == cudaSuccess && n > 0) {
@@ -500,12 +538,18 @@ int fwd_ids_blocks_per_sm(int vec) {
   return 1;
 }
 
-// Calls with per-token sequence ids: the general kernels with id masks.
+// Calls with per-token sequence ids: the ring kernel (4 channels a thread) or
+// the general kernels, with id masks.
 template <int ACT>
 static cudaError_t launch_fwd_ids(const FwdArgs& a, const FwdPlan& p, cudaStream_t stream) {
   if (p.kind == kLayoutChannelLast) {
     dim3 block(p.tx, p.ty), grid(p.gx, p.gy);
-    if (p.vec == 4) return launch_kernel(fwd_cl_kernel<4, ACT, true>, grid, block, 0, stream, true, a);
+    if (p.vec == 4) {
+      const cudaError_t err = fwd_smem_attributes();
+      if (err != cudaSuccess) return err;
+      return launch_kernel(fwd_clv_kernel<4, ACT, true>, grid, block, fwd_ring_bytes<4>(p.tx * p.ty),
+                           stream, true, a);
+    }
     return launch_kernel(fwd_cl_kernel<1, ACT, true>, grid, block, 0, stream, true, a);
   }
   return launch_kernel(fwd_bdt_kernel<ACT, true>, dim3(p.gx), dim3(256), 0, stream, true, a);

@@ -87,7 +87,9 @@ def test_seq_idx_strided_ids(cuda_device):
 
 
 def test_seq_idx_constant_ids_equal_plain_call(cuda_device):
-    """One id for every token: the same results as the call without ids."""
+    """One id for every token: the same results as the call without ids --
+    out and dx bitwise (every token takes the same operations in the same
+    order; only the weight sums' block partition may differ)."""
     B, D, T = 2, 128, 200
     inp = make_inputs(B, D, T, seed=9, grad=True)
     ids = torch.full((B, T), 4, dtype=torch.int32)
@@ -96,8 +98,8 @@ def test_seq_idx_constant_ids_equal_plain_call(cuda_device):
     x = d.x.detach().requires_grad_(True)
     out = ccc.causal_conv1d(x, d.weight, d.bias)
     out.backward(d.g)
-    assert_bf16_close(bits(a["out"]), bits(out.detach().cpu()), "out vs plain call")
-    assert_bf16_close(bits(a["dx"]), bits(x.grad.cpu()), "dx vs plain call")
+    assert torch.equal(a["out"], out.detach().cpu()), "out vs plain call"
+    assert torch.equal(a["dx"], x.grad.cpu()), "dx vs plain call"
 
 
 def test_seq_idx_deterministic_repeats_bitwise(cuda_device):
