@@ -637,9 +637,8 @@ __global__ void __launch_bounds__(kBwdThreads, V == 8 ? CCC_BWD_MIN_BLOCKS : (ID
       uint16_t* drow = dp + (r0 - kState - a0) * dst;  // dx rows of group k
       // a group of other ids than its window's takes the general steps
       auto mixed = [&](int64_t m0) {
-        slow(m0);
-        slow(m0 + 1);
-        slow(m0 + 2);
+#pragma unroll 1
+        for (int u = 0; u < 3; ++u) slow(m0 + u);
       };
       if (head) {
         if (take(xr, gr, r0)) group(Yes{}, No{}, xr, gr, drow);
