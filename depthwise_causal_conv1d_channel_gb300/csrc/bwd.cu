@@ -311,7 +311,7 @@ __global__ void __launch_bounds__(kGeneralThreads) bwd_cl_kernel(BwdArgs a) {
 #define CCC_BWD_MIN_BLOCKS 2
 #endif
 #ifndef CCC_BWD_RING
-#define CCC_BWD_RING 4
+#define CCC_BWD_RING 3
 #endif
 constexpr int kBwdRing = CCC_BWD_RING;
 static_assert(kBwdRing >= 2, "the ring needs a stage being filled and one being read");
