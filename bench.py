@@ -47,8 +47,8 @@ L2_BYTES = 129 * 2 ** 20
 # finalize kernel -- from one ncu capture of those two kernels
 # (profiles/traffic_dense_large_backward.md), per launch.  Valid only for the
 # kernel sources whose digest is recorded here (null otherwise).
-TRAFFIC = {"sources_sha256": "a7b1e5b18e69321991c7213dac412b39c7796870d9a6cd0bc459a65ff72d1b0b",
-           "bytes_per_launch": (1349982208 + 638056192) + (1543168 + 0)}
+TRAFFIC = {"sources_sha256": "3e063dfb9eb110a349f514d7b28d907465199808843d8cc0db3f87baaff2b4d2",
+           "bytes_per_launch": (1349953280 + 638793216) + (1543424 + 0)}
 
 
 # The sources the dominant call's kernels (the channel-last backward and the
