@@ -268,3 +268,43 @@ def test_python_api_seq_idx_rules_and_bad_activation():
         ccc.causal_conv1d(x, w, seq_idx=ids, return_final_states=True)
     with pytest.raises(ValueError):
         ccc.causal_conv1d(x, w, activation="gelu")
+
+
+def fc(x, pw, b, dil, out):
+    r = lambda d: None if d is None else ctypes.byref(d)
+    return _abi.lib.ccc_fullconv1d_fwd(r(x), r(pw), r(b), int(dil), r(out), None, None)
+
+
+def test_fullconv_rejects_bad_arguments_on_host():
+    """ccc_fullconv1d_fwd and ccc_fullconv1d_pack_weight: every call below
+    fails a host-side check before the first CUDA call."""
+    B, Cin, Cout, Tn, K = 2, 64, 96, 40, 3
+    x = cl(0, B, Cin, Tn)
+    pw = T(10 * MB, BF16, (K, Cout, Cin))
+    b = T(11 * MB, BF16, (Cout,))
+    out = cl(20 * MB, B, Cout, Tn)
+    inv, uns, ali = _abi.CCC_ERR_INVALID_ARG, _abi.CCC_ERR_UNSUPPORTED, _abi.CCC_ERR_ALIAS
+    assert fc(x, pw, b, 0, out) == inv                                   # dilation >= 1
+    assert fc(x, T(10 * MB, BF16, (K, Cout, Cin + 8)), b, 1, out) == inv  # Cin of x and weight differ
+    assert fc(x, pw, T(11 * MB, BF16, (Cout + 8,)), 1, out) == inv       # bias shape
+    assert fc(x, pw, b, 1, cl(20 * MB, B, Cout, Tn + 1)) == inv          # out shape
+    assert fc(x, pw, b, 1, T(20 * MB, F32, (B, Cout, Tn), (Tn * Cout, 1, Cout))) == inv  # out dtype
+    xt = T(0, BF16, (B, Cin, Tn))                                        # time-contiguous x
+    assert fc(xt, pw, b, 1, out) == uns
+    x60 = cl(0, B, 60, Tn)                                               # Cin not a multiple of 8
+    assert fc(x60, T(10 * MB, BF16, (K, Cout, 60)), b, 1, out) == uns
+    assert fc(x, T(10 * MB, BF16, (1025, Cout, Cin)), b, 1, out) == uns  # K above 1024
+    assert fc(x, pw, b, 1, cl(0, B, Cout, Tn)) == ali                    # out on top of x
+    assert fc(x, pw, b, 1, cl(10 * MB, B, Cout, Tn)) == ali              # out on top of the weight
+    # more 256 x 256 tiles than the persistent kernel numbers (2^31 here)
+    Bb, Tb, Cb = 4096, 1 << 24, 2048
+    xb = cl(0, Bb, Cin, Tb)
+    ob = T(1 << 50, BF16, (Bb, Cb, Tb), (Tb * Cb, 1, Cb))
+    assert fc(xb, T(1 << 49, BF16, (K, Cb, Cin)), None, 1, ob) == uns
+    # the pack: contiguous packed output, no overlap with the weight
+    w = T(40 * MB, BF16, (Cout, Cin, K))
+    r = lambda d: ctypes.byref(d)
+    assert _abi.lib.ccc_fullconv1d_pack_weight(r(w), r(T(50 * MB, BF16, (K, Cout, Cin + 8))), None) == inv
+    assert _abi.lib.ccc_fullconv1d_pack_weight(
+        r(w), r(T(50 * MB, BF16, (K, Cout, Cin), (Cout * Cin * 2, Cin, 1))), None) == uns
+    assert _abi.lib.ccc_fullconv1d_pack_weight(r(w), r(T(40 * MB, BF16, (K, Cout, Cin))), None) == ali
