@@ -258,8 +258,11 @@ ccc::WeightRef weight_ref(const ccc_tensor* weight, const ccc_tensor* bias) {
   r.bias = bias ? static_cast<const uint16_t*>(bias->data) : nullptr;
   r.b_sd = bias ? bias->stride[0] : 0;
   const int64_t D = weight->shape[0];
+  const bool bias_vec = !bias || ((D <= 1 || r.b_sd == 1) && aligned16(bias->data));
   r.w_vec = r.W == kWidth && (D <= 1 || r.w_sd == kWidth) && r.w_sk == 1 && aligned16(weight->data) &&
-            (!bias || ((D <= 1 || r.b_sd == 1) && aligned16(bias->data)));
+            bias_vec;
+  r.w_vec3 = r.W == 3 && (D <= 1 || r.w_sd == 3) && (r.W <= 1 || r.w_sk == 1) &&
+             aligned16(weight->data) && bias_vec;
   return r;
 }
 

@@ -345,7 +345,7 @@ __global__ void __launch_bounds__(kBwdThreads, V == 8 ? CCC_BWD_MIN_BLOCKS : (ID
   const int d0 = (blockIdx.x * blockDim.x + threadIdx.x) * V;
   const int64_t seg = int64_t(blockIdx.y) * blockDim.y + threadIdx.y;
   const bool active = d0 < a.D && seg < a.n_seg;
-  if (!a.wr.w_vec) stage_weights(a.wr, blockIdx.x * n_blk, n_blk, a.D, wsm);  // block-uniform
+  if (!a.wr.w_vec && !a.wr.w_vec3) stage_weights(a.wr, blockIdx.x * n_blk, n_blk, a.D, wsm);  // block-uniform
   float2 aw[H][kWidth], ab[H];
 #pragma unroll
   for (int h = 0; h < H; ++h) {
@@ -449,7 +449,7 @@ __global__ void __launch_bounds__(kBwdThreads, V == 8 ? CCC_BWD_MIN_BLOCKS : (ID
 #pragma unroll
       for (int j = 0; j < kBwdRing - 1; ++j) issue_next();
       if (!have_w) {
-        if (a.wr.w_vec) weights_direct2<V>(a.wr, d0, w, b);
+        if (a.wr.w_vec || a.wr.w_vec3) weights_direct2_any<V>(a.wr, d0, w, b);
         else weights_from_smem2<V>(wsm, n_blk, threadIdx.x * V, w, b);
         have_w = true;
       }

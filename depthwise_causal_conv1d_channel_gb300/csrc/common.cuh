@@ -359,6 +359,7 @@ struct WeightRef {
   const uint16_t* bias;  // [D] BF16 or nullptr
   int64_t b_sd;
   int w_vec;        // contiguous [D, 4] and bias, 16-byte aligned: read with vectors
+  int w_vec3;       // contiguous [D, 3] and bias, 16-byte aligned: read with vectors
 };
 
 // Widest channel slice a block stages: 32 threads x 8 channels.
@@ -457,6 +458,35 @@ __device__ __forceinline__ void weights_from_smem2(const float* ws, int n, int i
   }
 }
 
+// The contiguous bias of channels d0 .. d0+V-1 as pairs (zero without one).
+template <int V>
+__device__ __forceinline__ void bias_direct2(const WeightRef& r, int d0, float2 (&b)[V / 2]) {
+  if (r.bias) {
+    if constexpr (V == 8) {
+      const uint4 u = __ldg(reinterpret_cast<const uint4*>(r.bias + d0));
+      b[0] = unpack_bf16x2(u.x); b[1] = unpack_bf16x2(u.y);
+      b[2] = unpack_bf16x2(u.z); b[3] = unpack_bf16x2(u.w);
+    } else {
+      const uint2 u = __ldg(reinterpret_cast<const uint2*>(r.bias + d0));
+      b[0] = unpack_bf16x2(u.x); b[1] = unpack_bf16x2(u.y);
+    }
+  } else {
+#pragma unroll
+    for (int h = 0; h < V / 2; ++h) b[h] = splat2(0.0f);
+  }
+}
+
+// Weights and bias times one half (exact).
+template <int V>
+__device__ __forceinline__ void halve2(float2 (&w)[V / 2][kWidth], float2 (&b)[V / 2]) {
+#pragma unroll
+  for (int h = 0; h < V / 2; ++h) {
+    b[h] = fmul2(b[h], splat2(0.5f));
+#pragma unroll
+    for (int k = 0; k < kWidth; ++k) w[h][k] = fmul2(w[h][k], splat2(0.5f));
+  }
+}
+
 // Pair form read by each thread straight from global memory, for a contiguous
 // [D, 4] weight (and contiguous bias) aligned to 16 bytes: a thread's V
 // channels are 8V (BF16) or 16V (FP32) consecutive bytes, so a handful of
@@ -491,25 +521,51 @@ __device__ __forceinline__ void weights_direct2(const WeightRef& r, int d0,
       w[h][3] = make_float2(bf16_hi(q[h].y), bf16_hi(q[h].w));
     }
   }
-  if (r.bias) {
-    if constexpr (V == 8) {
-      const uint4 u = __ldg(reinterpret_cast<const uint4*>(r.bias + d0));
-      b[0] = unpack_bf16x2(u.x); b[1] = unpack_bf16x2(u.y);
-      b[2] = unpack_bf16x2(u.z); b[3] = unpack_bf16x2(u.w);
-    } else {
-      const uint2 u = __ldg(reinterpret_cast<const uint2*>(r.bias + d0));
-      b[0] = unpack_bf16x2(u.x); b[1] = unpack_bf16x2(u.y);
+  bias_direct2<V>(r, d0, b);
+  halve2<V>(w, b);
+}
+
+// Width three, contiguous [D, 3] weight and contiguous bias, 16-byte aligned.
+template <int V>
+__device__ __forceinline__ void weights_direct3(const WeightRef& r, int d0,
+                                                float2 (&w)[V / 2][kWidth], float2 (&b)[V / 2]) {
+  static_assert(V % 4 == 0, "vector weights need four channels at a time");
+  // width three: a thread's V channels are 3V consecutive taps (6V bytes of
+  // BF16: 8-byte aligned for V = 4, 16 for V = 8; 12V of FP32: 16-byte
+  // aligned); weight tap k is kernel tap k + 1, kernel tap 0 is zero
+  float f[3 * V];
+  if (r.w_f32) {
+    const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(r.w) + int64_t(d0) * 3);
+#pragma unroll
+    for (int i = 0; i < 3 * V / 4; ++i) {
+      const float4 v = __ldg(p + i);
+      f[4 * i] = v.x; f[4 * i + 1] = v.y; f[4 * i + 2] = v.z; f[4 * i + 3] = v.w;
     }
   } else {
+    const uint2* p = reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(r.w) + int64_t(d0) * 3);
 #pragma unroll
-    for (int h = 0; h < V / 2; ++h) b[h] = splat2(0.0f);
+    for (int i = 0; i < 3 * V / 4; ++i) {
+      const uint2 v = __ldg(p + i);
+      f[4 * i] = bf16_lo(v.x); f[4 * i + 1] = bf16_hi(v.x);
+      f[4 * i + 2] = bf16_lo(v.y); f[4 * i + 3] = bf16_hi(v.y);
+    }
   }
 #pragma unroll
   for (int h = 0; h < V / 2; ++h) {
-    b[h] = fmul2(b[h], splat2(0.5f));
+    w[h][0] = splat2(0.0f);
 #pragma unroll
-    for (int k = 0; k < kWidth; ++k) w[h][k] = fmul2(w[h][k], splat2(0.5f));
+    for (int k = 0; k < 3; ++k) w[h][k + 1] = make_float2(f[(2 * h) * 3 + k], f[(2 * h + 1) * 3 + k]);
   }
+  bias_direct2<V>(r, d0, b);
+  halve2<V>(w, b);
+}
+
+// The vector loaders: width four or width three.
+template <int V>
+__device__ __forceinline__ void weights_direct2_any(const WeightRef& r, int d0,
+                                                    float2 (&w)[V / 2][kWidth], float2 (&b)[V / 2]) {
+  if (r.w_vec3) weights_direct3<V>(r, d0, w, b);
+  else weights_direct2<V>(r, d0, w, b);
 }
 
 // Weights of one channel straight from global memory (warp-uniform channel:

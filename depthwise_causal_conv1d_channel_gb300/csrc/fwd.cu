@@ -191,7 +191,9 @@ extern __shared__ __align__(16) char fwd_dyn_smem[];
 #ifndef CCC_FWD_IDS_BLOCKS
 #define CCC_FWD_IDS_BLOCKS 2  // resident blocks an SM asked of the id instance
 #endif
-template <int V, int ACT, bool IDS = false>
+// W3: a contiguous [D, 3] weight read with vectors (its own instance, so the
+// width-four kernel's register allocation is untouched).
+template <int V, int ACT, bool IDS = false, bool W3 = false>
 __global__ void __launch_bounds__(kFwdThreads, IDS ? CCC_FWD_IDS_BLOCKS : 3) fwd_clv_kernel(FwdArgs a) {
   if (blockDim.x * blockDim.y * blockDim.z != kFwdThreads) return;  // the ring layout assumes it
   pdl_wait();     // inputs may come from the previous kernel in the stream
@@ -206,7 +208,7 @@ __global__ void __launch_bounds__(kFwdThreads, IDS ? CCC_FWD_IDS_BLOCKS : 3) fwd
   const int n_blk = blockDim.x * V;
   const int d0 = (blockIdx.x * blockDim.x + threadIdx.x) * V;
   const int64_t seg = int64_t(blockIdx.y) * blockDim.y + threadIdx.y;
-  if (!a.wr.w_vec) stage_weights(a.wr, blockIdx.x * n_blk, n_blk, a.D, ws);  // block-uniform
+  if (!a.wr.w_vec && !W3) stage_weights(a.wr, blockIdx.x * n_blk, n_blk, a.D, ws);  // block-uniform
   if (d0 >= a.D || seg >= a.n_seg) return;
   float2 w[H][kWidth], b[H];
   bool have_w = false;  // the weights are loaded once the first ring groups are in flight
@@ -255,7 +257,8 @@ __global__ void __launch_bounds__(kFwdThreads, IDS ? CCC_FWD_IDS_BLOCKS : 3) fwd
       cp_async_commit();
     }
     if (!have_w) {
-      if (a.wr.w_vec) weights_direct2<V>(a.wr, d0, w, b);
+      if constexpr (W3) weights_direct3<V>(a.wr, d0, w, b);
+      else if (a.wr.w_vec) weights_direct2<V>(a.wr, d0, w, b);
       else weights_from_smem2<V>(ws, n_blk, threadIdx.x * V, w, b);
       have_w = true;
     }
@@ -495,7 +498,8 @@ static cudaError_t fwd_smem_attributes() {
   const int bytes = int(fwd_ring_bytes<4>(kFwdThreads));
   cudaError_t err = cudaSuccess;
   for (auto f : {fwd_clv_kernel<4, kActSilu>, fwd_clv_kernel<4, kActNone>,
-                 fwd_clv_kernel<4, kActSilu, true>, fwd_clv_kernel<4, kActNone, true>})
+                 fwd_clv_kernel<4, kActSilu, true>, fwd_clv_kernel<4, kActNone, true>,
+                 fwd_clv_kernel<4, kActSilu, false, true>, fwd_clv_kernel<4, kActNone, false, true>})
     if (err == cudaSuccess) err = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (err == cudaSuccess) g_fwd_attr_done.put(1);
   return err;
@@ -563,6 +567,9 @@ static cudaError_t launch_fwd_act(const FwdArgs& a, const FwdPlan& p, cudaStream
     if (p.vec == 4) {
       const cudaError_t err = fwd_smem_attributes();
       if (err != cudaSuccess) return err;
+      if (a.wr.w_vec3)
+        return launch_kernel(fwd_clv_kernel<4, ACT, false, true>, grid, block,
+                             fwd_ring_bytes<4>(p.tx * p.ty), stream, true, a);
       return launch_kernel(fwd_clv_kernel<4, ACT>, grid, block, fwd_ring_bytes<4>(p.tx * p.ty),
                            stream, true, a);
     }

@@ -52,6 +52,8 @@ CASES = [
     (2, 48, 50, None, False, torch.bfloat16, True),
     (1, 24, 0, [5, 9, 1], False, torch.bfloat16, True),
     (2, 16, 264, None, False, torch.bfloat16, True),   # time-contiguous, 8 tokens a lane
+    (1, 2048, 20000, None, True, torch.float32, False),  # long ranges: the 8-channel backward
+    (1, 1024, 40000, None, True, torch.bfloat16, True),
 ]
 
 
