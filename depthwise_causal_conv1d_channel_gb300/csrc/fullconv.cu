@@ -270,6 +270,8 @@ __device__ __forceinline__ void store_accumulator(const Args& a, uint32_t tmem, 
 __global__ void __launch_bounds__(kThreads, 1)
     fullconv_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
                     Args a) {
+  pdl_wait();     // inputs may come from the previous kernel in the stream
+  pdl_release();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t0 = blockIdx.x * BM, n0 = blockIdx.y * BN, bb = blockIdx.z;
   const int n_iter = a.K * a.n_kblk;
@@ -512,6 +514,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot_p;
+  // The setup above reads nothing a previous kernel writes, so it runs while
+  // that kernel finishes (launched as its programmatic dependent); every read
+  // of x, the weight and the bias comes after this wait.
+  pdl_wait();
+  pdl_release();
 
   auto fail = [&]() {
     *abort_p = 1;
@@ -841,13 +848,13 @@ cudaError_t launch_fullconv(const FullConvArgs& f, cudaStream_t stream) {
     const Sched sc = make_sched(f.T, f.Cout, f.B, nsm);
     const unsigned grid = unsigned(std::min(nsm, sc.n_items));
     return launch_kernel(fullconv_persistent_kernel<kSharedN>, dim3(grid), dim3(kPThreads), smem, stream,
-                         false, mx, mw, a, sp, sc);
+                         true, mx, mw, a, sp, sc);
   }
   if (!make_map(&mx, f.x, uint64_t(f.Cin), uint64_t(f.T), uint64_t(f.B), xs_t, xs_b, BM) ||
       !make_map(&mw, f.w, uint64_t(f.Cin), uint64_t(f.Cout), uint64_t(f.K), ws_o, ws_k, BN))
     return cudaErrorInvalidValue;
   const dim3 grid(unsigned((f.T + BM - 1) / BM), unsigned((f.Cout + BN - 1) / BN), unsigned(f.B));
-  return launch_kernel(fullconv_kernel, grid, dim3(kThreads), kSmemBytes, stream, false, mx, mw, a);
+  return launch_kernel(fullconv_kernel, grid, dim3(kThreads), kSmemBytes, stream, true, mx, mw, a);
 }
 
 cudaError_t launch_pack_weight(const void* w, int w_f32, int64_t s_oc, int64_t s_ic, int64_t s_k,
