@@ -328,10 +328,11 @@ static FwdPlan plan_bdt(int64_t rows) {
 FwdPlan plan_fwd(int kind, int vec, int64_t Q, int D, int64_t rows, int sm_count, bool ids) {
   if (ids) {  // kernels with id masks: the ring kernel (vec 4) or the general ones
     FwdPlan p = kind == kLayoutTimeContiguous ? plan_bdt(rows)
-                : vec == 4 ? plan_cl(4, Q, D, sm_count, fwd_ids_blocks_per_sm(4), 1, 12, 256, 6)
+                : vec == 4 ? plan_cl(4, Q, D, sm_count, fwd_ids_blocks_per_sm(4), 1, 12, 256, kFwdGroupLong)
                            : plan_cl(vec, Q, D, sm_count, fwd_ids_blocks_per_sm(vec), 1, 12,
                                      kGeneralThreads);
     p.ids = 1;
+    p.group = kFwdGroupLong;
     if (kind == kLayoutTimeContiguous) p.vec = 1;
     return p;
   }
@@ -350,7 +351,10 @@ FwdPlan plan_fwd(int kind, int vec, int64_t Q, int D, int64_t rows, int sm_count
   const int64_t threads = int64_t(sm_count) * std::max(1, bps) * 256;
   const int64_t per_thread = ceil_div(std::max<int64_t>(Q, 1) * groups, std::max<int64_t>(threads, 1));
   const int waves = int(std::min<int64_t>(8, std::max<int64_t>(1, per_thread / 64)));
-  return plan_cl(vec, Q, D, sm_count, bps, waves, 12, 256, vec == 4 ? 6 : 1);
+  const int group = per_thread < kFwdShortTokens ? kFwdGroupShort : kFwdGroupLong;
+  FwdPlan p = plan_cl(vec, Q, D, sm_count, bps, waves, 12, 256, vec == 4 ? group : 1);
+  p.group = group;
+  return p;
 }
 
 BwdPlan plan_bwd(int kind, int vec, int64_t Q, int D, int64_t rows, int sm_count, bool ids) {

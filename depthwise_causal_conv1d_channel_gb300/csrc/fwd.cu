@@ -167,7 +167,7 @@ __global__ void __launch_bounds__(kGeneralThreads) fwd_cl_kernel(FwdArgs a) {
 // no registers are held by loads in flight.  Segments are planned in multiples
 // of kFwdGroup tokens, so only a sequence's last group can be partial; its
 // tokens take the physically shifting step from the same ring.
-constexpr int kFwdGroup = 6;  // tokens per ring stage (multiple of 3)
+constexpr int kFwdGroup = kFwdGroupLong;  // tokens per ring stage (multiple of 3)
 #ifndef CCC_FWD_RING
 #define CCC_FWD_RING 4
 #endif
@@ -175,8 +175,8 @@ constexpr int kFwdRing = CCC_FWD_RING;
 static_assert(kFwdRing >= 2, "the ring needs a stage being filled and one being read");
 constexpr int kFwdThreads = 256;
 template <int V>
-constexpr size_t fwd_ring_bytes(int threads) {
-  return size_t(threads) * kFwdRing * kFwdGroup * (2 * V);
+constexpr size_t fwd_ring_bytes(int threads, int group = kFwdGroup) {
+  return size_t(threads) * kFwdRing * group * (2 * V);
 }
 extern __shared__ __align__(16) char fwd_dyn_smem[];
 
@@ -193,7 +193,7 @@ extern __shared__ __align__(16) char fwd_dyn_smem[];
 #endif
 // W3: a contiguous [D, 3] weight read with vectors (its own instance, so the
 // width-four kernel's register allocation is untouched).
-template <int V, int ACT, bool IDS = false, bool W3 = false>
+template <int V, int ACT, bool IDS = false, bool W3 = false, int GT = kFwdGroup>
 __global__ void __launch_bounds__(kFwdThreads, IDS ? CCC_FWD_IDS_BLOCKS : 3) fwd_clv_kernel(FwdArgs a) {
   if (blockDim.x * blockDim.y * blockDim.z != kFwdThreads) return;  // the ring layout assumes it
   pdl_wait();     // inputs may come from the previous kernel in the stream
@@ -202,7 +202,8 @@ __global__ void __launch_bounds__(kFwdThreads, IDS ? CCC_FWD_IDS_BLOCKS : 3) fwd
   using Raw = typename VT::Raw;
   constexpr int H = V / 2;  // channel pairs
   constexpr int RB = int(sizeof(Raw));
-  constexpr int G = kFwdGroup;
+  constexpr int G = GT;
+  static_assert(G % 3 == 0, "a group is a whole number of window periods");
   __shared__ __align__(16) float ws[(kWidth + 1) * kMaxBlockChannels];
   if (block_rejects_cu_seqlens(a.seqs, a.status)) return;
   const int n_blk = blockDim.x * V;
@@ -499,7 +500,11 @@ static cudaError_t fwd_smem_attributes() {
   cudaError_t err = cudaSuccess;
   for (auto f : {fwd_clv_kernel<4, kActSilu>, fwd_clv_kernel<4, kActNone>,
                  fwd_clv_kernel<4, kActSilu, true>, fwd_clv_kernel<4, kActNone, true>,
-                 fwd_clv_kernel<4, kActSilu, false, true>, fwd_clv_kernel<4, kActNone, false, true>})
+                 fwd_clv_kernel<4, kActSilu, false, true>, fwd_clv_kernel<4, kActNone, false, true>,
+                 fwd_clv_kernel<4, kActSilu, false, false, kFwdGroupShort>,
+                 fwd_clv_kernel<4, kActNone, false, false, kFwdGroupShort>,
+                 fwd_clv_kernel<4, kActSilu, false, true, kFwdGroupShort>,
+                 fwd_clv_kernel<4, kActNone, false, true, kFwdGroupShort>})
     if (err == cudaSuccess) err = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (err == cudaSuccess) g_fwd_attr_done.put(1);
   return err;
@@ -567,9 +572,15 @@ static cudaError_t launch_fwd_act(const FwdArgs& a, const FwdPlan& p, cudaStream
     if (p.vec == 4) {
       const cudaError_t err = fwd_smem_attributes();
       if (err != cudaSuccess) return err;
+      if (a.wr.w_vec3 && p.group == kFwdGroupShort)
+        return launch_kernel(fwd_clv_kernel<4, ACT, false, true, kFwdGroupShort>, grid, block,
+                             fwd_ring_bytes<4>(p.tx * p.ty, kFwdGroupShort), stream, true, a);
       if (a.wr.w_vec3)
         return launch_kernel(fwd_clv_kernel<4, ACT, false, true>, grid, block,
                              fwd_ring_bytes<4>(p.tx * p.ty), stream, true, a);
+      if (p.group == kFwdGroupShort)
+        return launch_kernel(fwd_clv_kernel<4, ACT, false, false, kFwdGroupShort>, grid, block,
+                             fwd_ring_bytes<4>(p.tx * p.ty, kFwdGroupShort), stream, true, a);
       return launch_kernel(fwd_clv_kernel<4, ACT>, grid, block, fwd_ring_bytes<4>(p.tx * p.ty),
                            stream, true, a);
     }

@@ -114,6 +114,7 @@ struct FwdPlan {
   int tx, ty;    // block shape (channel-last)
   unsigned gx, gy;
   int64_t seg_len, n_seg;
+  int group;     // channel-last vector forward: tokens per ring stage
 };
 
 using BwdPlan = FwdPlan;
@@ -137,6 +138,13 @@ BwdPlan plan_bwd(int kind, int vec_ok, int64_t Q, int D, int64_t rows, int sm_co
                  bool ids = false);
 // Rows of FP32 partial sums the backward writes.
 int64_t bwd_partial_rows(const BwdPlan& p, int B, bool packed);
+
+// Tokens per ring stage of the channel-last vector forward (a multiple of 3;
+// its plans cut segments in multiples of it): six, or three when a thread gets
+// fewer than kFwdShortTokens tokens (the first rows are computed sooner; with
+// long ranges the longer groups keep more bytes in flight).
+constexpr int kFwdGroupLong = 6, kFwdGroupShort = 3;
+constexpr int kFwdShortTokens = 48;
 
 // Resident blocks per SM of the channel-last kernels (SiLU instance), cached.
 int fwd_blocks_per_sm(int vec);
