@@ -47,8 +47,8 @@ L2_BYTES = 129 * 2 ** 20
 # finalize kernel -- from one ncu capture of those two kernels
 # (profiles/traffic_dense_large_backward.md), per launch.  Valid only for the
 # kernel sources whose digest is recorded here (null otherwise).
-TRAFFIC = {"sources_sha256": "3e063dfb9eb110a349f514d7b28d907465199808843d8cc0db3f87baaff2b4d2",
-           "bytes_per_launch": (1349953280 + 638793216) + (1543424 + 0)}
+TRAFFIC = {"sources_sha256": "86eb6996d54c8a189cd9d8c6879eaa92a446b8a509bb83a0ae802a9d8336b319",
+           "bytes_per_launch": (1349961216 + 638923520) + (1543168 + 0)}
 
 
 # The sources the dominant call's kernels (the channel-last backward and the
