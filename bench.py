@@ -47,8 +47,8 @@ L2_BYTES = 129 * 2 ** 20
 # finalize kernel -- from one ncu capture of those two kernels
 # (profiles/traffic_dense_large_backward.md), per launch.  Valid only for the
 # kernel sources whose digest is recorded here (null otherwise).
-TRAFFIC = {"sources_sha256": "86eb6996d54c8a189cd9d8c6879eaa92a446b8a509bb83a0ae802a9d8336b319",
-           "bytes_per_launch": (1349961216 + 638923520) + (1543168 + 0)}
+TRAFFIC = {"sources_sha256": "7888c273d1355680cc10a7e3fef0e4335be3bf9c056971f9d2ebc2946a483e46",
+           "bytes_per_launch": (1349366528 + 635992320) + (724224 + 0)}
 
 
 # The sources the dominant call's kernels (the channel-last backward and the

@@ -306,10 +306,8 @@ __global__ void __launch_bounds__(kGeneralThreads) bwd_cl_kernel(BwdArgs a) {
 // (the three tokens after the piece, which emit its last dx rows); the few
 // tokens at sequence edges take the general step, loading their rows directly
 // (prefetched into L2 when the piece starts).
-// 128-thread blocks (two resident per SM for V = 8, four for V = 4).
-#ifndef CCC_BWD_MIN_BLOCKS
-#define CCC_BWD_MIN_BLOCKS 2
-#endif
+// 256-thread blocks for V = 8 (one resident per SM), 128-thread blocks for
+// V = 4 (four per SM).
 #ifndef CCC_BWD_RING
 #define CCC_BWD_RING 3
 #endif
@@ -319,7 +317,14 @@ template <int V>
 constexpr size_t bwd_ring_bytes(int threads) {
   return size_t(threads) * kBwdRing * 3 * 2 * (2 * V);
 }
-constexpr int kBwdThreads = 128;
+// Threads a block: 256 for eight channels a thread (one block an SM, ~240
+// registers), 128 for four (four blocks an SM).  Measured: at eight channels,
+// 256-thread blocks took 307 us against 311 us at 8 x 5120 x 8192 and 78.8
+// against 80.5 us on 16 packed sequences (half the partial rows); at four,
+// 25.0 against 22.9 us at 4 x 2048 x 1536.
+template <int V>
+__host__ __device__ constexpr int bwd_threads() { return V == 8 ? 256 : 128; }
+constexpr int kBwdThreads = 128;  // the four-channel block
 
 // With IDS (V = 4; dense calls without states), every token carries a sequence
 // id (cuDNN page, seq_idx[B, T]): a tap joins two tokens only when their ids
@@ -331,14 +336,15 @@ constexpr int kBwdThreads = 128;
 #define CCC_BWD_IDS_BLOCKS 3  // resident blocks an SM asked of the id instance
 #endif
 template <int V, int ACT, bool IDS = false>
-__global__ void __launch_bounds__(kBwdThreads, V == 8 ? CCC_BWD_MIN_BLOCKS : (IDS ? CCC_BWD_IDS_BLOCKS : 4))
+__global__ void __launch_bounds__(bwd_threads<V>(), V == 8 ? 1 : (IDS ? CCC_BWD_IDS_BLOCKS : 4))
     bwd_clv_kernel(BwdArgs a) {
   using VT = Vec<V>;
   using Raw = typename VT::Raw;
   constexpr int H = V / 2;  // channel pairs
   constexpr int RB = int(sizeof(Raw));
   __shared__ __align__(16) float wsm[(kWidth + 1) * kMaxBlockChannels];
-  if (blockDim.x * blockDim.y * blockDim.z != kBwdThreads) return;  // the ring layout assumes it
+  constexpr int NT = bwd_threads<V>();
+  if (blockDim.x * blockDim.y * blockDim.z != NT) return;  // the ring layout assumes it
   pdl_wait();  // inputs may come from the previous kernel in the stream
   if (block_rejects_cu_seqlens(a.seqs, a.status)) return;
   const int n_blk = blockDim.x * V;
@@ -357,13 +363,13 @@ __global__ void __launch_bounds__(kBwdThreads, V == 8 ? CCC_BWD_MIN_BLOCKS : (ID
     float2 w[H][kWidth], b[H];
     bool have_w = false;  // the weights are loaded once the first ring groups are in flight
     // this thread's ring: slot (stage, row u, tensor t) at byte
-    // (((stage * 3 + u) * 2 + t) * kBwdThreads + tid) * RB past the ring base: the
+    // (((stage * 3 + u) * 2 + t) * NT + tid) * RB past the ring base: the
     // block size is a compile-time constant, so every offset is an immediate
     const int tid = threadIdx.y * blockDim.x + threadIdx.x;
-    const char* ring = reinterpret_cast<const char*>(bwd_dyn_smem) + bwd_red_bytes<V>(kBwdThreads) +
+    const char* ring = reinterpret_cast<const char*>(bwd_dyn_smem) + bwd_red_bytes<V>(NT) +
                        size_t(tid) * RB;
     const uint32_t ring_s = smem_u32(ring);
-    constexpr uint32_t slot = uint32_t(kBwdThreads) * RB;
+    constexpr uint32_t slot = uint32_t(NT) * RB;
 
     int64_t q = seg * a.seg_len;
     const int64_t q_end = q + a.seg_len < a.seqs.Q ? q + a.seg_len : a.seqs.Q;
@@ -1092,7 +1098,7 @@ __global__ void bwd_empty_kernel(const uint16_t* dfin, uint16_t* dinit, int64_t 
 
 // ---- host launchers ------------------------------------------------------------
 
-int bwd_block_threads(int vec) { return vec >= 4 ? kBwdThreads : 256; }
+int bwd_block_threads(int vec) { return vec == 8 ? bwd_threads<8>() : vec == 4 ? bwd_threads<4>() : 256; }
 
 // Dynamic shared memory of one channel-last backward block of `threads` threads.
 static size_t bwd_smem_bytes(int vec, int threads) {
@@ -1108,7 +1114,7 @@ static cudaError_t bwd_smem_attributes() {
   long long done = 0;
   if (g_bwd_attr_done.get(&done) && done) return cudaSuccess;
   cudaError_t err = cudaSuccess;
-  const int b8 = int(bwd_smem_bytes(8, kBwdThreads)), b4 = int(bwd_smem_bytes(4, kBwdThreads));
+  const int b8 = int(bwd_smem_bytes(8, bwd_threads<8>())), b4 = int(bwd_smem_bytes(4, bwd_threads<4>()));
   for (auto f : {bwd_clv_kernel<8, kActSilu>, bwd_clv_kernel<8, kActNone>})
     if (err == cudaSuccess) err = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, b8);
   for (auto f : {bwd_clv_kernel<4, kActSilu>, bwd_clv_kernel<4, kActNone>, bwd_clv_kernel<4, kActSilu, true>,
