@@ -328,7 +328,7 @@ static FwdPlan plan_bdt(int64_t rows) {
 FwdPlan plan_fwd(int kind, int vec, int64_t Q, int D, int64_t rows, int sm_count, bool ids) {
   if (ids) {  // kernels with id masks: the ring kernel (vec 4) or the general ones
     FwdPlan p = kind == kLayoutTimeContiguous ? plan_bdt(rows)
-                : vec == 4 ? plan_cl(4, Q, D, sm_count, fwd_ids_blocks_per_sm(4), 1, 12, 256, kFwdGroupLong)
+                : vec == 4 ? plan_cl(4, Q, D, sm_count, fwd_ids_blocks_per_sm(4), 1, 12, kFwdThreads, kFwdGroupLong)
                            : plan_cl(vec, Q, D, sm_count, fwd_ids_blocks_per_sm(vec), 1, 12,
                                      kGeneralThreads);
     p.ids = 1;
@@ -348,11 +348,12 @@ FwdPlan plan_fwd(int kind, int vec, int64_t Q, int D, int64_t rows, int sm_count
   // packed 16 x U[1,4096] x 2048 in two, 8x8192x5120 in eight).
   const int bps = fwd_blocks_per_sm(vec);
   const int64_t groups = ceil_div(D, vec);
-  const int64_t threads = int64_t(sm_count) * std::max(1, bps) * 256;
+  const int64_t threads = int64_t(sm_count) * std::max(1, bps) * kFwdThreads;
   const int64_t per_thread = ceil_div(std::max<int64_t>(Q, 1) * groups, std::max<int64_t>(threads, 1));
   const int waves = int(std::min<int64_t>(8, std::max<int64_t>(1, per_thread / 64)));
   const int group = per_thread < kFwdShortTokens ? kFwdGroupShort : kFwdGroupLong;
-  FwdPlan p = plan_cl(vec, Q, D, sm_count, bps, waves, 12, 256, vec == 4 ? group : 1);
+  FwdPlan p = plan_cl(vec, Q, D, sm_count, bps, waves, 12, vec == 4 ? kFwdThreads : kGeneralThreads,
+                      vec == 4 ? group : 1);
   p.group = group;
   return p;
 }

@@ -173,7 +173,6 @@ constexpr int kFwdGroup = kFwdGroupLong;  // tokens per ring stage (multiple of 
 #endif
 constexpr int kFwdRing = CCC_FWD_RING;
 static_assert(kFwdRing >= 2, "the ring needs a stage being filled and one being read");
-constexpr int kFwdThreads = 256;
 template <int V>
 constexpr size_t fwd_ring_bytes(int threads, int group = kFwdGroup) {
   return size_t(threads) * kFwdRing * group * (2 * V);
@@ -194,7 +193,7 @@ extern __shared__ __align__(16) char fwd_dyn_smem[];
 // W3: a contiguous [D, 3] weight read with vectors (its own instance, so the
 // width-four kernel's register allocation is untouched).
 template <int V, int ACT, bool IDS = false, bool W3 = false, int GT = kFwdGroup>
-__global__ void __launch_bounds__(kFwdThreads, IDS ? CCC_FWD_IDS_BLOCKS : 3) fwd_clv_kernel(FwdArgs a) {
+__global__ void __launch_bounds__(kFwdThreads, (IDS ? CCC_FWD_IDS_BLOCKS : 3) * 256 / kFwdThreads) fwd_clv_kernel(FwdArgs a) {
   if (blockDim.x * blockDim.y * blockDim.z != kFwdThreads) return;  // the ring layout assumes it
   pdl_wait();     // inputs may come from the previous kernel in the stream
   pdl_release();
@@ -518,8 +517,8 @@ int fwd_blocks_per_sm(int vec) {
   int n = 0;
   fwd_smem_attributes();
   const cudaError_t err =
-      vec == 4 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fwd_clv_kernel<4, kActSilu>, 256,
-                                                               fwd_ring_bytes<4>(256))
+      vec == 4 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fwd_clv_kernel<4, kActSilu>, kFwdThreads,
+                                                               fwd_ring_bytes<4>(kFwdThreads))
                : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fwd_cl_kernel<1, kActSilu>, 256, 0);
   if (err == cudaSuccess && n > 0) {
     cache.put(n);
