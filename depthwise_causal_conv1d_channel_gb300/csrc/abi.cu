@@ -289,12 +289,12 @@ namespace ccc {
 // the token ranges are sized so the grid holds about `waves` full waves of
 // resident blocks, each range at least `min_seg` tokens long.
 static FwdPlan plan_cl(int vec, int64_t Q, int D, int sm_count, int blocks_per_sm, int waves,
-                       int64_t min_seg, int threads, int64_t seg_multiple = 1) {
+                       int64_t min_seg, int threads, int64_t seg_multiple = 1, int max_tx = 32) {
   FwdPlan p{};
   p.kind = kLayoutChannelLast;
   p.vec = vec;
   const int64_t G = ceil_div(D, vec);
-  p.tx = int(std::min<int64_t>(32, next_pow2(G)));
+  p.tx = int(std::min<int64_t>(max_tx, next_pow2(G)));
   p.ty = threads / p.tx;
   p.gx = unsigned(ceil_div(G, p.tx));
   const int64_t want = std::max<int64_t>(1, int64_t(sm_count) * std::max(1, blocks_per_sm) * waves);
@@ -386,7 +386,16 @@ BwdPlan plan_bwd(int kind, int vec, int64_t Q, int D, int64_t rows, int sm_count
   }
   // segments of a multiple of three tokens: the vector kernel's steady groups
   // of three then cover a whole segment inside a sequence, head and tail included
-  return plan_cl(vec, Q, D, sm_count, bwd_blocks_per_sm(vec), 1, 18, bwd_block_threads(vec), 3);
+  const BwdPlan p = plan_cl(vec, Q, D, sm_count, bwd_blocks_per_sm(vec), 1, 18, bwd_block_threads(vec), 3);
+  if (vec == 8) {
+    // Blocks two warps wide along channels (512 channels) when that puts more
+    // blocks in the wave: 8 x 5120 x 8192 takes 10 x 15 blocks instead of 20 x 7
+    // (302 against 308 us); where both fill the SMs, 32 lanes wide measured
+    // faster (16 packed sequences at D = 2048: 78.4 against 79.8 us).
+    const BwdPlan w = plan_cl(vec, Q, D, sm_count, bwd_blocks_per_sm(vec), 1, 18, bwd_block_threads(vec), 3, 64);
+    if (int64_t(w.gx) * w.gy > int64_t(p.gx) * p.gy) return w;
+  }
+  return p;
 }
 
 int64_t bwd_partial_rows(const BwdPlan& p, int B, bool packed) {

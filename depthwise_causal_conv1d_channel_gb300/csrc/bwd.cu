@@ -342,7 +342,7 @@ __global__ void __launch_bounds__(bwd_threads<V>(), V == 8 ? 1 : (IDS ? CCC_BWD_
   using Raw = typename VT::Raw;
   constexpr int H = V / 2;  // channel pairs
   constexpr int RB = int(sizeof(Raw));
-  __shared__ __align__(16) float wsm[(kWidth + 1) * kMaxBlockChannels];
+  __shared__ __align__(16) float wsm[(kWidth + 1) * (V == 8 ? 2 * kMaxBlockChannels : kMaxBlockChannels)];
   constexpr int NT = bwd_threads<V>();
   if (blockDim.x * blockDim.y * blockDim.z != NT) return;  // the ring layout assumes it
   pdl_wait();  // inputs may come from the previous kernel in the stream

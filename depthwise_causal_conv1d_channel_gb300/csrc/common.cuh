@@ -362,7 +362,8 @@ struct WeightRef {
   int w_vec3;       // contiguous [D, 3] and bias, 16-byte aligned: read with vectors
 };
 
-// Widest channel slice a block stages: 32 threads x 8 channels.
+// Widest channel slice a block stages: 32 threads x 8 channels (the
+// eight-channel backward, whose blocks may be 64 threads wide, sizes its own).
 constexpr int kMaxBlockChannels = 256;
 
 // The weight loaders below all return the weights and the bias times one half
