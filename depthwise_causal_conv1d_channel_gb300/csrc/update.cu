@@ -172,17 +172,18 @@ __global__ void __launch_bounds__(32 * TY, MULTI ? CCC_UPDATE_MULTI_BLOCKS : 1) 
       if (valid && j < a.L) xq[j - 1] = Vec<8>::ld(a.x + int64_t(b0) * a.x_sb + int64_t(j) * a.x_sl + d0);
   }
   if (valid) weights_direct2<8>(a.wr, d0, w, bias);  // after the state loads are in flight
-#pragma unroll
-  for (int r = 0; r < R; ++r)
-    if (b0 + r < a.B)
-#pragma unroll
-      for (int j = 0; j < kState; ++j)
-        if (lane + 32 * j < n_chunks) sbuf[wy][r][lane + 32 * j] = sr[r][j];
-  __syncwarp();
   if constexpr (!MULTI) {
+  // Row by row: the state run of row r goes through shared memory, its output
+  // and new state are computed and stored, then row r + 1, whose loads (issued
+  // with row r's above) may still be landing.
 #pragma unroll
   for (int r = 0; r < R; ++r) {
-    if (b0 + r >= a.B || !valid) continue;
+    if (b0 + r >= a.B) break;
+#pragma unroll
+    for (int j = 0; j < kState; ++j)
+      if (lane + 32 * j < n_chunks) sbuf[wy][r][lane + 32 * j] = sr[r][j];
+    __syncwarp();
+    if (valid) {
     union { uint4 q[kState]; uint16_t h[3 * 8]; } u;
 #pragma unroll
     for (int j = 0; j < kState; ++j) u.q[j] = sbuf[wy][r][kState * lane + j];
@@ -219,8 +220,21 @@ __global__ void __launch_bounds__(32 * TY, MULTI ? CCC_UPDATE_MULTI_BLOCKS : 1) 
     }
 #pragma unroll
     for (int j = 0; j < kState; ++j) sbuf[wy][r][kState * lane + j] = u.q[j];
+    }
+    __syncwarp();
+    uint4* run = reinterpret_cast<uint4*>(a.state + (int64_t(b0 + r) * a.D + int64_t(g0) * 8) * kState);
+#pragma unroll
+    for (int j = 0; j < kState; ++j)
+      if (lane + 32 * j < n_chunks) run[lane + 32 * j] = sbuf[wy][r][lane + 32 * j];
   }
   } else {
+#pragma unroll
+  for (int r = 0; r < R; ++r)
+    if (b0 + r < a.B)
+#pragma unroll
+      for (int j = 0; j < kState; ++j)
+        if (lane + 32 * j < n_chunks) sbuf[wy][r][lane + 32 * j] = sr[r][j];
+  __syncwarp();
 #pragma unroll
   for (int r = 0; r < R; ++r) {
     if (b0 + r >= a.B || !valid) continue;
@@ -280,7 +294,6 @@ __global__ void __launch_bounds__(32 * TY, MULTI ? CCC_UPDATE_MULTI_BLOCKS : 1) 
 #pragma unroll
     for (int j = 0; j < kState; ++j) sbuf[wy][r][kState * lane + j] = u.q[j];
   }
-  }
   __syncwarp();
 #pragma unroll
   for (int r = 0; r < R; ++r) {
@@ -290,16 +303,23 @@ __global__ void __launch_bounds__(32 * TY, MULTI ? CCC_UPDATE_MULTI_BLOCKS : 1) 
     for (int j = 0; j < kState; ++j)
       if (lane + 32 * j < n_chunks) run[lane + 32 * j] = sbuf[wy][r][lane + 32 * j];
   }
+  }
 }
+
+#ifndef CCC_UPDATE_W8_ROWS
+#define CCC_UPDATE_W8_ROWS 1  // batch rows a warp of the one-token instance
+#endif
 
 template <int ACT>
 static cudaError_t launch_update_w8(const UpdArgs& a, cudaStream_t stream) {
-  constexpr int TY = 4, R = 1;
+  constexpr int TY = 4, R = CCC_UPDATE_W8_ROWS;
   const int64_t groups = a.D / 8;
-  dim3 grid(unsigned((groups + 31) / 32), unsigned((a.B + int64_t(TY) * R - 1) / (int64_t(TY) * R)));
-  if (a.L == 1)
+  if (a.L == 1) {
+    dim3 grid(unsigned((groups + 31) / 32), unsigned((a.B + int64_t(TY) * R - 1) / (int64_t(TY) * R)));
     return launch_kernel(update_w8_kernel<ACT, TY, R, false>, grid, dim3(32, TY), 0, stream, true, a);
-  return launch_kernel(update_w8_kernel<ACT, TY, R, true>, grid, dim3(32, TY), 0, stream, true, a);
+  }
+  dim3 grid(unsigned((groups + 31) / 32), unsigned((a.B + int64_t(TY) - 1) / int64_t(TY)));
+  return launch_kernel(update_w8_kernel<ACT, TY, 1, true>, grid, dim3(32, TY), 0, stream, true, a);
 }
 
 #ifndef CCC_UPDATE_ROWS
