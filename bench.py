@@ -47,8 +47,8 @@ L2_BYTES = 129 * 2 ** 20
 # finalize kernel -- from one ncu capture of those two kernels
 # (profiles/traffic_dense_large_backward.md), per launch.  Valid only for the
 # kernel sources whose digest is recorded here (null otherwise).
-TRAFFIC = {"sources_sha256": "248737d8ec45c4b6ddb1ada960a1e331e5f4a715b289c0c210fb7cb0d6bc125e",
-           "bytes_per_launch": (1349991936 + 635016960) + (1543424 + 0)}
+TRAFFIC = {"sources_sha256": "ac1d9f1d1466aa4be310786bd10d24dc256162133d639c974a00e3be78b0d8ce",
+           "bytes_per_launch": (1350031104 + 635291648) + (1543424 + 0)}
 
 
 # The sources the dominant call's kernels (the channel-last backward and the

@@ -214,7 +214,8 @@ bool vec_ok(int V, const Problem& pb, std::initializer_list<const ccc_tensor*> a
 // eight, short ones the extra parallelism of four.
 int bwd_preferred_vec(int64_t Q, int D, int sm_count) {
   if (CCC_BWD_VEC) return CCC_BWD_VEC;
-  const int64_t resident_threads = int64_t(sm_count) * ccc::bwd_blocks_per_sm(8) * 128;
+  const int64_t resident_threads =
+      int64_t(sm_count) * ccc::bwd_blocks_per_sm(8) * ccc::bwd_block_threads(8);
   const int64_t tokens_per_thread = Q * ((D + 7) / 8) / std::max<int64_t>(resident_threads, 1);
   return tokens_per_thread >= 128 ? 8 : 4;
 }

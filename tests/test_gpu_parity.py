@@ -68,6 +68,9 @@ def check_bwd(inp, res):
 
 DENSE_CASES = [
     # (B, D, T, channel_last, options)
+    # eight channels a thread in blocks two warps wide, the last block column
+    # one channel group wide (D = 4104 = 64 * 64 + 8)
+    (1, 4104, 12000, True, dict(initial_states=True, grad=True)),
     (3, 264, 300, True, dict(initial_states=True, grad=True)),
     (2, 264, 300, True, dict(initial_states=True, grad=True, dfinal_states=True)),
     (2, 64, 37, True, dict(grad=True)),
