@@ -589,6 +589,21 @@ __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
+// Hint: bring `bytes` bytes from p into L2 (p 16-byte aligned, bytes a
+// multiple of 16).  One instruction for a whole contiguous run.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// Kernels launched as programmatic dependents may prefetch, before
+// pdl_wait(), inputs whose addresses need no memory read.  A prefetch only
+// moves lines into L2, the point of coherence for every SM, so the loads
+// after the wait still see everything the previous kernel wrote; the gain is
+// that the first loads' DRAM latency overlaps that kernel's tail.
+#ifndef CCC_PREWAIT_PREFETCH
+#define CCC_PREWAIT_PREFETCH 1
+#endif
+
 // ---- sequences -----------------------------------------------------------------
 //
 // A call's tokens form one index space q in [0, Q).  Dense calls: sequence n is

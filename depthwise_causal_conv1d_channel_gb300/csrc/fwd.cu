@@ -195,13 +195,30 @@ extern __shared__ __align__(16) char fwd_dyn_smem[];
 template <int V, int ACT, bool IDS = false, bool W3 = false, int GT = kFwdGroup>
 __global__ void __launch_bounds__(kFwdThreads, (IDS ? CCC_FWD_IDS_BLOCKS : 3) * 256 / kFwdThreads) fwd_clv_kernel(FwdArgs a) {
   if (blockDim.x * blockDim.y * blockDim.z != kFwdThreads) return;  // the ring layout assumes it
-  pdl_wait();     // inputs may come from the previous kernel in the stream
-  pdl_release();
   using VT = Vec<V>;
   using Raw = typename VT::Raw;
   constexpr int H = V / 2;  // channel pairs
   constexpr int RB = int(sizeof(Raw));
   constexpr int G = GT;
+#if CCC_PREWAIT_PREFETCH
+  // dense calls: the rows of the first ring groups and the three before them
+  // (measured: dense_state shape 11.9 -> 10.6 us, with seq_idx 15.2 -> 13.4 us;
+  // packed calls, whose first loads are a smaller share, 48.5 -> 48.7 us)
+  if (a.seqs.cu == nullptr) {
+    const int d0 = (blockIdx.x * blockDim.x + threadIdx.x) * V;
+    const int64_t seg = int64_t(blockIdx.y) * blockDim.y + threadIdx.y;
+    if (d0 < a.D && seg < a.n_seg) {
+      const int64_t q = seg * a.seg_len;
+      const int n = find_seq(a.seqs, q);
+      const int64_t t = q - int64_t(n) * a.seqs.T;  // token within its sequence
+      const int rows = int(min(min(a.seg_len, int64_t((kFwdRing - 1) * G)), a.seqs.T - t));
+      const uint16_t* xp = a.x + int64_t(n) * a.x_sb + t * a.x_st + d0;
+      for (int u = t < kState ? -int(t) : -kState; u < rows; ++u) prefetch_l2(xp + u * a.x_st);
+    }
+  }
+#endif
+  pdl_wait();     // inputs may come from the previous kernel in the stream
+  pdl_release();
   static_assert(G % 3 == 0, "a group is a whole number of window periods");
   __shared__ __align__(16) float ws[(kWidth + 1) * kMaxBlockChannels];
   if (block_rejects_cu_seqlens(a.seqs, a.status)) return;

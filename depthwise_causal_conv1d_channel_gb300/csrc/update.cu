@@ -136,8 +136,6 @@ __global__ void __launch_bounds__(256) update_kernel(UpdArgs a) {
 #endif
 template <int ACT, int TY, int R, bool MULTI>
 __global__ void __launch_bounds__(32 * TY, MULTI ? CCC_UPDATE_MULTI_BLOCKS : 1) update_w8_kernel(UpdArgs a) {
-  pdl_wait();
-  pdl_release();
   constexpr int kChunks = 32 * kState;  // 16-byte chunks of one warp-row of state
   __shared__ uint4 sbuf[TY][R][kChunks];
   const int lane = threadIdx.x, wy = threadIdx.y;
@@ -148,12 +146,26 @@ __global__ void __launch_bounds__(32 * TY, MULTI ? CCC_UPDATE_MULTI_BLOCKS : 1) 
   const bool valid = lane < n_lanes;
   const int d0 = (g0 + lane) * 8;
   const int b0 = (blockIdx.y * blockDim.y + wy) * R;
-  if (b0 >= a.B) return;  // the whole warp: it shares b0
-  float2 w[4][kWidth], bias[4];
-  uint4 sr[R][kState], xr[R];
   // L tokens a row: tokens are taken kTokChunk at a time, all loads of a chunk
   // in flight at once; the first chunk's go out with the state's
   constexpr int kTokChunk = 4;
+#if CCC_PREWAIT_PREFETCH
+  // the warp's state runs (16-byte aligned: D is a multiple of 8) and the x
+  // rows of its first tokens, one bulk prefetch each
+  if (lane < R && b0 + lane < a.B) {
+    const int64_t row = b0 + lane;
+    prefetch_l2_bulk(a.state + (row * a.D + int64_t(g0) * 8) * kState, uint32_t(n_chunks) * 16);
+    prefetch_l2_bulk(a.x + row * a.x_sb + int64_t(g0) * 8, uint32_t(n_lanes) * 16);
+  }
+  if (MULTI && lane >= 1 && lane < kTokChunk && lane < a.L && b0 < a.B)
+    prefetch_l2_bulk(a.x + int64_t(b0) * a.x_sb + int64_t(lane) * a.x_sl + int64_t(g0) * 8,
+                     uint32_t(n_lanes) * 16);
+#endif
+  pdl_wait();
+  pdl_release();
+  if (b0 >= a.B) return;  // the whole warp: it shares b0
+  float2 w[4][kWidth], bias[4];
+  uint4 sr[R][kState], xr[R];
   uint4 xq[kTokChunk - 1] = {};  // tokens 1 .. kTokChunk - 1 of row b0 (MULTI, R == 1)
 #pragma unroll
   for (int r = 0; r < R; ++r) {
