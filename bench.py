@@ -47,8 +47,8 @@ L2_BYTES = 129 * 2 ** 20
 # finalize kernel -- from one ncu capture of those two kernels
 # (profiles/traffic_dense_large_backward.md), per launch.  Valid only for the
 # kernel sources whose digest is recorded here (null otherwise).
-TRAFFIC = {"sources_sha256": "ac1d9f1d1466aa4be310786bd10d24dc256162133d639c974a00e3be78b0d8ce",
-           "bytes_per_launch": (1350031104 + 635291648) + (1543424 + 0)}
+TRAFFIC = {"sources_sha256": "12f467c4b977da76bd6d8d041de8d17a150f3c1ce9f04cb081070921f544635e",
+           "bytes_per_launch": (1349999616 + 634830592) + (1543680 + 0)}
 
 
 # The sources the dominant call's kernels (the channel-last backward and the
