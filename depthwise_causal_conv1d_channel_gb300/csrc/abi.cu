@@ -289,8 +289,12 @@ namespace ccc {
 // Channel-last launch shape: a block is (tx channel groups) x (ty token ranges);
 // the token ranges are sized so the grid holds about `waves` full waves of
 // resident blocks, each range at least `min_seg` tokens long.
+#ifndef CCC_SEG_PER_SEQ
+#define CCC_SEG_PER_SEQ 1  // 0: dense segments over the whole token index too
+#endif
 static FwdPlan plan_cl(int vec, int64_t Q, int D, int sm_count, int blocks_per_sm, int waves,
-                       int64_t min_seg, int threads, int64_t seg_multiple = 1, int max_tx = 32) {
+                       int64_t min_seg, int threads, int64_t seg_multiple = 1, int max_tx = 32,
+                       int64_t T_seq = 0) {
   FwdPlan p{};
   p.kind = kLayoutChannelLast;
   p.vec = vec;
@@ -309,6 +313,21 @@ static FwdPlan plan_cl(int vec, int64_t Q, int D, int sm_count, int blocks_per_s
     n_seg = ceil_div(Q, seg);
     gy = ceil_div(n_seg, p.ty);
   }
+  // Dense calls: segments per sequence, so that no thread's range straddles a
+  // sequence end (such a thread restarts its ring and steps the sequence ends
+  // one token at a time, and the call waits for it), when that fits the same
+  // block rows the plan asked for at the same segment length.
+  p.seg_per_seq = 0;
+  if (CCC_SEG_PER_SEQ && T_seq > 0 && Q > T_seq && Q % T_seq == 0) {
+    const int64_t sps = ceil_div(T_seq, seg);
+    const int64_t n2 = (Q / T_seq) * sps;
+    const int64_t gy2 = ceil_div(n2, p.ty);
+    if (gy2 <= std::max<int64_t>(gy, want / p.gx) && gy2 <= 65535) {
+      p.seg_per_seq = sps;
+      n_seg = n2;
+      gy = gy2;
+    }
+  }
   p.gy = unsigned(gy);
   p.seg_len = seg;
   p.n_seg = n_seg;
@@ -326,12 +345,14 @@ static FwdPlan plan_bdt(int64_t rows) {
   return p;
 }
 
-FwdPlan plan_fwd(int kind, int vec, int64_t Q, int D, int64_t rows, int sm_count, bool ids) {
+FwdPlan plan_fwd(int kind, int vec, int64_t Q, int D, int64_t rows, int sm_count, bool ids,
+                 int64_t T_seq) {
   if (ids) {  // kernels with id masks: the ring kernel (vec 4) or the general ones
     FwdPlan p = kind == kLayoutTimeContiguous ? plan_bdt(rows)
-                : vec == 4 ? plan_cl(4, Q, D, sm_count, fwd_ids_blocks_per_sm(4), 1, 12, kFwdThreads, kFwdGroupLong)
+                : vec == 4 ? plan_cl(4, Q, D, sm_count, fwd_ids_blocks_per_sm(4), 1, 12, kFwdThreads,
+                                     kFwdGroupLong, 32, T_seq)
                            : plan_cl(vec, Q, D, sm_count, fwd_ids_blocks_per_sm(vec), 1, 12,
-                                     kGeneralThreads);
+                                     kGeneralThreads, 1, 32, T_seq);
     p.ids = 1;
     p.group = kFwdGroupLong;
     if (kind == kLayoutTimeContiguous) p.vec = 1;
@@ -354,18 +375,19 @@ FwdPlan plan_fwd(int kind, int vec, int64_t Q, int D, int64_t rows, int sm_count
   const int waves = int(std::min<int64_t>(8, std::max<int64_t>(1, per_thread / 64)));
   const int group = per_thread < kFwdShortTokens ? kFwdGroupShort : kFwdGroupLong;
   FwdPlan p = plan_cl(vec, Q, D, sm_count, bps, waves, 12, vec == 4 ? kFwdThreads : kGeneralThreads,
-                      vec == 4 ? group : 1);
+                      vec == 4 ? group : 1, 32, T_seq);
   p.group = group;
   return p;
 }
 
-BwdPlan plan_bwd(int kind, int vec, int64_t Q, int D, int64_t rows, int sm_count, bool ids) {
+BwdPlan plan_bwd(int kind, int vec, int64_t Q, int D, int64_t rows, int sm_count, bool ids,
+                 int64_t T_seq) {
   if (ids) {  // kernels with id masks: the ring kernel (vec 4) or the general ones
     BwdPlan p = kind == kLayoutTimeContiguous ? plan_bdt(rows)
                 : vec == 4 ? plan_cl(4, Q, D, sm_count, bwd_ids_blocks_per_sm(4), 1, 18,
-                                     bwd_block_threads(4), 3)
+                                     bwd_ids_block_threads(4), 3, 32, T_seq)
                            : plan_cl(vec, Q, D, sm_count, bwd_ids_blocks_per_sm(vec), 1, 18,
-                                     kGeneralThreads);
+                                     kGeneralThreads, 1, 32, T_seq);
     p.ids = 1;
     if (kind == kLayoutTimeContiguous) p.vec = 1;
     return p;
@@ -387,13 +409,15 @@ BwdPlan plan_bwd(int kind, int vec, int64_t Q, int D, int64_t rows, int sm_count
   }
   // segments of a multiple of three tokens: the vector kernel's steady groups
   // of three then cover a whole segment inside a sequence, head and tail included
-  const BwdPlan p = plan_cl(vec, Q, D, sm_count, bwd_blocks_per_sm(vec), 1, 18, bwd_block_threads(vec), 3);
+  const BwdPlan p = plan_cl(vec, Q, D, sm_count, bwd_blocks_per_sm(vec), 1, 18, bwd_block_threads(vec), 3,
+                            32, T_seq);
   if (vec == 8) {
     // Blocks two warps wide along channels (512 channels) when that puts more
     // blocks in the wave: 8 x 5120 x 8192 takes 10 x 15 blocks instead of 20 x 7
     // (302 against 308 us); where both fill the SMs, 32 lanes wide measured
     // faster (16 packed sequences at D = 2048: 78.4 against 79.8 us).
-    const BwdPlan w = plan_cl(vec, Q, D, sm_count, bwd_blocks_per_sm(vec), 1, 18, bwd_block_threads(vec), 3, 64);
+    const BwdPlan w = plan_cl(vec, Q, D, sm_count, bwd_blocks_per_sm(vec), 1, 18, bwd_block_threads(vec), 3,
+                              64, T_seq);
     if (int64_t(w.gx) * w.gy > int64_t(p.gx) * p.gy) return w;
   }
   return p;
@@ -468,9 +492,11 @@ ccc_status ccc_conv1d_fwd(const ccc_tensor* x, const ccc_tensor* weight, const c
                       ? (bdt_vec_ok(pb, {x, out}) && !pb.ids ? 8 : 1)
                       : pick_vec(4, pb, {x, out}, {initial_states, final_states});
   const int64_t rows = pb.packed ? pb.D : int64_t(pb.B) * pb.D;
-  const ccc::FwdPlan p = ccc::plan_fwd(pb.layout, vec, a.seqs.Q, pb.D, rows, sms, pb.ids);
+  const ccc::FwdPlan p = ccc::plan_fwd(pb.layout, vec, a.seqs.Q, pb.D, rows, sms, pb.ids,
+                                       pb.packed ? 0 : pb.T);
   a.seg_len = p.seg_len;
   a.n_seg = p.n_seg;
+  a.seg_per_seq = p.seg_per_seq;
   return ccc::launch_fwd(a, p, activation, stream) == cudaSuccess ? CCC_OK : CCC_ERR_CUDA;
 }
 
@@ -480,7 +506,7 @@ static bool bwd_plan_for(const Problem& pb, int vec, bool ids, ccc::BwdPlan& p) 
   if (sms <= 0) return false;
   const int64_t Q = pb.packed ? pb.T : int64_t(pb.B) * pb.T;
   const int64_t rows = pb.packed ? pb.D : int64_t(pb.B) * pb.D;
-  p = ccc::plan_bwd(pb.layout, vec, Q, pb.D, rows, sms, ids);
+  p = ccc::plan_bwd(pb.layout, vec, Q, pb.D, rows, sms, ids, pb.packed ? 0 : pb.T);
   return true;
 }
 
@@ -597,6 +623,7 @@ ccc_status ccc_conv1d_bwd(const ccc_tensor* x, const ccc_tensor* weight, const c
   a.D = pb.D;
   a.seg_len = p.seg_len;
   a.n_seg = p.n_seg;
+  a.seg_per_seq = p.seg_per_seq;
   a.ws = static_cast<float*>(workspace);
   a.status = d_status;
 

@@ -282,8 +282,8 @@ __global__ void __launch_bounds__(kGeneralThreads) bwd_cl_kernel(BwdArgs a) {
   if (active) {
     float w[V][kWidth], b[V];
     weights_from_smem<V>(wsm, n_blk, threadIdx.x * V, w, b);
-    const int64_t q0 = seg * a.seg_len;
-    const int64_t q1 = q0 + a.seg_len < a.seqs.Q ? q0 + a.seg_len : a.seqs.Q;
+    int64_t q0, q1;
+    seg_range(a.seqs, seg, a.seg_len, a.seg_per_seq, q0, q1);
     const bool dense = a.seqs.cu == nullptr;
     const Stream xs{d0, dense ? a.x_sb - a.seqs.T * a.x_st : 0, a.x_st};
     const Stream gs{d0, dense ? a.g_sb - a.seqs.T * a.g_st : 0, a.g_st};
@@ -318,13 +318,17 @@ constexpr size_t bwd_ring_bytes(int threads) {
   return size_t(threads) * kBwdRing * 3 * 2 * (2 * V);
 }
 // Threads a block: 256 for eight channels a thread (one block an SM, ~240
-// registers), 128 for four (four blocks an SM).  Measured: at eight channels,
+// registers) and for four (two blocks an SM, 128 registers); 128 for the id
+// instance (~150 registers, three blocks an SM).  Measured: at eight channels,
 // 256-thread blocks took 307 us against 311 us at 8 x 5120 x 8192 and 78.8
-// against 80.5 us on 16 packed sequences (half the partial rows); at four,
-// 25.0 against 22.9 us at 4 x 2048 x 1536.
-template <int V>
-__host__ __device__ constexpr int bwd_threads() { return V == 8 ? 256 : 128; }
-constexpr int kBwdThreads = 128;  // the four-channel block
+// against 80.5 us on 16 packed sequences (half the partial rows).  At four,
+// with segments planned per sequence, 4 x 2048 x 1536 took 20.9-21.1 us in
+// 256-thread blocks against 21.7-21.8 us in 128 and 21.5 us in 512: the warp
+// scheduler favours a block's older warps, so with four blocks an SM the
+// last-placed block ran its loop about 4 us behind the first and finished
+// with the SM mostly idle.
+template <int V, bool IDS = false>
+__host__ __device__ constexpr int bwd_threads() { return V == 8 || !IDS ? 256 : 128; }
 
 // With IDS (V = 4; dense calls without states), every token carries a sequence
 // id (cuDNN page, seq_idx[B, T]): a tap joins two tokens only when their ids
@@ -336,14 +340,14 @@ constexpr int kBwdThreads = 128;  // the four-channel block
 #define CCC_BWD_IDS_BLOCKS 3  // resident blocks an SM asked of the id instance
 #endif
 template <int V, int ACT, bool IDS = false>
-__global__ void __launch_bounds__(bwd_threads<V>(), V == 8 ? 1 : (IDS ? CCC_BWD_IDS_BLOCKS : 4))
+__global__ void __launch_bounds__(bwd_threads<V, IDS>(), V == 8 ? 1 : (IDS ? CCC_BWD_IDS_BLOCKS : 2))
     bwd_clv_kernel(BwdArgs a) {
   using VT = Vec<V>;
   using Raw = typename VT::Raw;
   constexpr int H = V / 2;  // channel pairs
   constexpr int RB = int(sizeof(Raw));
   __shared__ __align__(16) float wsm[(kWidth + 1) * (V == 8 ? 2 * kMaxBlockChannels : kMaxBlockChannels)];
-  constexpr int NT = bwd_threads<V>();
+  constexpr int NT = bwd_threads<V, IDS>();
   if (blockDim.x * blockDim.y * blockDim.z != NT) return;  // the ring layout assumes it
   pdl_wait();  // inputs may come from the previous kernel in the stream
   if (block_rejects_cu_seqlens(a.seqs, a.status)) return;
@@ -371,8 +375,8 @@ __global__ void __launch_bounds__(bwd_threads<V>(), V == 8 ? 1 : (IDS ? CCC_BWD_
     const uint32_t ring_s = smem_u32(ring);
     constexpr uint32_t slot = uint32_t(NT) * RB;
 
-    int64_t q = seg * a.seg_len;
-    const int64_t q_end = q + a.seg_len < a.seqs.Q ? q + a.seg_len : a.seqs.Q;
+    int64_t q, q_end;
+    seg_range(a.seqs, seg, a.seg_len, a.seg_per_seq, q, q_end);
     const bool dense = a.seqs.cu == nullptr;
     int n = find_seq(a.seqs, q);
     using P0 = std::integral_constant<int, 0>;
@@ -1099,6 +1103,7 @@ __global__ void bwd_empty_kernel(const uint16_t* dfin, uint16_t* dinit, int64_t 
 // ---- host launchers ------------------------------------------------------------
 
 int bwd_block_threads(int vec) { return vec == 8 ? bwd_threads<8>() : vec == 4 ? bwd_threads<4>() : 256; }
+int bwd_ids_block_threads(int vec) { return vec == 4 ? bwd_threads<4, true>() : kGeneralThreads; }
 
 // Dynamic shared memory of one channel-last backward block of `threads` threads.
 static size_t bwd_smem_bytes(int vec, int threads) {
@@ -1114,12 +1119,14 @@ static cudaError_t bwd_smem_attributes() {
   long long done = 0;
   if (g_bwd_attr_done.get(&done) && done) return cudaSuccess;
   cudaError_t err = cudaSuccess;
-  const int b8 = int(bwd_smem_bytes(8, bwd_threads<8>())), b4 = int(bwd_smem_bytes(4, bwd_threads<4>()));
+  const int b8 = int(bwd_smem_bytes(8, bwd_threads<8>())), b4 = int(bwd_smem_bytes(4, bwd_threads<4>())),
+            b4i = int(bwd_smem_bytes(4, bwd_threads<4, true>()));
   for (auto f : {bwd_clv_kernel<8, kActSilu>, bwd_clv_kernel<8, kActNone>})
     if (err == cudaSuccess) err = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, b8);
-  for (auto f : {bwd_clv_kernel<4, kActSilu>, bwd_clv_kernel<4, kActNone>, bwd_clv_kernel<4, kActSilu, true>,
-                 bwd_clv_kernel<4, kActNone, true>})
+  for (auto f : {bwd_clv_kernel<4, kActSilu>, bwd_clv_kernel<4, kActNone>})
     if (err == cudaSuccess) err = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, b4);
+  for (auto f : {bwd_clv_kernel<4, kActSilu, true>, bwd_clv_kernel<4, kActNone, true>})
+    if (err == cudaSuccess) err = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, b4i);
   if (err == cudaSuccess) g_bwd_attr_done.put(1);
   return err;
 }
@@ -1152,8 +1159,9 @@ int bwd_ids_blocks_per_sm(int vec) {
   int n = 0;
   bwd_smem_attributes();
   const cudaError_t err =
-      vec == 4 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, bwd_clv_kernel<4, kActSilu, true>, kBwdThreads,
-                                                               bwd_smem_bytes(4, kBwdThreads))
+      vec == 4 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, bwd_clv_kernel<4, kActSilu, true>,
+                                                               bwd_threads<4, true>(),
+                                                               bwd_smem_bytes(4, bwd_threads<4, true>()))
                : cudaOccupancyMaxActiveBlocksPerMultiprocessor(
                      &n, bwd_cl_kernel<1, kActSilu, true>, kGeneralThreads, bwd_red_bytes<1>(kGeneralThreads));
   if (err == cudaSuccess && n > 0) {

@@ -631,6 +631,24 @@ __device__ __forceinline__ int find_seq(const Seqs& s, int64_t q) {
   return lo;
 }
 
+// Token range [q, q_end) of thread range (segment) seg of seg_len tokens.
+// With seg_per_seq > 0 (dense calls) every sequence has its own segments, the
+// last one shorter, so none straddles a sequence end; otherwise segments cut
+// the whole token index.
+__device__ __forceinline__ void seg_range(const Seqs& s, int64_t seg, int64_t seg_len,
+                                          int64_t seg_per_seq, int64_t& q, int64_t& q_end) {
+  int64_t end;
+  if (seg_per_seq > 0) {
+    const int64_t n = seg / seg_per_seq;
+    q = n * s.T + (seg - n * seg_per_seq) * seg_len;
+    end = (n + 1) * s.T;
+  } else {
+    q = seg * seg_len;
+    end = s.Q;
+  }
+  q_end = q + seg_len < end ? q + seg_len : end;
+}
+
 __device__ __forceinline__ void seq_bounds(const Seqs& s, int n, int64_t& lo, int64_t& hi) {
   if (!s.cu) {
     lo = int64_t(n) * s.T;

@@ -147,8 +147,8 @@ __global__ void __launch_bounds__(kGeneralThreads) fwd_cl_kernel(FwdArgs a) {
   if (d0 >= a.D || seg >= a.n_seg) return;
   float w[V][kWidth], b[V];
   weights_from_smem<V>(ws, n_blk, threadIdx.x * V, w, b);
-  const int64_t q0 = seg * a.seg_len;
-  const int64_t q1 = q0 + a.seg_len < a.seqs.Q ? q0 + a.seg_len : a.seqs.Q;
+  int64_t q0, q1;
+  seg_range(a.seqs, seg, a.seg_len, a.seg_per_seq, q0, q1);
   const bool dense = a.seqs.cu == nullptr;
   const Stream xs{d0, dense ? a.x_sb - a.seqs.T * a.x_st : 0, a.x_st};
   const Stream os{d0, dense ? a.o_sb - a.seqs.T * a.o_st : 0, a.o_st};
@@ -208,10 +208,11 @@ __global__ void __launch_bounds__(kFwdThreads, (IDS ? CCC_FWD_IDS_BLOCKS : 3) * 
     const int d0 = (blockIdx.x * blockDim.x + threadIdx.x) * V;
     const int64_t seg = int64_t(blockIdx.y) * blockDim.y + threadIdx.y;
     if (d0 < a.D && seg < a.n_seg) {
-      const int64_t q = seg * a.seg_len;
+      int64_t q, q_end;
+      seg_range(a.seqs, seg, a.seg_len, a.seg_per_seq, q, q_end);
       const int n = find_seq(a.seqs, q);
       const int64_t t = q - int64_t(n) * a.seqs.T;  // token within its sequence
-      const int rows = int(min(min(a.seg_len, int64_t((kFwdRing - 1) * G)), a.seqs.T - t));
+      const int rows = int(min(min(q_end - q, int64_t((kFwdRing - 1) * G)), a.seqs.T - t));
       const uint16_t* xp = a.x + int64_t(n) * a.x_sb + t * a.x_st + d0;
       for (int u = t < kState ? -int(t) : -kState; u < rows; ++u) prefetch_l2(xp + u * a.x_st);
     }
@@ -236,8 +237,8 @@ __global__ void __launch_bounds__(kFwdThreads, (IDS ? CCC_FWD_IDS_BLOCKS : 3) * 
   const uint32_t ring_s = smem_u32(ring);
   constexpr uint32_t slot = uint32_t(kFwdThreads) * RB;
 
-  int64_t q = seg * a.seg_len;
-  const int64_t q_end = q + a.seg_len < a.seqs.Q ? q + a.seg_len : a.seqs.Q;
+  int64_t q, q_end;
+  seg_range(a.seqs, seg, a.seg_len, a.seg_per_seq, q, q_end);
   const bool dense = a.seqs.cu == nullptr;
   int n = find_seq(a.seqs, q);
   using P0 = std::integral_constant<int, 0>;

@@ -72,6 +72,7 @@ struct FwdArgs {
   int64_t ids_sb, ids_st;
   int B, D;
   int64_t seg_len, n_seg;  // channel-last: tokens per thread range, number of ranges
+  int64_t seg_per_seq;     // dense: ranges per sequence (none straddles one), else 0
   int* status;
 };
 
@@ -101,6 +102,7 @@ struct BwdArgs {
   int64_t ids_sb, ids_st;
   int B, D;
   int64_t seg_len, n_seg;
+  int64_t seg_per_seq;    // dense: ranges per sequence (none straddles one), else 0
   float* ws;              // FP32 weight/bias-gradient partial sums, [R, D, 5]: block row r writes ws[r]
   int* status;
 };
@@ -114,6 +116,7 @@ struct FwdPlan {
   int tx, ty;    // block shape (channel-last)
   unsigned gx, gy;
   int64_t seg_len, n_seg;
+  int64_t seg_per_seq;  // dense: segments per sequence, each inside one; 0: over all tokens
   int group;     // channel-last vector forward: tokens per ring stage
 };
 
@@ -132,10 +135,11 @@ struct UpdArgs {
 };
 
 
+// T_seq: the sequence length of a dense call (Q = B * T_seq), 0 for packed.
 FwdPlan plan_fwd(int kind, int vec_ok, int64_t Q, int D, int64_t rows, int sm_count,
-                 bool ids = false);
+                 bool ids = false, int64_t T_seq = 0);
 BwdPlan plan_bwd(int kind, int vec_ok, int64_t Q, int D, int64_t rows, int sm_count,
-                 bool ids = false);
+                 bool ids = false, int64_t T_seq = 0);
 // Rows of FP32 partial sums the backward writes.
 int64_t bwd_partial_rows(const BwdPlan& p, int B, bool packed);
 
@@ -161,8 +165,10 @@ int fwd_ids_blocks_per_sm(int vec);
 int bwd_ids_blocks_per_sm(int vec);
 // Threads per block of the general channel-last kernels.
 constexpr int kGeneralThreads = 256;
-// Threads per block of the channel-last backward kernel for this vector width.
+// Threads per block of the channel-last backward kernel for this vector width,
+// without and with id masks.
 int bwd_block_threads(int vec);
+int bwd_ids_block_threads(int vec);
 
 cudaError_t launch_fwd(const FwdArgs& a, const FwdPlan& p, int act, cudaStream_t stream);
 cudaError_t launch_bwd(const BwdArgs& a, const BwdPlan& p, int act, const WgradOut& o,
