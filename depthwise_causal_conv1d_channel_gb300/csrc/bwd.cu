@@ -1054,8 +1054,11 @@ __global__ void __launch_bounds__(kBdtPairThreads, 4) bwd_bdt8x2_kernel(BwdArgs 
 constexpr int kFinClasses = 8;
 __global__ void __launch_bounds__(32 * kFinClasses) wgrad_finalize_kernel(const float* ws, int64_t R,
                                                                           int D, WgradOut o) {
-  // No early griddepcontrol.launch_dependents here: a following backward
-  // launched into this kernel's tail measured slower than one launched at its end.
+  // The next kernel may launch once every block has loaded its partial sums
+  // (not earlier: a following backward launched at this kernel's start
+  // measured slower).  Chains of backward calls at 4 x 2048 x 1536: 21.25 ->
+  // 21.2 us, with a width-three weight 21.4 -> 21.05 us, 16 packed sequences
+  // 79.2 -> 78.9 us, time-contiguous 24.3 -> 24.0 us.
   pdl_wait();  // the backward kernel's sums
   __shared__ float part[kFinClasses][32];
   const int tx = threadIdx.x & 31, c = threadIdx.x >> 5;
@@ -1076,6 +1079,7 @@ __global__ void __launch_bounds__(32 * kFinClasses) wgrad_finalize_kernel(const 
         if (r0 + j * kFinClasses < R) s += v[j];
     }
   }
+  pdl_release();
   part[c][tx] = s;
   __syncthreads();
   if (c != 0 || i >= n_val) return;
