@@ -346,7 +346,7 @@ def bench_stream_floor(inp: workloads.ConvInputs, device, stream, peak):
             "add_2read_1write": _rate(3 * nbytes, add_ms, inp.tokens, peak)}
 
 
-def bench_update(device, stream, peak, iters=50):
+def bench_update(device, stream, peak, iters=50, busy_s=0.0):
     from depthwise_causal_conv1d_channel_gb300 import _abi
 
     gen = torch.Generator(device=device).manual_seed(0)
@@ -377,6 +377,26 @@ def bench_update(device, stream, peak, iters=50):
     torch.cuda.synchronize()
     r["graph_chain_1000"] = {"us_per_step": round(a.elapsed_time(c) * 1e3 / 1000, 3),
                              "note": "one state, L2-resident, CUDA graph; not an HBM figure"}
+    t_end = time.time() + busy_s  # untimed replays, so that clock samples see the load
+    while time.time() < t_end:
+        g.replay()
+        torch.cuda.synchronize()
+    return r
+
+
+def bench_update_clocked(device, stream, peak, gpu_index):
+    """bench_update with the SM clock sampled meanwhile: the step time times the
+    median SM clock (thousands of cycles a step) separates the clock from the
+    step's latency."""
+    with ClockSampler(gpu_index) as clk:
+        r = bench_update(device, stream, peak, busy_s=1.5)
+    c = clk.summary()
+    r["clocks"] = c
+    if c.get("sm_mhz"):
+        u = r["update"]
+        u["kcycles_per_step"] = round(u["us"] * c["sm_mhz"] / 1000.0, 2)
+        r["graph_chain_1000"]["kcycles_per_step"] = round(
+            r["graph_chain_1000"]["us_per_step"] * c["sm_mhz"] / 1000.0, 2)
     return r
 
 
@@ -852,7 +872,7 @@ def main():
               bench_stream_floor(ds, device, stream, peak),
               bench_conv_workload("packed_varlen", workloads.packed_varlen(), device, stream, peak,
                                   True),
-              bench_update(device, stream, peak)]
+              bench_update_clocked(device, stream, peak, local)]
         # the same dense step on a contiguous [B, D, T] tensor (time-contiguous)
         tc = workloads.make_inputs(4, 1536, 2048, seed=0, initial_states=True, grad=True,
                                    channel_last=False)
