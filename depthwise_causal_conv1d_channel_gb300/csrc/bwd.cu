@@ -318,8 +318,10 @@ constexpr size_t bwd_ring_bytes(int threads) {
   return size_t(threads) * kBwdRing * 3 * 2 * (2 * V);
 }
 // Threads a block: 256 for eight channels a thread (one block an SM, ~240
-// registers) and for four (two blocks an SM, 128 registers); 128 for the id
-// instance (~150 registers, three blocks an SM).  Measured: at eight channels,
+// registers) and for four (two blocks an SM, 128 registers); 384 for the id
+// instance (~150 registers, one block an SM: 27.3 us with seq_idx at
+// 4 x 2048 x 1536 against 27.6 us for three 128-thread blocks and 29.0 us for
+// two of 192).  Measured: at eight channels,
 // 256-thread blocks took 307 us against 311 us at 8 x 5120 x 8192 and 78.8
 // against 80.5 us on 16 packed sequences (half the partial rows).  At four,
 // with segments planned per sequence, 4 x 2048 x 1536 took 20.9-21.1 us in
@@ -327,8 +329,11 @@ constexpr size_t bwd_ring_bytes(int threads) {
 // scheduler favours a block's older warps, so with four blocks an SM the
 // last-placed block ran its loop about 4 us behind the first and finished
 // with the SM mostly idle.
+#ifndef CCC_BWD_IDS_THREADS
+#define CCC_BWD_IDS_THREADS 384
+#endif
 template <int V, bool IDS = false>
-__host__ __device__ constexpr int bwd_threads() { return V == 8 || !IDS ? 256 : 128; }
+__host__ __device__ constexpr int bwd_threads() { return V == 8 || !IDS ? 256 : CCC_BWD_IDS_THREADS; }
 
 // With IDS (V = 4; dense calls without states), every token carries a sequence
 // id (cuDNN page, seq_idx[B, T]): a tap joins two tokens only when their ids
@@ -337,7 +342,7 @@ __host__ __device__ constexpr int bwd_threads() { return V == 8 || !IDS ? 256 : 
 // the fast steps; any other takes the general step, which masks every tap by
 // the ids.  Both leave the windows at phase 0 after a group.
 #ifndef CCC_BWD_IDS_BLOCKS
-#define CCC_BWD_IDS_BLOCKS 3  // resident blocks an SM asked of the id instance
+#define CCC_BWD_IDS_BLOCKS 1  // resident blocks an SM asked of the id instance
 #endif
 template <int V, int ACT, bool IDS = false>
 __global__ void __launch_bounds__(bwd_threads<V, IDS>(), V == 8 ? 1 : (IDS ? CCC_BWD_IDS_BLOCKS : 2))

@@ -71,6 +71,11 @@ DENSE_CASES = [
     # eight channels a thread in blocks two warps wide, the last block column
     # one channel group wide (D = 4104 = 64 * 64 + 8)
     (1, 4104, 12000, True, dict(initial_states=True, grad=True)),
+    # dense plans cut each sequence into its own segments: many short
+    # sequences (one segment each, shorter than a planned segment), and
+    # sequences whose last segment is ragged, with states in and out
+    (48, 512, 7, True, dict(initial_states=True, grad=True, dfinal_states=True)),
+    (5, 1024, 997, True, dict(initial_states=True, grad=True, dfinal_states=True)),
     (3, 264, 300, True, dict(initial_states=True, grad=True)),
     (2, 264, 300, True, dict(initial_states=True, grad=True, dfinal_states=True)),
     (2, 64, 37, True, dict(grad=True)),
