@@ -349,7 +349,7 @@ FwdPlan plan_fwd(int kind, int vec, int64_t Q, int D, int64_t rows, int sm_count
                  int64_t T_seq) {
   if (ids) {  // kernels with id masks: the ring kernel (vec 4) or the general ones
     FwdPlan p = kind == kLayoutTimeContiguous ? plan_bdt(rows)
-                : vec == 4 ? plan_cl(4, Q, D, sm_count, fwd_ids_blocks_per_sm(4), 1, 12, kFwdThreads,
+                : vec == 4 ? plan_cl(4, Q, D, sm_count, fwd_ids_blocks_per_sm(4), 1, 12, kFwdIdsThreads,
                                      kFwdGroupLong, 32, T_seq)
                            : plan_cl(vec, Q, D, sm_count, fwd_ids_blocks_per_sm(vec), 1, 12,
                                      kGeneralThreads, 1, 32, T_seq);

@@ -188,13 +188,17 @@ extern __shared__ __align__(16) char fwd_dyn_smem[];
 // any other takes the masked step with physical shifts.  A group is a whole
 // number of window periods, so both leave the window at phase 0.
 #ifndef CCC_FWD_IDS_BLOCKS
-#define CCC_FWD_IDS_BLOCKS 2  // resident blocks an SM asked of the id instance
+#define CCC_FWD_IDS_BLOCKS 4  // resident blocks an SM asked of the id instance
 #endif
+template <bool IDS>
+__host__ __device__ constexpr int fwd_threads() { return IDS ? kFwdIdsThreads : kFwdThreads; }
 // W3: a contiguous [D, 3] weight read with vectors (its own instance, so the
 // width-four kernel's register allocation is untouched).
 template <int V, int ACT, bool IDS = false, bool W3 = false, int GT = kFwdGroup>
-__global__ void __launch_bounds__(kFwdThreads, (IDS ? CCC_FWD_IDS_BLOCKS : 3) * 256 / kFwdThreads) fwd_clv_kernel(FwdArgs a) {
-  if (blockDim.x * blockDim.y * blockDim.z != kFwdThreads) return;  // the ring layout assumes it
+__global__ void __launch_bounds__(fwd_threads<IDS>(), IDS ? CCC_FWD_IDS_BLOCKS : 3 * 256 / kFwdThreads)
+    fwd_clv_kernel(FwdArgs a) {
+  constexpr int NT = fwd_threads<IDS>();
+  if (blockDim.x * blockDim.y * blockDim.z != NT) return;  // the ring layout assumes it
   using VT = Vec<V>;
   using Raw = typename VT::Raw;
   constexpr int H = V / 2;  // channel pairs
@@ -230,12 +234,12 @@ __global__ void __launch_bounds__(kFwdThreads, (IDS ? CCC_FWD_IDS_BLOCKS : 3) * 
   if (d0 >= a.D || seg >= a.n_seg) return;
   float2 w[H][kWidth], b[H];
   bool have_w = false;  // the weights are loaded once the first ring groups are in flight
-  // this thread's ring: slot (stage, row u) at byte ((stage * G + u) * kFwdThreads + tid) * RB
+  // this thread's ring: slot (stage, row u) at byte ((stage * G + u) * NT + tid) * RB
   // (a compile-time block size: the offsets are immediates)
   const int tid = threadIdx.y * blockDim.x + threadIdx.x;
   const char* ring = fwd_dyn_smem + size_t(tid) * RB;
   const uint32_t ring_s = smem_u32(ring);
-  constexpr uint32_t slot = uint32_t(kFwdThreads) * RB;
+  constexpr uint32_t slot = uint32_t(NT) * RB;
 
   int64_t q, q_end;
   seg_range(a.seqs, seg, a.seg_len, a.seg_per_seq, q, q_end);
@@ -513,10 +517,11 @@ static ContextCache g_fwd_attr_done;
 static cudaError_t fwd_smem_attributes() {
   long long done = 0;
   if (g_fwd_attr_done.get(&done) && done) return cudaSuccess;
-  const int bytes = int(fwd_ring_bytes<4>(kFwdThreads));
+  const int bytes = int(fwd_ring_bytes<4>(kFwdThreads)), bytes_ids = int(fwd_ring_bytes<4>(kFwdIdsThreads));
   cudaError_t err = cudaSuccess;
+  for (auto f : {fwd_clv_kernel<4, kActSilu, true>, fwd_clv_kernel<4, kActNone, true>})
+    if (err == cudaSuccess) err = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes_ids);
   for (auto f : {fwd_clv_kernel<4, kActSilu>, fwd_clv_kernel<4, kActNone>,
-                 fwd_clv_kernel<4, kActSilu, true>, fwd_clv_kernel<4, kActNone, true>,
                  fwd_clv_kernel<4, kActSilu, false, true>, fwd_clv_kernel<4, kActNone, false, true>,
                  fwd_clv_kernel<4, kActSilu, false, false, kFwdGroupShort>,
                  fwd_clv_kernel<4, kActNone, false, false, kFwdGroupShort>,
@@ -554,7 +559,7 @@ int fwd_ids_blocks_per_sm(int vec) {
   fwd_smem_attributes();
   const cudaError_t err =
       vec == 4 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fwd_clv_kernel<4, kActSilu, true>,
-                                                               kFwdThreads, fwd_ring_bytes<4>(kFwdThreads))
+                                                               kFwdIdsThreads, fwd_ring_bytes<4>(kFwdIdsThreads))
                : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fwd_cl_kernel<1, kActSilu, true>,
                                                                kGeneralThreads, 0);
   if (err == cudaSuccess && n > 0) {
