@@ -273,17 +273,6 @@ __global__ void __launch_bounds__(fwd_threads<IDS>(), IDS ? CCC_FWD_IDS_BLOCKS :
           if (k * G + u < n_tok) cp_async<RB>(s0 + uint32_t(u) * slot, xm + u * xst);
       }
     };
-#pragma unroll
-    for (int k = 0; k < kFwdRing - 1; ++k) {
-      if (k < n_grp) issue(k);
-      cp_async_commit();
-    }
-    if (!have_w) {
-      if constexpr (W3) weights_direct3<V>(a.wr, d0, w, b);
-      else if (a.wr.w_vec) weights_direct2<V>(a.wr, d0, w, b);
-      else weights_from_smem2<V>(ws, n_blk, threadIdx.x * V, w, b);
-      have_w = true;
-    }
 
     // W[j] = xe[q - 3 + j]; IW[j] = its id (IDS; any value before the row
     // start, where the window is zero)
@@ -291,6 +280,15 @@ __global__ void __launch_bounds__(fwd_threads<IDS>(), IDS ? CCC_FWD_IDS_BLOCKS :
     int IW[kState] = {0, 0, 0};
     const int64_t id_off = IDS ? int64_t(n) * a.ids_sb - lo * a.ids_st : 0;
     {
+      // With short ranges (3-token groups) or id masks, the window's own loads
+      // (the halo rows, or the initial state) and the weights go out before
+      // the ring's first groups: the first step needs them all, and requests
+      // are served about in the order issued.  Measured at 4 x 2048 x 1536:
+      // 10.2 -> 9.75 us, width three 10.14 -> 9.68 us, with seq_idx 13.0 ->
+      // 12.64 us.  Long ranges keep the ring first (8 x 5120 x 8192 lost
+      // 1.3 us the other way; with this setup, where the halo rows are held
+      // raw until the ring is out, it took 198.6 against 199.5 us, and 16
+      // packed sequences 47.9 against 48.6 us).
       float2 init[kState][H];
       if (q - kState < lo && a.init) {
         load_state2<V>(a.init, state_row, a.sw, init);
@@ -300,11 +298,41 @@ __global__ void __launch_bounds__(fwd_threads<IDS>(), IDS ? CCC_FWD_IDS_BLOCKS :
 #pragma unroll
           for (int h = 0; h < H; ++h) init[i][h] = splat2(0.0f);
       }
+      Raw hx[kState] = {};  // halo rows
+      auto load_halo = [&]() {
+#pragma unroll
+        for (int j = 0; j < kState; ++j)
+          if (q - kState + j >= lo) hx[j] = VT::ld(xp - (kState - j) * xst);
+      };
+      auto load_weights = [&]() {
+        if (!have_w) {
+          if constexpr (W3) weights_direct3<V>(a.wr, d0, w, b);
+          else if (a.wr.w_vec) weights_direct2<V>(a.wr, d0, w, b);
+          else weights_from_smem2<V>(ws, n_blk, threadIdx.x * V, w, b);
+          have_w = true;
+        }
+      };
+      auto issue_first = [&]() {
+#pragma unroll
+        for (int k = 0; k < kFwdRing - 1; ++k) {
+          if (k < n_grp) issue(k);
+          cp_async_commit();
+        }
+      };
+      if constexpr (G == kFwdGroupShort || IDS) {
+        load_halo();
+        load_weights();
+        issue_first();
+      } else {
+        issue_first();
+        load_weights();
+        load_halo();
+      }
 #pragma unroll
       for (int j = 0; j < kState; ++j) {
         const int64_t tok = q - kState + j;
         if (tok >= lo) {
-          VT::unpack2(VT::ld(xp - (kState - j) * xst), W[j]);
+          VT::unpack2(hx[j], W[j]);
           if constexpr (IDS) IW[j] = __ldg(a.ids + id_off + tok * a.ids_st);
         } else {
           const int64_t i = tok - lo + kState;
