@@ -47,8 +47,8 @@ L2_BYTES = 129 * 2 ** 20
 # finalize kernel -- from one ncu capture of those two kernels
 # (profiles/traffic_dense_large_backward.md), per launch.  Valid only for the
 # kernel sources whose digest is recorded here (null otherwise).
-TRAFFIC = {"sources_sha256": "055be62d529b9d55d3fcc544dfcc531c9cb29f03c7a850ba1b6617c1ee201847",
-           "bytes_per_launch": (1349988608 + 634812672) + (1543168 + 0)}
+TRAFFIC = {"sources_sha256": "b33be4fce96872be6f738607eab033b6ec576f8b5f65626dbb6babd3e00f1868",
+           "bytes_per_launch": (1349992960 + 635142144) + (1545472 + 0)}
 
 
 # The sources the dominant call's kernels (the channel-last backward and the
