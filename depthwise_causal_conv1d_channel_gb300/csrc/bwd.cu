@@ -415,7 +415,7 @@ __global__ void __launch_bounds__(bwd_threads<V, IDS>(), V == 8 ? 1 : (IDS ? CCC
       // when those end on e with three more rows in the sequence, the tail
       // group, which emits the last own rows; else the general step finishes.
       // The first groups go out before anything else of the piece is read but
-      // the window (halo rows or initial state) and, at four channels, the weights.
+      // the window (halo rows or initial state) and the weights.
       const bool head = a0 - kState >= lo && a0 + 3 <= e;
       const int64_t r0 = head ? a0 : (a0 + kState < m_end ? a0 + kState : m_end);
       const int n_main = e > r0 ? int((e - r0) / 3) : 0;  // a segment's groups: below 2^31
@@ -462,14 +462,40 @@ __global__ void __launch_bounds__(bwd_threads<V, IDS>(), V == 8 ? 1 : (IDS ? CCC
         st = (st + 1) % kBwdRing;
         return uniform;
       };
-      // Four channels a thread: the window's own loads (the halo rows, or the
-      // initial state) and the weights go out before the ring's first groups.
-      // The first step needs all of them, and requests are served about in
-      // the order issued (4 x 2048 x 1536: 20.85 -> 20.07 us, with seq_idx
-      // 27.4 -> 26.4 us).  Eight channels a thread keep the ring first (the
-      // other order cost 12 registers and 0.8 us at 8 x 5120 x 8192).
-      // rows the general steps may read at the piece's two ends: into L2
-      auto prefetch_ends = [&]() {
+      // The window's own loads (the halo rows, or the initial state) and the
+      // weights go out before the ring's first groups: the first step needs
+      // all of them, and requests are served about in the order issued.
+      // Measured: 4 x 2048 x 1536 20.85 -> 20.07 us, with seq_idx 27.4 ->
+      // 26.4 us; 16 packed sequences 77.86 -> 77.25 us; 8 x 5120 x 8192
+      // 302.8 -> 301.9 us.
+      float2 X[kState][H], G[kState][H];  // xe[m-3 .. m-1], gp[m-3 .. m-1]
+      if constexpr (IDS) {
+#pragma unroll
+        for (int j = 0; j < kState; ++j)
+          if (a0 - kState + j >= lo) IW[j] = id_at(a0 - kState + j);
+      }
+      {
+        float2 init[kState][H];
+        if (a0 - kState < lo && a.init) {
+          load_state2<V>(a.init, state_row, a.sw, init);
+        } else {
+#pragma unroll
+          for (int i = 0; i < kState; ++i)
+#pragma unroll
+            for (int h = 0; h < H; ++h) init[i][h] = splat2(0.0f);
+        }
+        Raw hx[kState] = {};  // halo rows, unpacked once the ring's first groups are out
+#pragma unroll
+        for (int j = 0; j < kState; ++j)
+          if (a0 - kState + j >= lo) hx[j] = VT::ld(xp - (kState - j) * xst);
+        if (!have_w) {
+          if (a.wr.w_vec || a.wr.w_vec3) weights_direct2_any<V>(a.wr, d0, w, b);
+          else weights_from_smem2<V>(wsm, n_blk, threadIdx.x * V, w, b);
+          have_w = true;
+        }
+#pragma unroll
+        for (int j = 0; j < kBwdRing - 1; ++j) issue_next();
+        // rows the general steps may read at the piece's two ends: into L2
         const int64_t r_end = m_end < hi ? m_end : hi;
         for (int64_t t = a0; t < a0 + kState && t < r_end; ++t) {
           prefetch_l2(xp + (t - a0) * xst);
@@ -479,37 +505,12 @@ __global__ void __launch_bounds__(bwd_threads<V, IDS>(), V == 8 ? 1 : (IDS ? CCC
           prefetch_l2(xp + (t - a0) * xst);
           prefetch_l2(gq + (t - a0) * gst);
         }
-      };
-      float2 X[kState][H], G[kState][H];  // xe[m-3 .. m-1], gp[m-3 .. m-1]
-      if constexpr (IDS) {
+        // X[j] from halo row j or the initial state; G zero
 #pragma unroll
-        for (int j = 0; j < kState; ++j)
-          if (a0 - kState + j >= lo) IW[j] = id_at(a0 - kState + j);
-      }
-      {
-        float2 init[kState][H];
-        auto load_init = [&]() {
-          if (a0 - kState < lo && a.init) {
-            load_state2<V>(a.init, state_row, a.sw, init);
-          } else {
-#pragma unroll
-            for (int i = 0; i < kState; ++i)
-#pragma unroll
-              for (int h = 0; h < H; ++h) init[i][h] = splat2(0.0f);
-          }
-        };
-        auto load_weights = [&]() {
-          if (!have_w) {
-            if (a.wr.w_vec || a.wr.w_vec3) weights_direct2_any<V>(a.wr, d0, w, b);
-            else weights_from_smem2<V>(wsm, n_blk, threadIdx.x * V, w, b);
-            have_w = true;
-          }
-        };
-        // X[j] from halo row j (raw) or the initial state; G zero
-        auto set_window = [&](int j, const Raw& raw) {
+        for (int j = 0; j < kState; ++j) {
           const int64_t tok = a0 - kState + j;
           if (tok >= lo) {
-            VT::unpack2(raw, X[j]);
+            VT::unpack2(hx[j], X[j]);
           } else {
             const int64_t i = tok - lo + kState;
 #pragma unroll
@@ -518,31 +519,6 @@ __global__ void __launch_bounds__(bwd_threads<V, IDS>(), V == 8 ? 1 : (IDS ? CCC
           }
 #pragma unroll
           for (int h = 0; h < H; ++h) G[j][h] = splat2(0.0f);
-        };
-        if constexpr (V == 4) {
-          load_init();
-          Raw hx[kState] = {};  // halo rows, unpacked once the ring's first groups are out
-#pragma unroll
-          for (int j = 0; j < kState; ++j)
-            if (a0 - kState + j >= lo) hx[j] = VT::ld(xp - (kState - j) * xst);
-          load_weights();
-#pragma unroll
-          for (int j = 0; j < kBwdRing - 1; ++j) issue_next();
-          prefetch_ends();
-#pragma unroll
-          for (int j = 0; j < kState; ++j) set_window(j, hx[j]);
-        } else {
-#pragma unroll
-          for (int j = 0; j < kBwdRing - 1; ++j) issue_next();
-          load_weights();
-          prefetch_ends();
-          load_init();
-#pragma unroll
-          for (int j = 0; j < kState; ++j) {
-            Raw r{};
-            if (a0 - kState + j >= lo) r = VT::ld(xp - (kState - j) * xst);
-            set_window(j, r);
-          }
         }
       }
 

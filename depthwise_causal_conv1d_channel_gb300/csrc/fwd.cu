@@ -285,10 +285,10 @@ __global__ void __launch_bounds__(fwd_threads<IDS>(), IDS ? CCC_FWD_IDS_BLOCKS :
       // the ring's first groups: the first step needs them all, and requests
       // are served about in the order issued.  Measured at 4 x 2048 x 1536:
       // 10.2 -> 9.75 us, width three 10.14 -> 9.68 us, with seq_idx 13.0 ->
-      // 12.64 us.  Long ranges keep the ring first (8 x 5120 x 8192 lost
-      // 1.3 us the other way; with this setup, where the halo rows are held
-      // raw until the ring is out, it took 198.6 against 199.5 us, and 16
-      // packed sequences 47.9 against 48.6 us).
+      // 12.64 us.  Long ranges keep the ring first (8 x 5120 x 8192 took
+      // 198.5 us this way against 201.3 us the other way, 16 packed sequences
+      // 47.8 against 48.1 us; holding the halo rows raw until the ring is out
+      // took them from 199.5 and 48.6 us).
       float2 init[kState][H];
       if (q - kState < lo && a.init) {
         load_state2<V>(a.init, state_row, a.sw, init);
