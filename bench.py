@@ -47,8 +47,8 @@ L2_BYTES = 129 * 2 ** 20
 # finalize kernel -- from one ncu capture of those two kernels
 # (profiles/traffic_dense_large_backward.md), per launch.  Valid only for the
 # kernel sources whose digest is recorded here (null otherwise).
-TRAFFIC = {"sources_sha256": "b33be4fce96872be6f738607eab033b6ec576f8b5f65626dbb6babd3e00f1868",
-           "bytes_per_launch": (1349992960 + 635142144) + (1545472 + 0)}
+TRAFFIC = {"sources_sha256": "c5b663cb85be5c244680f9f7ccb228167c5a616e40c642b0cd66ef71ea1effd5",
+           "bytes_per_launch": (1349969920 + 635004672) + (1543168 + 0)}
 
 
 # The sources the dominant call's kernels (the channel-last backward and the
