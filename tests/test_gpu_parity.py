@@ -75,6 +75,8 @@ DENSE_CASES = [
     # sequences (one segment each, shorter than a planned segment), and
     # sequences whose last segment is ragged, with states in and out
     (48, 512, 7, True, dict(initial_states=True, grad=True, dfinal_states=True)),
+    (64, 256, 1, True, dict(initial_states=True, grad=True, dfinal_states=True)),
+    (33, 136, 2, True, dict(initial_states=True, grad=True, dfinal_states=True)),
     (5, 1024, 997, True, dict(initial_states=True, grad=True, dfinal_states=True)),
     (3, 264, 300, True, dict(initial_states=True, grad=True)),
     (2, 264, 300, True, dict(initial_states=True, grad=True, dfinal_states=True)),
