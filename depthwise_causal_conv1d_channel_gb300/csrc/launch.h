@@ -148,11 +148,14 @@ int64_t bwd_partial_rows(const BwdPlan& p, int B, bool packed);
 // fewer than kFwdShortTokens tokens (the first rows are computed sooner; with
 // long ranges the longer groups keep more bytes in flight).
 constexpr int kFwdGroupLong = 6, kFwdGroupShort = 3;
-// Threads a block of the channel-last vector forward (six blocks an SM).
-// Measured against 256 (three an SM) and 512: 199.3 / 200.0 / 215.9 us at
-// 8 x 5120 x 8192, 11.9 / 12.0 / 12.9 us at 4 x 2048 x 1536.
+// Threads a block of the channel-last vector forward (three blocks an SM).
+// Measured with the per-sequence plan, the prefetch before the dependent
+// wait and the window loaded first: 9.46 us at 4 x 2048 x 1536 against
+// 9.75 us for six 128-thread blocks an SM (10.5 us for two of 384), 199.0
+// against 198.8 us at 8 x 5120 x 8192, 47.7 against 47.8 us on 16 packed
+// sequences.
 #ifndef CCC_FWD_THREADS
-#define CCC_FWD_THREADS 128
+#define CCC_FWD_THREADS 256
 #endif
 constexpr int kFwdThreads = CCC_FWD_THREADS;
 // Threads a block of the channel-last vector forward with id masks (four
