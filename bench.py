@@ -47,8 +47,8 @@ L2_BYTES = 129 * 2 ** 20
 # finalize kernel -- from one ncu capture of those two kernels
 # (profiles/traffic_dense_large_backward.md), per launch.  Valid only for the
 # kernel sources whose digest is recorded here (null otherwise).
-TRAFFIC = {"sources_sha256": "c5b663cb85be5c244680f9f7ccb228167c5a616e40c642b0cd66ef71ea1effd5",
-           "bytes_per_launch": (1349969920 + 635004672) + (1543168 + 0)}
+TRAFFIC = {"sources_sha256": "55a4fb9036913427f92dea08d831d8e51c3202032fa6756760b116a8998b0e32",
+           "bytes_per_launch": (1349961216 + 634909184) + (1543168 + 0)}
 
 
 # The sources the dominant call's kernels (the channel-last backward and the
