@@ -24,6 +24,7 @@ import dataclasses
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -46,8 +47,9 @@ L2_BYTES = 129 * 2 ** 20
 # call -- the backward on the large dense workload: backward kernel plus the
 # finalize kernel -- from one ncu capture of those two kernels
 # (profiles/traffic_dense_large_backward.md), per launch.  Valid only for the
-# kernel sources whose digest is recorded here (null otherwise).
-TRAFFIC = {"sources_sha256": "55a4fb9036913427f92dea08d831d8e51c3202032fa6756760b116a8998b0e32",
+# kernel sources whose digest (of their code, comments left out) is recorded
+# here (null otherwise).
+TRAFFIC = {"sources_sha256": "b83778852e62934e5e1bf69ce7729cd36de06b91b0ab751aecf40d2ab6642710",
            "bytes_per_launch": (1349961216 + 634909184) + (1543168 + 0)}
 
 
@@ -56,12 +58,20 @@ TRAFFIC = {"sources_sha256": "55a4fb9036913427f92dea08d831d8e51c3202032fa6756760
 TRAFFIC_SOURCES = ("abi.cu", "bwd.cu", "common.cuh", "launch.h")
 
 
+def _code_only(text: str) -> str:
+    """The source without its comments and blank lines (an edited comment
+    leaves the recorded traffic valid; any change to the code does not)."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    lines = (re.sub(r"//.*$", "", line).rstrip() for line in text.splitlines())
+    return "\n".join(line for line in lines if line)
+
+
 def kernel_sources_digest() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "depthwise_causal_conv1d_channel_gb300", "csrc")
     for name in TRAFFIC_SOURCES:
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + b"\0" + f.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            h.update(name.encode() + b"\0" + _code_only(f.read()).encode())
     return h.hexdigest()
 
 

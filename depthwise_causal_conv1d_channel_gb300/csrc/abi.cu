@@ -209,9 +209,9 @@ bool vec_ok(int V, const Problem& pb, std::initializer_list<const ccc_tensor*> a
 #endif
 
 // Backward vector width.  Eight channels a thread halve the per-token load,
-// address and prefetch work but need ~210 registers (two 128-thread blocks an
-// SM); four channels fit four blocks.  Long per-thread token ranges favour
-// eight, short ones the extra parallelism of four.
+// address and prefetch work but need ~240 registers (one 256-thread block an
+// SM); four channels fit two 256-thread blocks.  Long per-thread token ranges
+// favour eight, short ones the extra parallelism of four.
 int bwd_preferred_vec(int64_t Q, int D, int sm_count) {
   if (CCC_BWD_VEC) return CCC_BWD_VEC;
   const int64_t resident_threads =

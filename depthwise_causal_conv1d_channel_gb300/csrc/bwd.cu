@@ -306,8 +306,8 @@ __global__ void __launch_bounds__(kGeneralThreads) bwd_cl_kernel(BwdArgs a) {
 // (the three tokens after the piece, which emit its last dx rows); the few
 // tokens at sequence edges take the general step, loading their rows directly
 // (prefetched into L2 when the piece starts).
-// 256-thread blocks for V = 8 (one resident per SM), 128-thread blocks for
-// V = 4 (four per SM).
+// 256-thread blocks: one resident per SM for V = 8, two for V = 4 (the id
+// instance: one 384-thread block per SM).
 #ifndef CCC_BWD_RING
 #define CCC_BWD_RING 3
 #endif
