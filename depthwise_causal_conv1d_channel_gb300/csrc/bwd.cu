@@ -417,7 +417,12 @@ __global__ void __launch_bounds__(bwd_threads<V, IDS>(), V == 8 ? 1 : (IDS ? CCC
       // The first groups go out before anything else of the piece is read but
       // the window (halo rows or initial state) and the weights.
       const bool head = a0 - kState >= lo && a0 + 3 <= e;
-      const int64_t r0 = head ? a0 : (a0 + kState < m_end ? a0 + kState : m_end);
+      // A sequence's first piece, when it holds three tokens and the sequence
+      // six: its first ring group takes those tokens too, with the window from
+      // the initial state, and the group's emissions become the initial
+      // state's gradient (the general step's arithmetic, in its order).
+      const bool shead = !IDS && starts && a0 + 3 <= e && hi - lo >= 2 * kState;
+      const int64_t r0 = head || shead ? a0 : (a0 + kState < m_end ? a0 + kState : m_end);
       const int n_main = e > r0 ? int((e - r0) / 3) : 0;  // a segment's groups: below 2^31
       const bool tail = e > r0 && (e - r0) % 3 == 0 && e + kState <= hi && e - a0 >= kState;
       const int n_total = n_main + (tail ? 1 : 0);
@@ -667,6 +672,33 @@ __global__ void __launch_bounds__(bwd_threads<V, IDS>(), V == 8 ? 1 : (IDS ? CCC
       if (head) {
         if (take(xr, gr, r0)) group(Yes{}, No{}, xr, gr, drow);
         else mixed(r0);
+        k = 1;
+        drow += 3 * dst;
+      } else if (shead) {
+        take(xr, gr, r0);  // no ids: always uniform
+        group(Yes{}, No{}, xr, gr, drow);
+        // G[u] now holds gp of token lo + u.  Entry i of the initial state
+        // (token lo - 3 + i) is the emission at token lo + i, whose taps on
+        // tokens before lo read zero; no final-state gradient reaches it.
+        if (a.dinit) {
+          const float2 zero2 = splat2(0.0f);
+#pragma unroll
+          for (int i = 0; i < kState; ++i) {
+#pragma unroll
+            for (int h = 0; h < H; ++h) {
+              const float2 gm2 = i == 2 ? G[0][h] : zero2;  // gp of token lo + i - 2
+              const float2 gm1 = i == 2 ? G[1][h] : (i == 1 ? G[0][h] : zero2);
+              float2 acc = fmul2(w[h][3], zero2);
+              acc = ffma2(w[h][2], gm2, acc);
+              acc = ffma2(w[h][1], gm1, acc);
+              acc = ffma2(w[h][0], G[i][h], acc);
+              const int64_t k0 = state_slot(state_row + 2 * h, i, a.sw);
+              const int64_t k1 = state_slot(state_row + 2 * h + 1, i, a.sw);
+              if (k0 >= 0) a.dinit[k0] = f32_to_bf16(acc.x);
+              if (k1 >= 0) a.dinit[k1] = f32_to_bf16(acc.y);
+            }
+          }
+        }
         k = 1;
         drow += 3 * dst;
       }
