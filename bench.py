@@ -49,8 +49,8 @@ L2_BYTES = 129 * 2 ** 20
 # (profiles/traffic_dense_large_backward.md), per launch.  Valid only for the
 # kernel sources whose digest (of their code, comments left out) is recorded
 # here (null otherwise).
-TRAFFIC = {"sources_sha256": "b83778852e62934e5e1bf69ce7729cd36de06b91b0ab751aecf40d2ab6642710",
-           "bytes_per_launch": (1349961216 + 634909184) + (1543168 + 0)}
+TRAFFIC = {"sources_sha256": "64f4500756e417e35b06e79e5c091448159434ca347fb52d1980f92e25bdaf57",
+           "bytes_per_launch": (1349974528 + 635071744) + (1543424 + 0)}
 
 
 # The sources the dominant call's kernels (the channel-last backward and the
