@@ -663,7 +663,8 @@ __global__ void __launch_bounds__(bwd_threads<V, IDS>(), V == 8 ? 1 : (IDS ? CCC
       }
       Raw xr[3], gr[3];
       int k = 0;
-      uint16_t* drow = dp + (r0 - kState - a0) * dst;  // dx rows of group k
+      // dx rows of group k (a first group that stores nothing gets dp)
+      uint16_t* drow = shead ? dp : dp + (r0 - kState - a0) * dst;
       // a group of other ids than its window's takes the general steps
       auto mixed = [&](int64_t m0) {
 #pragma unroll 1
@@ -699,8 +700,7 @@ __global__ void __launch_bounds__(bwd_threads<V, IDS>(), V == 8 ? 1 : (IDS ? CCC
             }
           }
         }
-        k = 1;
-        drow += 3 * dst;
+        k = 1;  // drow stays at dp: group 1 emits rows lo .. lo + 2
       }
       for (; k < n_main; ++k) {
         const int64_t m0 = r0 + 3 * int64_t(k);
