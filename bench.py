@@ -75,6 +75,12 @@ def kernel_sources_digest() -> str:
     return h.hexdigest()
 
 
+def recorded_traffic():
+    """DRAM bytes per launch of the dominant call, or None once the code it was
+    captured from has changed."""
+    return TRAFFIC["bytes_per_launch"] if TRAFFIC["sources_sha256"] == kernel_sources_digest() else None
+
+
 # ---- sizes ------------------------------------------------------------------------
 
 def act_bytes(x):
@@ -842,7 +848,7 @@ def main():
 
     dominant = ("bwd", b_ms, step.bwd_bytes) if b_ms >= f_ms else ("fwd", f_ms, step.fwd_bytes)
     achieved = dominant[2] / (dominant[1] * 1e-3) / 1e9
-    traffic = TRAFFIC["bytes_per_launch"] if TRAFFIC["sources_sha256"] == kernel_sources_digest() else None
+    traffic = recorded_traffic()
 
     e2e_ms, h2d, d2h = time_e2e(inp, device, args.steps, args.warmup, stream)
     e2e_value = world * step_bytes / (e2e_ms * 1e-3) / 1e9
